@@ -1,0 +1,196 @@
+/*
+ * mla.h -- C ABI of libmla: MLA chunked prefill over a paged packed-latent KV
+ * cache, hand-written for NVIDIA GB300 (sm_103a).
+ *
+ * Geometry (fixed): latent d_c = 512, RoPE width d_r = 64, per-head no-RoPE key
+ * width d_nope = 128, value width d_v = 128, 64-token cache blocks.  One cached
+ * token is one packed row [c_kv 0..511 | k_rope 0..63] ("DeepSeek MLA — Prefix
+ * Cache 与 Chunked Prefill 深度解析", section 5.2; 64-token blocks from
+ * "PagedAttention assumed MHA. DeepSeek-V4 says that assumption is broken",
+ * section "Block size is not a tuning knob here").
+ *
+ * Conventions shared by every entry point
+ *  - All tensors are contiguous, row-major, little-endian.  "device" pointers
+ *    are CUDA device memory of the current device; "host" pointers are plain
+ *    host memory read synchronously before the call returns.
+ *  - The library never allocates and never frees; every buffer belongs to the
+ *    caller.  Calls are asynchronous on `stream` (NULL = legacy default stream).
+ *  - Host-side validation runs first and returns a status before anything is
+ *    launched.  No C++ exception crosses the ABI.  Device-side faults that the
+ *    kernels can detect (a block-table entry outside [0, num_blocks)) never
+ *    trap: the affected rows are read as zeros and a bit is set in a device
+ *    error word that the caller reads with mla_get_device_error().
+ *  - Return value: an mla_status (0 = MLA_OK).
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mla_stream_t; /* identical to cudaStream_t */
+
+enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent lengths */
+  MLA_ERR_UNSUPPORTED = 2,   /* a shape or mode this build does not implement */
+  MLA_ERR_BAD_BLOCK_ID = 3,  /* device saw a block-table entry outside [0, num_blocks) */
+  MLA_ERR_CUDA = 4,          /* a CUDA runtime call failed (see mla_last_cuda_error) */
+  MLA_ERR_WORKSPACE = 5,     /* workspace missing or smaller than required */
+  MLA_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up */
+};
+
+enum mla_kv_dtype {
+  MLA_KV_BF16 = 0,     /* rows of 576 bf16 = 1152 B */
+  MLA_KV_FP8_E4M3 = 1  /* rows of 640 B: 512 OCP E4M3FN codes of c_kv / kv_scale,
+                          then 64 bf16 k_rope values */
+};
+
+enum mla_out_dtype { MLA_OUT_FP32 = 0, MLA_OUT_BF16 = 1 };
+
+enum mla_parts { MLA_PART_CONTEXT = 1, MLA_PART_EXTEND = 2, MLA_PART_ALL = 3 };
+
+/* One relocated document segment of a request's cached context: key tokens
+ * [start, start+len) of request `req`, whose k_rope was cached at canonical
+ * positions so that token start+j carries position (rope_offset + j) - rope_offset
+ * = j.  Queries attend to it with q_rope rotated by (q_pos - rope_offset)
+ * ("RedKnot-MLA: Multi-Head Offline-Online Reuse for DeepSeek-V4 Long-Context
+ * Serving", section 2, "Online position restoration and merge"). */
+typedef struct {
+  int32_t req;
+  int32_t start;
+  int32_t len;
+  int32_t reserved; /* must be 0 */
+  int64_t rope_offset;
+} mla_segment;
+
+/* ------------------------------------------------------------------------
+ * mla_prefill_ctx -- the whole hot path of one layer's chunked prefill.
+ *
+ * Defines ("DeepSeek MLA — Prefix Cache 与 Chunked Prefill 深度解析",
+ * sections 4.2-4.4): for request r with C_r = seq_lens[r] - E_r cached context
+ * tokens and E_r = cu_q[r+1] - cu_q[r] new (extend) tokens, query i (global row
+ * cu_q[r] + i, token index C_r + i, RoPE position q_pos[row]) and head h:
+ *   context stage: keys = the request's segments (default one segment
+ *     [0, C_r) with rope_offset 0), cut into chunks of `chunk` tokens;
+ *   extend stage : keys C_r .. C_r + i (causal, diagonal included), offset 0;
+ *   each key t: x_t = row of token t via block_table[r][t/64], slot t%64
+ *     (FP8: c_kv = e4m3 * kv_scale); K_nope = c_kv * kv_b_proj[:, K cols of h],
+ *     V = c_kv * kv_b_proj[:, V cols of h]; K = [K_nope | k_rope] (k_rope shared
+ *     by all heads);
+ *   s_t = softmax_scale * (q_nope . K_nope_t + R(q_pos - offset) q_rope . k_rope_t),
+ *     R = rotation of interleaved pairs (2k, 2k+1) by theta^(-2k/64) per unit;
+ *   every chunk and the extend stage give (out, lse = ln sum e^s); they are folded
+ *   with merge_attn_states (see mla_merge_states).
+ * Full K/V never reaches global memory: the up-projection runs on the tensor
+ * cores inside the attention tile loop.
+ *
+ * Arguments
+ *  q            device bf16 [T_q, H, 192]: [q_nope 0..127 | q_rope 128..191],
+ *               q_rope NOT rotated.  T_q = cu_q[num_reqs].
+ *  q_pos        device int32 [T_q]: true RoPE position of each query row.
+ *  kv_cache     device [num_blocks, 64, row]: bf16 row of 576 (kv_dtype
+ *               MLA_KV_BF16) or 640-byte FP8 row (MLA_KV_FP8_E4M3).
+ *  kv_scale     FP8 per-tensor dequant scale (ignored for bf16).
+ *  block_table  device int32 [num_reqs, max_blocks_per_req].  Entries that
+ *               the request's tokens use must lie in [0, num_blocks).
+ *  seq_lens     HOST int32 [num_reqs]: C_r + E_r (extend rows are in the cache).
+ *  cu_q         HOST int32 [num_reqs + 1]: prefix sums of E_r, cu_q[0] = 0.
+ *  segments     HOST, optional (NULL, num_segments = 0 for the default): every
+ *               segment lies in [0, C_r) of its request; segments of a request
+ *               must not overlap.  A request with no segment listed while
+ *               segments != NULL has an empty context.
+ *  chunk        context chunk length, a positive multiple of 64.
+ *  kv_b_proj    device bf16 [512, H*256]: columns 0..H*128-1 are the K_nope
+ *               blocks of heads 0..H-1, columns H*128.. are the V blocks.
+ *  softmax_scale, rope_theta  scalars (rope_theta > 1).
+ *  parts        MLA_PART_CONTEXT | MLA_PART_EXTEND.
+ *  out          device [T_q, H, 128], fp32 or bf16 per out_dtype.
+ *  lse          device fp32 [T_q, H], natural log, softmax scale included;
+ *               -inf for a row with no visible key (its out row is 0).
+ *  workspace    device, at least mla_prefill_workspace_size(...) bytes, 256-B
+ *               aligned; holds fp32 partial states and the device error word.
+ *               Must not be shared by calls that may overlap on the GPU.
+ *  H            num_heads in [1, 128].
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H > 128, chunk not a
+ * multiple of 64), MLA_ERR_WORKSPACE, MLA_ERR_CUDA.  Bad block ids are reported
+ * by mla_get_device_error(workspace, stream) after the call.
+ * ---------------------------------------------------------------------- */
+size_t mla_prefill_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q,
+                                  int num_heads, const mla_segment* segments, int num_segments,
+                                  int chunk, int parts);
+
+int mla_prefill_ctx(const void* q, const int32_t* q_pos,
+                    const void* kv_cache, int kv_dtype, float kv_scale, int num_blocks,
+                    const int32_t* block_table, int max_blocks_per_req,
+                    const int32_t* seq_lens, const int32_t* cu_q, int num_reqs, int num_heads,
+                    const mla_segment* segments, int num_segments, int chunk,
+                    const void* kv_b_proj, float softmax_scale, float rope_theta, int parts,
+                    void* out, int out_dtype, float* lse,
+                    void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* Reads and clears the device error word kept in `workspace` (synchronises
+ * `stream`).  Returns MLA_OK, MLA_ERR_BAD_BLOCK_ID or MLA_ERR_TIMEOUT. */
+int mla_get_device_error(void* workspace, mla_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * mla_merge_states -- merge_attn_states ("DeepSeek MLA — Prefix Cache 与
+ * Chunked Prefill 深度解析", section 4.3), one warp per row:
+ *   m = max(lse_a, lse_b); wa = e^(lse_a - m); wb = e^(lse_b - m);
+ *   out = (wa out_a + wb out_b) / (wa + wb);  lse = m + ln(wa + wb);
+ * two rows with lse = -inf merge to (0, -inf).
+ *  out_a, out_b, out   device fp32 [rows, d_v]; out may alias out_a or out_b.
+ *  lse_a, lse_b, lse   device fp32 [rows]; lse may alias lse_a or lse_b.
+ *  d_v                 a positive multiple of 4 (128 on the prefill path).
+ * ---------------------------------------------------------------------- */
+int mla_merge_states(const float* out_a, const float* lse_a, const float* out_b, const float* lse_b,
+                     float* out, float* lse, int64_t rows, int d_v, mla_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * mla_rope_relocate -- query-side RoPE relocation ("RedKnot-MLA ...", section
+ * 2, "Online position restoration and merge"): rotate the 64 RoPE columns of
+ * every (token, head) row of x by angle (pos[token] - offset) * theta^(-2k/64)
+ * on interleaved pairs (2k, 2k+1), k = 0..31.
+ *  x, y        device bf16 [tokens, heads, row_stride]; the RoPE part is
+ *              columns rope_col .. rope_col+63 (rope_col a multiple of 8).
+ *              Only those columns of y are written; y may equal x.
+ *  pos         device int32 [tokens].
+ * ---------------------------------------------------------------------- */
+int mla_rope_relocate(const void* x, const int32_t* pos, int64_t offset, float theta, void* y,
+                      int tokens, int heads, int row_stride, int rope_col, mla_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * mla_gather_latent -- _gather_cache of one request's token range
+ * ("DeepSeek MLA — Prefix Cache 与 Chunked Prefill 深度解析", section 4.4,
+ * step 1): dst[i] = row of token start+i (block_table_row[t/64], slot t%64),
+ * as 576 bf16 values.  FP8 rows are dequantised to bf16(e4m3 * kv_scale),
+ * rounded to nearest even; bf16 rows are copied bit-exactly.
+ *  block_table_row  device int32 [max_blocks]: one request's row.
+ *  dst              device bf16 [len, 576].
+ *  dev_error        device uint32, optional: bit 0 is set when an entry is
+ *                   outside [0, num_blocks) (that row of dst is zeroed).
+ * ---------------------------------------------------------------------- */
+int mla_gather_latent(const void* kv_cache, int kv_dtype, float kv_scale, int num_blocks,
+                      const int32_t* block_table_row, int max_blocks, int start, int len,
+                      void* dst, uint32_t* dev_error, mla_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* mla_status_string(int status);
+
+/* Text of the last CUDA runtime error seen by this thread's calls ("" if none). */
+const char* mla_last_cuda_error(void);
+
+/* Number of kernels this library has launched in this process (all threads). */
+uint64_t mla_launch_count(void);
+
+/* ABI version: 1. */
+int mla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_H_ */

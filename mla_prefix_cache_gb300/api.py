@@ -1,0 +1,177 @@
+"""PyTorch-facing binding of libmla: argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; this module checks
+tensor placement/dtypes, allocates outputs and the workspace with torch when the
+caller does not pass them, and forwards raw pointers and the current stream.
+There is no CPU fallback: without a CUDA device or the built library every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import (KV_BF16, KV_FP8_E4M3, OUT_BF16, OUT_FP32, PART_ALL, PART_CONTEXT,  # noqa: F401
+                   PART_EXTEND, MLAError)
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> ctypes.c_void_p:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def launch_count() -> int:
+    """Kernels launched by libmla so far in this process."""
+    return int(_lib.load().mla_launch_count())
+
+
+def kv_dtype_code(kv_cache: torch.Tensor) -> int:
+    if kv_cache.dtype == torch.bfloat16 and kv_cache.shape[-1] == 576:
+        return KV_BF16
+    if kv_cache.dtype == torch.uint8 and kv_cache.shape[-1] == 640:
+        return KV_FP8_E4M3
+    raise ValueError("kv_cache must be bf16 [NB,64,576] or uint8 [NB,64,640]")
+
+
+def prefill_workspace_size(seq_lens, cu_q, num_heads: int, segments=None, chunk: int = 4096,
+                           parts: int = PART_ALL) -> int:
+    sl, _k1 = _lib.i32_host(seq_lens)
+    cq, _k2 = _lib.i32_host(cu_q)
+    sp, ns, _k3 = _lib.segments_host(segments)
+    n = _lib.load().mla_prefill_workspace_size(len(_k1), sl, cq, int(num_heads), sp, ns, int(chunk), int(parts))
+    if n == 0:
+        raise MLAError("mla_prefill_workspace_size", _lib.MLA_ERR_INVALID_ARG)
+    return int(n)
+
+
+def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+            seq_lens, cu_q, kv_b_proj: torch.Tensor, *, chunk: int, softmax_scale: float,
+            rope_theta: float = 10000.0, kv_scale: float = 1.0, segments=None, parts: int = PART_ALL,
+            out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
+            lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """MLA chunked prefill of one layer (mla_prefill_ctx).
+
+    q bf16 [T_q, H, 192] (q_rope unrotated); q_pos int32 [T_q]; kv_cache bf16
+    [NB,64,576] or uint8 [NB,64,640] (FP8); block_table int32 [B, max_blocks];
+    seq_lens / cu_q host int32 (numpy or lists); kv_b_proj bf16 [512, H*256];
+    segments optional host [S,4] (req, start, len, rope_offset).
+    Returns (out [T_q, H, 128] in out_dtype, lse fp32 [T_q, H])."""
+    T_q, H = int(q.shape[0]), int(q.shape[1])
+    L = _lib.load()
+    sl, keep_sl = _lib.i32_host(seq_lens)
+    cq, keep_cq = _lib.i32_host(cu_q)
+    sp, ns, keep_sp = _lib.segments_host(segments)
+    B = int(keep_sl.shape[0])
+    if keep_cq.shape[0] != B + 1 or int(keep_cq[-1]) != T_q:
+        raise ValueError("cu_q must have num_reqs+1 entries ending at T_q")
+    dev = q.device
+    if out is None:
+        out = torch.empty((T_q, H, 128), dtype=out_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
+    ws_bytes = prefill_workspace_size(keep_sl, keep_cq, H, segments, chunk, parts)
+    if workspace is None or workspace.numel() * workspace.element_size() < ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_FP32
+    st = L.mla_prefill_ctx(
+        _dev(q, "q", torch.bfloat16), _dev(q_pos, "q_pos", torch.int32), _dev(kv_cache, "kv_cache"),
+        kv_dtype_code(kv_cache), float(kv_scale), int(kv_cache.shape[0]),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        sl, cq, B, H, sp, ns, int(chunk), _dev(kv_b_proj, "kv_b_proj", torch.bfloat16),
+        float(softmax_scale), float(rope_theta), int(parts),
+        _dev(out, "out", (torch.float32, torch.bfloat16)), od, _dev(lse, "lse", torch.float32),
+        _dev(workspace, "workspace"), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+        _stream_ptr(stream))
+    _lib.check("mla_prefill_ctx", st)
+    prefill.last_workspace = workspace
+    return out, lse
+
+
+def device_error(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Reads and clears the device error word of a prefill workspace."""
+    return int(_lib.load().mla_get_device_error(_dev(workspace, "workspace"), _stream_ptr(stream)))
+
+
+def merge_states(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):
+    """merge_attn_states on fp32 [rows, d_v] states and fp32 [rows] lse."""
+    d_v = int(out_a.shape[-1])
+    rows = int(out_a.numel() // d_v)
+    out = torch.empty_like(out_a) if out is None else out
+    lse = torch.empty_like(lse_a) if lse is None else lse
+    f32 = torch.float32
+    st = _lib.load().mla_merge_states(_dev(out_a, "out_a", f32), _dev(lse_a, "lse_a", f32), _dev(out_b, "out_b", f32),
+                                      _dev(lse_b, "lse_b", f32), _dev(out, "out", f32), _dev(lse, "lse", f32),
+                                      rows, d_v, _stream_ptr(stream))
+    _lib.check("mla_merge_states", st)
+    return out, lse
+
+
+def rope_relocate(x: torch.Tensor, pos: torch.Tensor, offset: int, theta: float = 10000.0,
+                  y: Optional[torch.Tensor] = None, rope_col: Optional[int] = None, stream=None) -> torch.Tensor:
+    """Rotate the 64 RoPE columns of bf16 x [tokens, heads, row] by (pos - offset)."""
+    tokens, heads, row = int(x.shape[0]), int(x.shape[1]), int(x.shape[2])
+    rope_col = row - 64 if rope_col is None else int(rope_col)
+    if y is None:
+        y = x.clone()
+    st = _lib.load().mla_rope_relocate(_dev(x, "x", torch.bfloat16), _dev(pos, "pos", torch.int32), int(offset),
+                                       float(theta), _dev(y, "y", torch.bfloat16), tokens, heads, row, rope_col,
+                                       _stream_ptr(stream))
+    _lib.check("mla_rope_relocate", st)
+    return y
+
+
+def gather_latent(kv_cache: torch.Tensor, block_table_row: torch.Tensor, start: int, length: int,
+                  kv_scale: float = 1.0, dst: Optional[torch.Tensor] = None,
+                  dev_error: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Rows of tokens [start, start+length) of one request as bf16 [length, 576]."""
+    if dst is None:
+        dst = torch.empty((length, 576), dtype=torch.bfloat16, device=kv_cache.device)
+    errp = _dev(dev_error, "dev_error", (torch.int32, torch.uint32)) if dev_error is not None else None
+    st = _lib.load().mla_gather_latent(_dev(kv_cache, "kv_cache"), kv_dtype_code(kv_cache), float(kv_scale),
+                                       int(kv_cache.shape[0]), _dev(block_table_row, "block_table_row", torch.int32),
+                                       int(block_table_row.shape[0]), int(start), int(length),
+                                       _dev(dst, "dst", torch.bfloat16), errp, _stream_ptr(stream))
+    _lib.check("mla_gather_latent", st)
+    return dst
+
+
+# ---------------------------------------------------------------- workloads
+
+class DeviceWorkload:
+    """Device copies of a workload's inputs (see workload.Workload)."""
+
+    def __init__(self, wl, device="cuda"):
+        self.wl = wl
+        dev = torch.device(device)
+        self.q = torch.from_numpy(wl.q.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.q_pos = torch.from_numpy(wl.q_pos).to(dev)
+        if wl.kv_dtype == "bf16":
+            self.kv_cache = torch.from_numpy(wl.kv_cache.view(np.int16)).to(dev).view(torch.bfloat16)
+        else:
+            self.kv_cache = torch.from_numpy(wl.kv_cache).to(dev)
+        self.block_table = torch.from_numpy(wl.block_table).to(dev)
+        self.kv_b_proj = torch.from_numpy(wl.kv_b_proj.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.seq_lens = wl.seq_lens
+        self.cu_q = wl.cu_q
+
+    def run(self, parts=PART_ALL, out_dtype=torch.float32, chunk=None, **kw):
+        wl = self.wl
+        return prefill(self.q, self.q_pos, self.kv_cache, self.block_table, self.seq_lens, self.cu_q,
+                       self.kv_b_proj, chunk=wl.chunk if chunk is None else chunk,
+                       softmax_scale=wl.softmax_scale, rope_theta=wl.rope_theta, kv_scale=wl.kv_scale,
+                       segments=wl.segments, parts=parts, out_dtype=out_dtype, **kw)

@@ -1,0 +1,310 @@
+// C-ABI entry points of libmla: argument validation, the host-side planner of
+// KV splits, workspace layout and kernel launches.  See include/mla.h for the
+// contract of each call.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+#include "mla.h"
+
+namespace mla {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+static thread_local char g_cuda_err[256] = "";
+
+static int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MLA_OK;
+  std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return MLA_ERR_CUDA;
+}
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// RoPE inverse frequencies theta^(-2k/64) as binary fractions of a turn per
+// unit position (see rope_sincos).
+static void rope_fracs(double theta, uint64_t* frac) {
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int k = 0; k < kDr / 2; ++k) {
+    const double f = std::pow(theta, -2.0 * k / (double)kDr);
+    const double turns = f / two_pi;                 // in (0, 1/(2 pi)]
+    frac[k] = (uint64_t)std::ldexp(turns, 64);       // < 2^64
+  }
+}
+
+// ------------------------------------------------------------------ planner
+struct Plan {
+  std::vector<Split> splits;
+  std::vector<RowRange> ranges;
+  int max_slots = 0;
+  int64_t total_q = 0;
+};
+
+// Step "plan" of the path: per request, context chunks of every segment and
+// the extend stage become KV splits, each with its own partial-state slot.
+static int build_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,
+                      const mla_segment* segs, int nseg, int chunk, int parts, Plan* plan) {
+  if (num_reqs < 0 || num_heads < 1 || nseg < 0) return MLA_ERR_INVALID_ARG;
+  if (num_heads > kMaxHeads) return MLA_ERR_UNSUPPORTED;
+  if (chunk <= 0) return MLA_ERR_INVALID_ARG;
+  if (chunk % kBlock != 0) return MLA_ERR_UNSUPPORTED;
+  if (parts < 1 || parts > 3) return MLA_ERR_INVALID_ARG;
+  if (num_reqs > 0 && (seq_lens == nullptr || cu_q == nullptr)) return MLA_ERR_INVALID_ARG;
+  if (nseg > 0 && segs == nullptr) return MLA_ERR_INVALID_ARG;
+  if (num_reqs > 0 && cu_q[0] != 0) return MLA_ERR_INVALID_ARG;
+  for (int r = 0; r < num_reqs; ++r) {
+    const int64_t e = (int64_t)cu_q[r + 1] - cu_q[r];
+    if (e < 0 || seq_lens[r] < e) return MLA_ERR_INVALID_ARG;
+  }
+  // segments: inside their request's context, non-overlapping per request
+  std::vector<std::vector<const mla_segment*>> per_req(num_reqs);
+  for (int i = 0; i < nseg; ++i) {
+    const mla_segment& s = segs[i];
+    if (s.req < 0 || s.req >= num_reqs || s.reserved != 0 || s.start < 0 || s.len < 0) return MLA_ERR_INVALID_ARG;
+    const int64_t ctx = (int64_t)seq_lens[s.req] - (cu_q[s.req + 1] - cu_q[s.req]);
+    if ((int64_t)s.start + s.len > ctx) return MLA_ERR_INVALID_ARG;
+    per_req[s.req].push_back(&s);
+  }
+  for (auto& v : per_req) {
+    std::vector<const mla_segment*> sorted(v);
+    std::sort(sorted.begin(), sorted.end(), [](const mla_segment* a, const mla_segment* b) { return a->start < b->start; });
+    for (size_t i = 1; i < sorted.size(); ++i)
+      if (sorted[i - 1]->start + sorted[i - 1]->len > sorted[i]->start) return MLA_ERR_INVALID_ARG;
+  }
+
+  plan->splits.clear();
+  plan->ranges.clear();
+  plan->max_slots = 0;
+  plan->total_q = num_reqs > 0 ? cu_q[num_reqs] : 0;
+  for (int r = 0; r < num_reqs; ++r) {
+    const int E = cu_q[r + 1] - cu_q[r];
+    const int C = seq_lens[r] - E;
+    if (E == 0) continue;
+    int slots = 0;
+    auto add = [&](int k0, int k1, int64_t off) {
+      Split sp{};
+      sp.req = r;
+      sp.q_begin = cu_q[r];
+      sp.q_count = E;
+      sp.q_tok0 = C;
+      sp.k_begin = k0;
+      sp.k_end = k1;
+      sp.slot = slots++;
+      sp.rope_offset = off;
+      plan->splits.push_back(sp);
+    };
+    if (parts & MLA_PART_CONTEXT) {
+      if (segs == nullptr) {
+        for (int c0 = 0; c0 < C; c0 += chunk) add(c0, std::min(c0 + chunk, C), 0);
+      } else {
+        for (const mla_segment* s : per_req[r])
+          for (int c0 = s->start; c0 < s->start + s->len; c0 += chunk)
+            add(c0, std::min(c0 + chunk, s->start + s->len), s->rope_offset);
+      }
+    }
+    if (parts & MLA_PART_EXTEND) add(C, C + E, 0);
+    RowRange rr{};
+    rr.row_begin = cu_q[r];
+    rr.row_end = cu_q[r + 1];
+    rr.nslots = slots;
+    plan->ranges.push_back(rr);
+    plan->max_slots = std::max(plan->max_slots, slots);
+  }
+  return MLA_OK;
+}
+
+struct WsLayout {
+  size_t err_off = 0, lse_off = 0, out_off = 0, total = 0;
+};
+
+static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static WsLayout ws_layout(const Plan& plan, int num_heads) {
+  WsLayout w;
+  const size_t rows = (size_t)plan.max_slots * (size_t)plan.total_q * (size_t)num_heads;
+  w.err_off = 0;
+  w.lse_off = 256;
+  w.out_off = w.lse_off + up256(rows * sizeof(float));
+  w.total = w.out_off + rows * kDv * sizeof(float);
+  return w;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int mla_abi_version(void) { return 1; }
+
+uint64_t mla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* mla_last_cuda_error(void) { return g_cuda_err; }
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_BAD_BLOCK_ID: return "MLA_ERR_BAD_BLOCK_ID";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+size_t mla_prefill_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,
+                                  const mla_segment* segments, int num_segments, int chunk, int parts) {
+  Plan plan;
+  if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
+    return 0;
+  return ws_layout(plan, num_heads).total;
+}
+
+int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                    int num_blocks, const int32_t* block_table, int max_blocks_per_req, const int32_t* seq_lens,
+                    const int32_t* cu_q, int num_reqs, int num_heads, const mla_segment* segments,
+                    int num_segments, int chunk, const void* kv_b_proj, float softmax_scale, float rope_theta,
+                    int parts, void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                    mla_stream_t stream) {
+  Plan plan;
+  int st = build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan);
+  if (st != MLA_OK) return st;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_OUT_FP32 && out_dtype != MLA_OUT_BF16) return MLA_ERR_INVALID_ARG;
+  if (!(rope_theta > 1.f) || !std::isfinite(softmax_scale) || !std::isfinite(rope_theta)) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_KV_FP8_E4M3 && !(std::isfinite(kv_scale) && kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (plan.total_q == 0) return MLA_OK;
+  if (!q || !q_pos || !kv_cache || !block_table || !kv_b_proj || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (num_blocks <= 0 || max_blocks_per_req <= 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(kv_b_proj, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  for (int r = 0; r < num_reqs; ++r)
+    if ((seq_lens[r] + kBlock - 1) / kBlock > max_blocks_per_req) return MLA_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(plan, num_heads);
+  if (workspace == nullptr || workspace_bytes < wl.total || !aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws + wl.err_off);
+  st = cuda_status(cudaMemsetAsync(err, 0, sizeof(uint32_t), s));
+  if (st != MLA_OK) return st;
+
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const uint16_t*>(q);
+  p.q_pos = q_pos;
+  p.kv_cache = static_cast<const uint8_t*>(kv_cache);
+  p.block_table = block_table;
+  p.w = static_cast<const uint16_t*>(kv_b_proj);
+  p.part_out = reinterpret_cast<float*>(ws + wl.out_off);
+  p.part_lse = reinterpret_cast<float*>(ws + wl.lse_off);
+  p.err = err;
+  p.slot_stride_rows = plan.total_q;
+  p.num_heads = num_heads;
+  p.kv_fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  p.kv_scale = kv_scale;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_req;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  rope_fracs((double)rope_theta, p.rope_frac);
+
+  for (size_t b = 0; b < plan.splits.size(); b += kMaxSplitsPerLaunch) {
+    const size_t n = std::min(plan.splits.size() - b, (size_t)kMaxSplitsPerLaunch);
+    int tiles = 0;
+    for (size_t i = 0; i < n; ++i) {
+      Split sp = plan.splits[b + i];
+      sp.tile_begin = tiles;
+      tiles += (sp.q_count + 127) / 128;
+      p.splits[i] = sp;
+    }
+    p.num_splits = (int)n;
+    p.num_tiles = tiles;
+    st = cuda_status(launch_prefill(p, s));
+    if (st != MLA_OK) return st;
+  }
+
+  MergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  mp.part_out = p.part_out;
+  mp.part_lse = p.part_lse;
+  mp.slot_stride_rows = plan.total_q;
+  mp.out = out;
+  mp.lse = lse;
+  mp.out_bf16 = out_dtype == MLA_OUT_BF16;
+  mp.num_heads = num_heads;
+  for (size_t b = 0; b < plan.ranges.size(); b += kMaxRangesPerLaunch) {
+    const size_t n = std::min(plan.ranges.size() - b, (size_t)kMaxRangesPerLaunch);
+    int rows = 0;
+    for (size_t i = 0; i < n; ++i) {
+      RowRange rr = plan.ranges[b + i];
+      rr.prefix = rows;
+      rows += rr.row_end - rr.row_begin;
+      mp.ranges[i] = rr;
+    }
+    mp.num_ranges = (int)n;
+    mp.total_rows = rows;
+    st = cuda_status(launch_merge_slots(mp, s));
+    if (st != MLA_OK) return st;
+  }
+  return MLA_OK;
+}
+
+int mla_get_device_error(void* workspace, mla_stream_t stream) {
+  if (workspace == nullptr) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  int st = cuda_status(cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s));
+  if (st == MLA_OK) st = cuda_status(cudaStreamSynchronize(s));
+  if (st != MLA_OK) return st;
+  st = cuda_status(cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s));
+  if (st != MLA_OK) return st;
+  if (word & kErrBadBlock) return MLA_ERR_BAD_BLOCK_ID;
+  if (word & kErrTimeout) return MLA_ERR_TIMEOUT;
+  return MLA_OK;
+}
+
+int mla_merge_states(const float* out_a, const float* lse_a, const float* out_b, const float* lse_b, float* out,
+                     float* lse, int64_t rows, int d_v, mla_stream_t stream) {
+  if (rows < 0 || d_v <= 0 || d_v % 4 != 0) return MLA_ERR_INVALID_ARG;
+  if (rows == 0) return MLA_OK;
+  if (!out_a || !lse_a || !out_b || !lse_b || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (!aligned(out_a, 16) || !aligned(out_b, 16) || !aligned(out, 16)) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_merge2(out_a, lse_a, out_b, lse_b, out, lse, rows, d_v,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mla_rope_relocate(const void* x, const int32_t* pos, int64_t offset, float theta, void* y, int tokens,
+                      int heads, int row_stride, int rope_col, mla_stream_t stream) {
+  if (tokens < 0 || heads < 0) return MLA_ERR_INVALID_ARG;
+  if (rope_col < 0 || rope_col % 8 != 0 || row_stride % 8 != 0 || rope_col + kDr > row_stride) return MLA_ERR_INVALID_ARG;
+  if (!(theta > 1.f) || !std::isfinite(theta)) return MLA_ERR_INVALID_ARG;
+  if (tokens == 0 || heads == 0) return MLA_OK;
+  if (!x || !pos || !y || !aligned(x, 16) || !aligned(y, 16)) return MLA_ERR_INVALID_ARG;
+  uint64_t frac[kDr / 2];
+  rope_fracs((double)theta, frac);
+  return cuda_status(launch_rope(static_cast<const uint16_t*>(x), pos, offset, frac, static_cast<uint16_t*>(y),
+                                 tokens, heads, row_stride, rope_col, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mla_gather_latent(const void* kv_cache, int kv_dtype, float kv_scale, int num_blocks,
+                      const int32_t* block_table_row, int max_blocks, int start, int len, void* dst,
+                      uint32_t* dev_error, mla_stream_t stream) {
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (start < 0 || len < 0 || num_blocks <= 0 || max_blocks <= 0) return MLA_ERR_INVALID_ARG;
+  if (((int64_t)start + len + kBlock - 1) / kBlock > max_blocks) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_KV_FP8_E4M3 && !(std::isfinite(kv_scale) && kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (len == 0) return MLA_OK;
+  if (!kv_cache || !block_table_row || !dst || !aligned(kv_cache, 16) || !aligned(dst, 16)) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_gather(static_cast<const uint8_t*>(kv_cache), kv_dtype == MLA_KV_FP8_E4M3, kv_scale,
+                                   num_blocks, block_table_row, max_blocks, start, len, static_cast<uint16_t*>(dst),
+                                   dev_error, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+// Internal structures shared by the C-ABI layer (host planner) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+constexpr int kDc = 512;
+constexpr int kDr = 64;
+constexpr int kDnope = 128;
+constexpr int kDv = 128;
+constexpr int kDqk = kDnope + kDr;
+constexpr int kBlock = 64;
+constexpr int kRowBf16 = kDc + kDr;          // elements
+constexpr int kRowBytesBf16 = 2 * kRowBf16;  // 1152
+constexpr int kRowBytesFp8 = kDc + 2 * kDr;  // 640
+constexpr int kMaxHeads = 128;
+
+// Device error word bits (kept in the caller's workspace).
+constexpr uint32_t kErrBadBlock = 1u;
+constexpr uint32_t kErrTimeout = 2u;
+
+// One KV split: a contiguous key range of one request with one RoPE offset.
+// Every split gives a partial (out, lse) per (query row, head) in `slot`.
+struct Split {
+  int32_t req;        // request index (block-table row)
+  int32_t q_begin;    // global row of the request's first query
+  int32_t q_count;    // E_r
+  int32_t q_tok0;     // token index of the request's first query (= C_r)
+  int32_t k_begin;    // first key token
+  int32_t k_end;      // one past the last key token
+  int32_t slot;       // partial-state slot of this split within its request
+  int32_t tile_begin; // first CTA (blockIdx.x) of this split
+  int64_t rope_offset;
+};
+
+constexpr int kMaxSplitsPerLaunch = 192;
+
+struct PrefillParams {
+  const uint16_t* q;          // bf16 [T_q, H, 192]
+  const int32_t* q_pos;       // [T_q]
+  const uint8_t* kv_cache;    // rows of 1152 B or 640 B
+  const int32_t* block_table; // [B, max_blocks]
+  const uint16_t* w;          // bf16 [512, H*256]
+  float* part_out;            // fp32 [slots, T_q, H, 128]
+  float* part_lse;            // fp32 [slots, T_q, H]
+  uint32_t* err;
+  int64_t slot_stride_rows;   // T_q
+  int num_heads;
+  int kv_fp8;
+  float kv_scale;
+  int num_blocks;
+  int max_blocks;
+  float scale_log2;           // softmax_scale * log2(e)
+  int num_splits;
+  int num_tiles;              // gridDim.x
+  uint64_t rope_frac[kDr / 2];
+  Split splits[kMaxSplitsPerLaunch];
+};
+
+// Query rows [row_begin, row_end) whose partial states live in slots 0..nslots-1.
+struct RowRange {
+  int32_t row_begin;
+  int32_t row_end;
+  int32_t nslots;
+  int32_t prefix;             // rows of the launch's earlier ranges
+};
+
+constexpr int kMaxRangesPerLaunch = 512;
+
+struct MergeParams {
+  const float* part_out;      // [slots, T_q, H, 128]
+  const float* part_lse;      // [slots, T_q, H]
+  int64_t slot_stride_rows;   // T_q
+  void* out;                  // [T_q, H, 128] fp32 or bf16
+  float* lse;                 // [T_q, H]
+  int out_bf16;
+  int num_heads;
+  int num_ranges;
+  int total_rows;             // sum of range lengths in this launch
+  RowRange ranges[kMaxRangesPerLaunch];
+};
+
+// Kernel launchers (return cudaError_t of the launch).
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s);
+cudaError_t launch_merge_slots(const MergeParams& p, cudaStream_t s);
+cudaError_t launch_merge2(const float* oa, const float* la, const float* ob, const float* lb,
+                          float* o, float* l, int64_t rows, int d_v, cudaStream_t s);
+cudaError_t launch_rope(const uint16_t* x, const int32_t* pos, int64_t offset, const uint64_t* frac_host,
+                        uint16_t* y, int tokens, int heads, int row_stride, int rope_col,
+                        cudaStream_t s);
+cudaError_t launch_gather(const uint8_t* cache, int fp8, float scale, int num_blocks,
+                          const int32_t* table_row, int max_blocks, int start, int len,
+                          uint16_t* dst, uint32_t* err, cudaStream_t s);
+
+void count_launch(int n = 1);
+
+}  // namespace mla

@@ -1,0 +1,103 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol that
+include/mla.h declares, and its host-side validation and planner behave."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from mla_prefix_cache_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, n
+
+
+def test_status_strings(lib):
+    assert _lib.status_string(0) == "MLA_OK"
+    assert _lib.status_string(5) == "MLA_ERR_WORKSPACE"
+    assert lib.mla_abi_version() == 1
+
+
+def _ws(lib, seq, cu, H, segs=None, chunk=128, parts=3):
+    sl, k1 = _lib.i32_host(seq)
+    cq, k2 = _lib.i32_host(cu)
+    sp, ns, k3 = _lib.segments_host(segs)
+    return lib.mla_prefill_workspace_size(len(k1), sl, cq, H, sp, ns, chunk, parts)
+
+
+def test_workspace_size_follows_plan(lib):
+    # 1 request: C=256 in chunks of 128 -> 2 context splits + 1 extend = 3 slots
+    T, H = 64, 8
+    n = _ws(lib, [320], [0, 64], H, chunk=128)
+    rows = 3 * T * H
+    lse = ((rows * 4 + 255) // 256) * 256
+    assert n == 256 + lse + rows * 128 * 4
+    # context only, chunk larger than C -> 1 slot
+    assert _ws(lib, [320], [0, 64], H, chunk=4096, parts=1) == 256 + ((T * H * 4 + 255) // 256) * 256 + T * H * 512
+    # segments: 4 documents of 64 + extend = 5 slots
+    segs = [[0, 64 * d, 64, 64 * d] for d in range(4)]
+    n5 = _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64)
+    assert n5 == 256 + 256 + 5 * 2 * 512
+
+
+@pytest.mark.parametrize("bad", [
+    dict(chunk=100),                 # not a multiple of 64 -> unsupported
+    dict(H=129),                     # more heads than supported
+    dict(cu=[1, 64]),                # cu_q[0] != 0
+    dict(seq=[10], cu=[0, 64]),      # extend longer than sequence
+    dict(segs=[[0, 200, 100, 0]]),   # segment past the context
+    dict(segs=[[0, 0, 64, 0], [0, 32, 64, 0]]),  # overlapping segments
+    dict(parts=0),
+])
+def test_planner_rejects(lib, bad):
+    args = dict(seq=[320], cu=[0, 64], H=8, segs=None, chunk=128, parts=3)
+    args.update(bad)
+    assert _ws(lib, args["seq"], args["cu"], args["H"], args["segs"], args["chunk"], args["parts"]) == 0
+
+
+def test_prefill_host_validation_without_gpu(lib):
+    """Invalid calls return a status before any CUDA call is made."""
+    sl, k1 = _lib.i32_host([320])
+    cq, k2 = _lib.i32_host([0, 64])
+    dummy = ctypes.c_void_p(4096)
+    def call(chunk=128, H=8, ws=None, ws_bytes=0, kv_dtype=0, theta=10000.0):
+        return lib.mla_prefill_ctx(dummy, dummy, dummy, kv_dtype, 1.0, 8, dummy, 8, sl, cq, 1, H, None, 0, chunk,
+                                   dummy, 0.07, theta, 3, dummy, 0, dummy, ws, ws_bytes, None)
+    assert call(chunk=100) == _lib.MLA_ERR_UNSUPPORTED
+    assert call(H=200) == _lib.MLA_ERR_UNSUPPORTED
+    assert call(kv_dtype=7) == _lib.MLA_ERR_INVALID_ARG
+    assert call(theta=0.5) == _lib.MLA_ERR_INVALID_ARG
+    assert call(ws=None, ws_bytes=0) == _lib.MLA_ERR_WORKSPACE
+    assert call(ws=ctypes.c_void_p(4096 + 8), ws_bytes=1 << 30) == _lib.MLA_ERR_WORKSPACE  # misaligned
+
+
+def test_other_entry_points_validate(lib):
+    d = ctypes.c_void_p(4096)
+    assert lib.mla_merge_states(d, d, d, d, d, d, 10, 6, None) == _lib.MLA_ERR_INVALID_ARG   # d_v % 4
+    assert lib.mla_merge_states(d, d, d, d, d, d, 0, 128, None) == _lib.MLA_OK               # nothing to do
+    assert lib.mla_rope_relocate(d, d, 0, 10000.0, d, 4, 2, 192, 130, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_rope_relocate(d, d, 0, 10000.0, d, 4, 2, 192, 136, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_gather_latent(d, 0, 1.0, 4, d, 2, 100, 64, d, None, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_gather_latent(d, 1, 0.0, 4, d, 2, 0, 64, d, None, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_get_device_error(None, None) == _lib.MLA_ERR_INVALID_ARG

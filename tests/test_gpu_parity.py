@@ -1,0 +1,191 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Tolerances (bf16 inputs, fp32 accumulation): out max abs <= 2e-2 and mean abs
+<= 2e-3, lse within 1e-3, plus a stricter internal gate of relative RMS error
+<= 1e-2 on out.  Gather and block-table indexing are bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from mla_prefix_cache_gb300 import workload as W
+from oracle import mla_oracle as O
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+OUT_MAX, OUT_MEAN, LSE_MAX, REL_RMS = 2e-2, 2e-3, 1e-3, 1e-2
+
+
+@pytest.fixture(scope="module")
+def api():
+    from mla_prefix_cache_gb300 import api as A
+    from mla_prefix_cache_gb300 import _lib
+    _lib.load()
+    return A
+
+
+def assert_close(out, lse, ref_out, ref_lse):
+    out = np.asarray(out, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    ref_out = np.asarray(ref_out, dtype=np.float64)
+    ref_lse = np.asarray(ref_lse, dtype=np.float64)
+    assert np.isfinite(out).all(), "non-finite output"
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lse), fin), "empty rows differ"
+    err = np.abs(out - ref_out)
+    assert err.max() <= OUT_MAX, f"max abs {err.max():.3e}"
+    assert err.mean() <= OUT_MEAN, f"mean abs {err.mean():.3e}"
+    if fin.any():
+        le = np.abs(lse[fin] - ref_lse[fin]).max()
+        assert le <= LSE_MAX, f"lse err {le:.3e}"
+    den = math.sqrt(float((ref_out ** 2).mean())) or 1.0
+    rel = math.sqrt(float((err ** 2).mean())) / den
+    assert rel <= REL_RMS, f"rel rms {rel:.3e}"
+
+
+def run_and_compare(api, wl, parts=3, out_dtype=None, rows=None, heads=None):
+    dw = api.DeviceWorkload(wl)
+    out, lse = dw.run(parts=parts, out_dtype=out_dtype or torch.float32)
+    torch.cuda.synchronize()
+    assert api.device_error(api.prefill.last_workspace) == 0
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    ref_out, ref_lse = O.mla_prefill(**O.workload_args(wl), parts=parts, rows=rows, heads=heads)
+    if rows is not None:
+        out, lse = out[rows], lse[rows]
+    if heads is not None:
+        out, lse = out[:, heads], lse[:, heads]
+    assert_close(out, lse, ref_out, ref_lse)
+    return out, lse
+
+
+# ---------------------------------------------------------------- gather
+
+def test_gather_bf16_bit_exact(api):
+    wl = W.make_workload("g", 1, [200, 300], [5, 37], seed=21)
+    dw = api.DeviceWorkload(wl)
+    r = 1
+    got = api.gather_latent(dw.kv_cache, dw.block_table[r], 3, 330).cpu().view(torch.int16).numpy().view(np.uint16)
+    t = np.arange(3, 333)
+    exp = wl.kv_cache[wl.block_table[r][t // 64], t % 64]
+    assert np.array_equal(got, exp)
+
+
+def test_gather_fp8_dequant_bit_exact(api):
+    wl = W.make_workload("g8", 1, [130], [70], kv_dtype="fp8_e4m3", seed=22)
+    dw = api.DeviceWorkload(wl)
+    got = api.gather_latent(dw.kv_cache, dw.block_table[0], 0, 200, kv_scale=wl.kv_scale)
+    got = got.cpu().view(torch.int16).numpy().view(np.uint16)
+    t = np.arange(200)
+    raw = wl.kv_cache[wl.block_table[0][t // 64], t % 64]
+    lat = O.e4m3_to_float(raw[:, :512]).astype(np.float32) * np.float32(wl.kv_scale)
+    assert np.array_equal(got[:, :512], W.f32_to_bf16_bits(lat))
+    assert np.array_equal(got[:, 512:], np.ascontiguousarray(raw[:, 512:]).view(np.uint16))
+
+
+def test_gather_bad_block_reports_error(api):
+    wl = W.make_workload("gb", 1, [128], [1], seed=23)
+    dw = api.DeviceWorkload(wl)
+    table = dw.block_table[0].clone()
+    table[1] = 10_000                     # outside the pool
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = api.gather_latent(dw.kv_cache, table, 0, 129, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1
+    g = got.cpu().float().numpy()
+    assert (g[64:128] == 0).all() and np.isfinite(g[:64]).all()
+
+
+# ---------------------------------------------------------------- merge
+
+def test_merge_states_matches_oracle(api):
+    rng = np.random.default_rng(24)
+    rows = 1000
+    oa, ob = rng.standard_normal((rows, 128)).astype(np.float32), rng.standard_normal((rows, 128)).astype(np.float32)
+    la, lb = (rng.standard_normal(rows) * 20).astype(np.float32), (rng.standard_normal(rows) * 20).astype(np.float32)
+    la[::7] = -np.inf
+    lb[::11] = -np.inf
+    ref_o, ref_l = O.merge_attn_states(oa.astype(np.float64), la.astype(np.float64),
+                                       ob.astype(np.float64), lb.astype(np.float64))
+    t = [torch.from_numpy(x).cuda() for x in (oa, la, ob, lb)]
+    o, l = api.merge_states(*t)
+    np.testing.assert_allclose(o.cpu().numpy(), ref_o, atol=1e-5, rtol=1e-5)
+    np.testing.assert_allclose(l.cpu().numpy(), ref_l, atol=1e-5, rtol=1e-6)
+    # in place into the first state
+    api.merge_states(t[0], t[1], t[2], t[3], out=t[0], lse=t[1])
+    np.testing.assert_allclose(t[0].cpu().numpy(), ref_o, atol=1e-5, rtol=1e-5)
+    np.testing.assert_allclose(t[1].cpu().numpy(), ref_l, atol=1e-5, rtol=1e-6)
+
+
+# ---------------------------------------------------------------- rope
+
+def test_rope_relocate_matches_oracle(api):
+    rng = np.random.default_rng(25)
+    T, H = 300, 3
+    x = W.f32_to_bf16_bits(rng.standard_normal((T, H, 192), dtype=np.float32))
+    pos = (rng.integers(0, 300000, size=T)).astype(np.int32)
+    off = 16384 * 7
+    xt = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    y = api.rope_relocate(xt, torch.from_numpy(pos).cuda(), off, 10000.0)
+    y = y.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(y[..., :128], x[..., :128])
+    ref = O.rope_rotate(O.bf16_to_float(x[..., 128:], np.float64), (pos.astype(np.int64) - off)[:, None], 1e4,
+                        np.float64)
+    got = O.bf16_to_float(y[..., 128:], np.float64)
+    assert np.abs(got - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
+    assert (np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6).mean() > 0.999
+
+
+# ---------------------------------------------------------------- prefill
+
+def test_prefill_tiny(api):
+    run_and_compare(api, W.tiny())
+
+
+@pytest.mark.parametrize("case", [
+    dict(H=4, ctx=[300], ext=[200], chunk=128),                       # ragged kv and q tails
+    dict(H=2, ctx=[0], ext=[130], chunk=64),                          # no context
+    dict(H=3, ctx=[64, 0, 777], ext=[1, 64, 129], chunk=256),         # ragged batch
+    dict(H=2, ctx=[513], ext=[77], chunk=192, kv="fp8_e4m3"),         # FP8 cache
+    dict(H=2, ctx=[256], ext=[40], chunk=64, doc=64),                 # relocated documents
+    dict(H=128, ctx=[200], ext=[130], chunk=128),                     # full head count
+])
+def test_prefill_small(api, case):
+    wl = W.make_workload("s", case["H"], case["ctx"], case["ext"], chunk=case["chunk"],
+                         kv_dtype=case.get("kv", "bf16"), doc_len=case.get("doc"), seed=30)
+    run_and_compare(api, wl)
+
+
+@pytest.mark.parametrize("parts", [1, 2])
+def test_prefill_parts(api, parts):
+    wl = W.make_workload("p", 2, [260], [150], chunk=128, seed=31)
+    run_and_compare(api, wl, parts=parts)
+
+
+def test_prefill_bf16_out(api):
+    wl = W.make_workload("b", 2, [190], [70], chunk=128, seed=32)
+    run_and_compare(api, wl, out_dtype=torch.bfloat16)
+
+
+def test_prefill_bad_block_reports_error(api):
+    wl = W.make_workload("e", 2, [256], [16], chunk=128, seed=33)
+    dw = api.DeviceWorkload(wl)
+    dw.block_table[0, 1] = -5
+    out, lse = dw.run()
+    torch.cuda.synchronize()
+    assert api.device_error(api.prefill.last_workspace) == 3    # MLA_ERR_BAD_BLOCK_ID
+    assert torch.isfinite(out).all()
+    assert api.device_error(api.prefill.last_workspace) == 0    # cleared by the read
+
+
+def test_prefill_empty_context_segments(api):
+    # segments given but none for the request -> empty context; extend only
+    wl = W.make_workload("z", 1, [128], [20], chunk=64, seed=34)
+    dw = api.DeviceWorkload(wl)
+    out, lse = api.prefill(dw.q, dw.q_pos, dw.kv_cache, dw.block_table, wl.seq_lens, wl.cu_q, dw.kv_b_proj,
+                           chunk=64, softmax_scale=wl.softmax_scale, segments=np.zeros((0, 4), np.int64))
+    ref = O.mla_prefill(**O.workload_args(wl), parts=2)
+    assert_close(out.cpu().numpy(), lse.cpu().numpy(), *ref)
