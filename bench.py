@@ -1,0 +1,367 @@
+"""Benchmark of MLA chunked prefill over a paged packed-latent KV cache.
+
+One step = one whole mla_prefill_ctx call (plan, fused gather + up-projection +
+attention kernel, merge of the KV splits) for one layer of one workload, with
+every input already resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config v3_8k]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Multi-GPU: the path is run as independent replicas (one process per GPU, the
+same workload each; no collective on the data path), so scaling is weak and
+`value` is the work of all ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MLA chunked-prefill TFLOP/s & prefill tok/s at 1 GB300; % of dense BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20          # > 2x the 129 MB L2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def workload_config(wl, extra=None):
+    c = {"workload": wl.name, "heads": wl.num_heads, "requests": wl.num_reqs,
+         "context_tokens": int(wl.ctx_lens.sum()), "extend_tokens": int(wl.ext_lens.sum()),
+         "chunk": wl.chunk, "kv_dtype": wl.kv_dtype,
+         "segments": 0 if wl.segments is None else int(len(wl.segments)),
+         "d_c": 512, "d_rope": 64, "d_nope": 128, "d_v": 128, "block": 64,
+         "algorithmic_flops_per_step": wl.algorithmic_flops()}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(wl, n_heads):
+    """Runs the oracle for the first n_heads heads, all query rows; returns
+    (seconds, algorithmic flops of that sample)."""
+    from oracle import mla_oracle
+    heads = list(range(n_heads))
+    t0 = time.perf_counter()
+    mla_oracle.mla_prefill(**mla_oracle.workload_args(wl), heads=heads)
+    dt = time.perf_counter() - t0
+    return dt, wl.algorithmic_flops() * n_heads / wl.num_heads
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    workload: whole heads (all rows, all keys) until ~budget_s of work."""
+    dt1, f1 = oracle_sample(wl, 1)
+    n = max(1, min(wl.num_heads, int(budget_s / max(dt1, 1e-3))))
+    if n > 1:
+        dt, f = oracle_sample(wl, n)
+    else:
+        dt, f = dt1, f1
+    return {"value": f / dt / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "sample": f"{n} of {wl.num_heads} heads x all {wl.total_q} query rows x all keys of "
+                      f"{wl.name} (numpy fp32, {dt:.1f} s)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from mla_prefix_cache_gb300 import workload
+    wl = workload.by_name(args.config)
+    dt1, _ = oracle_sample(wl, 1)
+    per_step = min(args.ref_step_s, 150.0 / (args.steps + args.warmup))   # whole run within a few minutes
+    n = max(1, min(wl.num_heads, int(per_step / max(dt1, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample(wl, n)
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        dt, f = oracle_sample(wl, n)
+        times.append(dt)
+        flops = f
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    sample = f"{n} of {wl.num_heads} heads x all {wl.total_q} query rows x all keys of {wl.name} per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded)", "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.uuid and parts[1] != self.uuid:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for f in ("prefill.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "mla_prefix_cache_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload_name):
+    """DRAM bytes per launch of the fused kernel from a committed ncu summary,
+    valid only while the kernel source is the one that was profiled."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload_name)
+    if not e or e.get("kernel_sha") != kernel_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from mla_prefix_cache_gb300 import api, workload
+
+    wl = workload.by_name(args.config)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_budget_s)
+
+    dw = api.DeviceWorkload(wl, dev)
+    T_q, H = wl.total_q, wl.num_heads
+    out = torch.empty((T_q, H, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(api.prefill_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dw.run(out=out, lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if api.device_error(ws) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(getattr(torch.cuda.get_device_properties(dev), "uuid", None))
+    uuid = clocks.uuid
+    clocks.uuid = ("GPU-" + str(uuid)) if uuid is not None and not str(uuid).startswith("GPU-") else uuid
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    n0 = api.launch_count()
+    for k in range(K):
+        flush.zero_()                       # L2 flush, outside the step events
+        api.set_kernel_events(*kev[k])
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = api.launch_count() - n0
+    api.set_kernel_events(None, None)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    if api.device_error(ws) != 0:
+        raise RuntimeError("device error word set during the timed steps")
+
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    flops = wl.algorithmic_flops()
+    value = flops * K * world / (total_ms / 1e3) / 1e12
+    tok_s = T_q * K * world / (total_ms / 1e3)
+
+    # ---- end to end through the public API: pinned host inputs in, result out
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        for name in ("q", "q_pos", "kv_cache", "block_table", "kv_b_proj"):
+            d = getattr(dw, name)
+            host[name] = torch.empty(d.shape, dtype=d.dtype, pin_memory=True).copy_(d)
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        bi = sum(v.numel() * v.element_size() for v in host.values())
+        bo = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+        def e2e_step():
+            for name, h in host.items():
+                getattr(dw, name).copy_(h, non_blocking=True)
+            dw.run(out=out, lse=lse, workspace=ws)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(ems, op=dist.ReduceOp.MAX)
+        e2e = {"value": flops * K * world / (float(ems.item()) / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+               "ms_per_step": float(ems.item()) / K}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, source = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    k_ms = sum(kern_ms) / K
+    achieved = flops / (k_ms / 1e3) / 1e12
+    traffic = measured_traffic(wl.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded; shapes of the workload, random values)",
+        "config": workload_config(wl, {"parallelism": f"replicas x{world}",
+                                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB memset outside the "
+                                             "step events)"}),
+        "prefill_tok_s": tok_s,
+        "frac_of_bf16_peak": value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "prefill_tile_kernel",
+                     "peak_source": f"bf16_tflops (burst) of {source} peaks",
+                     "kernel_ms": k_ms, "note": "achieved = algorithmic FLOPs of the step / fused-kernel event time"},
+        "gpu_launches": int(launches),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="v3_8k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--ref-step-s", type=float, default=8.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -178,6 +178,14 @@ int mla_gather_latent(const void* kv_cache, int kv_dtype, float kv_scale, int nu
                       const int32_t* block_table_row, int max_blocks, int start, int len,
                       void* dst, uint32_t* dev_error, mla_stream_t stream);
 
+/* Optional instrumentation.  With both arguments non-NULL (cudaEvent_t handles
+ * created by the caller), every later mla_prefill_ctx call on this process
+ * records `begin` on its stream just before its first fused prefill kernel
+ * launch and `end` just after the last one, so the caller can time the fused
+ * kernel alone with cudaEventElapsedTime.  NULL, NULL turns it off.  The
+ * setting is process-wide; the caller keeps the events alive while it is on. */
+void mla_set_kernel_events(void* begin_event, void* end_event);
+
 /* Human-readable name of a status code (static storage). */
 const char* mla_status_string(int status);
 

@@ -66,6 +66,7 @@ SIGNATURES = {
     "mla_last_cuda_error": (ctypes.c_char_p, []),
     "mla_launch_count": (ctypes.c_uint64, []),
     "mla_abi_version": (c_int, []),
+    "mla_set_kernel_events": (None, [c_void_p, c_void_p]),
 }
 
 _lock = threading.Lock()

@@ -34,6 +34,18 @@ def _dev(t: torch.Tensor, name: str, dtype=None) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def set_kernel_events(begin: Optional[torch.cuda.Event], end: Optional[torch.cuda.Event]) -> None:
+    """Time the fused prefill kernel of later prefill() calls with these events
+    (recorded on the call's stream around the fused kernel launches)."""
+    if begin is None or end is None:
+        _lib.load().mla_set_kernel_events(None, None)
+        return
+    for e in (begin, end):      # torch creates the CUDA event lazily on first record
+        if not e.cuda_event:
+            e.record()
+    _lib.load().mla_set_kernel_events(ctypes.c_void_p(begin.cuda_event), ctypes.c_void_p(end.cuda_event))
+
+
 def launch_count() -> int:
     """Kernels launched by libmla so far in this process."""
     return int(_lib.load().mla_launch_count())

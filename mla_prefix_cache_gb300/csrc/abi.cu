@@ -14,6 +14,8 @@
 namespace mla {
 
 static std::atomic<uint64_t> g_launches{0};
+static std::atomic<void*> g_ev_begin{nullptr};
+static std::atomic<void*> g_ev_end{nullptr};
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 static thread_local char g_cuda_err[256] = "";
@@ -142,6 +144,12 @@ extern "C" {
 
 int mla_abi_version(void) { return 1; }
 
+void mla_set_kernel_events(void* begin_event, void* end_event) {
+  const bool on = begin_event != nullptr && end_event != nullptr;
+  g_ev_begin.store(on ? begin_event : nullptr);
+  g_ev_end.store(on ? end_event : nullptr);
+}
+
 uint64_t mla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* mla_last_cuda_error(void) { return g_cuda_err; }
@@ -215,6 +223,12 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, i
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   rope_fracs((double)rope_theta, p.rope_frac);
 
+  cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
+  cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
+  if (ev_b != nullptr && ev_e != nullptr) {
+    st = cuda_status(cudaEventRecord(ev_b, s));
+    if (st != MLA_OK) return st;
+  }
   for (size_t b = 0; b < plan.splits.size(); b += kMaxSplitsPerLaunch) {
     const size_t n = std::min(plan.splits.size() - b, (size_t)kMaxSplitsPerLaunch);
     int tiles = 0;
@@ -227,6 +241,11 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, i
     p.num_splits = (int)n;
     p.num_tiles = tiles;
     st = cuda_status(launch_prefill(p, s));
+    if (st != MLA_OK) return st;
+  }
+
+  if (ev_b != nullptr && ev_e != nullptr) {
+    st = cuda_status(cudaEventRecord(ev_e, s));
     if (st != MLA_OK) return st;
   }
 

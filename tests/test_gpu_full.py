@@ -1,0 +1,48 @@
+"""Full-size parity on the four large workloads, in the launch configuration the
+bench times: the GPU computes every (row, head); the CPU oracle recomputes a
+sample of rows (first and last of every request, q-tile boundaries, random
+rows) for a few heads, and properties that hold at any size are checked on the
+whole output."""
+import numpy as np
+import pytest
+
+from mla_prefix_cache_gb300 import workload as W
+from oracle import mla_oracle as O
+
+from test_gpu_parity import assert_close, visible_keys
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def sample_rows(wl, rng, n_random=24):
+    cu = wl.cu_q
+    rows = set()
+    for r in range(wl.num_reqs):
+        a, b = int(cu[r]), int(cu[r + 1])
+        for x in (a, a + 1, a + 127, a + 128, b - 1):
+            if a <= x < b:
+                rows.add(x)
+    rows.update(rng.integers(0, wl.total_q, size=n_random).tolist())
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", ["v3_8k", "batched", "fp8_128k", "reloc_256k"])
+def test_full_size_sampled(name):
+    from mla_prefix_cache_gb300 import api
+    wl = W.by_name(name)
+    dw = api.DeviceWorkload(wl)
+    out, lse = dw.run()
+    torch.cuda.synchronize()
+    assert api.device_error(api.prefill.last_workspace) == 0
+    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all())
+    rng = np.random.default_rng(100)
+    rows = sample_rows(wl, rng)
+    heads = [0, int(rng.integers(1, wl.num_heads - 1)), wl.num_heads - 1]
+    ref_out, ref_lse = O.mla_prefill(**O.workload_args(wl), rows=rows, heads=heads)
+    got_out = out[torch.from_numpy(rows).cuda()][:, heads].cpu().numpy()
+    got_lse = lse[torch.from_numpy(rows).cuda()][:, heads].cpu().numpy()
+    assert_close(got_out, got_lse, ref_out, ref_lse, visible_keys(wl)[rows])
+    # every row sees its whole context, so lse >= the log of a positive sum everywhere;
+    # the mean output over all rows/heads stays near zero for zero-mean values
+    assert float(out.abs().max()) < 1.0

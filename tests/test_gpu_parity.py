@@ -4,6 +4,16 @@ same seeded inputs.
 Tolerances (bf16 inputs, fp32 accumulation): out max abs <= 2e-2 and mean abs
 <= 2e-3, lse within 1e-3, plus a stricter internal gate of relative RMS error
 <= 1e-2 on out.  Gather and block-table indexing are bit-exact.
+
+lse and key count: the tensor cores take bf16 operands, so every score
+carries the rounding of K_nope (fp32 -> bf16 after the up-projection) and of the
+rotated q_rope.  For unit-variance scores that is ~1e-3 (one sigma) per score;
+lse averages it over the visible keys, and once a row sees >= 512 keys the
+error stays below ~7e-4 (measured by emulating exactly those roundings in
+numpy: the kernel matched the emulation to three digits).  Every row of the
+full-size workloads sees >= 1024 keys and is held to 1e-3.  Rows of the small
+edge cases that see fewer than 512 keys (down to a single key) are held to
+6e-3, six sigma of one score's rounding error.
 """
 import math
 
@@ -17,6 +27,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 OUT_MAX, OUT_MEAN, LSE_MAX, REL_RMS = 2e-2, 2e-3, 1e-3, 1e-2
+LSE_MAX_FEW_KEYS, FEW_KEYS = 6e-3, 512
 
 
 @pytest.fixture(scope="module")
@@ -27,7 +38,18 @@ def api():
     return A
 
 
-def assert_close(out, lse, ref_out, ref_lse):
+def visible_keys(wl, parts=3):
+    """Number of keys each query row attends to."""
+    n = np.zeros(wl.total_q, dtype=np.int64)
+    cu = wl.cu_q
+    for r in range(wl.num_reqs):
+        E, C = int(wl.ext_lens[r]), int(wl.ctx_lens[r])
+        ctx = C if wl.segments is None else int(sum(s[2] for s in wl.segments if s[0] == r))
+        n[cu[r]:cu[r + 1]] = (ctx if parts & 1 else 0) + (np.arange(1, E + 1) if parts & 2 else 0)
+    return n
+
+
+def assert_close(out, lse, ref_out, ref_lse, nvis=None):
     out = np.asarray(out, dtype=np.float64)
     lse = np.asarray(lse, dtype=np.float64)
     ref_out = np.asarray(ref_out, dtype=np.float64)
@@ -39,8 +61,13 @@ def assert_close(out, lse, ref_out, ref_lse):
     assert err.max() <= OUT_MAX, f"max abs {err.max():.3e}"
     assert err.mean() <= OUT_MEAN, f"mean abs {err.mean():.3e}"
     if fin.any():
-        le = np.abs(lse[fin] - ref_lse[fin]).max()
-        assert le <= LSE_MAX, f"lse err {le:.3e}"
+        tol = np.full(ref_lse.shape, LSE_MAX)
+        if nvis is not None:
+            nv = np.asarray(nvis).reshape(nvis.shape[0], *([1] * (ref_lse.ndim - 1)))
+            tol = np.where(np.broadcast_to(nv, ref_lse.shape) < FEW_KEYS, LSE_MAX_FEW_KEYS, LSE_MAX)
+        le = np.abs(lse - ref_lse)
+        bad = fin & (le > tol)
+        assert not bad.any(), f"lse err {le[fin].max():.3e} (tol {tol[bad].min():.0e} at {np.argwhere(bad)[:3].tolist()})"
     den = math.sqrt(float((ref_out ** 2).mean())) or 1.0
     rel = math.sqrt(float((err ** 2).mean())) / den
     assert rel <= REL_RMS, f"rel rms {rel:.3e}"
@@ -54,11 +81,12 @@ def run_and_compare(api, wl, parts=3, out_dtype=None, rows=None, heads=None):
     out = out.float().cpu().numpy()
     lse = lse.cpu().numpy()
     ref_out, ref_lse = O.mla_prefill(**O.workload_args(wl), parts=parts, rows=rows, heads=heads)
+    nvis = visible_keys(wl, parts)
     if rows is not None:
-        out, lse = out[rows], lse[rows]
+        out, lse, nvis = out[rows], lse[rows], nvis[rows]
     if heads is not None:
         out, lse = out[:, heads], lse[:, heads]
-    assert_close(out, lse, ref_out, ref_lse)
+    assert_close(out, lse, ref_out, ref_lse, nvis)
     return out, lse
 
 
@@ -188,4 +216,4 @@ def test_prefill_empty_context_segments(api):
     out, lse = api.prefill(dw.q, dw.q_pos, dw.kv_cache, dw.block_table, wl.seq_lens, wl.cu_q, dw.kv_b_proj,
                            chunk=64, softmax_scale=wl.softmax_scale, segments=np.zeros((0, 4), np.int64))
     ref = O.mla_prefill(**O.workload_args(wl), parts=2)
-    assert_close(out.cpu().numpy(), lse.cpu().numpy(), *ref)
+    assert_close(out.cpu().numpy(), lse.cpu().numpy(), *ref, visible_keys(wl, 2))
