@@ -179,7 +179,7 @@ class ClockSampler:
 
 def kernel_sha():
     h = hashlib.sha256()
-    for f in ("prefill.cu", "ptx.cuh", "internal.h"):
+    for f in ("fused.cu", "ptx.cuh", "internal.h"):
         with open(os.path.join(ROOT, "mla_prefix_cache_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -331,7 +331,7 @@ def run_ours(args):
         "frac_of_bf16_peak": value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "prefill_tile_kernel",
+                     "kernel": "fused_prefill_kernel",
                      "peak_source": f"bf16_tflops (burst) of {source} peaks",
                      "kernel_ms": k_ms, "note": "achieved = algorithmic FLOPs of the step / fused-kernel event time"},
         "gpu_launches": int(launches),

@@ -1,11 +1,15 @@
 // C-ABI entry points of libmla: argument validation, the host-side planner of
 // KV splits, workspace layout and kernel launches.  See include/mla.h for the
 // contract of each call.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "internal.h"
@@ -136,9 +140,262 @@ static WsLayout ws_layout(const Plan& plan, int num_heads) {
   return w;
 }
 
+
+// ------------------------------------------------------------------ fused path
+static int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  return (v && *v) ? std::atoi(v) : dflt;
+}
+
+static bool use_tile_path() {
+  const char* v = std::getenv("MLA_PREFILL_PATH");
+  return v && std::strcmp(v, "tile") == 0;
+}
+
+struct FusedPlan {
+  std::vector<Piece> pieces;      // LPT order, role_begin unset
+  std::vector<RowRange> merge;    // requests whose pieces go to partial slots
+  int max_slots = 0;
+  int64_t total_q = 0;
+};
+
+// Pieces: each request's key ranges in order (segments / context chunks, then
+// the extend stage); a range joins the previous piece when it continues it
+// with the same RoPE offset and the piece is still below max(chunk, 16384)
+// keys.  The online softmax inside a piece folds its chunks exactly as
+// merge_attn_states would; pieces of one request are folded by the merge
+// kernel.
+static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const int32_t* cu_q, int num_reqs,
+                            int chunk, FusedPlan* fp) {
+  fp->pieces.clear();
+  fp->merge.clear();
+  fp->max_slots = 0;
+  fp->total_q = splits.total_q;
+  const int max_keys = std::max(chunk, env_int("MLA_MAX_PIECE_KEYS", 16384));
+  const int n_prod_cfg = std::max(1, env_int("MLA_PRODUCERS", 2));
+  size_t si = 0;
+  for (int r = 0; r < num_reqs; ++r) {
+    const int E = cu_q[r + 1] - cu_q[r];
+    if (E == 0) continue;
+    const int C = seq_lens[r] - E;
+    std::vector<Piece> pr;
+    std::vector<Split> rs;
+    while (si < splits.splits.size() && splits.splits[si].req == r) rs.push_back(splits.splits[si++]);
+    std::stable_sort(rs.begin(), rs.end(), [](const Split& a, const Split& b) { return a.k_begin < b.k_begin; });
+    for (const Split& sp : rs) {
+      if (sp.k_end <= sp.k_begin) continue;
+      if (!pr.empty() && pr.back().rope_offset == sp.rope_offset && pr.back().k_end == sp.k_begin &&
+          pr.back().k_end - pr.back().k_begin < max_keys) {
+        pr.back().k_end = sp.k_end;
+        continue;
+      }
+      Piece pc{};
+      pc.req = r;
+      pc.q_begin = cu_q[r];
+      pc.q_count = E;
+      pc.q_tok0 = C;
+      pc.k_begin = sp.k_begin;
+      pc.k_end = sp.k_end;
+      pc.rope_offset = sp.rope_offset;
+      pr.push_back(pc);
+    }
+    const int np = (int)pr.size();
+    for (int i = 0; i < np; ++i) {
+      Piece& pc = pr[i];
+      pc.slot = np == 1 ? -1 : i;
+      pc.n_cons = (E + 255) / 256;
+      const int t0 = pc.k_begin & ~(kBlock - 1);
+      const int n_tiles = (pc.k_end - t0 + 127) / 128;
+      pc.n_prod = std::max(1, std::min(n_prod_cfg, (n_tiles + 1) / 2));
+      fp->pieces.push_back(pc);
+    }
+    if (np != 1) {
+      RowRange rr{};
+      rr.row_begin = cu_q[r];
+      rr.row_end = cu_q[r + 1];
+      rr.nslots = np;
+      fp->merge.push_back(rr);
+      fp->max_slots = std::max(fp->max_slots, np);
+    }
+  }
+  // longest pieces first
+  std::stable_sort(fp->pieces.begin(), fp->pieces.end(), [](const Piece& a, const Piece& b) {
+    return (int64_t)a.n_cons * (a.k_end - a.k_begin) > (int64_t)b.n_cons * (b.k_end - b.k_begin);
+  });
+  return MLA_OK;
+}
+
+struct FusedWs {
+  size_t err_off = 0, queue_off = 4, flags_off = 256, flags_bytes = 0, ring_off = 0, lse_off = 0, out_off = 0, total = 0;
+  int pieces_per_launch = 0;
+};
+
+static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads) {
+  FusedWs w;
+  w.pieces_per_launch = std::min((int)fp.pieces.size(), kMaxPieces);
+  const size_t jobs = (size_t)w.pieces_per_launch * num_heads;
+  w.flags_bytes = jobs * 2 * kRingDepth * sizeof(uint32_t);
+  w.ring_off = up256(w.flags_off + w.flags_bytes);
+  const size_t ring_bytes = jobs * kRingDepth * 128 * 256 * sizeof(uint16_t);
+  const size_t rows = (size_t)fp.max_slots * (size_t)fp.total_q * (size_t)num_heads;
+  w.lse_off = up256(w.ring_off + ring_bytes);
+  w.out_off = up256(w.lse_off + rows * sizeof(float));
+  w.total = w.out_off + rows * kDv * sizeof(float);
+  return w;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+static bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t d[3], st[2];
+  cuuint32_t b[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
+  return enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mla
 
 using namespace mla;
+
+static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                         int num_blocks, const int32_t* block_table, int max_blocks, int num_heads,
+                         const void* kv_b_proj, float softmax_scale, float rope_theta, void* out, int out_dtype,
+                         float* lse, void* workspace, const FusedPlan& fp, const FusedWs& fw, cudaStream_t s) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int H = num_heads;
+  const int64_t T_q = fp.total_q;
+  static FusedParams p;            // large; built on the host under a lock
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  std::memset(&p, 0, sizeof(p));
+
+  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const uint64_t cache_rows = (uint64_t)num_blocks * kBlock;
+  bool ok = true;
+  {
+    const uint64_t d[3] = {(uint64_t)kDqk, (uint64_t)H, (uint64_t)T_q};
+    const uint64_t st[2] = {(uint64_t)kDqk * 2, (uint64_t)H * kDqk * 2};
+    const uint32_t b[3] = {64, 1, 128};
+    ok &= encode_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!fp8) {
+    const uint64_t d[2] = {(uint64_t)kRowBf16, cache_rows};
+    const uint64_t st[1] = {(uint64_t)kRowBytesBf16};
+    const uint32_t b[2] = {64, 64};
+    ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    p.tm_c = p.tm_kr;
+  } else {
+    const uint64_t d[2] = {(uint64_t)kRowBytesFp8, cache_rows};
+    const uint64_t st[1] = {(uint64_t)kRowBytesFp8};
+    const uint32_t bkr[2] = {128, 64}, bc[2] = {64, 64};
+    ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_cache, d, st, bkr, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= encode_map(&p.tm_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_cache, d, st, bc, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  {
+    const uint64_t d[2] = {(uint64_t)H * (kDnope + kDv), (uint64_t)kDc};
+    const uint64_t st[1] = {(uint64_t)H * (kDnope + kDv) * 2};
+    const uint32_t b[2] = {64, 64};
+    ok &= encode_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_b_proj, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  {
+    const uint64_t jobs = (uint64_t)std::max(fw.pieces_per_launch, 1) * H;
+    const uint64_t d[2] = {256, jobs * kRingDepth * 128};
+    const uint64_t st[1] = {512};
+    const uint32_t b[2] = {64, 64};
+    ok &= encode_map(&p.tm_ring, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + fw.ring_off, d, st, b,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!ok) return MLA_ERR_CUDA;
+
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws + fw.err_off);
+  p.err = err;
+  p.queue = reinterpret_cast<uint32_t*>(ws + fw.queue_off);
+  p.flags = reinterpret_cast<uint32_t*>(ws + fw.flags_off);
+  p.ring = reinterpret_cast<uint16_t*>(ws + fw.ring_off);
+  p.block_table = block_table;
+  p.q_pos = q_pos;
+  p.out = out;
+  p.lse = lse;
+  p.part_out = reinterpret_cast<float*>(ws + fw.out_off);
+  p.part_lse = reinterpret_cast<float*>(ws + fw.lse_off);
+  p.slot_stride_rows = T_q;
+  p.max_blocks = max_blocks;
+  p.num_blocks = num_blocks;
+  p.num_heads = H;
+  p.out_bf16 = out_dtype == MLA_OUT_BF16;
+  p.kv_fp8 = fp8;
+  p.kv_scale = kv_scale;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  rope_fracs((double)rope_theta, p.rope_frac);
+
+  int grid = 0;
+  int st = cuda_status(fused_grid_size(&grid));
+  if (st != MLA_OK) return st;
+  st = cuda_status(cudaMemsetAsync(err, 0, 256, s));   // error word + role queue
+  if (st != MLA_OK) return st;
+
+  cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
+  cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
+  if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_b, s))) != MLA_OK) return st;
+  for (size_t b0 = 0; b0 < fp.pieces.size(); b0 += kMaxPieces) {
+    const size_t n = std::min(fp.pieces.size() - b0, (size_t)kMaxPieces);
+    int roles = 0;
+    for (size_t i = 0; i < n; ++i) {
+      Piece pc = fp.pieces[b0 + i];
+      pc.role_begin = roles;
+      roles += H * (pc.n_prod + pc.n_cons);
+      p.pieces[i] = pc;
+    }
+    p.n_pieces = (int)n;
+    p.n_roles = roles;
+    if (b0 > 0 && (st = cuda_status(cudaMemsetAsync(p.queue, 0, sizeof(uint32_t), s))) != MLA_OK) return st;
+    if ((st = cuda_status(cudaMemsetAsync(p.flags, 0, fw.flags_bytes, s))) != MLA_OK) return st;
+    if ((st = cuda_status(launch_fused(p, std::min(grid, roles), s))) != MLA_OK) return st;
+  }
+  if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_e, s))) != MLA_OK) return st;
+
+  if (!fp.merge.empty()) {
+    MergeParams mp;
+    std::memset(&mp, 0, sizeof(mp));
+    mp.part_out = p.part_out;
+    mp.part_lse = p.part_lse;
+    mp.slot_stride_rows = T_q;
+    mp.out = out;
+    mp.lse = lse;
+    mp.out_bf16 = p.out_bf16;
+    mp.num_heads = H;
+    for (size_t b0 = 0; b0 < fp.merge.size(); b0 += kMaxRangesPerLaunch) {
+      const size_t n = std::min(fp.merge.size() - b0, (size_t)kMaxRangesPerLaunch);
+      int rows = 0;
+      for (size_t i = 0; i < n; ++i) {
+        RowRange rr = fp.merge[b0 + i];
+        rr.prefix = rows;
+        rows += rr.row_end - rr.row_begin;
+        mp.ranges[i] = rr;
+      }
+      mp.num_ranges = (int)n;
+      mp.total_rows = rows;
+      if ((st = cuda_status(launch_merge_slots(mp, s))) != MLA_OK) return st;
+    }
+  }
+  return MLA_OK;
+}
 
 extern "C" {
 
@@ -172,7 +429,9 @@ size_t mla_prefill_workspace_size(int num_reqs, const int32_t* seq_lens, const i
   Plan plan;
   if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
     return 0;
-  return ws_layout(plan, num_heads).total;
+  FusedPlan fp;
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, &fp);
+  return std::max(ws_layout(plan, num_heads).total, fused_ws_layout(fp, num_heads).total);
 }
 
 int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
@@ -196,9 +455,17 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, i
   for (int r = 0; r < num_reqs; ++r)
     if ((seq_lens[r] + kBlock - 1) / kBlock > max_blocks_per_req) return MLA_ERR_INVALID_ARG;
   const WsLayout wl = ws_layout(plan, num_heads);
-  if (workspace == nullptr || workspace_bytes < wl.total || !aligned(workspace, 256)) return MLA_ERR_WORKSPACE;
+  FusedPlan fplan;
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, &fplan);
+  const FusedWs fw = fused_ws_layout(fplan, num_heads);
+  const bool tile_path = use_tile_path();
+  if (workspace == nullptr || workspace_bytes < (tile_path ? wl.total : fw.total) || !aligned(workspace, 256))
+    return MLA_ERR_WORKSPACE;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!tile_path)
+    return prefill_fused(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req, num_heads,
+                         kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, workspace, fplan, fw, s);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* err = reinterpret_cast<uint32_t*>(ws + wl.err_off);
   st = cuda_status(cudaMemsetAsync(err, 0, sizeof(uint32_t), s));

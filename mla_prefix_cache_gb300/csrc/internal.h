@@ -1,7 +1,9 @@
 // Internal structures shared by the C-ABI layer (host planner) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace mla {
@@ -81,6 +83,68 @@ struct MergeParams {
   int total_rows;             // sum of range lengths in this launch
   RowRange ranges[kMaxRangesPerLaunch];
 };
+
+// ------------------------------------------------------------ fused persistent kernel
+constexpr int kRingDepth = 6;     // 128-token K/V tiles per job ring
+constexpr int kMaxPieces = 448;   // pieces per launch (kernel-parameter budget)
+
+// One key range of one request attended with one RoPE offset, for every head.
+// Each (piece, head) is a job: n_prod producer roles then n_cons consumer roles.
+struct Piece {
+  int32_t req;
+  int32_t q_begin;     // global row of the request's first query
+  int32_t q_count;     // E_r
+  int32_t q_tok0;      // token index of the request's first query (C_r)
+  int32_t k_begin;     // first key token
+  int32_t k_end;       // one past the last key token
+  int32_t slot;        // partial-state slot, or -1: write the final out/lse
+  int32_t role_begin;  // first role of this piece in the launch's role queue
+  int32_t n_cons;      // consumer roles per head (256 queries each)
+  int32_t n_prod;      // producer roles per head
+  int64_t rope_offset;
+};
+
+// Device-side view of one job.
+struct Job {
+  int32_t req, head, q_begin, q_count, q_tok0, k_begin, k_end, t0, n_tiles, n_cons, n_prod, slot;
+  int64_t rope_offset;
+};
+
+struct FusedParams {
+  CUtensorMap tm_q;      // bf16 q [T_q][H][192], box 64 x 1 x 128
+  CUtensorMap tm_kr;     // cache rows, box = 64 rows x 128 B at the k_rope columns
+  CUtensorMap tm_c;      // cache rows, box = 64 rows x one 64-wide latent slice
+  CUtensorMap tm_w;      // bf16 kv_b_proj [512][H*256], box 64 x 64
+  CUtensorMap tm_ring;   // bf16 ring [jobs*ring*128][256], box 64 x 64
+  uint32_t* err;
+  uint32_t* queue;       // role counter
+  uint32_t* flags;       // per job: ready[ring], consumed[ring]
+  uint16_t* ring;
+  const int32_t* block_table;
+  const int32_t* q_pos;
+  void* out;
+  float* lse;
+  float* part_out;
+  float* part_lse;
+  int64_t slot_stride_rows;
+  int max_blocks;
+  int num_blocks;
+  int num_heads;
+  int out_bf16;
+  int kv_fp8;
+  float kv_scale;
+  float scale_log2;
+  int n_pieces;
+  int n_roles;
+  uint64_t rope_frac[kDr / 2];
+  Piece pieces[kMaxPieces];
+};
+
+static_assert(sizeof(FusedParams) <= 32000, "kernel parameter space");
+
+cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t s);
+cudaError_t fused_grid_size(int* grid);
+int fused_smem_bytes();
 
 // Kernel launchers (return cudaError_t of the launch).
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s);

@@ -46,19 +46,30 @@ def _ws(lib, seq, cu, H, segs=None, chunk=128, parts=3):
     return lib.mla_prefill_workspace_size(len(k1), sl, cq, H, sp, ns, chunk, parts)
 
 
+def _up(x, a=256):
+    return (x + a - 1) // a * a
+
+
+def fused_layout(pieces, heads, slots, total_q, ring_depth=6):
+    """Workspace of the fused path: 256 B header, per-job ring flags, per-job
+    K/V rings of `ring_depth` 128-token bf16 tiles, then partial states."""
+    jobs = pieces * heads
+    ring_off = _up(256 + jobs * 2 * ring_depth * 4)
+    lse_off = _up(ring_off + jobs * ring_depth * 128 * 256 * 2)
+    rows = slots * total_q * heads
+    return _up(lse_off + rows * 4) + rows * 128 * 4
+
+
 def test_workspace_size_follows_plan(lib):
-    # 1 request: C=256 in chunks of 128 -> 2 context splits + 1 extend = 3 slots
-    T, H = 64, 8
-    n = _ws(lib, [320], [0, 64], H, chunk=128)
-    rows = 3 * T * H
-    lse = ((rows * 4 + 255) // 256) * 256
-    assert n == 256 + lse + rows * 128 * 4
-    # context only, chunk larger than C -> 1 slot
-    assert _ws(lib, [320], [0, 64], H, chunk=4096, parts=1) == 256 + ((T * H * 4 + 255) // 256) * 256 + T * H * 512
-    # segments: 4 documents of 64 + extend = 5 slots
+    # 1 request, C=256 in chunks of 128 plus the extend: the three ranges share
+    # offset 0 and are contiguous, so they fold into one piece (no partial slots).
+    n = _ws(lib, [320], [0, 64], 8, chunk=128)
+    assert n == fused_layout(1, 8, 0, 64)
+    # segments: 4 documents of 64 (4 offsets) + extend = 5 pieces, 5 partial slots
     segs = [[0, 64 * d, 64, 64 * d] for d in range(4)]
-    n5 = _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64)
-    assert n5 == 256 + 256 + 5 * 2 * 512
+    assert _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64) == fused_layout(5, 1, 5, 2)
+    # a long context is cut into pieces of at most max(chunk, 16384) keys
+    assert _ws(lib, [40000 + 100], [0, 100], 2, chunk=4096) == fused_layout(3, 2, 3, 100)
 
 
 @pytest.mark.parametrize("bad", [
