@@ -41,7 +41,8 @@ enum mla_status {
   MLA_ERR_BAD_BLOCK_ID = 3,  /* device saw a block-table entry outside [0, num_blocks) */
   MLA_ERR_CUDA = 4,          /* a CUDA runtime call failed (see mla_last_cuda_error) */
   MLA_ERR_WORKSPACE = 5,     /* workspace missing or smaller than required */
-  MLA_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up */
+  MLA_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up */
+  MLA_ERR_TOO_LARGE = 7      /* needs more scratch than mla_prefill_ctx_noalloc holds */
 };
 
 enum mla_kv_dtype {
@@ -132,6 +133,43 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos,
                     const void* kv_b_proj, float softmax_scale, float rope_theta, int parts,
                     void* out, int out_dtype, float* lse,
                     void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * mla_prefill_ctx_noalloc -- mla_prefill_ctx for callers that cannot allocate
+ * device memory.  (No section of the pages has a counterpart: this is an
+ * integration entry point.)
+ *
+ * Some callers may not call cudaMalloc: a host framework that owns every
+ * device byte through its own pool, code that must not trigger the implicit
+ * device synchronisation an allocation can cause, or a caller that is in the
+ * middle of capturing a CUDA graph (allocation is refused under global
+ * capture mode).  This entry point takes the same arguments as
+ * mla_prefill_ctx minus the workspace and runs the same kernels, with their
+ * scratch in a fixed array that the library holds in every GPU's memory from
+ * the time the library is loaded on that device until the process exits:
+ * MLA_NOALLOC_SCRATCH_BYTES (32 MiB).  It calls no cudaMalloc, cudaFree or
+ * other device-allocating routine.
+ *
+ *  - The first call on a device looks up that device's address of the array
+ *    (cudaGetSymbolAddress) with the device current; make that first call
+ *    before any stream capture begins.
+ *  - A problem whose scratch would exceed the array returns MLA_ERR_TOO_LARGE
+ *    before anything is launched (mla_prefill_workspace_size gives the need).
+ *  - Every call shares the one array.  Each call re-zeroes the parts that must
+ *    start at zero, but calls that may overlap on the GPU (different streams
+ *    without ordering between them) race on it: order them.
+ *  - mla_get_device_error() does not apply to this entry point's scratch; pass
+ *    the same inputs to mla_prefill_ctx to diagnose a bad block table.
+ * ---------------------------------------------------------------------- */
+#define MLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos,
+                            const void* kv_cache, int kv_dtype, float kv_scale, int num_blocks,
+                            const int32_t* block_table, int max_blocks_per_req,
+                            const int32_t* seq_lens, const int32_t* cu_q, int num_reqs, int num_heads,
+                            const mla_segment* segments, int num_segments, int chunk,
+                            const void* kv_b_proj, float softmax_scale, float rope_theta, int parts,
+                            void* out, int out_dtype, float* lse, mla_stream_t stream);
 
 /* Reads and clears the device error word kept in `workspace` (synchronises
  * `stream`).  Returns MLA_OK, MLA_ERR_BAD_BLOCK_ID or MLA_ERR_TIMEOUT. */

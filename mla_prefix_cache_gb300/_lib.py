@@ -21,6 +21,8 @@ MLA_ERR_BAD_BLOCK_ID = 3
 MLA_ERR_CUDA = 4
 MLA_ERR_WORKSPACE = 5
 MLA_ERR_TIMEOUT = 6
+MLA_ERR_TOO_LARGE = 7
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
@@ -55,6 +57,9 @@ SIGNATURES = {
     "mla_prefill_ctx": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_float, c_int, c_void_p, c_int,
                                 i32p, i32p, c_int, c_int, segp, c_int, c_int, c_void_p, c_float, c_float,
                                 c_int, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "mla_prefill_ctx_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_float, c_int, c_void_p, c_int,
+                                        i32p, i32p, c_int, c_int, segp, c_int, c_int, c_void_p, c_float, c_float,
+                                        c_int, c_void_p, c_int, c_void_p, c_void_p]),
     "mla_get_device_error": (c_int, [c_void_p, c_void_p]),
     "mla_merge_states": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int,
                                  c_void_p]),

@@ -273,6 +273,30 @@ static bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const v
 
 using namespace mla;
 
+// Scratch of mla_prefill_ctx_noalloc: one fixed array per device, part of the
+// library image, so that entry point never allocates.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+static void* g_noalloc_ptr[128];
+static std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current.
+static int noalloc_scratch(void** out) {
+  int dev = 0;
+  int st = cuda_status(cudaGetDevice(&dev));
+  if (st != MLA_OK) return st;
+  if (dev < 0 || dev >= (int)(sizeof(g_noalloc_ptr) / sizeof(g_noalloc_ptr[0]))) return MLA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    st = cuda_status(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    if (st != MLA_OK) return st;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MLA_OK;
+}
+
 static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
                          int num_blocks, const int32_t* block_table, int max_blocks, int num_heads,
                          const void* kv_b_proj, float softmax_scale, float rope_theta, void* out, int out_dtype,
@@ -420,6 +444,7 @@ const char* mla_status_string(int status) {
     case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
     case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_TOO_LARGE: return "MLA_ERR_TOO_LARGE";
     default: return "MLA_ERR_UNKNOWN";
   }
 }
@@ -540,6 +565,29 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, i
     if (st != MLA_OK) return st;
   }
   return MLA_OK;
+}
+
+int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                            int num_blocks, const int32_t* block_table, int max_blocks_per_req,
+                            const int32_t* seq_lens, const int32_t* cu_q, int num_reqs, int num_heads,
+                            const mla_segment* segments, int num_segments, int chunk, const void* kv_b_proj,
+                            float softmax_scale, float rope_theta, int parts, void* out, int out_dtype, float* lse,
+                            mla_stream_t stream) {
+  const size_t need = mla_prefill_workspace_size(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk,
+                                                 parts);
+  if (need == 0) {  // the planner rejected the arguments: report why
+    Plan plan;
+    const int st = build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan);
+    return st != MLA_OK ? st : MLA_ERR_INVALID_ARG;
+  }
+  if (need > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_TOO_LARGE;
+  void* scratch = nullptr;
+  const int st = noalloc_scratch(&scratch);
+  if (st != MLA_OK) return st;
+  return mla_prefill_ctx(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                         seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
+                         softmax_scale, rope_theta, parts, out, out_dtype, lse, scratch, MLA_NOALLOC_SCRATCH_BYTES,
+                         stream);
 }
 
 int mla_get_device_error(void* workspace, mla_stream_t stream) {
