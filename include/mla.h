@@ -113,9 +113,13 @@ typedef struct {
  *  out          device [T_q, H, 128], fp32 or bf16 per out_dtype.
  *  lse          device fp32 [T_q, H], natural log, softmax scale included;
  *               -inf for a row with no visible key (its out row is 0).
- *  workspace    device, at least mla_prefill_workspace_size(...) bytes, 256-B
- *               aligned; holds fp32 partial states and the device error word.
- *               Must not be shared by calls that may overlap on the GPU.
+ *  workspace    device, 256-B aligned; mla_prefill_workspace_size(...) bytes
+ *               lets the whole call run as one kernel launch.  A smaller
+ *               workspace also works as long as it holds the partial states
+ *               and the K/V rings of one piece (one request's key range of at
+ *               most max(chunk, 16384) tokens, for all heads): the call then
+ *               runs its pieces in several launches.  Holds the device error
+ *               word; must not be shared by calls that may overlap on the GPU.
  *  H            num_heads in [1, 128].
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H > 128, chunk not a
  * multiple of 64), MLA_ERR_WORKSPACE, MLA_ERR_CUDA.  Bad block ids are reported
@@ -153,8 +157,8 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos,
  *  - The first call on a device looks up that device's address of the array
  *    (cudaGetSymbolAddress) with the device current; make that first call
  *    before any stream capture begins.
- *  - A problem whose scratch would exceed the array returns MLA_ERR_TOO_LARGE
- *    before anything is launched (mla_prefill_workspace_size gives the need).
+ *  - A problem that does not fit the array even one piece per launch returns
+ *    MLA_ERR_TOO_LARGE before anything is launched.
  *  - Every call shares the one array.  Each call re-zeroes the parts that must
  *    start at zero, but calls that may overlap on the GPU (different streams
  *    without ordering between them) race on it: order them.
@@ -223,6 +227,14 @@ int mla_gather_latent(const void* kv_cache, int kv_dtype, float kv_scale, int nu
  * kernel alone with cudaEventElapsedTime.  NULL, NULL turns it off.  The
  * setting is process-wide; the caller keeps the events alive while it is on. */
 void mla_set_kernel_events(void* begin_event, void* end_event);
+
+/* Optional tracing of the fused kernel.  With a non-NULL device buffer of at
+ * least 64 bytes per role of a call, later mla_prefill_ctx calls write, per
+ * role of the persistent kernel's queue, eight 64-bit words: start and end
+ * (ns, %globaltimer), CTA / role kind / job, and the ns spent in its main
+ * waits.  A call with more roles than the buffer holds is not traced.  NULL
+ * turns it off.  Process-wide, like the kernel events. */
+void mla_set_trace(void* device_buffer, size_t bytes);
 
 /* Human-readable name of a status code (static storage). */
 const char* mla_status_string(int status);

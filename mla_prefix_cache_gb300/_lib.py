@@ -72,6 +72,7 @@ SIGNATURES = {
     "mla_launch_count": (ctypes.c_uint64, []),
     "mla_abi_version": (c_int, []),
     "mla_set_kernel_events": (None, [c_void_p, c_void_p]),
+    "mla_set_trace": (None, [c_void_p, c_size_t]),
 }
 
 _lock = threading.Lock()

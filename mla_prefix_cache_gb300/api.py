@@ -96,8 +96,8 @@ def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_
         out = torch.empty((T_q, H, 128), dtype=out_dtype, device=dev)
     if lse is None:
         lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
-    ws_bytes = prefill_workspace_size(keep_sl, keep_cq, H, segments, chunk, parts)
-    if workspace is None or workspace.numel() * workspace.element_size() < ws_bytes:
+    if workspace is None:
+        ws_bytes = prefill_workspace_size(keep_sl, keep_cq, H, segments, chunk, parts)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_FP32
     st = L.mla_prefill_ctx(

@@ -20,6 +20,8 @@ namespace mla {
 static std::atomic<uint64_t> g_launches{0};
 static std::atomic<void*> g_ev_begin{nullptr};
 static std::atomic<void*> g_ev_end{nullptr};
+static std::atomic<void*> g_trace{nullptr};
+static std::atomic<size_t> g_trace_bytes{0};
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 static thread_local char g_cuda_err[256] = "";
@@ -124,32 +126,13 @@ static int build_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q
   return MLA_OK;
 }
 
-struct WsLayout {
-  size_t err_off = 0, lse_off = 0, out_off = 0, total = 0;
-};
-
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
-
-static WsLayout ws_layout(const Plan& plan, int num_heads) {
-  WsLayout w;
-  const size_t rows = (size_t)plan.max_slots * (size_t)plan.total_q * (size_t)num_heads;
-  w.err_off = 0;
-  w.lse_off = 256;
-  w.out_off = w.lse_off + up256(rows * sizeof(float));
-  w.total = w.out_off + rows * kDv * sizeof(float);
-  return w;
-}
 
 
 // ------------------------------------------------------------------ fused path
 static int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   return (v && *v) ? std::atoi(v) : dflt;
-}
-
-static bool use_tile_path() {
-  const char* v = std::getenv("MLA_PREFILL_PATH");
-  return v && std::strcmp(v, "tile") == 0;
 }
 
 struct FusedPlan {
@@ -172,7 +155,7 @@ static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const i
   fp->max_slots = 0;
   fp->total_q = splits.total_q;
   const int max_keys = std::max(chunk, env_int("MLA_MAX_PIECE_KEYS", 16384));
-  const int n_prod_cfg = std::max(1, env_int("MLA_PRODUCERS", 2));
+  const int n_prod_cfg = std::max(1, env_int("MLA_PRODUCERS", 4));
   size_t si = 0;
   for (int r = 0; r < num_reqs; ++r) {
     const int E = cu_q[r + 1] - cu_q[r];
@@ -203,7 +186,7 @@ static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const i
     for (int i = 0; i < np; ++i) {
       Piece& pc = pr[i];
       pc.slot = np == 1 ? -1 : i;
-      pc.n_cons = (E + 255) / 256;
+      pc.n_cons = (E + 127) / 128;
       const int t0 = pc.k_begin & ~(kBlock - 1);
       const int n_tiles = (pc.k_end - t0 + 127) / 128;
       pc.n_prod = std::max(1, std::min(n_prod_cfg, (n_tiles + 1) / 2));
@@ -230,10 +213,12 @@ struct FusedWs {
   int pieces_per_launch = 0;
 };
 
-static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads) {
+// Workspace of the fused path when `ppl` pieces run per launch: header (error
+// word, role queue), per-job ring flags, per-job K/V rings, partial states.
+static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads, int ppl) {
   FusedWs w;
-  w.pieces_per_launch = std::min((int)fp.pieces.size(), kMaxPieces);
-  const size_t jobs = (size_t)w.pieces_per_launch * num_heads;
+  w.pieces_per_launch = ppl;
+  const size_t jobs = (size_t)ppl * num_heads;
   w.flags_bytes = jobs * 2 * kRingDepth * sizeof(uint32_t);
   w.ring_off = up256(w.flags_off + w.flags_bytes);
   const size_t ring_bytes = jobs * kRingDepth * 128 * 256 * sizeof(uint16_t);
@@ -242,6 +227,21 @@ static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads) {
   w.out_off = up256(w.lse_off + rows * sizeof(float));
   w.total = w.out_off + rows * kDv * sizeof(float);
   return w;
+}
+
+// Preferred layout: every piece in one launch, up to kMaxPieces and a 4 GiB ring.
+static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads) {
+  const size_t per_piece = (size_t)num_heads * kRingDepth * 128 * 256 * sizeof(uint16_t);
+  const int cap = (int)std::max<size_t>(1, ((size_t)4 << 30) / per_piece);
+  const int ppl = std::max(1, std::min({(int)fp.pieces.size(), kMaxPieces, cap}));
+  return fused_ws_layout(fp, num_heads, ppl);
+}
+
+// Largest pieces-per-launch whose layout fits in `bytes` (0 if not even one).
+static int fused_pieces_fitting(const FusedPlan& fp, int num_heads, size_t bytes) {
+  int hi = fused_ws_layout(fp, num_heads).pieces_per_launch;
+  while (hi >= 1 && fused_ws_layout(fp, num_heads, hi).total > bytes) hi = hi > 8 ? hi - hi / 8 : hi - 1;
+  return std::max(hi, 0);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -312,12 +312,7 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
   const uint64_t cache_rows = (uint64_t)num_blocks * kBlock;
   bool ok = true;
-  {
-    const uint64_t d[3] = {(uint64_t)kDqk, (uint64_t)H, (uint64_t)T_q};
-    const uint64_t st[2] = {(uint64_t)kDqk * 2, (uint64_t)H * kDqk * 2};
-    const uint32_t b[3] = {64, 1, 128};
-    ok &= encode_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
-  }
+  p.q_bf16 = static_cast<const uint16_t*>(q);
   if (!fp8) {
     const uint64_t d[2] = {(uint64_t)kRowBf16, cache_rows};
     const uint64_t st[1] = {(uint64_t)kRowBytesBf16};
@@ -332,17 +327,19 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     ok &= encode_map(&p.tm_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_cache, d, st, bc, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   {
-    const uint64_t d[2] = {(uint64_t)H * (kDnope + kDv), (uint64_t)kDc};
-    const uint64_t st[1] = {(uint64_t)H * (kDnope + kDv) * 2};
-    const uint32_t b[2] = {64, 64};
-    ok &= encode_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_b_proj, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    // kv_b_proj [512][H*256] seen as 64-column blocks: (col in block, latent row, block)
+    const uint64_t d[3] = {64, (uint64_t)kDc, (uint64_t)H * (kDnope + kDv) / 64};
+    const uint64_t st[2] = {(uint64_t)H * (kDnope + kDv) * 2, 128};
+    const uint32_t b[3] = {64, 64, 2};
+    ok &= encode_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_b_proj, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   {
+    // ring: per job and slot four contiguous [128 x 64] blocks K_nope lo, K_nope hi, V lo, V hi
     const uint64_t jobs = (uint64_t)std::max(fw.pieces_per_launch, 1) * H;
-    const uint64_t d[2] = {256, jobs * kRingDepth * 128};
-    const uint64_t st[1] = {512};
-    const uint32_t b[2] = {64, 64};
-    ok &= encode_map(&p.tm_ring, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + fw.ring_off, d, st, b,
+    const uint64_t d[3] = {64, 128, jobs * kRingDepth * 4};
+    const uint64_t st[2] = {128, 128 * 128};
+    const uint32_t b[3] = {64, 128, 2};
+    ok &= encode_map(&p.tm_ring, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + fw.ring_off, d, st, b,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return MLA_ERR_CUDA;
@@ -377,8 +374,9 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
   cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
   if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_b, s))) != MLA_OK) return st;
-  for (size_t b0 = 0; b0 < fp.pieces.size(); b0 += kMaxPieces) {
-    const size_t n = std::min(fp.pieces.size() - b0, (size_t)kMaxPieces);
+  const size_t ppl = (size_t)std::max(fw.pieces_per_launch, 1);
+  for (size_t b0 = 0; b0 < fp.pieces.size(); b0 += ppl) {
+    const size_t n = std::min(fp.pieces.size() - b0, ppl);
     int roles = 0;
     for (size_t i = 0; i < n; ++i) {
       Piece pc = fp.pieces[b0 + i];
@@ -388,6 +386,12 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     }
     p.n_pieces = (int)n;
     p.n_roles = roles;
+    void* tr = g_trace.load();
+    p.trace = (tr != nullptr && g_trace_bytes.load() >= (size_t)roles * kTraceWords * 8 && fp.pieces.size() <= ppl)
+                  ? static_cast<unsigned long long*>(tr) : nullptr;
+    // per-stage detail of one role when the buffer has room for 4096 more stages
+    p.trace_detail_role = (p.trace && g_trace_bytes.load() >= ((size_t)roles * kTraceWords + 4096 * 8) * 8)
+                              ? env_int("MLA_TRACE_DETAIL_ROLE", -1) : -1;
     if (b0 > 0 && (st = cuda_status(cudaMemsetAsync(p.queue, 0, sizeof(uint32_t), s))) != MLA_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(p.flags, 0, fw.flags_bytes, s))) != MLA_OK) return st;
     if ((st = cuda_status(launch_fused(p, std::min(grid, roles), s))) != MLA_OK) return st;
@@ -425,6 +429,11 @@ extern "C" {
 
 int mla_abi_version(void) { return 1; }
 
+void mla_set_trace(void* device_buffer, size_t bytes) {
+  g_trace.store(bytes ? device_buffer : nullptr);
+  g_trace_bytes.store(device_buffer ? bytes : 0);
+}
+
 void mla_set_kernel_events(void* begin_event, void* end_event) {
   const bool on = begin_event != nullptr && end_event != nullptr;
   g_ev_begin.store(on ? begin_event : nullptr);
@@ -456,7 +465,7 @@ size_t mla_prefill_workspace_size(int num_reqs, const int32_t* seq_lens, const i
     return 0;
   FusedPlan fp;
   build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, &fp);
-  return std::max(ws_layout(plan, num_heads).total, fused_ws_layout(fp, num_heads).total);
+  return fused_ws_layout(fp, num_heads).total;
 }
 
 int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
@@ -479,92 +488,14 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, i
     return MLA_ERR_INVALID_ARG;
   for (int r = 0; r < num_reqs; ++r)
     if ((seq_lens[r] + kBlock - 1) / kBlock > max_blocks_per_req) return MLA_ERR_INVALID_ARG;
-  const WsLayout wl = ws_layout(plan, num_heads);
   FusedPlan fplan;
   build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, &fplan);
-  const FusedWs fw = fused_ws_layout(fplan, num_heads);
-  const bool tile_path = use_tile_path();
-  if (workspace == nullptr || workspace_bytes < (tile_path ? wl.total : fw.total) || !aligned(workspace, 256))
-    return MLA_ERR_WORKSPACE;
-
+  const int ppl = fused_pieces_fitting(fplan, num_heads, workspace_bytes);
+  if (workspace == nullptr || !aligned(workspace, 256) || ppl < 1) return MLA_ERR_WORKSPACE;
+  const FusedWs fw = fused_ws_layout(fplan, num_heads, ppl);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (!tile_path)
-    return prefill_fused(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req, num_heads,
+  return prefill_fused(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req, num_heads,
                          kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, workspace, fplan, fw, s);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint32_t* err = reinterpret_cast<uint32_t*>(ws + wl.err_off);
-  st = cuda_status(cudaMemsetAsync(err, 0, sizeof(uint32_t), s));
-  if (st != MLA_OK) return st;
-
-  PrefillParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.q = static_cast<const uint16_t*>(q);
-  p.q_pos = q_pos;
-  p.kv_cache = static_cast<const uint8_t*>(kv_cache);
-  p.block_table = block_table;
-  p.w = static_cast<const uint16_t*>(kv_b_proj);
-  p.part_out = reinterpret_cast<float*>(ws + wl.out_off);
-  p.part_lse = reinterpret_cast<float*>(ws + wl.lse_off);
-  p.err = err;
-  p.slot_stride_rows = plan.total_q;
-  p.num_heads = num_heads;
-  p.kv_fp8 = kv_dtype == MLA_KV_FP8_E4M3;
-  p.kv_scale = kv_scale;
-  p.num_blocks = num_blocks;
-  p.max_blocks = max_blocks_per_req;
-  p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  rope_fracs((double)rope_theta, p.rope_frac);
-
-  cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
-  cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
-  if (ev_b != nullptr && ev_e != nullptr) {
-    st = cuda_status(cudaEventRecord(ev_b, s));
-    if (st != MLA_OK) return st;
-  }
-  for (size_t b = 0; b < plan.splits.size(); b += kMaxSplitsPerLaunch) {
-    const size_t n = std::min(plan.splits.size() - b, (size_t)kMaxSplitsPerLaunch);
-    int tiles = 0;
-    for (size_t i = 0; i < n; ++i) {
-      Split sp = plan.splits[b + i];
-      sp.tile_begin = tiles;
-      tiles += (sp.q_count + 127) / 128;
-      p.splits[i] = sp;
-    }
-    p.num_splits = (int)n;
-    p.num_tiles = tiles;
-    st = cuda_status(launch_prefill(p, s));
-    if (st != MLA_OK) return st;
-  }
-
-  if (ev_b != nullptr && ev_e != nullptr) {
-    st = cuda_status(cudaEventRecord(ev_e, s));
-    if (st != MLA_OK) return st;
-  }
-
-  MergeParams mp;
-  std::memset(&mp, 0, sizeof(mp));
-  mp.part_out = p.part_out;
-  mp.part_lse = p.part_lse;
-  mp.slot_stride_rows = plan.total_q;
-  mp.out = out;
-  mp.lse = lse;
-  mp.out_bf16 = out_dtype == MLA_OUT_BF16;
-  mp.num_heads = num_heads;
-  for (size_t b = 0; b < plan.ranges.size(); b += kMaxRangesPerLaunch) {
-    const size_t n = std::min(plan.ranges.size() - b, (size_t)kMaxRangesPerLaunch);
-    int rows = 0;
-    for (size_t i = 0; i < n; ++i) {
-      RowRange rr = plan.ranges[b + i];
-      rr.prefix = rows;
-      rows += rr.row_end - rr.row_begin;
-      mp.ranges[i] = rr;
-    }
-    mp.num_ranges = (int)n;
-    mp.total_rows = rows;
-    st = cuda_status(launch_merge_slots(mp, s));
-    if (st != MLA_OK) return st;
-  }
-  return MLA_OK;
 }
 
 int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
@@ -580,7 +511,13 @@ int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos, const void* kv_
     const int st = build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan);
     return st != MLA_OK ? st : MLA_ERR_INVALID_ARG;
   }
-  if (need > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_TOO_LARGE;
+  // the smallest workspace the call can run in: one piece per launch
+  Plan plan;
+  if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
+    return MLA_ERR_INVALID_ARG;
+  FusedPlan fplan;
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, &fplan);
+  if (fused_pieces_fitting(fplan, num_heads, MLA_NOALLOC_SCRATCH_BYTES) < 1) return MLA_ERR_TOO_LARGE;
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
   if (st != MLA_OK) return st;

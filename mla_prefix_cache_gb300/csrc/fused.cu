@@ -38,38 +38,44 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 384;
 constexpr uint32_t kRing = kRingDepth;
 
 // ---------------------------------------------------------------- shared memory
-constexpr uint32_t kAtomQ = 16384;                  // [128 rows x 128 B]
-constexpr uint32_t kAtom64 = 8192;                  // [64 rows x 128 B]
-constexpr uint32_t kQBytes = 3 * kAtomQ;            // nope lo | nope hi | rope
-constexpr uint32_t kStageBase = 2 * kQBytes;        // 98304
-constexpr uint32_t kStageK = 0;                     // K_nope [64 x 128]: 2 atoms
-constexpr uint32_t kStageKR = 2 * kAtom64;          // k_rope [64 x 64]
-constexpr uint32_t kStageV = 3 * kAtom64;           // V [64 x 128]: 2 dv blocks
-constexpr uint32_t kStageBytes = 5 * kAtom64;       // 40960
-constexpr int kStages = 3;
+constexpr uint32_t kAtomQ = 16384;                  // [128 rows x 128 B] swizzled block
+constexpr uint32_t kAtom64 = 8192;                  // [64 rows x 128 B] swizzled block
+// consumer: K ring (K_nope 2 blocks + k_rope 1 block per 128 keys) and V ring (2 blocks)
+constexpr int kKStages = 3, kVStages = 2;
+constexpr uint32_t kKStageBytes = 3 * kAtomQ;       // 49152
+constexpr uint32_t kVStageBytes = 2 * kAtomQ;       // 32768
+constexpr uint32_t kKBase = 0;
+constexpr uint32_t kVBase = kKBase + kKStages * kKStageBytes;      // 147456
+constexpr uint32_t kXchgBase = kVBase + kVStages * kVStageBytes;   // 212992: row-max / row-sum exchange
+constexpr uint32_t kConsumerEnd = kXchgBase + 6 * 128 * 4;         // max x2 buffers x2 halves, sum x2 halves
 // producer
 constexpr uint32_t kPStageBytes = 65536;            // C_A 16K | C_B 16K | W 32K
 constexpr uint32_t kPCA = 0, kPCB = 16384, kPW = 32768;
 constexpr uint32_t kPRawBase = 2 * kPStageBytes;    // e4m3 staging, 16 KB per stage
-constexpr uint32_t kBarBase = kStageBase + kStages * kStageBytes;  // 221184
+constexpr uint32_t kPOutBase = kPRawBase + 2 * 16384; // bf16 output staging: 32 KB per warpgroup
+constexpr uint32_t kProducerEnd = kPOutBase + 2 * 32768;             // 229376
+constexpr uint32_t kBarBase = kConsumerEnd > kProducerEnd ? kConsumerEnd : kProducerEnd;
 constexpr uint32_t kSmemBytes = kBarBase + 256 + 1024;
+static_assert(kSmemBytes <= 232448, "more than 227 KB of shared memory per CTA");
 
 // consumer barriers
-constexpr uint32_t kBQFull = 0, kBQReady = 1, kBKvFull = 3, kBKvEmpty = 6, kBSFull = 9, kBPFull = 13, kBPvDone = 17;
+constexpr uint32_t kBQReady = 0, kBKFull = 1, kBKEmpty = 4, kBVFull = 7, kBVEmpty = 9, kBSFull = 11, kBPFull = 13,
+                   kBPvDone = 15 /* 2: PV of even / odd tiles */, kBKRel = 17, kBVRel = 20;
 // producer barriers
 constexpr uint32_t kBProdFull = 0, kBProdEmpty = 2, kBRawFull = 4, kBAccFull = 6, kBAccEmpty = 7;
-constexpr uint32_t kNumBars = 20;
+constexpr uint32_t kNumBars = 24;
 
 // TMEM columns
-constexpr uint32_t kTmO = 0;        // O of query tile u at u*128
-constexpr uint32_t kTmS = 256;      // S of (u, b) at 256 + (2u + b) * 64
-constexpr uint32_t kTmAccA = 0, kTmAccB = 256;
+constexpr uint32_t kTmQ = 0;        // consumer: Q as bf16 pairs, 96 columns
+constexpr uint32_t kTmO = 128;      // consumer: O [128 x 128] fp32
+constexpr uint32_t kTmS = 256;      // consumer: S buffer b at 256 + 128 b (P as bf16 pairs in its first 64)
+constexpr uint32_t kTmAccA = 0, kTmAccB = 256;   // producer
 
-constexpr uint32_t kIdescS = idesc_bf16(128, 64, false, false);
+constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
 constexpr uint32_t kIdescUp = idesc_bf16(128, 256, false, true);
 
@@ -82,6 +88,28 @@ struct Ctl {
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t sbase, uint32_t i) { return sbase + kBarBase + 8u * i; }
+
+// Optional tracing: per role kTraceWords words
+//   [0] start ns  [1] end ns  [2] cta << 32 | producer << 31 | job
+//   [3] ns waiting on the other role kind (consumer: `ready` flags; producer: `consumed`)
+//   [4] ns the MMA thread waited for operands (kv_full / prod_full)
+//   [5] ns the MMA thread waited for softmax (p_full) or conversion (acc_empty)
+//   [6] ns softmax warp 0 waited for S (s_full)   [7] stages / passes
+struct TraceAcc {
+  unsigned long long t = 0;
+  __device__ __forceinline__ uint64_t begin(const FusedParams& p) const { return p.trace ? global_timer_ns() : 0; }
+  __device__ __forceinline__ void end(const FusedParams& p, uint64_t t0) { if (p.trace) t += global_timer_ns() - t0; }
+};
+__device__ __forceinline__ void trace_put(const FusedParams& p, int role, int word, unsigned long long v) {
+  if (p.trace) p.trace[(size_t)role * kTraceWords + word] = v;
+}
+// Per-stage timestamps of one role (after the per-role words): 8 words per stage
+//   [0] K load issued  [1] V load issued  [2] MMA saw K  [3] MMA issued S
+//   [4] MMA saw P  [5] MMA saw V (PV issued next)  [6] softmax saw S  [7] softmax published P
+__device__ __forceinline__ void trace_stage(const FusedParams& p, int role, int stage, int word) {
+  if (p.trace && role == p.trace_detail_role && stage < 4096)
+    p.trace[(size_t)p.n_roles * kTraceWords + (size_t)stage * 8 + word] = global_timer_ns();
+}
 
 __device__ __forceinline__ bool aborted_global(const FusedParams& p) { return ld_volatile_u32(p.err) != 0u; }
 
@@ -113,20 +141,21 @@ __device__ bool wait_flag_geq(const FusedParams& p, const uint32_t* flag, uint32
   return true;
 }
 
-// Number of 64-key stages consumer `ci` of job `J` attends to (causal clip).
-__device__ __forceinline__ int consumer_stages(const Job& J, int ci) {
-  const int q0 = ci * 256;
-  const int nq = min(256, J.q_count - q0);
+// Number of 128-key tiles consumer `ci` (queries 128 ci .. 128 ci + 127 of the
+// request) of job `J` attends to (causal clip).
+__device__ __forceinline__ int consumer_tiles(const Job& J, int ci) {
+  const int q0 = ci * 128;
+  const int nq = min(128, J.q_count - q0);
   if (nq <= 0) return 0;
   const int last_tok = J.q_tok0 + q0 + nq - 1;
   const int k_end = min(J.k_end, last_tok + 1);
   if (k_end <= J.k_begin) return 0;
-  return (k_end - J.t0 + 63) >> 6;
+  return (k_end - J.t0 + 127) >> 7;
 }
 
 __device__ __forceinline__ int consumers_needing_tile(const Job& J, int t) {
   int n = 0;
-  for (int ci = 0; ci < J.n_cons; ++ci) n += ((consumer_stages(J, ci) + 1) >> 1) > t;
+  for (int ci = 0; ci < J.n_cons; ++ci) n += consumer_tiles(J, ci) > t;
   return n;
 }
 
@@ -151,169 +180,231 @@ __device__ __forceinline__ int block_row(const FusedParams& p, int req, int lb, 
 }
 
 // =============================================================== consumer
-__device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci, uint32_t sbase, uint8_t* sgen,
-                             uint32_t tmem, volatile Ctl* ctl) {
+// One 128-query tile of a job.  Warps: 0-7 softmax (warpgroup w owns key
+// columns 64w..64w+63 of every row; warpgroup 0 first loads and rotates Q into
+// TMEM), 8 K loader, 9 MMA issuer, 10 V loader, 11 releases ring slots.
+__device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci, int role, uint32_t sbase,
+                             uint8_t* sgen, uint32_t tmem, volatile Ctl* ctl) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q0 = ci * 256;
-  const int nq_all = min(256, J.q_count - q0);
-  const int nq0 = min(128, nq_all), nq1 = max(0, nq_all - 128);
+  const int q0 = ci * 128;
+  const int nq = min(128, J.q_count - q0);
   const int grow0 = J.q_begin + q0;
-  const int n_stages = consumer_stages(J, ci);
+  const int n_tiles = consumer_tiles(J, ci);
   const int H = p.num_heads;
-  const uint32_t sQ0 = sbase, sQ1 = sbase + kQBytes;
 
-  if (warp == 12) {
-    // ------------------------------------------------------------ TMA loads
-    if (lane == 0) {
-      const uint32_t qf = bar_addr(sbase, kBQFull);
-      mbar_arrive_expect_tx(qf, 2 * kQBytes);
-      for (int u = 0; u < 2; ++u)
-        for (int a = 0; a < 3; ++a)
-          tma_load_3d((u ? sQ1 : sQ0) + a * kAtomQ, &p.tm_q, 64 * a, J.head, grow0 + 128 * u, qf);
-      const int ring_row0 = job * (int)kRing * 128;
-      for (int j = 0; j < n_stages; ++j) {
-        const int s = j % kStages;
-        if (j >= kStages && !wait_bar(p, bar_addr(sbase, kBKvEmpty + s), ((j / kStages) - 1) & 1)) { ctl->abort = 1; break; }
-        const int t = j >> 1, half = j & 1;
-        if (half == 0) {
-          if (!wait_flag_geq(p, ready_flag(p, job, t % kRing), (uint32_t)t + 1)) { ctl->abort = 1; break; }
-          fence_proxy_async_global();
-        }
-        const int kt0 = J.t0 + 64 * j;
-        const int yk = block_row(p, J.req, kt0 >> 6, true);
-        const uint32_t st = sbase + kStageBase + s * kStageBytes;
-        const uint32_t full = bar_addr(sbase, kBKvFull + s);
-        mbar_arrive_expect_tx(full, kStageBytes);
-        const int ry = ring_row0 + (t % kRing) * 128 + half * 64;
-        tma_load_2d(st + kStageK, &p.tm_ring, 0, ry, full);
-        tma_load_2d(st + kStageK + kAtom64, &p.tm_ring, 64, ry, full);
-        tma_load_2d(st + kStageV, &p.tm_ring, 128, ry, full);
-        tma_load_2d(st + kStageV + kAtom64, &p.tm_ring, 192, ry, full);
-        tma_load_2d(st + kStageKR, &p.tm_kr, kDc, yk, full);   // element 512 (bf16) = byte 512 (fp8 row)
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ TMA loads (K or V)
+    if (lane != 0) return;
+    const bool is_k = warp == 8;
+    TraceAcc tr;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int ns = is_k ? kKStages : kVStages;
+      const int s = j % ns;
+      // stage reusable: its MMA finished reading it, and the release warp has seen its previous load land
+      if (j >= ns && !(wait_bar(p, bar_addr(sbase, (is_k ? kBKEmpty : kBVEmpty) + s), ((j / ns) - 1) & 1) &&
+                       wait_bar(p, bar_addr(sbase, (is_k ? kBKRel : kBVRel) + s), ((j / ns) - 1) & 1))) {
+        ctl->abort = 1;
+        return;
+      }
+      const uint64_t w0 = tr.begin(p);
+      if (!wait_flag_geq(p, ready_flag(p, job, j % kRing), (uint32_t)j + 1)) { ctl->abort = 1; return; }
+      tr.end(p, w0);
+      fence_proxy_async_global();
+      const int zb = (job * (int)kRing + j % kRing) * 4;   // first ring block of the tile
+      if (is_k) {
+        const uint32_t st = sbase + kKBase + s * kKStageBytes;
+        const uint32_t full = bar_addr(sbase, kBKFull + s);
+        mbar_arrive_expect_tx(full, kKStageBytes);
+        tma_load_3d(st, &p.tm_ring, 0, 0, zb, full);                      // K_nope, 32 KB
+        const int kt0 = J.t0 + 128 * j;
+        tma_load_2d(st + 2 * kAtomQ, &p.tm_kr, kDc, block_row(p, J.req, kt0 >> 6, true), full);
+        tma_load_2d(st + 2 * kAtomQ + kAtom64, &p.tm_kr, kDc,
+                    block_row(p, J.req, (kt0 >> 6) + 1, kt0 + 64 < J.k_end), full);
+        trace_stage(p, role, j, 0);
+      } else {
+        const uint32_t st = sbase + kVBase + s * kVStageBytes;
+        const uint32_t full = bar_addr(sbase, kBVFull + s);
+        mbar_arrive_expect_tx(full, kVStageBytes);
+        tma_load_3d(st, &p.tm_ring, 0, 0, zb + 2, full);                  // V, 32 KB
+        trace_stage(p, role, j, 1);
       }
     }
-  } else if (warp == 13) {
+    if (is_k) trace_put(p, role, 3, tr.t);
+    if (is_k) trace_put(p, role, 7, (unsigned long long)n_tiles);
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ ring-slot release
+    // lane 0 watches K loads land, lane 1 V loads; each adds one to the slot's
+    // consumed count (a tile is released after 2 per consumer) and re-arms its
+    // own loader, so K loads never wait for V loads or the other way round.
+    if (lane > 1) return;
+    const bool is_k = lane == 0;
+    const int ns = is_k ? kKStages : kVStages;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!wait_bar(p, bar_addr(sbase, (is_k ? kBKFull : kBVFull) + j % ns), (j / ns) & 1)) { ctl->abort = 1; return; }
+      fence_proxy_async_global();
+      red_release_gpu_add(consumed_flag(p, job, j % kRing), 1u);
+      mbar_arrive(bar_addr(sbase, (is_k ? kBKRel : kBVRel) + j % ns));
+    }
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      bool ok = wait_bar(p, bar_addr(sbase, kBQReady + 0), 0) && wait_bar(p, bar_addr(sbase, kBQReady + 1), 0);
-      const bool act[2] = {nq0 > 0, nq1 > 0};
-      auto issue_pv = [&](int jj) {
-        const int sp = jj % kStages, bp = jj & 1;
-        const uint32_t v = sbase + kStageBase + sp * kStageBytes + kStageV;
-        for (int u = 0; u < 2; ++u) {
-          if (!act[u]) continue;
-          if (!wait_bar(p, bar_addr(sbase, kBPFull + 2 * u + bp), (jj >> 1) & 1)) { ok = false; return; }
-          tc_fence_after();
-          const uint32_t a = tmem + kTmS + (2 * u + bp) * 64;
+    if (lane != 0) return;
+    TraceAcc tr_kv, tr_p;
+    bool ok = wait_bar(p, bar_addr(sbase, kBQReady), 0);
+    auto issue_s = [&](int j) {
+      const int sk = j % kKStages, b = j & 1;
+      trace_stage(p, role, j, 2);
+      tc_fence_after();
+      const uint32_t k = sbase + kKBase + sk * kKStageBytes;
+      const uint32_t d = tmem + kTmS + 128 * b;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(tmem + kTmO + 128 * u, a + kk * 8, sdesc_sw128(v + kk * 2048, kAtom64, 1024), kIdescPV,
-                        (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar_addr(sbase, kBPvDone + u));
-        }
-        mma_commit(bar_addr(sbase, kBKvEmpty + sp));
-      };
-      for (int j = 0; j < n_stages && ok; ++j) {
-        const int s = j % kStages;
-        if (!wait_bar(p, bar_addr(sbase, kBKvFull + s), (j / kStages) & 1)) { ok = false; break; }
-        if ((j & 1) || j == n_stages - 1) {   // whole ring tile now in shared memory
-          fence_proxy_async_global();
-          red_release_gpu_add(consumed_flag(p, job, (j >> 1) % kRing), 1u);
-        }
-        tc_fence_after();
-        const uint32_t st = sbase + kStageBase + s * kStageBytes;
-        const int b = j & 1;
-        for (int u = 0; u < 2; ++u) {
-          if (!act[u]) continue;
-          const uint32_t q = u ? sQ1 : sQ0;
-          const uint32_t d = tmem + kTmS + (2 * u + b) * 64;
+      for (int kk = 0; kk < 12; ++kk)
+        mma_bf16_ts(d, tmem + kTmQ + kk * 8, sdesc_sw128(k + (kk >> 2) * kAtomQ + (kk & 3) * 32, 16, 1024), kIdescS,
+                    kk > 0 ? 1u : 0u);
+      mma_commit(bar_addr(sbase, kBSFull + b));
+      mma_commit(bar_addr(sbase, kBKEmpty + sk));
+      trace_stage(p, role, j, 3);
+    };
+    auto issue_pv = [&](int jj) {
+      const int b = jj & 1, sv = jj % kVStages;
+      trace_stage(p, role, jj, 4);
+      if (!wait_bar(p, bar_addr(sbase, kBVFull + sv), (jj / kVStages) & 1)) { ok = false; return; }
+      trace_stage(p, role, jj, 5);
+      tc_fence_after();
+      const uint32_t v = sbase + kVBase + sv * kVStageBytes;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (uint32_t)(kk >> 2) * kAtomQ + (uint32_t)(kk & 3) * 32u;
-            const uint32_t offk = (uint32_t)(kk >> 2) * kAtom64 + (uint32_t)(kk & 3) * 32u;
-            mma_bf16(d, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(st + kStageK + offk, 16, 1024), kIdescS,
-                     kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16_ts(tmem + kTmO, tmem + kTmS + 128 * b + kk * 8, sdesc_sw128(v + kk * 2048, kAtomQ, 1024), kIdescPV,
+                    (jj > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(bar_addr(sbase, kBPvDone + b));
+      mma_commit(bar_addr(sbase, kBVEmpty + sv));
+    };
+    // S(j) needs K(j); PV(j-1) needs P(j-1) and V(j-1).  S(j) may run before
+    // PV(j-1) (its S buffer's previous P was consumed by PV(j-2), issued
+    // earlier), so issue whichever becomes ready first; S(j+1) always waits
+    // for PV(j-1) to have been issued.
+    int js = 0, jp = 0;           // next S to issue, next PV to issue
+    const uint64_t t_start = p.trace ? global_timer_ns() : 0;
+    uint64_t t_last = global_timer_ns();
+    uint32_t polls = 0;
+    while (ok && (js < n_tiles || jp < n_tiles)) {
+      bool progressed = false;
+      const bool want_s = js < n_tiles && js <= jp + 1;
+      const bool want_p = jp < js;
+      // sleep on the barrier of the older outstanding work; peek at the other one
+      const uint32_t hint = (want_s && want_p) ? 200u : 20000u;
+      if (want_s && mbar_try_wait_hint(bar_addr(sbase, kBKFull + js % kKStages), (js / kKStages) & 1,
+                                       want_p ? 0u : hint)) {
+        issue_s(js++);
+        progressed = true;
+      }
+      if (want_p && mbar_try_wait_hint(bar_addr(sbase, kBPFull + (jp & 1)), (jp >> 1) & 1, hint)) {
+        issue_pv(jp++);
+        progressed = true;
+      }
+      if (progressed) {
+        polls = 0;
+      } else if ((++polls & 255u) == 0u) {
+        const uint64_t now = global_timer_ns();
+        if (polls == 256u) t_last = now;
+        else if (now - t_last > kWaitLimitNs) {
+          atomicOr(p.err, kErrTimeout);
+          ok = false;
+        }
+      }
+    }
+    tr_kv.t = p.trace ? global_timer_ns() - t_start : 0;
+    if (ok && n_tiles > 0) {
+      // the last commits' arrivals must land before the barriers are reset for the next role
+      const int jl = n_tiles - 1;
+      if (ok && !wait_bar(p, bar_addr(sbase, kBVEmpty + jl % kVStages), (jl / kVStages) & 1)) ok = false;
+      if (ok && !wait_bar(p, bar_addr(sbase, kBKEmpty + jl % kKStages), (jl / kKStages) & 1)) ok = false;
+    }
+    if (!ok) ctl->abort = 1;
+    trace_put(p, role, 4, tr_kv.t);
+    trace_put(p, role, 5, tr_p.t);
+  } else {
+    if (warp < 4) {
+      // ---------------------------------------------------------- Q -> TMEM (warpgroup 0)
+    const int r = tid & 127;
+      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+      const bool live = r < nq;
+      const int grow = grow0 + r;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_bf16 + ((int64_t)(live ? grow : 0) * H + J.head) * kDqk);
+      const int64_t delta = live ? (int64_t)__ldg(p.q_pos + grow) - J.rope_offset : 0;
+      // 32 TMEM columns (64 bf16) at a time: q_nope 0..63, q_nope 64..127, rotated q_rope
+#pragma unroll 1
+      for (int part = 0; part < 3; ++part) {
+        uint32_t qv[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 a = live ? __ldg(src + 8 * part + c) : make_uint4(0, 0, 0, 0);
+          uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+          if (part == 2) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float sn, cs;
+              rope_sincos(delta, p.rope_frac[4 * c + i], &sn, &cs);
+              const float x0 = __uint_as_float(w4[i] << 16), x1 = __uint_as_float(w4[i] & 0xFFFF0000u);
+              w4[i] = pack_bf16(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+            }
           }
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(d, sdesc_sw128(q + 2 * kAtomQ + kk * 32, 16, 1024), sdesc_sw128(st + kStageKR + kk * 32, 16, 1024),
-                     kIdescS, 1u);
-          mma_commit(bar_addr(sbase, kBSFull + 2 * u + b));
+          for (int i = 0; i < 4; ++i) qv[4 * c + i] = w4[i];
         }
-        if (j >= 1) issue_pv(j - 1);
+        tmem_st32(tmem + lane_off + kTmQ + 32 * part, qv);
       }
-      if (ok && n_stages > 0) {
-        issue_pv(n_stages - 1);
-        // the last commit's arrival must land before the barriers are reset for the next role
-        const int jl = n_stages - 1;
-        if (ok && !wait_bar(p, bar_addr(sbase, kBKvEmpty + jl % kStages), (jl / kStages) & 1)) ok = false;
-      }
-      if (!ok) ctl->abort = 1;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_addr(sbase, kBQReady));
     }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ softmax / epilogue
-    const int u = warp >> 2;
+    // ------------------------------------------------------------ softmax / epilogue (warps 0..7)
+    const int w = warp >> 2;           // key half
     const int r = tid & 127;
-    const int nq = u ? nq1 : nq0;
-    const uint32_t q = u ? sQ1 : sQ0;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int grow = grow0 + 128 * u + r;
-    // rotate q_rope of this row into the document frame: angle (q_pos - offset)
-    if (!wait_bar_warp(p, bar_addr(sbase, kBQFull), 0)) ctl->abort = 1;
-    if (r < nq) {
-      const int64_t delta = (int64_t)__ldg(p.q_pos + grow) - J.rope_offset;
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = q + 2 * kAtomQ + sw128_off(r, c);
-        uint32_t w[4];
-        lds128(addr, w);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float sn, cs;
-          rope_sincos(delta, p.rope_frac[4 * c + i], &sn, &cs);
-          const float x0 = __uint_as_float(w[i] << 16), x1 = __uint_as_float(w[i] & 0xFFFF0000u);
-          w[i] = pack_bf16(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
-        }
-        sts128(addr, w[0], w[1], w[2], w[3]);
-      }
-    }
-    fence_proxy_async_smem();
-    named_bar_sync(1 + u, 128);
-    if (r == 0) mbar_arrive(bar_addr(sbase, kBQReady + u));
-    if (nq == 0) return;
-
-    const int qtok = J.q_tok0 + q0 + 128 * u + r;
+    float* xchg = reinterpret_cast<float*>(sgen + kXchgBase);   // [2 buffers][2 halves][128] maxima, then sums
+    const int qtok = J.q_tok0 + q0 + r;
     const float sl2 = p.scale_log2;
-    float m_used = -INFINITY, l_run = 0.f;
+    float m_used = -INFINITY, l_part = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_stages; ++j) {
+    TraceAcc tr_s;
+    for (int j = 0; j < n_tiles; ++j) {
       const int b = j & 1;
-      if (!wait_bar_warp(p, bar_addr(sbase, kBSFull + 2 * u + b), (j >> 1) & 1)) { ok = false; break; }
+      const uint64_t w0 = tr_s.begin(p);
+      if (ok && !wait_bar_warp(p, bar_addr(sbase, kBSFull + b), (j >> 1) & 1)) ok = false;
+      tr_s.end(p, w0);
+      if (tid == 0) trace_stage(p, role, j, 6);
       tc_fence_after();
-      const uint32_t scol = tmem + lane_off + kTmS + (2 * u + b) * 64;
+      const uint32_t scol = tmem + lane_off + kTmS + 128 * b + 64 * w;
       uint32_t v[64];
-      {
-        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-        tmem_ld32(scol, v0);
-        tmem_ld32(scol + 32, v1);
-      }
-      const int kt0 = J.t0 + 64 * j;
+      if (ok) tmem_ld64(scol, v);
+      const int kt0 = J.t0 + 128 * j + 64 * w;
       const bool full = kt0 >= J.k_begin && kt0 + 63 < J.k_end && kt0 + 63 <= qtok;
-      float mx = -INFINITY;
+      float m8[8];
       if (full) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(v[c]));
+        for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(v[i]);
+#pragma unroll
+        for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(v[c]));
       } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const int kt = kt0 + c;
           const bool okc = kt >= J.k_begin && kt < J.k_end && kt <= qtok;
           const float x = okc ? __uint_as_float(v[c]) : -INFINITY;
           v[c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          m8[c & 7] = fmaxf(m8[c & 7], x);
         }
       }
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      // row maximum over both key halves; the barrier also orders both
+      // warpgroups' S loads before either overwrites S with P
+      xchg[(b * 2 + w) * 128 + r] = mx;
+      tc_fence_before();
+      named_bar_sync(1, 256);
+      tc_fence_after();
+      mx = fmaxf(mx, xchg[(b * 2 + (1 - w)) * 128 + r]);
       const float m_tile = mx * sl2;
       float alpha = 1.f;
       const bool rescale = m_tile > m_used + kRescaleThreshold;
@@ -322,25 +413,26 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
         m_used = m_tile;
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      float sum = 0.f;
+      float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float a = ex2(fmaf(__uint_as_float(v[2 * c]), sl2, -mref));
         const float bb = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sl2, -mref));
-        sum += a + bb;
+        s8[c & 7] += a + bb;
         pk[c] = pack_bf16(a, bb);
       }
-      tmem_st32(scol, pk);
-      l_run = l_run * alpha + sum;
-      if (j >= 1) {
-        // O holds PV of stages < j: wait for the last one before touching O
-        if (!wait_bar_warp(p, bar_addr(sbase, kBPvDone + u), (j - 1) & 1)) { ok = false; break; }
+      if (ok) tmem_st32(tmem + lane_off + kTmS + 128 * b + 32 * w, pk);   // P over S's first 64 columns
+      l_part = l_part * alpha + (((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
+      if (j >= 1 && ok && __any_sync(0xffffffffu, rescale)) {
+        // O holds PV of tiles < j: PV(j-1) must be done before O is rescaled.  PV(j-2)
+        // finished before S(j) did, so this barrier is at most one phase behind.
+        if (!wait_bar_warp(p, bar_addr(sbase, kBPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) ok = false;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
-          const uint32_t ocol = tmem + lane_off + kTmO + 128 * u;
+        if (ok) {
+          const uint32_t ocol = tmem + lane_off + kTmO + 64 * w;
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t o[32];
             tmem_ld32(ocol + cc * 32, o);
 #pragma unroll
@@ -351,59 +443,66 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_addr(sbase, kBPFull + 2 * u + b));
+      mbar_arrive(bar_addr(sbase, kBPFull + b));
+      if (tid == 0) trace_stage(p, role, j, 7);
     }
-    if (ok && n_stages > 0 && !wait_bar_warp(p, bar_addr(sbase, kBPvDone + u), (n_stages - 1) & 1)) ok = false;
+    if (ok && n_tiles > 0 &&
+        !wait_bar_warp(p, bar_addr(sbase, kBPvDone + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1))
+      ok = false;
+    if (tid == 0) trace_put(p, role, 6, tr_s.t);
+    // row sum over both key halves (its own region: a slow partner may still read the maxima)
+    xchg[(4 + w) * 128 + r] = l_part;
+    named_bar_sync(1, 256);
+    const float l_run = l_part + xchg[(4 + (1 - w)) * 128 + r];
     if (!ok) { ctl->abort = 1; return; }
     tc_fence_after();
-    // ---- epilogue
-    const bool empty = n_stages == 0 || !(l_run > 0.f);
+    // ---- epilogue: this warpgroup writes output columns 64w .. 64w+63
+    const bool empty = n_tiles == 0 || !(l_run > 0.f);
     const float inv_l = empty ? 0.f : 1.f / l_run;
     const bool live = r < nq;
+    const int grow = grow0 + r;
     const int64_t orow = J.slot < 0 ? (int64_t)grow : (int64_t)J.slot * p.slot_stride_rows + grow;
-    const uint32_t ocol = tmem + lane_off + kTmO + 128 * u;
+    const uint32_t ocol = tmem + lane_off + kTmO + 64 * w;
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int cc = 0; cc < 2; ++cc) {
       uint32_t o[32];
-      if (n_stages > 0) tmem_ld32(ocol + cc * 32, o);
+      if (n_tiles > 0) tmem_ld32(ocol + cc * 32, o);
       if (!live) continue;
+      const int col0 = 64 * w + 32 * cc;
       if (J.slot < 0 && p.out_bf16) {
-        uint16_t* dst = static_cast<uint16_t*>(p.out) + (orow * H + J.head) * kDv + cc * 32;
+        uint16_t* dst = static_cast<uint16_t*>(p.out) + (orow * H + J.head) * kDv + col0;
 #pragma unroll
         for (int i = 0; i < 32; i += 8) {
-          uint4 w;
-          w.x = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 0]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 1]) * inv_l);
-          w.y = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 2]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 3]) * inv_l);
-          w.z = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 4]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 5]) * inv_l);
-          w.w = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 6]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(dst + i) = w;
+          uint4 q;
+          q.x = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 0]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 1]) * inv_l);
+          q.y = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 2]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 3]) * inv_l);
+          q.z = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 4]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 5]) * inv_l);
+          q.w = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 6]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 7]) * inv_l);
+          *reinterpret_cast<uint4*>(dst + i) = q;
         }
       } else {
-        float* dst = (J.slot < 0 ? static_cast<float*>(p.out) : p.part_out) + (orow * H + J.head) * kDv + cc * 32;
+        float* dst = (J.slot < 0 ? static_cast<float*>(p.out) : p.part_out) + (orow * H + J.head) * kDv + col0;
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          float4 w;
-          w.x = empty ? 0.f : __uint_as_float(o[i + 0]) * inv_l;
-          w.y = empty ? 0.f : __uint_as_float(o[i + 1]) * inv_l;
-          w.z = empty ? 0.f : __uint_as_float(o[i + 2]) * inv_l;
-          w.w = empty ? 0.f : __uint_as_float(o[i + 3]) * inv_l;
-          *reinterpret_cast<float4*>(dst + i) = w;
+          float4 q;
+          q.x = empty ? 0.f : __uint_as_float(o[i + 0]) * inv_l;
+          q.y = empty ? 0.f : __uint_as_float(o[i + 1]) * inv_l;
+          q.z = empty ? 0.f : __uint_as_float(o[i + 2]) * inv_l;
+          q.w = empty ? 0.f : __uint_as_float(o[i + 3]) * inv_l;
+          *reinterpret_cast<float4*>(dst + i) = q;
         }
       }
     }
-    if (live) {
+    if (live && w == 0) {
       const float lse = empty ? -INFINITY : m_used * 0.69314718055994531f + logf(l_run);
       (J.slot < 0 ? p.lse : p.part_lse)[orow * H + J.head] = lse;
     }
-  } else if (warp < 12) {
-    // warpgroup 2 waits for Q so no TMA is in flight when the role ends
-    if (!wait_bar(p, bar_addr(sbase, kBQFull), 0)) ctl->abort = 1;
   }
 }
 
 // =============================================================== producer
-__device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi, uint32_t sbase, uint32_t tmem,
-                             volatile Ctl* ctl) {
+__device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi, int role, uint32_t sbase,
+                             uint32_t tmem, volatile Ctl* ctl) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_pass = (J.n_tiles + 1) >> 1;
   const int H = p.num_heads;
@@ -412,8 +511,11 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
   for (int pp = pi; pp < n_pass; pp += J.n_prod) ++my_passes;
   if (my_passes == 0) return;
 
-  if (warp == 12) {
+  if (warp == 8 || (warp == 10 && !p.kv_fp8)) {
+    // TMA issue, split over two warps (BF16): warp 8 loads kv_b_proj and the first
+    // 128 tokens' latent slices, warp 10 the second 128 tokens'.  FP8: warp 8 alone.
     if (lane == 0) {
+      const bool primary = warp == 8;
       int g = 0;
       for (int n = 0; n < my_passes; ++n) {
         const int pass = pi + n * J.n_prod;
@@ -422,35 +524,40 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
           const int lb = (J.t0 >> 6) + 4 * pass + i;
           const int tok = lb * 64;
           const bool live = tok + 63 >= J.k_begin && tok < J.k_end;
-          rows[i] = live ? block_row(p, J.req, lb, true) : -kBlock;
+          rows[i] = live ? block_row(p, J.req, lb, primary) : -kBlock;
         }
         for (int k = 0; k < kDc / 64; ++k, ++g) {
           const int s = g & 1;
           if (g >= 2 && !wait_bar(p, bar_addr(sbase, kBProdEmpty + s), ((g >> 1) - 1) & 1)) { ctl->abort = 1; return; }
           const uint32_t st = sbase + s * kPStageBytes;
           const uint32_t bar = p.kv_fp8 ? bar_addr(sbase, kBRawFull + s) : bar_addr(sbase, kBProdFull + s);
-          mbar_arrive_expect_tx(bar, p.kv_fp8 ? (16384u + 32768u) : kPStageBytes);
+          if (primary) mbar_arrive_expect_tx(bar, p.kv_fp8 ? (16384u + 32768u) : kPStageBytes);
           for (int i = 0; i < 4; ++i) {
             if (p.kv_fp8)
               tma_load_2d(sbase + kPRawBase + s * 16384 + i * 4096, &p.tm_c, 64 * k, rows[i], bar);
-            else
+            else if ((i < 2) == primary)
               tma_load_2d(st + (i < 2 ? kPCA : kPCB) + (i & 1) * kAtom64, &p.tm_c, 64 * k, rows[i], bar);
           }
-          for (int w = 0; w < 4; ++w) {
-            const int x = (w < 2) ? (h * kDnope + 64 * w) : (H * kDnope + h * kDv + 64 * (w - 2));
-            tma_load_2d(st + kPW + w * kAtom64, &p.tm_w, x, 64 * k, bar);
+          if (primary) {
+            tma_load_3d(st + kPW, &p.tm_w, 0, 64 * k, 2 * h, bar);                                   // K_nope cols
+            tma_load_3d(st + kPW + 2 * kAtom64, &p.tm_w, 0, 64 * k, (H * kDnope + h * kDv) / 64, bar); // V cols
           }
         }
       }
     }
-  } else if (warp == 13) {
+  } else if (warp == 9) {
     if (lane == 0) {
+      TraceAcc tr_op, tr_acc;
       int g = 0;
       for (int n = 0; n < my_passes; ++n) {
+        const uint64_t wa = tr_acc.begin(p);
         if (n >= 1 && !wait_bar(p, bar_addr(sbase, kBAccEmpty), (n - 1) & 1)) { ctl->abort = 1; return; }
+        tr_acc.end(p, wa);
         for (int k = 0; k < kDc / 64; ++k, ++g) {
           const int s = g & 1;
+          const uint64_t w0 = tr_op.begin(p);
           if (!wait_bar(p, bar_addr(sbase, kBProdFull + s), (g >> 1) & 1)) { ctl->abort = 1; return; }
+          tr_op.end(p, w0);
           tc_fence_after();
           const uint32_t st = sbase + s * kPStageBytes;
 #pragma unroll
@@ -463,6 +570,9 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
         }
         mma_commit(bar_addr(sbase, kBAccFull));
       }
+      trace_put(p, role, 4, tr_op.t);
+      trace_put(p, role, 5, tr_acc.t);
+      trace_put(p, role, 7, (unsigned long long)my_passes);
     }
   } else if (warp < 8) {
     // conversion: warpgroup 0 -> tile 2*pass, warpgroup 1 -> tile 2*pass + 1
@@ -470,53 +580,92 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
     const int r = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float oscale = p.kv_fp8 ? p.kv_scale : 1.f;
+    const uint32_t stage_out = sbase + kPOutBase + wg * 32768;   // [128 rows x 128 cols] bf16, 2 SW128 blocks
+    TraceAcc tr_c;
     for (int n = 0; n < my_passes; ++n) {
       const int pass = pi + n * J.n_prod;
       const int t = 2 * pass + wg;
+      const bool live_tile = t < J.n_tiles;
+      const int slot = t % kRing;
+      const int tok = J.t0 + 128 * t + r;
+      const bool valid = tok >= J.k_begin && tok < J.k_end;
+      const uint32_t acc = tmem + lane_off + (wg ? kTmAccB : kTmAccA);
       if (!wait_bar_warp(p, bar_addr(sbase, kBAccFull), n & 1)) ctl->abort = 1;
       tc_fence_after();
-      if (t < J.n_tiles) {
-        const int slot = t % kRing;
-        if (r == 0 && !ctl->abort) {
-          if (t >= (int)kRing &&
-              !wait_flag_geq(p, consumed_flag(p, job, slot), (uint32_t)consumers_needing_tile(J, t - kRing)))
-            ctl->abort = 1;
-          *consumed_flag(p, job, slot) = 0u;   // ordered before the release of `ready` below
-        }
-        named_bar_sync(1 + wg, 128);
-        if (ctl->abort) return;                // every thread of the warpgroup leaves here together
-        const int tok = J.t0 + 128 * t + r;
-        const bool valid = tok >= J.k_begin && tok < J.k_end;
-        uint16_t* dst = p.ring + ((size_t)job * kRing * 128 + (size_t)slot * 128 + r) * 256;
-        const uint32_t acc = tmem + lane_off + (wg ? kTmAccB : kTmAccA);
+      // staging is free: thread 0 waited for the previous tile's stores to read it
+      named_bar_sync(1 + wg, 128);
+      uint32_t vpk[64];
+      if (live_tile && !ctl->abort) {
+        // K_nope half (accumulator columns 0..127) -> shared staging
 #pragma unroll 1
-        for (int cc = 0; cc < 8; ++cc) {
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t a[32];
           tmem_ld32(acc + cc * 32, a);
-          uint32_t w[16];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              w[i] = valid ? pack_bf16(__uint_as_float(a[8 * g + 2 * i]) * oscale,
+                                       __uint_as_float(a[8 * g + 2 * i + 1]) * oscale) : 0u;
+            sts128(stage_out + (cc >> 1) * kAtomQ + sw128_off(r, (cc & 1) * 4 + g), w[0], w[1], w[2], w[3]);
+          }
+        }
+        // V half (columns 128..255) -> registers, so the accumulators can be released now
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t a[32];
+          tmem_ld32(acc + 128 + cc * 32, a);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            w[i] = valid ? pack_bf16(__uint_as_float(a[2 * i]) * oscale, __uint_as_float(a[2 * i + 1]) * oscale) : 0u;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4*>(dst + cc * 32 + 8 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            vpk[16 * cc + i] = valid ? pack_bf16(__uint_as_float(a[2 * i]) * oscale, __uint_as_float(a[2 * i + 1]) * oscale) : 0u;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_addr(sbase, kBAccEmpty));     // the next pass may overwrite the accumulators
+      if (live_tile) {
+        fence_proxy_async_smem();
+        named_bar_sync(1 + wg, 128);
+        const int zb = (job * (int)kRing + slot) * 4;
+        if (r == 0 && !ctl->abort) {
+          const uint64_t w0 = tr_c.begin(p);
+          // the slot's previous occupant (tile t - ring) must be published and fully consumed
+          if (t >= (int)kRing &&
+              !(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - kRing + 1)) &&
+                wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - kRing))))
+            ctl->abort = 1;
+          tr_c.end(p, w0);
+          *consumed_flag(p, job, slot) = 0u;    // ordered before the release of `ready` below
+          tma_store_3d(&p.tm_ring, stage_out, 0, 0, zb);               // K_nope lo | hi
+          bulk_commit();
+          bulk_wait_read0();                    // staging free for the V half
         }
         named_bar_sync(1 + wg, 128);
+        if (ctl->abort) return;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            sts128(stage_out + (cc >> 1) * kAtomQ + sw128_off(r, (cc & 1) * 4 + g), vpk[16 * cc + 4 * g],
+                   vpk[16 * cc + 4 * g + 1], vpk[16 * cc + 4 * g + 2], vpk[16 * cc + 4 * g + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1 + wg, 128);
         if (r == 0) {
+          tma_store_3d(&p.tm_ring, stage_out, 0, 0, zb + 2);           // V lo | hi
+          bulk_commit();
+          bulk_wait0();                         // both halves have landed
+          fence_proxy_async_global();
           __threadfence();
           st_release_gpu(ready_flag(p, job, slot), (uint32_t)t + 1);
         }
-      } else {
-        named_bar_sync(1 + wg, 128);
-        if (ctl->abort) return;
       }
-      tc_fence_before();
-      mbar_arrive(bar_addr(sbase, kBAccEmpty));
+      if (ctl->abort) return;
     }
-  } else if (warp < 12) {
-    // e4m3 latent staging -> bf16 MMA operand (FP8 cache only)
+    if (tid == 0) trace_put(p, role, 3, tr_c.t);
+  } else if (warp >= 10) {
+    // e4m3 latent staging -> bf16 MMA operand (FP8 cache only), warps 10..11
     if (!p.kv_fp8) return;
-    const int r = tid - 256;
+    const int r = tid - 320;
     int g = 0;
     for (int n = 0; n < my_passes; ++n) {
       for (int k = 0; k < kDc / 64; ++k, ++g) {
@@ -526,7 +675,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
         const uint32_t raw = sbase + kPRawBase + s * 16384;
         const uint32_t st = sbase + s * kPStageBytes;
 #pragma unroll 4
-        for (int idx = r; okw && idx < 256 * 8; idx += 128) {
+        for (int idx = r; okw && idx < 256 * 8; idx += 64) {
           const int row = idx >> 3, c = idx & 7;   // row 0..255 of the pass, chunk of 8 values
           uint32_t lo, hi;
           asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(raw + row * 64 + c * 8));
@@ -534,7 +683,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
                  e4m3x2_to_bf16x2(lo >> 16), e4m3x2_to_bf16x2(hi & 0xFFFFu), e4m3x2_to_bf16x2(hi >> 16));
         }
         fence_proxy_async_smem();
-        named_bar_sync(3, 128);
+        named_bar_sync(3, 64);
         if (ctl->abort) return;                // together, after the barrier
         if (r == 0) mbar_arrive(bar_addr(sbase, kBProdFull + s));
       }
@@ -551,7 +700,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(const __grid
   const int tid = threadIdx.x;
 
   if (tid == 0) {
-    prefetch_tensormap(&p.tm_q);
     prefetch_tensormap(&p.tm_kr);
     prefetch_tensormap(&p.tm_c);
     prefetch_tensormap(&p.tm_w);
@@ -606,18 +754,24 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(const __grid
       for (uint32_t i = 0; i < kNumBars; ++i) {
         mbar_inval(bar_addr(sbase, i));
         uint32_t cnt = 1;
-        if (!producer && (i >= kBPFull && i < kBPFull + 4)) cnt = 128;
+        if (!producer && (i == kBPFull || i == kBPFull + 1)) cnt = 256;
+        if (!producer && i == kBQReady) cnt = 128;
         if (producer && i == kBAccEmpty) cnt = 256;
         mbar_init(bar_addr(sbase, i), cnt);
       }
       fence_mbar_init();
     }
     __syncthreads();
-    if (producer) run_producer(p, J, job, idx, sbase, tmem, ctl);
-    else run_consumer(p, J, job, idx - J.n_prod, sbase, sgen, tmem, ctl);
+    if (p.trace && tid == 0) {
+      trace_put(p, role, 0, global_timer_ns());
+      trace_put(p, role, 2, ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)producer << 31) | (unsigned)job);
+    }
+    if (producer) run_producer(p, J, job, idx, role, sbase, tmem, ctl);
+    else run_consumer(p, J, job, idx - J.n_prod, role, sbase, sgen, tmem, ctl);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (p.trace && tid == 0) trace_put(p, role, 1, global_timer_ns());
   }
   tc_fence_before();
   __syncthreads();

@@ -23,8 +23,8 @@ constexpr int kMaxHeads = 128;
 constexpr uint32_t kErrBadBlock = 1u;
 constexpr uint32_t kErrTimeout = 2u;
 
-// One KV split: a contiguous key range of one request with one RoPE offset.
-// Every split gives a partial (out, lse) per (query row, head) in `slot`.
+// One KV split of the plan: a contiguous key range of one request with one
+// RoPE offset (a context chunk of a segment, or the extend stage).
 struct Split {
   int32_t req;        // request index (block-table row)
   int32_t q_begin;    // global row of the request's first query
@@ -32,33 +32,9 @@ struct Split {
   int32_t q_tok0;     // token index of the request's first query (= C_r)
   int32_t k_begin;    // first key token
   int32_t k_end;      // one past the last key token
-  int32_t slot;       // partial-state slot of this split within its request
-  int32_t tile_begin; // first CTA (blockIdx.x) of this split
+  int32_t slot;       // index of this split within its request
+  int32_t pad;
   int64_t rope_offset;
-};
-
-constexpr int kMaxSplitsPerLaunch = 192;
-
-struct PrefillParams {
-  const uint16_t* q;          // bf16 [T_q, H, 192]
-  const int32_t* q_pos;       // [T_q]
-  const uint8_t* kv_cache;    // rows of 1152 B or 640 B
-  const int32_t* block_table; // [B, max_blocks]
-  const uint16_t* w;          // bf16 [512, H*256]
-  float* part_out;            // fp32 [slots, T_q, H, 128]
-  float* part_lse;            // fp32 [slots, T_q, H]
-  uint32_t* err;
-  int64_t slot_stride_rows;   // T_q
-  int num_heads;
-  int kv_fp8;
-  float kv_scale;
-  int num_blocks;
-  int max_blocks;
-  float scale_log2;           // softmax_scale * log2(e)
-  int num_splits;
-  int num_tiles;              // gridDim.x
-  uint64_t rope_frac[kDr / 2];
-  Split splits[kMaxSplitsPerLaunch];
 };
 
 // Query rows [row_begin, row_end) whose partial states live in slots 0..nslots-1.
@@ -85,7 +61,7 @@ struct MergeParams {
 };
 
 // ------------------------------------------------------------ fused persistent kernel
-constexpr int kRingDepth = 6;     // 128-token K/V tiles per job ring
+constexpr int kRingDepth = 32;    // 128-token K/V tiles per job ring
 constexpr int kMaxPieces = 448;   // pieces per launch (kernel-parameter budget)
 
 // One key range of one request attended with one RoPE offset, for every head.
@@ -99,7 +75,7 @@ struct Piece {
   int32_t k_end;       // one past the last key token
   int32_t slot;        // partial-state slot, or -1: write the final out/lse
   int32_t role_begin;  // first role of this piece in the launch's role queue
-  int32_t n_cons;      // consumer roles per head (256 queries each)
+  int32_t n_cons;      // consumer roles per head (128 queries each)
   int32_t n_prod;      // producer roles per head
   int64_t rope_offset;
 };
@@ -111,11 +87,11 @@ struct Job {
 };
 
 struct FusedParams {
-  CUtensorMap tm_q;      // bf16 q [T_q][H][192], box 64 x 1 x 128
   CUtensorMap tm_kr;     // cache rows, box = 64 rows x 128 B at the k_rope columns
   CUtensorMap tm_c;      // cache rows, box = 64 rows x one 64-wide latent slice
-  CUtensorMap tm_w;      // bf16 kv_b_proj [512][H*256], box 64 x 64
-  CUtensorMap tm_ring;   // bf16 ring [jobs*ring*128][256], box 64 x 64
+  CUtensorMap tm_w;      // bf16 kv_b_proj as [H*4 blocks][512 rows][64 cols], box 64 x 64 x 2
+  CUtensorMap tm_ring;   // bf16 ring as [jobs*ring*4 blocks][128 rows][64 cols], box 64 x 128 x 2
+  const uint16_t* q_bf16;  // q [T_q][H][192]
   uint32_t* err;
   uint32_t* queue;       // role counter
   uint32_t* flags;       // per job: ready[ring], consumed[ring]
@@ -136,9 +112,13 @@ struct FusedParams {
   float scale_log2;
   int n_pieces;
   int n_roles;
+  unsigned long long* trace;   // optional, kTraceWords per role (see fused.cu)
+  int trace_detail_role;       // role whose stages are timed one by one (-1: none)
   uint64_t rope_frac[kDr / 2];
   Piece pieces[kMaxPieces];
 };
+
+constexpr int kTraceWords = 8;
 
 static_assert(sizeof(FusedParams) <= 32000, "kernel parameter space");
 
@@ -147,7 +127,6 @@ cudaError_t fused_grid_size(int* grid);
 int fused_smem_bytes();
 
 // Kernel launchers (return cudaError_t of the launch).
-cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s);
 cudaError_t launch_merge_slots(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_merge2(const float* oa, const float* la, const float* ob, const float* lb,
                           float* o, float* l, int64_t rows, int d_v, cudaStream_t s);

@@ -50,7 +50,7 @@ def _up(x, a=256):
     return (x + a - 1) // a * a
 
 
-def fused_layout(pieces, heads, slots, total_q, ring_depth=6):
+def fused_layout(pieces, heads, slots, total_q, ring_depth=32):
     """Workspace of the fused path: 256 B header, per-job ring flags, per-job
     K/V rings of `ring_depth` 128-token bf16 tiles, then partial states."""
     jobs = pieces * heads

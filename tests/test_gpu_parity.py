@@ -217,3 +217,23 @@ def test_prefill_empty_context_segments(api):
                            chunk=64, softmax_scale=wl.softmax_scale, segments=np.zeros((0, 4), np.int64))
     ref = O.mla_prefill(**O.workload_args(wl), parts=2)
     assert_close(out.cpu().numpy(), lse.cpu().numpy(), *ref, visible_keys(wl, 2))
+
+
+def test_prefill_small_workspace_runs_in_several_launches(api):
+    """A workspace that holds the rings of one piece only: the call splits its
+    pieces over several launches and must give the same result."""
+    from mla_prefix_cache_gb300 import _lib
+    wl = W.make_workload("sw", 4, [192], [70], chunk=64, seed=35, doc_len=64)   # 3 documents + extend = 4 pieces
+    dw = api.DeviceWorkload(wl)
+    full = api.prefill_workspace_size(wl.seq_lens, wl.cu_q, 4, wl.segments, wl.chunk)
+    ring_per_piece = 4 * 32 * 128 * 256 * 2
+    small = torch.empty(full - 2 * ring_per_piece, dtype=torch.uint8, device="cuda")
+    n0 = api.launch_count()
+    out, lse = dw.run(workspace=small)
+    torch.cuda.synchronize()
+    assert api.launch_count() - n0 >= 3          # at least two fused launches plus the merge
+    ref = O.mla_prefill(**O.workload_args(wl))
+    assert_close(out.cpu().numpy(), lse.cpu().numpy(), *ref, visible_keys(wl))
+    tiny_ws = torch.empty(4096, dtype=torch.uint8, device="cuda")
+    with pytest.raises(_lib.MLAError):
+        dw.run(workspace=tiny_ws)

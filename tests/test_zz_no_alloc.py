@@ -58,7 +58,7 @@ def test_noalloc_matches_workspace_entry_point(wl):
 def test_noalloc_rejects_problems_beyond_its_scratch():
     from mla_prefix_cache_gb300 import _lib, api
     L = _lib.load()
-    wl = W.make_workload("big", 128, [64], [1], seed=41)   # 128 heads: 48 MiB of K/V rings
+    wl = W.make_workload("big", 128, [64], [1], seed=41)   # 128 heads: 256 MiB of K/V rings for one piece
     assert api.prefill_workspace_size(wl.seq_lens, wl.cu_q, 128, None, wl.chunk) > _lib.NOALLOC_SCRATCH_BYTES
     dw = api.DeviceWorkload(wl)
     out = torch.zeros((1, 128, 128), device="cuda")
