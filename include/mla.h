@@ -118,7 +118,9 @@ typedef struct {
  *               workspace also works as long as it holds the partial states
  *               and the K/V rings of one piece (one request's key range of at
  *               most max(chunk, 16384) tokens, for all heads): the call then
- *               runs its pieces in several launches.  Holds the device error
+ *               runs its pieces in several launches.  The size includes
+ *               room for the rows of an FP8 cache dequantised to bf16 by the
+ *               call's gather pass (1152 B per token).  Holds the device error
  *               word; must not be shared by calls that may overlap on the GPU.
  *  H            num_heads in [1, 128].
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H > 128, chunk not a

@@ -138,6 +138,8 @@ static int env_int(const char* name, int dflt) {
 struct FusedPlan {
   std::vector<Piece> pieces;      // LPT order, role_begin unset
   std::vector<RowRange> merge;    // requests whose pieces go to partial slots
+  std::vector<GatherReq> gather;  // FP8 caches: requests whose rows are dequantised up front
+  int gather_blocks = 0;
   int max_slots = 0;
   int64_t total_q = 0;
 };
@@ -149,9 +151,11 @@ struct FusedPlan {
 // merge_attn_states would; pieces of one request are folded by the merge
 // kernel.
 static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const int32_t* cu_q, int num_reqs,
-                            int chunk, FusedPlan* fp) {
+                            int chunk, bool gather_rows, FusedPlan* fp) {
   fp->pieces.clear();
   fp->merge.clear();
+  fp->gather.clear();
+  fp->gather_blocks = 0;
   fp->max_slots = 0;
   fp->total_q = splits.total_q;
   const int max_keys = std::max(chunk, env_int("MLA_MAX_PIECE_KEYS", 16384));
@@ -183,8 +187,19 @@ static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const i
       pr.push_back(pc);
     }
     const int np = (int)pr.size();
+    int row_block0 = -1;
+    if (gather_rows && np > 0) {
+      GatherReq g{};
+      g.req = r;
+      g.base_block = fp->gather_blocks;
+      g.seq_len = seq_lens[r];
+      fp->gather.push_back(g);
+      row_block0 = fp->gather_blocks;
+      fp->gather_blocks += (seq_lens[r] + kBlock - 1) / kBlock;
+    }
     for (int i = 0; i < np; ++i) {
       Piece& pc = pr[i];
+      pc.row_block0 = row_block0;
       pc.slot = np == 1 ? -1 : i;
       pc.n_cons = (E + 127) / 128;
       const int t0 = pc.k_begin & ~(kBlock - 1);
@@ -209,7 +224,8 @@ static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const i
 }
 
 struct FusedWs {
-  size_t err_off = 0, queue_off = 4, flags_off = 256, flags_bytes = 0, ring_off = 0, lse_off = 0, out_off = 0, total = 0;
+  size_t err_off = 0, queue_off = 4, flags_off = 256, flags_bytes = 0, ring_off = 0, gath_off = 0, lse_off = 0,
+         out_off = 0, total = 0;
   int pieces_per_launch = 0;
 };
 
@@ -223,7 +239,9 @@ static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads, int ppl) {
   w.ring_off = up256(w.flags_off + w.flags_bytes);
   const size_t ring_bytes = jobs * kRingDepth * 128 * 256 * sizeof(uint16_t);
   const size_t rows = (size_t)fp.max_slots * (size_t)fp.total_q * (size_t)num_heads;
-  w.lse_off = up256(w.ring_off + ring_bytes);
+  w.gath_off = up256(w.ring_off + ring_bytes);
+  const size_t gath_bytes = (size_t)fp.gather_blocks * kBlock * kRowBytesBf16;
+  w.lse_off = up256(w.gath_off + gath_bytes);
   w.out_off = up256(w.lse_off + rows * sizeof(float));
   w.total = w.out_off + rows * kDv * sizeof(float);
   return w;
@@ -310,21 +328,19 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   std::memset(&p, 0, sizeof(p));
 
   const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
-  const uint64_t cache_rows = (uint64_t)num_blocks * kBlock;
+  // FP8 caches: the gather pass first writes every needed row as exact bf16(e4m3) (no
+  // scale) into the workspace; the kernel then reads those rows and applies kv_scale to
+  // the fp32 up-projection accumulators.
+  const void* rows_base = fp8 ? static_cast<const void*>(ws + fw.gath_off) : kv_cache;
+  const uint64_t rows_total = fp8 ? (uint64_t)std::max(fp.gather_blocks, 1) * kBlock : (uint64_t)num_blocks * kBlock;
   bool ok = true;
   p.q_bf16 = static_cast<const uint16_t*>(q);
-  if (!fp8) {
-    const uint64_t d[2] = {(uint64_t)kRowBf16, cache_rows};
+  {
+    const uint64_t d[2] = {(uint64_t)kRowBf16, rows_total};
     const uint64_t st[1] = {(uint64_t)kRowBytesBf16};
     const uint32_t b[2] = {64, 64};
-    ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
     p.tm_c = p.tm_kr;
-  } else {
-    const uint64_t d[2] = {(uint64_t)kRowBytesFp8, cache_rows};
-    const uint64_t st[1] = {(uint64_t)kRowBytesFp8};
-    const uint32_t bkr[2] = {128, 64}, bc[2] = {64, 64};
-    ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_cache, d, st, bkr, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok &= encode_map(&p.tm_c, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_cache, d, st, bc, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   {
     // kv_b_proj [512][H*256] seen as 64-column blocks: (col in block, latent row, block)
@@ -360,8 +376,7 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   p.num_blocks = num_blocks;
   p.num_heads = H;
   p.out_bf16 = out_dtype == MLA_OUT_BF16;
-  p.kv_fp8 = fp8;
-  p.kv_scale = kv_scale;
+  p.out_scale = fp8 ? kv_scale : 1.f;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   rope_fracs((double)rope_theta, p.rope_frac);
 
@@ -370,6 +385,32 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   if (st != MLA_OK) return st;
   st = cuda_status(cudaMemsetAsync(err, 0, 256, s));   // error word + role queue
   if (st != MLA_OK) return st;
+  if (fp8) {
+    GatherBlocksParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.cache = static_cast<const uint8_t*>(kv_cache);
+    gp.block_table = block_table;
+    gp.dst = reinterpret_cast<uint16_t*>(ws + fw.gath_off);
+    gp.err = err;
+    gp.fp8 = 1;
+    gp.scale = 1.f;
+    gp.num_blocks = num_blocks;
+    gp.max_blocks = max_blocks;
+    for (size_t g0 = 0; g0 < fp.gather.size(); g0 += kMaxGatherReqs) {
+      const size_t n = std::min(fp.gather.size() - g0, (size_t)kMaxGatherReqs);
+      int base = fp.gather[g0].base_block, end = base;
+      for (size_t i = 0; i < n; ++i) {
+        GatherReq g = fp.gather[g0 + i];
+        end = g.base_block + (g.seq_len + kBlock - 1) / kBlock;
+        g.base_block -= base;
+        gp.reqs[i] = g;
+      }
+      gp.dst = reinterpret_cast<uint16_t*>(ws + fw.gath_off) + (size_t)base * kBlock * kRowBf16;
+      gp.n_reqs = (int)n;
+      gp.total_blocks = end - base;
+      if ((st = cuda_status(launch_gather_blocks(gp, s))) != MLA_OK) return st;
+    }
+  }
 
   cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
   cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
@@ -464,7 +505,7 @@ size_t mla_prefill_workspace_size(int num_reqs, const int32_t* seq_lens, const i
   if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
     return 0;
   FusedPlan fp;
-  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, &fp);
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fp);   // room for gathered rows (FP8 caches)
   return fused_ws_layout(fp, num_heads).total;
 }
 
@@ -489,7 +530,7 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, i
   for (int r = 0; r < num_reqs; ++r)
     if ((seq_lens[r] + kBlock - 1) / kBlock > max_blocks_per_req) return MLA_ERR_INVALID_ARG;
   FusedPlan fplan;
-  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, &fplan);
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, kv_dtype == MLA_KV_FP8_E4M3, &fplan);
   const int ppl = fused_pieces_fitting(fplan, num_heads, workspace_bytes);
   if (workspace == nullptr || !aligned(workspace, 256) || ppl < 1) return MLA_ERR_WORKSPACE;
   const FusedWs fw = fused_ws_layout(fplan, num_heads, ppl);
@@ -516,7 +557,7 @@ int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos, const void* kv_
   if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
     return MLA_ERR_INVALID_ARG;
   FusedPlan fplan;
-  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, &fplan);
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, kv_dtype == MLA_KV_FP8_E4M3, &fplan);
   if (fused_pieces_fitting(fplan, num_heads, MLA_NOALLOC_SCRATCH_BYTES) < 1) return MLA_ERR_TOO_LARGE;
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);

@@ -55,9 +55,8 @@ constexpr uint32_t kConsumerEnd = kXchgBase + 6 * 128 * 4;         // max x2 buf
 // producer
 constexpr uint32_t kPStageBytes = 65536;            // C_A 16K | C_B 16K | W 32K
 constexpr uint32_t kPCA = 0, kPCB = 16384, kPW = 32768;
-constexpr uint32_t kPRawBase = 2 * kPStageBytes;    // e4m3 staging, 16 KB per stage
-constexpr uint32_t kPOutBase = kPRawBase + 2 * 16384; // bf16 output staging: 32 KB per warpgroup
-constexpr uint32_t kProducerEnd = kPOutBase + 2 * 32768;             // 229376
+constexpr uint32_t kPOutBase = 2 * kPStageBytes;    // bf16 output staging: 32 KB per warpgroup
+constexpr uint32_t kProducerEnd = kPOutBase + 2 * 32768;             // 196608
 constexpr uint32_t kBarBase = kConsumerEnd > kProducerEnd ? kConsumerEnd : kProducerEnd;
 constexpr uint32_t kSmemBytes = kBarBase + 256 + 1024;
 static_assert(kSmemBytes <= 232448, "more than 227 KB of shared memory per CTA");
@@ -66,7 +65,7 @@ static_assert(kSmemBytes <= 232448, "more than 227 KB of shared memory per CTA")
 constexpr uint32_t kBQReady = 0, kBKFull = 1, kBKEmpty = 4, kBVFull = 7, kBVEmpty = 9, kBSFull = 11, kBPFull = 13,
                    kBPvDone = 15 /* 2: PV of even / odd tiles */, kBKRel = 17, kBVRel = 20;
 // producer barriers
-constexpr uint32_t kBProdFull = 0, kBProdEmpty = 2, kBRawFull = 4, kBAccFull = 6, kBAccEmpty = 7;
+constexpr uint32_t kBProdFull = 0, kBProdEmpty = 2, kBAccFull = 4, kBAccEmpty = 5;
 constexpr uint32_t kNumBars = 24;
 
 // TMEM columns
@@ -169,7 +168,9 @@ __device__ __forceinline__ uint32_t* consumed_flag(const FusedParams& p, int job
 // Physical cache row of logical block `lb` of request `req`, or a negative row
 // (TMA fills zeros) when the block lies outside the table; a table entry
 // outside [0, num_blocks) for a block holding live tokens is an error.
-__device__ __forceinline__ int block_row(const FusedParams& p, int req, int lb, bool live) {
+__device__ __forceinline__ int block_row(const FusedParams& p, const Job& J, int lb, bool live) {
+  if (J.row_block0 >= 0) return (J.row_block0 + lb) * kBlock;   // rows gathered (and dequantised) up front
+  const int req = J.req;
   if (lb < 0 || lb >= p.max_blocks) return -kBlock;
   const int blk = __ldg(p.block_table + (int64_t)req * p.max_blocks + lb);
   if (blk < 0 || blk >= p.num_blocks) {
@@ -217,9 +218,9 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
         mbar_arrive_expect_tx(full, kKStageBytes);
         tma_load_3d(st, &p.tm_ring, 0, 0, zb, full);                      // K_nope, 32 KB
         const int kt0 = J.t0 + 128 * j;
-        tma_load_2d(st + 2 * kAtomQ, &p.tm_kr, kDc, block_row(p, J.req, kt0 >> 6, true), full);
+        tma_load_2d(st + 2 * kAtomQ, &p.tm_kr, kDc, block_row(p, J, kt0 >> 6, true), full);
         tma_load_2d(st + 2 * kAtomQ + kAtom64, &p.tm_kr, kDc,
-                    block_row(p, J.req, (kt0 >> 6) + 1, kt0 + 64 < J.k_end), full);
+                    block_row(p, J, (kt0 >> 6) + 1, kt0 + 64 < J.k_end), full);
         trace_stage(p, role, j, 0);
       } else {
         const uint32_t st = sbase + kVBase + s * kVStageBytes;
@@ -511,9 +512,9 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
   for (int pp = pi; pp < n_pass; pp += J.n_prod) ++my_passes;
   if (my_passes == 0) return;
 
-  if (warp == 8 || (warp == 10 && !p.kv_fp8)) {
-    // TMA issue, split over two warps (BF16): warp 8 loads kv_b_proj and the first
-    // 128 tokens' latent slices, warp 10 the second 128 tokens'.  FP8: warp 8 alone.
+  if (warp == 8 || warp == 10) {
+    // TMA issue, split over two warps: warp 8 loads kv_b_proj and the first 128
+    // tokens' latent slices, warp 10 the second 128 tokens'.
     if (lane == 0) {
       const bool primary = warp == 8;
       int g = 0;
@@ -524,20 +525,17 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
           const int lb = (J.t0 >> 6) + 4 * pass + i;
           const int tok = lb * 64;
           const bool live = tok + 63 >= J.k_begin && tok < J.k_end;
-          rows[i] = live ? block_row(p, J.req, lb, primary) : -kBlock;
+          rows[i] = live ? block_row(p, J, lb, primary) : -kBlock;
         }
         for (int k = 0; k < kDc / 64; ++k, ++g) {
           const int s = g & 1;
           if (g >= 2 && !wait_bar(p, bar_addr(sbase, kBProdEmpty + s), ((g >> 1) - 1) & 1)) { ctl->abort = 1; return; }
           const uint32_t st = sbase + s * kPStageBytes;
-          const uint32_t bar = p.kv_fp8 ? bar_addr(sbase, kBRawFull + s) : bar_addr(sbase, kBProdFull + s);
-          if (primary) mbar_arrive_expect_tx(bar, p.kv_fp8 ? (16384u + 32768u) : kPStageBytes);
-          for (int i = 0; i < 4; ++i) {
-            if (p.kv_fp8)
-              tma_load_2d(sbase + kPRawBase + s * 16384 + i * 4096, &p.tm_c, 64 * k, rows[i], bar);
-            else if ((i < 2) == primary)
+          const uint32_t bar = bar_addr(sbase, kBProdFull + s);
+          if (primary) mbar_arrive_expect_tx(bar, kPStageBytes);
+          for (int i = 0; i < 4; ++i)
+            if ((i < 2) == primary)
               tma_load_2d(st + (i < 2 ? kPCA : kPCB) + (i & 1) * kAtom64, &p.tm_c, 64 * k, rows[i], bar);
-          }
           if (primary) {
             tma_load_3d(st + kPW, &p.tm_w, 0, 64 * k, 2 * h, bar);                                   // K_nope cols
             tma_load_3d(st + kPW + 2 * kAtom64, &p.tm_w, 0, 64 * k, (H * kDnope + h * kDv) / 64, bar); // V cols
@@ -579,7 +577,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
     const int wg = warp >> 2;
     const int r = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const float oscale = p.kv_fp8 ? p.kv_scale : 1.f;
+    const float oscale = p.out_scale;
     const uint32_t stage_out = sbase + kPOutBase + wg * 32768;   // [128 rows x 128 cols] bf16, 2 SW128 blocks
     TraceAcc tr_c;
     for (int n = 0; n < my_passes; ++n) {
@@ -662,32 +660,6 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       if (ctl->abort) return;
     }
     if (tid == 0) trace_put(p, role, 3, tr_c.t);
-  } else if (warp >= 10) {
-    // e4m3 latent staging -> bf16 MMA operand (FP8 cache only), warps 10..11
-    if (!p.kv_fp8) return;
-    const int r = tid - 320;
-    int g = 0;
-    for (int n = 0; n < my_passes; ++n) {
-      for (int k = 0; k < kDc / 64; ++k, ++g) {
-        const int s = g & 1;
-        const bool okw = wait_bar_warp(p, bar_addr(sbase, kBRawFull + s), (g >> 1) & 1);
-        if (!okw) ctl->abort = 1;
-        const uint32_t raw = sbase + kPRawBase + s * 16384;
-        const uint32_t st = sbase + s * kPStageBytes;
-#pragma unroll 4
-        for (int idx = r; okw && idx < 256 * 8; idx += 64) {
-          const int row = idx >> 3, c = idx & 7;   // row 0..255 of the pass, chunk of 8 values
-          uint32_t lo, hi;
-          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(raw + row * 64 + c * 8));
-          sts128(st + (row < 128 ? kPCA : kPCB) + sw128_off(row & 127, c), e4m3x2_to_bf16x2(lo & 0xFFFFu),
-                 e4m3x2_to_bf16x2(lo >> 16), e4m3x2_to_bf16x2(hi & 0xFFFFu), e4m3x2_to_bf16x2(hi >> 16));
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(3, 64);
-        if (ctl->abort) return;                // together, after the barrier
-        if (r == 0) mbar_arrive(bar_addr(sbase, kBProdFull + s));
-      }
-    }
   }
 }
 
@@ -745,6 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(const __grid
     J.n_cons = P.n_cons;
     J.n_prod = P.n_prod;
     J.slot = P.slot;
+    J.row_block0 = P.row_block0;
     J.rope_offset = P.rope_offset;
     const int job = lo * p.num_heads + J.head;
     const int idx = local - J.head * per_job;

@@ -63,7 +63,64 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint8_t* __restrict__
   reinterpret_cast<uint4*>(dst + i * kRowBf16)[c] = v;
 }
 
+// Every block of several requests into one contiguous bf16 buffer: request i's
+// logical block lb becomes rows (base_i + lb) * 64 .. +63 of dst.
+__global__ void __launch_bounds__(256) gather_blocks_kernel(const __grid_constant__ GatherBlocksParams p) {
+  const int64_t total_chunks = (int64_t)p.total_blocks * kBlock * kChunksPerRow;
+  for (int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gid < total_chunks;
+       gid += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t g = gid / kChunksPerRow;              // destination row
+    const int c = (int)(gid - g * kChunksPerRow);
+    const int gb = (int)(g >> 6);                       // destination block
+    int lo = 0, hi = p.n_reqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.reqs[mid].base_block <= gb) lo = mid; else hi = mid - 1;
+    }
+    const GatherReq rq = p.reqs[lo];
+    const int lb = gb - rq.base_block;
+    const int slot = (int)(g & 63);
+    const int blk = (lb < p.max_blocks) ? __ldg(p.block_table + (int64_t)rq.req * p.max_blocks + lb) : -1;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (blk < 0 || blk >= p.num_blocks) {
+      if (c == 0 && slot == 0 && lb * kBlock < rq.seq_len) atomicOr(p.err, kErrBadBlock);
+    } else {
+      const int64_t row = (int64_t)blk * kBlock + slot;
+      if (!p.fp8) {
+        v = __ldg(reinterpret_cast<const uint4*>(p.cache + row * kRowBytesBf16) + c);
+      } else {
+        const uint8_t* rp = p.cache + row * kRowBytesFp8;
+        if (c < 64) {
+          const uint2 b = __ldg(reinterpret_cast<const uint2*>(rp) + c);
+          uint32_t w[2] = {b.x, b.y}, o[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t src = w[k >> 1] >> ((k & 1) * 16);
+            o[k] = pack_bf16(e4m3_value(src & 0xFFu) * p.scale, e4m3_value((src >> 8) & 0xFFu) * p.scale);
+          }
+          v = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+          v = __ldg(reinterpret_cast<const uint4*>(rp + kDc) + (c - 64));
+        }
+      }
+    }
+    reinterpret_cast<uint4*>(p.dst + g * kRowBf16)[c] = v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_blocks(const GatherBlocksParams& p, cudaStream_t s) {
+  if (p.total_blocks == 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t threads = (int64_t)p.total_blocks * kBlock * kChunksPerRow;
+  const int64_t blocks = (threads + 255) / 256;
+  const int grid = (int)(blocks < (int64_t)sms * 8 ? blocks : (int64_t)sms * 8);
+  gather_blocks_kernel<<<grid, 256, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather(const uint8_t* cache, int fp8, float scale, int num_blocks, const int32_t* table_row,
                           int max_blocks, int start, int len, uint16_t* dst, uint32_t* err, cudaStream_t s) {

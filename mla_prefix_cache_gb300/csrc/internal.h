@@ -77,18 +77,20 @@ struct Piece {
   int32_t role_begin;  // first role of this piece in the launch's role queue
   int32_t n_cons;      // consumer roles per head (128 queries each)
   int32_t n_prod;      // producer roles per head
+  int32_t row_block0;  // >= 0: the request's rows were gathered contiguously from this block
+  int32_t pad;
   int64_t rope_offset;
 };
 
 // Device-side view of one job.
 struct Job {
-  int32_t req, head, q_begin, q_count, q_tok0, k_begin, k_end, t0, n_tiles, n_cons, n_prod, slot;
+  int32_t req, head, q_begin, q_count, q_tok0, k_begin, k_end, t0, n_tiles, n_cons, n_prod, slot, row_block0;
   int64_t rope_offset;
 };
 
 struct FusedParams {
-  CUtensorMap tm_kr;     // cache rows, box = 64 rows x 128 B at the k_rope columns
-  CUtensorMap tm_c;      // cache rows, box = 64 rows x one 64-wide latent slice
+  CUtensorMap tm_kr;     // bf16 latent rows [rows][576], box 64 x 64 (k_rope at column 512)
+  CUtensorMap tm_c;      // same rows, box 64 x 64 (one latent slice)
   CUtensorMap tm_w;      // bf16 kv_b_proj as [H*4 blocks][512 rows][64 cols], box 64 x 64 x 2
   CUtensorMap tm_ring;   // bf16 ring as [jobs*ring*4 blocks][128 rows][64 cols], box 64 x 128 x 2
   const uint16_t* q_bf16;  // q [T_q][H][192]
@@ -107,8 +109,7 @@ struct FusedParams {
   int num_blocks;
   int num_heads;
   int out_bf16;
-  int kv_fp8;
-  float kv_scale;
+  float out_scale;      // applied to the up-projection accumulators (FP8 dequant scale, else 1)
   float scale_log2;
   int n_pieces;
   int n_roles;
@@ -136,6 +137,28 @@ cudaError_t launch_rope(const uint16_t* x, const int32_t* pos, int64_t offset, c
 cudaError_t launch_gather(const uint8_t* cache, int fp8, float scale, int num_blocks,
                           const int32_t* table_row, int max_blocks, int start, int len,
                           uint16_t* dst, uint32_t* err, cudaStream_t s);
+
+struct GatherReq {
+  int32_t req;
+  int32_t base_block;  // first destination block
+  int32_t seq_len;
+  int32_t pad;
+};
+constexpr int kMaxGatherReqs = 1024;
+struct GatherBlocksParams {
+  const uint8_t* cache;
+  const int32_t* block_table;
+  uint16_t* dst;        // bf16 [total_blocks * 64][576]
+  uint32_t* err;
+  int fp8;
+  float scale;
+  int num_blocks;
+  int max_blocks;
+  int n_reqs;
+  int total_blocks;
+  GatherReq reqs[kMaxGatherReqs];
+};
+cudaError_t launch_gather_blocks(const GatherBlocksParams& p, cudaStream_t s);
 
 void count_launch(int n = 1);
 

@@ -50,12 +50,16 @@ def _up(x, a=256):
     return (x + a - 1) // a * a
 
 
-def fused_layout(pieces, heads, slots, total_q, ring_depth=32):
+def fused_layout(pieces, heads, slots, total_q, seq_lens, ring_depth=32):
     """Workspace of the fused path: 256 B header, per-job ring flags, per-job
-    K/V rings of `ring_depth` 128-token bf16 tiles, then partial states."""
+    K/V rings of `ring_depth` 128-token bf16 tiles, room for the dequantised
+    rows of an FP8 cache (1152 B per token, whole 64-token blocks), then
+    partial states."""
     jobs = pieces * heads
     ring_off = _up(256 + jobs * 2 * ring_depth * 4)
-    lse_off = _up(ring_off + jobs * ring_depth * 128 * 256 * 2)
+    gath_off = _up(ring_off + jobs * ring_depth * 128 * 256 * 2)
+    gath = sum((s + 63) // 64 for s in seq_lens) * 64 * 1152
+    lse_off = _up(gath_off + gath)
     rows = slots * total_q * heads
     return _up(lse_off + rows * 4) + rows * 128 * 4
 
@@ -64,12 +68,12 @@ def test_workspace_size_follows_plan(lib):
     # 1 request, C=256 in chunks of 128 plus the extend: the three ranges share
     # offset 0 and are contiguous, so they fold into one piece (no partial slots).
     n = _ws(lib, [320], [0, 64], 8, chunk=128)
-    assert n == fused_layout(1, 8, 0, 64)
+    assert n == fused_layout(1, 8, 0, 64, [320])
     # segments: 4 documents of 64 (4 offsets) + extend = 5 pieces, 5 partial slots
     segs = [[0, 64 * d, 64, 64 * d] for d in range(4)]
-    assert _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64) == fused_layout(5, 1, 5, 2)
+    assert _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64) == fused_layout(5, 1, 5, 2, [258])
     # a long context is cut into pieces of at most max(chunk, 16384) keys
-    assert _ws(lib, [40000 + 100], [0, 100], 2, chunk=4096) == fused_layout(3, 2, 3, 100)
+    assert _ws(lib, [40000 + 100], [0, 100], 2, chunk=4096) == fused_layout(3, 2, 3, 100, [40100])
 
 
 @pytest.mark.parametrize("bad", [
