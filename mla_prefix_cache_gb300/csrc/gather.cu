@@ -8,8 +8,12 @@
 // BF16 rows are copied bit-exactly.  FP8 rows (512 E4M3FN bytes + 64 bf16) are
 // dequantised to bf16(e4m3 * scale), rounded to nearest even.
 //
-// One thread per 16-byte output chunk (72 per row): consecutive threads write
-// consecutive chunks, so each warp stores 512 contiguous bytes.
+// Work is cut into tiles of 64 destination rows (72 KB of bf16 output).  One
+// 256-thread CTA moves a tile: thread i owns chunks i, i+256, ..., i+17*256 of
+// the tile's 4608 16-byte output chunks, issues all 18 loads before any store
+// (about 73 KB in flight per CTA, which is what keeps HBM busy), and
+// consecutive threads touch consecutive chunks, so every warp access is 512
+// contiguous bytes.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -17,61 +21,73 @@ namespace mla {
 namespace {
 
 constexpr int kChunksPerRow = kRowBytesBf16 / 16;  // 72
+constexpr int kGatherThreads = 256;
+constexpr int kChunksPerThread = kBlock * kChunksPerRow / kGatherThreads;  // 18
+static_assert(kChunksPerThread * kGatherThreads == kBlock * kChunksPerRow, "tile split");
 
-__device__ __forceinline__ float e4m3_value(uint32_t c) {
-  const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
-  float v;
-  if (e == 15u && m == 7u) v = __int_as_float(0x7FC00000);
-  else if (e == 0u) v = (float)m * 0.001953125f;  // m * 2^-9
-  else v = __uint_as_float(((e + 120u) << 23) | (m << 20));
-  return (c & 0x80u) ? -v : v;
+// Chunk c (0..71) of a cache row: BF16 rows are 72 chunks of 16 bytes; an FP8
+// row's chunk c < 64 is 8 e4m3 bytes (expanded to 16 bytes of bf16 later) and
+// chunk c >= 64 is 16 bytes of its bf16 k_rope.
+__device__ __forceinline__ uint4 load_chunk(const uint8_t* row, int c, int fp8) {
+  if (!fp8) return __ldg(reinterpret_cast<const uint4*>(row) + c);
+  if (c < 64) {
+    const uint2 b = __ldg(reinterpret_cast<const uint2*>(row) + c);
+    return make_uint4(b.x, b.y, 0u, 0u);
+  }
+  return __ldg(reinterpret_cast<const uint4*>(row + kDc) + (c - 64));
 }
 
-__global__ void __launch_bounds__(256) gather_kernel(const uint8_t* __restrict__ cache, int fp8, float scale,
-                                                     int num_blocks, const int32_t* __restrict__ table,
-                                                     int start, int len, uint16_t* __restrict__ dst,
-                                                     uint32_t* err) {
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t i = gid / kChunksPerRow;
-  const int c = (int)(gid - i * kChunksPerRow);
-  if (i >= len) return;
-  const int t = start + (int)i;
-  const int blk = __ldg(table + (t >> 6));
-  uint4 v = make_uint4(0, 0, 0, 0);
-  if (blk < 0 || blk >= num_blocks) {
-    if (err != nullptr && c == 0) atomicOr(err, kErrBadBlock);
-  } else {
-    const int64_t row = (int64_t)blk * kBlock + (t & 63);
-    if (!fp8) {
-      v = __ldg(reinterpret_cast<const uint4*>(cache + row * kRowBytesBf16) + c);
-    } else {
-      const uint8_t* rp = cache + row * kRowBytesFp8;
-      if (c < 64) {  // 8 latent values from 8 bytes
-        const uint2 b = __ldg(reinterpret_cast<const uint2*>(rp) + c);
-        uint32_t w[2] = {b.x, b.y}, o[4];
+__device__ __forceinline__ uint4 finish_chunk(uint4 v, int c, int fp8, float scale) {
+  if (!fp8 || c >= 64) return v;
+  return make_uint4(e4m3x2_scaled_bf16x2(v.x, scale), e4m3x2_scaled_bf16x2(v.x >> 16, scale),
+                    e4m3x2_scaled_bf16x2(v.y, scale), e4m3x2_scaled_bf16x2(v.y >> 16, scale));
+}
+
+// Tokens [start, start+len) of one request.  The tile's rows may straddle two
+// cache blocks, so each chunk looks up its own block (the table row is cached).
+__global__ void __launch_bounds__(kGatherThreads, 2) gather_kernel(const uint8_t* __restrict__ cache, int fp8,
+                                                                   float scale, int num_blocks,
+                                                                   const int32_t* __restrict__ table, int start,
+                                                                   int len, uint16_t* __restrict__ dst,
+                                                                   uint32_t* err) {
+  const int64_t row_bytes = fp8 ? kRowBytesFp8 : kRowBytesBf16;
+  const int tiles = (len + kBlock - 1) / kBlock;
+  for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    uint4 v[kChunksPerThread];
+    bool ok[kChunksPerThread];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t src = w[k >> 1] >> ((k & 1) * 16);
-          o[k] = pack_bf16(e4m3_value(src & 0xFFu) * scale, e4m3_value((src >> 8) & 0xFFu) * scale);
-        }
-        v = make_uint4(o[0], o[1], o[2], o[3]);
-      } else {       // k_rope bf16, copied
-        v = __ldg(reinterpret_cast<const uint4*>(rp + kDc) + (c - 64));
+    for (int j = 0; j < kChunksPerThread; ++j) {
+      const int k = threadIdx.x + j * kGatherThreads;
+      const int r = k / kChunksPerRow, c = k - r * kChunksPerRow;
+      const int g = tile * kBlock + r;
+      v[j] = make_uint4(0u, 0u, 0u, 0u);
+      ok[j] = false;
+      if (g < len) {
+        const int t = start + g;
+        const int blk = __ldg(table + (t >> 6));
+        ok[j] = (blk >= 0 && blk < num_blocks);
+        if (ok[j]) v[j] = load_chunk(cache + ((int64_t)blk * kBlock + (t & 63)) * row_bytes, c, fp8);
+        else if (c == 0 && err != nullptr) atomicOr(err, kErrBadBlock);
       }
     }
+#pragma unroll
+    for (int j = 0; j < kChunksPerThread; ++j) {
+      const int k = threadIdx.x + j * kGatherThreads;
+      const int r = k / kChunksPerRow, c = k - r * kChunksPerRow;
+      const int g = tile * kBlock + r;
+      if (g < len)
+        reinterpret_cast<uint4*>(dst + (int64_t)g * kRowBf16)[c] = ok[j] ? finish_chunk(v[j], c, fp8, scale) : v[j];
+    }
   }
-  reinterpret_cast<uint4*>(dst + i * kRowBf16)[c] = v;
 }
 
 // Every block of several requests into one contiguous bf16 buffer: request i's
-// logical block lb becomes rows (base_i + lb) * 64 .. +63 of dst.
-__global__ void __launch_bounds__(256) gather_blocks_kernel(const __grid_constant__ GatherBlocksParams p) {
-  const int64_t total_chunks = (int64_t)p.total_blocks * kBlock * kChunksPerRow;
-  for (int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gid < total_chunks;
-       gid += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t g = gid / kChunksPerRow;              // destination row
-    const int c = (int)(gid - g * kChunksPerRow);
-    const int gb = (int)(g >> 6);                       // destination block
+// logical block lb becomes rows (base_i + lb) * 64 .. +63 of dst.  A tile is
+// one destination block, so it reads one whole cache block (72 KB of BF16 or
+// 40 KB of FP8, contiguous in the pool) and the lookup is uniform over the CTA.
+__global__ void __launch_bounds__(kGatherThreads, 2) gather_blocks_kernel(const __grid_constant__ GatherBlocksParams p) {
+  const int64_t row_bytes = p.fp8 ? kRowBytesFp8 : kRowBytesBf16;
+  for (int gb = blockIdx.x; gb < p.total_blocks; gb += gridDim.x) {
     int lo = 0, hi = p.n_reqs - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -79,45 +95,39 @@ __global__ void __launch_bounds__(256) gather_blocks_kernel(const __grid_constan
     }
     const GatherReq rq = p.reqs[lo];
     const int lb = gb - rq.base_block;
-    const int slot = (int)(g & 63);
     const int blk = (lb < p.max_blocks) ? __ldg(p.block_table + (int64_t)rq.req * p.max_blocks + lb) : -1;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (blk < 0 || blk >= p.num_blocks) {
-      if (c == 0 && slot == 0 && lb * kBlock < rq.seq_len) atomicOr(p.err, kErrBadBlock);
-    } else {
-      const int64_t row = (int64_t)blk * kBlock + slot;
-      if (!p.fp8) {
-        v = __ldg(reinterpret_cast<const uint4*>(p.cache + row * kRowBytesBf16) + c);
-      } else {
-        const uint8_t* rp = p.cache + row * kRowBytesFp8;
-        if (c < 64) {
-          const uint2 b = __ldg(reinterpret_cast<const uint2*>(rp) + c);
-          uint32_t w[2] = {b.x, b.y}, o[4];
+    const bool ok = (blk >= 0 && blk < p.num_blocks);
+    if (!ok && threadIdx.x == 0 && lb * kBlock < rq.seq_len) atomicOr(p.err, kErrBadBlock);
+    const uint8_t* src = p.cache + (int64_t)(ok ? blk : 0) * kBlock * row_bytes;
+    uint16_t* out = p.dst + (int64_t)gb * kBlock * kRowBf16;
+    uint4 v[kChunksPerThread];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t src = w[k >> 1] >> ((k & 1) * 16);
-            o[k] = pack_bf16(e4m3_value(src & 0xFFu) * p.scale, e4m3_value((src >> 8) & 0xFFu) * p.scale);
-          }
-          v = make_uint4(o[0], o[1], o[2], o[3]);
-        } else {
-          v = __ldg(reinterpret_cast<const uint4*>(rp + kDc) + (c - 64));
-        }
-      }
+    for (int j = 0; j < kChunksPerThread; ++j) {
+      const int k = threadIdx.x + j * kGatherThreads;
+      const int r = k / kChunksPerRow, c = k - r * kChunksPerRow;
+      v[j] = ok ? load_chunk(src + r * row_bytes, c, p.fp8) : make_uint4(0u, 0u, 0u, 0u);
     }
-    reinterpret_cast<uint4*>(p.dst + g * kRowBf16)[c] = v;
+#pragma unroll
+    for (int j = 0; j < kChunksPerThread; ++j) {
+      const int k = threadIdx.x + j * kGatherThreads;
+      const int c = k % kChunksPerRow;
+      reinterpret_cast<uint4*>(out)[k] = ok ? finish_chunk(v[j], c, p.fp8, p.scale) : v[j];
+    }
   }
+}
+
+int gather_grid(int64_t tiles) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t cap = (int64_t)sms * 2;  // two resident CTAs per SM, each looping over tiles
+  return (int)(tiles < cap ? tiles : cap);
 }
 
 }  // namespace
 
 cudaError_t launch_gather_blocks(const GatherBlocksParams& p, cudaStream_t s) {
   if (p.total_blocks == 0) return cudaSuccess;
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t threads = (int64_t)p.total_blocks * kBlock * kChunksPerRow;
-  const int64_t blocks = (threads + 255) / 256;
-  const int grid = (int)(blocks < (int64_t)sms * 8 ? blocks : (int64_t)sms * 8);
-  gather_blocks_kernel<<<grid, 256, 0, s>>>(p);
+  gather_blocks_kernel<<<gather_grid(p.total_blocks), kGatherThreads, 0, s>>>(p);
   count_launch();
   return cudaGetLastError();
 }
@@ -126,9 +136,8 @@ cudaError_t launch_gather(const uint8_t* cache, int fp8, float scale, int num_bl
                           int max_blocks, int start, int len, uint16_t* dst, uint32_t* err, cudaStream_t s) {
   (void)max_blocks;
   if (len == 0) return cudaSuccess;
-  const int64_t threads = (int64_t)len * kChunksPerRow;
-  const int blocks = (int)((threads + 255) / 256);
-  gather_kernel<<<blocks, 256, 0, s>>>(cache, fp8, scale, num_blocks, table_row, start, len, dst, err);
+  gather_kernel<<<gather_grid((len + kBlock - 1) / kBlock), kGatherThreads, 0, s>>>(cache, fp8, scale, num_blocks,
+                                                                                      table_row, start, len, dst, err);
   count_launch();
   return cudaGetLastError();
 }

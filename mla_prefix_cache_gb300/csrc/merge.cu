@@ -36,16 +36,21 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_slots_kernel(const 
     const int ns = p.ranges[ri].nslots;
 
     float m = -INFINITY;
+#pragma unroll 4
     for (int s = 0; s < ns; ++s) m = fmaxf(m, __ldg(p.part_lse + ((int64_t)s * p.slot_stride_rows + row) * H + h));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
     if (m != -INFINITY) {
+      // Predicated rather than branched, so the unrolled loads of several
+      // slots are in flight together; an empty state (lse = -inf) adds 0.
+#pragma unroll 4
       for (int s = 0; s < ns; ++s) {
         const int64_t g = ((int64_t)s * p.slot_stride_rows + row) * H + h;
         const float l = __ldg(p.part_lse + g);
-        if (l == -INFINITY) continue;
-        const float w = __expf(l - m);
-        const float4 o = __ldg(reinterpret_cast<const float4*>(p.part_out + g * kDv) + lane);
+        const bool live = (l != -INFINITY);
+        const float w = live ? __expf(l - m) : 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) o = __ldg(reinterpret_cast<const float4*>(p.part_out + g * kDv) + lane);
         acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
         wsum += w;
       }
@@ -63,9 +68,47 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_slots_kernel(const 
   }
 }
 
-// Two states, arbitrary d_v (multiple of 4): warp per row, lanes stride over
-// float4 columns.  out/lse may alias either input (each lane reads its own
-// elements before writing them; lse is read by every lane before lane 0 writes).
+// Two states, d_v = 128: a warp merges 4 rows at a time, an 8-lane group per
+// row, each lane owning float4 columns l, l+8, l+16, l+24 of its row, so a
+// lane has 8 independent 16-byte loads in flight.  out/lse may alias either
+// input: each lane writes only the columns it read, and the group leader
+// writes lse after the whole warp has read it.
+__global__ void __launch_bounds__(256) merge2_d128_kernel(const float* oa, const float* la, const float* ob,
+                                                          const float* lb, float* o, float* l, int64_t rows) {
+  const int lane = threadIdx.x & 31, g = lane >> 3, q = lane & 7;
+  const int64_t w0 = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  for (int64_t base = w0 * 4; base < rows; base += (int64_t)gridDim.x * 8 * 4) {
+    const int64_t row = base + g;
+    const bool live = row < rows;
+    float a = -INFINITY, b = -INFINITY;
+    float4 x[4], y[4];
+    if (live) {
+      a = la[row];
+      b = lb[row];
+      const float4* pa = reinterpret_cast<const float4*>(oa + row * kDv);
+      const float4* pb = reinterpret_cast<const float4*>(ob + row * kDv);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) { x[k] = pa[q + 8 * k]; y[k] = pb[q + 8 * k]; }
+    }
+    __syncwarp();
+    if (live) {
+      const float m = fmaxf(a, b);
+      const bool empty = (m == -INFINITY);
+      const float wa = (a == -INFINITY) ? 0.f : __expf(a - m);
+      const float wb = (b == -INFINITY) ? 0.f : __expf(b - m);
+      const float inv = empty ? 0.f : 1.f / (wa + wb);
+      float4* po = reinterpret_cast<float4*>(o + row * kDv);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        po[q + 8 * k] = make_float4((wa * x[k].x + wb * y[k].x) * inv, (wa * x[k].y + wb * y[k].y) * inv,
+                                    (wa * x[k].z + wb * y[k].z) * inv, (wa * x[k].w + wb * y[k].w) * inv);
+      if (q == 0) l[row] = empty ? -INFINITY : m + logf(wa + wb);
+    }
+  }
+}
+
+// Two states, any d_v (multiple of 4): warp per row, lanes stride over float4
+// columns; same aliasing rule as above.
 __global__ void __launch_bounds__(256) merge2_kernel(const float* oa, const float* la,
                                                      const float* ob, const float* lb,
                                                      float* o, float* l, int64_t rows, int d_v) {
@@ -113,7 +156,10 @@ cudaError_t launch_merge_slots(const MergeParams& p, cudaStream_t s) {
 cudaError_t launch_merge2(const float* oa, const float* la, const float* ob, const float* lb, float* o,
                           float* l, int64_t rows, int d_v, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  merge2_kernel<<<grid_for(rows, 8), 256, 0, s>>>(oa, la, ob, lb, o, l, rows, d_v);
+  if (d_v == kDv)
+    merge2_d128_kernel<<<grid_for((rows + 3) / 4, 8), 256, 0, s>>>(oa, la, ob, lb, o, l, rows);
+  else
+    merge2_kernel<<<grid_for(rows, 8), 256, 0, s>>>(oa, la, ob, lb, o, l, rows, d_v);
   count_launch();
   return cudaGetLastError();
 }

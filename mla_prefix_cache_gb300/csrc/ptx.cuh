@@ -310,16 +310,21 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// Two OCP E4M3FN codes (low 16 bits of `pair`) -> two bf16 (exact): the
-// hardware converts to f16, and an f16 holding an e4m3 value has its 7 low
-// mantissa bits zero, so re-biasing the exponent by 127-15 is exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t pair) {
-  uint32_t h;
-  asm("{\n\t.reg .b16 in;\n\tcvt.u16.u32 in, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, in;\n\t}" : "=r"(h) : "r"(pair));
-  const uint32_t mlo = h & 0x7FFFu, mhi = (h >> 16) & 0x7FFFu;
-  const uint32_t lo = (mlo > 0x7C00u) ? 0x7FC0u : (mlo ? (mlo >> 3) + 0x3800u : 0u);
-  const uint32_t hi = (mhi > 0x7C00u) ? 0x7FC0u : (mhi ? (mhi >> 3) + 0x3800u : 0u);
-  return (h & 0x80008000u) | lo | (hi << 16);
+// Two OCP E4M3FN codes (low 16 bits of `pair`, the higher byte giving the
+// higher half of the result) -> bf16x2 of (code value * scale): the hardware
+// converts e4m3 to f16 exactly (every e4m3 value, subnormals included, is an
+// f16 normal or zero), f16 -> f32 is exact, and the product is rounded to
+// bf16 to nearest even once.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t pair, float scale) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 in, l, h;\n\t.reg .b32 hx;\n\t"
+      "cvt.u16.u32 in, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 hx, in;\n\t"
+      "mov.b32 {l, h}, hx;\n\t"
+      "cvt.f32.f16 %0, l;\n\t"
+      "cvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(pair));
+  return pack_bf16(lo * scale, hi * scale);
 }
 
 }  // namespace mla

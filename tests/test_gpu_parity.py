@@ -102,6 +102,16 @@ def test_gather_bf16_bit_exact(api):
     assert np.array_equal(got, exp)
 
 
+def test_gather_many_tiles_bit_exact(api):
+    # 20000 rows from an unaligned start: 313 tiles of 64 rows, more than the
+    # two resident CTAs per SM take in one round, and a ragged last tile
+    wl = W.make_workload("gm", 1, [20100], [1], seed=26)
+    dw = api.DeviceWorkload(wl)
+    got = api.gather_latent(dw.kv_cache, dw.block_table[0], 37, 20000).cpu().view(torch.int16).numpy().view(np.uint16)
+    t = np.arange(37, 20037)
+    assert np.array_equal(got, wl.kv_cache[wl.block_table[0][t // 64], t % 64])
+
+
 def test_gather_fp8_dequant_bit_exact(api):
     wl = W.make_workload("g8", 1, [130], [70], kv_dtype="fp8_e4m3", seed=22)
     dw = api.DeviceWorkload(wl)
@@ -129,10 +139,10 @@ def test_gather_bad_block_reports_error(api):
 
 # ---------------------------------------------------------------- merge
 
-def test_merge_states_matches_oracle(api):
+@pytest.mark.parametrize("rows,d_v", [(1000, 128), (1001, 128), (3, 128), (333, 64)])
+def test_merge_states_matches_oracle(api, rows, d_v):
     rng = np.random.default_rng(24)
-    rows = 1000
-    oa, ob = rng.standard_normal((rows, 128)).astype(np.float32), rng.standard_normal((rows, 128)).astype(np.float32)
+    oa, ob = rng.standard_normal((rows, d_v)).astype(np.float32), rng.standard_normal((rows, d_v)).astype(np.float32)
     la, lb = (rng.standard_normal(rows) * 20).astype(np.float32), (rng.standard_normal(rows) * 20).astype(np.float32)
     la[::7] = -np.inf
     lb[::11] = -np.inf
@@ -150,14 +160,14 @@ def test_merge_states_matches_oracle(api):
 
 # ---------------------------------------------------------------- rope
 
-def test_rope_relocate_matches_oracle(api):
+@pytest.mark.parametrize("T,H,inplace", [(300, 3, False), (77, 5, True), (64, 128, True)])
+def test_rope_relocate_matches_oracle(api, T, H, inplace):
     rng = np.random.default_rng(25)
-    T, H = 300, 3
     x = W.f32_to_bf16_bits(rng.standard_normal((T, H, 192), dtype=np.float32))
     pos = (rng.integers(0, 300000, size=T)).astype(np.int32)
     off = 16384 * 7
     xt = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
-    y = api.rope_relocate(xt, torch.from_numpy(pos).cuda(), off, 10000.0)
+    y = api.rope_relocate(xt, torch.from_numpy(pos).cuda(), off, 10000.0, y=xt if inplace else None)
     y = y.cpu().view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(y[..., :128], x[..., :128])
     ref = O.rope_rotate(O.bf16_to_float(x[..., 128:], np.float64), (pos.astype(np.int64) - off)[:, None], 1e4,
