@@ -129,9 +129,13 @@ def run_reference(args):
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons every 20 ms; `stop(t0, t1)` keeps
+    the samples whose own timestamps fall inside the timed region [t0, t1]
+    (wall clock), widened by one sampling period."""
+    FIELDS = ("timestamp,index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.02
 
     def __init__(self, uuid=None):
         self.uuid = uuid
@@ -142,37 +146,49 @@ class ClockSampler:
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                                          "-lms", str(int(self.PERIOD_S * 1000))], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        time.sleep(0.3)   # let the sampler come up before the timed region starts
 
-    def stop(self):
+    def stop(self, t0, t1):
         if self.proc is None:
             return None
+        time.sleep(2 * self.PERIOD_S)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
+        import datetime
+        lo = datetime.datetime.fromtimestamp(t0 - self.PERIOD_S)
+        hi = datetime.datetime.fromtimestamp(t1 + self.PERIOD_S)
         rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 10:
+                if len(parts) < 11:
                     continue
-                if self.uuid and parts[1] != self.uuid:
+                if self.uuid and parts[2] != self.uuid:
                     continue
-                rows.append(parts)
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                except ValueError:
+                    continue
+                if lo <= ts <= hi:
+                    rows.append(parts)
         os.unlink(self.path)
         if not rows:
-            return None
-        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        mx = [float(r[4]) for r in rows if r[4].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[7 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "period_ms": int(self.PERIOD_S * 1000)}
 
 
 # ---------------------------------------------------------------- our arm
@@ -300,10 +316,11 @@ def run_ours(args):
     clocks = ClockSampler(getattr(torch.cuda.get_device_properties(dev), "uuid", None))
     uuid = clocks.uuid
     clocks.uuid = ("GPU-" + str(uuid)) if uuid is not None and not str(uuid).startswith("GPU-") else uuid
+    clocks.start()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
+    t_wall0 = time.time()
     n0 = api.launch_count()
     for k in range(K):
         flush.zero_()                       # L2 flush, outside the step events
@@ -312,11 +329,12 @@ def run_ours(args):
         step()
         ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
     launches = api.launch_count() - n0
     api.set_kernel_events(None, None)
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(t_wall0, t_wall1)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     if api.device_error(ws) != 0:

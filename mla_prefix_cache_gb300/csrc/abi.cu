@@ -382,6 +382,9 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
 
   int grid = 0;
   int st = cuda_status(fused_grid_size(&grid));
+  // MLA_FUSED_GRID caps the persistent grid (a tuning and measurement knob; the
+  // role queue is correct for any grid with more CTAs than producers per job).
+  if (st == MLA_OK) grid = std::min(grid, std::max(8, env_int("MLA_FUSED_GRID", grid)));
   if (st != MLA_OK) return st;
   st = cuda_status(cudaMemsetAsync(err, 0, 256, s));   // error word + role queue
   if (st != MLA_OK) return st;

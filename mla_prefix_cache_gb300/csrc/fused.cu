@@ -201,15 +201,18 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
     for (int j = 0; j < n_tiles; ++j) {
       const int ns = is_k ? kKStages : kVStages;
       const int s = j % ns;
+      // The tile must be published.  Checked before the stage wait: producers
+      // run ahead, so the flag is normally set already, and the round trip to
+      // L2 overlaps the wait for the stage instead of following it.
+      const uint64_t w0 = tr.begin(p);
+      if (!wait_flag_geq(p, ready_flag(p, job, j % kRing), (uint32_t)j + 1)) { ctl->abort = 1; return; }
+      tr.end(p, w0);
       // stage reusable: its MMA finished reading it, and the release warp has seen its previous load land
       if (j >= ns && !(wait_bar(p, bar_addr(sbase, (is_k ? kBKEmpty : kBVEmpty) + s), ((j / ns) - 1) & 1) &&
                        wait_bar(p, bar_addr(sbase, (is_k ? kBKRel : kBVRel) + s), ((j / ns) - 1) & 1))) {
         ctl->abort = 1;
         return;
       }
-      const uint64_t w0 = tr.begin(p);
-      if (!wait_flag_geq(p, ready_flag(p, job, j % kRing), (uint32_t)j + 1)) { ctl->abort = 1; return; }
-      tr.end(p, w0);
       fence_proxy_async_global();
       const int zb = (job * (int)kRing + j % kRing) * 4;   // first ring block of the tile
       if (is_k) {
@@ -385,7 +388,8 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(v[i]);
 #pragma unroll
-        for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(v[c]));
+        for (int c = 8; c < 64; c += 2)
+          m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
@@ -414,17 +418,27 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
         m_used = m_tile;
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
+      // exponent arguments and row sums on packed pairs: s * scale - m, then 2^x
+      // P is packed in place over the scores (pair c lands in v[c], whose score
+      // was consumed at pair c/2) and stored in two 16-column halves, so the
+      // first half's store overlaps the second half's exponentials.
+      const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-mref, -mref);
+      uint64_t s4[4] = {0ull, 0ull, 0ull, 0ull};
+      const uint32_t pcol = tmem + lane_off + kTmS + 128 * b + 32 * w;   // P over S's first 64 columns
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float a = ex2(fmaf(__uint_as_float(v[2 * c]), sl2, -mref));
-        const float bb = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sl2, -mref));
-        s8[c & 7] += a + bb;
-        pk[c] = pack_bf16(a, bb);
+        float x0, x1;
+        f2unpack(ffma2(f2pack(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])), sc2, nm2), x0, x1);
+        const float a = ex2(x0), bb = ex2(x1);
+        s4[c & 3] = fadd2(s4[c & 3], f2pack(a, bb));
+        v[c] = pack_bf16(a, bb);
+        if (c == 15 && ok) tmem_st16(pcol, v);
       }
-      if (ok) tmem_st32(tmem + lane_off + kTmS + 128 * b + 32 * w, pk);   // P over S's first 64 columns
-      l_part = l_part * alpha + (((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
+      if (ok) tmem_st16(pcol + 16, v + 16);
+      float s8[8];
+      f2unpack(fadd2(s4[0], s4[1]), s8[0], s8[1]);
+      f2unpack(fadd2(s4[2], s4[3]), s8[2], s8[3]);
+      l_part = l_part * alpha + ((s8[0] + s8[2]) + (s8[1] + s8[3]));
       if (j >= 1 && ok && __any_sync(0xffffffffu, rescale)) {
         // O holds PV of tiles < j: PV(j-1) must be done before O is rescaled.  PV(j-2)
         // finished before S(j) did, so this barrier is at most one phase behind.
