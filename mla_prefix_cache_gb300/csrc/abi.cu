@@ -136,7 +136,7 @@ static int env_int(const char* name, int dflt) {
 }
 
 struct FusedPlan {
-  std::vector<Piece> pieces;      // LPT order, role_begin unset
+  std::vector<Piece> pieces;      // LPT order, group_begin unset
   std::vector<RowRange> merge;    // requests whose pieces go to partial slots
   std::vector<GatherReq> gather;  // FP8 caches: requests whose rows are dequantised up front
   int gather_blocks = 0;
@@ -328,19 +328,24 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   std::memset(&p, 0, sizeof(p));
 
   const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
-  // FP8 caches: the gather pass first writes every needed row as exact bf16(e4m3) (no
-  // scale) into the workspace; the kernel then reads those rows and applies kv_scale to
-  // the fp32 up-projection accumulators.
-  const void* rows_base = fp8 ? static_cast<const void*>(ws + fw.gath_off) : kv_cache;
-  const uint64_t rows_total = fp8 ? (uint64_t)std::max(fp.gather_blocks, 1) * kBlock : (uint64_t)num_blocks * kBlock;
+  // The gather pass first copies every block the requests use, in logical
+  // order, into the workspace (FP8 rows as exact bf16(e4m3), without the
+  // scale, which is applied to the fp32 up-projection accumulators), so the
+  // kernel reads each request's rows contiguously: one 256-row box per
+  // k-slice of a producer pass, one 128-row (or two 64-row, when paired) box
+  // of k_rope per consumer tile.
+  const void* rows_base = static_cast<const void*>(ws + fw.gath_off);
+  const uint64_t rows_total = (uint64_t)std::max(fp.gather_blocks, 1) * kBlock;
   bool ok = true;
   p.q_bf16 = static_cast<const uint16_t*>(q);
   {
     const uint64_t d[2] = {(uint64_t)kRowBf16, rows_total};
     const uint64_t st[1] = {(uint64_t)kRowBytesBf16};
-    const uint32_t b[2] = {64, 64};
-    ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
-    p.tm_c = p.tm_kr;
+    const uint32_t b64[2] = {64, 64}, b128[2] = {64, 128}, b256[2] = {64, 256};
+    ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d, st, b64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= encode_map(&p.tm_kr128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d, st, b128,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= encode_map(&p.tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d, st, b256, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   {
     // kv_b_proj [512][H*256] seen as 64-column blocks: (col in block, latent row, block)
@@ -356,6 +361,9 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     const uint64_t st[2] = {128, 128 * 128};
     const uint32_t b[3] = {64, 128, 2};
     ok &= encode_map(&p.tm_ring, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + fw.ring_off, d, st, b,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint32_t b1[3] = {64, 128, 1};
+    ok &= encode_map(&p.tm_ring1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + fw.ring_off, d, st, b1,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return MLA_ERR_CUDA;
@@ -380,22 +388,35 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   rope_fracs((double)rope_theta, p.rope_frac);
 
+  // MLA_PAIR=1: consumer pairs in clusters of two CTAs share every K/V load
+  // (multicast), halving the consumers' L2 reads.  Off by default: on GB300 it
+  // measured no faster, the consumers being bound by their softmax chain, not
+  // by L2.  Single CTAs are also the fallback when no cluster of two fits.
+  int pair = env_int("MLA_PAIR", 0) != 0 ? 1 : 0;
   int grid = 0;
-  int st = cuda_status(fused_grid_size(&grid));
+  int st = cuda_status(fused_grid_size(&grid, pair));
+  if (st != MLA_OK && pair) {
+    cudaGetLastError();
+    pair = 0;
+    st = cuda_status(fused_grid_size(&grid, pair));
+  }
+  if (st != MLA_OK) return st;
   // MLA_FUSED_GRID caps the persistent grid (a tuning and measurement knob; the
   // role queue is correct for any grid with more CTAs than producers per job).
-  if (st == MLA_OK) grid = std::min(grid, std::max(8, env_int("MLA_FUSED_GRID", grid)));
-  if (st != MLA_OK) return st;
+  grid = std::min(grid, std::max(8, env_int("MLA_FUSED_GRID", grid)));
+  if (pair) grid &= ~1;
+  p.pair = pair;
+  const int width = pair ? 2 : 1;
   st = cuda_status(cudaMemsetAsync(err, 0, 256, s));   // error word + role queue
   if (st != MLA_OK) return st;
-  if (fp8) {
+  {
     GatherBlocksParams gp;
     std::memset(&gp, 0, sizeof(gp));
     gp.cache = static_cast<const uint8_t*>(kv_cache);
     gp.block_table = block_table;
     gp.dst = reinterpret_cast<uint16_t*>(ws + fw.gath_off);
     gp.err = err;
-    gp.fp8 = 1;
+    gp.fp8 = fp8 ? 1 : 0;
     gp.scale = 1.f;
     gp.num_blocks = num_blocks;
     gp.max_blocks = max_blocks;
@@ -421,24 +442,25 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   const size_t ppl = (size_t)std::max(fw.pieces_per_launch, 1);
   for (size_t b0 = 0; b0 < fp.pieces.size(); b0 += ppl) {
     const size_t n = std::min(fp.pieces.size() - b0, ppl);
-    int roles = 0;
+    int groups = 0;
     for (size_t i = 0; i < n; ++i) {
       Piece pc = fp.pieces[b0 + i];
-      pc.role_begin = roles;
-      roles += H * (pc.n_prod + pc.n_cons);
+      pc.group_begin = groups;
+      groups += H * ((pc.n_prod + width - 1) / width + (pc.n_cons + width - 1) / width);
       p.pieces[i] = pc;
     }
     p.n_pieces = (int)n;
-    p.n_roles = roles;
+    p.n_groups = groups;
+    const size_t slots = (size_t)groups * 2;   // trace slot = group * 2 + cluster rank
     void* tr = g_trace.load();
-    p.trace = (tr != nullptr && g_trace_bytes.load() >= (size_t)roles * kTraceWords * 8 && fp.pieces.size() <= ppl)
+    p.trace = (tr != nullptr && g_trace_bytes.load() >= slots * kTraceWords * 8 && fp.pieces.size() <= ppl)
                   ? static_cast<unsigned long long*>(tr) : nullptr;
-    // per-stage detail of one role when the buffer has room for 4096 more stages
-    p.trace_detail_role = (p.trace && g_trace_bytes.load() >= ((size_t)roles * kTraceWords + 4096 * 8) * 8)
+    // per-stage detail of one role slot when the buffer has room for 4096 more stages
+    p.trace_detail_role = (p.trace && g_trace_bytes.load() >= (slots * kTraceWords + 4096 * 8) * 8)
                               ? env_int("MLA_TRACE_DETAIL_ROLE", -1) : -1;
     if (b0 > 0 && (st = cuda_status(cudaMemsetAsync(p.queue, 0, sizeof(uint32_t), s))) != MLA_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(p.flags, 0, fw.flags_bytes, s))) != MLA_OK) return st;
-    if ((st = cuda_status(launch_fused(p, std::min(grid, roles), s))) != MLA_OK) return st;
+    if ((st = cuda_status(launch_fused(p, std::min(grid, groups * width), s))) != MLA_OK) return st;
   }
   if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_e, s))) != MLA_OK) return st;
 
@@ -508,7 +530,7 @@ size_t mla_prefill_workspace_size(int num_reqs, const int32_t* seq_lens, const i
   if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
     return 0;
   FusedPlan fp;
-  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fp);   // room for gathered rows (FP8 caches)
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fp);   // room for the gathered rows
   return fused_ws_layout(fp, num_heads).total;
 }
 
@@ -533,7 +555,7 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, i
   for (int r = 0; r < num_reqs; ++r)
     if ((seq_lens[r] + kBlock - 1) / kBlock > max_blocks_per_req) return MLA_ERR_INVALID_ARG;
   FusedPlan fplan;
-  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, kv_dtype == MLA_KV_FP8_E4M3, &fplan);
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fplan);
   const int ppl = fused_pieces_fitting(fplan, num_heads, workspace_bytes);
   if (workspace == nullptr || !aligned(workspace, 256) || ppl < 1) return MLA_ERR_WORKSPACE;
   const FusedWs fw = fused_ws_layout(fplan, num_heads, ppl);
@@ -560,7 +582,7 @@ int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos, const void* kv_
   if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
     return MLA_ERR_INVALID_ARG;
   FusedPlan fplan;
-  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, kv_dtype == MLA_KV_FP8_E4M3, &fplan);
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fplan);
   if (fused_pieces_fitting(fplan, num_heads, MLA_NOALLOC_SCRATCH_BYTES) < 1) return MLA_ERR_TOO_LARGE;
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);

@@ -81,14 +81,14 @@ constexpr uint32_t kIdescUp = idesc_bf16(128, 256, false, true);
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 256
 
 struct Ctl {
-  int role;
+  int group;       // written by cluster rank 0 into both CTAs
   int abort;
   uint32_t tmem;
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t sbase, uint32_t i) { return sbase + kBarBase + 8u * i; }
 
-// Optional tracing: per role kTraceWords words
+// Optional tracing: per role slot (group * 2 + cluster rank) kTraceWords words
 //   [0] start ns  [1] end ns  [2] cta << 32 | producer << 31 | job
 //   [3] ns waiting on the other role kind (consumer: `ready` flags; producer: `consumed`)
 //   [4] ns the MMA thread waited for operands (kv_full / prod_full)
@@ -107,7 +107,7 @@ __device__ __forceinline__ void trace_put(const FusedParams& p, int role, int wo
 //   [4] MMA saw P  [5] MMA saw V (PV issued next)  [6] softmax saw S  [7] softmax published P
 __device__ __forceinline__ void trace_stage(const FusedParams& p, int role, int stage, int word) {
   if (p.trace && role == p.trace_detail_role && stage < 4096)
-    p.trace[(size_t)p.n_roles * kTraceWords + (size_t)stage * 8 + word] = global_timer_ns();
+    p.trace[(size_t)p.n_groups * 2 * kTraceWords + (size_t)stage * 8 + word] = global_timer_ns();
 }
 
 __device__ __forceinline__ bool aborted_global(const FusedParams& p) { return ld_volatile_u32(p.err) != 0u; }
@@ -152,9 +152,19 @@ __device__ __forceinline__ int consumer_tiles(const Job& J, int ci) {
   return (k_end - J.t0 + 127) >> 7;
 }
 
-__device__ __forceinline__ int consumers_needing_tile(const Job& J, int t) {
+// Tiles consumer `ci` loads: a paired consumer (ci and ci^1 in one cluster)
+// loads the tiles of both, since each CTA of the pair brings half of every
+// tile into both shared memories.
+__device__ __forceinline__ int consumer_load_tiles(const Job& J, int ci, int pair) {
+  int n = consumer_tiles(J, ci);
+  if (pair && (ci ^ 1) < J.n_cons) n = max(n, consumer_tiles(J, ci ^ 1));
+  return n;
+}
+
+// Consumer CTAs that load tile t (each adds 2 to the slot's consumed count).
+__device__ __forceinline__ int consumers_needing_tile(const Job& J, int t, int pair) {
   int n = 0;
-  for (int ci = 0; ci < J.n_cons; ++ci) n += consumer_tiles(J, ci) > t;
+  for (int ci = 0; ci < J.n_cons; ++ci) n += consumer_load_tiles(J, ci, pair) > t;
   return n;
 }
 
@@ -165,34 +175,32 @@ __device__ __forceinline__ uint32_t* consumed_flag(const FusedParams& p, int job
   return p.flags + (size_t)job * (2 * kRing) + kRing + slot;
 }
 
-// Physical cache row of logical block `lb` of request `req`, or a negative row
-// (TMA fills zeros) when the block lies outside the table; a table entry
-// outside [0, num_blocks) for a block holding live tokens is an error.
-__device__ __forceinline__ int block_row(const FusedParams& p, const Job& J, int lb, bool live) {
-  if (J.row_block0 >= 0) return (J.row_block0 + lb) * kBlock;   // rows gathered (and dequantised) up front
-  const int req = J.req;
-  if (lb < 0 || lb >= p.max_blocks) return -kBlock;
-  const int blk = __ldg(p.block_table + (int64_t)req * p.max_blocks + lb);
-  if (blk < 0 || blk >= p.num_blocks) {
-    if (live) atomicOr(p.err, kErrBadBlock);
-    return -kBlock;
-  }
-  return blk * kBlock;
-}
+// Row of logical block `lb` of the job's request in the gathered rows (the
+// gather pass copied the request's blocks in logical order from row_block0 on;
+// it also reported any bad block id).  Rows past the request's blocks are
+// read but belong to keys outside the job's range, which are masked.
+__device__ __forceinline__ int block_row(const Job& J, int lb) { return (J.row_block0 + lb) * kBlock; }
 
 // =============================================================== consumer
 // One 128-query tile of a job.  Warps: 0-7 softmax (warpgroup w owns key
 // columns 64w..64w+63 of every row; warpgroup 0 first loads and rotates Q into
 // TMEM), 8 K loader, 9 MMA issuer, 10 V loader, 11 releases ring slots.
+// `paired`: this CTA and its cluster peer own query tiles ci and ci^1 of the
+// same job and run the same key tiles; each CTA loads half of every K and V
+// stage (block `rank`) with multicast into both, and both MMAs must release a
+// stage (commits to both CTAs' empty barriers) before either refills it.
+template <bool kCompute>
 __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci, int role, uint32_t sbase,
-                             uint8_t* sgen, uint32_t tmem, volatile Ctl* ctl) {
+                             uint8_t* sgen, uint32_t tmem, volatile Ctl* ctl, bool paired, uint32_t rank) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q0 = ci * 128;
   const int nq = min(128, J.q_count - q0);
   const int grow0 = J.q_begin + q0;
-  const int n_tiles = consumer_tiles(J, ci);
+  const int n_tiles = consumer_load_tiles(J, ci, paired ? 1 : 0);
+  const uint16_t kBoth = 3;
   const int H = p.num_heads;
 
+  if constexpr (!kCompute) {
   if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ TMA loads (K or V)
     if (lane != 0) return;
@@ -218,18 +226,26 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
       if (is_k) {
         const uint32_t st = sbase + kKBase + s * kKStageBytes;
         const uint32_t full = bar_addr(sbase, kBKFull + s);
-        mbar_arrive_expect_tx(full, kKStageBytes);
-        tma_load_3d(st, &p.tm_ring, 0, 0, zb, full);                      // K_nope, 32 KB
+        mbar_arrive_expect_tx(full, kKStageBytes);       // both halves land here, the peer's by multicast
         const int kt0 = J.t0 + 128 * j;
-        tma_load_2d(st + 2 * kAtomQ, &p.tm_kr, kDc, block_row(p, J, kt0 >> 6, true), full);
-        tma_load_2d(st + 2 * kAtomQ + kAtom64, &p.tm_kr, kDc,
-                    block_row(p, J, (kt0 >> 6) + 1, kt0 + 64 < J.k_end), full);
+        if (paired) {
+          const int h = (int)rank;
+          tma_load_3d_mc(st + h * kAtomQ, &p.tm_ring1, 0, 0, zb + h, full, kBoth);          // K_nope block h
+          tma_load_2d_mc(st + 2 * kAtomQ + h * kAtom64, &p.tm_kr, kDc, block_row(J, (kt0 >> 6) + h), full,
+                         kBoth);                                                             // k_rope, 64 keys
+        } else {
+          tma_load_3d(st, &p.tm_ring, 0, 0, zb, full);                      // K_nope, 32 KB
+          tma_load_2d(st + 2 * kAtomQ, &p.tm_kr128, kDc, block_row(J, kt0 >> 6), full);   // k_rope, 16 KB
+        }
         trace_stage(p, role, j, 0);
       } else {
         const uint32_t st = sbase + kVBase + s * kVStageBytes;
         const uint32_t full = bar_addr(sbase, kBVFull + s);
         mbar_arrive_expect_tx(full, kVStageBytes);
-        tma_load_3d(st, &p.tm_ring, 0, 0, zb + 2, full);                  // V, 32 KB
+        if (paired)
+          tma_load_3d_mc(st + rank * kAtomQ, &p.tm_ring1, 0, 0, zb + 2 + (int)rank, full, kBoth);  // V block
+        else
+          tma_load_3d(st, &p.tm_ring, 0, 0, zb + 2, full);                  // V, 32 KB
         trace_stage(p, role, j, 1);
       }
     }
@@ -265,7 +281,8 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
         mma_bf16_ts(d, tmem + kTmQ + kk * 8, sdesc_sw128(k + (kk >> 2) * kAtomQ + (kk & 3) * 32, 16, 1024), kIdescS,
                     kk > 0 ? 1u : 0u);
       mma_commit(bar_addr(sbase, kBSFull + b));
-      mma_commit(bar_addr(sbase, kBKEmpty + sk));
+      if (paired) mma_commit_mc(bar_addr(sbase, kBKEmpty + sk), kBoth);
+      else mma_commit(bar_addr(sbase, kBKEmpty + sk));
       trace_stage(p, role, j, 3);
     };
     auto issue_pv = [&](int jj) {
@@ -280,7 +297,8 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
         mma_bf16_ts(tmem + kTmO, tmem + kTmS + 128 * b + kk * 8, sdesc_sw128(v + kk * 2048, kAtomQ, 1024), kIdescPV,
                     (jj > 0 || kk > 0) ? 1u : 0u);
       mma_commit(bar_addr(sbase, kBPvDone + b));
-      mma_commit(bar_addr(sbase, kBVEmpty + sv));
+      if (paired) mma_commit_mc(bar_addr(sbase, kBVEmpty + sv), kBoth);
+      else mma_commit(bar_addr(sbase, kBVEmpty + sv));
     };
     // S(j) needs K(j); PV(j-1) needs P(j-1) and V(j-1).  S(j) may run before
     // PV(j-1) (its S buffer's previous P was consumed by PV(j-2), issued
@@ -326,6 +344,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
     if (!ok) ctl->abort = 1;
     trace_put(p, role, 4, tr_kv.t);
     trace_put(p, role, 5, tr_p.t);
+  }
   } else {
     if (warp < 4) {
       // ---------------------------------------------------------- Q -> TMEM (warpgroup 0)
@@ -516,6 +535,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
 }
 
 // =============================================================== producer
+template <bool kCompute>
 __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi, int role, uint32_t sbase,
                              uint32_t tmem, volatile Ctl* ctl) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -526,31 +546,26 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
   for (int pp = pi; pp < n_pass; pp += J.n_prod) ++my_passes;
   if (my_passes == 0) return;
 
+  if constexpr (!kCompute) {
   if (warp == 8 || warp == 10) {
-    // TMA issue, split over two warps: warp 8 loads kv_b_proj and the first 128
-    // tokens' latent slices, warp 10 the second 128 tokens'.
+    // TMA issue, split over two warps: warp 8 loads the pass's 256 latent rows
+    // (one 256-row box per 64-wide slice) and arms the stage, warp 10 the
+    // head's kv_b_proj slices (K_nope columns, V columns).
     if (lane == 0) {
       const bool primary = warp == 8;
       int g = 0;
       for (int n = 0; n < my_passes; ++n) {
         const int pass = pi + n * J.n_prod;
-        int rows[4];
-        for (int i = 0; i < 4; ++i) {
-          const int lb = (J.t0 >> 6) + 4 * pass + i;
-          const int tok = lb * 64;
-          const bool live = tok + 63 >= J.k_begin && tok < J.k_end;
-          rows[i] = live ? block_row(p, J, lb, primary) : -kBlock;
-        }
+        const int row0 = block_row(J, (J.t0 >> 6) + 4 * pass);
         for (int k = 0; k < kDc / 64; ++k, ++g) {
           const int s = g & 1;
           if (g >= 2 && !wait_bar(p, bar_addr(sbase, kBProdEmpty + s), ((g >> 1) - 1) & 1)) { ctl->abort = 1; return; }
           const uint32_t st = sbase + s * kPStageBytes;
           const uint32_t bar = bar_addr(sbase, kBProdFull + s);
-          if (primary) mbar_arrive_expect_tx(bar, kPStageBytes);
-          for (int i = 0; i < 4; ++i)
-            if ((i < 2) == primary)
-              tma_load_2d(st + (i < 2 ? kPCA : kPCB) + (i & 1) * kAtom64, &p.tm_c, 64 * k, rows[i], bar);
           if (primary) {
+            mbar_arrive_expect_tx(bar, kPStageBytes);
+            tma_load_2d(st + kPCA, &p.tm_c, 64 * k, row0, bar);                                        // C_A | C_B
+          } else {
             tma_load_3d(st + kPW, &p.tm_w, 0, 64 * k, 2 * h, bar);                                   // K_nope cols
             tma_load_3d(st + kPW + 2 * kAtom64, &p.tm_w, 0, 64 * k, (H * kDnope + h * kDv) / 64, bar); // V cols
           }
@@ -586,7 +601,9 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       trace_put(p, role, 5, tr_acc.t);
       trace_put(p, role, 7, (unsigned long long)my_passes);
     }
-  } else if (warp < 8) {
+  }
+  } else {
+  {
     // conversion: warpgroup 0 -> tile 2*pass, warpgroup 1 -> tile 2*pass + 1
     const int wg = warp >> 2;
     const int r = tid & 127;
@@ -644,7 +661,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
           // the slot's previous occupant (tile t - ring) must be published and fully consumed
           if (t >= (int)kRing &&
               !(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - kRing + 1)) &&
-                wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - kRing))))
+                wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - kRing, p.pair))))
             ctl->abort = 1;
           tr_c.end(p, w0);
           *consumed_flag(p, job, slot) = 0u;    // ordered before the release of `ready` below
@@ -674,6 +691,96 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       if (ctl->abort) return;
     }
     if (tid == 0) trace_put(p, role, 3, tr_c.t);
+  }
+  }
+}
+
+// The role loop, instantiated once for the compute warps (0-7: softmax,
+// conversion, Q load) and once for the control warps (8-11: TMA, MMA issue,
+// ring release), which run it with different register budgets.
+template <bool kCompute>
+__device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, uint8_t* sgen, volatile Ctl* ctl,
+                                          uint32_t tmem) {
+  const int tid = threadIdx.x;
+  // Role groups: cluster rank 0 takes the next group from the queue and
+  // writes it into both CTAs; every exit decision is made there, so both CTAs
+  // of a cluster run the same sequence of cluster barriers.  A group holds up
+  // to two producer roles of one job (independent) or a consumer pair (query
+  // tiles 2k and 2k+1 of one job, sharing K/V loads); without pairing it holds
+  // one role.
+  const uint32_t rank = p.pair ? cluster_rank() : 0u;
+  const int width = p.pair ? 2 : 1;
+  cluster_sync_all();   // every CTA of the cluster has started before any shared::cluster access
+  for (;;) {
+    if (kCompute && tid == 0 && rank == 0) {
+      const int g = (ctl->abort || aborted_global(p)) ? p.n_groups : (int)atomicAdd(p.queue, 1u);
+      ctl->group = g;
+      if (p.pair) st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&ctl->group)), 1u), (uint32_t)g);
+    }
+    tc_fence_before();
+    cluster_sync_all();   // also: both CTAs are done with the previous group
+    tc_fence_after();
+    const int g = ctl->group;
+    if (g >= p.n_groups) break;
+    int lo = 0, hi = p.n_pieces - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.pieces[mid].group_begin <= g) lo = mid; else hi = mid - 1;
+    }
+    const Piece& P = p.pieces[lo];
+    const int gp = (P.n_prod + width - 1) / width, gc = (P.n_cons + width - 1) / width;
+    const int local = g - P.group_begin;
+    Job J;
+    J.req = P.req;
+    J.head = local / (gp + gc);
+    J.q_begin = P.q_begin;
+    J.q_count = P.q_count;
+    J.q_tok0 = P.q_tok0;
+    J.k_begin = P.k_begin;
+    J.k_end = P.k_end;
+    J.t0 = P.k_begin & ~(kBlock - 1);
+    J.n_tiles = (P.k_end - J.t0 + 127) >> 7;
+    J.n_cons = P.n_cons;
+    J.n_prod = P.n_prod;
+    J.slot = P.slot;
+    J.row_block0 = P.row_block0;
+    J.rope_offset = P.rope_offset;
+    const int job = lo * p.num_heads + J.head;
+    const int gi = local - J.head * (gp + gc);
+    const bool producer = gi < gp;
+    const int idx = (producer ? gi : gi - gp) * width + (int)rank;
+    const bool valid = idx < (producer ? J.n_prod : J.n_cons);
+    const bool paired = !producer && p.pair && ((gi - gp) * 2 + 1) < J.n_cons;
+    const int slot = g * 2 + (int)rank;   // trace slot
+    if (kCompute && tid == 32) {
+      // fresh barriers for this role (every barrier is idle here)
+      for (uint32_t i = 0; i < kNumBars; ++i) {
+        mbar_inval(bar_addr(sbase, i));
+        uint32_t cnt = 1;
+        if (!producer && (i == kBPFull || i == kBPFull + 1)) cnt = 256;
+        if (!producer && i == kBQReady) cnt = 128;
+        if (producer && i == kBAccEmpty) cnt = 256;
+        if (paired && ((i >= kBKEmpty && i < kBKEmpty + kKStages) || (i >= kBVEmpty && i < kBVEmpty + kVStages)))
+          cnt = 2;   // both MMAs of the pair release a stage
+        mbar_init(bar_addr(sbase, i), cnt);
+      }
+      fence_mbar_init();
+    }
+    cluster_sync_all();   // the peer's barriers exist before any multicast or commit reaches them
+    if (valid) {
+      if (kCompute && p.trace && tid == 0) {
+        trace_put(p, slot, 0, global_timer_ns());
+        trace_put(p, slot, 2, ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)producer << 31) | (unsigned)job);
+      }
+      if (!ctl->abort) {
+        if (producer) run_producer<kCompute>(p, J, job, idx, slot, sbase, tmem, ctl);
+        else run_consumer<kCompute>(p, J, job, idx, slot, sbase, sgen, tmem, ctl, paired, rank);
+      }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (kCompute && p.trace && tid == 0) trace_put(p, slot, 1, global_timer_ns());
+    }
   }
 }
 
@@ -705,60 +812,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
 
-  for (;;) {
-    if (tid == 0) ctl->role = (ctl->abort || aborted_global(p)) ? p.n_roles : (int)atomicAdd(p.queue, 1u);
-    __syncthreads();
-    const int role = ctl->role;
-    if (role >= p.n_roles) break;
-    int lo = 0, hi = p.n_pieces - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.pieces[mid].role_begin <= role) lo = mid; else hi = mid - 1;
-    }
-    const Piece& P = p.pieces[lo];
-    const int per_job = P.n_cons + P.n_prod;
-    const int local = role - P.role_begin;
-    Job J;
-    J.req = P.req;
-    J.head = local / per_job;
-    J.q_begin = P.q_begin;
-    J.q_count = P.q_count;
-    J.q_tok0 = P.q_tok0;
-    J.k_begin = P.k_begin;
-    J.k_end = P.k_end;
-    J.t0 = P.k_begin & ~(kBlock - 1);
-    J.n_tiles = (P.k_end - J.t0 + 127) >> 7;
-    J.n_cons = P.n_cons;
-    J.n_prod = P.n_prod;
-    J.slot = P.slot;
-    J.row_block0 = P.row_block0;
-    J.rope_offset = P.rope_offset;
-    const int job = lo * p.num_heads + J.head;
-    const int idx = local - J.head * per_job;
-    const bool producer = idx < J.n_prod;
-    if (tid == 32) {
-      // fresh barriers for this role (every barrier is idle here)
-      for (uint32_t i = 0; i < kNumBars; ++i) {
-        mbar_inval(bar_addr(sbase, i));
-        uint32_t cnt = 1;
-        if (!producer && (i == kBPFull || i == kBPFull + 1)) cnt = 256;
-        if (!producer && i == kBQReady) cnt = 128;
-        if (producer && i == kBAccEmpty) cnt = 256;
-        mbar_init(bar_addr(sbase, i), cnt);
-      }
-      fence_mbar_init();
-    }
-    __syncthreads();
-    if (p.trace && tid == 0) {
-      trace_put(p, role, 0, global_timer_ns());
-      trace_put(p, role, 2, ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)producer << 31) | (unsigned)job);
-    }
-    if (producer) run_producer(p, J, job, idx, role, sbase, tmem, ctl);
-    else run_consumer(p, J, job, idx - J.n_prod, role, sbase, sgen, tmem, ctl);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (p.trace && tid == 0) trace_put(p, role, 1, global_timer_ns());
+  // Registers: the control warps need few, the compute warps many.  At
+  // launch every thread has 168 (384 x 168 = 64512); warpgroup 2 gives back
+  // 112 each (128 x 112) and warpgroups 0 and 1 take 56 more each (256 x 56):
+  // the same total, so the increase never waits on registers that are not there.
+  if ((tid >> 5) >= 8) {
+    setmaxnreg_dec<56>();
+    role_loop<false>(p, sbase, sgen, ctl, tmem);
+  } else {
+    setmaxnreg_inc<224>();
+    role_loop<true>(p, sbase, sgen, ctl, tmem);
   }
   tc_fence_before();
   __syncthreads();
@@ -769,24 +832,37 @@ __global__ void __launch_bounds__(kThreads, 1) fused_prefill_kernel(const __grid
 
 int fused_smem_bytes() { return (int)kSmemBytes; }
 
-cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t s) {
+static cudaError_t configure(int dev) {
   static int configured_device = -1;
+  if (configured_device == dev) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fused_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e == cudaSuccess) configured_device = dev;
+  return e;
+}
+
+// Pairs: clusters of two CTAs (no cooperative attribute: a role only ever
+// waits on roles dequeued before it, which run on CTAs that are resident).
+// Without pairs: a cooperative launch of single CTAs.
+cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = configure(dev);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(fused_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (p.pair) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, fused_prefill_kernel, p);
@@ -794,14 +870,33 @@ cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t s) {
   return e;
 }
 
-cudaError_t fused_grid_size(int* grid) {
+cudaError_t fused_grid_size(int* grid, int pair) {
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(fused_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_prefill_kernel, kThreads, kSmemBytes);
+  if (e == cudaSuccess) e = configure(dev);
   if (e != cudaSuccess) return e;
-  *grid = sms * (per_sm > 0 ? per_sm : 0);
+  if (pair) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * ((sms + 1) / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, fused_prefill_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    *grid = 2 * clusters;
+  } else {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_prefill_kernel, kThreads, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    *grid = sms * (per_sm > 0 ? per_sm : 0);
+  }
   return *grid > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 

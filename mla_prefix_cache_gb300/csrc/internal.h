@@ -74,10 +74,10 @@ struct Piece {
   int32_t k_begin;     // first key token
   int32_t k_end;       // one past the last key token
   int32_t slot;        // partial-state slot, or -1: write the final out/lse
-  int32_t role_begin;  // first role of this piece in the launch's role queue
+  int32_t group_begin; // first role group of this piece in the launch's queue
   int32_t n_cons;      // consumer roles per head (128 queries each)
   int32_t n_prod;      // producer roles per head
-  int32_t row_block0;  // >= 0: the request's rows were gathered contiguously from this block
+  int32_t row_block0;  // the request's rows were gathered contiguously from this block on
   int32_t pad;
   int64_t rope_offset;
 };
@@ -89,13 +89,15 @@ struct Job {
 };
 
 struct FusedParams {
-  CUtensorMap tm_kr;     // bf16 latent rows [rows][576], box 64 x 64 (k_rope at column 512)
-  CUtensorMap tm_c;      // same rows, box 64 x 64 (one latent slice)
+  CUtensorMap tm_kr;     // gathered bf16 latent rows [rows][576], box 64 x 64 (k_rope at column 512)
+  CUtensorMap tm_kr128;  // same rows, box 64 x 128 (the k_rope of one 128-key tile)
+  CUtensorMap tm_c;      // same rows, box 64 x 256 (one 64-wide latent slice of a producer pass)
   CUtensorMap tm_w;      // bf16 kv_b_proj as [H*4 blocks][512 rows][64 cols], box 64 x 64 x 2
   CUtensorMap tm_ring;   // bf16 ring as [jobs*ring*4 blocks][128 rows][64 cols], box 64 x 128 x 2
+  CUtensorMap tm_ring1;  // same ring, box 64 x 128 x 1 (one block: half of a paired consumer's stage)
   const uint16_t* q_bf16;  // q [T_q][H][192]
   uint32_t* err;
-  uint32_t* queue;       // role counter
+  uint32_t* queue;       // role-group counter
   uint32_t* flags;       // per job: ready[ring], consumed[ring]
   uint16_t* ring;
   const int32_t* block_table;
@@ -112,9 +114,10 @@ struct FusedParams {
   float out_scale;      // applied to the up-projection accumulators (FP8 dequant scale, else 1)
   float scale_log2;
   int n_pieces;
-  int n_roles;
-  unsigned long long* trace;   // optional, kTraceWords per role (see fused.cu)
-  int trace_detail_role;       // role whose stages are timed one by one (-1: none)
+  int n_groups;         // role groups in the queue (one per cluster dequeue)
+  int pair;             // 1: clusters of two CTAs, consumer pairs share K/V loads by multicast
+  unsigned long long* trace;   // optional, kTraceWords per role slot (group * 2 + cluster rank; see fused.cu)
+  int trace_detail_role;       // role slot whose stages are timed one by one (-1: none)
   uint64_t rope_frac[kDr / 2];
   Piece pieces[kMaxPieces];
 };
@@ -124,7 +127,9 @@ constexpr int kTraceWords = 8;
 static_assert(sizeof(FusedParams) <= 32000, "kernel parameter space");
 
 cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t s);
-cudaError_t fused_grid_size(int* grid);
+// Persistent grid: CTAs resident at once, a multiple of the cluster size
+// (2 when `pair`, else 1); 0 clusters -> error.
+cudaError_t fused_grid_size(int* grid, int pair);
 int fused_smem_bytes();
 
 // Kernel launchers (return cudaError_t of the launch).
