@@ -362,8 +362,10 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     const uint32_t b[3] = {64, 128, 2};
     ok &= encode_map(&p.tm_ring, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + fw.ring_off, d, st, b,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-    const uint32_t b1[3] = {64, 128, 1};
+    const uint32_t b1[3] = {64, 128, 1}, b64[3] = {64, 64, 2};
     ok &= encode_map(&p.tm_ring1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + fw.ring_off, d, st, b1,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= encode_map(&p.tm_ring64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + fw.ring_off, d, st, b64,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return MLA_ERR_CUDA;
@@ -393,14 +395,18 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   // measured no faster, the consumers being bound by their softmax chain, not
   // by L2.  Single CTAs are also the fallback when no cluster of two fits.
   int pair = env_int("MLA_PAIR", 0) != 0 ? 1 : 0;
+  // MLA_CTA_PAIR=1: the CTA-pair kernel (fused2.cu), every role run by a
+  // cluster of two CTAs with M = 256 MMAs.
+  const bool v2 = env_int("MLA_CTA_PAIR", 0) != 0;
   int grid = 0;
-  int st = cuda_status(fused_grid_size(&grid, pair));
-  if (st != MLA_OK && pair) {
+  int st = v2 ? cuda_status(fused2_grid_size(&grid)) : cuda_status(fused_grid_size(&grid, pair));
+  if (st != MLA_OK && !v2 && pair) {
     cudaGetLastError();
     pair = 0;
     st = cuda_status(fused_grid_size(&grid, pair));
   }
   if (st != MLA_OK) return st;
+  if (v2) pair = 1;
   // MLA_FUSED_GRID caps the persistent grid (a tuning and measurement knob; the
   // role queue is correct for any grid with more CTAs than producers per job).
   grid = std::min(grid, std::max(8, env_int("MLA_FUSED_GRID", grid)));
@@ -446,7 +452,9 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     for (size_t i = 0; i < n; ++i) {
       Piece pc = fp.pieces[b0 + i];
       pc.group_begin = groups;
-      groups += H * ((pc.n_prod + width - 1) / width + (pc.n_cons + width - 1) / width);
+      if (v2) pc.n_prod = std::max(1, (pc.n_prod + 1) / 2);   // producer roles of a pair: two CTAs each
+      groups += v2 ? H * (pc.n_prod + (pc.n_cons + 1) / 2)
+                   : H * ((pc.n_prod + width - 1) / width + (pc.n_cons + width - 1) / width);
       p.pieces[i] = pc;
     }
     p.n_pieces = (int)n;
@@ -460,7 +468,9 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
                               ? env_int("MLA_TRACE_DETAIL_ROLE", -1) : -1;
     if (b0 > 0 && (st = cuda_status(cudaMemsetAsync(p.queue, 0, sizeof(uint32_t), s))) != MLA_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(p.flags, 0, fw.flags_bytes, s))) != MLA_OK) return st;
-    if ((st = cuda_status(launch_fused(p, std::min(grid, groups * width), s))) != MLA_OK) return st;
+    const cudaError_t le = v2 ? launch_fused2(p, std::min(grid, groups * 2), s)
+                              : launch_fused(p, std::min(grid, groups * width), s);
+    if ((st = cuda_status(le)) != MLA_OK) return st;
   }
   if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_e, s))) != MLA_OK) return st;
 

@@ -1,0 +1,753 @@
+// Persistent fused MLA prefill kernel on CTA pairs (tcgen05 cta_group::2).
+//
+// What it computes is the same as fused.cu ("DeepSeek MLA — Prefix Cache 与
+// Chunked Prefill 深度解析", section 4.4, with the query relocation of
+// "RedKnot-MLA: Multi-Head Offline-Online Reuse for DeepSeek-V4 Long-Context
+// Serving", section 2): per job (request, head, key range with one RoPE
+// offset) the keys are up-projected once, K_nope | V = c_kv * kv_b_proj[:, head],
+// and every query of the request attends to them.
+//
+// How it differs from fused.cu.  Clusters of two CTAs run every role
+// together and the pair's tensor-core work is issued by the first CTA (the
+// leader) as M = 256 MMAs: rows 0..127 of A and of the accumulator live in the
+// leader, rows 128..255 in its peer, and each CTA holds half of B.  So each
+// CTA stores half of every key tile, which frees shared memory for Q and TMEM
+// for a third score buffer:
+//   producer pair  up-projects passes of 256 tokens (128 per CTA); CTA r holds
+//                  the head's K_nope (r = 0) or V (r = 1) columns of
+//                  kv_b_proj; the accumulators (all 256 columns of the 128
+//                  tokens of the CTA) are double-buffered in TMEM, so the next
+//                  pass runs while 256 threads convert the previous one to
+//                  bf16 and store it into the job's ring (in L2);
+//   consumer pair  two 128-query tiles of the job (CTA r owns tile 2k + r;
+//                  Q, RoPE-rotated, in shared memory).  Per 128-key tile CTA r
+//                  loads keys 64r..64r+63 of K (K_nope and k_rope) and columns
+//                  64r..64r+63 of V; S = Q K^T lands in one of three TMEM
+//                  buffers of each CTA, so the MMA can run two tiles ahead of
+//                  the softmax; P is written back over S as bf16 and
+//                  O += P V reads it from TMEM.
+// Barriers the leader's MMA thread waits on (operands landed in both CTAs,
+// P written in both) live in the leader and count both CTAs; barriers of MMA
+// completion are signalled in both CTAs by multicast commits.
+#include <cuda.h>
+
+#include "fused_common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+namespace {
+using namespace fused_common;
+
+constexpr int kThreads = 384;
+constexpr uint32_t kRing = kRingDepth;
+constexpr uint32_t kAtomQ = 16384;                  // [128 rows x 128 B] swizzled block
+constexpr uint32_t kAtom64 = 8192;                  // [64 rows x 128 B] swizzled block
+
+// ---------------------------------------------------------------- shared memory (per CTA)
+// consumer
+constexpr int kKStages = 4, kVStages = 4, kSBufs = 3;
+constexpr uint32_t kQBase = 0;                                     // q_nope lo | q_nope hi | rotated q_rope
+constexpr uint32_t kKStageBytes = 3 * kAtom64;                     // this CTA's 64 keys: K_nope lo | hi | k_rope
+constexpr uint32_t kVStageBytes = kAtomQ;                          // 128 keys x this CTA's 64 columns of V
+constexpr uint32_t kKBase = 3 * kAtomQ;                            // 49152
+constexpr uint32_t kVBase = kKBase + kKStages * kKStageBytes;      // 147456
+constexpr uint32_t kXchgBase = kVBase + kVStages * kVStageBytes;   // 212992: row maxima / sums of the two halves
+constexpr uint32_t kConsumerEnd = kXchgBase + 6 * 128 * 4;
+// producer
+constexpr int kPStages = 4;
+constexpr uint32_t kPStageBytes = 2 * kAtomQ;                      // C: 128 tokens x 64 | W: 64 x 128 columns
+constexpr uint32_t kPC = 0, kPW = kAtomQ;
+constexpr uint32_t kPOutBase = kPStages * kPStageBytes;            // bf16 staging: [128 x 128] per warpgroup
+constexpr uint32_t kProducerEnd = kPOutBase + 2 * 2 * kAtomQ;
+constexpr uint32_t kBarBase = kConsumerEnd > kProducerEnd ? kConsumerEnd : kProducerEnd;
+constexpr uint32_t kNumBars = 26;
+constexpr uint32_t kSmemBytes = kBarBase + 8 * kNumBars + 64 + 1024;
+static_assert(kSmemBytes <= 232448, "more than 227 KB of shared memory per CTA");
+
+// consumer barriers ("leader": only the leader's copy is used, it counts both CTAs)
+constexpr uint32_t kBQReady = 0;          // leader, 256 arrivals (128 Q rows per CTA)
+constexpr uint32_t kBKFull = 1;           // leader, 4: both halves of a K stage landed
+constexpr uint32_t kBKEmpty = 5;          // both, 4: the MMAs reading a K stage are done
+constexpr uint32_t kBVFull = 9;           // leader, 4
+constexpr uint32_t kBVEmpty = 13;         // both, 4
+constexpr uint32_t kBSFull = 17;          // both, 3: S of a buffer computed
+constexpr uint32_t kBPFull = 20;          // leader, 3: P of a buffer written, 512 arrivals
+constexpr uint32_t kBPvDone = 23;         // both, 3: PV reading a buffer done
+// producer barriers
+constexpr uint32_t kBProdFull = 0;        // leader, 4
+constexpr uint32_t kBProdEmpty = 4;       // both, 4
+constexpr uint32_t kBAccFull = 8;         // both, 2
+constexpr uint32_t kBAccEmpty = 10;       // leader, 2: 512 arrivals
+
+// TMEM columns (per CTA)
+constexpr uint32_t kTmO = 0;              // consumer: O [128 x 128] fp32
+constexpr uint32_t kTmS = 128;            // consumer: S buffer b at 128 + 128 b (P as bf16 pairs in its first 64)
+constexpr uint32_t kTmAcc = 0;            // producer: accumulator b at 256 b
+
+constexpr uint32_t kIdescS = idesc_bf16(256, 128, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16(256, 128, false, true);
+constexpr uint32_t kIdescUp = idesc_bf16(256, 256, false, true);
+
+constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 256
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t sbase, uint32_t i) { return sbase + kBarBase + 8u * i; }
+
+// Key tiles of consumer pair k (query tiles 2k and 2k+1; the second may be past
+// the last one).  Both CTAs load and process all of them.
+__device__ __forceinline__ int pair_tiles(const Job& J, int k) {
+  int n = consumer_tiles(J, 2 * k);
+  if (2 * k + 1 < J.n_cons) n = max(n, consumer_tiles(J, 2 * k + 1));
+  return n;
+}
+// Consumer CTAs that load tile t (each adds 2 to the slot's consumed count).
+__device__ __forceinline__ int consumers_needing_tile(const Job& J, int t) {
+  int n = 0;
+  for (int k = 0; 2 * k < J.n_cons; ++k) n += 2 * (pair_tiles(J, k) > t);
+  return n;
+}
+
+// =============================================================== consumer pair
+// Warps: 0-7 softmax (warpgroup w owns key columns 64w..64w+63 of every row of
+// this CTA's S; warpgroup 0 first loads and rotates Q into shared memory),
+// 8 K loader, 10 V loader (each also releases ring slots once their stage is
+// consumed), 9 MMA issuer (leader only).
+template <bool kCompute>
+__device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k, int role, uint32_t sbase,
+                             uint8_t* sgen, uint32_t tmem, volatile Ctl* ctl, uint32_t rank) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ci = 2 * k + (int)rank;
+  const int q0 = ci * 128;
+  const int nq = max(0, min(128, J.q_count - q0));
+  const int grow0 = J.q_begin + q0;
+  const int n_tiles = pair_tiles(J, k);
+  const int H = p.num_heads;
+  const bool leader = rank == 0;
+
+  if constexpr (!kCompute) {
+    if (warp == 8 || warp == 10) {
+      // ---------------------------------------------------------- TMA loads of this CTA's half
+      if (lane != 0) return;
+      const bool is_k = warp == 8;
+      const int ns = is_k ? kKStages : kVStages;
+      const uint32_t full0 = is_k ? kBKFull : kBVFull, empty0 = is_k ? kBKEmpty : kBVEmpty;
+      TraceAcc tr;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % ns;
+        const uint64_t w0 = tr.begin(p);
+        if (!wait_flag_geq(p, ready_flag(p, job, j % kRing), (uint32_t)j + 1)) { ctl->abort = 1; return; }
+        tr.end(p, w0);
+        if (j >= ns) {
+          // the stage is free once the pair's MMAs read it; its tile's ring slot is then consumed here
+          if (!wait_bar(p, bar_addr(sbase, empty0 + s), ((j / ns) - 1) & 1)) { ctl->abort = 1; return; }
+          fence_proxy_async_global();
+          red_release_gpu_add(consumed_flag(p, job, (j - ns) % kRing), 1u);
+        }
+        fence_proxy_async_global();
+        const uint32_t full = bar_addr(sbase, full0 + s);
+        const uint32_t full_leader = mapa_shared(full, 0u);
+        const int zb = (job * (int)kRing + j % kRing) * 4;   // first ring block of the tile
+        if (is_k) {
+          const uint32_t st = sbase + kKBase + s * kKStageBytes;
+          if (leader) mbar_arrive_expect_tx(full, 2 * kKStageBytes);     // both halves land on the leader's count
+          const int kt0 = J.t0 + 128 * j;
+          tma_load_3d_pair(st, &p.tm_ring64, 0, 64 * (int)rank, zb, full_leader);                    // K_nope lo | hi
+          tma_load_2d_pair(st + 2 * kAtom64, &p.tm_kr, kDc, block_row(J, (kt0 >> 6) + (int)rank), full_leader);
+          trace_stage(p, role, j, 0);
+        } else {
+          const uint32_t st = sbase + kVBase + s * kVStageBytes;
+          if (leader) mbar_arrive_expect_tx(full, 2 * kVStageBytes);
+          tma_load_3d_pair(st, &p.tm_ring1, 0, 0, zb + 2 + (int)rank, full_leader);                  // V columns
+          trace_stage(p, role, j, 1);
+        }
+      }
+      // the last stages: wait for their MMAs (this also takes the leader's last
+      // commits into this CTA's barriers before they are reset), release the slots
+      for (int j = max(0, n_tiles - ns); j < n_tiles; ++j) {
+        if (!wait_bar(p, bar_addr(sbase, empty0 + j % ns), (j / ns) & 1)) { ctl->abort = 1; return; }
+        fence_proxy_async_global();
+        red_release_gpu_add(consumed_flag(p, job, j % kRing), 1u);
+      }
+      if (is_k) {
+        trace_put(p, role, 3, tr.t);
+        trace_put(p, role, 7, (unsigned long long)n_tiles);
+      }
+    } else if (warp == 9 && leader) {
+      // ---------------------------------------------------------- MMA issue (leader)
+      if (lane != 0) return;
+      bool ok = wait_bar(p, bar_addr(sbase, kBQReady), 0);
+      tc_fence_after();
+      auto issue_s = [&](int j) {
+        const int sk = j % kKStages, b = j % kSBufs;
+        trace_stage(p, role, j, 2);
+        tc_fence_after();
+        const uint32_t kst = sbase + kKBase + sk * kKStageBytes;
+        const uint32_t d = tmem + kTmS + 128 * b;
+#pragma unroll
+        for (int kk = 0; kk < 12; ++kk)
+          mma2_ss(d, sdesc_sw128(sbase + kQBase + (kk >> 2) * kAtomQ + (kk & 3) * 32, 16, 1024),
+                  sdesc_sw128(kst + (kk >> 2) * kAtom64 + (kk & 3) * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+        mma2_commit_both(bar_addr(sbase, kBSFull + b));
+        mma2_commit_both(bar_addr(sbase, kBKEmpty + sk));
+        trace_stage(p, role, j, 3);
+      };
+      auto issue_pv = [&](int j) {
+        const int b = j % kSBufs, sv = j % kVStages;
+        trace_stage(p, role, j, 4);
+        if (!wait_bar(p, bar_addr(sbase, kBVFull + sv), (j / kVStages) & 1)) { ok = false; return; }
+        trace_stage(p, role, j, 5);
+        tc_fence_after();
+        const uint32_t v = sbase + kVBase + sv * kVStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma2_ts(tmem + kTmO, tmem + kTmS + 128 * b + kk * 8, sdesc_sw128(v + kk * 2048, kAtomQ, 1024), kIdescPV,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        mma2_commit_both(bar_addr(sbase, kBPvDone + b));
+        mma2_commit_both(bar_addr(sbase, kBVEmpty + sv));
+      };
+      // S(j) needs K stage j and its buffer free (PV(j-3) issued: MMAs run in
+      // order); PV(j) needs P(j) from both CTAs and V stage j.
+      int js = 0, jp = 0;
+      const uint64_t t_start = p.trace ? global_timer_ns() : 0;
+      uint64_t t_last = global_timer_ns();
+      uint32_t polls = 0;
+      while (ok && (js < n_tiles || jp < n_tiles)) {
+        bool progressed = false;
+        const bool want_s = js < n_tiles && js <= jp + (kSBufs - 1);
+        const bool want_p = jp < js;
+        const uint32_t hint = (want_s && want_p) ? 200u : 20000u;
+        if (want_s && mbar_try_wait_hint(bar_addr(sbase, kBKFull + js % kKStages), (js / kKStages) & 1,
+                                         want_p ? 0u : hint)) {
+          issue_s(js++);
+          progressed = true;
+        }
+        if (want_p && mbar_try_wait_hint(bar_addr(sbase, kBPFull + jp % kSBufs), (jp / kSBufs) & 1, hint)) {
+          issue_pv(jp++);
+          progressed = true;
+        }
+        if (progressed) {
+          polls = 0;
+        } else if ((++polls & 255u) == 0u) {
+          const uint64_t now = global_timer_ns();
+          if (polls == 256u) t_last = now;
+          else if (now - t_last > kWaitLimitNs) {
+            atomicOr(p.err, kErrTimeout);
+            ok = false;
+          }
+        }
+      }
+      if (!ok) ctl->abort = 1;
+      trace_put(p, role, 4, p.trace ? global_timer_ns() - t_start : 0);
+    }
+  } else {
+    if (warp < 4) {
+      // ---------------------------------------------------------- Q -> shared memory (warpgroup 0)
+      const int r = tid & 127;
+      const bool live = r < nq;
+      const int grow = grow0 + r;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_bf16 + ((int64_t)(live ? grow : 0) * H + J.head) * kDqk);
+      const int64_t delta = live ? (int64_t)__ldg(p.q_pos + grow) - J.rope_offset : 0;
+#pragma unroll 1
+      for (int part = 0; part < 3; ++part) {   // q_nope 0..63, q_nope 64..127, rotated q_rope
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 a = live ? __ldg(src + 8 * part + c) : make_uint4(0, 0, 0, 0);
+          uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+          if (part == 2) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float sn, cs;
+              rope_sincos(delta, p.rope_frac[4 * c + i], &sn, &cs);
+              const float x0 = __uint_as_float(w4[i] << 16), x1 = __uint_as_float(w4[i] & 0xFFFF0000u);
+              w4[i] = pack_bf16(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+            }
+          }
+          sts128(sbase + kQBase + part * kAtomQ + sw128_off(r, c), w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+      fence_proxy_async_smem();   // visible to the tensor core before the leader issues S
+      mbar_arrive_cluster(mapa_shared(bar_addr(sbase, kBQReady), 0u));
+    }
+    // ------------------------------------------------------------ softmax / epilogue (warps 0..7)
+    const int w = warp >> 2;           // key half
+    const int r = tid & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    float* xchg = reinterpret_cast<float*>(sgen + kXchgBase);   // [2 slots][2 halves][128] maxima, then sums
+    const int qtok = J.q_tok0 + q0 + r;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY, l_part = 0.f;
+    bool ok = true;
+    TraceAcc tr_s;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j % kSBufs, x = j & 1;
+      const uint64_t w0 = tr_s.begin(p);
+      if (ok && !wait_bar_warp(p, bar_addr(sbase, kBSFull + b), (j / kSBufs) & 1)) ok = false;
+      tr_s.end(p, w0);
+      if (tid == 0) trace_stage(p, role, j, 6);
+      tc_fence_after();
+      const uint32_t scol = tmem + lane_off + kTmS + 128 * b + 64 * w;
+      uint32_t v[64];
+      if (ok) tmem_ld64(scol, v);
+      const int kt0 = J.t0 + 128 * j + 64 * w;
+      const bool full = kt0 >= J.k_begin && kt0 + 63 < J.k_end && kt0 + 63 <= qtok;
+      float m8[8];
+      if (full) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(v[i]);
+#pragma unroll
+        for (int c = 8; c < 64; c += 2)
+          m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const int kt = kt0 + c;
+          const bool okc = kt >= J.k_begin && kt < J.k_end && kt <= qtok;
+          const float xv = okc ? __uint_as_float(v[c]) : -INFINITY;
+          v[c] = __float_as_uint(xv);
+          m8[c & 7] = fmaxf(m8[c & 7], xv);
+        }
+      }
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      // row maximum over both key halves; the barrier also orders both
+      // warpgroups' S loads before either overwrites S with P
+      xchg[(x * 2 + w) * 128 + r] = mx;
+      tc_fence_before();
+      named_bar_sync(1, 256);
+      tc_fence_after();
+      mx = fmaxf(mx, xchg[(x * 2 + (1 - w)) * 128 + r]);
+      const float m_tile = mx * sl2;
+      float alpha = 1.f;
+      const bool rescale = m_tile > m_used + kRescaleThreshold;
+      if (rescale) {
+        alpha = ex2(m_used - m_tile);   // 0 when m_used = -inf
+        m_used = m_tile;
+      }
+      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+      // P packed in place over the scores and stored in two 16-column halves
+      const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-mref, -mref);
+      uint64_t s4[4] = {0ull, 0ull, 0ull, 0ull};
+      const uint32_t pcol = tmem + lane_off + kTmS + 128 * b + 32 * w;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float x0, x1;
+        f2unpack(ffma2(f2pack(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])), sc2, nm2), x0, x1);
+        const float a = ex2(x0), bb = ex2(x1);
+        s4[c & 3] = fadd2(s4[c & 3], f2pack(a, bb));
+        v[c] = pack_bf16(a, bb);
+        if (c == 15 && ok) tmem_st16(pcol, v);
+      }
+      if (ok) tmem_st16(pcol + 16, v + 16);
+      float s8[4];
+      f2unpack(fadd2(s4[0], s4[1]), s8[0], s8[1]);
+      f2unpack(fadd2(s4[2], s4[3]), s8[2], s8[3]);
+      l_part = l_part * alpha + ((s8[0] + s8[2]) + (s8[1] + s8[3]));
+      if (j >= 1 && ok && __any_sync(0xffffffffu, rescale)) {
+        // O holds PV of tiles < j: PV(j-1) must be done before O is rescaled.
+        // PV(j-4) finished before S(j) did, so the barrier is at most one phase behind.
+        if (!wait_bar_warp(p, bar_addr(sbase, kBPvDone + (j - 1) % kSBufs), ((j - 1) / kSBufs) & 1)) ok = false;
+        tc_fence_after();
+        if (ok) {
+          const uint32_t ocol = tmem + lane_off + kTmO + 64 * w;
+#pragma unroll 1
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(ocol + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(ocol + cc * 32, o);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_cluster(mapa_shared(bar_addr(sbase, kBPFull + b), 0u));   // the leader issues PV for both CTAs
+      if (tid == 0) trace_stage(p, role, j, 7);
+    }
+    // every PV done: O is final, and the leader's last commits reached this CTA's barriers
+    if (ok && n_tiles > 0 &&
+        !wait_bar_warp(p, bar_addr(sbase, kBPvDone + (n_tiles - 1) % kSBufs), ((n_tiles - 1) / kSBufs) & 1))
+      ok = false;
+    if (tid == 0) trace_put(p, role, 6, tr_s.t);
+    xchg[(4 + w) * 128 + r] = l_part;
+    named_bar_sync(1, 256);
+    const float l_run = l_part + xchg[(4 + (1 - w)) * 128 + r];
+    if (!ok) { ctl->abort = 1; return; }
+    tc_fence_after();
+    // ---- epilogue: this warpgroup writes output columns 64w .. 64w+63 of this CTA's rows
+    const bool empty = n_tiles == 0 || !(l_run > 0.f);
+    const float inv_l = empty ? 0.f : 1.f / l_run;
+    const bool live = r < nq;
+    const int grow = grow0 + r;
+    const int64_t orow = J.slot < 0 ? (int64_t)grow : (int64_t)J.slot * p.slot_stride_rows + grow;
+    const uint32_t ocol = tmem + lane_off + kTmO + 64 * w;
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t o[32];
+      if (n_tiles > 0) tmem_ld32(ocol + cc * 32, o);
+      if (!live) continue;
+      const int col0 = 64 * w + 32 * cc;
+      if (J.slot < 0 && p.out_bf16) {
+        uint16_t* dst = static_cast<uint16_t*>(p.out) + (orow * H + J.head) * kDv + col0;
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          uint4 q;
+          q.x = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 0]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 1]) * inv_l);
+          q.y = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 2]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 3]) * inv_l);
+          q.z = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 4]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 5]) * inv_l);
+          q.w = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 6]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 7]) * inv_l);
+          *reinterpret_cast<uint4*>(dst + i) = q;
+        }
+      } else {
+        float* dst = (J.slot < 0 ? static_cast<float*>(p.out) : p.part_out) + (orow * H + J.head) * kDv + col0;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          float4 q;
+          q.x = empty ? 0.f : __uint_as_float(o[i + 0]) * inv_l;
+          q.y = empty ? 0.f : __uint_as_float(o[i + 1]) * inv_l;
+          q.z = empty ? 0.f : __uint_as_float(o[i + 2]) * inv_l;
+          q.w = empty ? 0.f : __uint_as_float(o[i + 3]) * inv_l;
+          *reinterpret_cast<float4*>(dst + i) = q;
+        }
+      }
+    }
+    if (live && w == 0) {
+      const float lse = empty ? -INFINITY : m_used * 0.69314718055994531f + logf(l_run);
+      (J.slot < 0 ? p.lse : p.part_lse)[orow * H + J.head] = lse;
+    }
+  }
+}
+
+// =============================================================== producer pair
+// Passes pi, pi + n_prod, ... of 256 tokens; CTA r up-projects tokens
+// 128r..128r+127 of a pass (ring tile 2 pass + r).  Warps: 8 loads this CTA's
+// latent rows, 10 its half of the head's kv_b_proj columns (each waits for the
+// stage to be free), 9 MMA (leader), 0-7 conversion: warpgroup 0 the K_nope
+// columns, warpgroup 1 the V columns of the CTA's tile.
+template <bool kCompute>
+__device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi, int role, uint32_t sbase,
+                             uint32_t tmem, volatile Ctl* ctl, uint32_t rank) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_pass = (J.n_tiles + 1) >> 1;
+  const int H = p.num_heads;
+  const int h = J.head;
+  const bool leader = rank == 0;
+  int my_passes = 0;
+  for (int pp = pi; pp < n_pass; pp += J.n_prod) ++my_passes;
+  if (my_passes == 0) return;
+
+  if constexpr (!kCompute) {
+    if (warp == 8 || warp == 10) {
+      if (lane != 0) return;
+      const bool rows = warp == 8;
+      int g = 0;
+      for (int n = 0; n < my_passes; ++n) {
+        const int pass = pi + n * J.n_prod;
+        const int row0 = block_row(J, (J.t0 >> 6) + 4 * pass) + 128 * (int)rank;
+        for (int kx = 0; kx < kDc / 64; ++kx, ++g) {
+          const int s = g % kPStages;
+          if (g >= kPStages && !wait_bar(p, bar_addr(sbase, kBProdEmpty + s), ((g / kPStages) - 1) & 1)) {
+            ctl->abort = 1;
+            return;
+          }
+          const uint32_t st = sbase + s * kPStageBytes;
+          const uint32_t full = bar_addr(sbase, kBProdFull + s);
+          const uint32_t full_leader = mapa_shared(full, 0u);
+          if (rows) {
+            if (leader) mbar_arrive_expect_tx(full, 2 * kPStageBytes);     // both CTAs' rows and columns
+            tma_load_2d_pair(st + kPC, &p.tm_kr128, 64 * kx, row0, full_leader);
+          } else {
+            const int blk = rank == 0 ? 2 * h : (H * kDnope + h * kDv) / 64;   // K_nope or V columns of head h
+            tma_load_3d_pair(st + kPW, &p.tm_w, 0, 64 * kx, blk, full_leader);
+          }
+        }
+      }
+      // the stages' last MMAs: take the leader's commits before the barriers are reset
+      for (int gx = max(0, g - kPStages); gx < g; ++gx)
+        if (!wait_bar(p, bar_addr(sbase, kBProdEmpty + gx % kPStages), (gx / kPStages) & 1)) {
+          ctl->abort = 1;
+          return;
+        }
+    } else if (warp == 9 && leader) {
+      if (lane != 0) return;
+      TraceAcc tr_op, tr_acc;
+      int g = 0;
+      for (int n = 0; n < my_passes; ++n) {
+        const int b = n & 1;
+        const uint64_t wa = tr_acc.begin(p);
+        if (n >= 2 && !wait_bar(p, bar_addr(sbase, kBAccEmpty + b), ((n >> 1) - 1) & 1)) { ctl->abort = 1; return; }
+        tr_acc.end(p, wa);
+        tc_fence_after();
+        for (int kx = 0; kx < kDc / 64; ++kx, ++g) {
+          const int s = g % kPStages;
+          const uint64_t w0 = tr_op.begin(p);
+          if (!wait_bar(p, bar_addr(sbase, kBProdFull + s), (g / kPStages) & 1)) { ctl->abort = 1; return; }
+          tr_op.end(p, w0);
+          tc_fence_after();
+          const uint32_t st = sbase + s * kPStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma2_ss(tmem + kTmAcc + 256 * b, sdesc_sw128(st + kPC + kk * 32, 16, 1024),
+                    sdesc_sw128(st + kPW + kk * 2048, kAtom64, 1024), kIdescUp, (kx | kk) ? 1u : 0u);
+          mma2_commit_both(bar_addr(sbase, kBProdEmpty + s));
+        }
+        mma2_commit_both(bar_addr(sbase, kBAccFull + b));
+      }
+      trace_put(p, role, 4, tr_op.t);
+      trace_put(p, role, 5, tr_acc.t);
+      trace_put(p, role, 7, (unsigned long long)my_passes);
+    }
+  } else {
+    // conversion: warpgroup wg converts accumulator columns 128 wg .. 128 wg + 127
+    // (wg 0: K_nope, wg 1: V) of this CTA's 128 tokens into ring blocks 2 wg, 2 wg + 1
+    const int wg = warp >> 2;
+    const int r = tid & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float oscale = p.out_scale;
+    const uint32_t stage_out = sbase + kPOutBase + wg * 2 * kAtomQ;   // [128 rows x 128 cols] bf16, 2 SW128 blocks
+    TraceAcc tr_c;
+    for (int n = 0; n < my_passes; ++n) {
+      const int pass = pi + n * J.n_prod;
+      const int b = n & 1;
+      const int t = 2 * pass + (int)rank;
+      const bool live_tile = t < J.n_tiles;
+      const int slot = t % kRing;
+      const int tok = J.t0 + 128 * t + r;
+      const bool valid = tok >= J.k_begin && tok < J.k_end;
+      if (!wait_bar_warp(p, bar_addr(sbase, kBAccFull + b), (n >> 1) & 1)) ctl->abort = 1;
+      tc_fence_after();
+      uint32_t pk[64];
+      if (live_tile && !ctl->abort) {
+        const uint32_t acc = tmem + lane_off + kTmAcc + 256 * b + 128 * wg;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t a[32];
+          tmem_ld32(acc + cc * 32, a);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[16 * cc + i] = valid ? pack_bf16(__uint_as_float(a[2 * i]) * oscale, __uint_as_float(a[2 * i + 1]) * oscale) : 0u;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(mapa_shared(bar_addr(sbase, kBAccEmpty + b), 0u));   // the accumulator may be reused
+      if (live_tile) {
+        const int zb = (job * (int)kRing + slot) * 4;
+        if (tid == 0 && !ctl->abort) {
+          const uint64_t w0 = tr_c.begin(p);
+          // the slot's previous occupant (tile t - ring) must be published and fully consumed
+          if (t >= (int)kRing &&
+              !(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - kRing + 1)) &&
+                wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - kRing))))
+            ctl->abort = 1;
+          tr_c.end(p, w0);
+          *consumed_flag(p, job, slot) = 0u;    // ordered before the release of `ready` below
+        }
+        // the slot may be written and the staging of the last pass is free; the
+        // stop decision is taken once for both warpgroups
+        if (named_bar_or(1, 256, ctl->abort != 0)) return;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq)
+            sts128(stage_out + (cc >> 1) * kAtomQ + sw128_off(r, (cc & 1) * 4 + gq), pk[16 * cc + 4 * gq],
+                   pk[16 * cc + 4 * gq + 1], pk[16 * cc + 4 * gq + 2], pk[16 * cc + 4 * gq + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(2 + wg, 128);
+        if (r == 0) {
+          tma_store_3d(&p.tm_ring, stage_out, 0, 0, zb + 2 * wg);   // K_nope lo | hi, or V lo | hi
+          bulk_commit();
+          bulk_wait0();
+        }
+        named_bar_sync(1, 256);                 // both halves of the tile have landed
+        if (tid == 0) {
+          fence_proxy_async_global();
+          __threadfence();
+          st_release_gpu(ready_flag(p, job, slot), (uint32_t)t + 1);
+        }
+      }
+      if (named_bar_or(1, 256, ctl->abort != 0)) return;
+    }
+    if (tid == 0) trace_put(p, role, 3, tr_c.t);
+  }
+}
+
+// The role loop of the pair, instantiated for the compute warps (0-7) and the
+// control warps (8-11).  Cluster rank 0 takes the next role from the queue
+// and writes it into both CTAs; every exit decision is made there, so both
+// CTAs run the same sequence of cluster barriers.
+template <bool kCompute>
+__device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, uint8_t* sgen, volatile Ctl* ctl,
+                                          uint32_t tmem, uint32_t rank) {
+  const int tid = threadIdx.x;
+  for (;;) {
+    if (kCompute && tid == 0 && rank == 0) {
+      const int g = (ctl->abort || aborted_global(p)) ? p.n_groups : (int)atomicAdd(p.queue, 1u);
+      ctl->group = g;
+      st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&ctl->group)), 1u), (uint32_t)g);
+    }
+    tc_fence_before();
+    cluster_sync_all();   // also: both CTAs are done with the previous role
+    tc_fence_after();
+    const int g = ctl->group;
+    if (g >= p.n_groups) break;
+    int lo = 0, hi = p.n_pieces - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.pieces[mid].group_begin <= g) lo = mid; else hi = mid - 1;
+    }
+    const Piece& P = p.pieces[lo];
+    const int n_pairs = (P.n_cons + 1) >> 1;
+    const int local = g - P.group_begin;
+    Job J;
+    J.req = P.req;
+    J.head = local / (P.n_prod + n_pairs);
+    J.q_begin = P.q_begin;
+    J.q_count = P.q_count;
+    J.q_tok0 = P.q_tok0;
+    J.k_begin = P.k_begin;
+    J.k_end = P.k_end;
+    J.t0 = P.k_begin & ~(kBlock - 1);
+    J.n_tiles = (P.k_end - J.t0 + 127) >> 7;
+    J.n_cons = P.n_cons;
+    J.n_prod = P.n_prod;
+    J.slot = P.slot;
+    J.row_block0 = P.row_block0;
+    J.rope_offset = P.rope_offset;
+    const int job = lo * p.num_heads + J.head;
+    const int gi = local - J.head * (P.n_prod + n_pairs);
+    const bool producer = gi < P.n_prod;
+    const int idx = producer ? gi : gi - P.n_prod;
+    const int slot = g * 2 + (int)rank;   // trace slot
+    if (kCompute && tid == 32) {
+      // fresh barriers for this role (every barrier is idle here)
+      for (uint32_t i = 0; i < kNumBars; ++i) {
+        mbar_inval(bar_addr(sbase, i));
+        uint32_t cnt = 1;
+        if (!producer && i == kBQReady) cnt = 256;
+        if (!producer && i >= kBPFull && i < kBPFull + kSBufs) cnt = 512;
+        if (producer && (i == kBAccEmpty || i == kBAccEmpty + 1)) cnt = 512;
+        mbar_init(bar_addr(sbase, i), cnt);
+      }
+      fence_mbar_init();
+    }
+    cluster_sync_all();   // the peer's barriers exist before anything reaches them
+    if (kCompute && p.trace && tid == 0) {
+      trace_put(p, slot, 0, global_timer_ns());
+      trace_put(p, slot, 2, ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)producer << 31) | (unsigned)job);
+    }
+    if (!ctl->abort) {
+      if (producer) run_producer<kCompute>(p, J, job, idx, slot, sbase, tmem, ctl, rank);
+      else run_consumer<kCompute>(p, J, job, idx, slot, sbase, sgen, tmem, ctl, rank);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (kCompute && p.trace && tid == 0) trace_put(p, slot, 1, global_timer_ns());
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fused2_prefill_kernel(const __grid_constant__ FusedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw_base);
+  volatile Ctl* ctl = reinterpret_cast<volatile Ctl*>(sgen + kBarBase + 8 * kNumBars);
+  const int tid = threadIdx.x;
+  const uint32_t rank = cluster_rank();
+
+  if (tid == 0) {
+    prefetch_tensormap(&p.tm_kr);
+    prefetch_tensormap(&p.tm_kr128);
+    prefetch_tensormap(&p.tm_w);
+    prefetch_tensormap(&p.tm_ring);
+    prefetch_tensormap(&p.tm_ring1);
+    prefetch_tensormap(&p.tm_ring64);
+  }
+  if (tid == 32) {
+    ctl->abort = 0;
+    for (uint32_t i = 0; i < kNumBars; ++i) mbar_init(bar_addr(sbase, i), 1);
+    fence_mbar_init();
+  }
+  cluster_sync_all();   // both CTAs run before the pair allocates TMEM or touches the other's memory
+  if ((tid >> 5) == 0) {
+    tmem_alloc2(sbase + kBarBase + 8 * kNumBars + offsetof(Ctl, tmem), 512);
+    tmem_relinquish2();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+
+  // Registers: 384 x 168 at launch; warpgroup 2 gives back 112 each (128 x 112),
+  // warpgroups 0 and 1 take 56 more each (256 x 56): the same total.
+  if ((tid >> 5) >= 8) {
+    setmaxnreg_dec<56>();
+    role_loop<false>(p, sbase, sgen, ctl, tmem, rank);
+  } else {
+    setmaxnreg_inc<224>();
+    role_loop<true>(p, sbase, sgen, ctl, tmem, rank);
+  }
+  tc_fence_before();
+  cluster_sync_all();   // neither CTA releases TMEM while the pair's MMAs could still use it
+  if ((tid >> 5) == 0) tmem_dealloc2(tmem, 512);
+}
+
+}  // namespace
+
+int fused2_smem_bytes() { return (int)kSmemBytes; }
+
+static cudaError_t configure2(int dev) {
+  static int configured_device = -1;
+  if (configured_device == dev) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fused2_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e == cudaSuccess) configured_device = dev;
+  return e;
+}
+
+static void cluster_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, cudaStream_t s) {
+  *cfg = {};
+  cfg->gridDim = dim3(grid);
+  cfg->blockDim = dim3(kThreads);
+  cfg->dynamicSmemBytes = kSmemBytes;
+  cfg->stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
+// Clusters of two CTAs, no cooperative attribute: a role only ever waits on
+// roles dequeued before it, which run on resident CTAs.
+cudaError_t launch_fused2(const FusedParams& p, int grid, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = configure2(dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  cluster_config(&cfg, attr, grid, s);
+  e = cudaLaunchKernelEx(&cfg, fused2_prefill_kernel, p);
+  count_launch();
+  return e;
+}
+
+cudaError_t fused2_grid_size(int* grid) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = configure2(dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  cluster_config(&cfg, attr, 2 * ((sms + 1) / 2), nullptr);
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, fused2_prefill_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  *grid = 2 * clusters;
+  return *grid > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
+}  // namespace mla

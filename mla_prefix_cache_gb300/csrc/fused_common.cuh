@@ -1,0 +1,97 @@
+// Device helpers shared by the fused prefill kernels (single-CTA roles in
+// fused.cu, CTA-pair roles in fused2.cu): per-CTA control word, optional
+// tracing, bounded waits that record an error instead of hanging, and the
+// ring and tile bookkeeping of a job.
+#pragma once
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+namespace fused_common {
+
+struct Ctl {
+  int group;       // written by cluster rank 0 into both CTAs
+  int abort;
+  uint32_t tmem;
+};
+
+// Optional tracing: per role slot (group * 2 + cluster rank) kTraceWords words
+//   [0] start ns  [1] end ns  [2] cta << 32 | producer << 31 | job
+//   [3] ns waiting on the other role kind (consumer: `ready` flags; producer: `consumed`)
+//   [4] ns the MMA thread waited for operands (kv_full / prod_full)
+//   [5] ns the MMA thread waited for softmax (p_full) or conversion (acc_empty)
+//   [6] ns softmax warp 0 waited for S (s_full)   [7] stages / passes
+struct TraceAcc {
+  unsigned long long t = 0;
+  __device__ __forceinline__ uint64_t begin(const FusedParams& p) const { return p.trace ? global_timer_ns() : 0; }
+  __device__ __forceinline__ void end(const FusedParams& p, uint64_t t0) { if (p.trace) t += global_timer_ns() - t0; }
+};
+__device__ __forceinline__ void trace_put(const FusedParams& p, int role, int word, unsigned long long v) {
+  if (p.trace) p.trace[(size_t)role * kTraceWords + word] = v;
+}
+// Per-stage timestamps of one role (after the per-role words): 8 words per stage
+//   [0] K load issued  [1] V load issued  [2] MMA saw K  [3] MMA issued S
+//   [4] MMA saw P  [5] MMA saw V (PV issued next)  [6] softmax saw S  [7] softmax published P
+__device__ __forceinline__ void trace_stage(const FusedParams& p, int role, int stage, int word) {
+  if (p.trace && role == p.trace_detail_role && stage < 4096)
+    p.trace[(size_t)p.n_groups * 2 * kTraceWords + (size_t)stage * 8 + word] = global_timer_ns();
+}
+
+__device__ __forceinline__ bool aborted_global(const FusedParams& p) { return ld_volatile_u32(p.err) != 0u; }
+
+// Bounded mbarrier wait; on timeout records the error and returns false.
+__device__ __forceinline__ bool wait_bar(const FusedParams& p, uint32_t bar, uint32_t parity) {
+  if (mbar_wait(bar, parity)) return true;
+  atomicOr(p.err, kErrTimeout);
+  return false;
+}
+
+// Same, decided once for the whole warp (every lane must call it together), so a
+// timeout never splits a warp before a warp-collective tcgen05.ld/st.
+__device__ __forceinline__ bool wait_bar_warp(const FusedParams& p, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait_bar(p, bar, parity));
+}
+
+// Bounded wait until *flag >= target (acquire).  Gives up early when another
+// CTA has already recorded an error.
+__device__ inline bool wait_flag_geq(const FusedParams& p, const uint32_t* flag, uint32_t target) {
+  if (ld_acquire_gpu(flag) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire_gpu(flag) < target) {
+    if (global_timer_ns() - t0 > kWaitLimitNs || aborted_global(p)) {
+      atomicOr(p.err, kErrTimeout);
+      return false;
+    }
+    __nanosleep(32);
+  }
+  return true;
+}
+
+// Number of 128-key tiles consumer `ci` (queries 128 ci .. 128 ci + 127 of the
+// request) of job `J` attends to (causal clip).
+__device__ __forceinline__ int consumer_tiles(const Job& J, int ci) {
+  const int q0 = ci * 128;
+  const int nq = min(128, J.q_count - q0);
+  if (nq <= 0) return 0;
+  const int last_tok = J.q_tok0 + q0 + nq - 1;
+  const int k_end = min(J.k_end, last_tok + 1);
+  if (k_end <= J.k_begin) return 0;
+  return (k_end - J.t0 + 127) >> 7;
+}
+
+__device__ __forceinline__ uint32_t* ready_flag(const FusedParams& p, int job, int slot) {
+  return p.flags + (size_t)job * (2 * (size_t)kRingDepth) + slot;
+}
+__device__ __forceinline__ uint32_t* consumed_flag(const FusedParams& p, int job, int slot) {
+  return p.flags + (size_t)job * (2 * (size_t)kRingDepth) + kRingDepth + slot;
+}
+
+// Row of logical block `lb` of the job's request in the gathered rows (the
+// gather pass copied the request's blocks in logical order from row_block0 on;
+// it also reported any bad block id).  Rows past the request's blocks are
+// read but belong to keys outside the job's range, which are masked.
+__device__ __forceinline__ int block_row(const Job& J, int lb) { return (J.row_block0 + lb) * kBlock; }
+
+}  // namespace fused_common
+}  // namespace mla

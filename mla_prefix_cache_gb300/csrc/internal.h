@@ -95,6 +95,7 @@ struct FusedParams {
   CUtensorMap tm_w;      // bf16 kv_b_proj as [H*4 blocks][512 rows][64 cols], box 64 x 64 x 2
   CUtensorMap tm_ring;   // bf16 ring as [jobs*ring*4 blocks][128 rows][64 cols], box 64 x 128 x 2
   CUtensorMap tm_ring1;  // same ring, box 64 x 128 x 1 (one block: half of a paired consumer's stage)
+  CUtensorMap tm_ring64; // same ring, box 64 x 64 x 2 (64 keys of K_nope lo | hi: a CTA pair's half tile)
   const uint16_t* q_bf16;  // q [T_q][H][192]
   uint32_t* err;
   uint32_t* queue;       // role-group counter
@@ -131,6 +132,11 @@ cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t s);
 // (2 when `pair`, else 1); 0 clusters -> error.
 cudaError_t fused_grid_size(int* grid, int pair);
 int fused_smem_bytes();
+// CTA-pair kernel (fused2.cu): pieces carry n_prod producer *pair* roles and
+// group_begin counts pair roles (n_prod + ceil(n_cons / 2) per head).
+cudaError_t launch_fused2(const FusedParams& p, int grid, cudaStream_t s);
+cudaError_t fused2_grid_size(int* grid);
+int fused2_smem_bytes();
 
 // Kernel launchers (return cudaError_t of the launch).
 cudaError_t launch_merge_slots(const MergeParams& p, cudaStream_t s);
