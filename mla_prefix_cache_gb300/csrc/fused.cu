@@ -65,7 +65,7 @@ static_assert(kSmemBytes <= 232448, "more than 227 KB of shared memory per CTA")
 
 // consumer barriers
 constexpr uint32_t kBQReady = 0, kBKFull = 1, kBKEmpty = 4, kBVFull = 7, kBVEmpty = 9, kBSFull = 11, kBPFull = 13,
-                   kBPvDone = 15 /* 2: PV of even / odd tiles */, kBKRel = 17, kBVRel = 20;
+                   kBPvDone = 15 /* 2: PV of even / odd tiles */;
 // producer barriers
 constexpr uint32_t kBProdFull = 0, kBProdEmpty = 2, kBAccFull = 4, kBAccEmpty = 5;
 constexpr uint32_t kNumBars = 24;
@@ -103,7 +103,8 @@ __device__ __forceinline__ int consumers_needing_tile(const Job& J, int t, int p
 // =============================================================== consumer
 // One 128-query tile of a job.  Warps: 0-7 softmax (warpgroup w owns key
 // columns 64w..64w+63 of every row; warpgroup 0 first loads and rotates Q into
-// TMEM), 8 K loader, 9 MMA issuer, 10 V loader, 11 releases ring slots.
+// TMEM), 8 K loader, 9 MMA issuer, 10 V loader (the loaders also release the
+// ring slots of the tiles that leave their stages).
 // `paired`: this CTA and its cluster peer own query tiles ci and ci^1 of the
 // same job and run the same key tiles; each CTA loads half of every K and V
 // stage (block `rank`) with multicast into both, and both MMAs must release a
@@ -120,7 +121,30 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
   const int H = p.num_heads;
 
   if constexpr (!kCompute) {
-  if (warp == 8 || warp == 10) {
+  if (warp == 11 && !paired) {
+    // ------------------------------------------------------------ second K issuer
+    // K_nope hi and k_rope of every stage, so the K stage's boxes leave from
+    // two warps (the per-SM TMA rate grows with the number of issuing warps);
+    // warp 8 arms the stage's barrier and loads K_nope lo.
+    if (lane != 0) return;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j % kKStages;
+      if (!wait_flag_geq(p, ready_flag(p, job, j % kRing), (uint32_t)j + 1)) { ctl->abort = 1; return; }
+      if (j >= kKStages && !wait_bar(p, bar_addr(sbase, kBKEmpty + s), ((j / kKStages) - 1) & 1)) {
+        ctl->abort = 1;
+        return;
+      }
+      fence_proxy_async_global();
+      const uint32_t st = sbase + kKBase + s * kKStageBytes;
+      const uint32_t full = bar_addr(sbase, kBKFull + s);
+      const int zb = (job * (int)kRing + j % kRing) * 4;
+      tma_load_3d(st + kAtomQ, &p.tm_ring1, 0, 0, zb + 1, full);                               // K_nope hi
+      tma_load_2d(st + 2 * kAtomQ, &p.tm_kr128, kDc, block_row(J, (J.t0 + 128 * j) >> 6), full);   // k_rope
+    }
+    // the last stages' MMAs: their commits land before the barriers are reset
+    for (int j = max(0, n_tiles - kKStages); j < n_tiles; ++j)
+      if (!wait_bar(p, bar_addr(sbase, kBKEmpty + j % kKStages), (j / kKStages) & 1)) { ctl->abort = 1; return; }
+  } else if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ TMA loads (K or V)
     if (lane != 0) return;
     const bool is_k = warp == 8;
@@ -134,9 +158,8 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
       const uint64_t w0 = tr.begin(p);
       if (!wait_flag_geq(p, ready_flag(p, job, j % kRing), (uint32_t)j + 1)) { ctl->abort = 1; return; }
       tr.end(p, w0);
-      // stage reusable: its MMA finished reading it, and the release warp has seen its previous load land
-      if (j >= ns && !(wait_bar(p, bar_addr(sbase, (is_k ? kBKEmpty : kBVEmpty) + s), ((j / ns) - 1) & 1) &&
-                       wait_bar(p, bar_addr(sbase, (is_k ? kBKRel : kBVRel) + s), ((j / ns) - 1) & 1))) {
+      // stage reusable: the MMAs reading its previous tile are done
+      if (j >= ns && !wait_bar(p, bar_addr(sbase, (is_k ? kBKEmpty : kBVEmpty) + s), ((j / ns) - 1) & 1)) {
         ctl->abort = 1;
         return;
       }
@@ -153,8 +176,8 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
           tma_load_2d_mc(st + 2 * kAtomQ + h * kAtom64, &p.tm_kr, kDc, block_row(J, (kt0 >> 6) + h), full,
                          kBoth);                                                             // k_rope, 64 keys
         } else {
-          tma_load_3d(st, &p.tm_ring, 0, 0, zb, full);                      // K_nope, 32 KB
-          tma_load_2d(st + 2 * kAtomQ, &p.tm_kr128, kDc, block_row(J, kt0 >> 6), full);   // k_rope, 16 KB
+          tma_load_3d(st, &p.tm_ring1, 0, 0, zb, full);                     // K_nope lo (warp 11: hi, k_rope)
+          (void)kt0;
         }
         trace_stage(p, role, j, 0);
       } else {
@@ -167,23 +190,24 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
           tma_load_3d(st, &p.tm_ring, 0, 0, zb + 2, full);                  // V, 32 KB
         trace_stage(p, role, j, 1);
       }
+      // The tile that left the stage is consumed here: add one to its slot's
+      // count (a slot is free again after 2 per consumer).  Done after the
+      // next load is issued, so the release is off the path to the MMA.
+      if (j >= ns) {
+        fence_proxy_async_global();
+        red_release_gpu_add(consumed_flag(p, job, (j - ns) % kRing), 1u);
+      }
+    }
+    // the last stages: once their MMAs are done, release their tiles' slots
+    // (this also takes the last commits' arrivals before the barriers are reset)
+    const int ns = is_k ? kKStages : kVStages;
+    for (int j = max(0, n_tiles - ns); j < n_tiles; ++j) {
+      if (!wait_bar(p, bar_addr(sbase, (is_k ? kBKEmpty : kBVEmpty) + j % ns), (j / ns) & 1)) { ctl->abort = 1; return; }
+      fence_proxy_async_global();
+      red_release_gpu_add(consumed_flag(p, job, j % kRing), 1u);
     }
     if (is_k) trace_put(p, role, 3, tr.t);
     if (is_k) trace_put(p, role, 7, (unsigned long long)n_tiles);
-  } else if (warp == 11) {
-    // ------------------------------------------------------------ ring-slot release
-    // lane 0 watches K loads land, lane 1 V loads; each adds one to the slot's
-    // consumed count (a tile is released after 2 per consumer) and re-arms its
-    // own loader, so K loads never wait for V loads or the other way round.
-    if (lane > 1) return;
-    const bool is_k = lane == 0;
-    const int ns = is_k ? kKStages : kVStages;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!wait_bar(p, bar_addr(sbase, (is_k ? kBKFull : kBVFull) + j % ns), (j / ns) & 1)) { ctl->abort = 1; return; }
-      fence_proxy_async_global();
-      red_release_gpu_add(consumed_flag(p, job, j % kRing), 1u);
-      mbar_arrive(bar_addr(sbase, (is_k ? kBKRel : kBVRel) + j % ns));
-    }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issue
     if (lane != 0) return;
