@@ -66,19 +66,19 @@ constexpr uint32_t kSmemBytes = kBarBase + 8 * kNumBars + 64 + 1024;
 static_assert(kSmemBytes <= 232448, "more than 227 KB of shared memory per CTA");
 
 // consumer barriers ("leader": only the leader's copy is used, it counts both CTAs)
-constexpr uint32_t kBQReady = 0;          // leader, 256 arrivals (128 Q rows per CTA)
+constexpr uint32_t kBQReady = 0;          // leader, 8 arrivals (the 4 Q-loading warps of each CTA)
 constexpr uint32_t kBKFull = 1;           // leader, 4: both halves of a K stage landed
 constexpr uint32_t kBKEmpty = 5;          // both, 4: the MMAs reading a K stage are done
 constexpr uint32_t kBVFull = 9;           // leader, 4
 constexpr uint32_t kBVEmpty = 13;         // both, 4
 constexpr uint32_t kBSFull = 17;          // both, 3: S of a buffer computed
-constexpr uint32_t kBPFull = 20;          // leader, 3: P of a buffer written, 512 arrivals
+constexpr uint32_t kBPFull = 20;          // leader, 3: P of a buffer written, one arrival per softmax warp
 constexpr uint32_t kBPvDone = 23;         // both, 3: PV reading a buffer done
 // producer barriers
 constexpr uint32_t kBProdFull = 0;        // leader, 4
 constexpr uint32_t kBProdEmpty = 4;       // both, 4
 constexpr uint32_t kBAccFull = 8;         // both, 2
-constexpr uint32_t kBAccEmpty = 10;       // leader, 2: 512 arrivals
+constexpr uint32_t kBAccEmpty = 10;       // leader, 2: one arrival per conversion warp
 
 // TMEM columns (per CTA)
 constexpr uint32_t kTmO = 0;              // consumer: O [128 x 128] fp32
@@ -266,7 +266,8 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
         }
       }
       fence_proxy_async_smem();   // visible to the tensor core before the leader issues S
-      mbar_arrive_cluster(mapa_shared(bar_addr(sbase, kBQReady), 0u));
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_addr(sbase, kBQReady), 0u));   // one arrival per warp
     }
     // ------------------------------------------------------------ softmax / epilogue (warps 0..7)
     const int w = warp >> 2;           // key half
@@ -362,7 +363,8 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_cluster(mapa_shared(bar_addr(sbase, kBPFull + b), 0u));   // the leader issues PV for both CTAs
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(bar_addr(sbase, kBPFull + b), 0u));   // leader issues PV
       if (tid == 0) trace_stage(p, role, j, 7);
     }
     // every PV done: O is final, and the leader's last commits reached this CTA's barriers
@@ -530,7 +532,8 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
         }
       }
       tc_fence_before();
-      mbar_arrive_cluster(mapa_shared(bar_addr(sbase, kBAccEmpty + b), 0u));   // the accumulator may be reused
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(bar_addr(sbase, kBAccEmpty + b), 0u));   // accumulator free
       if (live_tile) {
         const int zb = (job * (int)kRing + slot) * 4;
         if (tid == 0 && !ctl->abort) {
@@ -624,9 +627,10 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
       for (uint32_t i = 0; i < kNumBars; ++i) {
         mbar_inval(bar_addr(sbase, i));
         uint32_t cnt = 1;
-        if (!producer && i == kBQReady) cnt = 256;
-        if (!producer && i >= kBPFull && i < kBPFull + kSBufs) cnt = 512;
-        if (producer && (i == kBAccEmpty || i == kBAccEmpty + 1)) cnt = 512;
+        // barriers the leader waits on count one arrival per warp of both CTAs
+        if (!producer && i == kBQReady) cnt = 2 * 4;
+        if (!producer && i >= kBPFull && i < kBPFull + kSBufs) cnt = 2 * 8;
+        if (producer && (i == kBAccEmpty || i == kBAccEmpty + 1)) cnt = 2 * 8;
         mbar_init(bar_addr(sbase, i), cnt);
       }
       fence_mbar_init();

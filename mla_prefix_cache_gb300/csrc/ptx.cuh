@@ -443,6 +443,14 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* map, 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
+// Relaxed arrive on a barrier of either CTA of the cluster: a thread
+// synchronisation without a cluster-scope release of prior memory operations
+// (which costs the arriving thread about 0.7 us).  For signalling tensor
+// memory written or read by tcgen05.st / tcgen05.ld, whose ordering comes
+// from tcgen05.wait::st / ld and tcgen05.fence::before_thread_sync.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
 
 // Packed fp32 pairs (sm_100 family): one instruction operates on two floats
 // held in a 64-bit register pair, rounding each lane exactly like the scalar
