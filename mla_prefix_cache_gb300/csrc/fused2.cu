@@ -172,72 +172,55 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
         trace_put(p, role, 3, tr.t);
         trace_put(p, role, 7, (unsigned long long)n_tiles);
       }
-    } else if (warp == 9 && leader) {
+    } else if ((warp == 9 || warp == 11) && leader) {
       // ---------------------------------------------------------- MMA issue (leader)
+      // Two issuing threads, so neither kind of MMA waits behind the other in
+      // a blocked issue: warp 9 issues S(j) once K stage j has landed and its
+      // score buffer is free (PV(j-3) complete: the threads' MMAs are not
+      // ordered with each other), warp 11 issues PV(j) once P(j) of both CTAs
+      // and V stage j are there.
       if (lane != 0) return;
-      bool ok = wait_bar(p, bar_addr(sbase, kBQReady), 0);
+      const bool s_side = warp == 9;
+      if (!wait_bar(p, bar_addr(sbase, kBQReady), 0)) { ctl->abort = 1; return; }
       tc_fence_after();
-      auto issue_s = [&](int j) {
-        const int sk = j % kKStages, b = j % kSBufs;
-        trace_stage(p, role, j, 2);
-        tc_fence_after();
-        const uint32_t kst = sbase + kKBase + sk * kKStageBytes;
-        const uint32_t d = tmem + kTmS + 128 * b;
-#pragma unroll
-        for (int kk = 0; kk < 12; ++kk)
-          mma2_ss(d, sdesc_sw128(sbase + kQBase + (kk >> 2) * kAtomQ + (kk & 3) * 32, 16, 1024),
-                  sdesc_sw128(kst + (kk >> 2) * kAtom64 + (kk & 3) * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-        mma2_commit_both(bar_addr(sbase, kBSFull + b));
-        mma2_commit_both(bar_addr(sbase, kBKEmpty + sk));
-        trace_stage(p, role, j, 3);
-      };
-      auto issue_pv = [&](int j) {
-        const int b = j % kSBufs, sv = j % kVStages;
-        trace_stage(p, role, j, 4);
-        if (!wait_bar(p, bar_addr(sbase, kBVFull + sv), (j / kVStages) & 1)) { ok = false; return; }
-        trace_stage(p, role, j, 5);
-        tc_fence_after();
-        const uint32_t v = sbase + kVBase + sv * kVStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma2_ts(tmem + kTmO, tmem + kTmS + 128 * b + kk * 8, sdesc_sw128(v + kk * 2048, kAtomQ, 1024), kIdescPV,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        mma2_commit_both(bar_addr(sbase, kBPvDone + b));
-        mma2_commit_both(bar_addr(sbase, kBVEmpty + sv));
-      };
-      // S(j) needs K stage j and its buffer free (PV(j-3) issued: MMAs run in
-      // order); PV(j) needs P(j) from both CTAs and V stage j.
-      int js = 0, jp = 0;
       const uint64_t t_start = p.trace ? global_timer_ns() : 0;
-      uint64_t t_last = global_timer_ns();
-      uint32_t polls = 0;
-      while (ok && (js < n_tiles || jp < n_tiles)) {
-        bool progressed = false;
-        const bool want_s = js < n_tiles && js <= jp + (kSBufs - 1);
-        const bool want_p = jp < js;
-        const uint32_t hint = (want_s && want_p) ? 200u : 20000u;
-        if (want_s && mbar_try_wait_hint(bar_addr(sbase, kBKFull + js % kKStages), (js / kKStages) & 1,
-                                         want_p ? 0u : hint)) {
-          issue_s(js++);
-          progressed = true;
-        }
-        if (want_p && mbar_try_wait_hint(bar_addr(sbase, kBPFull + jp % kSBufs), (jp / kSBufs) & 1, hint)) {
-          issue_pv(jp++);
-          progressed = true;
-        }
-        if (progressed) {
-          polls = 0;
-        } else if ((++polls & 255u) == 0u) {
-          const uint64_t now = global_timer_ns();
-          if (polls == 256u) t_last = now;
-          else if (now - t_last > kWaitLimitNs) {
-            atomicOr(p.err, kErrTimeout);
-            ok = false;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int b = j % kSBufs;
+        if (s_side) {
+          const int sk = j % kKStages;
+          if (!wait_bar(p, bar_addr(sbase, kBKFull + sk), (j / kKStages) & 1)) { ctl->abort = 1; return; }
+          if (j >= kSBufs && !wait_bar(p, bar_addr(sbase, kBPvDone + b), ((j / kSBufs) - 1) & 1)) {
+            ctl->abort = 1;
+            return;
           }
+          trace_stage(p, role, j, 2);
+          tc_fence_after();
+          const uint32_t kst = sbase + kKBase + sk * kKStageBytes;
+          const uint32_t d = tmem + kTmS + 128 * b;
+#pragma unroll
+          for (int kk = 0; kk < 12; ++kk)
+            mma2_ss(d, sdesc_sw128(sbase + kQBase + (kk >> 2) * kAtomQ + (kk & 3) * 32, 16, 1024),
+                    sdesc_sw128(kst + (kk >> 2) * kAtom64 + (kk & 3) * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+          mma2_commit_both(bar_addr(sbase, kBSFull + b));
+          mma2_commit_both(bar_addr(sbase, kBKEmpty + sk));
+          trace_stage(p, role, j, 3);
+        } else {
+          const int sv = j % kVStages;
+          if (!wait_bar(p, bar_addr(sbase, kBPFull + b), (j / kSBufs) & 1)) { ctl->abort = 1; return; }
+          trace_stage(p, role, j, 4);
+          if (!wait_bar(p, bar_addr(sbase, kBVFull + sv), (j / kVStages) & 1)) { ctl->abort = 1; return; }
+          trace_stage(p, role, j, 5);
+          tc_fence_after();
+          const uint32_t v = sbase + kVBase + sv * kVStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma2_ts(tmem + kTmO, tmem + kTmS + 128 * b + kk * 8, sdesc_sw128(v + kk * 2048, kAtomQ, 1024), kIdescPV,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+          mma2_commit_both(bar_addr(sbase, kBPvDone + b));
+          mma2_commit_both(bar_addr(sbase, kBVEmpty + sv));
         }
       }
-      if (!ok) ctl->abort = 1;
-      trace_put(p, role, 4, p.trace ? global_timer_ns() - t_start : 0);
+      if (s_side) trace_put(p, role, 4, p.trace ? global_timer_ns() - t_start : 0);
     }
   } else {
     if (warp < 4) {
