@@ -159,7 +159,9 @@ static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const i
   fp->max_slots = 0;
   fp->total_q = splits.total_q;
   const int max_keys = std::max(chunk, env_int("MLA_MAX_PIECE_KEYS", 16384));
-  const int n_prod_cfg = std::max(1, env_int("MLA_PRODUCERS", 4));
+  // producer CTAs per job (the CTA-pair kernel runs them as pairs): enough to
+  // keep a head's 16-32 consumers fed without idling on full rings
+  const int n_prod_cfg = std::max(1, env_int("MLA_PRODUCERS", 6));
   size_t si = 0;
   for (int r = 0; r < num_reqs; ++r) {
     const int E = cu_q[r + 1] - cu_q[r];
@@ -395,9 +397,10 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   // measured no faster, the consumers being bound by their softmax chain, not
   // by L2.  Single CTAs are also the fallback when no cluster of two fits.
   int pair = env_int("MLA_PAIR", 0) != 0 ? 1 : 0;
-  // MLA_CTA_PAIR=1: the CTA-pair kernel (fused2.cu), every role run by a
-  // cluster of two CTAs with M = 256 MMAs.
-  const bool v2 = env_int("MLA_CTA_PAIR", 0) != 0;
+  // The CTA-pair kernel (fused2.cu, every role run by a cluster of two CTAs
+  // with M = 256 MMAs) by default; MLA_CTA_PAIR=0 selects the single-CTA
+  // kernel (fused.cu).
+  const bool v2 = env_int("MLA_CTA_PAIR", 1) != 0;
   int grid = 0;
   int st = v2 ? cuda_status(fused2_grid_size(&grid)) : cuda_status(fused_grid_size(&grid, pair));
   if (st != MLA_OK && !v2 && pair) {

@@ -249,13 +249,18 @@ def test_prefill_small_workspace_runs_in_several_launches(api):
         dw.run(workspace=tiny_ws)
 
 
+@pytest.mark.parametrize("kernel", [
+    {"MLA_CTA_PAIR": "0", "MLA_PAIR": "0"},   # single-CTA kernel
+    {"MLA_CTA_PAIR": "0", "MLA_PAIR": "1"},   # single-CTA kernel, consumer pairs sharing K/V loads by multicast
+], ids=["single", "multicast"])
 @pytest.mark.parametrize("case", [
     dict(H=4, ctx=[700], ext=[300], chunk=256, doc=None),     # 3 query tiles: one pair and one single consumer
     dict(H=2, ctx=[256], ext=[200], chunk=64, doc=64),        # relocated documents, partial states + merge
 ], ids=["ragged", "docs"])
-def test_prefill_consumer_pairs(api, case, monkeypatch):
-    """Clusters of two CTAs whose consumer roles share K/V loads by multicast."""
-    monkeypatch.setenv("MLA_PAIR", "1")
+def test_prefill_other_kernels(api, case, kernel, monkeypatch):
+    """The kernel variants other than the default (CTA-pair) one."""
+    for k, v in kernel.items():
+        monkeypatch.setenv(k, v)
     wl = W.make_workload("pair", case["H"], case["ctx"], case["ext"], chunk=case["chunk"], seed=31,
                          doc_len=case["doc"])
     run_and_compare(api, wl)
