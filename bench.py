@@ -193,9 +193,14 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 
+def fused_kernel_name():
+    """The fused kernel mla_prefill_ctx launches (the library reads MLA_CTA_PAIR)."""
+    return "fused_prefill_kernel" if os.environ.get("MLA_CTA_PAIR", "1") == "0" else "fused2_prefill_kernel"
+
+
 def kernel_sha():
     h = hashlib.sha256()
-    for f in ("fused.cu", "ptx.cuh", "internal.h"):
+    for f in ("fused.cu", "fused2.cu", "fused_common.cuh", "ptx.cuh", "internal.h"):
         with open(os.path.join(ROOT, "mla_prefix_cache_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -210,7 +215,7 @@ def measured_traffic(workload_name):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload_name)
-    if not e or e.get("kernel_sha") != kernel_sha():
+    if not e or e.get("kernel_sha") != kernel_sha() or e.get("kernel") != fused_kernel_name():
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -408,7 +413,7 @@ def run_ours(args):
         "frac_of_bf16_peak": value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "fused_prefill_kernel",
+                     "kernel": fused_kernel_name(),
                      "peak_source": f"bf16_tflops (burst) of {source} peaks",
                      "kernel_ms": k_ms, "note": "achieved = algorithmic FLOPs of the step / fused-kernel event time"},
         "gpu_launches": int(launches),
