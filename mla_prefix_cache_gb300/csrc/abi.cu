@@ -229,17 +229,20 @@ struct FusedWs {
   size_t err_off = 0, queue_off = 4, flags_off = 256, flags_bytes = 0, ring_off = 0, gath_off = 0, lse_off = 0,
          out_off = 0, total = 0;
   int pieces_per_launch = 0;
+  int ring_depth = 0;
 };
 
-// Workspace of the fused path when `ppl` pieces run per launch: header (error
-// word, role queue), per-job ring flags, per-job K/V rings, partial states.
-static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads, int ppl) {
+// Workspace of the fused path when `ppl` pieces run per launch with rings of
+// `depth` tiles: header (error word, role queue), per-job ring flags, per-job
+// K/V rings, the gathered rows, partial states.
+static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads, int ppl, int depth) {
   FusedWs w;
   w.pieces_per_launch = ppl;
+  w.ring_depth = depth;
   const size_t jobs = (size_t)ppl * num_heads;
-  w.flags_bytes = jobs * 2 * kRingDepth * sizeof(uint32_t);
+  w.flags_bytes = jobs * 2 * (size_t)depth * sizeof(uint32_t);
   w.ring_off = up256(w.flags_off + w.flags_bytes);
-  const size_t ring_bytes = jobs * kRingDepth * 128 * 256 * sizeof(uint16_t);
+  const size_t ring_bytes = jobs * (size_t)depth * 128 * 256 * sizeof(uint16_t);
   const size_t rows = (size_t)fp.max_slots * (size_t)fp.total_q * (size_t)num_heads;
   w.gath_off = up256(w.ring_off + ring_bytes);
   const size_t gath_bytes = (size_t)fp.gather_blocks * kBlock * kRowBytesBf16;
@@ -249,19 +252,38 @@ static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads, int ppl) {
   return w;
 }
 
-// Preferred layout: every piece in one launch, up to kMaxPieces and a 4 GiB ring.
-static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads) {
-  const size_t per_piece = (size_t)num_heads * kRingDepth * 128 * 256 * sizeof(uint16_t);
-  const int cap = (int)std::max<size_t>(1, ((size_t)4 << 30) / per_piece);
-  const int ppl = std::max(1, std::min({(int)fp.pieces.size(), kMaxPieces, cap}));
-  return fused_ws_layout(fp, num_heads, ppl);
+// Preferred layout: the deepest rings (a head's consumers start over a spread
+// of tiles; a shallow ring makes the earliest wait for the latest), every
+// piece in one launch, up to kMaxPieces and 24 GiB of rings.
+// MLA_RING_DEPTH lowers the deepest ring (a tuning knob; a power of two >= 4).
+static int max_ring_depth() {
+  int d = kRingDepth;
+  const int cap = env_int("MLA_RING_DEPTH", kRingDepth);
+  while (d > 4 && d > cap) d /= 2;
+  return d;
 }
 
-// Largest pieces-per-launch whose layout fits in `bytes` (0 if not even one).
-static int fused_pieces_fitting(const FusedPlan& fp, int num_heads, size_t bytes) {
-  int hi = fused_ws_layout(fp, num_heads).pieces_per_launch;
-  while (hi >= 1 && fused_ws_layout(fp, num_heads, hi).total > bytes) hi = hi > 8 ? hi - hi / 8 : hi - 1;
-  return std::max(hi, 0);
+static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads) {
+  const int depth = max_ring_depth();
+  const size_t per_piece = (size_t)num_heads * depth * 128 * 256 * sizeof(uint16_t);
+  const int cap = (int)std::max<size_t>(1, ((size_t)24 << 30) / per_piece);
+  const int ppl = std::max(1, std::min({(int)fp.pieces.size(), kMaxPieces, cap}));
+  return fused_ws_layout(fp, num_heads, ppl, depth);
+}
+
+// Layout for a workspace of `bytes`: the preferred one when it fits, else the
+// most pieces per launch with the deepest ring that fits; pieces_per_launch 0
+// when not even one piece with a 4-tile ring fits.
+static FusedWs fused_ws_fitting(const FusedPlan& fp, int num_heads, size_t bytes) {
+  const int top = fused_ws_layout(fp, num_heads).pieces_per_launch;
+  for (int depth = max_ring_depth(); depth >= 4; depth /= 2) {
+    int hi = top;
+    while (hi >= 1 && fused_ws_layout(fp, num_heads, hi, depth).total > bytes) hi = hi > 8 ? hi - hi / 8 : hi - 1;
+    if (hi >= 1) return fused_ws_layout(fp, num_heads, hi, depth);
+  }
+  FusedWs none;
+  none.pieces_per_launch = 0;
+  return none;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -359,7 +381,7 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   {
     // ring: per job and slot four contiguous [128 x 64] blocks K_nope lo, K_nope hi, V lo, V hi
     const uint64_t jobs = (uint64_t)std::max(fw.pieces_per_launch, 1) * H;
-    const uint64_t d[3] = {64, 128, jobs * kRingDepth * 4};
+    const uint64_t d[3] = {64, 128, jobs * (uint64_t)fw.ring_depth * 4};
     const uint64_t st[2] = {128, 128 * 128};
     const uint32_t b[3] = {64, 128, 2};
     ok &= encode_map(&p.tm_ring, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + fw.ring_off, d, st, b,
@@ -415,6 +437,7 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   grid = std::min(grid, std::max(8, env_int("MLA_FUSED_GRID", grid)));
   if (pair) grid &= ~1;
   p.pair = pair;
+  p.ring_depth = fw.ring_depth;
   const int width = pair ? 2 : 1;
   st = cuda_status(cudaMemsetAsync(err, 0, 256, s));   // error word + role queue
   if (st != MLA_OK) return st;
@@ -569,9 +592,8 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, i
     if ((seq_lens[r] + kBlock - 1) / kBlock > max_blocks_per_req) return MLA_ERR_INVALID_ARG;
   FusedPlan fplan;
   build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fplan);
-  const int ppl = fused_pieces_fitting(fplan, num_heads, workspace_bytes);
-  if (workspace == nullptr || !aligned(workspace, 256) || ppl < 1) return MLA_ERR_WORKSPACE;
-  const FusedWs fw = fused_ws_layout(fplan, num_heads, ppl);
+  const FusedWs fw = fused_ws_fitting(fplan, num_heads, workspace_bytes);
+  if (workspace == nullptr || !aligned(workspace, 256) || fw.pieces_per_launch < 1) return MLA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return prefill_fused(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req, num_heads,
                          kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, workspace, fplan, fw, s);
@@ -596,7 +618,7 @@ int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos, const void* kv_
     return MLA_ERR_INVALID_ARG;
   FusedPlan fplan;
   build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fplan);
-  if (fused_pieces_fitting(fplan, num_heads, MLA_NOALLOC_SCRATCH_BYTES) < 1) return MLA_ERR_TOO_LARGE;
+  if (fused_ws_fitting(fplan, num_heads, MLA_NOALLOC_SCRATCH_BYTES).pieces_per_launch < 1) return MLA_ERR_TOO_LARGE;
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
   if (st != MLA_OK) return st;

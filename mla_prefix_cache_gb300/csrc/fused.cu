@@ -41,7 +41,6 @@ namespace {
 using namespace fused_common;
 
 constexpr int kThreads = 384;
-constexpr uint32_t kRing = kRingDepth;
 
 // ---------------------------------------------------------------- shared memory
 constexpr uint32_t kAtomQ = 16384;                  // [128 rows x 128 B] swizzled block
@@ -129,7 +128,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
     if (lane != 0) return;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % kKStages;
-      if (!wait_flag_geq(p, ready_flag(p, job, j % kRing), (uint32_t)j + 1)) { ctl->abort = 1; return; }
+      if (!wait_flag_geq(p, ready_flag(p, job, ring_slot(p, j)), (uint32_t)j + 1)) { ctl->abort = 1; return; }
       if (j >= kKStages && !wait_bar(p, bar_addr(sbase, kBKEmpty + s), ((j / kKStages) - 1) & 1)) {
         ctl->abort = 1;
         return;
@@ -137,7 +136,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
       fence_proxy_async_global();
       const uint32_t st = sbase + kKBase + s * kKStageBytes;
       const uint32_t full = bar_addr(sbase, kBKFull + s);
-      const int zb = (job * (int)kRing + j % kRing) * 4;
+      const int zb = (job * p.ring_depth + ring_slot(p, j)) * 4;
       tma_load_3d(st + kAtomQ, &p.tm_ring1, 0, 0, zb + 1, full);                               // K_nope hi
       tma_load_2d(st + 2 * kAtomQ, &p.tm_kr128, kDc, block_row(J, (J.t0 + 128 * j) >> 6), full);   // k_rope
     }
@@ -156,7 +155,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
       // run ahead, so the flag is normally set already, and the round trip to
       // L2 overlaps the wait for the stage instead of following it.
       const uint64_t w0 = tr.begin(p);
-      if (!wait_flag_geq(p, ready_flag(p, job, j % kRing), (uint32_t)j + 1)) { ctl->abort = 1; return; }
+      if (!wait_flag_geq(p, ready_flag(p, job, ring_slot(p, j)), (uint32_t)j + 1)) { ctl->abort = 1; return; }
       tr.end(p, w0);
       // stage reusable: the MMAs reading its previous tile are done
       if (j >= ns && !wait_bar(p, bar_addr(sbase, (is_k ? kBKEmpty : kBVEmpty) + s), ((j / ns) - 1) & 1)) {
@@ -164,7 +163,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
         return;
       }
       fence_proxy_async_global();
-      const int zb = (job * (int)kRing + j % kRing) * 4;   // first ring block of the tile
+      const int zb = (job * p.ring_depth + ring_slot(p, j)) * 4;   // first ring block of the tile
       if (is_k) {
         const uint32_t st = sbase + kKBase + s * kKStageBytes;
         const uint32_t full = bar_addr(sbase, kBKFull + s);
@@ -195,7 +194,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
       // next load is issued, so the release is off the path to the MMA.
       if (j >= ns) {
         fence_proxy_async_global();
-        red_release_gpu_add(consumed_flag(p, job, (j - ns) % kRing), 1u);
+        red_release_gpu_add(consumed_flag(p, job, ring_slot(p, j - ns)), 1u);
       }
     }
     // the last stages: once their MMAs are done, release their tiles' slots
@@ -204,7 +203,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int ci
     for (int j = max(0, n_tiles - ns); j < n_tiles; ++j) {
       if (!wait_bar(p, bar_addr(sbase, (is_k ? kBKEmpty : kBVEmpty) + j % ns), (j / ns) & 1)) { ctl->abort = 1; return; }
       fence_proxy_async_global();
-      red_release_gpu_add(consumed_flag(p, job, j % kRing), 1u);
+      red_release_gpu_add(consumed_flag(p, job, ring_slot(p, j)), 1u);
     }
     if (is_k) trace_put(p, role, 3, tr.t);
     if (is_k) trace_put(p, role, 7, (unsigned long long)n_tiles);
@@ -558,7 +557,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       const int pass = pi + n * J.n_prod;
       const int t = 2 * pass + wg;
       const bool live_tile = t < J.n_tiles;
-      const int slot = t % kRing;
+      const int slot = ring_slot(p, t);
       const int tok = J.t0 + 128 * t + r;
       const bool valid = tok >= J.k_begin && tok < J.k_end;
       const uint32_t acc = tmem + lane_off + (wg ? kTmAccB : kTmAccA);
@@ -598,13 +597,13 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       if (live_tile) {
         fence_proxy_async_smem();
         named_bar_sync(1 + wg, 128);
-        const int zb = (job * (int)kRing + slot) * 4;
+        const int zb = (job * p.ring_depth + slot) * 4;
         if (r == 0 && !ctl->abort) {
           const uint64_t w0 = tr_c.begin(p);
           // the slot's previous occupant (tile t - ring) must be published and fully consumed
-          if (t >= (int)kRing &&
-              !(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - kRing + 1)) &&
-                wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - kRing, p.pair))))
+          if (t >= p.ring_depth &&
+              !(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - p.ring_depth + 1)) &&
+                wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - p.ring_depth, p.pair))))
             ctl->abort = 1;
           tr_c.end(p, w0);
           *consumed_flag(p, job, slot) = 0u;    // ordered before the release of `ready` below

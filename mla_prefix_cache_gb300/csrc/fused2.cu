@@ -40,7 +40,6 @@ namespace {
 using namespace fused_common;
 
 constexpr int kThreads = 384;
-constexpr uint32_t kRing = kRingDepth;
 constexpr uint32_t kAtomQ = 16384;                  // [128 rows x 128 B] swizzled block
 constexpr uint32_t kAtom64 = 8192;                  // [64 rows x 128 B] swizzled block
 
@@ -135,18 +134,18 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       for (int j = 0; j < n_tiles; ++j) {
         const int s = j % ns;
         const uint64_t w0 = tr.begin(p);
-        if (!wait_flag_geq(p, ready_flag(p, job, j % kRing), (uint32_t)j + 1)) { ctl->abort = 1; return; }
+        if (!wait_flag_geq(p, ready_flag(p, job, ring_slot(p, j)), (uint32_t)j + 1)) { ctl->abort = 1; return; }
         tr.end(p, w0);
         if (j >= ns) {
           // the stage is free once the pair's MMAs read it; its tile's ring slot is then consumed here
           if (!wait_bar(p, bar_addr(sbase, empty0 + s), ((j / ns) - 1) & 1)) { ctl->abort = 1; return; }
           fence_proxy_async_global();
-          red_release_gpu_add(consumed_flag(p, job, (j - ns) % kRing), 1u);
+          red_release_gpu_add(consumed_flag(p, job, ring_slot(p, j - ns)), 1u);
         }
         fence_proxy_async_global();
         const uint32_t full = bar_addr(sbase, full0 + s);
         const uint32_t full_leader = mapa_shared(full, 0u);
-        const int zb = (job * (int)kRing + j % kRing) * 4;   // first ring block of the tile
+        const int zb = (job * p.ring_depth + ring_slot(p, j)) * 4;   // first ring block of the tile
         if (is_k) {
           const uint32_t st = sbase + kKBase + s * kKStageBytes;
           if (leader) mbar_arrive_expect_tx(full, 2 * kKStageBytes);     // both halves land on the leader's count
@@ -166,7 +165,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       for (int j = max(0, n_tiles - ns); j < n_tiles; ++j) {
         if (!wait_bar(p, bar_addr(sbase, empty0 + j % ns), (j / ns) & 1)) { ctl->abort = 1; return; }
         fence_proxy_async_global();
-        red_release_gpu_add(consumed_flag(p, job, j % kRing), 1u);
+        red_release_gpu_add(consumed_flag(p, job, ring_slot(p, j)), 1u);
       }
       if (is_k) {
         trace_put(p, role, 3, tr.t);
@@ -497,7 +496,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       const int b = n & 1;
       const int t = 2 * pass + (int)rank;
       const bool live_tile = t < J.n_tiles;
-      const int slot = t % kRing;
+      const int slot = ring_slot(p, t);
       const int tok = J.t0 + 128 * t + r;
       const bool valid = tok >= J.k_begin && tok < J.k_end;
       if (!wait_bar_warp(p, bar_addr(sbase, kBAccFull + b), (n >> 1) & 1)) ctl->abort = 1;
@@ -518,13 +517,13 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(bar_addr(sbase, kBAccEmpty + b), 0u));   // accumulator free
       if (live_tile) {
-        const int zb = (job * (int)kRing + slot) * 4;
+        const int zb = (job * p.ring_depth + slot) * 4;
         if (tid == 0 && !ctl->abort) {
           const uint64_t w0 = tr_c.begin(p);
           // the slot's previous occupant (tile t - ring) must be published and fully consumed
-          if (t >= (int)kRing &&
-              !(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - kRing + 1)) &&
-                wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - kRing))))
+          if (t >= p.ring_depth &&
+              !(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - p.ring_depth + 1)) &&
+                wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - p.ring_depth))))
             ctl->abort = 1;
           tr_c.end(p, w0);
           *consumed_flag(p, job, slot) = 0u;    // ordered before the release of `ready` below

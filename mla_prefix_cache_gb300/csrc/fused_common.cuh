@@ -80,11 +80,14 @@ __device__ __forceinline__ int consumer_tiles(const Job& J, int ci) {
   return (k_end - J.t0 + 127) >> 7;
 }
 
+// Ring slot of tile t (the depth is a power of two).
+__device__ __forceinline__ int ring_slot(const FusedParams& p, int t) { return t & (p.ring_depth - 1); }
+
 __device__ __forceinline__ uint32_t* ready_flag(const FusedParams& p, int job, int slot) {
-  return p.flags + (size_t)job * (2 * (size_t)kRingDepth) + slot;
+  return p.flags + (size_t)job * (2 * (size_t)p.ring_depth) + slot;
 }
 __device__ __forceinline__ uint32_t* consumed_flag(const FusedParams& p, int job, int slot) {
-  return p.flags + (size_t)job * (2 * (size_t)kRingDepth) + kRingDepth + slot;
+  return p.flags + (size_t)job * (2 * (size_t)p.ring_depth) + p.ring_depth + slot;
 }
 
 // Row of logical block `lb` of the job's request in the gathered rows (the

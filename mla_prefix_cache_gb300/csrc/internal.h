@@ -61,7 +61,7 @@ struct MergeParams {
 };
 
 // ------------------------------------------------------------ fused persistent kernel
-constexpr int kRingDepth = 32;    // 128-token K/V tiles per job ring
+constexpr int kRingDepth = 128;   // deepest job ring: 128-token K/V tiles (8 MB); a small workspace gets less
 constexpr int kMaxPieces = 448;   // pieces per launch (kernel-parameter budget)
 
 // One key range of one request attended with one RoPE offset, for every head.
@@ -117,6 +117,7 @@ struct FusedParams {
   int n_pieces;
   int n_groups;         // role groups in the queue (one per cluster dequeue)
   int pair;             // 1: clusters of two CTAs, consumer pairs share K/V loads by multicast
+  int ring_depth;       // 128-token tiles per job ring: a power of two <= kRingDepth (slots are t & (depth - 1))
   unsigned long long* trace;   // optional, kTraceWords per role slot (group * 2 + cluster rank; see fused.cu)
   int trace_detail_role;       // role slot whose stages are timed one by one (-1: none)
   uint64_t rope_frac[kDr / 2];

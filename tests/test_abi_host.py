@@ -50,7 +50,7 @@ def _up(x, a=256):
     return (x + a - 1) // a * a
 
 
-def fused_layout(pieces, heads, slots, total_q, seq_lens, ring_depth=32):
+def fused_layout(pieces, heads, slots, total_q, seq_lens, ring_depth=128):
     """Workspace of the fused path: 256 B header, per-job ring flags, per-job
     K/V rings of `ring_depth` 128-token bf16 tiles, room for the dequantised
     rows of an FP8 cache (1152 B per token, whole 64-token blocks), then
