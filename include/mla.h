@@ -114,14 +114,18 @@ typedef struct {
  *  lse          device fp32 [T_q, H], natural log, softmax scale included;
  *               -inf for a row with no visible key (its out row is 0).
  *  workspace    device, 256-B aligned; mla_prefill_workspace_size(...) bytes
- *               lets the whole call run as one kernel launch.  A smaller
- *               workspace also works as long as it holds the partial states
- *               and the K/V rings of one piece (one request's key range of at
- *               most max(chunk, 16384) tokens, for all heads): the call then
- *               runs its pieces in several launches.  The size includes
- *               room for the rows of an FP8 cache dequantised to bf16 by the
- *               call's gather pass (1152 B per token).  Holds the device error
- *               word; must not be shared by calls that may overlap on the GPU.
+ *               lets the whole call run as one kernel launch with K/V rings
+ *               of 128 up-projected tiles (8 MB) per (piece, head): for
+ *               long contexts this is several GB, from an HBM of 280 GB.  A
+ *               smaller workspace also works as long as it holds the
+ *               gathered rows, the partial states and rings of at least 4
+ *               tiles for one piece (one request's key range of at most
+ *               max(chunk, 16384) tokens, for all heads): the call then uses
+ *               shallower rings and runs its pieces in several launches,
+ *               more slowly.  The gathered rows are every block of the
+ *               requests, copied in logical order as bf16 (1152 B per
+ *               token; FP8 rows dequantised).  Holds the device error word;
+ *               must not be shared by calls that may overlap on the GPU.
  *  H            num_heads in [1, 128].
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H > 128, chunk not a
  * multiple of 64), MLA_ERR_WORKSPACE, MLA_ERR_CUDA.  Bad block ids are reported
