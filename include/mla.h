@@ -181,6 +181,42 @@ int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos,
                             const void* kv_b_proj, float softmax_scale, float rope_theta, int parts,
                             void* out, int out_dtype, float* lse, mla_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * mla_prefill_ctx_absorbed -- the same operation as mla_prefill_ctx (same
+ * arguments, same out and lse up to rounding), computed in latent space
+ * ("DeepSeek MLA — Prefix Cache 与 Chunked Prefill 深度解析", section 3, the
+ * absorbed attention path, named there for decode):
+ *   qlat = q_nope W_UK,h^T  (512 wide, per token and head);
+ *   s_t  = softmax_scale * (qlat . c_t + R(q_pos - offset) q_rope . k_rope_t),
+ *          with c_t, k_rope_t the cached latent row of key t itself, shared by
+ *          every head;
+ *   o    = sum_t softmax(s)_t c_t  (512 wide);  out = o W_UV,h;  lse as above.
+ * No key is up-projected.  Per (query, key, head) it costs 2 * (576 + 512)
+ * FLOP instead of 2 * (192 + 128), and it saves the 2 * 512 * 256 FLOP per
+ * (key, head) of the up-projection: faster than mla_prefill_ctx while the
+ * requests have few queries (about 170 or fewer per request), slower beyond.
+ * The caller chooses the entry point.
+ *  workspace    device, 256-B aligned, at least
+ *               mla_prefill_absorbed_workspace_size(...) bytes (gathered rows,
+ *               the absorbed queries [T_q, H, 512] bf16, and fp32 latent
+ *               partial states [slots, T_q, H, 512] for the key splits);
+ *               smaller -> MLA_ERR_WORKSPACE.  Holds the device error word
+ *               read by mla_get_device_error().
+ * Errors: as mla_prefill_ctx.
+ * ---------------------------------------------------------------------- */
+size_t mla_prefill_absorbed_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q,
+                                           int num_heads, const mla_segment* segments, int num_segments,
+                                           int chunk, int parts);
+
+int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos,
+                             const void* kv_cache, int kv_dtype, float kv_scale, int num_blocks,
+                             const int32_t* block_table, int max_blocks_per_req,
+                             const int32_t* seq_lens, const int32_t* cu_q, int num_reqs, int num_heads,
+                             const mla_segment* segments, int num_segments, int chunk,
+                             const void* kv_b_proj, float softmax_scale, float rope_theta, int parts,
+                             void* out, int out_dtype, float* lse,
+                             void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
 /* Reads and clears the device error word kept in `workspace` (synchronises
  * `stream`).  Returns MLA_OK, MLA_ERR_BAD_BLOCK_ID or MLA_ERR_TIMEOUT. */
 int mla_get_device_error(void* workspace, mla_stream_t stream);
@@ -229,7 +265,8 @@ int mla_gather_latent(const void* kv_cache, int kv_dtype, float kv_scale, int nu
 /* Optional instrumentation.  With both arguments non-NULL (cudaEvent_t handles
  * created by the caller), every later mla_prefill_ctx call on this process
  * records `begin` on its stream just before its first fused prefill kernel
- * launch and `end` just after the last one, so the caller can time the fused
+ * launch and `end` just after the last one (mla_prefill_ctx_absorbed: around
+ * its latent attention kernel launches), so the caller can time the fused
  * kernel alone with cudaEventElapsedTime.  NULL, NULL turns it off.  The
  * setting is process-wide; the caller keeps the events alive while it is on. */
 void mla_set_kernel_events(void* begin_event, void* end_event);

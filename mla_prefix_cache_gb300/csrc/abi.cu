@@ -339,6 +339,39 @@ static int noalloc_scratch(void** out) {
   return MLA_OK;
 }
 
+// The gather pass: every block of the plan's requests, in logical order, into
+// `dst` (FP8 rows as exact bf16(e4m3) without the scale).
+static int gather_rows(const FusedPlan& fp, const void* kv_cache, bool fp8, int num_blocks, const int32_t* block_table,
+                       int max_blocks, uint8_t* dst, uint32_t* err, cudaStream_t s) {
+  static GatherBlocksParams gp;   // large; built on the host under a lock
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  std::memset(&gp, 0, sizeof(gp));
+  gp.cache = static_cast<const uint8_t*>(kv_cache);
+  gp.block_table = block_table;
+  gp.err = err;
+  gp.fp8 = fp8 ? 1 : 0;
+  gp.scale = 1.f;
+  gp.num_blocks = num_blocks;
+  gp.max_blocks = max_blocks;
+  for (size_t g0 = 0; g0 < fp.gather.size(); g0 += kMaxGatherReqs) {
+    const size_t n = std::min(fp.gather.size() - g0, (size_t)kMaxGatherReqs);
+    int base = fp.gather[g0].base_block, end = base;
+    for (size_t i = 0; i < n; ++i) {
+      GatherReq g = fp.gather[g0 + i];
+      end = g.base_block + (g.seq_len + kBlock - 1) / kBlock;
+      g.base_block -= base;
+      gp.reqs[i] = g;
+    }
+    gp.dst = reinterpret_cast<uint16_t*>(dst) + (size_t)base * kBlock * kRowBf16;
+    gp.n_reqs = (int)n;
+    gp.total_blocks = end - base;
+    const int st = cuda_status(launch_gather_blocks(gp, s));
+    if (st != MLA_OK) return st;
+  }
+  return MLA_OK;
+}
+
 static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
                          int num_blocks, const int32_t* block_table, int max_blocks, int num_heads,
                          const void* kv_b_proj, float softmax_scale, float rope_theta, void* out, int out_dtype,
@@ -441,32 +474,8 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   const int width = pair ? 2 : 1;
   st = cuda_status(cudaMemsetAsync(err, 0, 256, s));   // error word + role queue
   if (st != MLA_OK) return st;
-  {
-    GatherBlocksParams gp;
-    std::memset(&gp, 0, sizeof(gp));
-    gp.cache = static_cast<const uint8_t*>(kv_cache);
-    gp.block_table = block_table;
-    gp.dst = reinterpret_cast<uint16_t*>(ws + fw.gath_off);
-    gp.err = err;
-    gp.fp8 = fp8 ? 1 : 0;
-    gp.scale = 1.f;
-    gp.num_blocks = num_blocks;
-    gp.max_blocks = max_blocks;
-    for (size_t g0 = 0; g0 < fp.gather.size(); g0 += kMaxGatherReqs) {
-      const size_t n = std::min(fp.gather.size() - g0, (size_t)kMaxGatherReqs);
-      int base = fp.gather[g0].base_block, end = base;
-      for (size_t i = 0; i < n; ++i) {
-        GatherReq g = fp.gather[g0 + i];
-        end = g.base_block + (g.seq_len + kBlock - 1) / kBlock;
-        g.base_block -= base;
-        gp.reqs[i] = g;
-      }
-      gp.dst = reinterpret_cast<uint16_t*>(ws + fw.gath_off) + (size_t)base * kBlock * kRowBf16;
-      gp.n_reqs = (int)n;
-      gp.total_blocks = end - base;
-      if ((st = cuda_status(launch_gather_blocks(gp, s))) != MLA_OK) return st;
-    }
-  }
+  if ((st = gather_rows(fp, kv_cache, fp8, num_blocks, block_table, max_blocks, ws + fw.gath_off, err, s)) != MLA_OK)
+    return st;
 
   cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
   cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
@@ -527,6 +536,243 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   return MLA_OK;
 }
 
+
+// ------------------------------------------------------------------ absorbed path
+struct AbsPlan {
+  std::vector<AbsPiece> pieces;    // the fused plan's pieces, LPT order
+  std::vector<RowRange> ranges;    // every request with queries, with its slot count
+  int max_slots = 0;
+  bool any_merge = false;
+  int64_t items = 0;
+};
+
+// Work items of the absorbed path: each piece's 128-row tiles of (token, head)
+// rows, each tile's keys cut into splits of split_keys (a multiple of 64).
+// The split size aims at about four waves of the GPU's clusters over the
+// whole call and stays within [512, 8192] keys; MLA_ABS_SPLIT_KEYS overrides
+// it (rounded up to a multiple of 64).
+static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int num_reqs, AbsPlan* ap) {
+  ap->pieces.clear();
+  ap->ranges.clear();
+  ap->max_slots = 0;
+  ap->any_merge = false;
+  ap->items = 0;
+  double work = 0.0;
+  for (const Piece& pc : fp.pieces)
+    work += (double)((pc.q_count * (int64_t)H + 127) / 128) * (double)(pc.k_end - pc.k_begin);
+  int split = (int)std::ceil(work / 304.0);
+  split = std::min(8192, std::max(512, (split + 63) & ~63));
+  const int forced = env_int("MLA_ABS_SPLIT_KEYS", 0);
+  if (forced > 0) split = (forced + 63) & ~63;
+  std::vector<int> next_slot(num_reqs, 0);
+  for (const Piece& pc : fp.pieces) {
+    AbsPiece a{};
+    a.req = pc.req;
+    a.q_begin = pc.q_begin;
+    a.q_count = pc.q_count;
+    a.q_tok0 = pc.q_tok0;
+    a.k_begin = pc.k_begin;
+    a.k_end = pc.k_end;
+    a.row_block0 = pc.row_block0;
+    a.rope_offset = pc.rope_offset;
+    a.n_row_tiles = (int)((pc.q_count * (int64_t)H + 127) / 128);
+    const int keys = pc.k_end - pc.k_begin;
+    a.n_splits = std::max(1, (keys + split - 1) / split);
+    a.split_keys = ((keys + a.n_splits - 1) / a.n_splits + 63) & ~63;
+    a.slot = next_slot[pc.req];
+    next_slot[pc.req] += a.n_splits;
+    ap->pieces.push_back(a);
+  }
+  for (int r = 0; r < num_reqs; ++r) {
+    if (cu_q[r + 1] == cu_q[r]) continue;
+    RowRange rr{};
+    rr.row_begin = cu_q[r];
+    rr.row_end = cu_q[r + 1];
+    rr.nslots = next_slot[r];
+    ap->ranges.push_back(rr);
+    ap->max_slots = std::max(ap->max_slots, rr.nslots);
+    ap->any_merge |= rr.nslots > 1;
+  }
+}
+
+struct AbsWs {
+  size_t gath_off = 0, qlat_off = 0, lat_out_off = 0, lat_lse_off = 0, part_out_off = 0, part_lse_off = 0, total = 0;
+};
+
+// Workspace of the absorbed path: header (error word), gathered rows, the
+// absorbed queries, the latent partial states of every slot, and (for requests
+// with several slots) their projected partial states for the merge.
+static AbsWs abs_ws_layout(const FusedPlan& fp, const AbsPlan& ap, int H) {
+  AbsWs w;
+  const size_t rows = (size_t)fp.total_q * (size_t)H;
+  const size_t slots = (size_t)std::max(ap.max_slots, 1);
+  w.gath_off = 256;
+  w.qlat_off = up256(w.gath_off + (size_t)fp.gather_blocks * kBlock * kRowBytesBf16);
+  w.lat_out_off = up256(w.qlat_off + rows * kDc * sizeof(uint16_t));
+  w.lat_lse_off = up256(w.lat_out_off + slots * rows * kDc * sizeof(float));
+  w.part_out_off = up256(w.lat_lse_off + slots * rows * sizeof(float));
+  const size_t part_slots = ap.any_merge ? slots : 0;
+  w.part_lse_off = up256(w.part_out_off + part_slots * rows * kDv * sizeof(float));
+  w.total = up256(w.part_lse_off + part_slots * rows * sizeof(float));
+  return w;
+}
+
+static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                            int num_blocks, const int32_t* block_table, int max_blocks, int H, const void* kv_b_proj,
+                            float softmax_scale, float rope_theta, void* out, int out_dtype, float* lse,
+                            void* workspace, const FusedPlan& fp, const AbsPlan& ap, const AbsWs& aw,
+                            cudaStream_t s) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int64_t T_q = fp.total_q;
+  static AbsorbParams p;           // large; built on the host under a lock
+  static ProjParams pp;
+  static MergeParams mp;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  std::memset(&p, 0, sizeof(p));
+  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const float vscale = fp8 ? kv_scale : 1.f;
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+
+  const void* rows_base = static_cast<const void*>(ws + aw.gath_off);
+  const uint64_t rows_total = (uint64_t)std::max(fp.gather_blocks, 1) * kBlock;
+  bool ok = true;
+  {
+    // the latent part of a row as 8 blocks of 64 columns: (column, row, block)
+    const uint64_t d[3] = {64, rows_total, 8};
+    const uint64_t st[2] = {(uint64_t)kRowBytesBf16, 128};
+    const uint32_t b[3] = {64, (uint32_t)64, 8};
+    ok &= encode_map(&p.tm_c8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rows_base, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint64_t d2[2] = {(uint64_t)kRowBf16, rows_total};
+    const uint64_t st2[1] = {(uint64_t)kRowBytesBf16};
+    const uint32_t b2[2] = {64, 64};
+    ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!ok) return MLA_ERR_CUDA;
+
+  int st = cuda_status(cudaMemsetAsync(err, 0, 256, s));
+  if (st != MLA_OK) return st;
+  if ((st = gather_rows(fp, kv_cache, fp8, num_blocks, block_table, max_blocks, ws + aw.gath_off, err, s)) != MLA_OK)
+    return st;
+  {
+    QAbsorbParams qp;
+    qp.q = static_cast<const uint16_t*>(q);
+    qp.w = static_cast<const uint16_t*>(kv_b_proj);
+    qp.qlat = reinterpret_cast<uint16_t*>(ws + aw.qlat_off);
+    qp.scale = vscale;
+    qp.tokens = (int)T_q;
+    qp.num_heads = H;
+    if ((st = cuda_status(launch_qabsorb(qp, s))) != MLA_OK) return st;
+  }
+
+  p.q = static_cast<const uint16_t*>(q);
+  p.qlat = reinterpret_cast<const uint16_t*>(ws + aw.qlat_off);
+  p.q_pos = q_pos;
+  p.lat_out = reinterpret_cast<float*>(ws + aw.lat_out_off);
+  p.lat_lse = reinterpret_cast<float*>(ws + aw.lat_lse_off);
+  p.slot_stride_rows = T_q * H;
+  p.err = err;
+  p.num_heads = H;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  rope_fracs((double)rope_theta, p.rope_frac);
+  cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
+  cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
+  if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_b, s))) != MLA_OK) return st;
+  for (size_t b0 = 0; b0 < ap.pieces.size(); b0 += kMaxAbsPieces) {
+    const size_t n = std::min(ap.pieces.size() - b0, (size_t)kMaxAbsPieces);
+    int64_t items = 0;
+    for (size_t i = 0; i < n; ++i) {
+      AbsPiece a = ap.pieces[b0 + i];
+      a.item_begin = (int32_t)items;
+      items += (int64_t)a.n_row_tiles * a.n_splits;
+      p.pieces[i] = a;
+    }
+    if (items > (int64_t)1 << 30) return MLA_ERR_UNSUPPORTED;
+    p.n_pieces = (int)n;
+    p.n_items = (int)items;
+    if ((st = cuda_status(launch_absorb_attn(p, s))) != MLA_OK) return st;
+  }
+  if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_e, s))) != MLA_OK) return st;
+
+  std::memset(&pp, 0, sizeof(pp));
+  pp.lat_out = p.lat_out;
+  pp.lat_lse = p.lat_lse;
+  pp.lat_slot_stride_rows = T_q * H;
+  pp.w = static_cast<const uint16_t*>(kv_b_proj);
+  pp.out = out;
+  pp.lse = lse;
+  pp.part_out = reinterpret_cast<float*>(ws + aw.part_out_off);
+  pp.part_lse = reinterpret_cast<float*>(ws + aw.part_lse_off);
+  pp.part_slot_stride_rows = T_q;
+  pp.out_bf16 = out_dtype == MLA_OUT_BF16;
+  pp.scale = vscale;
+  pp.num_heads = H;
+  pp.max_slots = std::max(ap.max_slots, 1);
+  for (size_t b0 = 0; b0 < ap.ranges.size(); b0 += kMaxRangesPerLaunch) {
+    const size_t n = std::min(ap.ranges.size() - b0, (size_t)kMaxRangesPerLaunch);
+    int rows = 0;
+    for (size_t i = 0; i < n; ++i) {
+      RowRange rr = ap.ranges[b0 + i];
+      rr.prefix = rows;
+      rows += rr.row_end - rr.row_begin;
+      pp.ranges[i] = rr;
+    }
+    pp.num_ranges = (int)n;
+    pp.total_rows = rows;
+    if ((st = cuda_status(launch_absorb_proj(pp, s))) != MLA_OK) return st;
+  }
+  if (ap.any_merge) {
+    std::memset(&mp, 0, sizeof(mp));
+    mp.part_out = pp.part_out;
+    mp.part_lse = pp.part_lse;
+    mp.slot_stride_rows = T_q;
+    mp.out = out;
+    mp.lse = lse;
+    mp.out_bf16 = pp.out_bf16;
+    mp.num_heads = H;
+    std::vector<RowRange> multi;
+    for (const RowRange& rr : ap.ranges)
+      if (rr.nslots > 1) multi.push_back(rr);
+    for (size_t b0 = 0; b0 < multi.size(); b0 += kMaxRangesPerLaunch) {
+      const size_t n = std::min(multi.size() - b0, (size_t)kMaxRangesPerLaunch);
+      int rows = 0;
+      for (size_t i = 0; i < n; ++i) {
+        RowRange rr = multi[b0 + i];
+        rr.prefix = rows;
+        rows += rr.row_end - rr.row_begin;
+        mp.ranges[i] = rr;
+      }
+      mp.num_ranges = (int)n;
+      mp.total_rows = rows;
+      if ((st = cuda_status(launch_merge_slots(mp, s))) != MLA_OK) return st;
+    }
+  }
+  return MLA_OK;
+}
+
+// Shared validation of the prefill entry points; fills the plans.
+static int prefill_plans(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                         int num_blocks, const int32_t* block_table, int max_blocks_per_req, const int32_t* seq_lens,
+                         const int32_t* cu_q, int num_reqs, int num_heads, const mla_segment* segments,
+                         int num_segments, int chunk, const void* kv_b_proj, float softmax_scale, float rope_theta,
+                         int parts, void* out, int out_dtype, float* lse, Plan* plan, FusedPlan* fplan) {
+  int st = build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, plan);
+  if (st != MLA_OK) return st;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_OUT_FP32 && out_dtype != MLA_OUT_BF16) return MLA_ERR_INVALID_ARG;
+  if (!(rope_theta > 1.f) || !std::isfinite(softmax_scale) || !std::isfinite(rope_theta)) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_KV_FP8_E4M3 && !(std::isfinite(kv_scale) && kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (plan->total_q == 0) return MLA_OK;
+  if (!q || !q_pos || !kv_cache || !block_table || !kv_b_proj || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (num_blocks <= 0 || max_blocks_per_req <= 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(kv_b_proj, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  for (int r = 0; r < num_reqs; ++r)
+    if ((seq_lens[r] + kBlock - 1) / kBlock > max_blocks_per_req) return MLA_ERR_INVALID_ARG;
+  build_fused_plan(*plan, seq_lens, cu_q, num_reqs, chunk, true, fplan);
+  return MLA_OK;
+}
+
 extern "C" {
 
 int mla_abi_version(void) { return 1; }
@@ -577,21 +823,11 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, i
                     int parts, void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes,
                     mla_stream_t stream) {
   Plan plan;
-  int st = build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan);
-  if (st != MLA_OK) return st;
-  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
-  if (out_dtype != MLA_OUT_FP32 && out_dtype != MLA_OUT_BF16) return MLA_ERR_INVALID_ARG;
-  if (!(rope_theta > 1.f) || !std::isfinite(softmax_scale) || !std::isfinite(rope_theta)) return MLA_ERR_INVALID_ARG;
-  if (kv_dtype == MLA_KV_FP8_E4M3 && !(std::isfinite(kv_scale) && kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
-  if (plan.total_q == 0) return MLA_OK;
-  if (!q || !q_pos || !kv_cache || !block_table || !kv_b_proj || !out || !lse) return MLA_ERR_INVALID_ARG;
-  if (num_blocks <= 0 || max_blocks_per_req <= 0) return MLA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(kv_b_proj, 16) || !aligned(out, 16) || !aligned(lse, 4))
-    return MLA_ERR_INVALID_ARG;
-  for (int r = 0; r < num_reqs; ++r)
-    if ((seq_lens[r] + kBlock - 1) / kBlock > max_blocks_per_req) return MLA_ERR_INVALID_ARG;
   FusedPlan fplan;
-  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fplan);
+  const int st = prefill_plans(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                               seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
+                               softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
+  if (st != MLA_OK || plan.total_q == 0) return st;
   const FusedWs fw = fused_ws_fitting(fplan, num_heads, workspace_bytes);
   if (workspace == nullptr || !aligned(workspace, 256) || fw.pieces_per_launch < 1) return MLA_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -626,6 +862,39 @@ int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos, const void* kv_
                          seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
                          softmax_scale, rope_theta, parts, out, out_dtype, lse, scratch, MLA_NOALLOC_SCRATCH_BYTES,
                          stream);
+}
+
+size_t mla_prefill_absorbed_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,
+                                           const mla_segment* segments, int num_segments, int chunk, int parts) {
+  Plan plan;
+  if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
+    return 0;
+  FusedPlan fp;
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fp);
+  AbsPlan ap;
+  build_abs_plan(fp, num_heads, cu_q, num_reqs, &ap);
+  return abs_ws_layout(fp, ap, num_heads).total;
+}
+
+int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                             int num_blocks, const int32_t* block_table, int max_blocks_per_req,
+                             const int32_t* seq_lens, const int32_t* cu_q, int num_reqs, int num_heads,
+                             const mla_segment* segments, int num_segments, int chunk, const void* kv_b_proj,
+                             float softmax_scale, float rope_theta, int parts, void* out, int out_dtype, float* lse,
+                             void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  Plan plan;
+  FusedPlan fplan;
+  const int st = prefill_plans(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                               seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
+                               softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
+  if (st != MLA_OK || plan.total_q == 0) return st;
+  AbsPlan ap;
+  build_abs_plan(fplan, num_heads, cu_q, num_reqs, &ap);
+  const AbsWs aw = abs_ws_layout(fplan, ap, num_heads);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < aw.total) return MLA_ERR_WORKSPACE;
+  return prefill_absorbed(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                          num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, workspace, fplan, ap,
+                          aw, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mla_get_device_error(void* workspace, mla_stream_t stream) {

@@ -1,0 +1,593 @@
+// Absorbed (latent-space) MLA attention for short extends ("DeepSeek MLA —
+// Prefix Cache 与 Chunked Prefill 深度解析", section 3, the absorbed path that
+// the page pairs with decode): W_UK is folded into the query and W_UV applied
+// after the attention, so the keys are the cached latent rows themselves,
+// shared by every head:
+//   qlat_h = q_nope_h W_UK,h^T                      [512]   (qabsorb_kernel)
+//   s_t    = scale (qlat_h . c_t + R q_rope_h . k_rope_t)
+//   o_h    = sum_t softmax(s)_t c_t                  [512]   (absorb_attn_kernel)
+//   out_h  = o_h W_UV,h                              [128]   (absorb_proj_kernel)
+// which equals the up-projected attention exactly, up to rounding.  Per
+// (query, key, head) it costs 2 (576 + 512) FLOP against 2 (192 + 128) for the
+// up-projected form, but it skips the 2 * 512 * 256 FLOP per (key, head) of the
+// up-projection: cheaper while a request has fewer than about 170 queries.
+//
+// absorb_attn_kernel: clusters of two CTAs own one work item (128 rows of
+// (token, head) pairs of one piece, one key split).  O [128 x 512] fp32 fills
+// a CTA's whole tensor memory, so the item is split by operation:
+//  - CTA 0 ("S side") keeps Q [128 x 576] bf16 in TMEM, computes
+//    S = Q [c | k_rope]^T for 64 keys per tile (M = 128, N = 64), runs the
+//    online softmax and sends P (bf16) and each row's rescale factor into CTA
+//    1's shared memory with st.async;
+//  - CTA 1 ("O side") accumulates O += P c (two N = 256 MMAs per 16 keys),
+//    rescales O rows in TMEM when the S side raised a row maximum, and writes
+//    O / l at the end.
+// Each 64-key stage of latent rows reaches both CTAs by one multicast TMA;
+// k_rope goes to the S side only.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kAThreads = 256;
+constexpr int kAKeys = 64;
+constexpr int kAStages = 3;
+constexpr uint32_t kAAtom = 8192;                              // [64 rows x 128 B] swizzled block
+constexpr uint32_t kACStage = 8 * kAAtom;                      // latent part of 64 rows
+constexpr uint32_t kACBase = 0;                                // both CTAs: multicast destination
+constexpr uint32_t kAKrBase = kACBase + kAStages * kACStage;   // S side: k_rope of each stage
+constexpr uint32_t kAPBase = kAKrBase;                         // O side: two P tiles [128 x 64] bf16
+constexpr uint32_t kAPBytes = 16384;
+constexpr uint32_t kAAlphaBase = kAPBase + 2 * kAPBytes;       // O side: per P tile, 128 row factors
+constexpr uint32_t kALBase = kAAlphaBase + 2 * 512;            // O side: 128 final row sums
+constexpr uint32_t kABarBase = kALBase + 512;
+enum : uint32_t {
+  kBFull = 0,      // 3, both: stage landed (S side: latent + k_rope; O side: latent)
+  kBEmpty = 3,     // 3, S side: S MMA and PV of the stage done (2 arrivals)
+  kBSFull = 6,     // 2, S side: S buffer written
+  kBSFree = 8,     // 2, S side: the 4 softmax warps read the S buffer
+  kBPFree = 10,    // 2, S side: PV of the P tile done (commit from the O side)
+  kBQReady = 12,   // S side: the 4 softmax warps wrote Q into TMEM
+  kBPFull = 13,    // 2, O side: P tile and row factors landed
+  kBCDone = 15,    // 2, O side: the 4 correction warps handled the tile
+  kBPvDone = 17,   // 2, O side: PV of the tile done
+  kBLFull = 19,    // O side: the final row sums landed
+  kANumBars = 20
+};
+constexpr uint32_t kATmemSlot = kABarBase + 8 * kANumBars;
+constexpr uint32_t kASmemBytes = kATmemSlot + 16 + 1024;       // + alignment of the base to 1024
+static_assert(kASmemBytes <= 232448, "more than 227 KB of shared memory per CTA");
+static_assert(kAKrBase + kAStages * kAAtom <= kABarBase, "k_rope stages overlap the barriers");
+
+constexpr uint32_t kATmS = 320;   // S side: S buffer b at 320 + 64 b (Q as bf16 pairs in columns 0..287)
+constexpr uint32_t kIdescSA = idesc_bf16(128, 64, false, false);
+constexpr uint32_t kIdescPVA = idesc_bf16(128, 256, false, true);
+constexpr uint32_t kTxS = kACStage + kAAtom;
+constexpr uint32_t kTxO = kACStage;
+constexpr uint32_t kTxP = 128 * (128 + 4);   // per row: 64 bf16 of P and one fp32 factor
+constexpr float kARescale = 8.f;             // log2 units: P stays <= 256
+
+__device__ __forceinline__ uint32_t abar(uint32_t sbase, uint32_t i) { return sbase + kABarBase + 8u * i; }
+
+// Bounded waits (a timeout records the error; the caller then skips its work).
+__device__ __forceinline__ bool await(const AbsorbParams& p, uint32_t bar, uint32_t parity) {
+  if (mbar_wait(bar, parity)) return true;
+  atomicOr(p.err, kErrTimeout);
+  return false;
+}
+__device__ __forceinline__ bool await_warp(const AbsorbParams& p, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, await(p, bar, parity));
+}
+
+struct AItem {
+  const AbsPiece* P;
+  int row0;      // first row of the tile within the piece (rows = token * H + head)
+  int k_lo, k_hi, t0, n_tiles;
+  int slot;
+};
+
+__device__ AItem decode_item(const AbsorbParams& p, int item) {
+  int lo = 0, hi = p.n_pieces - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.pieces[mid].item_begin <= item) lo = mid; else hi = mid - 1;
+  }
+  const AbsPiece& P = p.pieces[lo];
+  const int local = item - P.item_begin;
+  const int tile = local / P.n_splits, split = local - tile * P.n_splits;
+  AItem it;
+  it.P = &P;
+  it.row0 = tile * 128;
+  it.slot = P.slot + split;
+  // the tile's last query token bounds its causal keys
+  const int rows = P.q_count * p.num_heads;
+  const int last_t = min(rows - 1, it.row0 + 127) / p.num_heads;
+  const int k_hi_tile = min(P.k_end, P.q_tok0 + last_t + 1);
+  it.k_lo = P.k_begin + split * P.split_keys;
+  it.k_hi = min(it.k_lo + P.split_keys, k_hi_tile);
+  it.t0 = it.k_lo & ~(kAKeys - 1);
+  it.n_tiles = it.k_hi > it.k_lo ? (it.k_hi - it.t0 + kAKeys - 1) / kAKeys : 0;
+  return it;
+}
+
+__global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_constant__ AbsorbParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw_base);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const AItem it = decode_item(p, blockIdx.x >> 1);
+  const AbsPiece& P = *it.P;
+  const int H = p.num_heads;
+  const int n = it.n_tiles;
+
+  if (tid == 0) {
+    prefetch_tensormap(&p.tm_c8);
+    prefetch_tensormap(&p.tm_kr);
+    for (uint32_t i = 0; i < kANumBars; ++i) {
+      uint32_t cnt = 1;
+      if (i >= kBEmpty && i < kBEmpty + 3) cnt = 2;
+      if ((i >= kBSFree && i < kBSFree + 2) || i == kBQReady || (i >= kBCDone && i < kBCDone + 2)) cnt = 4;
+      mbar_init(abar(sbase, i), cnt);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(sbase + kATmemSlot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  cluster_sync_all();   // both CTAs' barriers exist before either signals the other's
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + kATmemSlot);
+  const int64_t row_base = (int64_t)P.row_block0 * kBlock;   // gathered row of key token 0
+
+  if (rank == 0) {
+    // ================================================================ S side
+    if (warp == 0) {
+      // ---------------------------------------------------------- TMA
+      if (lane == 0) {
+        bool ok = true;
+        for (int j = 0; j < n && ok; ++j) {
+          const int s = j % kAStages;
+          if (j >= kAStages && !await(p, abar(sbase, kBEmpty + s), ((j / kAStages) - 1) & 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(abar(sbase, kBFull + s), kTxS);
+          const int row = (int)(row_base + it.t0 + kAKeys * j);
+          tma_load_3d_mc(sbase + kACBase + s * kACStage, &p.tm_c8, 0, row, 0, abar(sbase, kBFull + s), 3);
+          tma_load_2d(sbase + kAKrBase + s * kAAtom, &p.tm_kr, kDc, row, abar(sbase, kBFull + s));
+        }
+        // the O side's last PV commits land on this CTA's barriers before it exits
+        for (int j = max(0, n - kAStages); j < n && ok; ++j)
+          if (!await(p, abar(sbase, kBEmpty + j % kAStages), (j / kAStages) & 1)) ok = false;
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- S = Q [c | k_rope]^T
+      if (lane == 0 && n > 0) {
+        bool ok = await(p, abar(sbase, kBQReady), 0);
+        for (int j = 0; j < n && ok; ++j) {
+          const int s = j % kAStages, b = j & 1;
+          if (!await(p, abar(sbase, kBFull + s), (j / kAStages) & 1)) { ok = false; break; }
+          if (j >= 2 && !await(p, abar(sbase, kBSFree + b), ((j >> 1) - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t c = sbase + kACBase + s * kACStage, kr = sbase + kAKrBase + s * kAAtom;
+          const uint32_t d = tmem + kATmS + 64 * b;
+#pragma unroll
+          for (int kk = 0; kk < 36; ++kk) {
+            const uint64_t bdesc = kk < 32 ? sdesc_sw128(c + (kk >> 2) * kAAtom + (kk & 3) * 32, 16, 1024)
+                                           : sdesc_sw128(kr + (kk - 32) * 32, 16, 1024);
+            mma_bf16_ts(d, tmem + kk * 8, bdesc, kIdescSA, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(abar(sbase, kBSFull + b));
+          mma_commit(abar(sbase, kBEmpty + s));
+        }
+      }
+    } else if (warp >= 4) {
+      // ---------------------------------------------------------- Q -> TMEM, then softmax
+      const int r = tid - 128;
+      const int prow = it.row0 + r;
+      const bool live = prow < P.q_count * H;
+      const int tl = live ? prow / H : 0, h = live ? prow - (prow / H) * H : 0;
+      const int64_t grow = (int64_t)P.q_begin + tl;
+      const int64_t orow = grow * H + h;
+      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+      {
+        const uint4* ql = reinterpret_cast<const uint4*>(p.qlat + orow * kDc);
+#pragma unroll 1
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 a = live ? __ldg(ql + 8 * cc + i) : make_uint4(0, 0, 0, 0);
+            w[4 * i] = a.x; w[4 * i + 1] = a.y; w[4 * i + 2] = a.z; w[4 * i + 3] = a.w;
+          }
+          tmem_st32(tmem + lane_off + 32 * cc, w);
+        }
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q + orow * kDqk + kDnope);
+        const int64_t delta = live ? (int64_t)__ldg(p.q_pos + grow) - P.rope_offset : 0;
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 a = live ? __ldg(qr + c) : make_uint4(0, 0, 0, 0);
+          const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float sn, cs;
+            rope_sincos(delta, p.rope_frac[4 * c + i], &sn, &cs);
+            const float x0 = __uint_as_float(w4[i] << 16), x1 = __uint_as_float(w4[i] & 0xFFFF0000u);
+            w[4 * c + i] = pack_bf16(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+          }
+        }
+        tmem_st32(tmem + lane_off + 256, w);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(abar(sbase, kBQReady));
+      }
+      const int qk = live ? P.q_tok0 + tl : -1;   // last visible key token of the row
+      const float sl2 = p.scale_log2;
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      const uint32_t peer_p = mapa_shared(sbase + kAPBase, 1u);
+      const uint32_t peer_alpha = mapa_shared(sbase + kAAlphaBase, 1u);
+      for (int j = 0; j < n; ++j) {
+        const int b = j & 1;
+        uint32_t v[64];
+        if (ok && !await_warp(p, abar(sbase, kBSFull + b), (j >> 1) & 1)) ok = false;
+        tc_fence_after();
+        if (ok) tmem_ld64(tmem + lane_off + kATmS + 64 * b, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(abar(sbase, kBSFree + b));
+        if (!ok) break;
+        const int kt0 = it.t0 + kAKeys * j;
+        float mx = -INFINITY;
+        if (kt0 >= it.k_lo && kt0 + kAKeys - 1 < it.k_hi && kt0 + kAKeys - 1 <= qk) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(v[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int kt = kt0 + c;
+            const bool vis = kt >= it.k_lo && kt < it.k_hi && kt <= qk;
+            const float x = vis ? __uint_as_float(v[c]) : -INFINITY;
+            v[c] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+        }
+        const float m_tile = mx * sl2;
+        float alpha = 1.f;
+        if (m_tile > m_used + kARescale) {
+          alpha = ex2(m_used - m_tile);   // 0 when m_used = -inf
+          m_used = m_tile;
+        }
+        const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+        float sum = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float a = ex2(fmaf(__uint_as_float(v[2 * c]), sl2, -mref));
+          const float bb = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sl2, -mref));
+          sum += a + bb;
+          pk[c] = pack_bf16(a, bb);
+        }
+        l = l * alpha + sum;
+        // P tile b is free once the PV of tile j - 2 is done
+        if (j >= 2 && !await_warp(p, abar(sbase, kBPFree + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
+        const uint32_t cbar = mapa_shared(abar(sbase, kBPFull + b), 1u);
+        const uint32_t prow_addr = peer_p + b * kAPBytes;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(prow_addr + sw128_off((uint32_t)r, (uint32_t)c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                      pk[4 * c + 3], cbar);
+        st_async_b32(peer_alpha + b * 512 + 4 * r, __float_as_uint(alpha), cbar);
+      }
+      // final row sums to the O side; lse of the item
+      st_async_b32(mapa_shared(sbase + kALBase + 4 * r, 1u), __float_as_uint(ok ? l : 0.f),
+                   mapa_shared(abar(sbase, kBLFull), 1u));
+      if (live) {
+        const float lse = (ok && l > 0.f) ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        p.lat_lse[(int64_t)it.slot * p.slot_stride_rows + orow] = lse;
+      }
+      // the last two PV commits land on this CTA's barriers before it exits
+      for (int j = max(0, n - 2); j < n && ok; ++j)
+        if (!await_warp(p, abar(sbase, kBPFree + (j & 1)), (j >> 1) & 1)) ok = false;
+    }
+  } else {
+    // ================================================================ O side
+    if (warp == 1) {
+      // ---------------------------------------------------------- O += P c
+      if (lane == 0) {
+        for (int s = 0; s < min(n, kAStages); ++s) mbar_arrive_expect_tx(abar(sbase, kBFull + s), kTxO);
+        for (int b = 0; b < min(n, 2); ++b) mbar_arrive_expect_tx(abar(sbase, kBPFull + b), kTxP);
+        mbar_arrive_expect_tx(abar(sbase, kBLFull), 512);
+        bool ok = true;
+        for (int j = 0; j < n && ok; ++j) {
+          const int s = j % kAStages, b = j & 1;
+          if (!await(p, abar(sbase, kBFull + s), (j / kAStages) & 1)) { ok = false; break; }
+          if (!await(p, abar(sbase, kBCDone + b), (j >> 1) & 1)) { ok = false; break; }
+          fence_proxy_async_smem();   // P was written by the peer's stores, the MMA reads it as an operand
+          tc_fence_after();
+          const uint32_t c = sbase + kACBase + s * kACStage, pt = sbase + kAPBase + b * kAPBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = sdesc_sw128(pt + kk * 32, 16, 1024);
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+              mma_bf16(tmem + 256 * half, adesc, sdesc_sw128(c + kk * 2048 + half * 4 * kAAtom, kAAtom, 1024),
+                       kIdescPVA, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(abar(sbase, kBPvDone + b));
+          mma_commit_mc(abar(sbase, kBEmpty + s), 1);
+          mma_commit_mc(abar(sbase, kBPFree + b), 1);
+          if (j + kAStages < n) mbar_arrive_expect_tx(abar(sbase, kBFull + s), kTxO);
+          if (j + 2 < n) mbar_arrive_expect_tx(abar(sbase, kBPFull + b), kTxP);
+        }
+      }
+    } else if (warp >= 4) {
+      // ---------------------------------------------------------- rescale O rows; epilogue
+      const int r = tid - 128;
+      const int prow = it.row0 + r;
+      const bool live = prow < P.q_count * H;
+      const int tl = live ? prow / H : 0, h = live ? prow - (prow / H) * H : 0;
+      const int64_t orow = ((int64_t)P.q_begin + tl) * H + h;
+      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+      const float* alpha_s = reinterpret_cast<const float*>(sgen + kAAlphaBase);
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int b = j & 1;
+        if (ok && !await_warp(p, abar(sbase, kBPFull + b), (j >> 1) & 1)) ok = false;
+        const float a = ok ? alpha_s[b * 128 + r] : 1.f;
+        if (ok && j > 0 && __any_sync(0xffffffffu, a != 1.f)) {
+          // O holds PV of tiles < j: PV(j - 1) must be done (PV(j - 2) is, P tile j needed it)
+          if (!await_warp(p, abar(sbase, kBPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) ok = false;
+          tc_fence_after();
+          if (ok) {
+#pragma unroll 1
+            for (int cc = 0; cc < 16; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(tmem + lane_off + 32 * cc, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+              tmem_st32(tmem + lane_off + 32 * cc, o);
+            }
+            tmem_wait_st();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(abar(sbase, kBCDone + b));
+        if (!ok) break;
+      }
+      if (ok && n > 0 && !await_warp(p, abar(sbase, kBPvDone + ((n - 1) & 1)), ((n - 1) >> 1) & 1)) ok = false;
+      if (ok && !await_warp(p, abar(sbase, kBLFull), 0)) ok = false;
+      tc_fence_after();
+      const float lsum = ok ? reinterpret_cast<const float*>(sgen + kALBase)[r] : 0.f;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      float4* dst = reinterpret_cast<float4*>(p.lat_out + ((int64_t)it.slot * p.slot_stride_rows + orow) * kDc);
+#pragma unroll 1
+      for (int cc = 0; cc < 16; ++cc) {
+        uint32_t o[32];
+        if (ok && n > 0) tmem_ld32(tmem + lane_off + 32 * cc, o);
+        else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        if (live) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[8 * cc + i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                          __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // no peer operation targets this CTA's shared memory any more
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- q absorption
+// Block: 32 tokens x 128 latent columns of one head; 256 threads, each 4 x 4
+// outputs, fp32 accumulation over the 128 q_nope columns.
+__global__ void __launch_bounds__(256) qabsorb_kernel(const QAbsorbParams p) {
+  __shared__ float qs[32][128];
+  __shared__ __align__(16) uint16_t wt[128][128];   // [d][c]
+  const int H = p.num_heads;
+  const int h = blockIdx.z, c0 = blockIdx.y * 128, t0 = blockIdx.x * 32;
+  const int tid = threadIdx.x;
+  const int64_t wrow = (int64_t)H * (kDnope + kDv);
+  for (int i = tid; i < 32 * 16; i += 256) {
+    const int t = i >> 4, ch = i & 15;
+    uint4 a = make_uint4(0, 0, 0, 0);
+    if (t0 + t < p.tokens) a = __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)(t0 + t) * H + h) * kDqk) + ch);
+    const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      qs[t][8 * ch + 2 * k] = __uint_as_float(w4[k] << 16);
+      qs[t][8 * ch + 2 * k + 1] = __uint_as_float(w4[k] & 0xFFFF0000u);
+    }
+  }
+  for (int i = tid; i < 128 * 16; i += 256) {
+    const int c = i >> 4, ch = i & 15;
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p.w + (int64_t)(c0 + c) * wrow + h * kDnope) + ch);
+    const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      wt[8 * ch + 2 * k][c] = (uint16_t)(w4[k] & 0xFFFFu);
+      wt[8 * ch + 2 * k + 1][c] = (uint16_t)(w4[k] >> 16);
+    }
+  }
+  __syncthreads();
+  const int ty = tid >> 5, tx = tid & 31;
+  float acc[4][4] = {};
+#pragma unroll 4
+  for (int d = 0; d < 128; ++d) {
+    const uint2 wb = *reinterpret_cast<const uint2*>(&wt[d][4 * tx]);
+    const float b0 = __uint_as_float(wb.x << 16), b1 = __uint_as_float(wb.x & 0xFFFF0000u);
+    const float b2 = __uint_as_float(wb.y << 16), b3 = __uint_as_float(wb.y & 0xFFFF0000u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = qs[4 * ty + i][d];
+      acc[i][0] = fmaf(a, b0, acc[i][0]);
+      acc[i][1] = fmaf(a, b1, acc[i][1]);
+      acc[i][2] = fmaf(a, b2, acc[i][2]);
+      acc[i][3] = fmaf(a, b3, acc[i][3]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + 4 * ty + i;
+    if (t >= p.tokens) continue;
+    uint2 o;
+    o.x = pack_bf16(acc[i][0] * p.scale, acc[i][1] * p.scale);
+    o.y = pack_bf16(acc[i][2] * p.scale, acc[i][3] * p.scale);
+    *reinterpret_cast<uint2*>(p.qlat + ((int64_t)t * H + h) * kDc + c0 + 4 * tx) = o;
+  }
+}
+
+// ---------------------------------------------------------------- output projection
+// Block: 32 rows (tokens of the launch's ranges) x 128 output columns of one
+// head and one slot; the 512 latent columns in chunks of 64.
+__global__ void __launch_bounds__(256) absorb_proj_kernel(const __grid_constant__ ProjParams p) {
+  __shared__ float as[32][64 + 4];
+  __shared__ __align__(16) uint16_t ws[64][128];
+  __shared__ int64_t grow_s[32];
+  __shared__ int nslots_s[32];
+  const int H = p.num_heads;
+  const int h = blockIdx.z, slot = blockIdx.y, r0 = blockIdx.x * 32;
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const int x = r0 + tid;
+    int64_t g = -1;
+    int ns = 0;
+    if (x < p.total_rows) {
+      int lo = 0, hi = p.num_ranges - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.ranges[mid].prefix <= x) lo = mid; else hi = mid - 1;
+      }
+      const RowRange rr = p.ranges[lo];
+      g = rr.row_begin + (x - rr.prefix);
+      ns = rr.nslots;
+    }
+    grow_s[tid] = (slot < ns) ? g : -1;
+    nslots_s[tid] = ns;
+  }
+  __syncthreads();
+  const int64_t wrow = (int64_t)H * (kDnope + kDv);
+  const int ty = tid >> 5, tx = tid & 31;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < kDc; k0 += 64) {
+    for (int i = tid; i < 32 * 16; i += 256) {
+      const int t = i >> 4, ch = i & 15;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int64_t g = grow_s[t];
+      if (g >= 0)
+        a = __ldg(reinterpret_cast<const float4*>(p.lat_out + ((int64_t)slot * p.lat_slot_stride_rows + g * H + h) * kDc +
+                                                  k0) + ch);
+      as[t][4 * ch] = a.x; as[t][4 * ch + 1] = a.y; as[t][4 * ch + 2] = a.z; as[t][4 * ch + 3] = a.w;
+    }
+    for (int i = tid; i < 64 * 16; i += 256) {
+      const int c = i >> 4, ch = i & 15;
+      reinterpret_cast<uint4*>(&ws[c][0])[ch] =
+          __ldg(reinterpret_cast<const uint4*>(p.w + (int64_t)(k0 + c) * wrow + (int64_t)H * kDnope + h * kDv) + ch);
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int c = 0; c < 64; ++c) {
+      const uint2 wb = *reinterpret_cast<const uint2*>(&ws[c][4 * tx]);
+      const float b0 = __uint_as_float(wb.x << 16), b1 = __uint_as_float(wb.x & 0xFFFF0000u);
+      const float b2 = __uint_as_float(wb.y << 16), b3 = __uint_as_float(wb.y & 0xFFFF0000u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = as[4 * ty + i][c];
+        acc[i][0] = fmaf(a, b0, acc[i][0]);
+        acc[i][1] = fmaf(a, b1, acc[i][1]);
+        acc[i][2] = fmaf(a, b2, acc[i][2]);
+        acc[i][3] = fmaf(a, b3, acc[i][3]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = 4 * ty + i;
+    const int64_t g = grow_s[t];
+    if (g < 0) continue;
+    const float o0 = acc[i][0] * p.scale, o1 = acc[i][1] * p.scale, o2 = acc[i][2] * p.scale, o3 = acc[i][3] * p.scale;
+    const int64_t lrow = (int64_t)slot * p.lat_slot_stride_rows + g * H + h;
+    if (nslots_s[t] == 1) {
+      const int64_t o = (g * H + h) * kDv + 4 * tx;
+      if (p.out_bf16) {
+        uint2 v;
+        v.x = pack_bf16(o0, o1);
+        v.y = pack_bf16(o2, o3);
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o) = v;
+      } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = make_float4(o0, o1, o2, o3);
+      }
+      if (tx == 0) p.lse[g * H + h] = p.lat_lse[lrow];
+    } else {
+      const int64_t prow = (int64_t)slot * p.part_slot_stride_rows * H + g * H + h;
+      *reinterpret_cast<float4*>(p.part_out + prow * kDv + 4 * tx) = make_float4(o0, o1, o2, o3);
+      if (tx == 0) p.part_lse[prow] = p.lat_lse[lrow];
+    }
+  }
+}
+
+}  // namespace
+
+static cudaError_t configure_absorb(int dev) {
+  static int configured_device = -1;
+  if (configured_device == dev) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(absorb_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmemBytes);
+  if (e == cudaSuccess) configured_device = dev;
+  return e;
+}
+
+cudaError_t launch_absorb_attn(const AbsorbParams& p, cudaStream_t s) {
+  if (p.n_items == 0) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = configure_absorb(dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(2 * p.n_items);
+  cfg.blockDim = dim3(kAThreads);
+  cfg.dynamicSmemBytes = kASmemBytes;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, absorb_attn_kernel, p);
+  count_launch();
+  return e;
+}
+
+cudaError_t launch_qabsorb(const QAbsorbParams& p, cudaStream_t s) {
+  if (p.tokens == 0) return cudaSuccess;
+  const dim3 grid((p.tokens + 31) / 32, kDc / 128, p.num_heads);
+  qabsorb_kernel<<<grid, 256, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_absorb_proj(const ProjParams& p, cudaStream_t s) {
+  if (p.total_rows == 0) return cudaSuccess;
+  const dim3 grid((p.total_rows + 31) / 32, p.max_slots, p.num_heads);
+  absorb_proj_kernel<<<grid, 256, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace mla

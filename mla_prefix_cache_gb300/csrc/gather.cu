@@ -100,18 +100,21 @@ __global__ void __launch_bounds__(kGatherThreads, 2) gather_blocks_kernel(const 
     if (!ok && threadIdx.x == 0 && lb * kBlock < rq.seq_len) atomicOr(p.err, kErrBadBlock);
     const uint8_t* src = p.cache + (int64_t)(ok ? blk : 0) * kBlock * row_bytes;
     uint16_t* out = p.dst + (int64_t)gb * kBlock * kRowBf16;
+    // slots past the request's length are zeroed: a kernel that reads a
+    // whole block multiplies them by zero weights, which must stay zero
+    const int live_rows = min(kBlock, rq.seq_len - lb * kBlock);
     uint4 v[kChunksPerThread];
 #pragma unroll
     for (int j = 0; j < kChunksPerThread; ++j) {
       const int k = threadIdx.x + j * kGatherThreads;
       const int r = k / kChunksPerRow, c = k - r * kChunksPerRow;
-      v[j] = ok ? load_chunk(src + r * row_bytes, c, p.fp8) : make_uint4(0u, 0u, 0u, 0u);
+      v[j] = (ok && r < live_rows) ? load_chunk(src + r * row_bytes, c, p.fp8) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int j = 0; j < kChunksPerThread; ++j) {
       const int k = threadIdx.x + j * kGatherThreads;
-      const int c = k % kChunksPerRow;
-      reinterpret_cast<uint4*>(out)[k] = ok ? finish_chunk(v[j], c, p.fp8, p.scale) : v[j];
+      const int r = k / kChunksPerRow, c = k - r * kChunksPerRow;
+      reinterpret_cast<uint4*>(out)[k] = (ok && r < live_rows) ? finish_chunk(v[j], c, p.fp8, p.scale) : v[j];
     }
   }
 }

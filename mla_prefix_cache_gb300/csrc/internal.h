@@ -172,6 +172,82 @@ struct GatherBlocksParams {
 };
 cudaError_t launch_gather_blocks(const GatherBlocksParams& p, cudaStream_t s);
 
+// ------------------------------------------------------------ absorbed (latent-space) path
+// One piece of the absorbed path: a key range of one request with one RoPE
+// offset, attended by all its (query, head) rows, which form 128-row tiles
+// (row = token * H + head); each tile's keys are cut into n_splits work items.
+struct AbsPiece {
+  int32_t req;
+  int32_t q_begin;     // global row of the request's first query
+  int32_t q_count;     // E_r
+  int32_t q_tok0;      // token index of the request's first query (C_r)
+  int32_t k_begin;     // first key token
+  int32_t k_end;       // one past the last key token
+  int32_t row_block0;  // the request's rows were gathered contiguously from this block on
+  int32_t slot;        // partial-state slot of split 0 (split i uses slot + i)
+  int32_t n_row_tiles; // ceil(q_count * H / 128)
+  int32_t n_splits;    // key splits per row tile
+  int32_t split_keys;  // keys per split (a multiple of 64)
+  int32_t item_begin;  // first work item of this piece in the launch
+  int64_t rope_offset;
+};
+constexpr int kMaxAbsPieces = 448;
+
+struct AbsorbParams {
+  CUtensorMap tm_c8;   // gathered rows: the latent part of 64 rows as 8 swizzled [64 x 64] blocks
+  CUtensorMap tm_kr;   // gathered rows, box 64 x 64 (k_rope at column 512)
+  const uint16_t* q;     // [T_q][H][192]: q_rope at 128..191, not rotated
+  const uint16_t* qlat;  // [T_q][H][512] bf16: kv_scale * q_nope W_UK,h^T
+  const int32_t* q_pos;
+  float* lat_out;        // [slots][T_q * H][512] fp32, normalised by the row sum
+  float* lat_lse;        // [slots][T_q * H], natural log
+  int64_t slot_stride_rows;   // T_q * H
+  uint32_t* err;
+  int num_heads;
+  int n_pieces;
+  int n_items;
+  float scale_log2;
+  uint64_t rope_frac[kDr / 2];
+  AbsPiece pieces[kMaxAbsPieces];
+};
+static_assert(sizeof(AbsorbParams) <= 32000, "kernel parameter space");
+
+// q absorption: qlat[t][h][c] = bf16(scale * sum_d q[t][h][d] W[c][128 h + d]).
+struct QAbsorbParams {
+  const uint16_t* q;       // [T_q][H][192]
+  const uint16_t* w;       // kv_b_proj [512][H * 256]
+  uint16_t* qlat;          // [T_q][H][512]
+  float scale;
+  int tokens;
+  int num_heads;
+};
+
+// Output projection of the latent partials: for each request row range and
+// slot < nslots, o[t][h][d] = scale * sum_c lat[slot][t H + h][c] W[c][128 H + 128 h + d];
+// one slot -> the final out / lse, several -> part_out / part_lse for the merge.
+struct ProjParams {
+  const float* lat_out;
+  const float* lat_lse;
+  int64_t lat_slot_stride_rows;   // T_q * H
+  const uint16_t* w;
+  void* out;
+  float* lse;
+  float* part_out;                // [slots][T_q][H][128]
+  float* part_lse;                // [slots][T_q][H]
+  int64_t part_slot_stride_rows;  // T_q
+  int out_bf16;
+  float scale;
+  int num_heads;
+  int max_slots;
+  int num_ranges;
+  int total_rows;                 // tokens of this launch's ranges
+  RowRange ranges[kMaxRangesPerLaunch];
+};
+
+cudaError_t launch_absorb_attn(const AbsorbParams& p, cudaStream_t s);
+cudaError_t launch_qabsorb(const QAbsorbParams& p, cudaStream_t s);
+cudaError_t launch_absorb_proj(const ProjParams& p, cudaStream_t s);
+
 void count_launch(int n = 1);
 
 }  // namespace mla

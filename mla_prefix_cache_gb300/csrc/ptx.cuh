@@ -452,6 +452,22 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 
+// Asynchronous stores into another CTA of the cluster: each store adds its
+// bytes to the complete-tx count of an mbarrier in that CTA (`caddr` and
+// `cbar` are shared::cluster addresses), whose phase completion then makes
+// the data visible to the threads that wait on it.
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(caddr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(cbar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t caddr, uint32_t v, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr), "r"(v),
+               "r"(cbar)
+               : "memory");
+}
+
 // Packed fp32 pairs (sm_100 family): one instruction operates on two floats
 // held in a 64-bit register pair, rounding each lane exactly like the scalar
 // instruction.

@@ -73,9 +73,9 @@ def assert_close(out, lse, ref_out, ref_lse, nvis=None):
     assert rel <= REL_RMS, f"rel rms {rel:.3e}"
 
 
-def run_and_compare(api, wl, parts=3, out_dtype=None, rows=None, heads=None):
+def run_and_compare(api, wl, parts=3, out_dtype=None, rows=None, heads=None, **kw):
     dw = api.DeviceWorkload(wl)
-    out, lse = dw.run(parts=parts, out_dtype=out_dtype or torch.float32)
+    out, lse = dw.run(parts=parts, out_dtype=out_dtype or torch.float32, **kw)
     torch.cuda.synchronize()
     assert api.device_error(api.prefill.last_workspace) == 0
     out = out.float().cpu().numpy()
@@ -264,3 +264,75 @@ def test_prefill_other_kernels(api, case, kernel, monkeypatch):
     wl = W.make_workload("pair", case["H"], case["ctx"], case["ext"], chunk=case["chunk"], seed=31,
                          doc_len=case["doc"])
     run_and_compare(api, wl)
+
+
+# ---------------------------------------------------------------- absorbed (latent-space) path
+
+ABSORBED_CASES = [
+    dict(H=4, ctx=[300], ext=[20], chunk=128),                        # ragged kv tail, one row tile
+    dict(H=2, ctx=[0], ext=[130], chunk=64),                          # no context, causal only
+    dict(H=3, ctx=[64, 0, 777], ext=[1, 64, 29], chunk=256),          # ragged batch
+    dict(H=2, ctx=[513], ext=[77], chunk=192, kv="fp8_e4m3"),         # FP8 cache
+    dict(H=2, ctx=[256], ext=[40], chunk=64, doc=64),                 # relocated documents
+    dict(H=128, ctx=[200], ext=[3], chunk=128),                       # full head count, 3 row tiles
+]
+
+
+def test_absorbed_tiny(api):
+    run_and_compare(api, W.tiny(), absorbed=True)
+
+
+@pytest.mark.parametrize("split", [None, "64", "192"], ids=["auto", "split64", "split192"])
+@pytest.mark.parametrize("case", ABSORBED_CASES, ids=["ragged", "noctx", "batch", "fp8", "docs", "h128"])
+def test_absorbed_small(api, case, split, monkeypatch):
+    """Same workloads as the up-projected path; MLA_ABS_SPLIT_KEYS forces key
+    splits (several partial states per row, projected then merged)."""
+    if split is not None:
+        monkeypatch.setenv("MLA_ABS_SPLIT_KEYS", split)
+    wl = W.make_workload("a", case["H"], case["ctx"], case["ext"], chunk=case["chunk"],
+                         kv_dtype=case.get("kv", "bf16"), doc_len=case.get("doc"), seed=40)
+    run_and_compare(api, wl, absorbed=True)
+
+
+@pytest.mark.parametrize("parts", [1, 2])
+def test_absorbed_parts(api, parts):
+    wl = W.make_workload("ap", 2, [260], [50], chunk=128, seed=41)
+    run_and_compare(api, wl, parts=parts, absorbed=True)
+
+
+def test_absorbed_bf16_out(api):
+    wl = W.make_workload("ab", 2, [190], [70], chunk=128, seed=42)
+    run_and_compare(api, wl, out_dtype=torch.bfloat16, absorbed=True)
+
+
+def test_absorbed_matches_fused_path(api):
+    """Both entry points compute the same function: their outputs agree to the
+    rounding of their different bf16 operands."""
+    wl = W.make_workload("am", 8, [1000], [33], chunk=256, seed=43)
+    dw = api.DeviceWorkload(wl)
+    o1, l1 = dw.run()
+    o2, l2 = dw.run(absorbed=True)
+    torch.cuda.synchronize()
+    assert (o1 - o2).abs().max().item() <= OUT_MAX
+    assert (l1 - l2).abs().max().item() <= LSE_MAX
+
+
+def test_absorbed_long_context_sampled(api):
+    """128 heads, 16K cached tokens (FP8) and 64 new ones: the bench's
+    short-extend shape at a quarter of its context, checked on sampled rows."""
+    wl = W.make_workload("al", 128, [16384], [64], chunk=8192, kv_dtype="fp8_e4m3", seed=44)
+    rows = np.array([0, 1, 31, 62, 63])
+    run_and_compare(api, wl, rows=rows, heads=np.arange(0, 128, 9), absorbed=True)
+
+
+def test_absorbed_bad_block_and_workspace(api):
+    from mla_prefix_cache_gb300 import _lib
+    wl = W.make_workload("ae", 2, [256], [16], chunk=128, seed=45)
+    dw = api.DeviceWorkload(wl)
+    dw.block_table[0, 1] = -5
+    out, lse = dw.run(absorbed=True)
+    torch.cuda.synchronize()
+    assert api.device_error(api.prefill.last_workspace) == 3    # MLA_ERR_BAD_BLOCK_ID
+    assert torch.isfinite(out).all()
+    with pytest.raises(_lib.MLAError):
+        dw.run(absorbed=True, workspace=torch.empty(4096, dtype=torch.uint8, device="cuda"))
