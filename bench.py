@@ -198,24 +198,31 @@ def fused_kernel_name():
     return "fused_prefill_kernel" if os.environ.get("MLA_CTA_PAIR", "1") == "0" else "fused2_prefill_kernel"
 
 
-def kernel_sha():
+KERNEL_SOURCES = {
+    "fused": ("fused.cu", "fused2.cu", "fused_common.cuh", "ptx.cuh", "internal.h"),
+    "absorbed": ("absorb.cu", "ptx.cuh", "internal.h"),
+}
+
+
+def kernel_sha(path="fused"):
     h = hashlib.sha256()
-    for f in ("fused.cu", "fused2.cu", "fused_common.cuh", "ptx.cuh", "internal.h"):
+    for f in KERNEL_SOURCES[path]:
         with open(os.path.join(ROOT, "mla_prefix_cache_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload_name):
-    """DRAM bytes per launch of the fused kernel from a committed ncu summary,
+def measured_traffic(workload_name, path="fused"):
+    """DRAM bytes per launch of the timed kernel from a committed ncu summary,
     valid only while the kernel source is the one that was profiled."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(workload_name)
-    if not e or e.get("kernel_sha") != kernel_sha() or e.get("kernel") != fused_kernel_name():
+    e = d.get(workload_name if path == "fused" else f"{workload_name}/{path}")
+    kernel = fused_kernel_name() if path == "fused" else "absorb_attn_kernel"
+    if not e or e.get("kernel_sha") != kernel_sha(path) or e.get("kernel") != kernel:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -278,6 +285,55 @@ def hbm_kernels(dev, flush, peak_gbs, reps=10):
     return res
 
 
+def absorbed_compare(dev, flush, peak, source, reps=10):
+    """The short-extend workload (128 heads, 32K cached + 64 new tokens)
+    through both entry points on the same inputs: median CUDA-event time of a
+    whole call (L2 flushed before each), and the latent attention kernel's
+    tensor-core roofline."""
+    import torch
+    from mla_prefix_cache_gb300 import api, workload
+
+    wl = workload.short_ext_32k()
+    dw = api.DeviceWorkload(wl, dev)
+    T_q, H = wl.total_q, wl.num_heads
+    out = torch.empty((T_q, H, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for absorbed in (False, True):
+        size_fn = api.absorbed_workspace_size if absorbed else api.prefill_workspace_size
+        ws = torch.empty(size_fn(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            flush.zero_()
+            dw.run(out=out, lse=lse, workspace=ws, absorbed=absorbed)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for k in range(reps):
+            flush.zero_()
+            api.set_kernel_events(*kev[k])
+            ev[k][0].record(stream)
+            dw.run(out=out, lse=lse, workspace=ws, absorbed=absorbed)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        api.set_kernel_events(None, None)
+        if api.device_error(ws) != 0:
+            raise RuntimeError("device error word set in the absorbed comparison")
+        res[absorbed] = (float(statistics.median([a.elapsed_time(b) for a, b in ev])),
+                         float(statistics.median([a.elapsed_time(b) for a, b in kev])))
+        del ws
+    (ms_f, _), (ms_a, kms_a) = res[False], res[True]
+    att = wl.absorbed_attention_flops()
+    achieved = att / (kms_a / 1e3) / 1e12
+    return {"workload": workload_config(wl), "ms_fused": ms_f, "ms_absorbed": ms_a, "speedup": ms_f / ms_a,
+            "prefill_tok_s_absorbed": T_q / (ms_a / 1e3), "prefill_tok_s_fused": T_q / (ms_f / 1e3),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": measured_traffic(wl.name, "absorbed"),
+                         "kernel": "absorb_attn_kernel",
+                         "kernel_ms": kms_a, "peak_source": f"bf16_tflops (burst) of {source} peaks",
+                         "note": "tensor-core FLOPs of the latent attention, 2 (576 + 512) per visible "
+                                 "query-key-head, / its event time"}}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -300,13 +356,14 @@ def run_ours(args):
     T_q, H = wl.total_q, wl.num_heads
     out = torch.empty((T_q, H, 128), dtype=torch.float32, device=dev)
     lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
-    ws = torch.empty(api.prefill_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk),
-                     dtype=torch.uint8, device=dev)
+    absorbed = args.path == "absorbed"
+    size_fn = api.absorbed_workspace_size if absorbed else api.prefill_workspace_size
+    ws = torch.empty(size_fn(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        dw.run(out=out, lse=lse, workspace=ws)
+        dw.run(out=out, lse=lse, workspace=ws, absorbed=absorbed)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -369,7 +426,7 @@ def run_ours(args):
         def e2e_step():
             for name, h in host.items():
                 getattr(dw, name).copy_(h, non_blocking=True)
-            dw.run(out=out, lse=lse, workspace=ws)
+            dw.run(out=out, lse=lse, workspace=ws, absorbed=absorbed)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
 
@@ -399,9 +456,18 @@ def run_ours(args):
     peaks, source = load_peaks()
     peak = float(peaks["bf16_tflops"])
     hbm = None if args.no_hbm_kernels else hbm_kernels(dev, flush, float(peaks["hbm_gbs"]))
+    cmp_abs = None
+    if not args.no_absorbed and world == 1 and not absorbed:
+        cmp_abs = absorbed_compare(dev, flush, peak, source)
     k_ms = sum(kern_ms) / K
-    achieved = flops / (k_ms / 1e3) / 1e12
-    traffic = measured_traffic(wl.name)
+    if absorbed:
+        kflops = wl.absorbed_attention_flops()
+        knote = "achieved = tensor-core FLOPs of the latent attention (2 (576 + 512) per visible query-key-head) / its event time"
+    else:
+        kflops = flops
+        knote = "achieved = algorithmic FLOPs of the step / fused-kernel event time"
+    achieved = kflops / (k_ms / 1e3) / 1e12
+    traffic = measured_traffic(wl.name, args.path)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -413,12 +479,14 @@ def run_ours(args):
         "frac_of_bf16_peak": value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": fused_kernel_name(),
+                     "kernel": "absorb_attn_kernel" if absorbed else fused_kernel_name(),
                      "peak_source": f"bf16_tflops (burst) of {source} peaks",
-                     "kernel_ms": k_ms, "note": "achieved = algorithmic FLOPs of the step / fused-kernel event time"},
+                     "kernel_ms": k_ms, "note": knote},
+        "path": args.path,
         "gpu_launches": int(launches),
         "hbm_kernels": hbm,
         "hbm_peak_source": f"hbm_gbs of {source} peaks",
+        "absorbed": cmp_abs,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clk,
@@ -436,6 +504,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="v3_8k")
+    ap.add_argument("--path", choices=["fused", "absorbed"], default="fused",
+                    help="entry point timed: mla_prefill_ctx (up-projected, fused) or mla_prefill_ctx_absorbed")
+    ap.add_argument("--no-absorbed", action="store_true",
+                    help="skip the absorbed-vs-fused comparison on the short-extend workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hbm-kernels", action="store_true")

@@ -596,12 +596,12 @@ static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int 
 }
 
 struct AbsWs {
-  size_t gath_off = 0, qlat_off = 0, lat_out_off = 0, lat_lse_off = 0, part_out_off = 0, part_lse_off = 0, total = 0;
+  size_t gath_off = 0, qlat_off = 0, lat_out_off = 0, lat_lse_off = 0, total = 0;
 };
 
 // Workspace of the absorbed path: header (error word), gathered rows, the
-// absorbed queries, the latent partial states of every slot, and (for requests
-// with several slots) their projected partial states for the merge.
+// absorbed queries and the latent states of every slot (a request's slots are
+// merged into slot 0 before the output projection).
 static AbsWs abs_ws_layout(const FusedPlan& fp, const AbsPlan& ap, int H) {
   AbsWs w;
   const size_t rows = (size_t)fp.total_q * (size_t)H;
@@ -610,10 +610,7 @@ static AbsWs abs_ws_layout(const FusedPlan& fp, const AbsPlan& ap, int H) {
   w.qlat_off = up256(w.gath_off + (size_t)fp.gather_blocks * kBlock * kRowBytesBf16);
   w.lat_out_off = up256(w.qlat_off + rows * kDc * sizeof(uint16_t));
   w.lat_lse_off = up256(w.lat_out_off + slots * rows * kDc * sizeof(float));
-  w.part_out_off = up256(w.lat_lse_off + slots * rows * sizeof(float));
-  const size_t part_slots = ap.any_merge ? slots : 0;
-  w.part_lse_off = up256(w.part_out_off + part_slots * rows * kDv * sizeof(float));
-  w.total = up256(w.part_lse_off + part_slots * rows * sizeof(float));
+  w.total = up256(w.lat_lse_off + slots * rows * sizeof(float));
   return w;
 }
 
@@ -638,15 +635,20 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
   const uint64_t rows_total = (uint64_t)std::max(fp.gather_blocks, 1) * kBlock;
   bool ok = true;
   {
-    // the latent part of a row as 8 blocks of 64 columns: (column, row, block)
+    // the latent part of a row as 8 blocks of 64 columns: (column, row, block); a box is 4 blocks
     const uint64_t d[3] = {64, rows_total, 8};
     const uint64_t st[2] = {(uint64_t)kRowBytesBf16, 128};
-    const uint32_t b[3] = {64, (uint32_t)64, 8};
-    ok &= encode_map(&p.tm_c8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rows_base, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint32_t b[3] = {64, (uint32_t)64, 4};
+    ok &= encode_map(&p.tm_c4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rows_base, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
     const uint64_t d2[2] = {(uint64_t)kRowBf16, rows_total};
     const uint64_t st2[1] = {(uint64_t)kRowBytesBf16};
     const uint32_t b2[2] = {64, 64};
     ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint64_t d3[2] = {(uint64_t)kDc, (uint64_t)T_q * H};
+    const uint64_t st3[1] = {(uint64_t)kDc * 2};
+    const uint32_t b3[2] = {64, 128};
+    ok &= encode_map(&p.tm_qlat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + aw.qlat_off, d3, st3, b3,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return MLA_ERR_CUDA;
 
@@ -675,6 +677,11 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
   p.num_heads = H;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   rope_fracs((double)rope_theta, p.rope_frac);
+  // tracing: per-tile timestamps of one work item (MLA_ABS_TRACE_ITEM, default 0)
+  void* tr = g_trace.load();
+  p.trace = (tr != nullptr && g_trace_bytes.load() >= (size_t)8 * 4096 * 8) ? static_cast<unsigned long long*>(tr)
+                                                                             : nullptr;
+  p.trace_item = env_int("MLA_ABS_TRACE_ITEM", 0);
   cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
   cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
   if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_b, s))) != MLA_OK) return st;
@@ -694,41 +701,15 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
   }
   if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_e, s))) != MLA_OK) return st;
 
-  std::memset(&pp, 0, sizeof(pp));
-  pp.lat_out = p.lat_out;
-  pp.lat_lse = p.lat_lse;
-  pp.lat_slot_stride_rows = T_q * H;
-  pp.w = static_cast<const uint16_t*>(kv_b_proj);
-  pp.out = out;
-  pp.lse = lse;
-  pp.part_out = reinterpret_cast<float*>(ws + aw.part_out_off);
-  pp.part_lse = reinterpret_cast<float*>(ws + aw.part_lse_off);
-  pp.part_slot_stride_rows = T_q;
-  pp.out_bf16 = out_dtype == MLA_OUT_BF16;
-  pp.scale = vscale;
-  pp.num_heads = H;
-  pp.max_slots = std::max(ap.max_slots, 1);
-  for (size_t b0 = 0; b0 < ap.ranges.size(); b0 += kMaxRangesPerLaunch) {
-    const size_t n = std::min(ap.ranges.size() - b0, (size_t)kMaxRangesPerLaunch);
-    int rows = 0;
-    for (size_t i = 0; i < n; ++i) {
-      RowRange rr = ap.ranges[b0 + i];
-      rr.prefix = rows;
-      rows += rr.row_end - rr.row_begin;
-      pp.ranges[i] = rr;
-    }
-    pp.num_ranges = (int)n;
-    pp.total_rows = rows;
-    if ((st = cuda_status(launch_absorb_proj(pp, s))) != MLA_OK) return st;
-  }
+  // fold each request's slots into slot 0, in latent space
   if (ap.any_merge) {
     std::memset(&mp, 0, sizeof(mp));
-    mp.part_out = pp.part_out;
-    mp.part_lse = pp.part_lse;
+    mp.part_out = p.lat_out;
+    mp.part_lse = p.lat_lse;
     mp.slot_stride_rows = T_q;
-    mp.out = out;
-    mp.lse = lse;
-    mp.out_bf16 = pp.out_bf16;
+    mp.out = p.lat_out;
+    mp.lse = p.lat_lse;
+    mp.out_bf16 = 0;
     mp.num_heads = H;
     std::vector<RowRange> multi;
     for (const RowRange& rr : ap.ranges)
@@ -744,8 +725,30 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
       }
       mp.num_ranges = (int)n;
       mp.total_rows = rows;
-      if ((st = cuda_status(launch_merge_slots(mp, s))) != MLA_OK) return st;
+      if ((st = cuda_status(launch_merge_slots_latent(mp, s))) != MLA_OK) return st;
     }
+  }
+  std::memset(&pp, 0, sizeof(pp));
+  pp.lat_out = p.lat_out;
+  pp.lat_lse = p.lat_lse;
+  pp.w = static_cast<const uint16_t*>(kv_b_proj);
+  pp.out = out;
+  pp.lse = lse;
+  pp.out_bf16 = out_dtype == MLA_OUT_BF16;
+  pp.scale = vscale;
+  pp.num_heads = H;
+  for (size_t b0 = 0; b0 < ap.ranges.size(); b0 += kMaxRangesPerLaunch) {
+    const size_t n = std::min(ap.ranges.size() - b0, (size_t)kMaxRangesPerLaunch);
+    int rows = 0;
+    for (size_t i = 0; i < n; ++i) {
+      RowRange rr = ap.ranges[b0 + i];
+      rr.prefix = rows;
+      rows += rr.row_end - rr.row_begin;
+      pp.ranges[i] = rr;
+    }
+    pp.num_ranges = (int)n;
+    pp.total_rows = rows;
+    if ((st = cuda_status(launch_absorb_proj(pp, s))) != MLA_OK) return st;
   }
   return MLA_OK;
 }

@@ -19,11 +19,17 @@
 //    S = Q [c | k_rope]^T for 64 keys per tile (M = 128, N = 64), runs the
 //    online softmax and sends P (bf16) and each row's rescale factor into CTA
 //    1's shared memory with st.async;
-//  - CTA 1 ("O side") accumulates O += P c (two N = 256 MMAs per 16 keys),
-//    rescales O rows in TMEM when the S side raised a row maximum, and writes
-//    O / l at the end.
-// Each 64-key stage of latent rows reaches both CTAs by one multicast TMA;
-// k_rope goes to the S side only.
+//  - CTA 1 ("O side") accumulates O += P c (two N = 256 MMAs per 16 keys)
+//    and writes O / l at the end.  With each P tile comes one flag per S-side
+//    warp, set when one of its rows raised its maximum (the lazy rescale, so
+//    rarely after the first tiles): only then does the MMA thread wait for the
+//    previous PV and hand the tile to the correction warps, which rescale
+//    those rows of O in TMEM before the tile's PV.
+// Each CTA loads its own 64-key stages (the S side latent + k_rope, the O
+// side latent only) and frees a stage as soon as its own MMA has read it: a
+// stage shared by multicast would stay busy from its load until the O side's
+// PV, a chain that three stages cannot cover.  The rows are read by every row
+// tile of the piece and stay in L2.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -35,25 +41,29 @@ constexpr int kAKeys = 64;
 constexpr int kAStages = 3;
 constexpr uint32_t kAAtom = 8192;                              // [64 rows x 128 B] swizzled block
 constexpr uint32_t kACStage = 8 * kAAtom;                      // latent part of 64 rows
-constexpr uint32_t kACBase = 0;                                // both CTAs: multicast destination
+constexpr uint32_t kACBase = 0;                                // both CTAs
 constexpr uint32_t kAKrBase = kACBase + kAStages * kACStage;   // S side: k_rope of each stage
 constexpr uint32_t kAPBase = kAKrBase;                         // O side: two P tiles [128 x 64] bf16
 constexpr uint32_t kAPBytes = 16384;
 constexpr uint32_t kAAlphaBase = kAPBase + 2 * kAPBytes;       // O side: per P tile, 128 row factors
 constexpr uint32_t kALBase = kAAlphaBase + 2 * 512;            // O side: 128 final row sums
-constexpr uint32_t kABarBase = kALBase + 512;
+constexpr uint32_t kAFlagBase = kALBase + 512;                 // O side: per P tile, 4 rescale flags; then
+                                                               // the tile handed to the correction warps
+constexpr uint32_t kABarBase = kAFlagBase + 2 * 16 + 16;
 enum : uint32_t {
   kBFull = 0,      // 3, both: stage landed (S side: latent + k_rope; O side: latent)
-  kBEmpty = 3,     // 3, S side: S MMA and PV of the stage done (2 arrivals)
+  kBEmpty = 3,     // 3, both: the CTA's MMA that reads the stage is done
   kBSFull = 6,     // 2, S side: S buffer written
   kBSFree = 8,     // 2, S side: the 4 softmax warps read the S buffer
   kBPFree = 10,    // 2, S side: PV of the P tile done (commit from the O side)
-  kBQReady = 12,   // S side: the 4 softmax warps wrote Q into TMEM
-  kBPFull = 13,    // 2, O side: P tile and row factors landed
-  kBCDone = 15,    // 2, O side: the 4 correction warps handled the tile
+  kBQReady = 12,   // S side: the 4 softmax warps copied Q into TMEM (stages 1-2 free again)
+  kBPFull = 13,    // 2, O side: P tile, row factors and flags landed
+  kBCNeed = 15,    // O side: the MMA thread handed a tile (or the end) to the correction warps
+  kBCDone = 16,    // O side: the 4 correction warps rescaled the tile's rows
   kBPvDone = 17,   // 2, O side: PV of the tile done
   kBLFull = 19,    // O side: the final row sums landed
-  kANumBars = 20
+  kBQFull = 20,    // S side: the tile's absorbed queries landed in stages 1-2
+  kANumBars = 21
 };
 constexpr uint32_t kATmemSlot = kABarBase + 8 * kANumBars;
 constexpr uint32_t kASmemBytes = kATmemSlot + 16 + 1024;       // + alignment of the base to 1024
@@ -65,7 +75,9 @@ constexpr uint32_t kIdescSA = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescPVA = idesc_bf16(128, 256, false, true);
 constexpr uint32_t kTxS = kACStage + kAAtom;
 constexpr uint32_t kTxO = kACStage;
-constexpr uint32_t kTxP = 128 * (128 + 4);   // per row: 64 bf16 of P and one fp32 factor
+constexpr uint32_t kTxQ = 8 * 16384;          // qlat of 128 rows, 8 boxes [128 rows x 64]
+constexpr uint32_t kAQStage = kACBase + kACStage;   // S side: qlat staged over stages 1-2 at the start
+constexpr uint32_t kTxP = 128 * (128 + 4) + 16;   // per row: 64 bf16 of P and one fp32 factor; 4 flags
 constexpr float kARescale = 8.f;             // log2 units: P stays <= 256
 
 __device__ __forceinline__ uint32_t abar(uint32_t sbase, uint32_t i) { return sbase + kABarBase + 8u * i; }
@@ -78,6 +90,15 @@ __device__ __forceinline__ bool await(const AbsorbParams& p, uint32_t bar, uint3
 }
 __device__ __forceinline__ bool await_warp(const AbsorbParams& p, uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, await(p, bar, parity));
+}
+
+// Optional tracing (p.trace non-null): %globaltimer of each tile j of work
+// item p.trace_item (j < 4096) in words 8 j + k:
+//   [0] S side: loads issued    [1] S MMA thread: stage landed   [2] S issued
+//   [3] softmax saw S           [4] P computed (before waiting for its tile buffer)
+//   [5] P sent                  [6] O side: PV issued            [7] O side: P landed
+__device__ __forceinline__ void tstamp(const AbsorbParams& p, bool on, int j, int k) {
+  if (on && j < 4096) p.trace[8 * j + k] = global_timer_ns();
 }
 
 struct AItem {
@@ -122,14 +143,15 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
   const AbsPiece& P = *it.P;
   const int H = p.num_heads;
   const int n = it.n_tiles;
+  const bool tr = p.trace != nullptr && (int)(blockIdx.x >> 1) == p.trace_item;
 
   if (tid == 0) {
-    prefetch_tensormap(&p.tm_c8);
+    prefetch_tensormap(&p.tm_c4);
     prefetch_tensormap(&p.tm_kr);
+    prefetch_tensormap(&p.tm_qlat);
     for (uint32_t i = 0; i < kANumBars; ++i) {
       uint32_t cnt = 1;
-      if (i >= kBEmpty && i < kBEmpty + 3) cnt = 2;
-      if ((i >= kBSFree && i < kBSFree + 2) || i == kBQReady || (i >= kBCDone && i < kBCDone + 2)) cnt = 4;
+      if ((i >= kBSFree && i < kBSFree + 2) || i == kBQReady || i == kBCDone) cnt = 4;
       mbar_init(abar(sbase, i), cnt);
     }
     fence_mbar_init();
@@ -146,21 +168,40 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
 
   if (rank == 0) {
     // ================================================================ S side
-    if (warp == 0) {
-      // ---------------------------------------------------------- TMA
+    if (warp == 0 || warp == 2 || warp == 3) {
+      // ---------------------------------------------------------- TMA: a stage's boxes leave from three
+      // warps (warp 0: latent blocks 0-3, warp 3: blocks 4-7, warp 2: k_rope), since the per-SM load
+      // rate grows with the number of issuing warps; warp 0 arms the stage's barrier and loads Q
       if (lane == 0) {
         bool ok = true;
+        if (warp == 0 && n > 0) {
+          // the tile's absorbed queries: rows q_begin H + row0 .. +127 of qlat, staged over stages 1-2
+          mbar_arrive_expect_tx(abar(sbase, kBQFull), kTxQ);
+          const int qrow = P.q_begin * H + it.row0;
+#pragma unroll 1
+          for (int cc = 0; cc < 8; ++cc)
+            tma_load_2d(sbase + kAQStage + cc * 16384, &p.tm_qlat, 64 * cc, qrow, abar(sbase, kBQFull));
+        }
         for (int j = 0; j < n && ok; ++j) {
           const int s = j % kAStages;
           if (j >= kAStages && !await(p, abar(sbase, kBEmpty + s), ((j / kAStages) - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(abar(sbase, kBFull + s), kTxS);
+          if (j == 1 && !await(p, abar(sbase, kBQReady), 0)) { ok = false; break; }   // Q copied out of stages 1-2
           const int row = (int)(row_base + it.t0 + kAKeys * j);
-          tma_load_3d_mc(sbase + kACBase + s * kACStage, &p.tm_c8, 0, row, 0, abar(sbase, kBFull + s), 3);
-          tma_load_2d(sbase + kAKrBase + s * kAAtom, &p.tm_kr, kDc, row, abar(sbase, kBFull + s));
+          const uint32_t full = abar(sbase, kBFull + s);
+          if (warp == 0) {
+            mbar_arrive_expect_tx(full, kTxS);
+            tstamp(p, tr, j, 0);
+            tma_load_3d(sbase + kACBase + s * kACStage, &p.tm_c4, 0, row, 0, full);
+          } else if (warp == 3) {
+            tma_load_3d(sbase + kACBase + s * kACStage + 4 * kAAtom, &p.tm_c4, 0, row, 4, full);
+          } else {
+            tma_load_2d(sbase + kAKrBase + s * kAAtom, &p.tm_kr, kDc, row, full);
+          }
         }
-        // the O side's last PV commits land on this CTA's barriers before it exits
-        for (int j = max(0, n - kAStages); j < n && ok; ++j)
-          if (!await(p, abar(sbase, kBEmpty + j % kAStages), (j / kAStages) & 1)) ok = false;
+        // the last commits land on this CTA's barriers before it exits
+        if (warp == 0)
+          for (int j = max(0, n - kAStages); j < n && ok; ++j)
+            if (!await(p, abar(sbase, kBEmpty + j % kAStages), (j / kAStages) & 1)) ok = false;
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------- S = Q [c | k_rope]^T
@@ -169,6 +210,7 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
         for (int j = 0; j < n && ok; ++j) {
           const int s = j % kAStages, b = j & 1;
           if (!await(p, abar(sbase, kBFull + s), (j / kAStages) & 1)) { ok = false; break; }
+          tstamp(p, tr, j, 1);
           if (j >= 2 && !await(p, abar(sbase, kBSFree + b), ((j >> 1) - 1) & 1)) { ok = false; break; }
           tc_fence_after();
           const uint32_t c = sbase + kACBase + s * kACStage, kr = sbase + kAKrBase + s * kAAtom;
@@ -181,6 +223,7 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
           }
           mma_commit(abar(sbase, kBSFull + b));
           mma_commit(abar(sbase, kBEmpty + s));
+          tstamp(p, tr, j, 2);
         }
       }
     } else if (warp >= 4) {
@@ -192,25 +235,17 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
       const int64_t grow = (int64_t)P.q_begin + tl;
       const int64_t orow = grow * H + h;
       const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-      {
-        const uint4* ql = reinterpret_cast<const uint4*>(p.qlat + orow * kDc);
-#pragma unroll 1
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t w[32];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 a = live ? __ldg(ql + 8 * cc + i) : make_uint4(0, 0, 0, 0);
-            w[4 * i] = a.x; w[4 * i + 1] = a.y; w[4 * i + 2] = a.z; w[4 * i + 3] = a.w;
-          }
-          tmem_st32(tmem + lane_off + 32 * cc, w);
-        }
+      if (n > 0) {
+        // rotated q_rope from global memory (its loads overlap the qlat TMA)
         const uint4* qr = reinterpret_cast<const uint4*>(p.q + orow * kDqk + kDnope);
         const int64_t delta = live ? (int64_t)__ldg(p.q_pos + grow) - P.rope_offset : 0;
+        uint4 qv[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) qv[c] = live ? __ldg(qr + c) : make_uint4(0, 0, 0, 0);
         uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 a = live ? __ldg(qr + c) : make_uint4(0, 0, 0, 0);
-          const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+          const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float sn, cs;
@@ -220,6 +255,20 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
           }
         }
         tmem_st32(tmem + lane_off + 256, w);
+        // qlat: shared memory (TMA, 128-byte swizzled [128 x 64] blocks) -> TMEM columns 0..255
+        const bool qok = await_warp(p, abar(sbase, kBQFull), 0);
+#pragma unroll 1
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t u[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t v4[4];
+            if (qok) lds128(sbase + kAQStage + cc * 16384 + sw128_off((uint32_t)r, (uint32_t)c), v4);
+            else v4[0] = v4[1] = v4[2] = v4[3] = 0u;
+            u[4 * c] = v4[0]; u[4 * c + 1] = v4[1]; u[4 * c + 2] = v4[2]; u[4 * c + 3] = v4[3];
+          }
+          tmem_st32(tmem + lane_off + 32 * cc, u);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -241,21 +290,30 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
         __syncwarp();
         if (lane == 0) mbar_arrive(abar(sbase, kBSFree + b));
         if (!ok) break;
+        if (tid == 128) tstamp(p, tr, j, 3);
         const int kt0 = it.t0 + kAKeys * j;
-        float mx = -INFINITY;
+        float m8[8];
         if (kt0 >= it.k_lo && kt0 + kAKeys - 1 < it.k_hi && kt0 + kAKeys - 1 <= qk) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(v[c]));
+          for (int i = 0; i < 8; ++i) m8[i] = fmax3(__uint_as_float(v[i]), __uint_as_float(v[i + 8]), __uint_as_float(v[i + 16]));
+#pragma unroll
+          for (int c = 24; c < 64; c += 8)
+#pragma unroll
+            for (int i = 0; i < 8; i += 2)
+              m8[i >> 1] = fmax3(m8[i >> 1], __uint_as_float(v[c + i]), __uint_as_float(v[c + i + 1]));
         } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const int kt = kt0 + c;
             const bool vis = kt >= it.k_lo && kt < it.k_hi && kt <= qk;
             const float x = vis ? __uint_as_float(v[c]) : -INFINITY;
             v[c] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
+            m8[c & 7] = fmaxf(m8[c & 7], x);
           }
         }
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         const float m_tile = mx * sl2;
         float alpha = 1.f;
         if (m_tile > m_used + kARescale) {
@@ -263,16 +321,22 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
           m_used = m_tile;
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-        float sum = 0.f;
+        const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-mref, -mref);
+        uint64_t s4[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float a = ex2(fmaf(__uint_as_float(v[2 * c]), sl2, -mref));
-          const float bb = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sl2, -mref));
-          sum += a + bb;
+          float x0, x1;
+          f2unpack(ffma2(f2pack(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])), sc2, nm2), x0, x1);
+          const float a = ex2(x0), bb = ex2(x1);
+          s4[c & 3] = fadd2(s4[c & 3], f2pack(a, bb));
           pk[c] = pack_bf16(a, bb);
         }
-        l = l * alpha + sum;
+        float s8[4];
+        f2unpack(fadd2(s4[0], s4[1]), s8[0], s8[1]);
+        f2unpack(fadd2(s4[2], s4[3]), s8[2], s8[3]);
+        l = l * alpha + ((s8[0] + s8[2]) + (s8[1] + s8[3]));
+        if (tid == 128) tstamp(p, tr, j, 4);
         // P tile b is free once the PV of tile j - 2 is done
         if (j >= 2 && !await_warp(p, abar(sbase, kBPFree + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
         const uint32_t cbar = mapa_shared(abar(sbase, kBPFull + b), 1u);
@@ -282,6 +346,9 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
           st_async_v4(prow_addr + sw128_off((uint32_t)r, (uint32_t)c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
                       pk[4 * c + 3], cbar);
         st_async_b32(peer_alpha + b * 512 + 4 * r, __float_as_uint(alpha), cbar);
+        const uint32_t any_rescale = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
+        if (lane == 0) st_async_b32(mapa_shared(sbase + kAFlagBase + 16 * b + 4 * (warp & 3), 1u), any_rescale, cbar);
+        if (tid == 128) tstamp(p, tr, j, 5);
       }
       // final row sums to the O side; lse of the item
       st_async_b32(mapa_shared(sbase + kALBase + 4 * r, 1u), __float_as_uint(ok ? l : 0.f),
@@ -296,17 +363,51 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
     }
   } else {
     // ================================================================ O side
-    if (warp == 1) {
+    if (warp == 0 || warp == 3) {
+      // ---------------------------------------------------------- TMA (latent rows; blocks 0-3 from warp 0,
+      // which arms the barrier, blocks 4-7 from warp 3)
+      if (lane == 0) {
+        bool ok = true;
+        for (int j = 0; j < n && ok; ++j) {
+          const int s = j % kAStages;
+          if (j >= kAStages && !await(p, abar(sbase, kBEmpty + s), ((j / kAStages) - 1) & 1)) { ok = false; break; }
+          const int row = (int)(row_base + it.t0 + kAKeys * j);
+          if (warp == 0) {
+            mbar_arrive_expect_tx(abar(sbase, kBFull + s), kTxO);
+            tma_load_3d(sbase + kACBase + s * kACStage, &p.tm_c4, 0, row, 0, abar(sbase, kBFull + s));
+          } else {
+            tma_load_3d(sbase + kACBase + s * kACStage + 4 * kAAtom, &p.tm_c4, 0, row, 4, abar(sbase, kBFull + s));
+          }
+        }
+        if (warp == 0)
+          for (int j = max(0, n - kAStages); j < n && ok; ++j)
+            if (!await(p, abar(sbase, kBEmpty + j % kAStages), (j / kAStages) & 1)) ok = false;
+      }
+    } else if (warp == 1) {
       // ---------------------------------------------------------- O += P c
       if (lane == 0) {
-        for (int s = 0; s < min(n, kAStages); ++s) mbar_arrive_expect_tx(abar(sbase, kBFull + s), kTxO);
         for (int b = 0; b < min(n, 2); ++b) mbar_arrive_expect_tx(abar(sbase, kBPFull + b), kTxP);
         mbar_arrive_expect_tx(abar(sbase, kBLFull), 512);
         bool ok = true;
+        volatile int* hand = reinterpret_cast<volatile int*>(sgen + kAFlagBase + 32);
+        int events = 0;
         for (int j = 0; j < n && ok; ++j) {
           const int s = j % kAStages, b = j & 1;
           if (!await(p, abar(sbase, kBFull + s), (j / kAStages) & 1)) { ok = false; break; }
-          if (!await(p, abar(sbase, kBCDone + b), (j >> 1) & 1)) { ok = false; break; }
+          if (!await(p, abar(sbase, kBPFull + b), (j >> 1) & 1)) { ok = false; break; }
+          tstamp(p, tr, j, 7);
+          if (j > 0) {
+            uint32_t f[4];
+            lds128(sbase + kAFlagBase + 16 * b, f);
+            if (f[0] | f[1] | f[2] | f[3]) {
+              // O must hold PV of every earlier tile before its rows are rescaled
+              if (!await(p, abar(sbase, kBPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
+              *hand = b;
+              mbar_arrive(abar(sbase, kBCNeed));
+              if (!await(p, abar(sbase, kBCDone), events & 1)) { ok = false; break; }
+              ++events;
+            }
+          }
           fence_proxy_async_smem();   // P was written by the peer's stores, the MMA reads it as an operand
           tc_fence_after();
           const uint32_t c = sbase + kACBase + s * kACStage, pt = sbase + kAPBase + b * kAPBytes;
@@ -319,11 +420,13 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
                        kIdescPVA, (j > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(abar(sbase, kBPvDone + b));
-          mma_commit_mc(abar(sbase, kBEmpty + s), 1);
+          mma_commit(abar(sbase, kBEmpty + s));
+          tstamp(p, tr, j, 6);
           mma_commit_mc(abar(sbase, kBPFree + b), 1);
-          if (j + kAStages < n) mbar_arrive_expect_tx(abar(sbase, kBFull + s), kTxO);
           if (j + 2 < n) mbar_arrive_expect_tx(abar(sbase, kBPFull + b), kTxP);
         }
+        *hand = -1;   // no more tiles: the correction warps go on to the epilogue
+        mbar_arrive(abar(sbase, kBCNeed));
       }
     } else if (warp >= 4) {
       // ---------------------------------------------------------- rescale O rows; epilogue
@@ -334,31 +437,28 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
       const int64_t orow = ((int64_t)P.q_begin + tl) * H + h;
       const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
       const float* alpha_s = reinterpret_cast<const float*>(sgen + kAAlphaBase);
+      const volatile int* hand = reinterpret_cast<const volatile int*>(sgen + kAFlagBase + 32);
       bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        const int b = j & 1;
-        if (ok && !await_warp(p, abar(sbase, kBPFull + b), (j >> 1) & 1)) ok = false;
-        const float a = ok ? alpha_s[b * 128 + r] : 1.f;
-        if (ok && j > 0 && __any_sync(0xffffffffu, a != 1.f)) {
-          // O holds PV of tiles < j: PV(j - 1) must be done (PV(j - 2) is, P tile j needed it)
-          if (!await_warp(p, abar(sbase, kBPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) ok = false;
-          tc_fence_after();
-          if (ok) {
+      for (int ev = 0;; ++ev) {
+        if (!await_warp(p, abar(sbase, kBCNeed), ev & 1)) { ok = false; break; }
+        const int b = *hand;
+        if (b < 0) break;
+        tc_fence_after();
+        const float a = alpha_s[b * 128 + r];
+        if (__any_sync(0xffffffffu, a != 1.f)) {
 #pragma unroll 1
-            for (int cc = 0; cc < 16; ++cc) {
-              uint32_t o[32];
-              tmem_ld32(tmem + lane_off + 32 * cc, o);
+          for (int cc = 0; cc < 16; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + 32 * cc, o);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-              tmem_st32(tmem + lane_off + 32 * cc, o);
-            }
-            tmem_wait_st();
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+            tmem_st32(tmem + lane_off + 32 * cc, o);
           }
+          tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(abar(sbase, kBCDone + b));
-        if (!ok) break;
+        if (lane == 0) mbar_arrive(abar(sbase, kBCDone));
       }
       if (ok && n > 0 && !await_warp(p, abar(sbase, kBPvDone + ((n - 1) & 1)), ((n - 1) >> 1) & 1)) ok = false;
       if (ok && !await_warp(p, abar(sbase, kBLFull), 0)) ok = false;
@@ -453,31 +553,26 @@ __global__ void __launch_bounds__(256) qabsorb_kernel(const QAbsorbParams p) {
 
 // ---------------------------------------------------------------- output projection
 // Block: 32 rows (tokens of the launch's ranges) x 128 output columns of one
-// head and one slot; the 512 latent columns in chunks of 64.
+// head; the 512 latent columns in chunks of 64.
 __global__ void __launch_bounds__(256) absorb_proj_kernel(const __grid_constant__ ProjParams p) {
   __shared__ float as[32][64 + 4];
   __shared__ __align__(16) uint16_t ws[64][128];
   __shared__ int64_t grow_s[32];
-  __shared__ int nslots_s[32];
   const int H = p.num_heads;
-  const int h = blockIdx.z, slot = blockIdx.y, r0 = blockIdx.x * 32;
+  const int h = blockIdx.z, r0 = blockIdx.x * 32;
   const int tid = threadIdx.x;
   if (tid < 32) {
     const int x = r0 + tid;
     int64_t g = -1;
-    int ns = 0;
     if (x < p.total_rows) {
       int lo = 0, hi = p.num_ranges - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (p.ranges[mid].prefix <= x) lo = mid; else hi = mid - 1;
       }
-      const RowRange rr = p.ranges[lo];
-      g = rr.row_begin + (x - rr.prefix);
-      ns = rr.nslots;
+      g = p.ranges[lo].row_begin + (x - p.ranges[lo].prefix);
     }
-    grow_s[tid] = (slot < ns) ? g : -1;
-    nslots_s[tid] = ns;
+    grow_s[tid] = g;
   }
   __syncthreads();
   const int64_t wrow = (int64_t)H * (kDnope + kDv);
@@ -488,9 +583,7 @@ __global__ void __launch_bounds__(256) absorb_proj_kernel(const __grid_constant_
       const int t = i >> 4, ch = i & 15;
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
       const int64_t g = grow_s[t];
-      if (g >= 0)
-        a = __ldg(reinterpret_cast<const float4*>(p.lat_out + ((int64_t)slot * p.lat_slot_stride_rows + g * H + h) * kDc +
-                                                  k0) + ch);
+      if (g >= 0) a = __ldg(reinterpret_cast<const float4*>(p.lat_out + (g * H + h) * kDc + k0) + ch);
       as[t][4 * ch] = a.x; as[t][4 * ch + 1] = a.y; as[t][4 * ch + 2] = a.z; as[t][4 * ch + 3] = a.w;
     }
     for (int i = tid; i < 64 * 16; i += 256) {
@@ -517,27 +610,19 @@ __global__ void __launch_bounds__(256) absorb_proj_kernel(const __grid_constant_
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int t = 4 * ty + i;
-    const int64_t g = grow_s[t];
+    const int64_t g = grow_s[4 * ty + i];
     if (g < 0) continue;
     const float o0 = acc[i][0] * p.scale, o1 = acc[i][1] * p.scale, o2 = acc[i][2] * p.scale, o3 = acc[i][3] * p.scale;
-    const int64_t lrow = (int64_t)slot * p.lat_slot_stride_rows + g * H + h;
-    if (nslots_s[t] == 1) {
-      const int64_t o = (g * H + h) * kDv + 4 * tx;
-      if (p.out_bf16) {
-        uint2 v;
-        v.x = pack_bf16(o0, o1);
-        v.y = pack_bf16(o2, o3);
-        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o) = v;
-      } else {
-        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = make_float4(o0, o1, o2, o3);
-      }
-      if (tx == 0) p.lse[g * H + h] = p.lat_lse[lrow];
+    const int64_t o = (g * H + h) * kDv + 4 * tx;
+    if (p.out_bf16) {
+      uint2 v;
+      v.x = pack_bf16(o0, o1);
+      v.y = pack_bf16(o2, o3);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o) = v;
     } else {
-      const int64_t prow = (int64_t)slot * p.part_slot_stride_rows * H + g * H + h;
-      *reinterpret_cast<float4*>(p.part_out + prow * kDv + 4 * tx) = make_float4(o0, o1, o2, o3);
-      if (tx == 0) p.part_lse[prow] = p.lat_lse[lrow];
+      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = make_float4(o0, o1, o2, o3);
     }
+    if (tx == 0) p.lse[g * H + h] = p.lat_lse[g * H + h];
   }
 }
 
@@ -584,7 +669,7 @@ cudaError_t launch_qabsorb(const QAbsorbParams& p, cudaStream_t s) {
 
 cudaError_t launch_absorb_proj(const ProjParams& p, cudaStream_t s) {
   if (p.total_rows == 0) return cudaSuccess;
-  const dim3 grid((p.total_rows + 31) / 32, p.max_slots, p.num_heads);
+  const dim3 grid((p.total_rows + 31) / 32, 1, p.num_heads);
   absorb_proj_kernel<<<grid, 256, 0, s>>>(p);
   count_launch();
   return cudaGetLastError();

@@ -141,6 +141,8 @@ int fused2_smem_bytes();
 
 // Kernel launchers (return cudaError_t of the launch).
 cudaError_t launch_merge_slots(const MergeParams& p, cudaStream_t s);
+// The same merge over 512-wide fp32 latent states ([slots][T_q][H][512]).
+cudaError_t launch_merge_slots_latent(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_merge2(const float* oa, const float* la, const float* ob, const float* lb,
                           float* o, float* l, int64_t rows, int d_v, cudaStream_t s);
 cudaError_t launch_rope(const uint16_t* x, const int32_t* pos, int64_t offset, const uint64_t* frac_host,
@@ -194,8 +196,9 @@ struct AbsPiece {
 constexpr int kMaxAbsPieces = 448;
 
 struct AbsorbParams {
-  CUtensorMap tm_c8;   // gathered rows: the latent part of 64 rows as 8 swizzled [64 x 64] blocks
+  CUtensorMap tm_c4;   // gathered rows: half the latent part of 64 rows as 4 swizzled [64 x 64] blocks
   CUtensorMap tm_kr;   // gathered rows, box 64 x 64 (k_rope at column 512)
+  CUtensorMap tm_qlat; // qlat as [T_q * H rows][512], box 64 x 128
   const uint16_t* q;     // [T_q][H][192]: q_rope at 128..191, not rotated
   const uint16_t* qlat;  // [T_q][H][512] bf16: kv_scale * q_nope W_UK,h^T
   const int32_t* q_pos;
@@ -207,6 +210,8 @@ struct AbsorbParams {
   int n_pieces;
   int n_items;
   float scale_log2;
+  unsigned long long* trace;   // optional: per-tile timestamps of work item trace_item (see absorb.cu)
+  int trace_item;
   uint64_t rope_frac[kDr / 2];
   AbsPiece pieces[kMaxAbsPieces];
 };
@@ -222,23 +227,19 @@ struct QAbsorbParams {
   int num_heads;
 };
 
-// Output projection of the latent partials: for each request row range and
-// slot < nslots, o[t][h][d] = scale * sum_c lat[slot][t H + h][c] W[c][128 H + 128 h + d];
-// one slot -> the final out / lse, several -> part_out / part_lse for the merge.
+// Output projection of the latent states: for the rows of each request
+// range, out[t][h][d] = scale * sum_c lat[t H + h][c] W[c][128 H + 128 h + d]
+// and lse[t][h] = lat_lse[t H + h] (slot 0, where a request's splits were
+// merged).
 struct ProjParams {
-  const float* lat_out;
-  const float* lat_lse;
-  int64_t lat_slot_stride_rows;   // T_q * H
+  const float* lat_out;           // [T_q * H][512]
+  const float* lat_lse;           // [T_q * H]
   const uint16_t* w;
   void* out;
   float* lse;
-  float* part_out;                // [slots][T_q][H][128]
-  float* part_lse;                // [slots][T_q][H]
-  int64_t part_slot_stride_rows;  // T_q
   int out_bf16;
   float scale;
   int num_heads;
-  int max_slots;
   int num_ranges;
   int total_rows;                 // tokens of this launch's ranges
   RowRange ranges[kMaxRangesPerLaunch];

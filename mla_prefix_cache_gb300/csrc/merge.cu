@@ -7,8 +7,11 @@
 // context chunks and extend stage) in one pass, which equals the pages'
 // sequential fold up to rounding.
 //
-// One warp per (row, head) of 128 values: lane i owns 4 consecutive floats, so
-// every load/store is a 16-byte vector and a warp moves 512 contiguous bytes.
+// One warp per (row, head) of W values (W = 128 for attention outputs, 512 for
+// the latent states of the absorbed path): lane i owns float4 columns
+// i, i + 32, ..., so every load/store is a 16-byte vector and a warp moves 512
+// contiguous bytes per access.  The output may alias slot 0 of the states:
+// each lane writes only the columns it read, after a warp barrier.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -17,7 +20,9 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
+template <int W>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_slots_kernel(const __grid_constant__ MergeParams p) {
+  constexpr int kV = W / 128;   // float4 columns per lane
   const int lane = threadIdx.x & 31;
   const int64_t wid = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int H = p.num_heads;
@@ -38,7 +43,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_slots_kernel(const 
     float m = -INFINITY;
 #pragma unroll 4
     for (int s = 0; s < ns; ++s) m = fmaxf(m, __ldg(p.part_lse + ((int64_t)s * p.slot_stride_rows + row) * H + h));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc[kV];
+#pragma unroll
+    for (int v = 0; v < kV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
     if (m != -INFINITY) {
       // Predicated rather than branched, so the unrolled loads of several
@@ -49,20 +56,27 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_slots_kernel(const 
         const float l = __ldg(p.part_lse + g);
         const bool live = (l != -INFINITY);
         const float w = live ? __expf(l - m) : 0.f;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (live) o = __ldg(reinterpret_cast<const float4*>(p.part_out + g * kDv) + lane);
-        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+#pragma unroll
+        for (int v = 0; v < kV; ++v) {
+          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (live) o = reinterpret_cast<const float4*>(p.part_out + g * W)[lane + 32 * v];
+          acc[v].x += w * o.x; acc[v].y += w * o.y; acc[v].z += w * o.z; acc[v].w += w * o.w;
+        }
         wsum += w;
       }
     }
     const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
     const int64_t orow = row * H + h;
-    const float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (p.out_bf16) {
-      uint2 v = make_uint2(pack_bf16(r.x, r.y), pack_bf16(r.z, r.w));
-      reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * kDv)[lane] = v;
-    } else {
-      reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * kDv)[lane] = r;
+    __syncwarp();   // every lane has read the states (the output may alias slot 0)
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+      const float4 r = make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
+      if (p.out_bf16) {
+        uint2 b = make_uint2(pack_bf16(r.x, r.y), pack_bf16(r.z, r.w));
+        reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * W)[lane + 32 * v] = b;
+      } else {
+        reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * W)[lane + 32 * v] = r;
+      }
     }
     if (lane == 0) p.lse[orow] = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
   }
@@ -148,7 +162,15 @@ int grid_for(int64_t warps_needed, int warps_per_block) {
 cudaError_t launch_merge_slots(const MergeParams& p, cudaStream_t s) {
   const int64_t items = (int64_t)p.total_rows * p.num_heads;
   if (items == 0) return cudaSuccess;
-  merge_slots_kernel<<<grid_for(items, kWarpsPerBlock), kWarpsPerBlock * 32, 0, s>>>(p);
+  merge_slots_kernel<kDv><<<grid_for(items, kWarpsPerBlock), kWarpsPerBlock * 32, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_slots_latent(const MergeParams& p, cudaStream_t s) {
+  const int64_t items = (int64_t)p.total_rows * p.num_heads;
+  if (items == 0) return cudaSuccess;
+  merge_slots_kernel<kDc><<<grid_for(items, kWarpsPerBlock), kWarpsPerBlock * 32, 0, s>>>(p);
   count_launch();
   return cudaGetLastError();
 }

@@ -117,6 +117,18 @@ class Workload:
             f += (c + e) * up + e * c * att + e * (e + 1) / 2.0 * att
         return f
 
+    def visible_pairs(self) -> float:
+        """(query, key) pairs the attention covers, per head."""
+        f = 0.0
+        for c, e in zip(self.ctx_lens.tolist(), self.ext_lens.tolist()):
+            f += e * c + e * (e + 1) / 2.0
+        return f
+
+    def absorbed_attention_flops(self) -> float:
+        """Tensor-core work of the latent-space attention: per (query, key, head)
+        a 576-wide score and a 512-wide P c product."""
+        return 2.0 * (D_C + D_R + D_C) * self.num_heads * self.visible_pairs()
+
     def nbytes_inputs(self) -> int:
         return int(self.q.nbytes + self.kv_cache.nbytes + self.kv_b_proj.nbytes
                    + self.block_table.nbytes + self.q_pos.nbytes)
@@ -249,12 +261,19 @@ def reloc_256k() -> Workload:
     return make_workload("reloc_256k", 128, [262144], [4096], chunk=16384, seed=4, doc_len=16384)
 
 
+def short_ext_32k() -> Workload:
+    """A short extend for the absorbed (latent-space) path: 128 heads, 32K
+    cached tokens + 64 new ones, chunk 16K, BF16."""
+    return make_workload("short_ext_32k", 128, [32768], [64], chunk=16384, seed=5)
+
+
 CONFIGS = {
     "tiny": tiny,
     "v3_8k": v3_8k,
     "batched": batched,
     "fp8_128k": fp8_128k,
     "reloc_256k": reloc_256k,
+    "short_ext_32k": short_ext_32k,
 }
 
 

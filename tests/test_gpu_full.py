@@ -46,3 +46,27 @@ def test_full_size_sampled(name):
     # every row sees its whole context, so lse >= the log of a positive sum everywhere;
     # the mean output over all rows/heads stays near zero for zero-mean values
     assert float(out.abs().max()) < 1.0
+
+
+def test_absorbed_short_extend_full_size():
+    """The absorbed path on the short-extend workload the bench times (128
+    heads, 32K cached + 64 new tokens), sampled rows against the oracle, every
+    row against the up-projected path."""
+    from mla_prefix_cache_gb300 import api
+    wl = W.by_name("short_ext_32k")
+    dw = api.DeviceWorkload(wl)
+    out, lse = dw.run(absorbed=True)
+    torch.cuda.synchronize()
+    assert api.device_error(api.prefill.last_workspace) == 0
+    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all())
+    rng = np.random.default_rng(101)
+    rows = np.array([0, 1, 17, 40, 62, 63])
+    heads = [0, int(rng.integers(1, wl.num_heads - 1)), wl.num_heads - 1]
+    ref_out, ref_lse = O.mla_prefill(**O.workload_args(wl), rows=rows, heads=heads)
+    got_out = out[torch.from_numpy(rows).cuda()][:, heads].cpu().numpy()
+    got_lse = lse[torch.from_numpy(rows).cuda()][:, heads].cpu().numpy()
+    assert_close(got_out, got_lse, ref_out, ref_lse, visible_keys(wl)[rows])
+    o2, l2 = dw.run()
+    torch.cuda.synchronize()
+    assert float((out - o2).abs().max()) <= 2e-2
+    assert float((lse - l2).abs().max()) <= 1e-3
