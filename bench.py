@@ -232,7 +232,9 @@ def hbm_kernels(dev, flush, peak_gbs, reps=10):
     CUDA events (L2 flushed before every launch, median of `reps`), on inputs
     shaped like the long-context workloads: a 128K-token paged gather (BF16
     and FP8 rows), merge_attn_states of 4096 tokens x 128 heads of fp32
-    states, and RoPE relocation of a [4096, 128, 192] bf16 query in place.
+    states, RoPE relocation of a [4096, 128, 192] bf16 query in place, and
+    the block store's content hash of all 2304 bf16 blocks of the pool and
+    byte comparison of 1152 block pairs.
     Bytes are algorithmic (each byte the operation must read or write once)."""
     import torch
     from mla_prefix_cache_gb300 import api
@@ -253,6 +255,8 @@ def hbm_kernels(dev, flush, peak_gbs, reps=10):
     om, lm = torch.empty_like(oa), torch.empty_like(la)
     q = torch.randn((4096, 128, 192), generator=g, device=dev).to(torch.bfloat16)
     pos = torch.arange(4096, dtype=torch.int32, device=dev) + 262144
+    all_ids = torch.randperm(n_blocks, generator=g, device=dev).to(torch.int32)
+    pair_a, pair_b = all_ids[: n_blocks // 2].contiguous(), all_ids[n_blocks // 2:].contiguous()
 
     cases = {
         "gather_bf16": (lambda: api.gather_latent(bf16_cache, perm, 0, n_tok, dst=dst),
@@ -263,6 +267,9 @@ def hbm_kernels(dev, flush, peak_gbs, reps=10):
                          rows * (2 * (128 * 4 + 4) + (128 * 4 + 4))),
         "rope_relocate": (lambda: api.rope_relocate(q, pos, 65536, 10000.0, y=q),
                           4096 * 128 * 64 * 2 * 2 + 4096 * 4),
+        "block_hash": (lambda: api.block_hash(bf16_cache, all_ids), n_blocks * (64 * 1152 + 4 + 8)),
+        "block_compare": (lambda: api.block_compare(bf16_cache, pair_a, pair_b),
+                          (n_blocks // 2) * (2 * 64 * 1152 + 8 + 4)),
     }
     stream = torch.cuda.current_stream(dev)
     res = {}

@@ -262,6 +262,39 @@ int mla_gather_latent(const void* kv_cache, int kv_dtype, float kv_scale, int nu
                       const int32_t* block_table_row, int max_blocks, int start, int len,
                       void* dst, uint32_t* dev_error, mla_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Content-addressed block store, GPU steps ("PagedAttention assumed MHA.
+ * DeepSeek-V4 says that assumption is broken", sections "Position
+ * independence beats prefix matching" and "The finding: content-addressed
+ * dedup needs byte verification").  A sealed 64-token block is hashed and
+ * looked up; on a hash match its bytes are compared with the installed
+ * block's, and the candidate is shared only when they are equal (else it is
+ * installed fresh and a collision is counted).  The table, that decision and
+ * the counter are the caller's; these two calls are the parts that read
+ * whole blocks.
+ *
+ * mla_block_hash: hashes[i] = h(block block_ids[i]) for i < n, where the
+ * block's bytes as stored (64 rows of 1152 B bf16 or 640 B FP8) are read as
+ * little-endian 64-bit words w_0 .. w_{m-1} and
+ *   h = mix(m ^ sum_i mix(w_i + (i + 1) * 0x9e3779b97f4a7c15))  (mod 2^64),
+ *   mix(z): z ^= z >> 30; z *= 0xbf58476d1ce4e5b9; z ^= z >> 27;
+ *           z *= 0x94d049bb133111eb; z ^= z >> 31   (SplitMix64's output
+ *           function).  The page's store uses xxh3; any non-cryptographic
+ *           64-bit hash serves, since byte verification decides sharing.
+ * mla_block_compare: equal[i] = 1 when blocks block_a[i] and block_b[i] hold
+ * the same bytes, else 0.
+ *  kv_cache            device, [num_blocks, 64, row] as for mla_prefill_ctx.
+ *  block_ids, block_a, block_b   device int32 [n].
+ *  hashes              device uint64 [n];  equal  device int32 [n].
+ *  dev_error           device uint32, optional: bit 0 is set for an id
+ *                      outside [0, num_blocks) (its hash is 0, its equal -1).
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+int mla_block_hash(const void* kv_cache, int kv_dtype, int num_blocks, const int32_t* block_ids, int n,
+                   uint64_t* hashes, uint32_t* dev_error, mla_stream_t stream);
+int mla_block_compare(const void* kv_cache, int kv_dtype, int num_blocks, const int32_t* block_a,
+                      const int32_t* block_b, int n, int32_t* equal, uint32_t* dev_error, mla_stream_t stream);
+
 /* Optional instrumentation.  With both arguments non-NULL (cudaEvent_t handles
  * created by the caller), every later mla_prefill_ctx call on this process
  * records `begin` on its stream just before its first fused prefill kernel

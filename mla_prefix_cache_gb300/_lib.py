@@ -71,6 +71,8 @@ SIGNATURES = {
                                   c_void_p]),
     "mla_gather_latent": (c_int, [c_void_p, c_int, c_float, c_int, c_void_p, c_int, c_int, c_int, c_void_p,
                                   c_void_p, c_void_p]),
+    "mla_block_hash": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p]),
+    "mla_block_compare": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]),
     "mla_status_string": (ctypes.c_char_p, [c_int]),
     "mla_last_cuda_error": (ctypes.c_char_p, []),
     "mla_launch_count": (ctypes.c_uint64, []),

@@ -177,6 +177,35 @@ def gather_latent(kv_cache: torch.Tensor, block_table_row: torch.Tensor, start: 
     return dst
 
 
+def block_hash(kv_cache: torch.Tensor, block_ids: torch.Tensor, dev_error: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """Content hash of whole cache blocks (mla_block_hash): int64 [n] holding
+    the uint64 hash bits."""
+    n = int(block_ids.numel())
+    hashes = torch.empty(n, dtype=torch.int64, device=kv_cache.device)
+    errp = _dev(dev_error, "dev_error", (torch.int32, torch.uint32)) if dev_error is not None else None
+    st = _lib.load().mla_block_hash(_dev(kv_cache, "kv_cache"), kv_dtype_code(kv_cache), int(kv_cache.shape[0]),
+                                    _dev(block_ids, "block_ids", torch.int32), n, _dev(hashes, "hashes"), errp,
+                                    _stream_ptr(stream))
+    _lib.check("mla_block_hash", st)
+    return hashes
+
+
+def block_compare(kv_cache: torch.Tensor, block_a: torch.Tensor, block_b: torch.Tensor,
+                  dev_error: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Byte equality of block pairs (mla_block_compare): int32 [n], 1 equal, 0 not."""
+    n = int(block_a.numel())
+    if int(block_b.numel()) != n:
+        raise ValueError("block_a and block_b differ in length")
+    equal = torch.empty(n, dtype=torch.int32, device=kv_cache.device)
+    errp = _dev(dev_error, "dev_error", (torch.int32, torch.uint32)) if dev_error is not None else None
+    st = _lib.load().mla_block_compare(_dev(kv_cache, "kv_cache"), kv_dtype_code(kv_cache), int(kv_cache.shape[0]),
+                                       _dev(block_a, "block_a", torch.int32), _dev(block_b, "block_b", torch.int32),
+                                       n, _dev(equal, "equal"), errp, _stream_ptr(stream))
+    _lib.check("mla_block_compare", st)
+    return equal
+
+
 # ---------------------------------------------------------------- workloads
 
 class DeviceWorkload:

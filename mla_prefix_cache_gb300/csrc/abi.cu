@@ -951,4 +951,25 @@ int mla_gather_latent(const void* kv_cache, int kv_dtype, float kv_scale, int nu
                                    dev_error, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int mla_block_hash(const void* kv_cache, int kv_dtype, int num_blocks, const int32_t* block_ids, int n,
+                   uint64_t* hashes, uint32_t* dev_error, mla_stream_t stream) {
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (n < 0 || num_blocks <= 0) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  if (!kv_cache || !block_ids || !hashes || !aligned(kv_cache, 16) || !aligned(hashes, 8)) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_block_hash(static_cast<const uint8_t*>(kv_cache), kv_dtype == MLA_KV_FP8_E4M3, num_blocks,
+                                       block_ids, n, hashes, dev_error, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mla_block_compare(const void* kv_cache, int kv_dtype, int num_blocks, const int32_t* block_a,
+                      const int32_t* block_b, int n, int32_t* equal, uint32_t* dev_error, mla_stream_t stream) {
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (n < 0 || num_blocks <= 0) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  if (!kv_cache || !block_a || !block_b || !equal || !aligned(kv_cache, 16)) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_block_compare(static_cast<const uint8_t*>(kv_cache), kv_dtype == MLA_KV_FP8_E4M3,
+                                          num_blocks, block_a, block_b, n, equal, dev_error,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

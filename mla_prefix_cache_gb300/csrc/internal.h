@@ -249,6 +249,13 @@ cudaError_t launch_absorb_attn(const AbsorbParams& p, cudaStream_t s);
 cudaError_t launch_qabsorb(const QAbsorbParams& p, cudaStream_t s);
 cudaError_t launch_absorb_proj(const ProjParams& p, cudaStream_t s);
 
+// Content-addressed block store (blocks.cu): content hash of whole cache
+// blocks and byte comparison of block pairs.
+cudaError_t launch_block_hash(const uint8_t* cache, int fp8, int num_blocks, const int32_t* ids, int n,
+                              uint64_t* hashes, uint32_t* err, cudaStream_t s);
+cudaError_t launch_block_compare(const uint8_t* cache, int fp8, int num_blocks, const int32_t* a, const int32_t* b,
+                                 int n, int32_t* equal, uint32_t* err, cudaStream_t s);
+
 void count_launch(int n = 1);
 
 }  // namespace mla

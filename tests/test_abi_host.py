@@ -116,3 +116,25 @@ def test_other_entry_points_validate(lib):
     assert lib.mla_gather_latent(d, 0, 1.0, 4, d, 2, 100, 64, d, None, None) == _lib.MLA_ERR_INVALID_ARG
     assert lib.mla_gather_latent(d, 1, 0.0, 4, d, 2, 0, 64, d, None, None) == _lib.MLA_ERR_INVALID_ARG
     assert lib.mla_get_device_error(None, None) == _lib.MLA_ERR_INVALID_ARG
+    # block store: bad dtype, negative count, null or misaligned pointers; n = 0 launches nothing
+    assert lib.mla_block_hash(d, 2, 4, d, 3, d, None, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_block_hash(d, 0, 4, d, -1, d, None, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_block_hash(None, 0, 4, d, 3, d, None, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_block_hash(d, 0, 4, d, 3, ctypes.c_void_p(4100), None, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_block_hash(d, 0, 4, d, 0, d, None, None) == _lib.MLA_OK
+    assert lib.mla_block_compare(d, 0, 0, d, d, 3, d, None, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_block_compare(d, 0, 4, d, None, 3, d, None, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_block_compare(d, 1, 4, d, d, 0, d, None, None) == _lib.MLA_OK
+
+
+def test_absorbed_entry_validates_and_sizes(lib):
+    sl, cq = (ctypes.c_int32 * 1)(320), (ctypes.c_int32 * 2)(0, 64)
+    n = lib.mla_prefill_absorbed_workspace_size(1, sl, cq, 8, None, 0, 128, 3)
+    # header + gathered rows (5 blocks) + qlat + one slot of latent states and lse
+    rows = 64 * 8
+    want = 256 + 5 * 64 * 1152
+    want = (want + 255) // 256 * 256 + rows * 512 * 2
+    want = (want + 255) // 256 * 256 + rows * 512 * 4
+    want = (want + 255) // 256 * 256 + rows * 4
+    assert n == (want + 255) // 256 * 256
+    assert lib.mla_prefill_absorbed_workspace_size(1, sl, cq, 8, None, 0, 100, 3) == 0   # chunk not a multiple of 64

@@ -336,3 +336,72 @@ def test_absorbed_bad_block_and_workspace(api):
     assert torch.isfinite(out).all()
     with pytest.raises(_lib.MLAError):
         dw.run(absorbed=True, workspace=torch.empty(4096, dtype=torch.uint8, device="cuda"))
+
+
+# ---------------------------------------------------------------- content-addressed block store
+
+def _pool(kv):
+    return W.make_workload("bs", 2, [900, 333], [40, 7], chunk=128, kv_dtype=kv, seed=50)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_block_hash_bit_exact(api, kv):
+    from oracle import block_store as BS
+    wl = _pool(kv)
+    dw = api.DeviceWorkload(wl)
+    nb = wl.kv_cache.shape[0]
+    ids = np.concatenate([np.arange(nb), np.random.default_rng(51).integers(0, nb, size=37)]).astype(np.int32)
+    got = api.block_hash(dw.kv_cache, torch.from_numpy(ids).cuda()).cpu().numpy().view(np.uint64)
+    want = np.array([BS.block_hash(wl.kv_cache, int(b)) for b in ids], dtype=np.uint64)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_block_compare_and_bad_ids(api, kv):
+    wl = _pool(kv)
+    dw = api.DeviceWorkload(wl)
+    nb = wl.kv_cache.shape[0]
+    dw.kv_cache[5] = dw.kv_cache[2]          # planted equal content
+    dw.kv_cache[9] = dw.kv_cache[2]
+    dw.kv_cache[9].view(torch.uint8).view(-1)[-1] ^= 1   # same but the very last byte
+    a = torch.tensor([2, 5, 2, 0, 3, 2, -1, 1], dtype=torch.int32, device="cuda")
+    b = torch.tensor([5, 2, 9, 0, 4, 2, 1, nb], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    eq = api.block_compare(dw.kv_cache, a, b, dev_error=err).cpu().tolist()
+    assert eq == [1, 1, 0, 1, 0, 1, -1, -1]
+    assert int(err.item()) & 1
+    err.zero_()
+    h = api.block_hash(dw.kv_cache, torch.tensor([2, 5, 9, nb + 3], dtype=torch.int32, device="cuda"), dev_error=err)
+    h = h.cpu().tolist()
+    assert h[0] == h[1] != h[2] and h[3] == 0 and int(err.item()) & 1
+
+
+def test_seal_protocol_on_gpu_matches_oracle(api):
+    """The page's seal protocol driven by the two GPU calls (hash, then byte
+    comparison on a hash match) gives the oracle's holders and collision
+    count; 3-bit hashes make distinct blocks collide."""
+    from oracle import block_store as BS
+    wl = _pool("bf16")
+    dw = api.DeviceWorkload(wl)
+    for dst, src in ((7, 1), (12, 1), (20, 4)):
+        dw.kv_cache[dst] = dw.kv_cache[src]
+    cache_np = dw.kv_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+    nb = cache_np.shape[0]
+    ids = torch.arange(nb, dtype=torch.int32, device="cuda")
+    keys = (api.block_hash(dw.kv_cache, ids).cpu().numpy().view(np.uint64) & np.uint64(7)).tolist()
+    table, holders, coll = {}, [], 0
+    for c in range(nb):
+        same = table.get(keys[c], [])
+        if same:
+            eq = api.block_compare(dw.kv_cache, torch.tensor(same, dtype=torch.int32, device="cuda"),
+                                   torch.full((len(same),), c, dtype=torch.int32, device="cuda")).cpu().tolist()
+            hit = [b for b, e in zip(same, eq) if e == 1]
+            if hit:
+                holders.append(hit[0])
+                continue
+            coll += 1
+        table.setdefault(keys[c], []).append(c)
+        holders.append(c)
+    want_holders, want_coll = BS.seal_all(cache_np, range(nb), hash_bits=3)
+    assert holders == want_holders and coll == want_coll and coll > 0
+    assert holders[7] == 1 and holders[12] == 1 and holders[20] == 4
