@@ -217,6 +217,43 @@ int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos,
                              void* out, int out_dtype, float* lse,
                              void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * mla_prefill_reuse -- head-split reuse with protected-row replacement
+ * ("RedKnot-MLA: Multi-Head Offline-Online Reuse for DeepSeek-V4 Long-Context
+ * Serving", section 2: Local and Global heads over one packed latent stream;
+ * the Global heads and the protected Local rows are recomputed online, the
+ * other Local states come from the offline artifact, replaced rather than
+ * double counted).  For query row t and head h:
+ *   (out, lse)[t, h] = the state mla_prefill_ctx computes with the same
+ *                      arguments, if h is a Global head or row t is protected;
+ *                      (art_out, art_lse)[t, h] otherwise.
+ * Only the recomputed (row, head) pairs are computed: the Global heads for
+ * every row, and the Local heads for the protected rows.
+ *  global_heads   HOST int32 [n_global], head indices in [0, H) (repeats ignored).
+ *  row_protected  HOST uint8 [T_q], nonzero for a protected row; NULL: none.
+ *  art_out        device fp32 [T_q, H, 128];  art_lse  device fp32 [T_q, H].
+ *  other arguments, out and lse as mla_prefill_ctx.
+ *  workspace      device, 256-B aligned, at least
+ *                 mla_prefill_reuse_workspace_size(...) bytes (a smaller one
+ *                 returns MLA_ERR_WORKSPACE); holds the device error word.
+ * Errors: as mla_prefill_ctx; MLA_ERR_INVALID_ARG for a head outside [0, H).
+ * ---------------------------------------------------------------------- */
+size_t mla_prefill_reuse_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q,
+                                        int num_heads, const mla_segment* segments, int num_segments,
+                                        int chunk, int parts, const int32_t* global_heads, int n_global,
+                                        const uint8_t* row_protected);
+
+int mla_prefill_reuse(const void* q, const int32_t* q_pos,
+                      const void* kv_cache, int kv_dtype, float kv_scale, int num_blocks,
+                      const int32_t* block_table, int max_blocks_per_req,
+                      const int32_t* seq_lens, const int32_t* cu_q, int num_reqs, int num_heads,
+                      const mla_segment* segments, int num_segments, int chunk,
+                      const void* kv_b_proj, float softmax_scale, float rope_theta, int parts,
+                      const int32_t* global_heads, int n_global, const uint8_t* row_protected,
+                      const float* art_out, const float* art_lse,
+                      void* out, int out_dtype, float* lse,
+                      void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
 /* Reads and clears the device error word kept in `workspace` (synchronises
  * `stream`).  Returns MLA_OK, MLA_ERR_BAD_BLOCK_ID or MLA_ERR_TIMEOUT. */
 int mla_get_device_error(void* workspace, mla_stream_t stream);

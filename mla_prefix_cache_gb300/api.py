@@ -129,6 +129,74 @@ def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_
     return out, lse
 
 
+def _protected_host(protected_rows, T_q: int):
+    if protected_rows is None:
+        return None, None
+    m = np.zeros(T_q, dtype=np.uint8)
+    pr = np.asarray(protected_rows)
+    if pr.dtype == bool and pr.shape == (T_q,):
+        m[:] = pr
+    else:
+        m[pr.astype(np.int64)] = 1
+    return ctypes.c_void_p(m.ctypes.data), m
+
+
+def reuse_workspace_size(seq_lens, cu_q, num_heads: int, global_heads, protected_rows=None, segments=None,
+                         chunk: int = 4096, parts: int = PART_ALL) -> int:
+    sl, keep_sl = _lib.i32_host(seq_lens)
+    cq, keep_cq = _lib.i32_host(cu_q)
+    sp, ns, _k3 = _lib.segments_host(segments)
+    gh, keep_gh = _lib.i32_host(list(global_heads))
+    pp, _k4 = _protected_host(protected_rows, int(keep_cq[-1]))
+    n = _lib.load().mla_prefill_reuse_workspace_size(len(keep_sl), sl, cq, int(num_heads), sp, ns, int(chunk),
+                                                     int(parts), gh, int(keep_gh.shape[0]), pp)
+    if n == 0:
+        raise MLAError("mla_prefill_reuse_workspace_size", _lib.MLA_ERR_INVALID_ARG)
+    return int(n)
+
+
+def prefill_reuse(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                  seq_lens, cu_q, kv_b_proj: torch.Tensor, art_out: torch.Tensor, art_lse: torch.Tensor, *,
+                  global_heads, protected_rows=None, chunk: int, softmax_scale: float, rope_theta: float = 10000.0,
+                  kv_scale: float = 1.0, segments=None, parts: int = PART_ALL,
+                  out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
+                  lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Head-split reuse (mla_prefill_reuse): the Global heads and the
+    protected rows (host indices or a bool mask over T_q) are recomputed,
+    every other (row, head) takes the artifact (art_out fp32 [T_q, H, 128],
+    art_lse fp32 [T_q, H])."""
+    T_q, H = int(q.shape[0]), int(q.shape[1])
+    sl, keep_sl = _lib.i32_host(seq_lens)
+    cq, keep_cq = _lib.i32_host(cu_q)
+    sp, ns, keep_sp = _lib.segments_host(segments)
+    gh, keep_gh = _lib.i32_host(list(global_heads))
+    pp, keep_pp = _protected_host(protected_rows, T_q)
+    dev = q.device
+    if out is None:
+        out = torch.empty((T_q, H, 128), dtype=out_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        ws_bytes = reuse_workspace_size(keep_sl, keep_cq, H, keep_gh, keep_pp.astype(bool) if keep_pp is not None
+                                        else None, segments, chunk, parts)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_FP32
+    st = _lib.load().mla_prefill_reuse(
+        _dev(q, "q", torch.bfloat16), _dev(q_pos, "q_pos", torch.int32), _dev(kv_cache, "kv_cache"),
+        kv_dtype_code(kv_cache), float(kv_scale), int(kv_cache.shape[0]),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        sl, cq, int(keep_sl.shape[0]), H, sp, ns, int(chunk), _dev(kv_b_proj, "kv_b_proj", torch.bfloat16),
+        float(softmax_scale), float(rope_theta), int(parts), gh, int(keep_gh.shape[0]), pp,
+        _dev(art_out, "art_out", torch.float32), _dev(art_lse, "art_lse", torch.float32),
+        _dev(out, "out", (torch.float32, torch.bfloat16)), od, _dev(lse, "lse", torch.float32),
+        _dev(workspace, "workspace"), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+        _stream_ptr(stream))
+    _lib.check("mla_prefill_reuse", st)
+    prefill_reuse.last_workspace = workspace
+    return out, lse
+
+
 def device_error(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
     """Reads and clears the device error word of a prefill workspace."""
     return int(_lib.load().mla_get_device_error(_dev(workspace, "workspace"), _stream_ptr(stream)))

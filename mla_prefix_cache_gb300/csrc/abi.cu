@@ -55,8 +55,13 @@ struct Plan {
 
 // Step "plan" of the path: per request, context chunks of every segment and
 // the extend stage become KV splits, each with its own partial-state slot.
+// ctx_lens (optional): each request's context length C_r, its extend keys
+// then being [C_r, seq_lens[r]) and its cu_q rows a sorted subset of those
+// queries (their token indices given to the kernel); default C_r =
+// seq_lens[r] - E_r with every query present.
 static int build_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,
-                      const mla_segment* segs, int nseg, int chunk, int parts, Plan* plan) {
+                      const mla_segment* segs, int nseg, int chunk, int parts, Plan* plan,
+                      const int32_t* ctx_lens = nullptr) {
   if (num_reqs < 0 || num_heads < 1 || nseg < 0) return MLA_ERR_INVALID_ARG;
   if (num_heads > kMaxHeads) return MLA_ERR_UNSUPPORTED;
   if (chunk <= 0) return MLA_ERR_INVALID_ARG;
@@ -68,13 +73,14 @@ static int build_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q
   for (int r = 0; r < num_reqs; ++r) {
     const int64_t e = (int64_t)cu_q[r + 1] - cu_q[r];
     if (e < 0 || seq_lens[r] < e) return MLA_ERR_INVALID_ARG;
+    if (ctx_lens != nullptr && (ctx_lens[r] < 0 || seq_lens[r] - ctx_lens[r] < e)) return MLA_ERR_INVALID_ARG;
   }
   // segments: inside their request's context, non-overlapping per request
   std::vector<std::vector<const mla_segment*>> per_req(num_reqs);
   for (int i = 0; i < nseg; ++i) {
     const mla_segment& s = segs[i];
     if (s.req < 0 || s.req >= num_reqs || s.reserved != 0 || s.start < 0 || s.len < 0) return MLA_ERR_INVALID_ARG;
-    const int64_t ctx = (int64_t)seq_lens[s.req] - (cu_q[s.req + 1] - cu_q[s.req]);
+    const int64_t ctx = ctx_lens ? (int64_t)ctx_lens[s.req] : (int64_t)seq_lens[s.req] - (cu_q[s.req + 1] - cu_q[s.req]);
     if ((int64_t)s.start + s.len > ctx) return MLA_ERR_INVALID_ARG;
     per_req[s.req].push_back(&s);
   }
@@ -91,7 +97,7 @@ static int build_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q
   plan->total_q = num_reqs > 0 ? cu_q[num_reqs] : 0;
   for (int r = 0; r < num_reqs; ++r) {
     const int E = cu_q[r + 1] - cu_q[r];
-    const int C = seq_lens[r] - E;
+    const int C = ctx_lens ? ctx_lens[r] : seq_lens[r] - E;
     if (E == 0) continue;
     int slots = 0;
     auto add = [&](int k0, int k1, int64_t off) {
@@ -115,7 +121,7 @@ static int build_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q
             add(c0, std::min(c0 + chunk, s->start + s->len), s->rope_offset);
       }
     }
-    if (parts & MLA_PART_EXTEND) add(C, C + E, 0);
+    if (parts & MLA_PART_EXTEND) add(C, seq_lens[r], 0);
     RowRange rr{};
     rr.row_begin = cu_q[r];
     rr.row_end = cu_q[r + 1];
@@ -151,7 +157,7 @@ struct FusedPlan {
 // merge_attn_states would; pieces of one request are folded by the merge
 // kernel.
 static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const int32_t* cu_q, int num_reqs,
-                            int chunk, bool gather_rows, FusedPlan* fp) {
+                            int chunk, bool gather_rows, FusedPlan* fp, const int32_t* ctx_lens = nullptr) {
   fp->pieces.clear();
   fp->merge.clear();
   fp->gather.clear();
@@ -166,7 +172,7 @@ static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const i
   for (int r = 0; r < num_reqs; ++r) {
     const int E = cu_q[r + 1] - cu_q[r];
     if (E == 0) continue;
-    const int C = seq_lens[r] - E;
+    const int C = ctx_lens ? ctx_lens[r] : seq_lens[r] - E;
     std::vector<Piece> pr;
     std::vector<Split> rs;
     while (si < splits.splits.size() && splits.splits[si].req == r) rs.push_back(splits.splits[si++]);
@@ -375,7 +381,8 @@ static int gather_rows(const FusedPlan& fp, const void* kv_cache, bool fp8, int 
 static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
                          int num_blocks, const int32_t* block_table, int max_blocks, int num_heads,
                          const void* kv_b_proj, float softmax_scale, float rope_theta, void* out, int out_dtype,
-                         float* lse, void* workspace, const FusedPlan& fp, const FusedWs& fw, cudaStream_t s) {
+                         float* lse, void* workspace, const FusedPlan& fp, const FusedWs& fw, cudaStream_t s,
+                         const int32_t* q_tok = nullptr, bool keep_err = false) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int H = num_heads;
   const int64_t T_q = fp.total_q;
@@ -395,6 +402,7 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   const uint64_t rows_total = (uint64_t)std::max(fp.gather_blocks, 1) * kBlock;
   bool ok = true;
   p.q_bf16 = static_cast<const uint16_t*>(q);
+  p.q_tok = q_tok;
   {
     const uint64_t d[2] = {(uint64_t)kRowBf16, rows_total};
     const uint64_t st[1] = {(uint64_t)kRowBytesBf16};
@@ -472,7 +480,8 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   p.pair = pair;
   p.ring_depth = fw.ring_depth;
   const int width = pair ? 2 : 1;
-  st = cuda_status(cudaMemsetAsync(err, 0, 256, s));   // error word + role queue
+  // error word + role queue (keep_err: a caller running several sub-calls keeps the error word)
+  st = keep_err ? cuda_status(cudaMemsetAsync(err + 1, 0, 256 - 4, s)) : cuda_status(cudaMemsetAsync(err, 0, 256, s));
   if (st != MLA_OK) return st;
   if ((st = gather_rows(fp, kv_cache, fp8, num_blocks, block_table, max_blocks, ws + fw.gath_off, err, s)) != MLA_OK)
     return st;
@@ -776,6 +785,174 @@ static int prefill_plans(const void* q, const int32_t* q_pos, const void* kv_cac
   return MLA_OK;
 }
 
+// ------------------------------------------------------------------ head-split reuse
+struct ReusePlan {
+  std::vector<int32_t> global, local, prot_rows, prot_tok, gidx, lidx, pidx, cu_p, ctx;
+  Plan plan_g, plan_p;
+  FusedPlan fp_g, fp_p;
+  FusedWs fw_g, fw_p;
+  size_t off_maps = 0, off_qg = 0, off_wg = 0, off_og = 0, off_lg = 0, off_qp = 0, off_posp = 0, off_tokp = 0,
+         off_wp = 0, off_op = 0, off_lp = 0, off_fused = 0, total = 0;
+  size_t map_words = 0;
+};
+
+// The two compacted sub-problems and the workspace that holds them, in order:
+// one fused workspace shared by the two sub-calls (they run one after the
+// other; its header, with the device error word, is the call's header); index
+// maps (gidx[H], lidx[H], pidx[T_q], protected rows and their token indices,
+// the Global and the Local head lists); Global part (q, kv_b_proj columns,
+// out, lse); protected part (q, q_pos, kv_b_proj columns, out, lse).
+static int build_reuse_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int H,
+                            const mla_segment* segs, int nseg, int chunk, int parts, const int32_t* global_heads,
+                            int n_global, const uint8_t* row_protected, ReusePlan* rp) {
+  if (n_global < 0 || (n_global > 0 && global_heads == nullptr)) return MLA_ERR_INVALID_ARG;
+  Plan base;
+  int st = build_plan(num_reqs, seq_lens, cu_q, H, segs, nseg, chunk, parts, &base);
+  if (st != MLA_OK) return st;
+  const int64_t T_q = base.total_q;
+  rp->gidx.assign(H, -1);
+  rp->lidx.assign(H, -1);
+  rp->global.clear();
+  rp->local.clear();
+  for (int i = 0; i < n_global; ++i) {
+    const int h = global_heads[i];
+    if (h < 0 || h >= H) return MLA_ERR_INVALID_ARG;
+    if (rp->gidx[h] < 0) {
+      rp->gidx[h] = (int32_t)rp->global.size();
+      rp->global.push_back(h);
+    }
+  }
+  for (int h = 0; h < H; ++h)
+    if (rp->gidx[h] < 0) {
+      rp->lidx[h] = (int32_t)rp->local.size();
+      rp->local.push_back(h);
+    }
+  rp->pidx.assign((size_t)T_q, -1);
+  rp->prot_rows.clear();
+  rp->prot_tok.clear();
+  rp->cu_p.assign(num_reqs + 1, 0);
+  rp->ctx.assign(num_reqs, 0);
+  for (int r = 0; r < num_reqs; ++r) {
+    const int E = cu_q[r + 1] - cu_q[r];
+    rp->ctx[r] = seq_lens[r] - E;
+    for (int i = 0; i < E && row_protected != nullptr; ++i)
+      if (row_protected[cu_q[r] + i]) {
+        rp->pidx[cu_q[r] + i] = (int32_t)rp->prot_rows.size();
+        rp->prot_rows.push_back(cu_q[r] + i);
+        rp->prot_tok.push_back(rp->ctx[r] + i);
+      }
+    rp->cu_p[r + 1] = (int32_t)rp->prot_rows.size();
+  }
+  const int nG = (int)rp->global.size(), nL = (int)rp->local.size(), nP = (int)rp->prot_rows.size();
+  size_t fused_bytes = 0;
+  if (nG > 0) {
+    if ((st = build_plan(num_reqs, seq_lens, cu_q, nG, segs, nseg, chunk, parts, &rp->plan_g)) != MLA_OK) return st;
+    build_fused_plan(rp->plan_g, seq_lens, cu_q, num_reqs, chunk, true, &rp->fp_g);
+    rp->fw_g = fused_ws_layout(rp->fp_g, nG);
+    fused_bytes = std::max(fused_bytes, rp->fw_g.total);
+  }
+  if (nP > 0 && nL > 0) {
+    if ((st = build_plan(num_reqs, seq_lens, rp->cu_p.data(), nL, segs, nseg, chunk, parts, &rp->plan_p,
+                         rp->ctx.data())) != MLA_OK)
+      return st;
+    build_fused_plan(rp->plan_p, seq_lens, rp->cu_p.data(), num_reqs, chunk, true, &rp->fp_p, rp->ctx.data());
+    rp->fw_p = fused_ws_layout(rp->fp_p, nL);
+    fused_bytes = std::max(fused_bytes, rp->fw_p.total);
+  }
+  rp->map_words = 2 * (size_t)H + (size_t)T_q + 2 * (size_t)nP + (size_t)nG + (size_t)nL;
+  rp->off_fused = 0;
+  rp->off_maps = up256(std::max(fused_bytes, (size_t)256));
+  rp->off_qg = up256(rp->off_maps + rp->map_words * 4);
+  rp->off_wg = up256(rp->off_qg + (size_t)T_q * nG * kDqk * 2);
+  rp->off_og = up256(rp->off_wg + (size_t)kDc * nG * 256 * 2);
+  rp->off_lg = up256(rp->off_og + (size_t)T_q * nG * kDv * 4);
+  rp->off_qp = up256(rp->off_lg + (size_t)T_q * nG * 4);
+  rp->off_posp = up256(rp->off_qp + (size_t)nP * nL * kDqk * 2);
+  rp->off_tokp = up256(rp->off_posp + (size_t)nP * 4);
+  rp->off_wp = up256(rp->off_tokp + (size_t)nP * 4);
+  rp->off_op = up256(rp->off_wp + (size_t)kDc * nL * 256 * 2);
+  rp->off_lp = up256(rp->off_op + (size_t)nP * nL * kDv * 4);
+  rp->total = up256(rp->off_lp + (size_t)nP * nL * 4);
+  return MLA_OK;
+}
+
+static int prefill_reuse(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                         int num_blocks, const int32_t* block_table, int max_blocks, int H, const void* kv_b_proj,
+                         float softmax_scale, float rope_theta, const float* art_out, const float* art_lse,
+                         void* out, int out_dtype, float* lse, uint8_t* ws, const ReusePlan& rp, int64_t T_q,
+                         cudaStream_t s) {
+  int st = cuda_status(cudaMemsetAsync(ws, 0, 256, s));
+  if (st != MLA_OK) return st;
+  // index maps: host vectors -> workspace (pageable copies complete their host reads before returning)
+  std::vector<int32_t> maps;
+  maps.reserve(rp.map_words);
+  maps.insert(maps.end(), rp.gidx.begin(), rp.gidx.end());
+  maps.insert(maps.end(), rp.lidx.begin(), rp.lidx.end());
+  maps.insert(maps.end(), rp.pidx.begin(), rp.pidx.end());
+  maps.insert(maps.end(), rp.prot_rows.begin(), rp.prot_rows.end());
+  maps.insert(maps.end(), rp.prot_tok.begin(), rp.prot_tok.end());
+  maps.insert(maps.end(), rp.global.begin(), rp.global.end());
+  maps.insert(maps.end(), rp.local.begin(), rp.local.end());
+  int32_t* dmaps = reinterpret_cast<int32_t*>(ws + rp.off_maps);
+  if (!maps.empty() && (st = cuda_status(cudaMemcpyAsync(dmaps, maps.data(), maps.size() * 4,
+                                                         cudaMemcpyHostToDevice, s))) != MLA_OK)
+    return st;
+  const int32_t* d_gidx = dmaps;
+  const int32_t* d_lidx = dmaps + H;
+  const int32_t* d_pidx = dmaps + 2 * H;
+  const int32_t* d_prows = dmaps + 2 * H + T_q;
+  const int32_t* d_ptok = d_prows + rp.prot_rows.size();
+  const int nG = (int)rp.global.size(), nL = (int)rp.local.size(), nP = (int)rp.prot_rows.size();
+  const int32_t* d_global = d_ptok + nP;
+  const int32_t* d_local = d_global + nG;
+  const uint16_t* qb = static_cast<const uint16_t*>(q);
+  const uint16_t* wb = static_cast<const uint16_t*>(kv_b_proj);
+  uint8_t* fused_ws = ws + rp.off_fused;
+  if (nG > 0) {
+    uint16_t* qg = reinterpret_cast<uint16_t*>(ws + rp.off_qg);
+    uint16_t* wg = reinterpret_cast<uint16_t*>(ws + rp.off_wg);
+    if ((st = cuda_status(launch_gather_q(qb, q_pos, nullptr, d_global, (int)T_q, nG, H, qg, nullptr, s))) != MLA_OK)
+      return st;
+    if ((st = cuda_status(launch_gather_w(wb, d_global, nG, H, wg, s))) != MLA_OK) return st;
+    if ((st = prefill_fused(qg, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks, nG, wg,
+                            softmax_scale, rope_theta, ws + rp.off_og, MLA_OUT_FP32,
+                            reinterpret_cast<float*>(ws + rp.off_lg), fused_ws, rp.fp_g, rp.fw_g, s, nullptr,
+                            true)) != MLA_OK)
+      return st;
+  }
+  if (nP > 0 && nL > 0) {
+    uint16_t* qp = reinterpret_cast<uint16_t*>(ws + rp.off_qp);
+    int32_t* posp = reinterpret_cast<int32_t*>(ws + rp.off_posp);
+    uint16_t* wp = reinterpret_cast<uint16_t*>(ws + rp.off_wp);
+    if ((st = cuda_status(launch_gather_q(qb, q_pos, d_prows, d_local, nP, nL, H, qp, posp, s))) != MLA_OK)
+      return st;
+    if ((st = cuda_status(launch_gather_w(wb, d_local, nL, H, wp, s))) != MLA_OK) return st;
+    if ((st = prefill_fused(qp, posp, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks, nL, wp,
+                            softmax_scale, rope_theta, ws + rp.off_op, MLA_OUT_FP32,
+                            reinterpret_cast<float*>(ws + rp.off_lp), fused_ws, rp.fp_p, rp.fw_p, s, d_ptok,
+                            true)) != MLA_OK)
+      return st;
+  }
+  ReuseAssemble ra;
+  ra.out_g = reinterpret_cast<const float*>(ws + rp.off_og);
+  ra.lse_g = reinterpret_cast<const float*>(ws + rp.off_lg);
+  ra.out_p = reinterpret_cast<const float*>(ws + rp.off_op);
+  ra.lse_p = reinterpret_cast<const float*>(ws + rp.off_lp);
+  ra.art_out = art_out;
+  ra.art_lse = art_lse;
+  ra.gidx = d_gidx;
+  ra.lidx = d_lidx;
+  ra.pidx = d_pidx;
+  ra.out = out;
+  ra.lse = lse;
+  ra.out_bf16 = out_dtype == MLA_OUT_BF16;
+  ra.rows = (int)T_q;
+  ra.H = H;
+  ra.n_global = nG;
+  ra.n_local = nL;
+  return cuda_status(launch_reuse_assemble(ra, s));
+}
+
 extern "C" {
 
 int mla_abi_version(void) { return 1; }
@@ -898,6 +1075,42 @@ int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos, const void* kv
   return prefill_absorbed(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
                           num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, workspace, fplan, ap,
                           aw, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t mla_prefill_reuse_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,
+                                        const mla_segment* segments, int num_segments, int chunk, int parts,
+                                        const int32_t* global_heads, int n_global, const uint8_t* row_protected) {
+  ReusePlan rp;
+  if (build_reuse_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, global_heads,
+                       n_global, row_protected, &rp) != MLA_OK)
+    return 0;
+  return rp.total;
+}
+
+int mla_prefill_reuse(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                      int num_blocks, const int32_t* block_table, int max_blocks_per_req, const int32_t* seq_lens,
+                      const int32_t* cu_q, int num_reqs, int num_heads, const mla_segment* segments,
+                      int num_segments, int chunk, const void* kv_b_proj, float softmax_scale, float rope_theta,
+                      int parts, const int32_t* global_heads, int n_global, const uint8_t* row_protected,
+                      const float* art_out, const float* art_lse, void* out, int out_dtype, float* lse,
+                      void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  Plan plan;
+  FusedPlan fplan;
+  int st = prefill_plans(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                         seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
+                         softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
+  if (st != MLA_OK || plan.total_q == 0) return st;
+  if (!art_out || !art_lse || !aligned(art_out, 16) || !aligned(art_lse, 4)) return MLA_ERR_INVALID_ARG;
+  static ReusePlan rp;             // large; built on the host under a lock
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if ((st = build_reuse_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, global_heads,
+                             n_global, row_protected, &rp)) != MLA_OK)
+    return st;
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < rp.total) return MLA_ERR_WORKSPACE;
+  return prefill_reuse(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                       num_heads, kv_b_proj, softmax_scale, rope_theta, art_out, art_lse, out, out_dtype, lse,
+                       static_cast<uint8_t*>(workspace), rp, plan.total_q, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mla_get_device_error(void* workspace, mla_stream_t stream) {

@@ -256,7 +256,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
     const int r = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     float* xchg = reinterpret_cast<float*>(sgen + kXchgBase);   // [2 slots][2 halves][128] maxima, then sums
-    const int qtok = J.q_tok0 + q0 + r;
+    const int qtok = query_token(J, q0 + r);
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l_part = 0.f;
     bool ok = true;
@@ -590,6 +590,7 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
     J.q_begin = P.q_begin;
     J.q_count = P.q_count;
     J.q_tok0 = P.q_tok0;
+    J.q_tok = p.q_tok;
     J.k_begin = P.k_begin;
     J.k_end = P.k_end;
     J.t0 = P.k_begin & ~(kBlock - 1);

@@ -74,10 +74,16 @@ __device__ __forceinline__ int consumer_tiles(const Job& J, int ci) {
   const int q0 = ci * 128;
   const int nq = min(128, J.q_count - q0);
   if (nq <= 0) return 0;
-  const int last_tok = J.q_tok0 + q0 + nq - 1;
+  const int last_tok = J.q_tok ? J.q_tok[J.q_begin + q0 + nq - 1] : J.q_tok0 + q0 + nq - 1;
   const int k_end = min(J.k_end, last_tok + 1);
   if (k_end <= J.k_begin) return 0;
   return (k_end - J.t0 + 127) >> 7;
+}
+
+// Token index of query row q (within the job's rows; rows past the job's
+// last are padding and take its last row's token).
+__device__ __forceinline__ int query_token(const Job& J, int q) {
+  return J.q_tok ? J.q_tok[J.q_begin + min(q, J.q_count - 1)] : J.q_tok0 + q;
 }
 
 // Ring slot of tile t (the depth is a power of two).

@@ -86,6 +86,7 @@ struct Piece {
 struct Job {
   int32_t req, head, q_begin, q_count, q_tok0, k_begin, k_end, t0, n_tiles, n_cons, n_prod, slot, row_block0;
   int64_t rope_offset;
+  const int32_t* q_tok;   // FusedParams::q_tok
 };
 
 struct FusedParams {
@@ -97,6 +98,8 @@ struct FusedParams {
   CUtensorMap tm_ring1;  // same ring, box 64 x 128 x 1 (one block: half of a paired consumer's stage)
   CUtensorMap tm_ring64; // same ring, box 64 x 64 x 2 (64 keys of K_nope lo | hi: a CTA pair's half tile)
   const uint16_t* q_bf16;  // q [T_q][H][192]
+  const int32_t* q_tok;    // optional [T_q]: token index of each query row within its request (rows that are
+                           // a sorted subset of the request's queries); nullptr: q_tok0 + row - q_begin
   uint32_t* err;
   uint32_t* queue;       // role-group counter
   uint32_t* flags;       // per job: ready[ring], consumed[ring]
@@ -255,6 +258,28 @@ cudaError_t launch_block_hash(const uint8_t* cache, int fp8, int num_blocks, con
                               uint64_t* hashes, uint32_t* err, cudaStream_t s);
 cudaError_t launch_block_compare(const uint8_t* cache, int fp8, int num_blocks, const int32_t* a, const int32_t* b,
                                  int n, int32_t* equal, uint32_t* err, cudaStream_t s);
+
+// Head-split reuse (reuse.cu).
+struct ReuseAssemble {
+  const float* out_g;    // [rows][n_global][128]: Global heads, every row
+  const float* lse_g;
+  const float* out_p;    // [n_protected][n_local][128]: Local heads, protected rows
+  const float* lse_p;
+  const float* art_out;  // [rows][H][128]: the offline artifact
+  const float* art_lse;
+  const int32_t* gidx;   // [H]: index among the Global heads, or -1
+  const int32_t* lidx;   // [H]: index among the Local heads, or -1
+  const int32_t* pidx;   // [rows]: index among the protected rows, or -1
+  void* out;             // [rows][H][128] fp32 or bf16
+  float* lse;
+  int out_bf16;
+  int rows, H, n_global, n_local;
+};
+cudaError_t launch_gather_q(const uint16_t* q, const int32_t* q_pos, const int32_t* rows, const int32_t* heads,
+                            int n_rows, int n_heads, int H, uint16_t* q_sub, int32_t* pos_sub, cudaStream_t s);
+cudaError_t launch_gather_w(const uint16_t* w, const int32_t* heads, int n_heads, int H, uint16_t* w_sub,
+                            cudaStream_t s);
+cudaError_t launch_reuse_assemble(const ReuseAssemble& p, cudaStream_t s);
 
 void count_launch(int n = 1);
 

@@ -405,3 +405,52 @@ def test_seal_protocol_on_gpu_matches_oracle(api):
     want_holders, want_coll = BS.seal_all(cache_np, range(nb), hash_bits=3)
     assert holders == want_holders and coll == want_coll and coll > 0
     assert holders[7] == 1 and holders[12] == 1 and holders[20] == 4
+
+
+# ---------------------------------------------------------------- head-split reuse (Global heads, protected rows)
+
+REUSE_CASES = [
+    dict(H=6, ctx=[300, 77], ext=[140, 9], chunk=128, glob=[1, 4], prot=[0, 5, 77, 139, 140, 148]),
+    dict(H=4, ctx=[256], ext=[200], chunk=64, doc=64, glob=[3], prot=list(range(0, 200, 7))),
+    dict(H=3, ctx=[513], ext=[77], chunk=192, kv="fp8_e4m3", glob=[], prot=[1, 2, 76]),
+    dict(H=128, ctx=[300], ext=[130], chunk=128, glob=list(range(0, 128, 8)), prot=[0, 64, 127, 128, 129]),
+    dict(H=5, ctx=[200], ext=[50], chunk=128, glob=[0, 1, 2, 3, 4], prot=[]),          # every head Global
+    dict(H=5, ctx=[200], ext=[50], chunk=128, glob=[], prot=[]),                       # all from the artifact
+]
+
+
+@pytest.mark.parametrize("case", REUSE_CASES, ids=["batch", "docs", "fp8", "h128", "all_global", "all_artifact"])
+def test_prefill_reuse_matches_oracle(api, case):
+    from oracle import head_reuse as R
+    wl = W.make_workload("ru", case["H"], case["ctx"], case["ext"], chunk=case["chunk"],
+                         kv_dtype=case.get("kv", "bf16"), doc_len=case.get("doc"), seed=70)
+    dw = api.DeviceWorkload(wl)
+    rng = np.random.default_rng(71)
+    art_out = rng.standard_normal((wl.total_q, wl.num_heads, 128)).astype(np.float32)
+    art_lse = rng.standard_normal((wl.total_q, wl.num_heads)).astype(np.float32)
+    out, lse = api.prefill_reuse(dw.q, dw.q_pos, dw.kv_cache, dw.block_table, wl.seq_lens, wl.cu_q, dw.kv_b_proj,
+                                 torch.from_numpy(art_out).cuda(), torch.from_numpy(art_lse).cuda(),
+                                 global_heads=case["glob"], protected_rows=case["prot"], chunk=wl.chunk,
+                                 softmax_scale=wl.softmax_scale, kv_scale=wl.kv_scale, segments=wl.segments)
+    torch.cuda.synchronize()
+    assert api.device_error(api.prefill_reuse.last_workspace) == 0
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    ref_out, ref_lse = R.prefill_reuse(O.workload_args(wl), case["glob"], case["prot"], art_out, art_lse)
+    m = R.reuse_mask(wl.total_q, wl.num_heads, case["glob"], case["prot"])
+    # reused entries are copied bit for bit; recomputed ones meet the attention tolerances
+    assert np.array_equal(out[~m], art_out[~m]) and np.array_equal(lse[~m], art_lse[~m])
+    if m.any():
+        nvis = np.broadcast_to(visible_keys(wl)[:, None], m.shape)[m]
+        assert_close(out[m][:, None], lse[m][:, None], ref_out[m][:, None], ref_lse[m][:, None], nvis)
+
+
+def test_prefill_reuse_reports_bad_blocks(api):
+    wl = W.make_workload("rb", 2, [256], [16], chunk=128, seed=72)
+    dw = api.DeviceWorkload(wl)
+    dw.block_table[0, 1] = -5
+    z = torch.zeros((wl.total_q, 2, 128), dtype=torch.float32, device="cuda")
+    zl = torch.zeros((wl.total_q, 2), dtype=torch.float32, device="cuda")
+    api.prefill_reuse(dw.q, dw.q_pos, dw.kv_cache, dw.block_table, wl.seq_lens, wl.cu_q, dw.kv_b_proj, z, zl,
+                      global_heads=[1], protected_rows=[3], chunk=128, softmax_scale=wl.softmax_scale)
+    torch.cuda.synchronize()
+    assert api.device_error(api.prefill_reuse.last_workspace) == 3
