@@ -341,6 +341,62 @@ def absorbed_compare(dev, flush, peak, source, reps=10):
                                  "query-key-head, / its event time"}}
 
 
+def reuse_compare(dev, flush, reps=5, config="v3_8k", n_global=16, protected_frac=0.10):
+    """Head-split reuse against full recomputation on the same inputs: the
+    Global heads (every 8th head: 16 of 128, the RedKnot page's 8 of 64) and
+    a seeded 10% of the query rows recomputed, the rest taken from an
+    artifact.  Median CUDA-event time of a whole call, L2 flushed before each."""
+    import torch
+    from mla_prefix_cache_gb300 import api, workload
+
+    wl = workload.by_name(config)
+    dw = api.DeviceWorkload(wl, dev)
+    T_q, H = wl.total_q, wl.num_heads
+    glob = list(range(0, H, max(1, H // n_global)))[:n_global]
+    rng = np.random.default_rng(9)
+    prot = np.sort(rng.choice(T_q, size=max(1, int(round(protected_frac * T_q))), replace=False))
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    art_out = torch.randn((T_q, H, 128), generator=g, device=dev)
+    art_lse = torch.randn((T_q, H), generator=g, device=dev)
+    out = torch.empty((T_q, H, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
+    ws_f = torch.empty(api.prefill_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk), dtype=torch.uint8,
+                       device=dev)
+    ws_r = torch.empty(api.reuse_workspace_size(wl.seq_lens, wl.cu_q, H, glob, prot, wl.segments, wl.chunk),
+                       dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def full():
+        dw.run(out=out, lse=lse, workspace=ws_f)
+
+    def reuse():
+        api.prefill_reuse(dw.q, dw.q_pos, dw.kv_cache, dw.block_table, wl.seq_lens, wl.cu_q, dw.kv_b_proj,
+                          art_out, art_lse, global_heads=glob, protected_rows=prot, chunk=wl.chunk,
+                          softmax_scale=wl.softmax_scale, rope_theta=wl.rope_theta, kv_scale=wl.kv_scale,
+                          segments=wl.segments, out=out, lse=lse, workspace=ws_r)
+
+    res = {}
+    for name, fn in (("full", full), ("reuse", reuse)):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = float(statistics.median([a.elapsed_time(b) for a, b in ev]))
+    if api.device_error(ws_r) != 0:
+        raise RuntimeError("device error word set in the reuse comparison")
+    recomputed = (len(glob) * T_q + (H - len(glob)) * len(prot)) / (H * T_q)
+    return {"workload": config, "global_heads": len(glob), "protected_rows": int(len(prot)),
+            "recomputed_fraction": recomputed, "ms_full": res["full"], "ms_reuse": res["reuse"],
+            "speedup": res["full"] / res["reuse"]}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -466,6 +522,9 @@ def run_ours(args):
     cmp_abs = None
     if not args.no_absorbed and world == 1 and not absorbed:
         cmp_abs = absorbed_compare(dev, flush, peak, source)
+    cmp_reuse = None
+    if not args.no_reuse and world == 1:
+        cmp_reuse = reuse_compare(dev, flush)
     k_ms = sum(kern_ms) / K
     if absorbed:
         kflops = wl.absorbed_attention_flops()
@@ -494,6 +553,7 @@ def run_ours(args):
         "hbm_kernels": hbm,
         "hbm_peak_source": f"hbm_gbs of {source} peaks",
         "absorbed": cmp_abs,
+        "reuse": cmp_reuse,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clk,
@@ -515,6 +575,8 @@ def main(argv=None):
                     help="entry point timed: mla_prefill_ctx (up-projected, fused) or mla_prefill_ctx_absorbed")
     ap.add_argument("--no-absorbed", action="store_true",
                     help="skip the absorbed-vs-fused comparison on the short-extend workload")
+    ap.add_argument("--no-reuse", action="store_true",
+                    help="skip the head-split reuse comparison (16 Global heads, 10% protected rows on v3_8k)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hbm-kernels", action="store_true")
