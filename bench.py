@@ -474,34 +474,63 @@ def run_ours(args):
     value = flops * K * world / (total_ms / 1e3) / 1e12
     tok_s = T_q * K * world / (total_ms / 1e3)
 
-    # ---- end to end through the public API: pinned host inputs in, result out
+    # ---- end to end through the public API: pinned host inputs in, result out.
+    # A serving loop: step k's inputs go up (one copy stream) while step k-1
+    # computes and step k-2's result comes down (another copy stream); two
+    # device buffer sets alternate, and events order each buffer's reuse.
     e2e = None
     if not args.no_e2e:
-        host = {}
-        for name in ("q", "q_pos", "kv_cache", "block_table", "kv_b_proj"):
-            d = getattr(dw, name)
-            host[name] = torch.empty(d.shape, dtype=d.dtype, pin_memory=True).copy_(d)
-        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        import copy
+        names = ("q", "q_pos", "kv_cache", "block_table", "kv_b_proj")
+        host = {n: torch.empty(getattr(dw, n).shape, dtype=getattr(dw, n).dtype, pin_memory=True).copy_(getattr(dw, n))
+                for n in names}
+        sets = [dw, copy.copy(dw)]
+        for n in names:
+            setattr(sets[1], n, torch.empty_like(getattr(dw, n)))
+        outs = [out, torch.empty_like(out)]
+        lses = [lse, torch.empty_like(lse)]
+        out_h = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+        lse_h = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
         bi = sum(v.numel() * v.element_size() for v in host.values())
-        bo = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        bo = out_h[0].numel() * out_h[0].element_size() + lse_h[0].numel() * lse_h[0].element_size()
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()
+        done_compute = [ev(), ev()]
+        done_down = [ev(), ev()]
+        for e_ in done_compute + done_down:
+            e_.record(stream)
 
-        def e2e_step():
-            for name, h in host.items():
-                getattr(dw, name).copy_(h, non_blocking=True)
-            dw.run(out=out, lse=lse, workspace=ws, absorbed=absorbed)
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+        def e2e_step(k):
+            b = k & 1
+            up.wait_event(done_compute[b])            # step k-2 no longer reads these inputs
+            with torch.cuda.stream(up):
+                for n in names:
+                    getattr(sets[b], n).copy_(host[n], non_blocking=True)
+            uploaded = ev()
+            uploaded.record(up)
+            stream.wait_event(uploaded)
+            stream.wait_event(done_down[b])           # step k-2's result has left this buffer
+            sets[b].run(out=outs[b], lse=lses[b], workspace=ws, absorbed=absorbed)
+            done_compute[b].record(stream)
+            down.wait_event(done_compute[b])
+            with torch.cuda.stream(down):
+                out_h[b].copy_(outs[b], non_blocking=True)
+                lse_h[b].copy_(lses[b], non_blocking=True)
+            done_down[b].record(down)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        for k in range(max(1, args.warmup)):
+            e2e_step(k)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
-        e0.record(stream)
-        for _ in range(K):
-            e2e_step()
+        e0.record(up)
+        stream.wait_event(e0)
+        down.wait_event(e0)
+        for k in range(K):
+            e2e_step(k)
+        stream.wait_event(done_down[(K - 1) & 1])
+        stream.wait_event(done_down[K & 1])
         e1.record(stream)
         torch.cuda.synchronize(dev)
         ems = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
@@ -509,7 +538,9 @@ def run_ours(args):
             dist.all_reduce(ems, op=dist.ReduceOp.MAX)
         e2e = {"value": flops * K * world / (float(ems.item()) / 1e3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
-               "ms_per_step": float(ems.item()) / K}
+               "ms_per_step": float(ems.item()) / K,
+               "note": "pinned host inputs copied up and results copied down every step, on two copy streams "
+                       "overlapping the neighbouring steps' compute (two device buffer sets)"}
 
     if rank != 0:
         if world > 1:
