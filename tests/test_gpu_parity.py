@@ -454,3 +454,65 @@ def test_prefill_reuse_reports_bad_blocks(api):
                       global_heads=[1], protected_rows=[3], chunk=128, softmax_scale=wl.softmax_scale)
     torch.cuda.synchronize()
     assert api.device_error(api.prefill_reuse.last_workspace) == 3
+
+
+# ---------------------------------------------------------------- edge cases of the extra entry points
+
+@pytest.mark.parametrize("case", [
+    dict(H=1, ctx=[300], ext=[45], chunk=128),                 # one head
+    dict(H=4, ctx=[0], ext=[1], chunk=64),                     # a single query with no context: itself only
+    dict(H=3, ctx=[100, 64, 0], ext=[0, 5, 0], chunk=64),      # requests without queries in the batch
+])
+@pytest.mark.parametrize("absorbed", [False, True], ids=["fused", "absorbed"])
+def test_prefill_degenerate_shapes(api, case, absorbed):
+    wl = W.make_workload("dg", case["H"], case["ctx"], case["ext"], chunk=case["chunk"], seed=80)
+    run_and_compare(api, wl, absorbed=absorbed)
+
+
+def test_absorbed_many_splits(api, monkeypatch):
+    """64-key splits of a 2K context: 33 partial states per row, merged in latent space."""
+    monkeypatch.setenv("MLA_ABS_SPLIT_KEYS", "64")
+    wl = W.make_workload("as", 4, [2048], [6], chunk=512, seed=81)
+    run_and_compare(api, wl, absorbed=True)
+
+
+@pytest.mark.parametrize("mode", ["all_protected", "one_head", "bf16_out"])
+def test_prefill_reuse_edges(api, mode):
+    from oracle import head_reuse as R
+    H = 1 if mode == "one_head" else 3
+    wl = W.make_workload("re", H, [190, 64], [30, 0], chunk=64, seed=82)
+    dw = api.DeviceWorkload(wl)
+    rng = np.random.default_rng(83)
+    art_out = rng.standard_normal((wl.total_q, H, 128)).astype(np.float32)
+    art_lse = rng.standard_normal((wl.total_q, H)).astype(np.float32)
+    glob = [] if mode != "bf16_out" else [2]
+    prot = list(range(wl.total_q)) if mode == "all_protected" else [0, 29]
+    out, lse = api.prefill_reuse(dw.q, dw.q_pos, dw.kv_cache, dw.block_table, wl.seq_lens, wl.cu_q, dw.kv_b_proj,
+                                 torch.from_numpy(art_out).cuda(), torch.from_numpy(art_lse).cuda(),
+                                 global_heads=glob, protected_rows=prot, chunk=wl.chunk,
+                                 softmax_scale=wl.softmax_scale,
+                                 out_dtype=torch.bfloat16 if mode == "bf16_out" else torch.float32)
+    torch.cuda.synchronize()
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    ref_out, ref_lse = R.prefill_reuse(O.workload_args(wl), glob, prot, art_out, art_lse)
+    m = R.reuse_mask(wl.total_q, H, glob, prot)
+    if mode == "bf16_out":
+        bf = torch.from_numpy(art_out[~m]).bfloat16().float().numpy()
+        assert np.array_equal(out[~m], bf) and np.array_equal(lse[~m], art_lse[~m])
+    else:
+        assert np.array_equal(out[~m], art_out[~m]) and np.array_equal(lse[~m], art_lse[~m])
+    nvis = np.broadcast_to(visible_keys(wl)[:, None], m.shape)[m]
+    assert_close(out[m][:, None], lse[m][:, None], ref_out[m][:, None], ref_lse[m][:, None], nvis)
+    if mode == "all_protected":   # every row recomputed: plain attention
+        po, pl = O.mla_prefill(**O.workload_args(wl))
+        assert_close(out, lse, po, pl, visible_keys(wl))
+
+
+def test_block_store_empty_calls(api):
+    wl = _pool("fp8_e4m3")
+    dw = api.DeviceWorkload(wl)
+    e = torch.zeros(0, dtype=torch.int32, device="cuda")
+    n0 = api.launch_count()
+    assert api.block_hash(dw.kv_cache, e).numel() == 0
+    assert api.block_compare(dw.kv_cache, e, e).numel() == 0
+    assert api.launch_count() == n0
