@@ -218,6 +218,32 @@ int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos,
                              void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * mla_prefill_ctx_absorbed_fp8 -- mla_prefill_ctx_absorbed for an FP8 cache
+ * with the latent part of every score on the FP8 tensor cores: the cache's
+ * E4M3 codes are read as stored, and qlat is rounded to E4M3 with one scale
+ * per (token, head) row (amax / 448); the k_rope part of the score, the
+ * softmax and P c stay as in mla_prefill_ctx_absorbed.  The E4M3 rounding of
+ * qlat (relative error up to 2^-4) makes the result an approximation of
+ * mla_prefill_ctx's: about 2.5% noise on each score's latent part, which
+ * averages over the keys (lse moves by about 0.03 / sqrt(visible keys)).
+ *  kv_dtype       must be MLA_KV_FP8_E4M3 (MLA_KV_BF16: MLA_ERR_UNSUPPORTED).
+ *  workspace      at least mla_prefill_absorbed_fp8_workspace_size(...) bytes.
+ *  other arguments as mla_prefill_ctx.
+ * ---------------------------------------------------------------------- */
+size_t mla_prefill_absorbed_fp8_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q,
+                                               int num_heads, const mla_segment* segments, int num_segments,
+                                               int chunk, int parts);
+
+int mla_prefill_ctx_absorbed_fp8(const void* q, const int32_t* q_pos,
+                                 const void* kv_cache, int kv_dtype, float kv_scale, int num_blocks,
+                                 const int32_t* block_table, int max_blocks_per_req,
+                                 const int32_t* seq_lens, const int32_t* cu_q, int num_reqs, int num_heads,
+                                 const mla_segment* segments, int num_segments, int chunk,
+                                 const void* kv_b_proj, float softmax_scale, float rope_theta, int parts,
+                                 void* out, int out_dtype, float* lse,
+                                 void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * mla_prefill_reuse -- head-split reuse with protected-row replacement
  * ("RedKnot-MLA: Multi-Head Offline-Online Reuse for DeepSeek-V4 Long-Context
  * Serving", section 2: Local and Global heads over one packed latent stream;

@@ -71,12 +71,13 @@ def prefill_workspace_size(seq_lens, cu_q, num_heads: int, segments=None, chunk:
 
 
 def absorbed_workspace_size(seq_lens, cu_q, num_heads: int, segments=None, chunk: int = 4096,
-                            parts: int = PART_ALL) -> int:
+                            parts: int = PART_ALL, fp8_scores: bool = False) -> int:
     sl, _k1 = _lib.i32_host(seq_lens)
     cq, _k2 = _lib.i32_host(cu_q)
     sp, ns, _k3 = _lib.segments_host(segments)
-    n = _lib.load().mla_prefill_absorbed_workspace_size(len(_k1), sl, cq, int(num_heads), sp, ns, int(chunk),
-                                                        int(parts))
+    L = _lib.load()
+    fn = L.mla_prefill_absorbed_fp8_workspace_size if fp8_scores else L.mla_prefill_absorbed_workspace_size
+    n = fn(len(_k1), sl, cq, int(num_heads), sp, ns, int(chunk), int(parts))
     if n == 0:
         raise MLAError("mla_prefill_absorbed_workspace_size", _lib.MLA_ERR_INVALID_ARG)
     return int(n)
@@ -87,9 +88,11 @@ def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_
             rope_theta: float = 10000.0, kv_scale: float = 1.0, segments=None, parts: int = PART_ALL,
             out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
             lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-            stream: Optional[torch.cuda.Stream] = None, absorbed: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
-    """MLA chunked prefill of one layer (mla_prefill_ctx, or with absorbed=True
-    mla_prefill_ctx_absorbed: the same result computed in latent space).
+            stream: Optional[torch.cuda.Stream] = None, absorbed=False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """MLA chunked prefill of one layer (mla_prefill_ctx; absorbed=True:
+    mla_prefill_ctx_absorbed, the same result computed in latent space;
+    absorbed="fp8": mla_prefill_ctx_absorbed_fp8, FP8 caches, latent scores
+    on the FP8 tensor cores).
 
     q bf16 [T_q, H, 192] (q_rope unrotated); q_pos int32 [T_q]; kv_cache bf16
     [NB,64,576] or uint8 [NB,64,640] (FP8); block_table int32 [B, max_blocks];
@@ -109,12 +112,16 @@ def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_
         out = torch.empty((T_q, H, 128), dtype=out_dtype, device=dev)
     if lse is None:
         lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
+    fp8 = absorbed == "fp8"
     if workspace is None:
-        size_fn = absorbed_workspace_size if absorbed else prefill_workspace_size
-        ws_bytes = size_fn(keep_sl, keep_cq, H, segments, chunk, parts)
+        if absorbed:
+            ws_bytes = absorbed_workspace_size(keep_sl, keep_cq, H, segments, chunk, parts, fp8_scores=fp8)
+        else:
+            ws_bytes = prefill_workspace_size(keep_sl, keep_cq, H, segments, chunk, parts)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_FP32
-    fn = L.mla_prefill_ctx_absorbed if absorbed else L.mla_prefill_ctx
+    name = "mla_prefill_ctx_absorbed_fp8" if fp8 else ("mla_prefill_ctx_absorbed" if absorbed else "mla_prefill_ctx")
+    fn = getattr(L, name)
     st = fn(
         _dev(q, "q", torch.bfloat16), _dev(q_pos, "q_pos", torch.int32), _dev(kv_cache, "kv_cache"),
         kv_dtype_code(kv_cache), float(kv_scale), int(kv_cache.shape[0]),
@@ -124,7 +131,7 @@ def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_
         _dev(out, "out", (torch.float32, torch.bfloat16)), od, _dev(lse, "lse", torch.float32),
         _dev(workspace, "workspace"), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
         _stream_ptr(stream))
-    _lib.check("mla_prefill_ctx_absorbed" if absorbed else "mla_prefill_ctx", st)
+    _lib.check(name, st)
     prefill.last_workspace = workspace
     return out, lse
 

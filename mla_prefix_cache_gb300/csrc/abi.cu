@@ -378,6 +378,37 @@ static int gather_rows(const FusedPlan& fp, const void* kv_cache, bool fp8, int 
   return MLA_OK;
 }
 
+// The FP8 rows of the plan's requests as stored (640 B), in the same order.
+static int gather_rows_raw(const FusedPlan& fp, const void* kv_cache, int num_blocks, const int32_t* block_table,
+                           int max_blocks, uint8_t* dst, uint32_t* err, cudaStream_t s) {
+  static GatherBlocksParams gp;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  std::memset(&gp, 0, sizeof(gp));
+  gp.cache = static_cast<const uint8_t*>(kv_cache);
+  gp.block_table = block_table;
+  gp.err = err;
+  gp.fp8 = 1;
+  gp.num_blocks = num_blocks;
+  gp.max_blocks = max_blocks;
+  for (size_t g0 = 0; g0 < fp.gather.size(); g0 += kMaxGatherReqs) {
+    const size_t n = std::min(fp.gather.size() - g0, (size_t)kMaxGatherReqs);
+    int base = fp.gather[g0].base_block, end = base;
+    for (size_t i = 0; i < n; ++i) {
+      GatherReq g = fp.gather[g0 + i];
+      end = g.base_block + (g.seq_len + kBlock - 1) / kBlock;
+      g.base_block -= base;
+      gp.reqs[i] = g;
+    }
+    gp.dst = reinterpret_cast<uint16_t*>(dst + (size_t)base * kBlock * kRowBytesFp8);
+    gp.n_reqs = (int)n;
+    gp.total_blocks = end - base;
+    const int st = cuda_status(launch_gather_blocks_raw(gp, s));
+    if (st != MLA_OK) return st;
+  }
+  return MLA_OK;
+}
+
 static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
                          int num_blocks, const int32_t* block_table, int max_blocks, int num_heads,
                          const void* kv_b_proj, float softmax_scale, float rope_theta, void* out, int out_dtype,
@@ -605,13 +636,14 @@ static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int 
 }
 
 struct AbsWs {
-  size_t gath_off = 0, qlat_off = 0, lat_out_off = 0, lat_lse_off = 0, total = 0;
+  size_t gath_off = 0, qlat_off = 0, lat_out_off = 0, lat_lse_off = 0, raw_off = 0, qlat8_off = 0, qscale_off = 0,
+         total = 0;
 };
 
 // Workspace of the absorbed path: header (error word), gathered rows, the
 // absorbed queries and the latent states of every slot (a request's slots are
 // merged into slot 0 before the output projection).
-static AbsWs abs_ws_layout(const FusedPlan& fp, const AbsPlan& ap, int H) {
+static AbsWs abs_ws_layout(const FusedPlan& fp, const AbsPlan& ap, int H, bool fp8_scores = false) {
   AbsWs w;
   const size_t rows = (size_t)fp.total_q * (size_t)H;
   const size_t slots = (size_t)std::max(ap.max_slots, 1);
@@ -620,6 +652,12 @@ static AbsWs abs_ws_layout(const FusedPlan& fp, const AbsPlan& ap, int H) {
   w.lat_out_off = up256(w.qlat_off + rows * kDc * sizeof(uint16_t));
   w.lat_lse_off = up256(w.lat_out_off + slots * rows * kDc * sizeof(float));
   w.total = up256(w.lat_lse_off + slots * rows * sizeof(float));
+  if (fp8_scores) {   // E4M3 scores: the FP8 rows as stored, E4M3 qlat and its row scales
+    w.raw_off = w.total;
+    w.qlat8_off = up256(w.raw_off + (size_t)fp.gather_blocks * kBlock * kRowBytesFp8);
+    w.qscale_off = up256(w.qlat8_off + rows * kDc);
+    w.total = up256(w.qscale_off + rows * sizeof(float));
+  }
   return w;
 }
 
@@ -627,7 +665,7 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
                             int num_blocks, const int32_t* block_table, int max_blocks, int H, const void* kv_b_proj,
                             float softmax_scale, float rope_theta, void* out, int out_dtype, float* lse,
                             void* workspace, const FusedPlan& fp, const AbsPlan& ap, const AbsWs& aw,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool fp8_scores = false) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int64_t T_q = fp.total_q;
   static AbsorbParams p;           // large; built on the host under a lock
@@ -659,11 +697,34 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
     ok &= encode_map(&p.tm_qlat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + aw.qlat_off, d3, st3, b3,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  if (fp8_scores) {
+    const void* raw = static_cast<const void*>(ws + aw.raw_off);
+    // latent codes of a 640-byte row as 4 blocks of 128 bytes: (byte, row, block); one box is a stage
+    const uint64_t d[3] = {128, rows_total, 4};
+    const uint64_t st[2] = {(uint64_t)kRowBytesFp8, 128};
+    const uint32_t b[3] = {128, 64, 4};
+    ok &= encode_map(&p.tm_f8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, raw, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint64_t d2[2] = {(uint64_t)kRowBytesFp8 / 2, rows_total};   // the rows as bf16 [rows][320]
+    const uint64_t st2[1] = {(uint64_t)kRowBytesFp8};
+    const uint32_t b2[2] = {64, 64};
+    ok &= encode_map(&p.tm_kr8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, raw, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint64_t d3[2] = {(uint64_t)kDc, (uint64_t)T_q * H};
+    const uint64_t st3[1] = {(uint64_t)kDc};
+    const uint32_t b3[2] = {128, 128};
+    ok &= encode_map(&p.tm_qlat8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ws + aw.qlat8_off, d3, st3, b3,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    p.qscale = reinterpret_cast<const float*>(ws + aw.qscale_off);
+    p.kv_scale = kv_scale;
+    p.fp8_scores = 1;
+  }
   if (!ok) return MLA_ERR_CUDA;
 
   int st = cuda_status(cudaMemsetAsync(err, 0, 256, s));
   if (st != MLA_OK) return st;
   if ((st = gather_rows(fp, kv_cache, fp8, num_blocks, block_table, max_blocks, ws + aw.gath_off, err, s)) != MLA_OK)
+    return st;
+  if (fp8_scores && (st = gather_rows_raw(fp, kv_cache, num_blocks, block_table, max_blocks, ws + aw.raw_off, err, s)) !=
+                        MLA_OK)
     return st;
   {
     QAbsorbParams qp;
@@ -673,7 +734,14 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
     qp.scale = vscale;
     qp.tokens = (int)T_q;
     qp.num_heads = H;
-    if ((st = cuda_status(launch_qabsorb(qp, s))) != MLA_OK) return st;
+    if (fp8_scores) {
+      qp.scale = 1.f;   // kv_scale enters through the per-row score factor
+      if ((st = cuda_status(launch_qabsorb_e4m3(qp, ws + aw.qlat8_off, reinterpret_cast<float*>(ws + aw.qscale_off),
+                                                s))) != MLA_OK)
+        return st;
+    } else if ((st = cuda_status(launch_qabsorb(qp, s))) != MLA_OK) {
+      return st;
+    }
   }
 
   p.q = static_cast<const uint16_t*>(q);
@@ -1111,6 +1179,41 @@ int mla_prefill_reuse(const void* q, const int32_t* q_pos, const void* kv_cache,
   return prefill_reuse(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
                        num_heads, kv_b_proj, softmax_scale, rope_theta, art_out, art_lse, out, out_dtype, lse,
                        static_cast<uint8_t*>(workspace), rp, plan.total_q, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t mla_prefill_absorbed_fp8_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q,
+                                               int num_heads, const mla_segment* segments, int num_segments,
+                                               int chunk, int parts) {
+  Plan plan;
+  if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
+    return 0;
+  FusedPlan fp;
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fp);
+  AbsPlan ap;
+  build_abs_plan(fp, num_heads, cu_q, num_reqs, &ap);
+  return abs_ws_layout(fp, ap, num_heads, true).total;
+}
+
+int mla_prefill_ctx_absorbed_fp8(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype,
+                                 float kv_scale, int num_blocks, const int32_t* block_table, int max_blocks_per_req,
+                                 const int32_t* seq_lens, const int32_t* cu_q, int num_reqs, int num_heads,
+                                 const mla_segment* segments, int num_segments, int chunk, const void* kv_b_proj,
+                                 float softmax_scale, float rope_theta, int parts, void* out, int out_dtype,
+                                 float* lse, void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  if (kv_dtype != MLA_KV_FP8_E4M3) return kv_dtype == MLA_KV_BF16 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  Plan plan;
+  FusedPlan fplan;
+  const int st = prefill_plans(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                               seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
+                               softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
+  if (st != MLA_OK || plan.total_q == 0) return st;
+  AbsPlan ap;
+  build_abs_plan(fplan, num_heads, cu_q, num_reqs, &ap);
+  const AbsWs aw = abs_ws_layout(fplan, ap, num_heads, true);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < aw.total) return MLA_ERR_WORKSPACE;
+  return prefill_absorbed(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                          num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, workspace, fplan, ap,
+                          aw, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 int mla_get_device_error(void* workspace, mla_stream_t stream) {

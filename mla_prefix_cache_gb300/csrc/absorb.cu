@@ -38,12 +38,11 @@ namespace {
 
 constexpr int kAThreads = 256;
 constexpr int kAKeys = 64;
-constexpr int kAStages = 3;
+constexpr int kAStages = 3;                                    // O side
 constexpr uint32_t kAAtom = 8192;                              // [64 rows x 128 B] swizzled block
-constexpr uint32_t kACStage = 8 * kAAtom;                      // latent part of 64 rows
+constexpr uint32_t kACStage = 8 * kAAtom;                      // O side: bf16 latent part of 64 rows
 constexpr uint32_t kACBase = 0;                                // both CTAs
-constexpr uint32_t kAKrBase = kACBase + kAStages * kACStage;   // S side: k_rope of each stage
-constexpr uint32_t kAPBase = kAKrBase;                         // O side: two P tiles [128 x 64] bf16
+constexpr uint32_t kAPBase = kAStages * kACStage;              // O side: two P tiles [128 x 64] bf16
 constexpr uint32_t kAPBytes = 16384;
 constexpr uint32_t kAAlphaBase = kAPBase + 2 * kAPBytes;       // O side: per P tile, 128 row factors
 constexpr uint32_t kALBase = kAAlphaBase + 2 * 512;            // O side: 128 final row sums
@@ -51,32 +50,46 @@ constexpr uint32_t kAFlagBase = kALBase + 512;                 // O side: per P 
                                                                // the tile handed to the correction warps
 constexpr uint32_t kABarBase = kAFlagBase + 2 * 16 + 16;
 enum : uint32_t {
-  kBFull = 0,      // 3, both: stage landed (S side: latent + k_rope; O side: latent)
-  kBEmpty = 3,     // 3, both: the CTA's MMA that reads the stage is done
-  kBSFull = 6,     // 2, S side: S buffer written
-  kBSFree = 8,     // 2, S side: the 4 softmax warps read the S buffer
-  kBPFree = 10,    // 2, S side: PV of the P tile done (commit from the O side)
-  kBQReady = 12,   // S side: the 4 softmax warps copied Q into TMEM (stages 1-2 free again)
-  kBPFull = 13,    // 2, O side: P tile, row factors and flags landed
-  kBCNeed = 15,    // O side: the MMA thread handed a tile (or the end) to the correction warps
-  kBCDone = 16,    // O side: the 4 correction warps rescaled the tile's rows
-  kBPvDone = 17,   // 2, O side: PV of the tile done
-  kBLFull = 19,    // O side: the final row sums landed
-  kBQFull = 20,    // S side: the tile's absorbed queries landed in stages 1-2
-  kANumBars = 21
+  kBFull = 0,      // 5, both: stage landed (S side: latent + k_rope; O side: latent)
+  kBEmpty = 5,     // 5, both: the CTA's MMA that reads the stage is done
+  kBSFull = 10,    // 2, S side: S buffer written
+  kBSFree = 12,    // 2, S side: the 4 softmax warps read the S buffer
+  kBPFree = 14,    // 2, S side: PV of the P tile done (commit from the O side)
+  kBQReady = 16,   // S side: the 4 softmax warps copied Q into TMEM (stages 1-2 free again)
+  kBPFull = 17,    // 2, O side: P tile, row factors and flags landed
+  kBCNeed = 19,    // O side: the MMA thread handed a tile (or the end) to the correction warps
+  kBCDone = 20,    // O side: the 4 correction warps rescaled the tile's rows
+  kBPvDone = 21,   // 2, O side: PV of the tile done
+  kBLFull = 23,    // O side: the final row sums landed
+  kBQFull = 24,    // S side: the tile's absorbed queries landed in stages 1-2
+  kANumBars = 25
 };
 constexpr uint32_t kATmemSlot = kABarBase + 8 * kANumBars;
 constexpr uint32_t kASmemBytes = kATmemSlot + 16 + 1024;       // + alignment of the base to 1024
 static_assert(kASmemBytes <= 232448, "more than 227 KB of shared memory per CTA");
-static_assert(kAKrBase + kAStages * kAAtom <= kABarBase, "k_rope stages overlap the barriers");
 
-constexpr uint32_t kATmS = 320;   // S side: S buffer b at 320 + 64 b (Q as bf16 pairs in columns 0..287)
+// S side, by score precision: a stage is [latent | k_rope] of 64 keys
+// (bf16: 8 + 1 swizzled [64 x 128 B] blocks; E4M3 latent: 4 + 1), and the
+// tile's absorbed queries are staged over stages 1-2 at the start.
+template <bool kF8>
+struct SSide {
+  static constexpr int kCAtoms = kF8 ? 4 : 8;
+  static constexpr int kStages = kF8 ? 5 : 3;
+  static constexpr uint32_t kStage = (kCAtoms + 1) * kAAtom;
+  static constexpr uint32_t kKr = kCAtoms * kAAtom;           // k_rope block within a stage
+  static constexpr uint32_t kTx = kStage;
+  static constexpr int kQBoxes = kF8 ? 4 : 8;                 // [128 rows x 128 B] boxes of qlat
+  static constexpr uint32_t kQStage = kStage;                 // stage 1 on
+  static constexpr uint32_t kTmRope = kF8 ? 128 : 256;        // TMEM column of the rotated q_rope
+  static_assert(kStages * kStage <= kABarBase, "S-side stages overlap the barriers");
+  static_assert(kQStage + kQBoxes * 16384 <= 3 * kStage, "staged queries spill past stage 2");
+};
+
+constexpr uint32_t kATmS = 320;   // S side: S buffer b at 320 + 64 b (Q in columns 0..287)
 constexpr uint32_t kIdescSA = idesc_bf16(128, 64, false, false);
+constexpr uint32_t kIdescS8 = idesc_e4m3(128, 64);
 constexpr uint32_t kIdescPVA = idesc_bf16(128, 256, false, true);
-constexpr uint32_t kTxS = kACStage + kAAtom;
 constexpr uint32_t kTxO = kACStage;
-constexpr uint32_t kTxQ = 8 * 16384;          // qlat of 128 rows, 8 boxes [128 rows x 64]
-constexpr uint32_t kAQStage = kACBase + kACStage;   // S side: qlat staged over stages 1-2 at the start
 constexpr uint32_t kTxP = 128 * (128 + 4) + 16;   // per row: 64 bf16 of P and one fp32 factor; 4 flags
 constexpr float kARescale = 8.f;             // log2 units: P stays <= 256
 
@@ -132,7 +145,9 @@ __device__ AItem decode_item(const AbsorbParams& p, int item) {
   return it;
 }
 
+template <bool kF8>
 __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_constant__ AbsorbParams p) {
+  using SS = SSide<kF8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
@@ -147,8 +162,14 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
 
   if (tid == 0) {
     prefetch_tensormap(&p.tm_c4);
-    prefetch_tensormap(&p.tm_kr);
-    prefetch_tensormap(&p.tm_qlat);
+    if (kF8) {
+      prefetch_tensormap(&p.tm_f8);
+      prefetch_tensormap(&p.tm_kr8);
+      prefetch_tensormap(&p.tm_qlat8);
+    } else {
+      prefetch_tensormap(&p.tm_kr);
+      prefetch_tensormap(&p.tm_qlat);
+    }
     for (uint32_t i = 0; i < kANumBars; ++i) {
       uint32_t cnt = 1;
       if ((i >= kBSFree && i < kBSFree + 2) || i == kBQReady || i == kBCDone) cnt = 4;
@@ -169,58 +190,66 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
   if (rank == 0) {
     // ================================================================ S side
     if (warp == 0 || warp == 2 || warp == 3) {
-      // ---------------------------------------------------------- TMA: a stage's boxes leave from three
-      // warps (warp 0: latent blocks 0-3, warp 3: blocks 4-7, warp 2: k_rope), since the per-SM load
-      // rate grows with the number of issuing warps; warp 0 arms the stage's barrier and loads Q
+      // ---------------------------------------------------------- TMA: a stage's boxes leave from up to
+      // three warps (warp 0: latent blocks 0-3, warp 3: bf16 blocks 4-7, warp 2: k_rope); warp 0 arms the
+      // stage's barrier and loads Q
       if (lane == 0) {
         bool ok = true;
         if (warp == 0 && n > 0) {
           // the tile's absorbed queries: rows q_begin H + row0 .. +127 of qlat, staged over stages 1-2
-          mbar_arrive_expect_tx(abar(sbase, kBQFull), kTxQ);
+          mbar_arrive_expect_tx(abar(sbase, kBQFull), SS::kQBoxes * 16384);
           const int qrow = P.q_begin * H + it.row0;
 #pragma unroll 1
-          for (int cc = 0; cc < 8; ++cc)
-            tma_load_2d(sbase + kAQStage + cc * 16384, &p.tm_qlat, 64 * cc, qrow, abar(sbase, kBQFull));
+          for (int cc = 0; cc < SS::kQBoxes; ++cc)
+            tma_load_2d(sbase + SS::kQStage + cc * 16384, kF8 ? &p.tm_qlat8 : &p.tm_qlat, (kF8 ? 128 : 64) * cc, qrow,
+                        abar(sbase, kBQFull));
         }
         for (int j = 0; j < n && ok; ++j) {
-          const int s = j % kAStages;
-          if (j >= kAStages && !await(p, abar(sbase, kBEmpty + s), ((j / kAStages) - 1) & 1)) { ok = false; break; }
+          const int s = j % SS::kStages;
+          if (j >= SS::kStages && !await(p, abar(sbase, kBEmpty + s), ((j / SS::kStages) - 1) & 1)) { ok = false; break; }
           if (j == 1 && !await(p, abar(sbase, kBQReady), 0)) { ok = false; break; }   // Q copied out of stages 1-2
           const int row = (int)(row_base + it.t0 + kAKeys * j);
-          const uint32_t full = abar(sbase, kBFull + s);
+          const uint32_t full = abar(sbase, kBFull + s), st = sbase + s * SS::kStage;
           if (warp == 0) {
-            mbar_arrive_expect_tx(full, kTxS);
+            mbar_arrive_expect_tx(full, SS::kTx);
             tstamp(p, tr, j, 0);
-            tma_load_3d(sbase + kACBase + s * kACStage, &p.tm_c4, 0, row, 0, full);
+            tma_load_3d(st, kF8 ? &p.tm_f8 : &p.tm_c4, 0, row, 0, full);
           } else if (warp == 3) {
-            tma_load_3d(sbase + kACBase + s * kACStage + 4 * kAAtom, &p.tm_c4, 0, row, 4, full);
+            if (!kF8) tma_load_3d(st + 4 * kAAtom, &p.tm_c4, 0, row, 4, full);
+          } else if (kF8) {
+            tma_load_2d(st + SS::kKr, &p.tm_kr8, kDc / 2, row, full);   // k_rope at byte 512 of a 640-byte row
           } else {
-            tma_load_2d(sbase + kAKrBase + s * kAAtom, &p.tm_kr, kDc, row, full);
+            tma_load_2d(st + SS::kKr, &p.tm_kr, kDc, row, full);
           }
         }
         // the last commits land on this CTA's barriers before it exits
         if (warp == 0)
-          for (int j = max(0, n - kAStages); j < n && ok; ++j)
-            if (!await(p, abar(sbase, kBEmpty + j % kAStages), (j / kAStages) & 1)) ok = false;
+          for (int j = max(0, n - SS::kStages); j < n && ok; ++j)
+            if (!await(p, abar(sbase, kBEmpty + j % SS::kStages), (j / SS::kStages) & 1)) ok = false;
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------- S = Q [c | k_rope]^T
       if (lane == 0 && n > 0) {
         bool ok = await(p, abar(sbase, kBQReady), 0);
         for (int j = 0; j < n && ok; ++j) {
-          const int s = j % kAStages, b = j & 1;
-          if (!await(p, abar(sbase, kBFull + s), (j / kAStages) & 1)) { ok = false; break; }
+          const int s = j % SS::kStages, b = j & 1;
+          if (!await(p, abar(sbase, kBFull + s), (j / SS::kStages) & 1)) { ok = false; break; }
           tstamp(p, tr, j, 1);
           if (j >= 2 && !await(p, abar(sbase, kBSFree + b), ((j >> 1) - 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t c = sbase + kACBase + s * kACStage, kr = sbase + kAKrBase + s * kAAtom;
+          const uint32_t c = sbase + s * SS::kStage, kr = c + SS::kKr;
           const uint32_t d = tmem + kATmS + 64 * b;
+          // latent part: K = 16 (bf16) or 32 (E4M3) per MMA, four k-steps per 128-byte block
+          constexpr int kLat = kF8 ? 16 : 32;
 #pragma unroll
-          for (int kk = 0; kk < 36; ++kk) {
-            const uint64_t bdesc = kk < 32 ? sdesc_sw128(c + (kk >> 2) * kAAtom + (kk & 3) * 32, 16, 1024)
-                                           : sdesc_sw128(kr + (kk - 32) * 32, 16, 1024);
-            mma_bf16_ts(d, tmem + kk * 8, bdesc, kIdescSA, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kLat; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(c + (kk >> 2) * kAAtom + (kk & 3) * 32, 16, 1024);
+            if (kF8) mma_e4m3_ts(d, tmem + kk * 8, bdesc, kIdescS8, kk > 0 ? 1u : 0u);
+            else mma_bf16_ts(d, tmem + kk * 8, bdesc, kIdescSA, kk > 0 ? 1u : 0u);
           }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(d, tmem + SS::kTmRope + kk * 8, sdesc_sw128(kr + kk * 32, 16, 1024), kIdescSA, 1u);
           mma_commit(abar(sbase, kBSFull + b));
           mma_commit(abar(sbase, kBEmpty + s));
           tstamp(p, tr, j, 2);
@@ -235,10 +264,14 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
       const int64_t grow = (int64_t)P.q_begin + tl;
       const int64_t orow = grow * H + h;
       const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+      // E4M3 scores: the latent part of S counts in units of qscale[row] * kv_scale, so q_rope is divided
+      // by it (the two parts share one accumulator) and the softmax multiplies it back
+      const float qs = kF8 ? (live ? __ldg(p.qscale + orow) : 1.f) * p.kv_scale : 1.f;
       if (n > 0) {
         // rotated q_rope from global memory (its loads overlap the qlat TMA)
         const uint4* qr = reinterpret_cast<const uint4*>(p.q + orow * kDqk + kDnope);
         const int64_t delta = live ? (int64_t)__ldg(p.q_pos + grow) - P.rope_offset : 0;
+        const float rq = 1.f / qs;
         uint4 qv[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) qv[c] = live ? __ldg(qr + c) : make_uint4(0, 0, 0, 0);
@@ -251,19 +284,19 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
             float sn, cs;
             rope_sincos(delta, p.rope_frac[4 * c + i], &sn, &cs);
             const float x0 = __uint_as_float(w4[i] << 16), x1 = __uint_as_float(w4[i] & 0xFFFF0000u);
-            w[4 * c + i] = pack_bf16(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+            w[4 * c + i] = pack_bf16((x0 * cs - x1 * sn) * rq, (x0 * sn + x1 * cs) * rq);
           }
         }
-        tmem_st32(tmem + lane_off + 256, w);
-        // qlat: shared memory (TMA, 128-byte swizzled [128 x 64] blocks) -> TMEM columns 0..255
+        tmem_st32(tmem + lane_off + SS::kTmRope, w);
+        // qlat: shared memory (TMA, 128-byte swizzled [128 x 128 B] blocks) -> TMEM columns from 0
         const bool qok = await_warp(p, abar(sbase, kBQFull), 0);
 #pragma unroll 1
-        for (int cc = 0; cc < 8; ++cc) {
+        for (int cc = 0; cc < SS::kQBoxes; ++cc) {
           uint32_t u[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint32_t v4[4];
-            if (qok) lds128(sbase + kAQStage + cc * 16384 + sw128_off((uint32_t)r, (uint32_t)c), v4);
+            if (qok) lds128(sbase + SS::kQStage + cc * 16384 + sw128_off((uint32_t)r, (uint32_t)c), v4);
             else v4[0] = v4[1] = v4[2] = v4[3] = 0u;
             u[4 * c] = v4[0]; u[4 * c + 1] = v4[1]; u[4 * c + 2] = v4[2]; u[4 * c + 3] = v4[3];
           }
@@ -275,7 +308,7 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
         if (lane == 0) mbar_arrive(abar(sbase, kBQReady));
       }
       const int qk = live ? P.q_tok0 + tl : -1;   // last visible key token of the row
-      const float sl2 = p.scale_log2;
+      const float sl2 = p.scale_log2 * qs;
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       const uint32_t peer_p = mapa_shared(sbase + kAPBase, 1u);
@@ -551,6 +584,85 @@ __global__ void __launch_bounds__(256) qabsorb_kernel(const QAbsorbParams p) {
   }
 }
 
+// ---------------------------------------------------------------- q absorption, E4M3 output
+// Block: 32 tokens x all 512 latent columns of one head, so each row's amax
+// is known: qlat8 = e4m3(qlat / s), s = amax / 448 per row (1 for a zero row),
+// qscale = s.  The 512 columns go in four chunks of 128 through the same
+// shared tiles as qabsorb_kernel.
+__global__ void __launch_bounds__(256) qabsorb_e4m3_kernel(const QAbsorbParams p, uint8_t* __restrict__ qlat8,
+                                                           float* __restrict__ qscale) {
+  __shared__ float qs[32][128];
+  __shared__ __align__(16) uint16_t wt[128][128];   // [d][c]
+  const int H = p.num_heads;
+  const int h = blockIdx.z, t0 = blockIdx.x * 32;
+  const int tid = threadIdx.x;
+  const int64_t wrow = (int64_t)H * (kDnope + kDv);
+  for (int i = tid; i < 32 * 16; i += 256) {
+    const int t = i >> 4, ch = i & 15;
+    uint4 a = make_uint4(0, 0, 0, 0);
+    if (t0 + t < p.tokens) a = __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)(t0 + t) * H + h) * kDqk) + ch);
+    const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      qs[t][8 * ch + 2 * k] = __uint_as_float(w4[k] << 16);
+      qs[t][8 * ch + 2 * k + 1] = __uint_as_float(w4[k] & 0xFFFF0000u);
+    }
+  }
+  const int ty = tid >> 5, tx = tid & 31;
+  float acc[4][4][4] = {};   // [chunk][token][column]
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    __syncthreads();         // q tile loaded / previous chunk's W tile consumed
+    for (int i = tid; i < 128 * 16; i += 256) {
+      const int c = i >> 4, ch = i & 15;
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(p.w + (int64_t)(128 * cc + c) * wrow + h * kDnope) + ch);
+      const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        wt[8 * ch + 2 * k][c] = (uint16_t)(w4[k] & 0xFFFFu);
+        wt[8 * ch + 2 * k + 1][c] = (uint16_t)(w4[k] >> 16);
+      }
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int d = 0; d < 128; ++d) {
+      const uint2 wb = *reinterpret_cast<const uint2*>(&wt[d][4 * tx]);
+      const float b0 = __uint_as_float(wb.x << 16), b1 = __uint_as_float(wb.x & 0xFFFF0000u);
+      const float b2 = __uint_as_float(wb.y << 16), b3 = __uint_as_float(wb.y & 0xFFFF0000u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = qs[4 * ty + i][d];
+        acc[cc][i][0] = fmaf(a, b0, acc[cc][i][0]);
+        acc[cc][i][1] = fmaf(a, b1, acc[cc][i][1]);
+        acc[cc][i][2] = fmaf(a, b2, acc[cc][i][2]);
+        acc[cc][i][3] = fmaf(a, b3, acc[cc][i][3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float m = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m = fmaxf(m, fabsf(acc[cc][i][k]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float sc = m > 0.f ? m / 448.f : 1.f;
+    const float inv = 1.f / sc;
+    const int t = t0 + 4 * ty + i;
+    if (t >= p.tokens) continue;
+    const int64_t row = (int64_t)t * H + h;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const uint32_t lo = pack_e4m3x2(acc[cc][i][0] * inv, acc[cc][i][1] * inv);
+      const uint32_t hi = pack_e4m3x2(acc[cc][i][2] * inv, acc[cc][i][3] * inv);
+      *reinterpret_cast<uint32_t*>(qlat8 + row * kDc + 128 * cc + 4 * tx) = lo | (hi << 16);
+    }
+    if (tx == 0) qscale[row] = sc;
+  }
+}
+
 // ---------------------------------------------------------------- output projection
 // Block: 32 rows (tokens of the launch's ranges) x 128 output columns of one
 // head; the 512 latent columns in chunks of 64.
@@ -631,7 +743,10 @@ __global__ void __launch_bounds__(256) absorb_proj_kernel(const __grid_constant_
 static cudaError_t configure_absorb(int dev) {
   static int configured_device = -1;
   if (configured_device == dev) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(absorb_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(absorb_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kASmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(absorb_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmemBytes);
   if (e == cudaSuccess) configured_device = dev;
   return e;
 }
@@ -654,7 +769,8 @@ cudaError_t launch_absorb_attn(const AbsorbParams& p, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, absorb_attn_kernel, p);
+  e = p.fp8_scores ? cudaLaunchKernelEx(&cfg, absorb_attn_kernel<true>, p)
+                   : cudaLaunchKernelEx(&cfg, absorb_attn_kernel<false>, p);
   count_launch();
   return e;
 }
@@ -663,6 +779,14 @@ cudaError_t launch_qabsorb(const QAbsorbParams& p, cudaStream_t s) {
   if (p.tokens == 0) return cudaSuccess;
   const dim3 grid((p.tokens + 31) / 32, kDc / 128, p.num_heads);
   qabsorb_kernel<<<grid, 256, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qabsorb_e4m3(const QAbsorbParams& p, uint8_t* qlat8, float* qscale, cudaStream_t s) {
+  if (p.tokens == 0) return cudaSuccess;
+  const dim3 grid((p.tokens + 31) / 32, 1, p.num_heads);
+  qabsorb_e4m3_kernel<<<grid, 256, 0, s>>>(p, qlat8, qscale);
   count_launch();
   return cudaGetLastError();
 }

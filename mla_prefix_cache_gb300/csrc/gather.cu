@@ -119,6 +119,30 @@ __global__ void __launch_bounds__(kGatherThreads, 2) gather_blocks_kernel(const 
   }
 }
 
+// The FP8 rows of every block, as stored (640 B: 512 E4M3 codes, then k_rope
+// as bf16), in the same logical order as gather_blocks_kernel; slots past a
+// request's length and blocks with a bad id are zeroed.
+__global__ void __launch_bounds__(kGatherThreads, 2) gather_blocks_raw_kernel(const __grid_constant__ GatherBlocksParams p) {
+  constexpr int kChunks = kBlock * kRowBytesFp8 / 16;   // 2560 per block
+  constexpr int kRowChunks = kRowBytesFp8 / 16;         // 40
+  for (int gb = blockIdx.x; gb < p.total_blocks; gb += gridDim.x) {
+    int lo = 0, hi = p.n_reqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.reqs[mid].base_block <= gb) lo = mid; else hi = mid - 1;
+    }
+    const GatherReq rq = p.reqs[lo];
+    const int lb = gb - rq.base_block;
+    const int blk = (lb < p.max_blocks) ? __ldg(p.block_table + (int64_t)rq.req * p.max_blocks + lb) : -1;
+    const bool ok = (blk >= 0 && blk < p.num_blocks);
+    const int live_rows = min(kBlock, rq.seq_len - lb * kBlock);
+    const uint4* src = reinterpret_cast<const uint4*>(p.cache + (int64_t)(ok ? blk : 0) * kBlock * kRowBytesFp8);
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dst) + (int64_t)gb * kBlock * kRowBytesFp8);
+    for (int k = threadIdx.x; k < kChunks; k += kGatherThreads)
+      dst[k] = (ok && k / kRowChunks < live_rows) ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 int gather_grid(int64_t tiles) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -131,6 +155,13 @@ int gather_grid(int64_t tiles) {
 cudaError_t launch_gather_blocks(const GatherBlocksParams& p, cudaStream_t s) {
   if (p.total_blocks == 0) return cudaSuccess;
   gather_blocks_kernel<<<gather_grid(p.total_blocks), kGatherThreads, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_blocks_raw(const GatherBlocksParams& p, cudaStream_t s) {
+  if (p.total_blocks == 0) return cudaSuccess;
+  gather_blocks_raw_kernel<<<gather_grid(p.total_blocks), kGatherThreads, 0, s>>>(p);
   count_launch();
   return cudaGetLastError();
 }

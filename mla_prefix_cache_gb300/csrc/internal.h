@@ -176,6 +176,8 @@ struct GatherBlocksParams {
   GatherReq reqs[kMaxGatherReqs];
 };
 cudaError_t launch_gather_blocks(const GatherBlocksParams& p, cudaStream_t s);
+// FP8 caches: the rows as stored (640 B), same order; dst is a byte buffer.
+cudaError_t launch_gather_blocks_raw(const GatherBlocksParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------ absorbed (latent-space) path
 // One piece of the absorbed path: a key range of one request with one RoPE
@@ -202,6 +204,13 @@ struct AbsorbParams {
   CUtensorMap tm_c4;   // gathered rows: half the latent part of 64 rows as 4 swizzled [64 x 64] blocks
   CUtensorMap tm_kr;   // gathered rows, box 64 x 64 (k_rope at column 512)
   CUtensorMap tm_qlat; // qlat as [T_q * H rows][512], box 64 x 128
+  // E4M3 scores (fp8_scores): the cache's FP8 rows gathered as stored (640 B)
+  CUtensorMap tm_f8;    // their latent codes as 4 swizzled [64 rows x 128 B] blocks
+  CUtensorMap tm_kr8;   // their k_rope as bf16 [rows][320], box 64 x 64 at column 256
+  CUtensorMap tm_qlat8; // E4M3 qlat as [T_q * H rows][512 B], box 128 x 128
+  const float* qscale;  // [T_q * H]: the E4M3 qlat row's scale
+  float kv_scale;
+  int fp8_scores;
   const uint16_t* q;     // [T_q][H][192]: q_rope at 128..191, not rotated
   const uint16_t* qlat;  // [T_q][H][512] bf16: kv_scale * q_nope W_UK,h^T
   const int32_t* q_pos;
@@ -251,6 +260,7 @@ struct ProjParams {
 cudaError_t launch_absorb_attn(const AbsorbParams& p, cudaStream_t s);
 cudaError_t launch_qabsorb(const QAbsorbParams& p, cudaStream_t s);
 cudaError_t launch_absorb_proj(const ProjParams& p, cudaStream_t s);
+cudaError_t launch_qabsorb_e4m3(const QAbsorbParams& p, uint8_t* qlat8, float* qscale, cudaStream_t s);
 
 // Content-addressed block store (blocks.cu): content hash of whole cache
 // blocks and byte comparison of block pairs.

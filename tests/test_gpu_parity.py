@@ -516,3 +516,70 @@ def test_block_store_empty_calls(api):
     assert api.block_hash(dw.kv_cache, e).numel() == 0
     assert api.block_compare(dw.kv_cache, e, e).numel() == 0
     assert api.launch_count() == n0
+
+
+# ---------------------------------------------------------------- absorbed path with E4M3 scores (FP8 caches)
+
+def assert_close_fp8_scores(out, lse, ref_out, ref_lse, nvis):
+    """Tolerances of mla_prefill_ctx_absorbed_fp8, derived from its one extra
+    rounding: qlat to E4M3, a relative error up to 2^-4 (RMS ~0.024) on each
+    of its 512 components.  With unit-variance inputs a scaled logit's latent
+    part has std ~ sqrt(512 * 0.25) / sqrt(192) ~ 0.8, so each logit carries
+    ~0.02 of noise.  That noise is shared by every key of a row, because the
+    rounded qlat is, and the softmax-weighted mean of the keys leans towards
+    qlat (by scale * qlat for unit-variance keys).  So lse moves by
+    ~scale^2 * sum_c dqlat_c qlat_c, RMS ~1e-3 whatever the key count (held
+    to 5e-3), plus the per-key part ~0.02 / sqrt(n) (held to 0.1 / sqrt(n)).
+    A row seeing few keys takes single-logit noise on its output, RMS
+    ~0.02 * |v - out| / sqrt(n) ~ 0.03 / sqrt(n): held per row to 2e-2 +
+    0.2 / sqrt(n) (max) and, averaged over the rows, to 2e-3 + 0.05 / sqrt(n)
+    (mean).  Relative RMS 5e-2 over all.  A CPU emulation of the E4M3
+    rounding reproduces the measured errors."""
+    out, lse = np.asarray(out, np.float64), np.asarray(lse, np.float64)
+    ref_out, ref_lse = np.asarray(ref_out, np.float64), np.asarray(ref_lse, np.float64)
+    assert np.isfinite(out).all()
+    nv = np.broadcast_to(np.asarray(nvis, np.float64).reshape(-1, 1), ref_lse.shape)
+    err = np.abs(out - ref_out)
+    row_max = err.max(axis=-1)
+    assert (row_max <= 2e-2 + 0.2 / np.sqrt(nv)).all(), f"max abs {row_max.max():.3e}"
+    mean_tol = float((OUT_MEAN + 0.05 / np.sqrt(nv)).mean())
+    assert err.mean() <= mean_tol, f"mean abs {err.mean():.3e} (tol {mean_tol:.2e})"
+    le = np.abs(lse - ref_lse)
+    assert (le <= 5e-3 + 0.1 / np.sqrt(nv)).all(), f"lse err {le.max():.3e}"
+    rel = math.sqrt(float((err ** 2).mean())) / (math.sqrt(float((ref_out ** 2).mean())) or 1.0)
+    assert rel <= 5e-2, f"rel rms {rel:.3e}"
+
+
+@pytest.mark.parametrize("case", [
+    dict(H=4, ctx=[513], ext=[20], chunk=192),
+    dict(H=3, ctx=[64, 0, 777], ext=[1, 64, 29], chunk=256),
+    dict(H=2, ctx=[256], ext=[40], chunk=64, doc=64),
+    dict(H=128, ctx=[300], ext=[3], chunk=128),
+], ids=["ragged", "batch", "docs", "h128"])
+def test_absorbed_fp8_scores(api, case):
+    wl = W.make_workload("af", case["H"], case["ctx"], case["ext"], chunk=case["chunk"], kv_dtype="fp8_e4m3",
+                         doc_len=case.get("doc"), seed=90)
+    dw = api.DeviceWorkload(wl)
+    out, lse = dw.run(absorbed="fp8")
+    torch.cuda.synchronize()
+    assert api.device_error(api.prefill.last_workspace) == 0
+    ref_out, ref_lse = O.mla_prefill(**O.workload_args(wl))
+    assert_close_fp8_scores(out.cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, visible_keys(wl))
+
+
+def test_absorbed_fp8_scores_long_context_sampled(api):
+    wl = W.make_workload("afl", 128, [16384], [64], chunk=8192, kv_dtype="fp8_e4m3", seed=91)
+    dw = api.DeviceWorkload(wl)
+    out, lse = dw.run(absorbed="fp8")
+    torch.cuda.synchronize()
+    rows, heads = np.array([0, 31, 63]), np.arange(0, 128, 11)
+    ref_out, ref_lse = O.mla_prefill(**O.workload_args(wl), rows=rows, heads=heads)
+    assert_close_fp8_scores(out.cpu().numpy()[rows][:, heads], lse.cpu().numpy()[rows][:, heads], ref_out, ref_lse,
+                            visible_keys(wl)[rows])
+
+
+def test_absorbed_fp8_scores_needs_fp8_cache(api):
+    from mla_prefix_cache_gb300 import _lib
+    wl = W.make_workload("afb", 2, [128], [4], chunk=64, seed=92)
+    with pytest.raises(_lib.MLAError):
+        api.DeviceWorkload(wl).run(absorbed="fp8")
