@@ -216,7 +216,7 @@ def measured_traffic(workload_name, path="fused"):
     """DRAM bytes per launch of the timed kernel from a committed ncu summary,
     valid only while the kernel source is the one that was profiled."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+    if path not in KERNEL_SOURCES or not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
@@ -292,24 +292,30 @@ def hbm_kernels(dev, flush, peak_gbs, reps=10):
     return res
 
 
-def absorbed_compare(dev, flush, peak, source, reps=10):
-    """The short-extend workload (128 heads, 32K cached + 64 new tokens)
-    through both entry points on the same inputs: median CUDA-event time of a
-    whole call (L2 flushed before each), and the latent attention kernel's
-    tensor-core roofline."""
+def absorbed_compare(dev, flush, peak, source, reps=10, config="short_ext_32k", fp8_scores=False):
+    """A short-extend workload (default: 128 heads, 32K cached + 64 new
+    tokens) through the up-projected and the absorbed entry points (with
+    fp8_scores, the FP8-score one: FP8 caches) on the same inputs: median
+    CUDA-event time of a whole call (L2 flushed before each), and the latent
+    attention kernel's tensor-core roofline."""
     import torch
     from mla_prefix_cache_gb300 import api, workload
 
-    wl = workload.short_ext_32k()
+    wl = workload.by_name(config)
+    mode = "fp8" if fp8_scores else True
     dw = api.DeviceWorkload(wl, dev)
     T_q, H = wl.total_q, wl.num_heads
     out = torch.empty((T_q, H, 128), dtype=torch.float32, device=dev)
     lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     res = {}
-    for absorbed in (False, True):
-        size_fn = api.absorbed_workspace_size if absorbed else api.prefill_workspace_size
-        ws = torch.empty(size_fn(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk), dtype=torch.uint8, device=dev)
+    for absorbed in (False, mode):
+        if absorbed:
+            nbytes = api.absorbed_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk,
+                                                 fp8_scores=fp8_scores)
+        else:
+            nbytes = api.prefill_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         for _ in range(3):
             flush.zero_()
             dw.run(out=out, lse=lse, workspace=ws, absorbed=absorbed)
@@ -328,17 +334,20 @@ def absorbed_compare(dev, flush, peak, source, reps=10):
         res[absorbed] = (float(statistics.median([a.elapsed_time(b) for a, b in ev])),
                          float(statistics.median([a.elapsed_time(b) for a, b in kev])))
         del ws
-    (ms_f, _), (ms_a, kms_a) = res[False], res[True]
+    (ms_f, _), (ms_a, kms_a) = res[False], res[mode]
     att = wl.absorbed_attention_flops()
     achieved = att / (kms_a / 1e3) / 1e12
     return {"workload": workload_config(wl), "ms_fused": ms_f, "ms_absorbed": ms_a, "speedup": ms_f / ms_a,
             "prefill_tok_s_absorbed": T_q / (ms_a / 1e3), "prefill_tok_s_fused": T_q / (ms_f / 1e3),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": measured_traffic(wl.name, "absorbed"),
+                         "frac": achieved / peak,
+                         "traffic": None if fp8_scores else measured_traffic(wl.name, "absorbed"),
                          "kernel": "absorb_attn_kernel",
                          "kernel_ms": kms_a, "peak_source": f"bf16_tflops (burst) of {source} peaks",
                          "note": "tensor-core FLOPs of the latent attention, 2 (576 + 512) per visible "
-                                 "query-key-head, / its event time"}}
+                                 "query-key-head, / its event time" + ("; the 512-wide score part on E4M3 "
+                                 "tensor cores, counted at the bf16 peak" if fp8_scores else "")},
+            "path": "absorbed_fp8" if fp8_scores else "absorbed"}
 
 
 def reuse_compare(dev, flush, reps=5, config="v3_8k", n_global=16, protected_frac=0.10):
@@ -419,9 +428,13 @@ def run_ours(args):
     T_q, H = wl.total_q, wl.num_heads
     out = torch.empty((T_q, H, 128), dtype=torch.float32, device=dev)
     lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
-    absorbed = args.path == "absorbed"
-    size_fn = api.absorbed_workspace_size if absorbed else api.prefill_workspace_size
-    ws = torch.empty(size_fn(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk), dtype=torch.uint8, device=dev)
+    absorbed = {"fused": False, "absorbed": True, "absorbed_fp8": "fp8"}[args.path]
+    if absorbed:
+        nbytes = api.absorbed_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk,
+                                             fp8_scores=absorbed == "fp8")
+    else:
+        nbytes = api.prefill_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -550,9 +563,10 @@ def run_ours(args):
     peaks, source = load_peaks()
     peak = float(peaks["bf16_tflops"])
     hbm = None if args.no_hbm_kernels else hbm_kernels(dev, flush, float(peaks["hbm_gbs"]))
-    cmp_abs = None
+    cmp_abs = cmp_abs8 = None
     if not args.no_absorbed and world == 1 and not absorbed:
         cmp_abs = absorbed_compare(dev, flush, peak, source)
+        cmp_abs8 = absorbed_compare(dev, flush, peak, source, reps=5, config="short_ext_fp8_128k", fp8_scores=True)
     cmp_reuse = None
     if not args.no_reuse and world == 1:
         cmp_reuse = reuse_compare(dev, flush)
@@ -584,6 +598,7 @@ def run_ours(args):
         "hbm_kernels": hbm,
         "hbm_peak_source": f"hbm_gbs of {source} peaks",
         "absorbed": cmp_abs,
+        "absorbed_fp8": cmp_abs8,
         "reuse": cmp_reuse,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -602,8 +617,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="v3_8k")
-    ap.add_argument("--path", choices=["fused", "absorbed"], default="fused",
-                    help="entry point timed: mla_prefill_ctx (up-projected, fused) or mla_prefill_ctx_absorbed")
+    ap.add_argument("--path", choices=["fused", "absorbed", "absorbed_fp8"], default="fused",
+                    help="entry point timed: mla_prefill_ctx (up-projected, fused), mla_prefill_ctx_absorbed, or "
+                         "mla_prefill_ctx_absorbed_fp8 (FP8 caches)")
     ap.add_argument("--no-absorbed", action="store_true",
                     help="skip the absorbed-vs-fused comparison on the short-extend workload")
     ap.add_argument("--no-reuse", action="store_true",

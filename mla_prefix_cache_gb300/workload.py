@@ -267,6 +267,12 @@ def short_ext_32k() -> Workload:
     return make_workload("short_ext_32k", 128, [32768], [64], chunk=16384, seed=5)
 
 
+def short_ext_fp8_128k() -> Workload:
+    """A short extend on the long FP8 cache: 128 heads, 128K FP8-e4m3 cached
+    tokens + 64 new ones, chunk 16K."""
+    return make_workload("short_ext_fp8_128k", 128, [131072], [64], kv_dtype=KV_FP8, chunk=16384, seed=6)
+
+
 CONFIGS = {
     "tiny": tiny,
     "v3_8k": v3_8k,
@@ -274,6 +280,7 @@ CONFIGS = {
     "fp8_128k": fp8_128k,
     "reloc_256k": reloc_256k,
     "short_ext_32k": short_ext_32k,
+    "short_ext_fp8_128k": short_ext_fp8_128k,
 }
 
 
