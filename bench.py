@@ -51,6 +51,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """The largest value over the ranks (replicas: the job ends when its
+    slowest rank does); the process group must exist when world > 1."""
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(units_per_rank_step: float, steps: int, world: int, max_total_ms: float) -> float:
+    """Whole-job throughput of `world` replicas: every rank's units over the
+    slowest rank's time, per second."""
+    return units_per_rank_step * steps * world / (max_total_ms / 1e3)
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -478,14 +495,10 @@ def run_ours(args):
     if api.device_error(ws) != 0:
         raise RuntimeError("device error word set during the timed steps")
 
-    total_ms = sum(step_ms)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     flops = wl.algorithmic_flops()
-    value = flops * K * world / (total_ms / 1e3) / 1e12
-    tok_s = T_q * K * world / (total_ms / 1e3)
+    value = weak_scaling_value(flops, K, world, total_ms) / 1e12
+    tok_s = weak_scaling_value(T_q, K, world, total_ms)
 
     # ---- end to end through the public API: pinned host inputs in, result out.
     # A serving loop: step k's inputs go up (one copy stream) while step k-1
@@ -546,12 +559,10 @@ def run_ours(args):
         stream.wait_event(done_down[K & 1])
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        ems = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(ems, op=dist.ReduceOp.MAX)
-        e2e = {"value": flops * K * world / (float(ems.item()) / 1e3) / 1e12, "unit": UNIT,
+        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": weak_scaling_value(flops, K, world, ems) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
-               "ms_per_step": float(ems.item()) / K,
+               "ms_per_step": ems / K,
                "note": "pinned host inputs copied up and results copied down every step, on two copy streams "
                        "overlapping the neighbouring steps' compute (two device buffer sets)"}
 
