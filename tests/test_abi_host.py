@@ -138,3 +138,30 @@ def test_absorbed_entry_validates_and_sizes(lib):
     want = (want + 255) // 256 * 256 + rows * 4
     assert n == (want + 255) // 256 * 256
     assert lib.mla_prefill_absorbed_workspace_size(1, sl, cq, 8, None, 0, 100, 3) == 0   # chunk not a multiple of 64
+
+
+def test_fp8_score_and_reuse_workspaces(lib):
+    """Host-side sizing of the FP8-score absorbed path and of head-split reuse."""
+    sl, cq = (ctypes.c_int32 * 1)(320), (ctypes.c_int32 * 2)(0, 64)
+    base = lib.mla_prefill_absorbed_workspace_size(1, sl, cq, 8, None, 0, 128, 3)
+    fp8 = lib.mla_prefill_absorbed_fp8_workspace_size(1, sl, cq, 8, None, 0, 128, 3)
+    rows = 64 * 8
+    extra = (5 * 64 * 640 + 255) // 256 * 256 + (rows * 512 + 255) // 256 * 256 + (rows * 4 + 255) // 256 * 256
+    assert fp8 == base + extra          # the FP8 rows as stored, E4M3 qlat, its row scales
+
+    g = (ctypes.c_int32 * 2)(1, 5)
+    none = lib.mla_prefill_reuse_workspace_size(1, sl, cq, 8, None, 0, 128, 3, g, 0, None)
+    two = lib.mla_prefill_reuse_workspace_size(1, sl, cq, 8, None, 0, 128, 3, g, 2, None)
+    prot = (ctypes.c_uint8 * 64)(*([1] * 8 + [0] * 56))
+    both = lib.mla_prefill_reuse_workspace_size(1, sl, cq, 8, None, 0, 128, 3, g, 2, prot)
+    assert 0 < none < two < both
+    bad = (ctypes.c_int32 * 1)(8)       # head outside [0, 8)
+    assert lib.mla_prefill_reuse_workspace_size(1, sl, cq, 8, None, 0, 128, 3, bad, 1, None) == 0
+
+
+def test_fp8_score_entry_needs_fp8_cache(lib):
+    d = ctypes.c_void_p(4096)
+    sl, cq = (ctypes.c_int32 * 1)(320), (ctypes.c_int32 * 2)(0, 64)
+    st = lib.mla_prefill_ctx_absorbed_fp8(d, d, d, 0, 1.0, 8, d, 8, sl, cq, 1, 8, None, 0, 128, d, 0.07, 10000.0, 3,
+                                          d, 0, d, d, 1 << 30, None)
+    assert st == _lib.MLA_ERR_UNSUPPORTED
