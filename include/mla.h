@@ -218,6 +218,31 @@ int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos,
                              void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * mla_prefill_ctx_auto -- mla_prefill_ctx with the path chosen per request:
+ * a request with at most 128 queries (E_r <= 128) goes through the absorbed
+ * path (mla_prefill_ctx_absorbed), the others through the up-projected one,
+ * both writing their rows of the same out and lse.  On GB300 the absorbed
+ * path is faster below about 150 queries per request (9x at one query, 1.8x
+ * at 64, on 32K cached tokens and 128 heads) and slower above.
+ *  workspace      at least mla_prefill_auto_workspace_size(...) bytes: the
+ *                 two paths' workspaces side by side; holds the device error
+ *                 word both report into.
+ *  other arguments as mla_prefill_ctx.
+ * ---------------------------------------------------------------------- */
+size_t mla_prefill_auto_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q,
+                                       int num_heads, const mla_segment* segments, int num_segments,
+                                       int chunk, int parts);
+
+int mla_prefill_ctx_auto(const void* q, const int32_t* q_pos,
+                         const void* kv_cache, int kv_dtype, float kv_scale, int num_blocks,
+                         const int32_t* block_table, int max_blocks_per_req,
+                         const int32_t* seq_lens, const int32_t* cu_q, int num_reqs, int num_heads,
+                         const mla_segment* segments, int num_segments, int chunk,
+                         const void* kv_b_proj, float softmax_scale, float rope_theta, int parts,
+                         void* out, int out_dtype, float* lse,
+                         void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * mla_prefill_ctx_absorbed_fp8 -- mla_prefill_ctx_absorbed for an FP8 cache
  * with the latent part of every score on the FP8 tensor cores: the cache's
  * E4M3 codes are read as stored, and qlat is rounded to E4M3 with one scale

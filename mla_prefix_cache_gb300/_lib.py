@@ -64,6 +64,10 @@ SIGNATURES = {
     "mla_prefill_ctx_absorbed": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_float, c_int, c_void_p, c_int,
                                          i32p, i32p, c_int, c_int, segp, c_int, c_int, c_void_p, c_float, c_float,
                                          c_int, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "mla_prefill_auto_workspace_size": (c_size_t, [c_int, i32p, i32p, c_int, segp, c_int, c_int, c_int]),
+    "mla_prefill_ctx_auto": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_float, c_int, c_void_p, c_int,
+                                     i32p, i32p, c_int, c_int, segp, c_int, c_int, c_void_p, c_float, c_float,
+                                     c_int, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "mla_prefill_absorbed_fp8_workspace_size": (c_size_t, [c_int, i32p, i32p, c_int, segp, c_int, c_int, c_int]),
     "mla_prefill_ctx_absorbed_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_float, c_int, c_void_p, c_int,
                                              i32p, i32p, c_int, c_int, segp, c_int, c_int, c_void_p, c_float,

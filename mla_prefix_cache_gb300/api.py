@@ -77,6 +77,8 @@ def absorbed_workspace_size(seq_lens, cu_q, num_heads: int, segments=None, chunk
     sp, ns, _k3 = _lib.segments_host(segments)
     L = _lib.load()
     fn = L.mla_prefill_absorbed_fp8_workspace_size if fp8_scores else L.mla_prefill_absorbed_workspace_size
+    if fp8_scores == "auto":
+        fn = L.mla_prefill_auto_workspace_size
     n = fn(len(_k1), sl, cq, int(num_heads), sp, ns, int(chunk), int(parts))
     if n == 0:
         raise MLAError("mla_prefill_absorbed_workspace_size", _lib.MLA_ERR_INVALID_ARG)
@@ -92,7 +94,8 @@ def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_
     """MLA chunked prefill of one layer (mla_prefill_ctx; absorbed=True:
     mla_prefill_ctx_absorbed, the same result computed in latent space;
     absorbed="fp8": mla_prefill_ctx_absorbed_fp8, FP8 caches, latent scores
-    on the FP8 tensor cores).
+    on the FP8 tensor cores; absorbed="auto": mla_prefill_ctx_auto, the path
+    chosen per request by its number of queries).
 
     q bf16 [T_q, H, 192] (q_rope unrotated); q_pos int32 [T_q]; kv_cache bf16
     [NB,64,576] or uint8 [NB,64,640] (FP8); block_table int32 [B, max_blocks];
@@ -113,14 +116,17 @@ def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_
     if lse is None:
         lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
     fp8 = absorbed == "fp8"
+    auto = absorbed == "auto"
     if workspace is None:
         if absorbed:
-            ws_bytes = absorbed_workspace_size(keep_sl, keep_cq, H, segments, chunk, parts, fp8_scores=fp8)
+            ws_bytes = absorbed_workspace_size(keep_sl, keep_cq, H, segments, chunk, parts,
+                                               fp8_scores="auto" if auto else fp8)
         else:
             ws_bytes = prefill_workspace_size(keep_sl, keep_cq, H, segments, chunk, parts)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_FP32
-    name = "mla_prefill_ctx_absorbed_fp8" if fp8 else ("mla_prefill_ctx_absorbed" if absorbed else "mla_prefill_ctx")
+    name = ("mla_prefill_ctx_auto" if auto else "mla_prefill_ctx_absorbed_fp8" if fp8
+            else "mla_prefill_ctx_absorbed" if absorbed else "mla_prefill_ctx")
     fn = getattr(L, name)
     st = fn(
         _dev(q, "q", torch.bfloat16), _dev(q_pos, "q_pos", torch.int32), _dev(kv_cache, "kv_cache"),

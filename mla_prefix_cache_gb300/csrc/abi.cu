@@ -49,6 +49,7 @@ static void rope_fracs(double theta, uint64_t* frac) {
 struct Plan {
   std::vector<Split> splits;
   std::vector<RowRange> ranges;
+  std::vector<uint8_t> skip;   // per request, 1: left to another call (its rows are not touched)
   int max_slots = 0;
   int64_t total_q = 0;
 };
@@ -59,9 +60,10 @@ struct Plan {
 // then being [C_r, seq_lens[r]) and its cu_q rows a sorted subset of those
 // queries (their token indices given to the kernel); default C_r =
 // seq_lens[r] - E_r with every query present.
+// skip (optional): requests to leave out; their rows keep their places.
 static int build_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,
                       const mla_segment* segs, int nseg, int chunk, int parts, Plan* plan,
-                      const int32_t* ctx_lens = nullptr) {
+                      const int32_t* ctx_lens = nullptr, const uint8_t* skip = nullptr) {
   if (num_reqs < 0 || num_heads < 1 || nseg < 0) return MLA_ERR_INVALID_ARG;
   if (num_heads > kMaxHeads) return MLA_ERR_UNSUPPORTED;
   if (chunk <= 0) return MLA_ERR_INVALID_ARG;
@@ -93,12 +95,15 @@ static int build_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q
 
   plan->splits.clear();
   plan->ranges.clear();
+  plan->skip.assign(num_reqs, 0);
+  if (skip != nullptr)
+    for (int r = 0; r < num_reqs; ++r) plan->skip[r] = skip[r] ? 1 : 0;
   plan->max_slots = 0;
   plan->total_q = num_reqs > 0 ? cu_q[num_reqs] : 0;
   for (int r = 0; r < num_reqs; ++r) {
     const int E = cu_q[r + 1] - cu_q[r];
     const int C = ctx_lens ? ctx_lens[r] : seq_lens[r] - E;
-    if (E == 0) continue;
+    if (E == 0 || plan->skip[r]) continue;
     int slots = 0;
     auto add = [&](int k0, int k1, int64_t off) {
       Split sp{};
@@ -142,6 +147,7 @@ static int env_int(const char* name, int dflt) {
 }
 
 struct FusedPlan {
+  std::vector<uint8_t> skip;      // the plan's skipped requests
   std::vector<Piece> pieces;      // LPT order, group_begin unset
   std::vector<RowRange> merge;    // requests whose pieces go to partial slots
   std::vector<GatherReq> gather;  // FP8 caches: requests whose rows are dequantised up front
@@ -158,6 +164,7 @@ struct FusedPlan {
 // kernel.
 static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const int32_t* cu_q, int num_reqs,
                             int chunk, bool gather_rows, FusedPlan* fp, const int32_t* ctx_lens = nullptr) {
+  fp->skip = splits.skip;
   fp->pieces.clear();
   fp->merge.clear();
   fp->gather.clear();
@@ -171,7 +178,7 @@ static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const i
   size_t si = 0;
   for (int r = 0; r < num_reqs; ++r) {
     const int E = cu_q[r + 1] - cu_q[r];
-    if (E == 0) continue;
+    if (E == 0 || (!fp->skip.empty() && fp->skip[r])) continue;
     const int C = ctx_lens ? ctx_lens[r] : seq_lens[r] - E;
     std::vector<Piece> pr;
     std::vector<Split> rs;
@@ -624,7 +631,7 @@ static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int 
     ap->pieces.push_back(a);
   }
   for (int r = 0; r < num_reqs; ++r) {
-    if (cu_q[r + 1] == cu_q[r]) continue;
+    if (cu_q[r + 1] == cu_q[r] || (!fp.skip.empty() && fp.skip[r])) continue;
     RowRange rr{};
     rr.row_begin = cu_q[r];
     rr.row_end = cu_q[r + 1];
@@ -665,7 +672,7 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
                             int num_blocks, const int32_t* block_table, int max_blocks, int H, const void* kv_b_proj,
                             float softmax_scale, float rope_theta, void* out, int out_dtype, float* lse,
                             void* workspace, const FusedPlan& fp, const AbsPlan& ap, const AbsWs& aw,
-                            cudaStream_t s, bool fp8_scores = false) {
+                            cudaStream_t s, bool fp8_scores = false, uint32_t* err_word = nullptr) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int64_t T_q = fp.total_q;
   static AbsorbParams p;           // large; built on the host under a lock
@@ -676,7 +683,8 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
   std::memset(&p, 0, sizeof(p));
   const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
   const float vscale = fp8 ? kv_scale : 1.f;
-  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  // err_word: a caller running several sub-calls gives the one word they all report into
+  uint32_t* err = err_word ? err_word : reinterpret_cast<uint32_t*>(ws);
 
   const void* rows_base = static_cast<const void*>(ws + aw.gath_off);
   const uint64_t rows_total = (uint64_t)std::max(fp.gather_blocks, 1) * kBlock;
@@ -719,7 +727,7 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
   }
   if (!ok) return MLA_ERR_CUDA;
 
-  int st = cuda_status(cudaMemsetAsync(err, 0, 256, s));
+  int st = err_word ? MLA_OK : cuda_status(cudaMemsetAsync(err, 0, 256, s));
   if (st != MLA_OK) return st;
   if ((st = gather_rows(fp, kv_cache, fp8, num_blocks, block_table, max_blocks, ws + aw.gath_off, err, s)) != MLA_OK)
     return st;
@@ -731,16 +739,19 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
     qp.q = static_cast<const uint16_t*>(q);
     qp.w = static_cast<const uint16_t*>(kv_b_proj);
     qp.qlat = reinterpret_cast<uint16_t*>(ws + aw.qlat_off);
-    qp.scale = vscale;
-    qp.tokens = (int)T_q;
+    qp.scale = fp8_scores ? 1.f : vscale;   // E4M3 scores: kv_scale enters through the per-row score factor
     qp.num_heads = H;
-    if (fp8_scores) {
-      qp.scale = 1.f;   // kv_scale enters through the per-row score factor
-      if ((st = cuda_status(launch_qabsorb_e4m3(qp, ws + aw.qlat8_off, reinterpret_cast<float*>(ws + aw.qscale_off),
-                                                s))) != MLA_OK)
-        return st;
-    } else if ((st = cuda_status(launch_qabsorb(qp, s))) != MLA_OK) {
-      return st;
+    // only the rows of this call's requests, one launch per run of adjacent ones
+    for (size_t i = 0; i < ap.ranges.size();) {
+      size_t j = i + 1;
+      while (j < ap.ranges.size() && ap.ranges[j].row_begin == ap.ranges[j - 1].row_end) ++j;
+      qp.row0 = ap.ranges[i].row_begin;
+      qp.tokens = ap.ranges[j - 1].row_end - ap.ranges[i].row_begin;
+      st = fp8_scores ? cuda_status(launch_qabsorb_e4m3(qp, ws + aw.qlat8_off,
+                                                        reinterpret_cast<float*>(ws + aw.qscale_off), s))
+                      : cuda_status(launch_qabsorb(qp, s));
+      if (st != MLA_OK) return st;
+      i = j;
     }
   }
 
@@ -1021,6 +1032,47 @@ static int prefill_reuse(const void* q, const int32_t* q_pos, const void* kv_cac
   return cuda_status(launch_reuse_assemble(ra, s));
 }
 
+// ------------------------------------------------------------------ per-request dispatch
+// A request with at most this many queries goes through the absorbed path,
+// the others through the up-projected one (measured crossover between 128
+// and 192 on GB300; the FLOP counts put it near 170).
+constexpr int kAutoAbsorbedMaxQueries = 128;
+
+struct AutoPlan {
+  Plan plan_f, plan_a;
+  FusedPlan fp_f, fp_a;
+  AbsPlan ap;
+  FusedWs fw;
+  AbsWs aw;
+  size_t off_abs = 0, total = 0;
+  bool any_f = false, any_a = false;
+};
+
+static int build_auto_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int H,
+                           const mla_segment* segs, int nseg, int chunk, int parts, AutoPlan* au) {
+  std::vector<uint8_t> is_short(num_reqs), is_long(num_reqs);
+  for (int r = 0; r < num_reqs; ++r) {
+    const int E = cu_q[r + 1] - cu_q[r];
+    is_short[r] = E <= kAutoAbsorbedMaxQueries;
+    is_long[r] = !is_short[r];
+    au->any_a |= E > 0 && is_short[r];
+    au->any_f |= E > 0 && is_long[r];
+  }
+  int st = build_plan(num_reqs, seq_lens, cu_q, H, segs, nseg, chunk, parts, &au->plan_f, nullptr, is_short.data());
+  if (st != MLA_OK) return st;
+  if ((st = build_plan(num_reqs, seq_lens, cu_q, H, segs, nseg, chunk, parts, &au->plan_a, nullptr,
+                       is_long.data())) != MLA_OK)
+    return st;
+  build_fused_plan(au->plan_f, seq_lens, cu_q, num_reqs, chunk, true, &au->fp_f);
+  build_fused_plan(au->plan_a, seq_lens, cu_q, num_reqs, chunk, true, &au->fp_a);
+  build_abs_plan(au->fp_a, H, cu_q, num_reqs, &au->ap);
+  au->fw = fused_ws_layout(au->fp_f, H);
+  au->aw = abs_ws_layout(au->fp_a, au->ap, H);
+  au->off_abs = up256(std::max(au->fw.total, (size_t)256));
+  au->total = up256(au->off_abs + au->aw.total);
+  return MLA_OK;
+}
+
 extern "C" {
 
 int mla_abi_version(void) { return 1; }
@@ -1214,6 +1266,53 @@ int mla_prefill_ctx_absorbed_fp8(const void* q, const int32_t* q_pos, const void
   return prefill_absorbed(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
                           num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, workspace, fplan, ap,
                           aw, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+size_t mla_prefill_auto_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,
+                                       const mla_segment* segments, int num_segments, int chunk, int parts) {
+  static AutoPlan au;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  au = AutoPlan();
+  if (build_auto_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &au) != MLA_OK)
+    return 0;
+  return au.total;
+}
+
+int mla_prefill_ctx_auto(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                         int num_blocks, const int32_t* block_table, int max_blocks_per_req, const int32_t* seq_lens,
+                         const int32_t* cu_q, int num_reqs, int num_heads, const mla_segment* segments,
+                         int num_segments, int chunk, const void* kv_b_proj, float softmax_scale, float rope_theta,
+                         int parts, void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                         mla_stream_t stream) {
+  Plan plan;
+  FusedPlan fplan;
+  int st = prefill_plans(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                         seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
+                         softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
+  if (st != MLA_OK || plan.total_q == 0) return st;
+  static AutoPlan au;              // large; built on the host under a lock
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  au = AutoPlan();
+  if ((st = build_auto_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &au)) != MLA_OK)
+    return st;
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < au.total) return MLA_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);   // the up-projected part's header is the call's
+  if ((st = cuda_status(cudaMemsetAsync(ws, 0, 256, s))) != MLA_OK) return st;
+  if (au.any_f &&
+      (st = prefill_fused(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                          num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, ws, au.fp_f, au.fw, s,
+                          nullptr, true)) != MLA_OK)
+    return st;
+  if (au.any_a &&
+      (st = prefill_absorbed(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                             num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, ws + au.off_abs,
+                             au.fp_a, au.ap, au.aw, s, false, err)) != MLA_OK)
+    return st;
+  return MLA_OK;
 }
 
 int mla_get_device_error(void* workspace, mla_stream_t stream) {

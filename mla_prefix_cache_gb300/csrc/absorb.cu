@@ -532,13 +532,14 @@ __global__ void __launch_bounds__(256) qabsorb_kernel(const QAbsorbParams p) {
   __shared__ float qs[32][128];
   __shared__ __align__(16) uint16_t wt[128][128];   // [d][c]
   const int H = p.num_heads;
-  const int h = blockIdx.z, c0 = blockIdx.y * 128, t0 = blockIdx.x * 32;
+  const int h = blockIdx.z, c0 = blockIdx.y * 128, t0 = p.row0 + blockIdx.x * 32;
+  const int t_end = p.row0 + p.tokens;
   const int tid = threadIdx.x;
   const int64_t wrow = (int64_t)H * (kDnope + kDv);
   for (int i = tid; i < 32 * 16; i += 256) {
     const int t = i >> 4, ch = i & 15;
     uint4 a = make_uint4(0, 0, 0, 0);
-    if (t0 + t < p.tokens) a = __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)(t0 + t) * H + h) * kDqk) + ch);
+    if (t0 + t < t_end) a = __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)(t0 + t) * H + h) * kDqk) + ch);
     const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -576,7 +577,7 @@ __global__ void __launch_bounds__(256) qabsorb_kernel(const QAbsorbParams p) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int t = t0 + 4 * ty + i;
-    if (t >= p.tokens) continue;
+    if (t >= t_end) continue;
     uint2 o;
     o.x = pack_bf16(acc[i][0] * p.scale, acc[i][1] * p.scale);
     o.y = pack_bf16(acc[i][2] * p.scale, acc[i][3] * p.scale);
@@ -594,13 +595,14 @@ __global__ void __launch_bounds__(256) qabsorb_e4m3_kernel(const QAbsorbParams p
   __shared__ float qs[32][128];
   __shared__ __align__(16) uint16_t wt[128][128];   // [d][c]
   const int H = p.num_heads;
-  const int h = blockIdx.z, t0 = blockIdx.x * 32;
+  const int h = blockIdx.z, t0 = p.row0 + blockIdx.x * 32;
+  const int t_end = p.row0 + p.tokens;
   const int tid = threadIdx.x;
   const int64_t wrow = (int64_t)H * (kDnope + kDv);
   for (int i = tid; i < 32 * 16; i += 256) {
     const int t = i >> 4, ch = i & 15;
     uint4 a = make_uint4(0, 0, 0, 0);
-    if (t0 + t < p.tokens) a = __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)(t0 + t) * H + h) * kDqk) + ch);
+    if (t0 + t < t_end) a = __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)(t0 + t) * H + h) * kDqk) + ch);
     const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -651,7 +653,7 @@ __global__ void __launch_bounds__(256) qabsorb_e4m3_kernel(const QAbsorbParams p
     const float sc = m > 0.f ? m / 448.f : 1.f;
     const float inv = 1.f / sc;
     const int t = t0 + 4 * ty + i;
-    if (t >= p.tokens) continue;
+    if (t >= t_end) continue;
     const int64_t row = (int64_t)t * H + h;
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {

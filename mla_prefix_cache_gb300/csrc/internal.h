@@ -235,7 +235,8 @@ struct QAbsorbParams {
   const uint16_t* w;       // kv_b_proj [512][H * 256]
   uint16_t* qlat;          // [T_q][H][512]
   float scale;
-  int tokens;
+  int row0;                // first token row of this launch
+  int tokens;              // rows row0 .. row0 + tokens - 1
   int num_heads;
 };
 

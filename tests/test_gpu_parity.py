@@ -583,3 +583,28 @@ def test_absorbed_fp8_scores_needs_fp8_cache(api):
     wl = W.make_workload("afb", 2, [128], [4], chunk=64, seed=92)
     with pytest.raises(_lib.MLAError):
         api.DeviceWorkload(wl).run(absorbed="fp8")
+
+
+# ---------------------------------------------------------------- per-request dispatch
+
+@pytest.mark.parametrize("case", [
+    dict(H=4, ctx=[300, 500, 64, 0, 200], ext=[5, 300, 64, 129, 1], chunk=128),   # both paths, interleaved
+    dict(H=3, ctx=[256, 128], ext=[200, 40], chunk=64, doc=64),                   # relocated documents
+    dict(H=2, ctx=[513, 64], ext=[160, 7], chunk=192, kv="fp8_e4m3"),            # FP8 cache
+    dict(H=4, ctx=[300], ext=[20], chunk=128),                                    # absorbed only
+    dict(H=4, ctx=[300], ext=[200], chunk=128),                                   # up-projected only
+], ids=["mixed", "docs", "fp8", "short_only", "long_only"])
+def test_prefill_auto_matches_oracle(api, case):
+    wl = W.make_workload("au", case["H"], case["ctx"], case["ext"], chunk=case["chunk"],
+                         kv_dtype=case.get("kv", "bf16"), doc_len=case.get("doc"), seed=95)
+    run_and_compare(api, wl, absorbed="auto")
+
+
+def test_prefill_auto_reports_bad_blocks_of_either_path(api):
+    wl = W.make_workload("ab2", 2, [256, 256], [16, 200], chunk=128, seed=96)
+    for req in (0, 1):                 # request 0: absorbed path, request 1: up-projected
+        dw = api.DeviceWorkload(wl)
+        dw.block_table[req, 1] = -5
+        dw.run(absorbed="auto")
+        torch.cuda.synchronize()
+        assert api.device_error(api.prefill.last_workspace) == 3
