@@ -377,6 +377,45 @@ def absorbed_compare(dev, flush, peak, source, reps=10, config="short_ext_32k", 
             "path": "absorbed_fp8" if fp8_scores else "absorbed"}
 
 
+def auto_compare(dev, flush, reps=5, config="mixed_32k"):
+    """Per-request dispatch against the up-projected path alone, on a mixed
+    batch of long and short requests: median CUDA-event time of a whole call,
+    L2 flushed before each."""
+    import torch
+    from mla_prefix_cache_gb300 import api, workload
+
+    wl = workload.by_name(config)
+    dw = api.DeviceWorkload(wl, dev)
+    T_q, H = wl.total_q, wl.num_heads
+    out = torch.empty((T_q, H, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for mode in (False, "auto"):
+        nbytes = (api.absorbed_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk, fp8_scores="auto")
+                  if mode else api.prefill_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk))
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            flush.zero_()
+            dw.run(out=out, lse=lse, workspace=ws, absorbed=mode)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            flush.zero_()
+            gpu_delay()
+            a.record(stream)
+            dw.run(out=out, lse=lse, workspace=ws, absorbed=mode)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        if api.device_error(ws) != 0:
+            raise RuntimeError("device error word set in the dispatch comparison")
+        res[mode] = float(statistics.median([a.elapsed_time(b) for a, b in ev]))
+        del ws
+    short = int(sum(1 for e in wl.ext_lens.tolist() if 0 < e <= 128))
+    return {"workload": workload_config(wl), "requests_absorbed": short, "ms_fused": res[False],
+            "ms_auto": res["auto"], "speedup": res[False] / res["auto"],
+            "prefill_tok_s_auto": T_q / (res["auto"] / 1e3)}
+
+
 def reuse_compare(dev, flush, reps=5, config="v3_8k", n_global=16, protected_frac=0.10):
     """Head-split reuse against full recomputation on the same inputs: the
     Global heads (every 8th head: 16 of 128, the RedKnot page's 8 of 64) and
@@ -590,9 +629,11 @@ def run_ours(args):
     if not args.no_absorbed and world == 1 and not absorbed:
         cmp_abs = absorbed_compare(dev, flush, peak, source)
         cmp_abs8 = absorbed_compare(dev, flush, peak, source, reps=5, config="short_ext_fp8_128k", fp8_scores=True)
-    cmp_reuse = None
+    cmp_reuse = cmp_auto = None
     if not args.no_reuse and world == 1:
         cmp_reuse = reuse_compare(dev, flush)
+    if not args.no_auto and world == 1 and not absorbed:
+        cmp_auto = auto_compare(dev, flush)
     k_ms = sum(kern_ms) / K
     if absorbed:
         kflops = wl.absorbed_attention_flops()
@@ -624,6 +665,7 @@ def run_ours(args):
         "absorbed": cmp_abs,
         "absorbed_fp8": cmp_abs8,
         "reuse": cmp_reuse,
+        "auto": cmp_auto,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clk,
@@ -646,6 +688,8 @@ def main(argv=None):
                          "mla_prefill_ctx_absorbed_fp8 (FP8 caches)")
     ap.add_argument("--no-absorbed", action="store_true",
                     help="skip the absorbed-vs-fused comparison on the short-extend workload")
+    ap.add_argument("--no-auto", action="store_true",
+                    help="skip the per-request dispatch comparison on the mixed batch")
     ap.add_argument("--no-reuse", action="store_true",
                     help="skip the head-split reuse comparison (16 Global heads, 10% protected rows on v3_8k)")
     ap.add_argument("--no-e2e", action="store_true")

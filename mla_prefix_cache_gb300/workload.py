@@ -273,6 +273,15 @@ def short_ext_fp8_128k() -> Workload:
     return make_workload("short_ext_fp8_128k", 128, [131072], [64], kv_dtype=KV_FP8, chunk=16384, seed=6)
 
 
+def mixed_32k() -> Workload:
+    """A mixed serving batch, 128 heads, BF16: 4 requests with 32K cached +
+    1024 new tokens and 12 short ones with 16K cached + 1 to 64 new tokens,
+    chunk 16K."""
+    ctx = [32768] * 4 + [16384] * 12
+    ext = [1024] * 4 + [1, 4, 16, 64] * 3
+    return make_workload("mixed_32k", 128, ctx, ext, chunk=16384, seed=7)
+
+
 CONFIGS = {
     "tiny": tiny,
     "v3_8k": v3_8k,
@@ -281,6 +290,7 @@ CONFIGS = {
     "reloc_256k": reloc_256k,
     "short_ext_32k": short_ext_32k,
     "short_ext_fp8_128k": short_ext_fp8_128k,
+    "mixed_32k": mixed_32k,
 }
 
 
