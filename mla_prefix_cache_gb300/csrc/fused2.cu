@@ -229,11 +229,16 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       const int grow = grow0 + r;
       const uint4* src = reinterpret_cast<const uint4*>(p.q_bf16 + ((int64_t)(live ? grow : 0) * H + J.head) * kDqk);
       const int64_t delta = live ? (int64_t)__ldg(p.q_pos + grow) - J.rope_offset : 0;
-#pragma unroll 1
+      // all 24 chunks of the row in flight at once: the rows are 384 B pieces
+      // at a stride of H * 384 B, so each load waits a full HBM round trip
+      uint4 qa[24];
+#pragma unroll
+      for (int c = 0; c < 24; ++c) qa[c] = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
       for (int part = 0; part < 3; ++part) {   // q_nope 0..63, q_nope 64..127, rotated q_rope
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 a = live ? __ldg(src + 8 * part + c) : make_uint4(0, 0, 0, 0);
+          const uint4 a = qa[8 * part + c];
           uint32_t w4[4] = {a.x, a.y, a.z, a.w};
           if (part == 2) {
 #pragma unroll
@@ -270,17 +275,12 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       tc_fence_after();
       const uint32_t scol = tmem + lane_off + kTmS + 128 * b + 64 * w;
       uint32_t v[64];
-      if (ok) tmem_ld64(scol, v);
+      float mx = -INFINITY;
+      if (ok) mx = tmem_ld64_max(scol, v);   // the half-row maximum comes with the load
       const int kt0 = J.t0 + 128 * j + 64 * w;
       const bool full = kt0 >= J.k_begin && kt0 + 63 < J.k_end && kt0 + 63 <= qtok;
-      float m8[8];
-      if (full) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(v[i]);
-#pragma unroll
-        for (int c = 8; c < 64; c += 2)
-          m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-      } else {
+      if (!full) {
+        float m8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
@@ -291,8 +291,8 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
           v[c] = __float_as_uint(xv);
           m8[c & 7] = fmaxf(m8[c & 7], xv);
         }
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       // row maximum over both key halves; the barrier also orders both
       // warpgroups' S loads before either overwrites S with P
       xchg[(x * 2 + w) * 128 + r] = mx;

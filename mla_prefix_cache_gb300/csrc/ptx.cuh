@@ -185,6 +185,23 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : "memory");
 }
 
+// tmem_ld64 that also returns the largest of the thread's 64 values as f32
+// (tcgen05.ld.red, sm_103a): the row maximum comes with the load.
+__device__ __forceinline__ float tmem_ld64_max(uint32_t taddr, uint32_t (&r)[64]) {
+  float m;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x64.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %64, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : MLA_R8(0), MLA_R8(8), MLA_R8(16), MLA_R8(24), MLA_R8(32), MLA_R8(40), MLA_R8(48), MLA_R8(56), "=f"(m)
+      : "r"(taddr)
+      : "memory");
+  return m;
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
