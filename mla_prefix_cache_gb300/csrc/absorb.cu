@@ -316,25 +316,18 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
       for (int j = 0; j < n; ++j) {
         const int b = j & 1;
         uint32_t v[64];
+        float mx = -INFINITY;
         if (ok && !await_warp(p, abar(sbase, kBSFull + b), (j >> 1) & 1)) ok = false;
         tc_fence_after();
-        if (ok) tmem_ld64(tmem + lane_off + kATmS + 64 * b, v);
+        if (ok) mx = tmem_ld64_max(tmem + lane_off + kATmS + 64 * b, v);   // the row maximum comes with the load
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(abar(sbase, kBSFree + b));
         if (!ok) break;
         if (tid == 128) tstamp(p, tr, j, 3);
         const int kt0 = it.t0 + kAKeys * j;
-        float m8[8];
-        if (kt0 >= it.k_lo && kt0 + kAKeys - 1 < it.k_hi && kt0 + kAKeys - 1 <= qk) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) m8[i] = fmax3(__uint_as_float(v[i]), __uint_as_float(v[i + 8]), __uint_as_float(v[i + 16]));
-#pragma unroll
-          for (int c = 24; c < 64; c += 8)
-#pragma unroll
-            for (int i = 0; i < 8; i += 2)
-              m8[i >> 1] = fmax3(m8[i >> 1], __uint_as_float(v[c + i]), __uint_as_float(v[c + i + 1]));
-        } else {
+        if (!(kt0 >= it.k_lo && kt0 + kAKeys - 1 < it.k_hi && kt0 + kAKeys - 1 <= qk)) {
+          float m8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
@@ -345,8 +338,8 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
             v[c] = __float_as_uint(x);
             m8[c & 7] = fmaxf(m8[c & 7], x);
           }
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         const float m_tile = mx * sl2;
         float alpha = 1.f;
         if (m_tile > m_used + kARescale) {

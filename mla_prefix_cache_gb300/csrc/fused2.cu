@@ -131,18 +131,31 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       const int ns = is_k ? kKStages : kVStages;
       const uint32_t full0 = is_k ? kBKFull : kBVFull, empty0 = is_k ? kBKEmpty : kBVEmpty;
       TraceAcc tr;
+      // A tile's ring slot is released once the pair's MMAs have read its
+      // stage, before the next tile is waited for, in batches behind one fence
+      // when the ring is deep enough; produced tiles are polled a window at a
+      // time.  Per-tile flag round trips would otherwise pace the loads.
+      const int batch = p.ring_depth >= ns + 4 ? 4 : 1;
+      int rel0 = 0, pend = 0;   // tiles [rel0, rel0 + pend) read but not yet released
+      int ready_to = 0;         // tiles below are known to be produced
       for (int j = 0; j < n_tiles; ++j) {
         const int s = j % ns;
-        const uint64_t w0 = tr.begin(p);
-        if (!wait_flag_geq(p, ready_flag(p, job, ring_slot(p, j)), (uint32_t)j + 1)) { ctl->abort = 1; return; }
-        tr.end(p, w0);
         if (j >= ns) {
-          // the stage is free once the pair's MMAs read it; its tile's ring slot is then consumed here
+          // the stage is free once the pair's MMAs read it
           if (!wait_bar(p, bar_addr(sbase, empty0 + s), ((j / ns) - 1) & 1)) { ctl->abort = 1; return; }
-          fence_proxy_async_global();
-          red_release_gpu_add(consumed_flag(p, job, ring_slot(p, j - ns)), 1u);
+          if (++pend == batch) {
+            release_tiles(p, job, rel0, pend);
+            rel0 += pend;
+            pend = 0;
+          }
         }
-        fence_proxy_async_global();
+        if (j >= ready_to) {
+          const uint64_t w0 = tr.begin(p);
+          ready_to = wait_ready_window(p, job, j, min(n_tiles, j + min(8, p.ring_depth)));
+          tr.end(p, w0);
+          if (ready_to < 0) { ctl->abort = 1; return; }
+          fence_proxy_async_global();   // the acquired tiles, to the TMA reads below
+        }
         const uint32_t full = bar_addr(sbase, full0 + s);
         const uint32_t full_leader = mapa_shared(full, 0u);
         const int zb = (job * p.ring_depth + ring_slot(p, j)) * 4;   // first ring block of the tile
@@ -164,9 +177,9 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       // commits into this CTA's barriers before they are reset), release the slots
       for (int j = max(0, n_tiles - ns); j < n_tiles; ++j) {
         if (!wait_bar(p, bar_addr(sbase, empty0 + j % ns), (j / ns) & 1)) { ctl->abort = 1; return; }
-        fence_proxy_async_global();
-        red_release_gpu_add(consumed_flag(p, job, ring_slot(p, j)), 1u);
+        ++pend;
       }
+      if (pend > 0) release_tiles(p, job, rel0, pend);
       if (is_k) {
         trace_put(p, role, 3, tr.t);
         trace_put(p, role, 7, (unsigned long long)n_tiles);

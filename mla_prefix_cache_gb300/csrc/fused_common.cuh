@@ -96,6 +96,42 @@ __device__ __forceinline__ uint32_t* consumed_flag(const FusedParams& p, int job
   return p.flags + (size_t)job * (2 * (size_t)p.ring_depth) + p.ring_depth + slot;
 }
 
+// Ring tiles [t, end) (end - t <= 8) that are produced, polled together: the
+// relaxed reads of their ready flags go out at once and one fence makes the
+// ones seen an acquire.  Returns the first tile of the range not yet seen
+// produced (> t), waiting (bounded) until tile t is; -1 after a timeout or
+// another CTA's error.
+__device__ inline int wait_ready_window(const FusedParams& p, int job, int t, int end) {
+  uint64_t t0 = 0;
+  for (;;) {
+    uint32_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = t + i < end ? ld_relaxed_gpu(ready_flag(p, job, ring_slot(p, t + i))) : 0u;
+    int k = t;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (k == t + i && t + i < end && v[i] >= (uint32_t)(t + i + 1)) k = t + i + 1;
+    if (k > t) {
+      fence_acq_rel_gpu();
+      return k;
+    }
+    if (t0 == 0) t0 = global_timer_ns();
+    else if (global_timer_ns() - t0 > kWaitLimitNs || aborted_global(p)) {
+      atomicOr(p.err, kErrTimeout);
+      return -1;
+    }
+    __nanosleep(32);
+  }
+}
+
+// Adds 1 to the consumed counts of ring tiles [t, t + n), whose reads (async
+// proxy) are complete, behind a single release fence.
+__device__ inline void release_tiles(const FusedParams& p, int job, int t, int n) {
+  fence_proxy_async_global();
+  fence_acq_rel_gpu();
+  for (int i = 0; i < n; ++i) red_relaxed_gpu_add(consumed_flag(p, job, ring_slot(p, t + i)), 1u);
+}
+
 // Row of logical block `lb` of the job's request in the gathered rows (the
 // gather pass copied the request's blocks in logical order from row_block0 on;
 // it also reported any bad block id).  Rows past the request's blocks are
