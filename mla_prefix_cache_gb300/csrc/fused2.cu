@@ -244,6 +244,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       const int64_t delta = live ? (int64_t)__ldg(p.q_pos + grow) - J.rope_offset : 0;
       // all 24 chunks of the row in flight at once: the rows are 384 B pieces
       // at a stride of H * 384 B, so each load waits a full HBM round trip
+      if (tid == 0) trace_stage(p, role, kTraceOnce, 0);
       uint4 qa[24];
 #pragma unroll
       for (int c = 0; c < 24; ++c) qa[c] = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
@@ -264,9 +265,11 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
           }
           sts128(sbase + kQBase + part * kAtomQ + sw128_off(r, c), w4[0], w4[1], w4[2], w4[3]);
         }
+        if (tid == 0 && part == 0) trace_stage(p, role, kTraceOnce, 1);
       }
       fence_proxy_async_smem();   // visible to the tensor core before the leader issues S
       __syncwarp();
+      if (tid == 0) trace_stage(p, role, kTraceOnce, 2);
       if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_addr(sbase, kBQReady), 0u));   // one arrival per warp
     }
     // ------------------------------------------------------------ softmax / epilogue (warps 0..7)
@@ -367,6 +370,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
         !wait_bar_warp(p, bar_addr(sbase, kBPvDone + (n_tiles - 1) % kSBufs), ((n_tiles - 1) / kSBufs) & 1))
       ok = false;
     if (tid == 0) trace_put(p, role, 6, tr_s.t);
+    if (tid == 0) trace_stage(p, role, kTraceOnce, 3);
     xchg[(4 + w) * 128 + r] = l_part;
     named_bar_sync(1, 256);
     const float l_run = l_part + xchg[(4 + (1 - w)) * 128 + r];
@@ -413,6 +417,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       const float lse = empty ? -INFINITY : m_used * 0.69314718055994531f + logf(l_run);
       (J.slot < 0 ? p.lse : p.part_lse)[orow * H + J.head] = lse;
     }
+    if (tid == 0) trace_stage(p, role, kTraceOnce, 4);
   }
 }
 
@@ -458,6 +463,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
             const int blk = rank == 0 ? 2 * h : (H * kDnope + h * kDv) / 64;   // K_nope or V columns of head h
             tma_load_3d_pair(st + kPW, &p.tm_w, 0, 64 * kx, blk, full_leader);
           }
+          if (kx == 0) trace_stage(p, role, n, rows ? 6 : 7);
         }
       }
       // the stages' last MMAs: take the leader's commits before the barriers are reset
@@ -475,6 +481,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
         const uint64_t wa = tr_acc.begin(p);
         if (n >= 2 && !wait_bar(p, bar_addr(sbase, kBAccEmpty + b), ((n >> 1) - 1) & 1)) { ctl->abort = 1; return; }
         tr_acc.end(p, wa);
+        trace_stage(p, role, n, 0);
         tc_fence_after();
         for (int kx = 0; kx < kDc / 64; ++kx, ++g) {
           const int s = g % kPStages;
@@ -490,6 +497,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
           mma2_commit_both(bar_addr(sbase, kBProdEmpty + s));
         }
         mma2_commit_both(bar_addr(sbase, kBAccFull + b));
+        trace_stage(p, role, n, 1);
       }
       trace_put(p, role, 4, tr_op.t);
       trace_put(p, role, 5, tr_acc.t);
@@ -504,6 +512,12 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
     const float oscale = p.out_scale;
     const uint32_t stage_out = sbase + kPOutBase + wg * 2 * kAtomQ;   // [128 rows x 128 cols] bf16, 2 SW128 blocks
     TraceAcc tr_c;
+    // A pass's ring tile is published one pass later, once this pass's
+    // store is under way: the wait for the store's completion and the
+    // release fences then overlap the next accumulator instead of
+    // delaying it.
+    bool pend = false;        // the previous pass stored a tile not yet published
+    int pend_t = 0, pend_slot = 0;
     for (int n = 0; n < my_passes; ++n) {
       const int pass = pi + n * J.n_prod;
       const int b = n & 1;
@@ -513,6 +527,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       const int tok = J.t0 + 128 * t + r;
       const bool valid = tok >= J.k_begin && tok < J.k_end;
       if (!wait_bar_warp(p, bar_addr(sbase, kBAccFull + b), (n >> 1) & 1)) ctl->abort = 1;
+      if (tid == 0) trace_stage(p, role, n, 2);
       tc_fence_after();
       uint32_t pk[64];
       if (live_tile && !ctl->abort) {
@@ -529,21 +544,24 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(bar_addr(sbase, kBAccEmpty + b), 0u));   // accumulator free
+      if (live_tile && tid == 0 && !ctl->abort) {
+        const uint64_t w0 = tr_c.begin(p);
+        // the slot's previous occupant (tile t - ring) must be published and fully consumed
+        if (t >= p.ring_depth &&
+            !(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - p.ring_depth + 1)) &&
+              wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - p.ring_depth))))
+          ctl->abort = 1;
+        tr_c.end(p, w0);
+        *consumed_flag(p, job, slot) = 0u;    // ordered before the release of `ready`
+      }
+      // the staging buffer is free once the previous store has read it; the
+      // stop decision is taken once for both warpgroups
+      if (r == 0) bulk_wait_read0();
+      if (named_bar_or(1, 256, ctl->abort != 0)) {
+        if (r == 0) bulk_wait0();
+        return;
+      }
       if (live_tile) {
-        const int zb = (job * p.ring_depth + slot) * 4;
-        if (tid == 0 && !ctl->abort) {
-          const uint64_t w0 = tr_c.begin(p);
-          // the slot's previous occupant (tile t - ring) must be published and fully consumed
-          if (t >= p.ring_depth &&
-              !(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - p.ring_depth + 1)) &&
-                wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - p.ring_depth))))
-            ctl->abort = 1;
-          tr_c.end(p, w0);
-          *consumed_flag(p, job, slot) = 0u;    // ordered before the release of `ready` below
-        }
-        // the slot may be written and the staging of the last pass is free; the
-        // stop decision is taken once for both warpgroups
-        if (named_bar_or(1, 256, ctl->abort != 0)) return;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
@@ -552,19 +570,39 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
                    pk[16 * cc + 4 * gq + 1], pk[16 * cc + 4 * gq + 2], pk[16 * cc + 4 * gq + 3]);
         fence_proxy_async_smem();
         named_bar_sync(2 + wg, 128);
+        if (tid == 0) trace_stage(p, role, n, 3);
         if (r == 0) {
-          tma_store_3d(&p.tm_ring, stage_out, 0, 0, zb + 2 * wg);   // K_nope lo | hi, or V lo | hi
+          tma_store_3d(&p.tm_ring, stage_out, 0, 0, (job * p.ring_depth + slot) * 4 + 2 * wg);   // K_nope or V lo | hi
           bulk_commit();
-          bulk_wait0();
-        }
-        named_bar_sync(1, 256);                 // both halves of the tile have landed
-        if (tid == 0) {
-          fence_proxy_async_global();
-          __threadfence();
-          st_release_gpu(ready_flag(p, job, slot), (uint32_t)t + 1);
         }
       }
-      if (named_bar_or(1, 256, ctl->abort != 0)) return;
+      if (pend) {
+        // both halves of the previous tile have landed (each issuing thread
+        // waits for its older store)
+        if (r == 0) {
+          if (live_tile) bulk_wait1(); else bulk_wait0();
+        }
+        named_bar_sync(1, 256);
+        if (tid == 0) {
+          trace_stage(p, role, n, 4);
+          // the stores (async proxy) before the release; the release covers
+          // the other half's store, ordered before it by the barrier
+          fence_proxy_async_global();
+          st_release_gpu(ready_flag(p, job, pend_slot), (uint32_t)pend_t + 1);
+          trace_stage(p, role, n, 5);
+        }
+      }
+      pend = live_tile;
+      pend_t = t;
+      pend_slot = slot;
+    }
+    if (pend) {
+      if (r == 0) bulk_wait0();
+      named_bar_sync(1, 256);
+      if (tid == 0) {
+        fence_proxy_async_global();
+        st_release_gpu(ready_flag(p, job, pend_slot), (uint32_t)pend_t + 1);
+      }
     }
     if (tid == 0) trace_put(p, role, 3, tr_c.t);
   }

@@ -240,11 +240,14 @@ __device__ __forceinline__ float ex2(float x) {
 // RoPE angle of integer position delta for pair k: turns = delta * F_k mod 1,
 // with F_k = theta^(-2k/64) / (2 pi) held as a 64-bit binary fraction.  The
 // wrap-around of the 64-bit product is exactly the reduction modulo one turn.
+// The angle is then in [-pi, pi), where the SFU's sine and cosine are within
+// about 2^-21 absolute: far below the bf16 rounding of the rotated values, and
+// an order of magnitude cheaper than the range-reducing sincosf.
 __device__ __forceinline__ void rope_sincos(int64_t delta, uint64_t frac_turns, float* s, float* c) {
   const uint64_t t = (uint64_t)delta * frac_turns;
   const int32_t hi = (int32_t)(t >> 32);                  // signed turns in [-1/2, 1/2) * 2^32
   const float ang = (float)hi * 1.4629180792671596e-09f;  // 2 pi / 2^32
-  sincosf(ang, s, c);
+  __sincosf(ang, s, c);
 }
 
 }  // namespace mla
@@ -364,6 +367,7 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // all committed bulk stores have completed their writes
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait1() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
 
 // Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
 // Named barrier that also returns the OR of `pred` over the participating
