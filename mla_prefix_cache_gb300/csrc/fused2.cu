@@ -53,12 +53,12 @@ constexpr uint32_t kKBase = 3 * kAtomQ;                            // 49152
 constexpr uint32_t kVBase = kKBase + kKStages * kKStageBytes;      // 147456
 constexpr uint32_t kXchgBase = kVBase + kVStages * kVStageBytes;   // 212992: row maxima / sums of the two halves
 constexpr uint32_t kConsumerEnd = kXchgBase + 6 * 128 * 4;
-// producer
+// producer: this CTA's 128 kv_b_proj columns stay resident for the role
 constexpr int kPStages = 4;
-constexpr uint32_t kPStageBytes = 2 * kAtomQ;                      // C: 128 tokens x 64 | W: 64 x 128 columns
-constexpr uint32_t kPC = 0, kPW = kAtomQ;
-constexpr uint32_t kPOutBase = kPStages * kPStageBytes;            // bf16 staging: [128 x 128] per warpgroup
-constexpr uint32_t kProducerEnd = kPOutBase + 2 * 2 * kAtomQ;
+constexpr uint32_t kPWBase = 0;                                    // W: 8 k-slices [64 x 128 columns]
+constexpr uint32_t kPCBase = 8 * kAtomQ;                           // 131072: latent rows, [128 tokens x 64] a stage
+constexpr uint32_t kPStageBytes = kAtomQ;
+constexpr uint32_t kProducerEnd = kPCBase + kPStages * kPStageBytes;   // 196608
 constexpr uint32_t kBarBase = kConsumerEnd > kProducerEnd ? kConsumerEnd : kProducerEnd;
 constexpr uint32_t kNumBars = 26;
 constexpr uint32_t kSmemBytes = kBarBase + 8 * kNumBars + 64 + 1024;
@@ -78,6 +78,7 @@ constexpr uint32_t kBProdFull = 0;        // leader, 4
 constexpr uint32_t kBProdEmpty = 4;       // both, 4
 constexpr uint32_t kBAccFull = 8;         // both, 2
 constexpr uint32_t kBAccEmpty = 10;       // leader, 2: one arrival per conversion warp
+constexpr uint32_t kBWFull = 12;          // leader: the resident kv_b_proj columns of both CTAs landed
 
 // TMEM columns (per CTA)
 constexpr uint32_t kTmO = 0;              // consumer: O [128 x 128] fp32
@@ -440,9 +441,18 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
   if (my_passes == 0) return;
 
   if constexpr (!kCompute) {
-    if (warp == 8 || warp == 10) {
+    if (warp == 10) {
+      // the head's K_nope (CTA 0) or V (CTA 1) columns, once for every pass of the role
       if (lane != 0) return;
-      const bool rows = warp == 8;
+      const uint32_t full = bar_addr(sbase, kBWFull);
+      const uint32_t full_leader = mapa_shared(full, 0u);
+      if (leader) mbar_arrive_expect_tx(full, 2 * 8 * kAtomQ);
+      const int blk = rank == 0 ? 2 * h : (H * kDnope + h * kDv) / 64;
+      for (int kx = 0; kx < kDc / 64; ++kx)
+        tma_load_3d_pair(sbase + kPWBase + kx * kAtomQ, &p.tm_w, 0, 64 * kx, blk, full_leader);
+      trace_stage(p, role, 0, 7);
+    } else if (warp == 8) {
+      if (lane != 0) return;
       int g = 0;
       for (int n = 0; n < my_passes; ++n) {
         const int pass = pi + n * J.n_prod;
@@ -453,17 +463,10 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
             ctl->abort = 1;
             return;
           }
-          const uint32_t st = sbase + s * kPStageBytes;
           const uint32_t full = bar_addr(sbase, kBProdFull + s);
-          const uint32_t full_leader = mapa_shared(full, 0u);
-          if (rows) {
-            if (leader) mbar_arrive_expect_tx(full, 2 * kPStageBytes);     // both CTAs' rows and columns
-            tma_load_2d_pair(st + kPC, &p.tm_kr128, 64 * kx, row0, full_leader);
-          } else {
-            const int blk = rank == 0 ? 2 * h : (H * kDnope + h * kDv) / 64;   // K_nope or V columns of head h
-            tma_load_3d_pair(st + kPW, &p.tm_w, 0, 64 * kx, blk, full_leader);
-          }
-          if (kx == 0) trace_stage(p, role, n, rows ? 6 : 7);
+          if (leader) mbar_arrive_expect_tx(full, 2 * kPStageBytes);     // both CTAs' rows
+          tma_load_2d_pair(sbase + kPCBase + s * kPStageBytes, &p.tm_kr128, 64 * kx, row0, mapa_shared(full, 0u));
+          if (kx == 0) trace_stage(p, role, n, 6);
         }
       }
       // the stages' last MMAs: take the leader's commits before the barriers are reset
@@ -475,6 +478,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
     } else if (warp == 9 && leader) {
       if (lane != 0) return;
       TraceAcc tr_op, tr_acc;
+      if (!wait_bar(p, bar_addr(sbase, kBWFull), 0)) { ctl->abort = 1; return; }
       int g = 0;
       for (int n = 0; n < my_passes; ++n) {
         const int b = n & 1;
@@ -489,11 +493,12 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
           if (!wait_bar(p, bar_addr(sbase, kBProdFull + s), (g / kPStages) & 1)) { ctl->abort = 1; return; }
           tr_op.end(p, w0);
           tc_fence_after();
-          const uint32_t st = sbase + s * kPStageBytes;
+          const uint32_t st = sbase + kPCBase + s * kPStageBytes;
+          const uint32_t wst = sbase + kPWBase + kx * kAtomQ;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma2_ss(tmem + kTmAcc + 256 * b, sdesc_sw128(st + kPC + kk * 32, 16, 1024),
-                    sdesc_sw128(st + kPW + kk * 2048, kAtom64, 1024), kIdescUp, (kx | kk) ? 1u : 0u);
+            mma2_ss(tmem + kTmAcc + 256 * b, sdesc_sw128(st + kk * 32, 16, 1024),
+                    sdesc_sw128(wst + kk * 2048, kAtom64, 1024), kIdescUp, (kx | kk) ? 1u : 0u);
           mma2_commit_both(bar_addr(sbase, kBProdEmpty + s));
         }
         mma2_commit_both(bar_addr(sbase, kBAccFull + b));
@@ -510,12 +515,13 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
     const int r = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float oscale = p.out_scale;
-    const uint32_t stage_out = sbase + kPOutBase + wg * 2 * kAtomQ;   // [128 rows x 128 cols] bf16, 2 SW128 blocks
+    // after the transpose lane l holds 16-byte chunk l % 8 of rows 8 (l / 8) + e of the warp's 32
+    const int st_row = (warp & 3) * 32 + 8 * (lane >> 3), st_chunk = lane & 7;
     TraceAcc tr_c;
-    // A pass's ring tile is published one pass later, once this pass's
-    // store is under way: the wait for the store's completion and the
-    // release fences then overlap the next accumulator instead of
-    // delaying it.
+    // A pass's tile is stored straight from registers and published at the
+    // next pass's barrier (which orders every thread's stores before the
+    // release), so neither the stores' completion nor the release fence
+    // delays the next accumulator.
     bool pend = false;        // the previous pass stored a tile not yet published
     int pend_t = 0, pend_slot = 0;
     for (int n = 0; n < my_passes; ++n) {
@@ -544,65 +550,53 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(bar_addr(sbase, kBAccEmpty + b), 0u));   // accumulator free
-      if (live_tile && tid == 0 && !ctl->abort) {
-        const uint64_t w0 = tr_c.begin(p);
-        // the slot's previous occupant (tile t - ring) must be published and fully consumed
-        if (t >= p.ring_depth &&
-            !(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - p.ring_depth + 1)) &&
-              wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - p.ring_depth))))
-          ctl->abort = 1;
-        tr_c.end(p, w0);
-        *consumed_flag(p, job, slot) = 0u;    // ordered before the release of `ready`
+      // every thread's stores of the previous tile are behind this barrier;
+      // the stop decision is taken here for both warpgroups
+      if (named_bar_or(1, 256, ctl->abort != 0)) return;
+      // publish the previous tile before waiting for this tile's slot: a
+      // consumer may need it to get to the release that frees the slot
+      if (pend && tid == 0) {
+        trace_stage(p, role, n, 4);
+        st_release_gpu(ready_flag(p, job, pend_slot), (uint32_t)pend_t + 1);
+        trace_stage(p, role, n, 5);
       }
-      // the staging buffer is free once the previous store has read it; the
-      // stop decision is taken once for both warpgroups
-      if (r == 0) bulk_wait_read0();
-      if (named_bar_or(1, 256, ctl->abort != 0)) {
-        if (r == 0) bulk_wait0();
-        return;
+      if (live_tile && t >= p.ring_depth) {
+        // the slot's previous occupant (tile t - ring) must be published and
+        // fully consumed before anyone writes it
+        if (tid == 0 && !ctl->abort) {
+          const uint64_t w0 = tr_c.begin(p);
+          if (!(wait_flag_geq(p, ready_flag(p, job, slot), (uint32_t)(t - p.ring_depth + 1)) &&
+                wait_flag_geq(p, consumed_flag(p, job, slot), 2u * (uint32_t)consumers_needing_tile(J, t - p.ring_depth))))
+            ctl->abort = 1;
+          tr_c.end(p, w0);
+        }
+        if (named_bar_or(1, 256, ctl->abort != 0)) return;
       }
+      if (live_tile && tid == 0) *consumed_flag(p, job, slot) = 0u;   // ordered before the release of `ready`
       if (live_tile) {
+        // ring block [128 tokens x 64 columns]: each warp store covers four
+        // whole 128-byte rows
+        uint16_t* dst = p.ring + ((size_t)(job * p.ring_depth + slot) * 4 + 2 * wg) * (128 * 64);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+        for (int hb = 0; hb < 2; ++hb) {
+          uint4 c[8];
 #pragma unroll
-          for (int gq = 0; gq < 4; ++gq)
-            sts128(stage_out + (cc >> 1) * kAtomQ + sw128_off(r, (cc & 1) * 4 + gq), pk[16 * cc + 4 * gq],
-                   pk[16 * cc + 4 * gq + 1], pk[16 * cc + 4 * gq + 2], pk[16 * cc + 4 * gq + 3]);
-        fence_proxy_async_smem();
-        named_bar_sync(2 + wg, 128);
+          for (int e = 0; e < 8; ++e)
+            c[e] = make_uint4(pk[32 * hb + 4 * e], pk[32 * hb + 4 * e + 1], pk[32 * hb + 4 * e + 2], pk[32 * hb + 4 * e + 3]);
+          transpose8x16B(c, lane);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<uint4*>(dst + (size_t)hb * (128 * 64) + (size_t)(st_row + e) * 64 + st_chunk * 8) = c[e];
+        }
         if (tid == 0) trace_stage(p, role, n, 3);
-        if (r == 0) {
-          tma_store_3d(&p.tm_ring, stage_out, 0, 0, (job * p.ring_depth + slot) * 4 + 2 * wg);   // K_nope or V lo | hi
-          bulk_commit();
-        }
-      }
-      if (pend) {
-        // both halves of the previous tile have landed (each issuing thread
-        // waits for its older store)
-        if (r == 0) {
-          if (live_tile) bulk_wait1(); else bulk_wait0();
-        }
-        named_bar_sync(1, 256);
-        if (tid == 0) {
-          trace_stage(p, role, n, 4);
-          // the stores (async proxy) before the release; the release covers
-          // the other half's store, ordered before it by the barrier
-          fence_proxy_async_global();
-          st_release_gpu(ready_flag(p, job, pend_slot), (uint32_t)pend_t + 1);
-          trace_stage(p, role, n, 5);
-        }
       }
       pend = live_tile;
       pend_t = t;
       pend_slot = slot;
     }
     if (pend) {
-      if (r == 0) bulk_wait0();
       named_bar_sync(1, 256);
-      if (tid == 0) {
-        fence_proxy_async_global();
-        st_release_gpu(ready_flag(p, job, pend_slot), (uint32_t)pend_t + 1);
-      }
+      if (tid == 0) st_release_gpu(ready_flag(p, job, pend_slot), (uint32_t)pend_t + 1);
     }
     if (tid == 0) trace_put(p, role, 3, tr_c.t);
   }

@@ -225,6 +225,28 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Transpose of 8 x 8 16-byte chunks within each group of 8 lanes: on entry
+// lane l holds chunks 0..7 of row l; on return it holds chunk l % 8 of rows
+// 8 (l / 8) + 0..7.  Three exchange rounds (lane distance 4, 2, 1), each
+// swapping the off-diagonal half of the current blocks with the partner lane.
+__device__ __forceinline__ void transpose8x16B(uint4 (&c)[8], int lane) {
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (e & m) continue;
+      const uint4 send = hi ? c[e] : c[e | m];
+      uint4 got;
+      got.x = __shfl_xor_sync(0xffffffffu, send.x, m);
+      got.y = __shfl_xor_sync(0xffffffffu, send.y, m);
+      got.z = __shfl_xor_sync(0xffffffffu, send.z, m);
+      got.w = __shfl_xor_sync(0xffffffffu, send.w, m);
+      if (hi) c[e] = got; else c[e | m] = got;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi

@@ -249,6 +249,15 @@ def test_prefill_small_workspace_runs_in_several_launches(api):
         dw.run(workspace=tiny_ws)
 
 
+@pytest.mark.parametrize("depth", [4, 8])
+def test_prefill_shallow_ring_wraps(api, depth, monkeypatch):
+    """K/V rings shallower than a piece: producers reuse ring slots once every
+    consumer has released them (single releases at depth 4, batched at 8)."""
+    monkeypatch.setenv("MLA_RING_DEPTH", str(depth))
+    wl = W.make_workload("ring", 2, [1500, 600], [300, 200], chunk=2048, seed=36)   # 15 and 7 tiles
+    run_and_compare(api, wl)
+
+
 @pytest.mark.parametrize("kernel", [
     {"MLA_CTA_PAIR": "0", "MLA_PAIR": "0"},   # single-CTA kernel
     {"MLA_CTA_PAIR": "0", "MLA_PAIR": "1"},   # single-CTA kernel, consumer pairs sharing K/V loads by multicast
