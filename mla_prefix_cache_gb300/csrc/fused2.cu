@@ -629,9 +629,27 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
     const Piece& P = p.pieces[lo];
     const int n_pairs = (P.n_cons + 1) >> 1;
     const int local = g - P.group_begin;
+    // Roles of a piece in queue order: the producers of head 0, then per head
+    // h the producers of head h + 1 followed by the consumers of head h.  A
+    // head's producers thus run one head ahead of its consumers, which find
+    // their first tiles ready, and still precede them in the queue.
+    const int per_head = P.n_prod + n_pairs;
+    int head, idx;
+    bool producer;
+    if (local < P.n_prod) {
+      head = 0;
+      producer = true;
+      idx = local;
+    } else {
+      const int hb = (local - P.n_prod) / per_head, r = local - P.n_prod - hb * per_head;
+      const bool ahead = hb + 1 < p.num_heads;
+      producer = ahead && r < P.n_prod;
+      head = producer ? hb + 1 : hb;
+      idx = ahead ? (producer ? r : r - P.n_prod) : r;
+    }
     Job J;
     J.req = P.req;
-    J.head = local / (P.n_prod + n_pairs);
+    J.head = head;
     J.q_begin = P.q_begin;
     J.q_count = P.q_count;
     J.q_tok0 = P.q_tok0;
@@ -646,9 +664,6 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
     J.row_block0 = P.row_block0;
     J.rope_offset = P.rope_offset;
     const int job = lo * p.num_heads + J.head;
-    const int gi = local - J.head * (P.n_prod + n_pairs);
-    const bool producer = gi < P.n_prod;
-    const int idx = producer ? gi : gi - P.n_prod;
     const int slot = g * 2 + (int)rank;   // trace slot
     if (kCompute && tid == 32) {
       // fresh barriers for this role (every barrier is idle here)
