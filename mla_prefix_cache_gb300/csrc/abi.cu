@@ -471,6 +471,12 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     ok &= encode_map(&p.tm_ring64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + fw.ring_off, d, st, b64,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  if (T_q > 0) {
+    const uint64_t d[3] = {(uint64_t)kDqk, (uint64_t)H, (uint64_t)T_q};
+    const uint64_t st[2] = {(uint64_t)kDqk * 2, (uint64_t)H * kDqk * 2};
+    const uint32_t b[3] = {64, 1, 128};
+    ok &= encode_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   if (!ok) return MLA_ERR_CUDA;
 
   uint32_t* err = reinterpret_cast<uint32_t*>(ws + fw.err_off);

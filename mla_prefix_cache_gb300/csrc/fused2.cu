@@ -60,7 +60,7 @@ constexpr uint32_t kPCBase = 8 * kAtomQ;                           // 131072: la
 constexpr uint32_t kPStageBytes = kAtomQ;
 constexpr uint32_t kProducerEnd = kPCBase + kPStages * kPStageBytes;   // 196608
 constexpr uint32_t kBarBase = kConsumerEnd > kProducerEnd ? kConsumerEnd : kProducerEnd;
-constexpr uint32_t kNumBars = 26;
+constexpr uint32_t kNumBars = 27;
 constexpr uint32_t kSmemBytes = kBarBase + 8 * kNumBars + 64 + 1024;
 static_assert(kSmemBytes <= 232448, "more than 227 KB of shared memory per CTA");
 
@@ -73,6 +73,7 @@ constexpr uint32_t kBVEmpty = 13;         // both, 4
 constexpr uint32_t kBSFull = 17;          // both, 3: S of a buffer computed
 constexpr uint32_t kBPFull = 20;          // leader, 3: P of a buffer written, one arrival per softmax warp
 constexpr uint32_t kBPvDone = 23;         // both, 3: PV reading a buffer done
+constexpr uint32_t kBQLand = 26;          // both, own: this CTA's Q rows landed (TMA)
 // producer barriers
 constexpr uint32_t kBProdFull = 0;        // leader, 4
 constexpr uint32_t kBProdEmpty = 4;       // both, 4
@@ -129,6 +130,13 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       // ---------------------------------------------------------- TMA loads of this CTA's half
       if (lane != 0) return;
       const bool is_k = warp == 8;
+      if (!is_k) {
+        // this CTA's 128 query rows of the head, rotated in place by warps 0-3
+        const uint32_t qb = bar_addr(sbase, kBQLand);
+        mbar_arrive_expect_tx(qb, 3 * kAtomQ);
+        for (int part = 0; part < 3; ++part)
+          tma_load_3d(sbase + kQBase + part * kAtomQ, &p.tm_q, 64 * part, J.head, grow0, qb);
+      }
       const int ns = is_k ? kKStages : kVStages;
       const uint32_t full0 = is_k ? kBKFull : kBVFull, empty0 = is_k ? kBKEmpty : kBVEmpty;
       TraceAcc tr;
@@ -237,36 +245,32 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
     }
   } else {
     if (warp < 4) {
-      // ---------------------------------------------------------- Q -> shared memory (warpgroup 0)
+      // ---------------------------------------------------------- Q: RoPE of the landed rows (warpgroup 0)
+      // q_nope and q_rope arrive by TMA (rows past the piece's queries are
+      // other rows or zeros, and their results are not written); q_rope is
+      // rotated by q_pos - offset in place while the angles are computed
+      // during the load.
       const int r = tid & 127;
-      const bool live = r < nq;
-      const int grow = grow0 + r;
-      const uint4* src = reinterpret_cast<const uint4*>(p.q_bf16 + ((int64_t)(live ? grow : 0) * H + J.head) * kDqk);
-      const int64_t delta = live ? (int64_t)__ldg(p.q_pos + grow) - J.rope_offset : 0;
-      // all 24 chunks of the row in flight at once: the rows are 384 B pieces
-      // at a stride of H * 384 B, so each load waits a full HBM round trip
+      const int64_t delta = r < nq ? (int64_t)__ldg(p.q_pos + grow0 + r) - J.rope_offset : 0;
       if (tid == 0) trace_stage(p, role, kTraceOnce, 0);
-      uint4 qa[24];
+      float sn[32], cs[32];
 #pragma unroll
-      for (int c = 0; c < 24; ++c) qa[c] = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int part = 0; part < 3; ++part) {   // q_nope 0..63, q_nope 64..127, rotated q_rope
+      for (int i = 0; i < 32; ++i) rope_sincos(delta, p.rope_frac[i], &sn[i], &cs[i]);
+      const bool landed = wait_bar_warp(p, bar_addr(sbase, kBQLand), 0);
+      if (tid == 0) trace_stage(p, role, kTraceOnce, 1);
+      if (landed) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 a = qa[8 * part + c];
-          uint32_t w4[4] = {a.x, a.y, a.z, a.w};
-          if (part == 2) {
+          const uint32_t addr = sbase + kQBase + 2 * kAtomQ + sw128_off(r, c);
+          uint32_t w4[4];
+          lds128(addr, w4);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float sn, cs;
-              rope_sincos(delta, p.rope_frac[4 * c + i], &sn, &cs);
-              const float x0 = __uint_as_float(w4[i] << 16), x1 = __uint_as_float(w4[i] & 0xFFFF0000u);
-              w4[i] = pack_bf16(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
-            }
+          for (int i = 0; i < 4; ++i) {
+            const float x0 = __uint_as_float(w4[i] << 16), x1 = __uint_as_float(w4[i] & 0xFFFF0000u);
+            w4[i] = pack_bf16(x0 * cs[4 * c + i] - x1 * sn[4 * c + i], x0 * sn[4 * c + i] + x1 * cs[4 * c + i]);
           }
-          sts128(sbase + kQBase + part * kAtomQ + sw128_off(r, c), w4[0], w4[1], w4[2], w4[3]);
+          sts128(addr, w4[0], w4[1], w4[2], w4[3]);
         }
-        if (tid == 0 && part == 0) trace_stage(p, role, kTraceOnce, 1);
       }
       fence_proxy_async_smem();   // visible to the tensor core before the leader issues S
       __syncwarp();
@@ -710,6 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused2_prefill_kernel(const __gri
     prefetch_tensormap(&p.tm_ring);
     prefetch_tensormap(&p.tm_ring1);
     prefetch_tensormap(&p.tm_ring64);
+    prefetch_tensormap(&p.tm_q);
   }
   if (tid == 32) {
     ctl->abort = 0;

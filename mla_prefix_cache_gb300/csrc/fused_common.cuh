@@ -34,7 +34,7 @@ __device__ __forceinline__ void trace_put(const FusedParams& p, int role, int wo
 //   [0] K load issued  [1] V load issued  [2] MMA saw K  [3] MMA issued S
 //   [4] MMA saw P  [5] MMA saw V (PV issued next)  [6] softmax saw S  [7] softmax published P
 // Stage kTraceOnce holds one-off stamps of the role (consumer: Q load start,
-// first part stored, Q ready, last PV seen, epilogue done).
+// Q landed, Q ready, last PV seen, epilogue done).
 constexpr int kTraceOnce = 4000;
 __device__ __forceinline__ void trace_stage(const FusedParams& p, int role, int stage, int word) {
   if (p.trace && role == p.trace_detail_role && stage < 4096)

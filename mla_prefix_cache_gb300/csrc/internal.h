@@ -97,6 +97,7 @@ struct FusedParams {
   CUtensorMap tm_ring;   // bf16 ring as [jobs*ring*4 blocks][128 rows][64 cols], box 64 x 128 x 2
   CUtensorMap tm_ring1;  // same ring, box 64 x 128 x 1 (one block: half of a paired consumer's stage)
   CUtensorMap tm_ring64; // same ring, box 64 x 64 x 2 (64 keys of K_nope lo | hi: a CTA pair's half tile)
+  CUtensorMap tm_q;      // q as (column, head, row) of [T_q][H][192], box 64 x 1 x 128: 128 rows of one head
   const uint16_t* q_bf16;  // q [T_q][H][192]
   const int32_t* q_tok;    // optional [T_q]: token index of each query row within its request (rows that are
                            // a sorted subset of the request's queries); nullptr: q_tok0 + row - q_begin
