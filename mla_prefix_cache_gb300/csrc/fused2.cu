@@ -301,13 +301,15 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       const int kt0 = J.t0 + 128 * j + 64 * w;
       const bool full = kt0 >= J.k_begin && kt0 + 63 < J.k_end && kt0 + 63 <= qtok;
       if (!full) {
+        // visible columns form one range [lo, lo + span] of the half tile
+        const int lo = max(J.k_begin - kt0, 0);
+        const int span = min(J.k_end - 1, qtok) - kt0 - lo;   // negative: none
         float m8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const int kt = kt0 + c;
-          const bool okc = kt >= J.k_begin && kt < J.k_end && kt <= qtok;
+          const bool okc = span >= 0 && (uint32_t)(c - lo) <= (uint32_t)span;
           const float xv = okc ? __uint_as_float(v[c]) : -INFINITY;
           v[c] = __float_as_uint(xv);
           m8[c & 7] = fmaxf(m8[c & 7], xv);
@@ -380,6 +382,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
     named_bar_sync(1, 256);
     const float l_run = l_part + xchg[(4 + (1 - w)) * 128 + r];
     if (!ok) { ctl->abort = 1; return; }
+    if (tid == 0) trace_stage(p, role, kTraceOnce, 5);
     tc_fence_after();
     // ---- epilogue: this warpgroup writes output columns 64w .. 64w+63 of this CTA's rows
     const bool empty = n_tiles == 0 || !(l_run > 0.f);
