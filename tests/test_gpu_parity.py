@@ -602,7 +602,8 @@ def test_absorbed_fp8_scores_needs_fp8_cache(api):
     dict(H=2, ctx=[513, 64], ext=[160, 7], chunk=192, kv="fp8_e4m3"),            # FP8 cache
     dict(H=4, ctx=[300], ext=[20], chunk=128),                                    # absorbed only
     dict(H=4, ctx=[300], ext=[200], chunk=128),                                   # up-projected only
-], ids=["mixed", "docs", "fp8", "short_only", "long_only"])
+    dict(H=2, ctx=[200, 100], ext=[96, 97], chunk=128),                           # either side of the threshold
+], ids=["mixed", "docs", "fp8", "short_only", "long_only", "threshold"])
 def test_prefill_auto_matches_oracle(api, case):
     wl = W.make_workload("au", case["H"], case["ctx"], case["ext"], chunk=case["chunk"],
                          kv_dtype=case.get("kv", "bf16"), doc_len=case.get("doc"), seed=95)
