@@ -255,7 +255,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       if (tid == 0) trace_stage(p, role, kTraceOnce, 0);
       float sn[32], cs[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) rope_sincos(delta, p.rope_frac[i], &sn[i], &cs[i]);
+      for (int i = 0; i < 32; ++i) rope_sincos_sfu(delta, p.rope_frac[i], &sn[i], &cs[i]);
       const bool landed = wait_bar_warp(p, bar_addr(sbase, kBQLand), 0);
       if (tid == 0) trace_stage(p, role, kTraceOnce, 1);
       if (landed) {

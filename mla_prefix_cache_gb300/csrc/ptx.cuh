@@ -262,14 +262,20 @@ __device__ __forceinline__ float ex2(float x) {
 // RoPE angle of integer position delta for pair k: turns = delta * F_k mod 1,
 // with F_k = theta^(-2k/64) / (2 pi) held as a 64-bit binary fraction.  The
 // wrap-around of the 64-bit product is exactly the reduction modulo one turn.
-// The angle is then in [-pi, pi), where the SFU's sine and cosine are within
-// about 2^-21 absolute: far below the bf16 rounding of the rotated values, and
-// an order of magnitude cheaper than the range-reducing sincosf.
-__device__ __forceinline__ void rope_sincos(int64_t delta, uint64_t frac_turns, float* s, float* c) {
+__device__ __forceinline__ float rope_angle(int64_t delta, uint64_t frac_turns) {
   const uint64_t t = (uint64_t)delta * frac_turns;
   const int32_t hi = (int32_t)(t >> 32);                  // signed turns in [-1/2, 1/2) * 2^32
-  const float ang = (float)hi * 1.4629180792671596e-09f;  // 2 pi / 2^32
-  __sincosf(ang, s, c);
+  return (float)hi * 1.4629180792671596e-09f;             // 2 pi / 2^32
+}
+__device__ __forceinline__ void rope_sincos(int64_t delta, uint64_t frac_turns, float* s, float* c) {
+  sincosf(rope_angle(delta, frac_turns), s, c);
+}
+// The same with the SFU's sine and cosine, for a path where the angles are
+// latency-critical: on [-pi, pi) they are within about 2^-21 absolute, far
+// below the bf16 rounding of the rotated values.  (In the absorbed kernels,
+// where the angles are off the critical path, the SFU form measured slower.)
+__device__ __forceinline__ void rope_sincos_sfu(int64_t delta, uint64_t frac_turns, float* s, float* c) {
+  __sincosf(rope_angle(delta, frac_turns), s, c);
 }
 
 }  // namespace mla
