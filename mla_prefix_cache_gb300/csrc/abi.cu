@@ -476,6 +476,22 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     const uint64_t st[2] = {(uint64_t)kDqk * 2, (uint64_t)H * kDqk * 2};
     const uint32_t b[3] = {64, 1, 128};
     ok &= encode_map(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    // out and the partial states as (column, head, row): a consumer stores a
+    // full 128-row tile of one head with 128-byte boxes
+    const bool ob = out_dtype == MLA_OUT_BF16;
+    const uint64_t es = ob ? 2 : 4;
+    const uint64_t dout[3] = {(uint64_t)kDv, (uint64_t)H, (uint64_t)T_q};
+    const uint64_t sout[2] = {(uint64_t)kDv * es, (uint64_t)H * kDv * es};
+    const uint32_t bout[3] = {ob ? 64u : 32u, 1, 128};
+    ok &= encode_map(&p.tm_out, ob ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dout,
+                     sout, bout, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (fp.max_slots > 0) {
+      const uint64_t dpart[3] = {(uint64_t)kDv, (uint64_t)H, (uint64_t)fp.max_slots * (uint64_t)T_q};
+      const uint64_t spart[2] = {(uint64_t)kDv * 4, (uint64_t)H * kDv * 4};
+      const uint32_t bpart[3] = {32, 1, 128};
+      ok &= encode_map(&p.tm_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws + fw.out_off, dpart, spart, bpart,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+    }
   }
   if (!ok) return MLA_ERR_CUDA;
 

@@ -54,11 +54,11 @@ constexpr uint32_t kVBase = kKBase + kKStages * kKStageBytes;      // 147456
 constexpr uint32_t kXchgBase = kVBase + kVStages * kVStageBytes;   // 212992: row maxima / sums of the two halves
 constexpr uint32_t kConsumerEnd = kXchgBase + 6 * 128 * 4;
 // producer: this CTA's 128 kv_b_proj columns stay resident for the role
-constexpr int kPStages = 4;
+constexpr int kPStages = 6;
 constexpr uint32_t kPWBase = 0;                                    // W: 8 k-slices [64 x 128 columns]
 constexpr uint32_t kPCBase = 8 * kAtomQ;                           // 131072: latent rows, [128 tokens x 64] a stage
 constexpr uint32_t kPStageBytes = kAtomQ;
-constexpr uint32_t kProducerEnd = kPCBase + kPStages * kPStageBytes;   // 196608
+constexpr uint32_t kProducerEnd = kPCBase + kPStages * kPStageBytes;   // 229376
 constexpr uint32_t kBarBase = kConsumerEnd > kProducerEnd ? kConsumerEnd : kProducerEnd;
 constexpr uint32_t kNumBars = 27;
 constexpr uint32_t kSmemBytes = kBarBase + 8 * kNumBars + 64 + 1024;
@@ -75,11 +75,12 @@ constexpr uint32_t kBPFull = 20;          // leader, 3: P of a buffer written, o
 constexpr uint32_t kBPvDone = 23;         // both, 3: PV reading a buffer done
 constexpr uint32_t kBQLand = 26;          // both, own: this CTA's Q rows landed (TMA)
 // producer barriers
-constexpr uint32_t kBProdFull = 0;        // leader, 4
-constexpr uint32_t kBProdEmpty = 4;       // both, 4
-constexpr uint32_t kBAccFull = 8;         // both, 2
-constexpr uint32_t kBAccEmpty = 10;       // leader, 2: one arrival per conversion warp
-constexpr uint32_t kBWFull = 12;          // leader: the resident kv_b_proj columns of both CTAs landed
+constexpr uint32_t kBProdFull = 0;                     // leader, kPStages
+constexpr uint32_t kBProdEmpty = kPStages;             // both, kPStages
+constexpr uint32_t kBAccFull = 2 * kPStages;           // both, 2
+constexpr uint32_t kBAccEmpty = 2 * kPStages + 2;      // leader, 2: one arrival per conversion warp
+constexpr uint32_t kBWFull = 2 * kPStages + 4;         // leader: the resident kv_b_proj columns of both CTAs landed
+static_assert(kBWFull < kNumBars, "producer barriers");
 
 // TMEM columns (per CTA)
 constexpr uint32_t kTmO = 0;              // consumer: O [128 x 128] fp32
@@ -391,33 +392,74 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
     const int grow = grow0 + r;
     const int64_t orow = J.slot < 0 ? (int64_t)grow : (int64_t)J.slot * p.slot_stride_rows + grow;
     const uint32_t ocol = tmem + lane_off + kTmO + 64 * w;
+    if (nq == 128 && n_tiles > 0) {
+      // A whole tile: the warpgroup stages its 64 columns in the idle K stages
+      // (128-byte swizzled boxes) and one thread stores them by TMA, instead
+      // of 32 scattered 16-byte pieces per warp store.
+      const bool ob = J.slot < 0 && p.out_bf16;
+      const uint32_t stg = sbase + kKBase + (uint32_t)w * 2 * kAtomQ;
 #pragma unroll 1
-    for (int cc = 0; cc < 2; ++cc) {
-      uint32_t o[32];
-      if (n_tiles > 0) tmem_ld32(ocol + cc * 32, o);
-      if (!live) continue;
-      const int col0 = 64 * w + 32 * cc;
-      if (J.slot < 0 && p.out_bf16) {
-        uint16_t* dst = static_cast<uint16_t*>(p.out) + (orow * H + J.head) * kDv + col0;
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(ocol + cc * 32, o);
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          uint4 q;
-          q.x = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 0]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 1]) * inv_l);
-          q.y = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 2]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 3]) * inv_l);
-          q.z = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 4]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 5]) * inv_l);
-          q.w = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 6]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(dst + i) = q;
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(empty ? 0.f : __uint_as_float(o[i]) * inv_l);
+        if (ob) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            sts128(stg + sw128_off(r, 4 * cc + g), pack_bf16(__uint_as_float(o[8 * g]), __uint_as_float(o[8 * g + 1])),
+                   pack_bf16(__uint_as_float(o[8 * g + 2]), __uint_as_float(o[8 * g + 3])),
+                   pack_bf16(__uint_as_float(o[8 * g + 4]), __uint_as_float(o[8 * g + 5])),
+                   pack_bf16(__uint_as_float(o[8 * g + 6]), __uint_as_float(o[8 * g + 7])));
+        } else {
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            sts128(stg + cc * kAtomQ + sw128_off(r, g), o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
         }
-      } else {
-        float* dst = (J.slot < 0 ? static_cast<float*>(p.out) : p.part_out) + (orow * H + J.head) * kDv + col0;
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(2 + w, 128);
+      if (r == 0) {
+        const int row0 = J.slot < 0 ? grow0 : J.slot * p.slot_stride_rows + grow0;
+        if (ob) {
+          tma_store_3d(&p.tm_out, stg, 64 * w, J.head, row0);
+        } else {
+          const CUtensorMap* m = J.slot < 0 ? &p.tm_out : &p.tm_part;
+          tma_store_3d(m, stg, 64 * w, J.head, row0);
+          tma_store_3d(m, stg + kAtomQ, 64 * w + 32, J.head, row0);
+        }
+        bulk_commit();
+        bulk_wait_read0();   // the stages are free again before the role ends
+      }
+    } else {
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t o[32];
+        if (n_tiles > 0) tmem_ld32(ocol + cc * 32, o);
+        if (!live) continue;
+        const int col0 = 64 * w + 32 * cc;
+        if (J.slot < 0 && p.out_bf16) {
+          uint16_t* dst = static_cast<uint16_t*>(p.out) + (orow * H + J.head) * kDv + col0;
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          float4 q;
-          q.x = empty ? 0.f : __uint_as_float(o[i + 0]) * inv_l;
-          q.y = empty ? 0.f : __uint_as_float(o[i + 1]) * inv_l;
-          q.z = empty ? 0.f : __uint_as_float(o[i + 2]) * inv_l;
-          q.w = empty ? 0.f : __uint_as_float(o[i + 3]) * inv_l;
-          *reinterpret_cast<float4*>(dst + i) = q;
+          for (int i = 0; i < 32; i += 8) {
+            uint4 q;
+            q.x = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 0]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 1]) * inv_l);
+            q.y = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 2]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 3]) * inv_l);
+            q.z = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 4]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 5]) * inv_l);
+            q.w = pack_bf16(empty ? 0.f : __uint_as_float(o[i + 6]) * inv_l, empty ? 0.f : __uint_as_float(o[i + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(dst + i) = q;
+          }
+        } else {
+          float* dst = (J.slot < 0 ? static_cast<float*>(p.out) : p.part_out) + (orow * H + J.head) * kDv + col0;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4 q;
+            q.x = empty ? 0.f : __uint_as_float(o[i + 0]) * inv_l;
+            q.y = empty ? 0.f : __uint_as_float(o[i + 1]) * inv_l;
+            q.z = empty ? 0.f : __uint_as_float(o[i + 2]) * inv_l;
+            q.w = empty ? 0.f : __uint_as_float(o[i + 3]) * inv_l;
+            *reinterpret_cast<float4*>(dst + i) = q;
+          }
         }
       }
     }
@@ -718,6 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused2_prefill_kernel(const __gri
     prefetch_tensormap(&p.tm_ring1);
     prefetch_tensormap(&p.tm_ring64);
     prefetch_tensormap(&p.tm_q);
+    prefetch_tensormap(&p.tm_out);
   }
   if (tid == 32) {
     ctl->abort = 0;

@@ -98,6 +98,8 @@ struct FusedParams {
   CUtensorMap tm_ring1;  // same ring, box 64 x 128 x 1 (one block: half of a paired consumer's stage)
   CUtensorMap tm_ring64; // same ring, box 64 x 64 x 2 (64 keys of K_nope lo | hi: a CTA pair's half tile)
   CUtensorMap tm_q;      // q as (column, head, row) of [T_q][H][192], box 64 x 1 x 128: 128 rows of one head
+  CUtensorMap tm_out;    // out as (column, head, row) of [T_q][H][128], box 32 (fp32) or 64 (bf16) x 1 x 128
+  CUtensorMap tm_part;   // partial states, fp32 [slots * T_q][H][128], box 32 x 1 x 128
   const uint16_t* q_bf16;  // q [T_q][H][192]
   const int32_t* q_tok;    // optional [T_q]: token index of each query row within its request (rows that are
                            // a sorted subset of the request's queries); nullptr: q_tok0 + row - q_begin
