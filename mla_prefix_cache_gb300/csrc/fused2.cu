@@ -679,9 +679,10 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
     const int n_pairs = (P.n_cons + 1) >> 1;
     const int local = g - P.group_begin;
     // Roles of a piece in queue order: the producers of head 0, then per head
-    // h the producers of head h + 1 followed by the consumers of head h.  A
-    // head's producers thus run one head ahead of its consumers, which find
-    // their first tiles ready, and still precede them in the queue.
+    // h the producers of head h + 1 followed by the consumers of head h (the
+    // longest first).  A head's producers thus run one head ahead of its
+    // consumers, which find their first tiles ready, and still precede them
+    // in the queue.
     const int per_head = P.n_prod + n_pairs;
     int head, idx;
     bool producer;
@@ -695,6 +696,9 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
       producer = ahead && r < P.n_prod;
       head = producer ? hb + 1 : hb;
       idx = ahead ? (producer ? r : r - P.n_prod) : r;
+      // a head's consumer pairs longest first (later query tiles see more
+      // keys), so the last roles of the queue are its shortest
+      if (!producer) idx = n_pairs - 1 - idx;
     }
     Job J;
     J.req = P.req;
