@@ -189,6 +189,7 @@ def test_prefill_tiny(api):
     dict(H=3, ctx=[64, 0, 777], ext=[1, 64, 129], chunk=256),         # ragged batch
     dict(H=2, ctx=[513], ext=[77], chunk=192, kv="fp8_e4m3"),         # FP8 cache
     dict(H=2, ctx=[256], ext=[40], chunk=64, doc=64),                 # relocated documents
+    dict(H=2, ctx=[256], ext=[160], chunk=64, doc=64),                # documents, a whole tile of partial states
     dict(H=128, ctx=[200], ext=[130], chunk=128),                     # full head count
 ])
 def test_prefill_small(api, case):
@@ -203,8 +204,10 @@ def test_prefill_parts(api, parts):
     run_and_compare(api, wl, parts=parts)
 
 
-def test_prefill_bf16_out(api):
-    wl = W.make_workload("b", 2, [190], [70], chunk=128, seed=32)
+@pytest.mark.parametrize("ext", [70, 200], ids=["partial_tile", "whole_and_partial_tiles"])
+def test_prefill_bf16_out(api, ext):
+    """bf16 output: whole 128-row tiles go out by TMA, partial ones by thread stores."""
+    wl = W.make_workload("b", 2, [190], [ext], chunk=128, seed=32)
     run_and_compare(api, wl, out_dtype=torch.bfloat16)
 
 
