@@ -718,17 +718,16 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
     J.rope_offset = P.rope_offset;
     const int job = lo * p.num_heads + J.head;
     const int slot = g * 2 + (int)rank;   // trace slot
-    if (kCompute && tid == 32) {
-      // fresh barriers for this role (every barrier is idle here)
-      for (uint32_t i = 0; i < kNumBars; ++i) {
-        mbar_inval(bar_addr(sbase, i));
-        uint32_t cnt = 1;
-        // barriers the leader waits on count one arrival per warp of both CTAs
-        if (!producer && i == kBQReady) cnt = 2 * 4;
-        if (!producer && i >= kBPFull && i < kBPFull + kSBufs) cnt = 2 * 8;
-        if (producer && (i == kBAccEmpty || i == kBAccEmpty + 1)) cnt = 2 * 8;
-        mbar_init(bar_addr(sbase, i), cnt);
-      }
+    if (kCompute && tid >= 32 && tid < 32 + (int)kNumBars) {
+      // fresh barriers for this role (every barrier is idle here), one per lane of warp 1
+      const uint32_t i = (uint32_t)(tid - 32);
+      mbar_inval(bar_addr(sbase, i));
+      uint32_t cnt = 1;
+      // barriers the leader waits on count one arrival per warp of both CTAs
+      if (!producer && i == kBQReady) cnt = 2 * 4;
+      if (!producer && i >= kBPFull && i < kBPFull + kSBufs) cnt = 2 * 8;
+      if (producer && (i == kBAccEmpty || i == kBAccEmpty + 1)) cnt = 2 * 8;
+      mbar_init(bar_addr(sbase, i), cnt);
       fence_mbar_init();
     }
     cluster_sync_all();   // the peer's barriers exist before anything reaches them
