@@ -473,10 +473,11 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
 
 // =============================================================== producer pair
 // Passes pi, pi + n_prod, ... of 256 tokens; CTA r up-projects tokens
-// 128r..128r+127 of a pass (ring tile 2 pass + r).  Warps: 8 loads this CTA's
-// latent rows, 10 its half of the head's kv_b_proj columns (each waits for the
-// stage to be free), 9 MMA (leader), 0-7 conversion: warpgroup 0 the K_nope
-// columns, warpgroup 1 the V columns of the CTA's tile.
+// 128r..128r+127 of a pass (ring tile 2 pass + r).  Warps: 10 loads this CTA's
+// half of the head's kv_b_proj columns once for the role, 8 streams its latent
+// rows through the stages (waiting for each to be free), 9 MMA (leader), 0-7
+// conversion: warpgroup 0 the K_nope columns, warpgroup 1 the V columns of the
+// CTA's tile, stored from registers into the ring.
 template <bool kCompute>
 __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi, int role, uint32_t sbase,
                              uint32_t tmem, volatile Ctl* ctl, uint32_t rank) {
