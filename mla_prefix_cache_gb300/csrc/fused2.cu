@@ -679,27 +679,31 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
     const Piece& P = p.pieces[lo];
     const int n_pairs = (P.n_cons + 1) >> 1;
     const int local = g - P.group_begin;
-    // Roles of a piece in queue order: the producers of head 0, then per head
-    // h the producers of head h + 1 followed by the consumers of head h (the
-    // longest first).  A head's producers thus run one head ahead of its
-    // consumers, which find their first tiles ready, and still precede them
-    // in the queue.
-    const int per_head = P.n_prod + n_pairs;
+    // Roles of a piece in queue order: the producers of heads 0 .. L-1, then
+    // per head h the producers of head h + L followed by the consumers of head
+    // h (the longest first), L = p.prod_ahead.  A head's producers thus run L
+    // heads ahead of its consumers, which find their first tiles ready, and
+    // still precede them in the queue.
+    const int np = P.n_prod, la = min(p.prod_ahead, p.num_heads);
     int head, idx;
     bool producer;
-    if (local < P.n_prod) {
-      head = 0;
+    if (local < np * la) {
       producer = true;
-      idx = local;
+      head = local / np;
+      idx = local - head * np;
     } else {
-      const int hb = (local - P.n_prod) / per_head, r = local - P.n_prod - hb * per_head;
-      const bool ahead = hb + 1 < p.num_heads;
-      producer = ahead && r < P.n_prod;
-      head = producer ? hb + 1 : hb;
-      idx = ahead ? (producer ? r : r - P.n_prod) : r;
-      // a head's consumer pairs longest first (later query tiles see more
-      // keys), so the last roles of the queue are its shortest
-      if (!producer) idx = n_pairs - 1 - idx;
+      const int l = local - np * la, seg = np + n_pairs, n_full = p.num_heads - la;
+      if (l < n_full * seg) {
+        const int h = l / seg, r = l - h * seg;
+        producer = r < np;
+        head = producer ? h + la : h;
+        idx = producer ? r : n_pairs - 1 - (r - np);
+      } else {
+        const int l2 = l - n_full * seg;
+        producer = false;
+        head = n_full + l2 / n_pairs;
+        idx = n_pairs - 1 - (l2 - (l2 / n_pairs) * n_pairs);
+      }
     }
     Job J;
     J.req = P.req;

@@ -124,6 +124,7 @@ struct FusedParams {
   int n_groups;         // role groups in the queue (one per cluster dequeue)
   int pair;             // 1: clusters of two CTAs, consumer pairs share K/V loads by multicast
   int ring_depth;       // 128-token tiles per job ring: a power of two <= kRingDepth (slots are t & (depth - 1))
+  int prod_ahead;       // pair kernel: heads by which a job's producers precede its consumers in the queue
   unsigned long long* trace;   // optional, kTraceWords per role slot (group * 2 + cluster rank; see fused.cu)
   int trace_detail_role;       // role slot whose stages are timed one by one (-1: none)
   uint64_t rope_frac[kDr / 2];
