@@ -261,6 +261,20 @@ def test_prefill_shallow_ring_wraps(api, depth, monkeypatch):
     run_and_compare(api, wl)
 
 
+@pytest.mark.parametrize("knobs", [
+    {"MLA_PRODUCER_LOOKAHEAD": "1"},
+    {"MLA_PRODUCER_LOOKAHEAD": "5", "MLA_PRODUCERS": "2"},
+    {"MLA_PRODUCERS": "8", "MLA_RING_DEPTH": "8"},
+], ids=["lookahead1", "lookahead5_one_producer", "four_producers_shallow"])
+def test_prefill_queue_knobs(api, knobs, monkeypatch):
+    """The role queue's tuning knobs (producer count, lookahead, ring depth)
+    change the schedule, never the result."""
+    for k, v in knobs.items():
+        monkeypatch.setenv(k, v)
+    wl = W.make_workload("q", 6, [700, 300], [260, 130], chunk=256, seed=37)
+    run_and_compare(api, wl)
+
+
 @pytest.mark.parametrize("kernel", [
     {"MLA_CTA_PAIR": "0", "MLA_PAIR": "0"},   # single-CTA kernel
     {"MLA_CTA_PAIR": "0", "MLA_PAIR": "1"},   # single-CTA kernel, consumer pairs sharing K/V loads by multicast
