@@ -540,8 +540,11 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   if (pair) grid &= ~1;
   p.pair = pair;
   p.ring_depth = fw.ring_depth;
-  // producers two heads ahead of their consumers in the queue (measured best of 1-3)
-  p.prod_ahead = std::max(1, env_int("MLA_PRODUCER_LOOKAHEAD", 2));
+  // producers two heads ahead of their consumers in the queue (measured best
+  // of 1-3).  Capped at 8: on a ring shallower than a piece, producers that
+  // run ahead wait for their consumers, and fewer than the grid's pairs may
+  // wait at once.
+  p.prod_ahead = std::min(8, std::max(1, env_int("MLA_PRODUCER_LOOKAHEAD", 2)));
   const int width = pair ? 2 : 1;
   // error word + role queue (keep_err: a caller running several sub-calls keeps the error word)
   st = keep_err ? cuda_status(cudaMemsetAsync(err + 1, 0, 256 - 4, s)) : cuda_status(cudaMemsetAsync(err, 0, 256, s));
