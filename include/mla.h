@@ -37,7 +37,7 @@ typedef struct CUstream_st* mla_stream_t; /* identical to cudaStream_t */
 enum mla_status {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent lengths */
-  MLA_ERR_UNSUPPORTED = 2,   /* a shape or mode this build does not implement */
+  MLA_ERR_UNSUPPORTED = 2,   /* a shape or mode the library does not implement */
   MLA_ERR_BAD_BLOCK_ID = 3,  /* device saw a block-table entry outside [0, num_blocks) */
   MLA_ERR_CUDA = 4,          /* a CUDA runtime call failed (see mla_last_cuda_error) */
   MLA_ERR_WORKSPACE = 5,     /* workspace missing or smaller than required */

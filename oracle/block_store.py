@@ -10,7 +10,7 @@ a fresh block and count a dedup collision).
 
 Reading: the page's hash is xxh3, a fast non-cryptographic 64-bit hash; the
 scheme needs only some such hash, since byte verification makes sharing exact
-whatever the hash.  This build defines its own, from a published mixer so
+whatever the hash.  This library defines its own, from a published mixer so
 that the GPU can reduce a block in any order:
 
     h(block) = mix(n XOR sum_i mix(w_i + (i + 1) * GAMMA))      (mod 2^64)
