@@ -4,8 +4,13 @@ One step = one whole mla_prefill_ctx call (plan, fused gather + up-projection +
 attention kernel, merge of the KV splits) for one layer of one workload, with
 every input already resident in HBM.  Prints ONE JSON line (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config v3_8k]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config reloc_256k]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+The default workload is the largest one that fits a GPU: 16 relocated
+documents of 16K tokens (256K cached) and 4K new tokens, 128 heads.  The same
+line carries `target_128k`: the 128K-token FP8 cache with 4K new tokens, timed
+the same way, with its own fused-kernel roofline.
 
 Multi-GPU: the path is run as independent replicas (one process per GPU, the
 same workload each; no collective on the data path), so scaling is weak and
@@ -83,6 +88,84 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), with the architecture."""
+    import platform
+    name = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        fields = dict(line.split(":", 1) for line in out.splitlines() if ":" in line)
+        fields = {k.strip(): v.strip() for k, v in fields.items()}
+        name = fields.get("Model name", "")
+        if fields.get("Vendor ID") and fields["Vendor ID"] not in name:
+            name = f"{fields['Vendor ID']} {name}".strip()
+    except (OSError, subprocess.SubprocessError, ValueError):
+        name = ""
+    if not name:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        name = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return f"{name or 'unknown'} ({platform.machine()})"
+
+
+def executed_flops(wl) -> float:
+    """Tensor-core FLOPs the fused kernel issues for one call, as its planner
+    cuts the work: per (piece, head) every producer pass up-projects 256
+    tokens (M = 256 per CTA pair, the last pass's second half included), and
+    every consumer pair runs M = 256 (its two query tiles) x N = 128 score and
+    PV MMAs over as many 128-key tiles as the longer of its two tiles needs
+    (masked columns of the causal diagonal and of the piece edges included).
+    The algorithmic count (wl.algorithmic_flops) takes each unmasked pair once."""
+    H = wl.num_heads
+    max_keys = max(wl.chunk, 16384)
+    f = 0.0
+    for r in range(wl.num_reqs):
+        C, E = int(wl.ctx_lens[r]), int(wl.ext_lens[r])
+        if E == 0:
+            continue
+        if wl.segments is None:
+            ranges = [(c0, min(c0 + wl.chunk, C), 0) for c0 in range(0, C, wl.chunk)]
+        else:
+            ranges = []
+            for req, start, length, off in wl.segments.tolist():
+                if req == r:
+                    ranges += [(c0, min(c0 + wl.chunk, start + length), off)
+                               for c0 in range(start, start + length, wl.chunk)]
+        ranges.append((C, C + E, 0))
+        ranges.sort(key=lambda x: x[0])
+        pieces = []
+        for k0, k1, off in ranges:
+            if k1 <= k0:
+                continue
+            if pieces and pieces[-1][2] == off and pieces[-1][1] == k0 and pieces[-1][1] - pieces[-1][0] < max_keys:
+                pieces[-1][1] = k1
+            else:
+                pieces.append([k0, k1, off])
+        n_cons = (E + 127) // 128
+        for k0, k1, _ in pieces:
+            t0 = k0 & ~63
+            n_tiles = (k1 - t0 + 127) // 128
+            f += H * ((n_tiles + 1) // 2) * 256 * 2.0 * 512 * 256
+
+            def tiles(ci):
+                q0 = 128 * ci
+                nq = min(128, E - q0)
+                if nq <= 0:
+                    return 0
+                ke = min(k1, C + q0 + nq)
+                return 0 if ke <= k0 else (ke - t0 + 127) // 128
+
+            for k in range((n_cons + 1) // 2):
+                n = max(tiles(2 * k), tiles(2 * k + 1) if 2 * k + 1 < n_cons else 0)
+                f += H * n * 256 * 128 * 2.0 * (192 + 128)
+    return f
+
+
 def workload_config(wl, extra=None):
     c = {"workload": wl.name, "heads": wl.num_heads, "requests": wl.num_reqs,
          "context_tokens": int(wl.ctx_lens.sum()), "extend_tokens": int(wl.ext_lens.sum()),
@@ -117,7 +200,7 @@ def cpu_baseline(wl, budget_s=15.0):
         dt, f = oracle_sample(wl, n)
     else:
         dt, f = dt1, f1
-    return {"value": f / dt / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+    return {"value": f / dt / 1e12, "unit": UNIT, "cores": host_cores(), "cpu": cpu_model(), "kind": "oracle",
             "sample": f"{n} of {wl.num_heads} heads x all {wl.total_q} query rows x all keys of "
                       f"{wl.name} (numpy fp32, {dt:.1f} s)"}
 
@@ -145,7 +228,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded)", "config": workload_config(wl),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "cpu": cpu_model(), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -219,12 +303,12 @@ class ClockSampler:
 # ---------------------------------------------------------------- our arm
 
 def fused_kernel_name():
-    """The fused kernel mla_prefill_ctx launches (the library reads MLA_CTA_PAIR)."""
-    return "fused_prefill_kernel" if os.environ.get("MLA_CTA_PAIR", "1") == "0" else "fused2_prefill_kernel"
+    """The fused kernel mla_prefill_ctx launches."""
+    return "fused2_prefill_kernel"
 
 
 KERNEL_SOURCES = {
-    "fused": ("fused.cu", "fused2.cu", "fused_common.cuh", "ptx.cuh", "internal.h"),
+    "fused": ("fused2.cu", "fused_common.cuh", "ptx.cuh", "internal.h"),
     "absorbed": ("absorb.cu", "ptx.cuh", "internal.h"),
 }
 
@@ -473,49 +557,40 @@ def reuse_compare(dev, flush, reps=5, config="v3_8k", n_global=16, protected_fra
             "speedup": res["full"] / res["reuse"]}
 
 
-def run_ours(args):
+def time_prefill(wl, dev, flush, steps, warmup, world, absorbed=False, with_e2e=True):
+    """Times `steps` whole calls of the prefill entry point on `wl` (inputs
+    resident, L2 flushed before each step, outside its events), with the
+    fused (or latent attention) kernel's own events, the host time of each
+    call (planning and launches, from entry to return), the clocks sampled
+    during the timed region and, with_e2e, the end-to-end loop through the
+    public API with host buffers."""
     import torch
     import torch.distributed as dist
-
-    rank, world, local = dist_env()
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-
-    from mla_prefix_cache_gb300 import api, workload
-
-    wl = workload.by_name(args.config)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, args.cpu_budget_s)
+    from mla_prefix_cache_gb300 import api
 
     dw = api.DeviceWorkload(wl, dev)
     T_q, H = wl.total_q, wl.num_heads
     out = torch.empty((T_q, H, 128), dtype=torch.float32, device=dev)
     lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
-    absorbed = {"fused": False, "absorbed": True, "absorbed_fp8": "fp8"}[args.path]
     if absorbed:
         nbytes = api.absorbed_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk,
                                              fp8_scores=absorbed == "fp8")
     else:
         nbytes = api.prefill_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         dw.run(out=out, lse=lse, workspace=ws, absorbed=absorbed)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize(dev)
     if api.device_error(ws) != 0:
         raise RuntimeError("device error word set during warm-up")
 
-    K = args.steps
+    K = steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     clocks = ClockSampler(getattr(torch.cuda.get_device_properties(dev), "uuid", None))
@@ -527,12 +602,15 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
     n0 = api.launch_count()
+    host_us = []
     for k in range(K):
         flush.zero_()                       # L2 flush, outside the step events
-        gpu_delay()
+        torch.cuda.synchronize(dev)         # the step's events then also hold the call's host time
         api.set_kernel_events(*kev[k])
         ev[k][0].record(stream)
+        h0 = time.perf_counter()
         step()
+        host_us.append((time.perf_counter() - h0) * 1e6)
         ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
@@ -545,18 +623,14 @@ def run_ours(args):
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     if api.device_error(ws) != 0:
         raise RuntimeError("device error word set during the timed steps")
-
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
-    flops = wl.algorithmic_flops()
-    value = weak_scaling_value(flops, K, world, total_ms) / 1e12
-    tok_s = weak_scaling_value(T_q, K, world, total_ms)
+    res = {"step_ms": step_ms, "kern_ms": kern_ms, "launches": launches, "clocks": clk,
+           "host_us": statistics.median(host_us), "ws_bytes": int(nbytes), "e2e_ms": None}
 
     # ---- end to end through the public API: pinned host inputs in, result out.
     # A serving loop: step k's inputs go up (one copy stream) while step k-1
     # computes and step k-2's result comes down (another copy stream); two
     # device buffer sets alternate, and events order each buffer's reuse.
-    e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         import copy
         names = ("q", "q_pos", "kv_cache", "block_table", "kv_b_proj")
         host = {n: torch.empty(getattr(dw, n).shape, dtype=getattr(dw, n).dtype, pin_memory=True).copy_(getattr(dw, n))
@@ -568,12 +642,12 @@ def run_ours(args):
         lses = [lse, torch.empty_like(lse)]
         out_h = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
         lse_h = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
-        bi = sum(v.numel() * v.element_size() for v in host.values())
-        bo = out_h[0].numel() * out_h[0].element_size() + lse_h[0].numel() * lse_h[0].element_size()
+        res["h2d_bytes"] = sum(v.numel() * v.element_size() for v in host.values())
+        res["d2h_bytes"] = out_h[0].numel() * out_h[0].element_size() + lse_h[0].numel() * lse_h[0].element_size()
         up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev = lambda: torch.cuda.Event()
-        done_compute = [ev(), ev()]
-        done_down = [ev(), ev()]
+        mk = lambda: torch.cuda.Event()
+        done_compute = [mk(), mk()]
+        done_down = [mk(), mk()]
         for e_ in done_compute + done_down:
             e_.record(stream)
 
@@ -583,7 +657,7 @@ def run_ours(args):
             with torch.cuda.stream(up):
                 for n in names:
                     getattr(sets[b], n).copy_(host[n], non_blocking=True)
-            uploaded = ev()
+            uploaded = mk()
             uploaded.record(up)
             stream.wait_event(uploaded)
             stream.wait_event(done_down[b])           # step k-2's result has left this buffer
@@ -595,7 +669,7 @@ def run_ours(args):
                 lse_h[b].copy_(lses[b], non_blocking=True)
             done_down[b].record(down)
 
-        for k in range(max(1, args.warmup)):
+        for k in range(max(1, warmup)):
             e2e_step(k)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -610,9 +684,64 @@ def run_ours(args):
         stream.wait_event(done_down[K & 1])
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        res["e2e_ms"] = e0.elapsed_time(e1)
+        del sets, outs, lses, out_h, lse_h, host
+    del dw, out, lse, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def kernel_roofline(wl, res, peak, source, path="fused"):
+    """The timed kernel's roofline: algorithmic FLOPs (latent attention for the
+    absorbed paths) over its mean event time per call, against the measured
+    bf16 burst peak, with the executed FLOPs of the fused kernel beside it."""
+    k_ms = sum(res["kern_ms"]) / len(res["kern_ms"])
+    if path == "fused":
+        kflops, xflops = wl.algorithmic_flops(), executed_flops(wl)
+    else:
+        kflops, xflops = wl.absorbed_attention_flops(), None
+    achieved = kflops / (k_ms / 1e3) / 1e12
+    r = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+         "traffic": measured_traffic(wl.name, path), "kernel": "absorb_attn_kernel" if path != "fused" else fused_kernel_name(),
+         "peak_source": f"bf16_tflops (burst) of {source} peaks", "kernel_ms": k_ms,
+         "algorithmic_flops": kflops}
+    if xflops is not None:
+        r["executed_flops"] = xflops
+        r["executed_tflops"] = xflops / (k_ms / 1e3) / 1e12
+    return r
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from mla_prefix_cache_gb300 import workload
+
+    wl = workload.by_name(args.config)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_budget_s)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    absorbed = {"fused": False, "absorbed": True, "absorbed_fp8": "fp8"}[args.path]
+    res = time_prefill(wl, dev, flush, args.steps, args.warmup, world, absorbed, with_e2e=not args.no_e2e)
+    K = args.steps
+    total_ms = max_over_ranks(sum(res["step_ms"]), world, dev)
+    flops = wl.algorithmic_flops()
+    value = weak_scaling_value(flops, K, world, total_ms) / 1e12
+    tok_s = weak_scaling_value(wl.total_q, K, world, total_ms)
+    e2e = None
+    if res["e2e_ms"] is not None:
+        ems = max_over_ranks(res["e2e_ms"], world, dev)
         e2e = {"value": weak_scaling_value(flops, K, world, ems) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+               "h2d_bytes_per_step": int(res["h2d_bytes"]), "d2h_bytes_per_step": int(res["d2h_bytes"]),
                "ms_per_step": ems / K,
                "note": "pinned host inputs copied up and results copied down every step, on two copy streams "
                        "overlapping the neighbouring steps' compute (two device buffer sets)"}
@@ -624,6 +753,19 @@ def run_ours(args):
 
     peaks, source = load_peaks()
     peak = float(peaks["bf16_tflops"])
+    path = "fused" if not absorbed else args.path
+    roof = kernel_roofline(wl, res, peak, source, path)
+    # the 128K FP8 configuration, timed the same way (its own fused-kernel roofline)
+    target = None
+    if not args.no_target and world == 1 and not absorbed and args.config != "fp8_128k":
+        wt = workload.by_name("fp8_128k")
+        rt = time_prefill(wt, dev, flush, max(3, min(K, 10)), args.warmup, 1, False, with_e2e=False)
+        tms = sum(rt["step_ms"]) / len(rt["step_ms"])
+        target = {"workload": "fp8_128k", "value": wt.algorithmic_flops() / (tms / 1e3) / 1e12, "unit": UNIT,
+                  "ms_per_step": tms, "prefill_tok_s": wt.total_q / (tms / 1e3), "steps": len(rt["step_ms"]),
+                  "roofline": kernel_roofline(wt, rt, peak, source), "host_us_per_call": rt["host_us"],
+                  "clocks": rt["clocks"]}
+        del wt
     hbm = None if args.no_hbm_kernels else hbm_kernels(dev, flush, float(peaks["hbm_gbs"]))
     cmp_abs = cmp_abs8 = None
     if not args.no_absorbed and world == 1 and not absorbed:
@@ -634,32 +776,21 @@ def run_ours(args):
         cmp_reuse = reuse_compare(dev, flush)
     if not args.no_auto and world == 1 and not absorbed:
         cmp_auto = auto_compare(dev, flush)
-    k_ms = sum(kern_ms) / K
-    if absorbed:
-        kflops = wl.absorbed_attention_flops()
-        knote = "achieved = tensor-core FLOPs of the latent attention (2 (576 + 512) per visible query-key-head) / its event time"
-    else:
-        kflops = flops
-        knote = "achieved = algorithmic FLOPs of the step / fused-kernel event time"
-    achieved = kflops / (k_ms / 1e3) / 1e12
-    traffic = measured_traffic(wl.name, args.path)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded; shapes of the workload, random values)",
         "config": workload_config(wl, {"parallelism": f"replicas x{world}",
-                                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB memset outside the "
-                                             "step events, then a 1 ms GPU spin so the host has queued the "
-                                             "step before its start event)"}),
+                                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB memset and a "
+                                             "synchronize outside the step events; the events hold the "
+                                             "call's host planning and launches too)"}),
         "prefill_tok_s": tok_s,
         "frac_of_bf16_peak": value / world / peak,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "absorb_attn_kernel" if absorbed else fused_kernel_name(),
-                     "peak_source": f"bf16_tflops (burst) of {source} peaks",
-                     "kernel_ms": k_ms, "note": knote},
+        "roofline": roof,
+        "host_us_per_call": res["host_us"],
+        "workspace_bytes": res["ws_bytes"],
         "path": args.path,
-        "gpu_launches": int(launches),
+        "gpu_launches": int(res["launches"]),
         "hbm_kernels": hbm,
         "hbm_peak_source": f"hbm_gbs of {source} peaks",
         "absorbed": cmp_abs,
@@ -668,7 +799,8 @@ def run_ours(args):
         "auto": cmp_auto,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "clocks": clk,
+        "clocks": res["clocks"],
+        "target_128k": target,
     }
     print(json.dumps(line))
     if world > 1:
@@ -682,7 +814,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="v3_8k")
+    ap.add_argument("--config", default="reloc_256k")
     ap.add_argument("--path", choices=["fused", "absorbed", "absorbed_fp8"], default="fused",
                     help="entry point timed: mla_prefill_ctx (up-projected, fused), mla_prefill_ctx_absorbed, or "
                          "mla_prefill_ctx_absorbed_fp8 (FP8 caches)")
@@ -693,6 +825,8 @@ def main(argv=None):
     ap.add_argument("--no-reuse", action="store_true",
                     help="skip the head-split reuse comparison (16 Global heads, 10% protected rows on v3_8k)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-target", action="store_true",
+                    help="skip the second timed line on the 128K FP8 configuration (target_128k)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hbm-kernels", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)

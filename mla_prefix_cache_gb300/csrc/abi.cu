@@ -516,36 +516,26 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   rope_fracs((double)rope_theta, p.rope_frac);
 
-  // MLA_PAIR=1: consumer pairs in clusters of two CTAs share every K/V load
-  // (multicast), halving the consumers' L2 reads.  Off by default: on GB300 it
-  // measured no faster, the consumers being bound by their softmax chain, not
-  // by L2.  Single CTAs are also the fallback when no cluster of two fits.
-  int pair = env_int("MLA_PAIR", 0) != 0 ? 1 : 0;
-  // The CTA-pair kernel (fused2.cu, every role run by a cluster of two CTAs
-  // with M = 256 MMAs) by default; MLA_CTA_PAIR=0 selects the single-CTA
-  // kernel (fused.cu).
-  const bool v2 = env_int("MLA_CTA_PAIR", 1) != 0;
+  // The persistent CTA-pair kernel (fused2.cu): every role runs on a cluster
+  // of two CTAs with M = 256 MMAs.  MLA_FUSED_GRID caps the persistent grid (a
+  // tuning and measurement knob; the role queue is correct for any grid with
+  // more CTA pairs than producer pairs per job).
   int grid = 0;
-  int st = v2 ? cuda_status(fused2_grid_size(&grid)) : cuda_status(fused_grid_size(&grid, pair));
-  if (st != MLA_OK && !v2 && pair) {
-    cudaGetLastError();
-    pair = 0;
-    st = cuda_status(fused_grid_size(&grid, pair));
-  }
+  int st = cuda_status(fused2_grid_size(&grid));
   if (st != MLA_OK) return st;
-  if (v2) pair = 1;
-  // MLA_FUSED_GRID caps the persistent grid (a tuning and measurement knob; the
-  // role queue is correct for any grid with more CTAs than producers per job).
-  grid = std::min(grid, std::max(8, env_int("MLA_FUSED_GRID", grid)));
-  if (pair) grid &= ~1;
-  p.pair = pair;
+  grid = std::min(grid, std::max(8, env_int("MLA_FUSED_GRID", grid))) & ~1;
   p.ring_depth = fw.ring_depth;
   // producers two heads ahead of their consumers in the queue (measured best
   // of 1-3).  Capped at 8: on a ring shallower than a piece, producers that
   // run ahead wait for their consumers, and fewer than the grid's pairs may
   // wait at once.
   p.prod_ahead = std::min(8, std::max(1, env_int("MLA_PRODUCER_LOOKAHEAD", 2)));
-  const int width = pair ? 2 : 1;
+  // Every wait of the kernel gives up after 2 s (the error word then reads
+  // MLA_ERR_TIMEOUT).  Tests shorten it (MLA_WAIT_LIMIT_US, at least 1 ms) and
+  // withhold the producers of one job (MLA_TEST_WITHHOLD_JOB) to make a wait
+  // run out on purpose.
+  p.wait_limit_ns = (uint64_t)std::max(1000, std::min(2000000, env_int("MLA_WAIT_LIMIT_US", 2000000))) * 1000ull;
+  p.withhold_job = env_int("MLA_TEST_WITHHOLD_JOB", -1);
   // error word + role queue (keep_err: a caller running several sub-calls keeps the error word)
   st = keep_err ? cuda_status(cudaMemsetAsync(err + 1, 0, 256 - 4, s)) : cuda_status(cudaMemsetAsync(err, 0, 256, s));
   if (st != MLA_OK) return st;
@@ -562,9 +552,8 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     for (size_t i = 0; i < n; ++i) {
       Piece pc = fp.pieces[b0 + i];
       pc.group_begin = groups;
-      if (v2) pc.n_prod = std::max(1, (pc.n_prod + 1) / 2);   // producer roles of a pair: two CTAs each
-      groups += v2 ? H * (pc.n_prod + (pc.n_cons + 1) / 2)
-                   : H * ((pc.n_prod + width - 1) / width + (pc.n_cons + width - 1) / width);
+      pc.n_prod = std::max(1, (pc.n_prod + 1) / 2);   // producer roles of a pair: two CTAs each
+      groups += H * (pc.n_prod + (pc.n_cons + 1) / 2);
       p.pieces[i] = pc;
     }
     p.n_pieces = (int)n;
@@ -578,8 +567,7 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
                               ? env_int("MLA_TRACE_DETAIL_ROLE", -1) : -1;
     if (b0 > 0 && (st = cuda_status(cudaMemsetAsync(p.queue, 0, sizeof(uint32_t), s))) != MLA_OK) return st;
     if ((st = cuda_status(cudaMemsetAsync(p.flags, 0, fw.flags_bytes, s))) != MLA_OK) return st;
-    const cudaError_t le = v2 ? launch_fused2(p, std::min(grid, groups * 2), s)
-                              : launch_fused(p, std::min(grid, groups * width), s);
+    const cudaError_t le = launch_fused2(p, std::min(grid, groups * 2), s);
     if ((st = cuda_status(le)) != MLA_OK) return st;
   }
   if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_e, s))) != MLA_OK) return st;

@@ -1,16 +1,16 @@
 // Persistent fused MLA prefill kernel on CTA pairs (tcgen05 cta_group::2).
 //
-// What it computes is the same as fused.cu ("DeepSeek MLA — Prefix Cache 与
-// Chunked Prefill 深度解析", section 4.4, with the query relocation of
-// "RedKnot-MLA: Multi-Head Offline-Online Reuse for DeepSeek-V4 Long-Context
-// Serving", section 2): per job (request, head, key range with one RoPE
-// offset) the keys are up-projected once, K_nope | V = c_kv * kv_b_proj[:, head],
-// and every query of the request attends to them.
+// What it computes ("DeepSeek MLA — Prefix Cache 与 Chunked Prefill 深度解析",
+// sections 4.2-4.4, with the query relocation of "RedKnot-MLA: Multi-Head
+// Offline-Online Reuse for DeepSeek-V4 Long-Context Serving", section 2): per
+// job (request, head, key range with one RoPE offset) the keys are
+// up-projected once, K_nope | V = c_kv * kv_b_proj[:, head], and every query of
+// the request attends to them with an online softmax that yields (out, lse).
 //
-// How it differs from fused.cu.  Clusters of two CTAs run every role
-// together and the pair's tensor-core work is issued by the first CTA (the
-// leader) as M = 256 MMAs: rows 0..127 of A and of the accumulator live in the
-// leader, rows 128..255 in its peer, and each CTA holds half of B.  So each
+// A queue of roles feeds the persistent grid.  Clusters of two CTAs run every
+// role together and the pair's tensor-core work is issued by the first CTA
+// (the leader) as M = 256 MMAs: rows 0..127 of A and of the accumulator live in
+// the leader, rows 128..255 in its peer, and each CTA holds half of B.  So each
 // CTA stores half of every key tile, which frees shared memory for Q and TMEM
 // for a third score buffer:
 //   producer pair  up-projects passes of 256 tokens (128 per CTA); CTA r holds
@@ -740,7 +740,7 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
       trace_put(p, slot, 0, global_timer_ns());
       trace_put(p, slot, 2, ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)producer << 31) | (unsigned)job);
     }
-    if (!ctl->abort) {
+    if (!ctl->abort && !(producer && job == p.withhold_job)) {
       if (producer) run_producer<kCompute>(p, J, job, idx, slot, sbase, tmem, ctl, rank);
       else run_consumer<kCompute>(p, J, job, idx, slot, sbase, sgen, tmem, ctl, rank);
     }

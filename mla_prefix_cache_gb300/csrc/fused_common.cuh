@@ -1,6 +1,5 @@
-// Device helpers shared by the fused prefill kernels (single-CTA roles in
-// fused.cu, CTA-pair roles in fused2.cu): per-CTA control word, optional
-// tracing, bounded waits that record an error instead of hanging, and the
+// Device helpers of the fused prefill kernel (fused2.cu): per-CTA control
+// word, optional tracing, bounded waits that record an error instead of hanging, and the
 // ring and tile bookkeeping of a job.
 #pragma once
 
@@ -45,7 +44,7 @@ __device__ __forceinline__ bool aborted_global(const FusedParams& p) { return ld
 
 // Bounded mbarrier wait; on timeout records the error and returns false.
 __device__ __forceinline__ bool wait_bar(const FusedParams& p, uint32_t bar, uint32_t parity) {
-  if (mbar_wait(bar, parity)) return true;
+  if (mbar_wait(bar, parity, p.wait_limit_ns)) return true;
   atomicOr(p.err, kErrTimeout);
   return false;
 }
@@ -62,7 +61,7 @@ __device__ inline bool wait_flag_geq(const FusedParams& p, const uint32_t* flag,
   if (ld_acquire_gpu(flag) >= target) return true;
   const uint64_t t0 = global_timer_ns();
   while (ld_acquire_gpu(flag) < target) {
-    if (global_timer_ns() - t0 > kWaitLimitNs || aborted_global(p)) {
+    if (global_timer_ns() - t0 > p.wait_limit_ns || aborted_global(p)) {
       atomicOr(p.err, kErrTimeout);
       return false;
     }
@@ -119,7 +118,7 @@ __device__ inline int wait_ready_window(const FusedParams& p, int job, int t, in
       return k;
     }
     if (t0 == 0) t0 = global_timer_ns();
-    else if (global_timer_ns() - t0 > kWaitLimitNs || aborted_global(p)) {
+    else if (global_timer_ns() - t0 > p.wait_limit_ns || aborted_global(p)) {
       atomicOr(p.err, kErrTimeout);
       return -1;
     }

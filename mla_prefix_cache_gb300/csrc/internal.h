@@ -122,10 +122,12 @@ struct FusedParams {
   float scale_log2;
   int n_pieces;
   int n_groups;         // role groups in the queue (one per cluster dequeue)
-  int pair;             // 1: clusters of two CTAs, consumer pairs share K/V loads by multicast
   int ring_depth;       // 128-token tiles per job ring: a power of two <= kRingDepth (slots are t & (depth - 1))
-  int prod_ahead;       // pair kernel: heads by which a job's producers precede its consumers in the queue
-  unsigned long long* trace;   // optional, kTraceWords per role slot (group * 2 + cluster rank; see fused.cu)
+  int prod_ahead;       // heads by which a job's producers precede their consumers in the queue
+  uint64_t wait_limit_ns;   // bound of every wait of the kernel (a timeout sets kErrTimeout)
+  int withhold_job;     // test hook: this job's producer roles do nothing, so its consumers' waits run
+                        // out (-1: none)
+  unsigned long long* trace;   // optional, kTraceWords per role slot (group * 2 + cluster rank; see fused_common.cuh)
   int trace_detail_role;       // role slot whose stages are timed one by one (-1: none)
   uint64_t rope_frac[kDr / 2];
   Piece pieces[kMaxPieces];
@@ -135,13 +137,9 @@ constexpr int kTraceWords = 8;
 
 static_assert(sizeof(FusedParams) <= 32000, "kernel parameter space");
 
-cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t s);
-// Persistent grid: CTAs resident at once, a multiple of the cluster size
-// (2 when `pair`, else 1); 0 clusters -> error.
-cudaError_t fused_grid_size(int* grid, int pair);
-int fused_smem_bytes();
-// CTA-pair kernel (fused2.cu): pieces carry n_prod producer *pair* roles and
-// group_begin counts pair roles (n_prod + ceil(n_cons / 2) per head).
+// The persistent CTA-pair kernel (fused2.cu): pieces carry n_prod producer
+// *pair* roles and group_begin counts pair roles (n_prod + ceil(n_cons / 2)
+// per head).  The grid is the number of CTAs resident at once (a multiple of 2).
 cudaError_t launch_fused2(const FusedParams& p, int grid, cudaStream_t s);
 cudaError_t fused2_grid_size(int* grid);
 int fused2_smem_bytes();

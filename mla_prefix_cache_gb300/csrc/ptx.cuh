@@ -62,12 +62,13 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
       : "memory");
   return ok;
 }
-// Waits for the phase with the given parity to complete; false after the limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete; false after
+// `limit_ns` nanoseconds of %globaltimer.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }
@@ -457,21 +458,6 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t caddr, uint32_t v
 __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
                ::"r"(bar), "h"(mask) : "memory");
-}
-// TMA loads delivered to the same shared-memory offset (data and complete_tx on
-// the barrier at the same offset) in every CTA of `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* map, int x, int y, uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* map, int x, int y, int z, uint32_t bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask)
-      : "memory");
 }
 
 // ---------------------------------------------------------------- CTA pairs (cta_group::2)

@@ -275,19 +275,41 @@ def test_prefill_queue_knobs(api, knobs, monkeypatch):
     run_and_compare(api, wl)
 
 
-@pytest.mark.parametrize("kernel", [
-    {"MLA_CTA_PAIR": "0", "MLA_PAIR": "0"},   # single-CTA kernel
-    {"MLA_CTA_PAIR": "0", "MLA_PAIR": "1"},   # single-CTA kernel, consumer pairs sharing K/V loads by multicast
-], ids=["single", "multicast"])
+def test_prefill_wait_runs_out_and_reports_timeout(api, monkeypatch):
+    """Failure detection without a fault: the one job's producers are withheld
+    (a test hook of the library), so its consumers' bounded waits for ready
+    tiles run out after the shortened limit; the kernel records
+    MLA_ERR_TIMEOUT, frees its tensor memory and returns, and the next call on
+    the same device and workspace is correct.  One head, one piece: no K/V
+    load or MMA is ever issued, only the Q loads, which complete."""
+    wl = W.make_workload("to", 1, [300], [200], chunk=128, seed=38)
+    dw = api.DeviceWorkload(wl)
+    ws = torch.empty(api.prefill_workspace_size(wl.seq_lens, wl.cu_q, 1, None, wl.chunk), dtype=torch.uint8,
+                     device="cuda")
+    monkeypatch.setenv("MLA_WAIT_LIMIT_US", "2000")
+    monkeypatch.setenv("MLA_TEST_WITHHOLD_JOB", "0")
+    dw.run(workspace=ws)
+    torch.cuda.synchronize()
+    assert api.device_error(ws) == 6                 # MLA_ERR_TIMEOUT
+    assert api.device_error(ws) == 0                 # cleared by the read
+    monkeypatch.delenv("MLA_TEST_WITHHOLD_JOB")
+    monkeypatch.delenv("MLA_WAIT_LIMIT_US")
+    out, lse = dw.run(workspace=ws)
+    torch.cuda.synchronize()
+    assert api.device_error(ws) == 0
+    ref = O.mla_prefill(**O.workload_args(wl))
+    assert_close(out.cpu().numpy(), lse.cpu().numpy(), *ref, visible_keys(wl))
+
+
 @pytest.mark.parametrize("case", [
-    dict(H=4, ctx=[700], ext=[300], chunk=256, doc=None),     # 3 query tiles: one pair and one single consumer
+    dict(H=4, ctx=[700], ext=[300], chunk=256, doc=None),     # 3 query tiles: one full pair, one half pair
     dict(H=2, ctx=[256], ext=[200], chunk=64, doc=64),        # relocated documents, partial states + merge
 ], ids=["ragged", "docs"])
-def test_prefill_other_kernels(api, case, kernel, monkeypatch):
-    """The kernel variants other than the default (CTA-pair) one."""
-    for k, v in kernel.items():
-        monkeypatch.setenv(k, v)
-    wl = W.make_workload("pair", case["H"], case["ctx"], case["ext"], chunk=case["chunk"], seed=31,
+def test_prefill_small_grid(api, case, monkeypatch):
+    """Four CTA pairs take every role of the queue in turn: a role only ever
+    waits on roles dequeued before it, so any grid finishes."""
+    monkeypatch.setenv("MLA_FUSED_GRID", "8")
+    wl = W.make_workload("grid", case["H"], case["ctx"], case["ext"], chunk=case["chunk"], seed=31,
                          doc_len=case["doc"])
     run_and_compare(api, wl)
 
