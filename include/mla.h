@@ -87,8 +87,17 @@ typedef struct {
  *     R = rotation of interleaved pairs (2k, 2k+1) by theta^(-2k/64) per unit;
  *   every chunk and the extend stage give (out, lse = ln sum e^s); they are folded
  *   with merge_attn_states (see mla_merge_states).
- * Full K/V never reaches global memory: the up-projection runs on the tensor
- * cores inside the attention tile loop.
+ * The up-projection runs on the tensor cores inside the persistent attention
+ * kernel, once per (key, head).  Its bf16 K_nope/V tiles pass from producer to
+ * consumer CTAs through a few K/V ring lanes in the workspace (4 to 12 lanes
+ * of 128 slots of 128 keys, whatever the problem size, sized so that the
+ * lanes hold about 32 MiB of tiles); the jobs of the call take turns on the
+ * lanes, and the tiles are cached in L2 with an evict-last policy, so a lane's
+ * lines are rewritten while they sit in the 126 MB L2: the up-projected K/V
+ * is not written back to HBM (measured on GB300 with 128 heads: the fused
+ * kernel writes 100 MB per call on 8K + 2K tokens, where the output alone is
+ * 134 MB, and 5.5 GB on 256K + 4K tokens, where the partial states of the 17
+ * pieces are 4.6 GB).
  *
  * Arguments
  *  q            device bf16 [T_q, H, 192]: [q_nope 0..127 | q_rope 128..191],
@@ -114,17 +123,15 @@ typedef struct {
  *  lse          device fp32 [T_q, H], natural log, softmax scale included;
  *               -inf for a row with no visible key (its out row is 0).
  *  workspace    device, 256-B aligned; mla_prefill_workspace_size(...) bytes
- *               lets the whole call run as one kernel launch with K/V rings
- *               of 128 up-projected tiles (8 MB) per (piece, head): for
- *               long contexts this is several GB, from an HBM of 280 GB.  A
- *               smaller workspace also works as long as it holds the
- *               gathered rows, the partial states and rings of at least 4
- *               tiles for one piece (one request's key range of at most
- *               max(chunk, 16384) tokens, for all heads): the call then uses
- *               shallower rings and runs its pieces in several launches,
- *               more slowly.  The gathered rows are every block of the
- *               requests, copied in logical order as bf16 (1152 B per
- *               token; FP8 rows dequantised).  Holds the device error word;
+ *               lets the whole call run as one kernel launch at full speed:
+ *               the K/V ring lanes (32 to 96 MiB), per-job ring flags, every block
+ *               of the requests gathered in logical order as bf16 (1152 B per
+ *               token; FP8 rows dequantised) and fp32 partial states
+ *               (516 B per query row, head and piece of a request cut into
+ *               several pieces: one per relocated segment and per 16384 keys).
+ *               Any size down to mla_prefill_min_workspace_size(...) also
+ *               works, with shallower and fewer lanes and, at the bottom, one
+ *               piece per launch: more slowly.  Holds the device error word;
  *               must not be shared by calls that may overlap on the GPU.
  *  H            num_heads in [1, 128].
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (H > 128, chunk not a
@@ -134,6 +141,13 @@ typedef struct {
 size_t mla_prefill_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q,
                                   int num_heads, const mla_segment* segments, int num_segments,
                                   int chunk, int parts);
+
+/* The smallest workspace mla_prefill_ctx accepts for these arguments (two
+ * ring lanes of 4 tiles, one piece per launch); 0 when the planner rejects
+ * the arguments. */
+size_t mla_prefill_min_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q,
+                                      int num_heads, const mla_segment* segments, int num_segments,
+                                      int chunk, int parts);
 
 int mla_prefill_ctx(const void* q, const int32_t* q_pos,
                     const void* kv_cache, int kv_dtype, float kv_scale, int num_blocks,
@@ -161,10 +175,17 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos,
  * other device-allocating routine.
  *
  *  - The first call on a device looks up that device's address of the array
- *    (cudaGetSymbolAddress) with the device current; make that first call
- *    before any stream capture begins.
- *  - A problem that does not fit the array even one piece per launch returns
- *    MLA_ERR_TOO_LARGE before anything is launched.
+ *    (cudaGetSymbolAddress) with the device current and keeps it for the
+ *    life of the process; make that first call before any stream capture
+ *    begins.
+ *  - Arguments are validated as by mla_prefill_ctx first (a call with no
+ *    query rows returns MLA_OK without launching).  A problem whose
+ *    mla_prefill_min_workspace_size exceeds the array returns
+ *    MLA_ERR_TOO_LARGE before anything is launched.  That size is about
+ *    0.6 MB of ring lanes plus 1152 B per cached token of the requests and,
+ *    for a request cut into several pieces (more than about 16K keys, or
+ *    relocated segments), 516 B per query row, head and piece: at 128 heads
+ *    one request of up to 16K tokens fits, and little beyond that.
  *  - Every call shares the one array.  Each call re-zeroes the parts that must
  *    start at zero, but calls that may overlap on the GPU (different streams
  *    without ordering between them) race on it: order them.

@@ -54,6 +54,7 @@ segp = ctypes.POINTER(Segment)
 # name -> (restype, argtypes); must match include/mla.h
 SIGNATURES = {
     "mla_prefill_workspace_size": (c_size_t, [c_int, i32p, i32p, c_int, segp, c_int, c_int, c_int]),
+    "mla_prefill_min_workspace_size": (c_size_t, [c_int, i32p, i32p, c_int, segp, c_int, c_int, c_int]),
     "mla_prefill_ctx": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_float, c_int, c_void_p, c_int,
                                 i32p, i32p, c_int, c_int, segp, c_int, c_int, c_void_p, c_float, c_float,
                                 c_int, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),

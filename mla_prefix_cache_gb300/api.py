@@ -70,6 +70,19 @@ def prefill_workspace_size(seq_lens, cu_q, num_heads: int, segments=None, chunk:
     return int(n)
 
 
+def prefill_min_workspace_size(seq_lens, cu_q, num_heads: int, segments=None, chunk: int = 4096,
+                               parts: int = PART_ALL) -> int:
+    """The smallest workspace mla_prefill_ctx runs in (shallow K/V rings, one
+    piece per launch: slower)."""
+    sl, _k1 = _lib.i32_host(seq_lens)
+    cq, _k2 = _lib.i32_host(cu_q)
+    sp, ns, _k3 = _lib.segments_host(segments)
+    n = _lib.load().mla_prefill_min_workspace_size(len(_k1), sl, cq, int(num_heads), sp, ns, int(chunk), int(parts))
+    if n == 0:
+        raise MLAError("mla_prefill_min_workspace_size", _lib.MLA_ERR_INVALID_ARG)
+    return int(n)
+
+
 def absorbed_workspace_size(seq_lens, cu_q, num_heads: int, segments=None, chunk: int = 4096,
                             parts: int = PART_ALL, fp8_scores: bool = False) -> int:
     sl, _k1 = _lib.i32_host(seq_lens)

@@ -244,19 +244,23 @@ struct FusedWs {
          out_off = 0, total = 0;
   int pieces_per_launch = 0;
   int ring_depth = 0;
+  int ring_lanes = 0;
 };
 
-// Workspace of the fused path when `ppl` pieces run per launch with rings of
-// `depth` tiles: header (error word, role queue), per-job ring flags, per-job
-// K/V rings, the gathered rows, partial states.
-static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads, int ppl, int depth) {
+// Workspace of the fused path when `ppl` pieces run per launch with `lanes`
+// K/V ring lanes of `depth` tiles: header (error word, role queue), per-job
+// ring flags, the ring lanes (jobs take turns on them), the gathered rows,
+// partial states.
+static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads, int ppl, int depth, int lanes) {
   FusedWs w;
+  const size_t jobs = (size_t)ppl * num_heads;
+  lanes = (int)std::min<size_t>((size_t)lanes, jobs);   // more lanes than jobs would stay unused
   w.pieces_per_launch = ppl;
   w.ring_depth = depth;
-  const size_t jobs = (size_t)ppl * num_heads;
-  w.flags_bytes = jobs * 2 * (size_t)depth * sizeof(uint32_t);
+  w.ring_lanes = lanes;
+  w.flags_bytes = jobs * 2 * (size_t)depth * sizeof(uint32_t);   // ready and consumed per ring slot
   w.ring_off = up256(w.flags_off + w.flags_bytes);
-  const size_t ring_bytes = jobs * (size_t)depth * 128 * 256 * sizeof(uint16_t);
+  const size_t ring_bytes = (size_t)lanes * (size_t)depth * 128 * 256 * sizeof(uint16_t);
   const size_t rows = (size_t)fp.max_slots * (size_t)fp.total_q * (size_t)num_heads;
   w.gath_off = up256(w.ring_off + ring_bytes);
   const size_t gath_bytes = (size_t)fp.gather_blocks * kBlock * kRowBytesBf16;
@@ -266,10 +270,8 @@ static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads, int ppl, int 
   return w;
 }
 
-// Preferred layout: the deepest rings (a head's consumers start over a spread
-// of tiles; a shallow ring makes the earliest wait for the latest), every
-// piece in one launch, up to kMaxPieces and 24 GiB of rings.
-// MLA_RING_DEPTH lowers the deepest ring (a tuning knob; a power of two >= 4).
+// Deepest ring lane: 128 tiles (16384 keys, a whole piece of the default
+// plan).  MLA_RING_DEPTH lowers it (a tuning knob; a power of two >= 4).
 static int max_ring_depth() {
   int d = kRingDepth;
   const int cap = env_int("MLA_RING_DEPTH", kRingDepth);
@@ -277,23 +279,49 @@ static int max_ring_depth() {
   return d;
 }
 
-static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads) {
-  const int depth = max_ring_depth();
-  const size_t per_piece = (size_t)num_heads * depth * 128 * 256 * sizeof(uint16_t);
-  const int cap = (int)std::max<size_t>(1, ((size_t)24 << 30) / per_piece);
-  const int ppl = std::max(1, std::min({(int)fp.pieces.size(), kMaxPieces, cap}));
-  return fused_ws_layout(fp, num_heads, ppl, depth);
+// Heads by which a job's producers precede its consumers in the queue
+// (measured best of 1-3); MLA_PRODUCER_LOOKAHEAD, at most 8.
+static int producer_lookahead() { return std::min(8, std::max(1, env_int("MLA_PRODUCER_LOOKAHEAD", 2))); }
+
+// Ring lanes: the up-projected tiles of the lanes stay in L2 while the lanes
+// hold about 32 MiB of tiles (measured on GB300: 4 lanes of 16384-key pieces
+// keep the fused kernel's DRAM traffic at its compulsory bytes, 6 lanes of
+// them write most tiles back), so the count is 32 MiB over the longest
+// piece's tiles, within [lookahead + 2, 12].  A producer waits for the lane's
+// previous job, so lanes > lookahead is needed (its consumers then precede
+// the producer in the queue), and one more lane keeps those waits short.
+// MLA_RING_LANES sets the count (at least lookahead + 1).
+static int ring_lanes_cfg(const FusedPlan& fp, int depth) {
+  const int ahead = producer_lookahead();
+  const int forced = env_int("MLA_RING_LANES", 0);
+  if (forced > 0) return std::max(ahead + 1, forced);
+  int max_tiles = 1;
+  for (const Piece& pc : fp.pieces)
+    max_tiles = std::max(max_tiles, (pc.k_end - (pc.k_begin & ~(kBlock - 1)) + 127) / 128);
+  const size_t tile_bytes = (size_t)128 * 256 * sizeof(uint16_t);
+  const int fit = (int)(((size_t)32 << 20) / (tile_bytes * (size_t)std::min(max_tiles, depth)));
+  return std::max(ahead + 2, std::min(kRingLanes, fit));
 }
 
-// Layout for a workspace of `bytes`: the preferred one when it fits, else the
-// most pieces per launch with the deepest ring that fits; pieces_per_launch 0
-// when not even one piece with a 4-tile ring fits.
+static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads) {
+  const int ppl = std::max(1, std::min((int)fp.pieces.size(), kMaxPieces));
+  const int depth = max_ring_depth();
+  return fused_ws_layout(fp, num_heads, ppl, depth, ring_lanes_cfg(fp, depth));
+}
+
+// Layout for a workspace of `bytes`: the preferred one when it fits, else
+// shallower lanes, then fewer lanes (down to 2, the producers then running
+// one head ahead), then fewer pieces per launch; pieces_per_launch 0 when not
+// even one piece with two 4-tile lanes fits.
 static FusedWs fused_ws_fitting(const FusedPlan& fp, int num_heads, size_t bytes) {
-  const int top = fused_ws_layout(fp, num_heads).pieces_per_launch;
-  for (int depth = max_ring_depth(); depth >= 4; depth /= 2) {
-    int hi = top;
-    while (hi >= 1 && fused_ws_layout(fp, num_heads, hi, depth).total > bytes) hi = hi > 8 ? hi - hi / 8 : hi - 1;
-    if (hi >= 1) return fused_ws_layout(fp, num_heads, hi, depth);
+  const FusedWs pref = fused_ws_layout(fp, num_heads);
+  if (pref.total <= bytes) return pref;
+  for (int depth = pref.ring_depth; depth >= 4; depth /= 2) {
+    for (int lanes = pref.ring_lanes; lanes >= 2; --lanes) {
+      int hi = pref.pieces_per_launch;
+      while (hi >= 1 && fused_ws_layout(fp, num_heads, hi, depth, lanes).total > bytes) hi = hi > 8 ? hi - hi / 8 : hi - 1;
+      if (hi >= 1) return fused_ws_layout(fp, num_heads, hi, depth, lanes);
+    }
   }
   FusedWs none;
   none.pieces_per_launch = 0;
@@ -459,9 +487,8 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     ok &= encode_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_b_proj, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   {
-    // ring: per job and slot four contiguous [128 x 64] blocks K_nope lo, K_nope hi, V lo, V hi
-    const uint64_t jobs = (uint64_t)std::max(fw.pieces_per_launch, 1) * H;
-    const uint64_t d[3] = {64, 128, jobs * (uint64_t)fw.ring_depth * 4};
+    // ring lanes: per lane and slot four contiguous [128 x 64] blocks K_nope lo, K_nope hi, V lo, V hi
+    const uint64_t d[3] = {64, 128, (uint64_t)fw.ring_lanes * (uint64_t)fw.ring_depth * 4};
     const uint64_t st[2] = {128, 128 * 128};
     const uint32_t b[3] = {64, 128, 2};
     ok &= encode_map(&p.tm_ring, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + fw.ring_off, d, st, b,
@@ -525,17 +552,20 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   if (st != MLA_OK) return st;
   grid = std::min(grid, std::max(8, env_int("MLA_FUSED_GRID", grid))) & ~1;
   p.ring_depth = fw.ring_depth;
-  // producers two heads ahead of their consumers in the queue (measured best
-  // of 1-3).  Capped at 8: on a ring shallower than a piece, producers that
-  // run ahead wait for their consumers, and fewer than the grid's pairs may
-  // wait at once.
-  p.prod_ahead = std::min(8, std::max(1, env_int("MLA_PRODUCER_LOOKAHEAD", 2)));
+  p.ring_lanes = fw.ring_lanes;
+  // Producers run prod_ahead heads ahead of their consumers in the queue
+  // (capped at 8: on a ring shallower than a piece, producers that run ahead
+  // wait for their consumers, and fewer than the grid's pairs may wait at
+  // once), and fewer than the ring lanes: a producer waits for the lane's
+  // previous job, whose consumers must precede it in the queue.
+  p.prod_ahead = std::max(1, std::min(producer_lookahead(), fw.ring_lanes - 1));
   // Every wait of the kernel gives up after 2 s (the error word then reads
   // MLA_ERR_TIMEOUT).  Tests shorten it (MLA_WAIT_LIMIT_US, at least 1 ms) and
   // withhold the producers of one job (MLA_TEST_WITHHOLD_JOB) to make a wait
   // run out on purpose.
   p.wait_limit_ns = (uint64_t)std::max(1000, std::min(2000000, env_int("MLA_WAIT_LIMIT_US", 2000000))) * 1000ull;
   p.withhold_job = env_int("MLA_TEST_WITHHOLD_JOB", -1);
+  p.l2_hints = env_int("MLA_L2_HINTS", 1) != 0 ? 1 : 0;
   // error word + role queue (keep_err: a caller running several sub-calls keeps the error word)
   st = keep_err ? cuda_status(cudaMemsetAsync(err + 1, 0, 256 - 4, s)) : cuda_status(cudaMemsetAsync(err, 0, 256, s));
   if (st != MLA_OK) return st;
@@ -1135,6 +1165,16 @@ size_t mla_prefill_workspace_size(int num_reqs, const int32_t* seq_lens, const i
   return fused_ws_layout(fp, num_heads).total;
 }
 
+size_t mla_prefill_min_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,
+                                      const mla_segment* segments, int num_segments, int chunk, int parts) {
+  Plan plan;
+  if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
+    return 0;
+  FusedPlan fp;
+  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fp);
+  return fused_ws_layout(fp, num_heads, 1, 4, 2).total;
+}
+
 int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
                     int num_blocks, const int32_t* block_table, int max_blocks_per_req, const int32_t* seq_lens,
                     const int32_t* cu_q, int num_reqs, int num_heads, const mla_segment* segments,
@@ -1160,27 +1200,21 @@ int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos, const void* kv_
                             const mla_segment* segments, int num_segments, int chunk, const void* kv_b_proj,
                             float softmax_scale, float rope_theta, int parts, void* out, int out_dtype, float* lse,
                             mla_stream_t stream) {
-  const size_t need = mla_prefill_workspace_size(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk,
-                                                 parts);
-  if (need == 0) {  // the planner rejected the arguments: report why
-    Plan plan;
-    const int st = build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan);
-    return st != MLA_OK ? st : MLA_ERR_INVALID_ARG;
-  }
-  // the smallest workspace the call can run in: one piece per launch
+  // the same validation as mla_prefill_ctx first, then one plan for the size
+  // check and the launches
   Plan plan;
-  if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
-    return MLA_ERR_INVALID_ARG;
   FusedPlan fplan;
-  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fplan);
-  if (fused_ws_fitting(fplan, num_heads, MLA_NOALLOC_SCRATCH_BYTES).pieces_per_launch < 1) return MLA_ERR_TOO_LARGE;
+  int st = prefill_plans(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req, seq_lens,
+                         cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj, softmax_scale,
+                         rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
+  if (st != MLA_OK || plan.total_q == 0) return st;
+  const FusedWs fw = fused_ws_fitting(fplan, num_heads, MLA_NOALLOC_SCRATCH_BYTES);
+  if (fw.pieces_per_launch < 1) return MLA_ERR_TOO_LARGE;
   void* scratch = nullptr;
-  const int st = noalloc_scratch(&scratch);
-  if (st != MLA_OK) return st;
-  return mla_prefill_ctx(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
-                         seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
-                         softmax_scale, rope_theta, parts, out, out_dtype, lse, scratch, MLA_NOALLOC_SCRATCH_BYTES,
-                         stream);
+  if ((st = noalloc_scratch(&scratch)) != MLA_OK) return st;
+  return prefill_fused(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req, num_heads,
+                       kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, scratch, fplan, fw,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t mla_prefill_absorbed_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,

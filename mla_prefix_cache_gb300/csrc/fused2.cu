@@ -93,6 +93,17 @@ constexpr uint32_t kIdescUp = idesc_bf16(256, 256, false, true);
 
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 256
 
+// L2 policies: ring tiles are kept (evict_last: written, read by every
+// consumer pair of the job, rewritten by the lane's next job), what streams
+// through once (q, kv_b_proj columns, out and partial states) goes first.
+// With p.l2_hints = 0 both are evict_normal.
+__device__ __forceinline__ uint64_t policy_keep(const FusedParams& p) {
+  return p.l2_hints ? l2_policy_evict_last() : l2_policy_evict_normal();
+}
+__device__ __forceinline__ uint64_t policy_stream(const FusedParams& p) {
+  return p.l2_hints ? l2_policy_evict_first() : l2_policy_evict_normal();
+}
+
 __device__ __forceinline__ uint32_t bar_addr(uint32_t sbase, uint32_t i) { return sbase + kBarBase + 8u * i; }
 
 // Key tiles of consumer pair k (query tiles 2k and 2k+1; the second may be past
@@ -136,10 +147,11 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
         const uint32_t qb = bar_addr(sbase, kBQLand);
         mbar_arrive_expect_tx(qb, 3 * kAtomQ);
         for (int part = 0; part < 3; ++part)
-          tma_load_3d(sbase + kQBase + part * kAtomQ, &p.tm_q, 64 * part, J.head, grow0, qb);
+          tma_load_3d_hint(sbase + kQBase + part * kAtomQ, &p.tm_q, 64 * part, J.head, grow0, qb, policy_stream(p));
       }
       const int ns = is_k ? kKStages : kVStages;
       const uint32_t full0 = is_k ? kBKFull : kBVFull, empty0 = is_k ? kBKEmpty : kBVEmpty;
+      const uint64_t pol_ring = policy_keep(p);
       TraceAcc tr;
       // A tile's ring slot is released once the pair's MMAs have read its
       // stage, before the next tile is waited for, in batches behind one fence
@@ -168,18 +180,18 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
         }
         const uint32_t full = bar_addr(sbase, full0 + s);
         const uint32_t full_leader = mapa_shared(full, 0u);
-        const int zb = (job * p.ring_depth + ring_slot(p, j)) * 4;   // first ring block of the tile
+        const int zb = ring_block(p, job, ring_slot(p, j));   // first ring block of the tile
         if (is_k) {
           const uint32_t st = sbase + kKBase + s * kKStageBytes;
           if (leader) mbar_arrive_expect_tx(full, 2 * kKStageBytes);     // both halves land on the leader's count
           const int kt0 = J.t0 + 128 * j;
-          tma_load_3d_pair(st, &p.tm_ring64, 0, 64 * (int)rank, zb, full_leader);                    // K_nope lo | hi
+          tma_load_3d_pair_hint(st, &p.tm_ring64, 0, 64 * (int)rank, zb, full_leader, pol_ring);       // K_nope lo | hi
           tma_load_2d_pair(st + 2 * kAtom64, &p.tm_kr, kDc, block_row(J, (kt0 >> 6) + (int)rank), full_leader);
           trace_stage(p, role, j, 0);
         } else {
           const uint32_t st = sbase + kVBase + s * kVStageBytes;
           if (leader) mbar_arrive_expect_tx(full, 2 * kVStageBytes);
-          tma_load_3d_pair(st, &p.tm_ring1, 0, 0, zb + 2 + (int)rank, full_leader);                  // V columns
+          tma_load_3d_pair_hint(st, &p.tm_ring1, 0, 0, zb + 2 + (int)rank, full_leader, pol_ring);     // V columns
           trace_stage(p, role, j, 1);
         }
       }
@@ -421,12 +433,13 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       named_bar_sync(2 + w, 128);
       if (r == 0) {
         const int row0 = J.slot < 0 ? grow0 : J.slot * p.slot_stride_rows + grow0;
+        const uint64_t pol = policy_stream(p);
         if (ob) {
-          tma_store_3d(&p.tm_out, stg, 64 * w, J.head, row0);
+          tma_store_3d_hint(&p.tm_out, stg, 64 * w, J.head, row0, pol);
         } else {
           const CUtensorMap* m = J.slot < 0 ? &p.tm_out : &p.tm_part;
-          tma_store_3d(m, stg, 64 * w, J.head, row0);
-          tma_store_3d(m, stg + kAtomQ, 64 * w + 32, J.head, row0);
+          tma_store_3d_hint(m, stg, 64 * w, J.head, row0, pol);
+          tma_store_3d_hint(m, stg + kAtomQ, 64 * w + 32, J.head, row0, pol);
         }
         bulk_commit();
         bulk_wait_read0();   // the stages are free again before the role ends
@@ -498,15 +511,51 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       const uint32_t full_leader = mapa_shared(full, 0u);
       if (leader) mbar_arrive_expect_tx(full, 2 * 8 * kAtomQ);
       const int blk = rank == 0 ? 2 * h : (H * kDnope + h * kDv) / 64;
+      const uint64_t pol = policy_stream(p);
       for (int kx = 0; kx < kDc / 64; ++kx)
-        tma_load_3d_pair(sbase + kPWBase + kx * kAtomQ, &p.tm_w, 0, 64 * kx, blk, full_leader);
+        tma_load_3d_pair_hint(sbase + kPWBase + kx * kAtomQ, &p.tm_w, 0, 64 * kx, blk, full_leader, pol);
       trace_stage(p, role, 0, 7);
+      // This CTA writes tile t = 2 pass + rank of each pass into ring slot
+      // t mod depth of lane job mod ring_lanes.  On the first lap the lane's
+      // previous job, job - ring_lanes, must be done with that slot: its last
+      // tile there published and read by every consumer that needs it.  Its
+      // roles precede this one in the queue (ring_lanes > prod_ahead) and never
+      // wait on it, so the wait ends.  This thread checks pass by pass and
+      // releases lane_ok to the row loader, which loads a pass's rows only
+      // after its check; the pass's stores follow through the loads, the MMAs
+      // and their barriers.  The checks stay off the loads' and MMAs' path.
+      const int prev = job - p.ring_lanes;
+      if (prev < 0) return;
+      const Job Jp = make_job(p, prev / p.num_heads, prev % p.num_heads);
+      int* ok = const_cast<int*>(&ctl->lane_ok);
+      TraceAcc tr_lane;
+      for (int n = 0; n < my_passes; ++n) {
+        const int t = 2 * (pi + n * J.n_prod) + (int)rank;
+        if (t < J.n_tiles && t < p.ring_depth && t < Jp.n_tiles) {
+          const int tl = t + ((Jp.n_tiles - 1 - t) / p.ring_depth) * p.ring_depth;   // its last tile in slot t
+          const uint64_t w0 = tr_lane.begin(p);
+          if (!(wait_flag_geq(p, ready_flag(p, prev, t), (uint32_t)tl + 1) &&
+                wait_flag_geq(p, consumed_flag(p, prev, t), 2u * (uint32_t)consumers_needing_tile(Jp, tl)))) {
+            ctl->abort = 1;
+            return;
+          }
+          tr_lane.end(p, w0);
+        }
+        st_release_cta_s32(ok, n + 1);
+      }
+      trace_put(p, role, 6, tr_lane.t);
     } else if (warp == 8) {
       if (lane != 0) return;
+      const bool lane_wait = job >= p.ring_lanes;
       int g = 0;
       for (int n = 0; n < my_passes; ++n) {
         const int pass = pi + n * J.n_prod;
         const int row0 = block_row(J, (J.t0 >> 6) + 4 * pass) + 128 * (int)rank;
+        // the ring slot of this pass's tile is free (checked by warp 10)
+        if (lane_wait && !wait_shared_geq(p, ctl, const_cast<const int*>(&ctl->lane_ok), n + 1)) {
+          ctl->abort = 1;
+          return;
+        }
         for (int kx = 0; kx < kDc / 64; ++kx, ++g) {
           const int s = g % kPStages;
           if (g >= kPStages && !wait_bar(p, bar_addr(sbase, kBProdEmpty + s), ((g / kPStages) - 1) & 1)) {
@@ -574,6 +623,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
     // delays the next accumulator.
     bool pend = false;        // the previous pass stored a tile not yet published
     int pend_t = 0, pend_slot = 0;
+    const uint64_t pol_ring = policy_keep(p);
     for (int n = 0; n < my_passes; ++n) {
       const int pass = pi + n * J.n_prod;
       const int b = n & 1;
@@ -626,7 +676,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       if (live_tile) {
         // ring block [128 tokens x 64 columns]: each warp store covers four
         // whole 128-byte rows
-        uint16_t* dst = p.ring + ((size_t)(job * p.ring_depth + slot) * 4 + 2 * wg) * (128 * 64);
+        uint16_t* dst = p.ring + ((size_t)ring_block(p, job, slot) + 2 * wg) * (128 * 64);
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
           uint4 c[8];
@@ -636,7 +686,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
           transpose8x16B(c, lane);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            *reinterpret_cast<uint4*>(dst + (size_t)hb * (128 * 64) + (size_t)(st_row + e) * 64 + st_chunk * 8) = c[e];
+            st_global_v4_hint(dst + (size_t)hb * (128 * 64) + (size_t)(st_row + e) * 64 + st_chunk * 8, c[e], pol_ring);
         }
         if (tid == 0) trace_stage(p, role, n, 3);
       }
@@ -705,22 +755,7 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
         idx = n_pairs - 1 - (l2 - (l2 / n_pairs) * n_pairs);
       }
     }
-    Job J;
-    J.req = P.req;
-    J.head = head;
-    J.q_begin = P.q_begin;
-    J.q_count = P.q_count;
-    J.q_tok0 = P.q_tok0;
-    J.q_tok = p.q_tok;
-    J.k_begin = P.k_begin;
-    J.k_end = P.k_end;
-    J.t0 = P.k_begin & ~(kBlock - 1);
-    J.n_tiles = (P.k_end - J.t0 + 127) >> 7;
-    J.n_cons = P.n_cons;
-    J.n_prod = P.n_prod;
-    J.slot = P.slot;
-    J.row_block0 = P.row_block0;
-    J.rope_offset = P.rope_offset;
+    const Job J = make_job(p, lo, head);
     const int job = lo * p.num_heads + J.head;
     const int slot = g * 2 + (int)rank;   // trace slot
     if (kCompute && tid >= 32 && tid < 32 + (int)kNumBars) {
@@ -735,6 +770,7 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
       mbar_init(bar_addr(sbase, i), cnt);
       fence_mbar_init();
     }
+    if (kCompute && tid == 0) ctl->lane_ok = 0;
     cluster_sync_all();   // the peer's barriers exist before anything reaches them
     if (kCompute && p.trace && tid == 0) {
       trace_put(p, slot, 0, global_timer_ns());

@@ -13,6 +13,7 @@ struct Ctl {
   int group;       // written by cluster rank 0 into both CTAs
   int abort;
   uint32_t tmem;
+  int lane_ok;     // producer role: passes whose ring slot the lane's previous job is done with
 };
 
 // Optional tracing: per role slot (group * 2 + cluster rank) kTraceWords words
@@ -20,7 +21,8 @@ struct Ctl {
 //   [3] ns waiting on the other role kind (consumer: `ready` flags; producer: `consumed`)
 //   [4] ns the MMA thread waited for operands (kv_full / prod_full)
 //   [5] ns the MMA thread waited for softmax (p_full) or conversion (acc_empty)
-//   [6] ns softmax warp 0 waited for S (s_full)   [7] stages / passes
+//   [6] consumer: ns softmax warp 0 waited for S (s_full); producer: ns its row
+//       loader waited for the ring lane's previous job   [7] stages / passes
 struct TraceAcc {
   unsigned long long t = 0;
   __device__ __forceinline__ uint64_t begin(const FusedParams& p) const { return p.trace ? global_timer_ns() : 0; }
@@ -70,6 +72,21 @@ __device__ inline bool wait_flag_geq(const FusedParams& p, const uint32_t* flag,
   return true;
 }
 
+// Bounded wait until the shared word *w >= target (acquire, CTA scope);
+// gives up when this CTA aborts or another CTA records an error.
+__device__ inline bool wait_shared_geq(const FusedParams& p, volatile Ctl* ctl, const int* w, int target) {
+  if (ld_acquire_cta_s32(w) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire_cta_s32(w) < target) {
+    if (ctl->abort || global_timer_ns() - t0 > p.wait_limit_ns || aborted_global(p)) {
+      atomicOr(p.err, kErrTimeout);
+      return false;
+    }
+    __nanosleep(32);
+  }
+  return true;
+}
+
 // Number of 128-key tiles consumer `ci` (queries 128 ci .. 128 ci + 127 of the
 // request) of job `J` attends to (causal clip).
 __device__ __forceinline__ int consumer_tiles(const Job& J, int ci) {
@@ -88,8 +105,40 @@ __device__ __forceinline__ int query_token(const Job& J, int q) {
   return J.q_tok ? J.q_tok[J.q_begin + min(q, J.q_count - 1)] : J.q_tok0 + q;
 }
 
+// Device view of job (piece, head) of the launch; its index is piece * H + head.
+__device__ __forceinline__ Job make_job(const FusedParams& p, int piece, int head) {
+  const Piece& P = p.pieces[piece];
+  Job J;
+  J.req = P.req;
+  J.head = head;
+  J.q_begin = P.q_begin;
+  J.q_count = P.q_count;
+  J.q_tok0 = P.q_tok0;
+  J.q_tok = p.q_tok;
+  J.k_begin = P.k_begin;
+  J.k_end = P.k_end;
+  J.t0 = P.k_begin & ~(kBlock - 1);
+  J.n_tiles = (P.k_end - J.t0 + 127) >> 7;
+  J.n_cons = P.n_cons;
+  J.n_prod = P.n_prod;
+  J.slot = P.slot;
+  J.row_block0 = P.row_block0;
+  J.rope_offset = P.rope_offset;
+  return J;
+}
+
 // Ring slot of tile t (the depth is a power of two).
 __device__ __forceinline__ int ring_slot(const FusedParams& p, int t) { return t & (p.ring_depth - 1); }
+
+// First of the four [128 x 64] bf16 blocks of ring slot `slot` of job `job`
+// (K_nope cols 0-63, 64-127, V cols 0-63, 64-127).  Jobs take turns on
+// ring_lanes lanes of ring_depth slots: job j writes a slot of lane
+// j mod ring_lanes once job j - ring_lanes is done with it, so the rings of a
+// launch span a fixed number of lanes, whatever its number of jobs, and a
+// lane's slots are rewritten soon enough to be still in L2.
+__device__ __forceinline__ int ring_block(const FusedParams& p, int job, int slot) {
+  return ((job % p.ring_lanes) * p.ring_depth + slot) * 4;
+}
 
 __device__ __forceinline__ uint32_t* ready_flag(const FusedParams& p, int job, int slot) {
   return p.flags + (size_t)job * (2 * (size_t)p.ring_depth) + slot;
@@ -97,7 +146,6 @@ __device__ __forceinline__ uint32_t* ready_flag(const FusedParams& p, int job, i
 __device__ __forceinline__ uint32_t* consumed_flag(const FusedParams& p, int job, int slot) {
   return p.flags + (size_t)job * (2 * (size_t)p.ring_depth) + p.ring_depth + slot;
 }
-
 // Ring tiles [t, end) (end - t <= 8) that are produced, polled together: the
 // relaxed reads of their ready flags go out at once and one fence makes the
 // ones seen an acquire.  Returns the first tile of the range not yet seen

@@ -61,7 +61,8 @@ struct MergeParams {
 };
 
 // ------------------------------------------------------------ fused persistent kernel
-constexpr int kRingDepth = 128;   // deepest job ring: 128-token K/V tiles (8 MB); a small workspace gets less
+constexpr int kRingDepth = 128;   // deepest ring lane: 128-token K/V tiles (8 MB); a small workspace gets less
+constexpr int kRingLanes = 12;    // most ring lanes the jobs of a launch take turns on
 constexpr int kMaxPieces = 448;   // pieces per launch (kernel-parameter budget)
 
 // One key range of one request attended with one RoPE offset, for every head.
@@ -105,7 +106,7 @@ struct FusedParams {
                            // a sorted subset of the request's queries); nullptr: q_tok0 + row - q_begin
   uint32_t* err;
   uint32_t* queue;       // role-group counter
-  uint32_t* flags;       // per job: ready[ring], consumed[ring]
+  uint32_t* flags;       // per job: ready[ring_depth], consumed[ring_depth]
   uint16_t* ring;
   const int32_t* block_table;
   const int32_t* q_pos;
@@ -122,9 +123,11 @@ struct FusedParams {
   float scale_log2;
   int n_pieces;
   int n_groups;         // role groups in the queue (one per cluster dequeue)
-  int ring_depth;       // 128-token tiles per job ring: a power of two <= kRingDepth (slots are t & (depth - 1))
+  int ring_depth;       // 128-token tiles per ring lane: a power of two <= kRingDepth (slots are t & (depth - 1))
+  int ring_lanes;       // job j writes its tiles into lane j % ring_lanes
   int prod_ahead;       // heads by which a job's producers precede their consumers in the queue
   uint64_t wait_limit_ns;   // bound of every wait of the kernel (a timeout sets kErrTimeout)
+  int l2_hints;         // 1: ring tiles evict_last, streamed data evict_first; 0: evict_normal
   int withhold_job;     // test hook: this job's producer roles do nothing, so its consumers' waits run
                         // out (-1: none)
   unsigned long long* trace;   // optional, kTraceWords per role slot (group * 2 + cluster rank; see fused_common.cuh)

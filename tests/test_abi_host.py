@@ -50,14 +50,17 @@ def _up(x, a=256):
     return (x + a - 1) // a * a
 
 
-def fused_layout(pieces, heads, slots, total_q, seq_lens, ring_depth=128):
-    """Workspace of the fused path: 256 B header, per-job ring flags, per-job
-    K/V rings of `ring_depth` 128-token bf16 tiles, room for the dequantised
-    rows of an FP8 cache (1152 B per token, whole 64-token blocks), then
-    partial states."""
+def fused_layout(pieces, heads, slots, total_q, seq_lens, ring_depth=128, ring_lanes=None, max_tiles=None):
+    """Workspace of the fused path: 256 B header, per-job ring flags, the K/V
+    ring lanes (`ring_lanes` x `ring_depth` 128-token bf16 tiles, shared by
+    the jobs in turn), the gathered rows (1152 B per token, whole 64-token
+    blocks), then partial states."""
     jobs = pieces * heads
+    if ring_lanes is None:                   # 32 MiB of the longest piece's tiles, within [4, 12]
+        ring_lanes = max(4, min(12, (32 << 20) // (128 * 256 * 2 * min(max_tiles, ring_depth))))
+    ring_lanes = min(ring_lanes, jobs)       # no more lanes than jobs
     ring_off = _up(256 + jobs * 2 * ring_depth * 4)
-    gath_off = _up(ring_off + jobs * ring_depth * 128 * 256 * 2)
+    gath_off = _up(ring_off + ring_lanes * ring_depth * 128 * 256 * 2)
     gath = sum((s + 63) // 64 for s in seq_lens) * 64 * 1152
     lse_off = _up(gath_off + gath)
     rows = slots * total_q * heads
@@ -68,12 +71,27 @@ def test_workspace_size_follows_plan(lib):
     # 1 request, C=256 in chunks of 128 plus the extend: the three ranges share
     # offset 0 and are contiguous, so they fold into one piece (no partial slots).
     n = _ws(lib, [320], [0, 64], 8, chunk=128)
-    assert n == fused_layout(1, 8, 0, 64, [320])
+    assert n == fused_layout(1, 8, 0, 64, [320], max_tiles=3)
     # segments: 4 documents of 64 (4 offsets) + extend = 5 pieces, 5 partial slots
     segs = [[0, 64 * d, 64, 64 * d] for d in range(4)]
-    assert _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64) == fused_layout(5, 1, 5, 2, [258])
-    # a long context is cut into pieces of at most max(chunk, 16384) keys
-    assert _ws(lib, [40000 + 100], [0, 100], 2, chunk=4096) == fused_layout(3, 2, 3, 100, [40100])
+    assert _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64) == fused_layout(5, 1, 5, 2, [258], max_tiles=1)
+    # a long context is cut into pieces of at most max(chunk, 16384) keys:
+    # 16384 + 16384 + 7232 + 100, the longest 128 tiles -> 4 lanes
+    assert _ws(lib, [40000 + 100], [0, 100], 2, chunk=4096) == fused_layout(3, 2, 3, 100, [40100], max_tiles=128)
+    # 8192 + 2048 keys in one piece: 80 tiles -> 6 lanes
+    assert _ws(lib, [10240], [0, 2048], 2, chunk=4096) == fused_layout(1, 2, 0, 2048, [10240], max_tiles=80)
+
+
+def test_min_workspace_size(lib):
+    """The smallest workspace: two ring lanes of 4 tiles, flags of one piece's jobs."""
+    sl, k1 = _lib.i32_host([258])
+    cq, k2 = _lib.i32_host([0, 2])
+    segs = [[0, 64 * d, 64, 64 * d] for d in range(4)]
+    sp, ns, k3 = _lib.segments_host(segs)
+    n = lib.mla_prefill_min_workspace_size(1, sl, cq, 3, sp, ns, 64, 3)
+    assert n == fused_layout(1, 3, 5, 2, [258], ring_depth=4, ring_lanes=2)
+    assert n < _ws(lib, [258], [0, 2], 3, segs=segs, chunk=64)
+    assert lib.mla_prefill_min_workspace_size(1, sl, cq, 3, sp, ns, 100, 3) == 0    # chunk not a multiple of 64
 
 
 @pytest.mark.parametrize("bad", [

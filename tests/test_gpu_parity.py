@@ -233,23 +233,24 @@ def test_prefill_empty_context_segments(api):
 
 
 def test_prefill_small_workspace_runs_in_several_launches(api):
-    """A workspace that holds the rings of one piece only: the call splits its
-    pieces over several launches and must give the same result."""
+    """The smallest workspace the call accepts: two ring lanes of 4 tiles and
+    the ring flags of one piece (of two here, where both round up to the same
+    256 bytes).  The call splits its pieces over several launches and must
+    give the same result; a smaller one is refused."""
     from mla_prefix_cache_gb300 import _lib
     wl = W.make_workload("sw", 4, [192], [70], chunk=64, seed=35, doc_len=64)   # 3 documents + extend = 4 pieces
     dw = api.DeviceWorkload(wl)
-    full = api.prefill_workspace_size(wl.seq_lens, wl.cu_q, 4, wl.segments, wl.chunk)
-    ring_per_piece = 4 * 32 * 128 * 256 * 2
-    small = torch.empty(full - 2 * ring_per_piece, dtype=torch.uint8, device="cuda")
+    n_min = api.prefill_min_workspace_size(wl.seq_lens, wl.cu_q, 4, wl.segments, wl.chunk)
+    assert n_min < api.prefill_workspace_size(wl.seq_lens, wl.cu_q, 4, wl.segments, wl.chunk)
+    small = torch.empty(n_min, dtype=torch.uint8, device="cuda")
     n0 = api.launch_count()
     out, lse = dw.run(workspace=small)
     torch.cuda.synchronize()
-    assert api.launch_count() - n0 >= 3          # at least two fused launches plus the merge
+    assert api.launch_count() - n0 >= 4          # the gather, two fused launches or more, the merge
     ref = O.mla_prefill(**O.workload_args(wl))
     assert_close(out.cpu().numpy(), lse.cpu().numpy(), *ref, visible_keys(wl))
-    tiny_ws = torch.empty(4096, dtype=torch.uint8, device="cuda")
     with pytest.raises(_lib.MLAError):
-        dw.run(workspace=tiny_ws)
+        dw.run(workspace=torch.empty(n_min - 256, dtype=torch.uint8, device="cuda"))
 
 
 @pytest.mark.parametrize("depth", [4, 8])
@@ -265,9 +266,11 @@ def test_prefill_shallow_ring_wraps(api, depth, monkeypatch):
     {"MLA_PRODUCER_LOOKAHEAD": "1"},
     {"MLA_PRODUCER_LOOKAHEAD": "5", "MLA_PRODUCERS": "2"},
     {"MLA_PRODUCERS": "8", "MLA_RING_DEPTH": "8"},
-], ids=["lookahead1", "lookahead5_one_producer", "four_producers_shallow"])
+    {"MLA_RING_LANES": "3"},                                  # every job waits for the lane's job 3 before it
+    {"MLA_RING_LANES": "2", "MLA_PRODUCER_LOOKAHEAD": "1", "MLA_RING_DEPTH": "4"},   # the fewest lanes
+], ids=["lookahead1", "lookahead5_one_producer", "four_producers_shallow", "three_lanes", "two_shallow_lanes"])
 def test_prefill_queue_knobs(api, knobs, monkeypatch):
-    """The role queue's tuning knobs (producer count, lookahead, ring depth)
+    """The role queue's tuning knobs (producer count, lookahead, ring depth, ring lanes)
     change the schedule, never the result."""
     for k, v in knobs.items():
         monkeypatch.setenv(k, v)

@@ -38,7 +38,8 @@ def _noalloc(L, dw, wl, out, lse):
 @pytest.mark.parametrize("wl", [
     W.tiny(),
     W.make_workload("docs", 8, [128], [70], chunk=64, seed=40, doc_len=64),   # partial states + merge
-], ids=["tiny", "segments"])
+    W.make_workload("h128", 128, [300], [70], chunk=128, seed=42),            # DeepSeek head count
+], ids=["tiny", "segments", "h128"])
 def test_noalloc_matches_workspace_entry_point(wl):
     from mla_prefix_cache_gb300 import _lib, api
     L = _lib.load()
@@ -58,11 +59,24 @@ def test_noalloc_matches_workspace_entry_point(wl):
 def test_noalloc_rejects_problems_beyond_its_scratch():
     from mla_prefix_cache_gb300 import _lib, api
     L = _lib.load()
-    wl = W.make_workload("big", 128, [64], [1], seed=41)   # 128 heads: 256 MiB of K/V rings for one piece
-    assert api.prefill_workspace_size(wl.seq_lens, wl.cu_q, 128, None, wl.chunk) > _lib.NOALLOC_SCRATCH_BYTES
+    wl = W.make_workload("big", 2, [40000], [1], seed=41)   # 46 MB of gathered rows alone
+    assert api.prefill_min_workspace_size(wl.seq_lens, wl.cu_q, 2, None, wl.chunk) > _lib.NOALLOC_SCRATCH_BYTES
     dw = api.DeviceWorkload(wl)
-    out = torch.zeros((1, 128, 128), device="cuda")
-    lse = torch.zeros((1, 128), device="cuda")
+    out = torch.zeros((1, 2, 128), device="cuda")
+    lse = torch.zeros((1, 2), device="cuda")
     n0 = api.launch_count()
     assert _noalloc(L, dw, wl, out, lse) == _lib.MLA_ERR_TOO_LARGE
+    assert api.launch_count() == n0
+
+
+def test_noalloc_without_queries_launches_nothing():
+    """A call with no query rows is valid and does nothing, as for mla_prefill_ctx."""
+    from mla_prefix_cache_gb300 import _lib, api
+    L = _lib.load()
+    wl = W.make_workload("none", 2, [128], [0], seed=43)
+    dw = api.DeviceWorkload(wl)
+    out = torch.zeros((1, 2, 128), device="cuda")
+    lse = torch.zeros((1, 2), device="cuda")
+    n0 = api.launch_count()
+    assert _noalloc(L, dw, wl, out, lse) == _lib.MLA_OK
     assert api.launch_count() == n0
