@@ -162,8 +162,35 @@ struct FusedPlan {
 // keys.  The online softmax inside a piece folds its chunks exactly as
 // merge_attn_states would; pieces of one request are folded by the merge
 // kernel.
+// Exact-score fields of a request's pieces: its leading rows that see fewer
+// than kExactKeys keys in all (context keys of every piece plus the causal
+// extend keys), and per piece the tiles those rows see and the consumer
+// pairs that hold them.  q_tok (host, optional): the token of each row.
+static void set_exact(std::vector<Piece>& pr, int C, int E, const int32_t* q_tok) {
+  int64_t ctx_keys = 0;
+  bool has_ext = false;
+  for (const Piece& pc : pr) {
+    ctx_keys += std::max(0, std::min(pc.k_end, C) - pc.k_begin);
+    has_ext |= pc.k_end > C;
+  }
+  auto tok = [&](int i) { return q_tok ? q_tok[i] : C + i; };
+  int rows = 0;   // rows [0, rows) need exact scores
+  while (rows < E && ctx_keys + (has_ext ? (int64_t)tok(rows) - C + 1 : 0) < kExactKeys) ++rows;
+  for (Piece& pc : pr) {
+    pc.exact = 0;
+    if (rows == 0) continue;
+    const int t0 = pc.k_begin & ~(kBlock - 1);
+    const int vis_end = std::min(pc.k_end, std::max(C, tok(rows - 1) + 1));   // keys those rows see end here
+    if (vis_end <= pc.k_begin) continue;
+    const int tiles = std::min(kExactSlots, (vis_end - t0 + 127) / 128);
+    const int pairs = (rows + 255) / 256;
+    pc.exact = tiles | (pairs << 8);
+  }
+}
+
 static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const int32_t* cu_q, int num_reqs,
-                            int chunk, bool gather_rows, FusedPlan* fp, const int32_t* ctx_lens = nullptr) {
+                            int chunk, bool gather_rows, FusedPlan* fp, const int32_t* ctx_lens = nullptr,
+                            const int32_t* q_tok = nullptr) {
   fp->skip = splits.skip;
   fp->pieces.clear();
   fp->merge.clear();
@@ -202,6 +229,7 @@ static int build_fused_plan(const Plan& splits, const int32_t* seq_lens, const i
       pc.rope_offset = sp.rope_offset;
       pr.push_back(pc);
     }
+    set_exact(pr, C, E, q_tok ? q_tok + cu_q[r] : nullptr);
     const int np = (int)pr.size();
     int row_block0 = -1;
     if (gather_rows && np > 0) {
@@ -260,7 +288,9 @@ static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads, int ppl, int 
   w.ring_lanes = lanes;
   w.flags_bytes = jobs * 2 * (size_t)depth * sizeof(uint32_t);   // ready and consumed per ring slot
   w.ring_off = up256(w.flags_off + w.flags_bytes);
-  const size_t ring_bytes = (size_t)lanes * (size_t)depth * 128 * 256 * sizeof(uint16_t);
+  // per lane: depth slots of [K_nope | V] tiles, then the K_nope residuals of its first kExactSlots slots
+  const size_t ring_bytes = (size_t)lanes * ((size_t)depth * 128 * 256 + (size_t)std::min(depth, kExactSlots) * 128 * 128) *
+                            sizeof(uint16_t);
   const size_t rows = (size_t)fp.max_slots * (size_t)fp.total_q * (size_t)num_heads;
   w.gath_off = up256(w.ring_off + ring_bytes);
   const size_t gath_bytes = (size_t)fp.gather_blocks * kBlock * kRowBytesBf16;
@@ -303,10 +333,18 @@ static int ring_lanes_cfg(const FusedPlan& fp, int depth) {
   return std::max(ahead + 2, std::min(kRingLanes, fit));
 }
 
+// The preferred layout: every piece in one launch (up to kMaxPieces), lanes
+// as deep as the longest piece (a power of two, 4 to 128 tiles), so no job
+// wraps around its lane; no lanes when there is no piece.
 static FusedWs fused_ws_layout(const FusedPlan& fp, int num_heads) {
   const int ppl = std::max(1, std::min((int)fp.pieces.size(), kMaxPieces));
-  const int depth = max_ring_depth();
-  return fused_ws_layout(fp, num_heads, ppl, depth, ring_lanes_cfg(fp, depth));
+  int max_tiles = 1;
+  for (const Piece& pc : fp.pieces)
+    max_tiles = std::max(max_tiles, (pc.k_end - (pc.k_begin & ~(kBlock - 1)) + 127) / 128);
+  int depth = 4;
+  while (depth < max_tiles && depth < max_ring_depth()) depth *= 2;
+  depth = std::min(depth, max_ring_depth());
+  return fused_ws_layout(fp, num_heads, ppl, depth, fp.pieces.empty() ? 0 : ring_lanes_cfg(fp, depth));
 }
 
 // Layout for a workspace of `bytes`: the preferred one when it fits, else
@@ -487,8 +525,10 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     ok &= encode_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_b_proj, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   {
-    // ring lanes: per lane and slot four contiguous [128 x 64] blocks K_nope lo, K_nope hi, V lo, V hi
-    const uint64_t d[3] = {64, 128, (uint64_t)fw.ring_lanes * (uint64_t)fw.ring_depth * 4};
+    // ring lanes: per lane and slot four contiguous [128 x 64] blocks K_nope cols 0-63, 64-127, V cols 0-63,
+    // 64-127; after every lane's slots, per lane and residual slot two blocks of the K_nope residual
+    const uint64_t d[3] = {64, 128, (uint64_t)fw.ring_lanes * ((uint64_t)fw.ring_depth * 4 +
+                                                            (uint64_t)std::min(fw.ring_depth, kExactSlots) * 2)};
     const uint64_t st[2] = {128, 128 * 128};
     const uint32_t b[3] = {64, 128, 2};
     ok &= encode_map(&p.tm_ring, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + fw.ring_off, d, st, b,
@@ -980,7 +1020,8 @@ static int build_reuse_plan(int num_reqs, const int32_t* seq_lens, const int32_t
     if ((st = build_plan(num_reqs, seq_lens, rp->cu_p.data(), nL, segs, nseg, chunk, parts, &rp->plan_p,
                          rp->ctx.data())) != MLA_OK)
       return st;
-    build_fused_plan(rp->plan_p, seq_lens, rp->cu_p.data(), num_reqs, chunk, true, &rp->fp_p, rp->ctx.data());
+    build_fused_plan(rp->plan_p, seq_lens, rp->cu_p.data(), num_reqs, chunk, true, &rp->fp_p, rp->ctx.data(),
+                     rp->prot_tok.data());
     rp->fw_p = fused_ws_layout(rp->fp_p, nL);
     fused_bytes = std::max(fused_bytes, rp->fw_p.total);
   }
@@ -1097,17 +1138,41 @@ struct AutoPlan {
   bool any_f = false, any_a = false;
 };
 
+// Keys the first query row of each request sees (its context keys, plus
+// itself when the extend stage is attended): the fewest of any of its rows.
+static std::vector<int64_t> first_row_keys(const Plan& plan, const int32_t* seq_lens, const int32_t* cu_q,
+                                           int num_reqs, int parts) {
+  std::vector<int64_t> n(num_reqs, 0);
+  for (const Split& sp : plan.splits)
+    if (sp.k_begin < sp.q_tok0) n[sp.req] += std::min(sp.k_end, sp.q_tok0) - sp.k_begin;
+  for (int r = 0; r < num_reqs; ++r)
+    if ((parts & MLA_PART_EXTEND) && cu_q[r + 1] > cu_q[r]) n[r] += 1;
+  return n;
+}
+
+// The requests of a call split between the up-projected and the absorbed
+// paths.  The absorbed path takes a request when all its rows see at least
+// kExactKeys keys (it rounds the absorbed query to bf16, which moves each
+// score by about 1.4e-3 and a row's lse by as much when it has few keys; the
+// up-projected kernel takes such rows with exact scores) and, for the
+// per-request dispatch (by_queries), when it has at most
+// kAutoAbsorbedMaxQueries queries.
 static int build_auto_plan(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int H,
-                           const mla_segment* segs, int nseg, int chunk, int parts, AutoPlan* au) {
+                           const mla_segment* segs, int nseg, int chunk, int parts, AutoPlan* au,
+                           bool by_queries = true) {
+  Plan all;
+  int st = build_plan(num_reqs, seq_lens, cu_q, H, segs, nseg, chunk, parts, &all);
+  if (st != MLA_OK) return st;
+  const std::vector<int64_t> keys = first_row_keys(all, seq_lens, cu_q, num_reqs, parts);
   std::vector<uint8_t> is_short(num_reqs), is_long(num_reqs);
   for (int r = 0; r < num_reqs; ++r) {
     const int E = cu_q[r + 1] - cu_q[r];
-    is_short[r] = E <= kAutoAbsorbedMaxQueries;
+    is_short[r] = (!by_queries || E <= kAutoAbsorbedMaxQueries) && keys[r] >= kExactKeys;
     is_long[r] = !is_short[r];
     au->any_a |= E > 0 && is_short[r];
     au->any_f |= E > 0 && is_long[r];
   }
-  int st = build_plan(num_reqs, seq_lens, cu_q, H, segs, nseg, chunk, parts, &au->plan_f, nullptr, is_short.data());
+  st = build_plan(num_reqs, seq_lens, cu_q, H, segs, nseg, chunk, parts, &au->plan_f, nullptr, is_short.data());
   if (st != MLA_OK) return st;
   if ((st = build_plan(num_reqs, seq_lens, cu_q, H, segs, nseg, chunk, parts, &au->plan_a, nullptr,
                        is_long.data())) != MLA_OK)
@@ -1219,14 +1284,52 @@ int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos, const void* kv_
 
 size_t mla_prefill_absorbed_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,
                                            const mla_segment* segments, int num_segments, int chunk, int parts) {
-  Plan plan;
-  if (build_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &plan) != MLA_OK)
+  static AutoPlan au;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  au = AutoPlan();
+  if (build_auto_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &au, false) != MLA_OK)
     return 0;
-  FusedPlan fp;
-  build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fp);
-  AbsPlan ap;
-  build_abs_plan(fp, num_heads, cu_q, num_reqs, &ap);
-  return abs_ws_layout(fp, ap, num_heads).total;
+  return au.total;
+}
+
+// The absorbed and the per-request paths: the requests split by build_auto_plan,
+// the up-projected part first (its workspace header holds the call's error word).
+static int prefill_split(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                         int num_blocks, const int32_t* block_table, int max_blocks_per_req, const int32_t* seq_lens,
+                         const int32_t* cu_q, int num_reqs, int num_heads, const mla_segment* segments,
+                         int num_segments, int chunk, const void* kv_b_proj, float softmax_scale, float rope_theta,
+                         int parts, void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                         mla_stream_t stream, bool by_queries) {
+  Plan plan;
+  FusedPlan fplan;
+  int st = prefill_plans(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                         seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
+                         softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
+  if (st != MLA_OK || plan.total_q == 0) return st;
+  static AutoPlan au;              // large; built on the host under a lock
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  au = AutoPlan();
+  if ((st = build_auto_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &au,
+                            by_queries)) != MLA_OK)
+    return st;
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < au.total) return MLA_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);   // the up-projected part's header is the call's
+  if ((st = cuda_status(cudaMemsetAsync(ws, 0, 256, s))) != MLA_OK) return st;
+  if (au.any_f &&
+      (st = prefill_fused(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                          num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, ws, au.fp_f, au.fw, s,
+                          nullptr, true)) != MLA_OK)
+    return st;
+  if (au.any_a &&
+      (st = prefill_absorbed(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                             num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, ws + au.off_abs,
+                             au.fp_a, au.ap, au.aw, s, false, err)) != MLA_OK)
+    return st;
+  return MLA_OK;
 }
 
 int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
@@ -1235,19 +1338,9 @@ int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos, const void* kv
                              const mla_segment* segments, int num_segments, int chunk, const void* kv_b_proj,
                              float softmax_scale, float rope_theta, int parts, void* out, int out_dtype, float* lse,
                              void* workspace, size_t workspace_bytes, mla_stream_t stream) {
-  Plan plan;
-  FusedPlan fplan;
-  const int st = prefill_plans(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
-                               seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
-                               softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
-  if (st != MLA_OK || plan.total_q == 0) return st;
-  AbsPlan ap;
-  build_abs_plan(fplan, num_heads, cu_q, num_reqs, &ap);
-  const AbsWs aw = abs_ws_layout(fplan, ap, num_heads);
-  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < aw.total) return MLA_ERR_WORKSPACE;
-  return prefill_absorbed(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
-                          num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, workspace, fplan, ap,
-                          aw, reinterpret_cast<cudaStream_t>(stream));
+  return prefill_split(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req, seq_lens,
+                       cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj, softmax_scale, rope_theta,
+                       parts, out, out_dtype, lse, workspace, workspace_bytes, stream, false);
 }
 
 size_t mla_prefill_reuse_workspace_size(int num_reqs, const int32_t* seq_lens, const int32_t* cu_q, int num_heads,
@@ -1338,34 +1431,9 @@ int mla_prefill_ctx_auto(const void* q, const int32_t* q_pos, const void* kv_cac
                          int num_segments, int chunk, const void* kv_b_proj, float softmax_scale, float rope_theta,
                          int parts, void* out, int out_dtype, float* lse, void* workspace, size_t workspace_bytes,
                          mla_stream_t stream) {
-  Plan plan;
-  FusedPlan fplan;
-  int st = prefill_plans(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
-                         seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj,
-                         softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
-  if (st != MLA_OK || plan.total_q == 0) return st;
-  static AutoPlan au;              // large; built on the host under a lock
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
-  au = AutoPlan();
-  if ((st = build_auto_plan(num_reqs, seq_lens, cu_q, num_heads, segments, num_segments, chunk, parts, &au)) != MLA_OK)
-    return st;
-  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < au.total) return MLA_ERR_WORKSPACE;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint32_t* err = reinterpret_cast<uint32_t*>(ws);   // the up-projected part's header is the call's
-  if ((st = cuda_status(cudaMemsetAsync(ws, 0, 256, s))) != MLA_OK) return st;
-  if (au.any_f &&
-      (st = prefill_fused(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
-                          num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, ws, au.fp_f, au.fw, s,
-                          nullptr, true)) != MLA_OK)
-    return st;
-  if (au.any_a &&
-      (st = prefill_absorbed(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
-                             num_heads, kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, ws + au.off_abs,
-                             au.fp_a, au.ap, au.aw, s, false, err)) != MLA_OK)
-    return st;
-  return MLA_OK;
+  return prefill_split(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req, seq_lens,
+                       cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj, softmax_scale, rope_theta,
+                       parts, out, out_dtype, lse, workspace, workspace_bytes, stream, true);
 }
 
 int mla_get_device_error(void* workspace, mla_stream_t stream) {

@@ -52,6 +52,7 @@ constexpr uint32_t kVStageBytes = kAtomQ;                          // 128 keys x
 constexpr uint32_t kKBase = 3 * kAtomQ;                            // 49152
 constexpr uint32_t kVBase = kKBase + kKStages * kKStageBytes;      // 147456
 constexpr uint32_t kXchgBase = kVBase + kVStages * kVStageBytes;   // 212992: row maxima / sums of the two halves
+constexpr uint32_t kQResBase = kVBase + 3 * kVStageBytes;           // exact pairs: rotated q_rope residual (V stage 3)
 constexpr uint32_t kConsumerEnd = kXchgBase + 6 * 128 * 4;
 // producer: this CTA's 128 kv_b_proj columns stay resident for the role
 constexpr int kPStages = 6;
@@ -120,12 +121,24 @@ __device__ __forceinline__ int consumers_needing_tile(const Job& J, int t) {
   return n;
 }
 
+// Exact scores: K-side tiles of consumer pair k that also take the K_nope
+// residual (a second stage use each, right after the tile's own).
+__device__ __forceinline__ int exact_tiles_produced(const FusedParams& p, const Job& J) {
+  return J.n_exact_pairs > 0 ? min(J.n_exact_tiles, p.ring_depth) : 0;
+}
+__device__ __forceinline__ int exact_tiles(const FusedParams& p, const Job& J, int k, int n_tiles) {
+  return k < J.n_exact_pairs ? min(exact_tiles_produced(p, J), n_tiles) : 0;
+}
+__device__ __forceinline__ int use_tile(int u, int ex) { return u < 2 * ex ? (u >> 1) : u - ex; }
+__device__ __forceinline__ bool use_is_residual(int u, int ex) { return u < 2 * ex && (u & 1); }
+__device__ __forceinline__ bool last_use_of_tile(int u, int ex) { return u >= 2 * ex || (u & 1); }
+
 // =============================================================== consumer pair
 // Warps: 0-7 softmax (warpgroup w owns key columns 64w..64w+63 of every row of
 // this CTA's S; warpgroup 0 first loads and rotates Q into shared memory),
 // 8 K loader, 10 V loader (each also releases ring slots once their stage is
 // consumed), 9 MMA issuer (leader only).
-template <bool kCompute>
+template <bool kCompute, bool kExact>
 __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k, int role, uint32_t sbase,
                              uint8_t* sgen, uint32_t tmem, volatile Ctl* ctl, uint32_t rank) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -149,7 +162,8 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
         for (int part = 0; part < 3; ++part)
           tma_load_3d_hint(sbase + kQBase + part * kAtomQ, &p.tm_q, 64 * part, J.head, grow0, qb, policy_stream(p));
       }
-      const int ns = is_k ? kKStages : kVStages;
+      // an exact pair keeps its rotated q_rope residual in V stage 3, so its V side runs 3 stages
+      const int ns = is_k ? kKStages : (kExact && exact_tiles(p, J, k, n_tiles) > 0 ? kVStages - 1 : kVStages);
       const uint32_t full0 = is_k ? kBKFull : kBVFull, empty0 = is_k ? kBKEmpty : kBVEmpty;
       const uint64_t pol_ring = policy_keep(p);
       TraceAcc tr;
@@ -158,20 +172,29 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       // when the ring is deep enough; produced tiles are polled a window at a
       // time.  Per-tile flag round trips would otherwise pace the loads.
       const int batch = p.ring_depth >= ns + 4 ? 4 : 1;
-      int rel0 = 0, pend = 0;   // tiles [rel0, rel0 + pend) read but not yet released
+      // Stage uses: one per tile, and on the K side a second one for the
+      // K_nope residual of the first `ex` tiles when this pair takes exact scores.
+      const int ex = kExact && is_k ? exact_tiles(p, J, k, n_tiles) : 0;
+      const int n_uses = n_tiles + ex;
+      int rel0 = 0;             // tiles below are released
+      int done_to = 0;          // tiles below are read completely (every stage use consumed)
       int ready_to = 0;         // tiles below are known to be produced
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % ns;
-        if (j >= ns) {
+      for (int u = 0; u < n_uses; ++u) {
+        const int s = u % ns;
+        const int j = use_tile(u, ex);
+        if (u >= ns) {
           // the stage is free once the pair's MMAs read it
-          if (!wait_bar(p, bar_addr(sbase, empty0 + s), ((j / ns) - 1) & 1)) { ctl->abort = 1; return; }
-          if (++pend == batch) {
-            release_tiles(p, job, rel0, pend);
-            rel0 += pend;
-            pend = 0;
+          if (!wait_bar(p, bar_addr(sbase, empty0 + s), ((u / ns) - 1) & 1)) { ctl->abort = 1; return; }
+          if (last_use_of_tile(u - ns, ex)) {
+            done_to = use_tile(u - ns, ex) + 1;
+            if (done_to - rel0 == batch) {
+              release_tiles(p, job, rel0, done_to - rel0);
+              rel0 = done_to;
+            }
           }
         }
-        if (j >= ready_to) {
+        const bool res = use_is_residual(u, ex);
+        if (!res && j >= ready_to) {
           const uint64_t w0 = tr.begin(p);
           ready_to = wait_ready_window(p, job, j, min(n_tiles, j + min(8, p.ring_depth)));
           tr.end(p, w0);
@@ -181,7 +204,12 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
         const uint32_t full = bar_addr(sbase, full0 + s);
         const uint32_t full_leader = mapa_shared(full, 0u);
         const int zb = ring_block(p, job, ring_slot(p, j));   // first ring block of the tile
-        if (is_k) {
+        if (is_k && res) {
+          const uint32_t st = sbase + kKBase + s * kKStageBytes;
+          if (leader) mbar_arrive_expect_tx(full, 2 * 2 * kAtom64);
+          tma_load_3d_pair_hint(st, &p.tm_ring64, 0, 64 * (int)rank, residual_block(p, job, ring_slot(p, j)),
+                                full_leader, pol_ring);                                              // K_nope residual
+        } else if (is_k) {
           const uint32_t st = sbase + kKBase + s * kKStageBytes;
           if (leader) mbar_arrive_expect_tx(full, 2 * kKStageBytes);     // both halves land on the leader's count
           const int kt0 = J.t0 + 128 * j;
@@ -197,11 +225,11 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       }
       // the last stages: wait for their MMAs (this also takes the leader's last
       // commits into this CTA's barriers before they are reset), release the slots
-      for (int j = max(0, n_tiles - ns); j < n_tiles; ++j) {
-        if (!wait_bar(p, bar_addr(sbase, empty0 + j % ns), (j / ns) & 1)) { ctl->abort = 1; return; }
-        ++pend;
+      for (int u = max(0, n_uses - ns); u < n_uses; ++u) {
+        if (!wait_bar(p, bar_addr(sbase, empty0 + u % ns), (u / ns) & 1)) { ctl->abort = 1; return; }
+        if (last_use_of_tile(u, ex)) done_to = use_tile(u, ex) + 1;
       }
-      if (pend > 0) release_tiles(p, job, rel0, pend);
+      if (done_to > rel0) release_tiles(p, job, rel0, done_to - rel0);
       if (is_k) {
         trace_put(p, role, 3, tr.t);
         trace_put(p, role, 7, (unsigned long long)n_tiles);
@@ -218,15 +246,21 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       if (!wait_bar(p, bar_addr(sbase, kBQReady), 0)) { ctl->abort = 1; return; }
       tc_fence_after();
       const uint64_t t_start = p.trace ? global_timer_ns() : 0;
+      const int ex = kExact ? exact_tiles(p, J, k, n_tiles) : 0;
+      const int nv = ex > 0 ? kVStages - 1 : kVStages;
       for (int j = 0; j < n_tiles; ++j) {
         const int b = j % kSBufs;
         if (s_side) {
-          const int sk = j % kKStages;
-          if (!wait_bar(p, bar_addr(sbase, kBKFull + sk), (j / kKStages) & 1)) { ctl->abort = 1; return; }
+          const int g = j + min(j, ex);   // stage use of the tile (its residual, when exact, is the next one)
+          const int sk = g % kKStages;
+          if (!wait_bar(p, bar_addr(sbase, kBKFull + sk), (g / kKStages) & 1)) { ctl->abort = 1; return; }
           if (j >= kSBufs && !wait_bar(p, bar_addr(sbase, kBPvDone + b), ((j / kSBufs) - 1) & 1)) {
             ctl->abort = 1;
             return;
           }
+          const bool res = kExact && j < ex;
+          const int sr = (g + 1) % kKStages;
+          if (res && !wait_bar(p, bar_addr(sbase, kBKFull + sr), ((g + 1) / kKStages) & 1)) { ctl->abort = 1; return; }
           trace_stage(p, role, j, 2);
           tc_fence_after();
           const uint32_t kst = sbase + kKBase + sk * kKStageBytes;
@@ -235,14 +269,29 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
           for (int kk = 0; kk < 12; ++kk)
             mma2_ss(d, sdesc_sw128(sbase + kQBase + (kk >> 2) * kAtomQ + (kk & 3) * 32, 16, 1024),
                     sdesc_sw128(kst + (kk >> 2) * kAtom64 + (kk & 3) * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+          if (res) {
+            // exact scores, added to the same accumulator: q_nope . (K_nope - bf16(K_nope))
+            // and (rotated q_rope - its bf16) . k_rope
+            const uint32_t krs = sbase + kKBase + sr * kKStageBytes;
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+              mma2_ss(d, sdesc_sw128(sbase + kQBase + (kk >> 2) * kAtomQ + (kk & 3) * 32, 16, 1024),
+                      sdesc_sw128(krs + (kk >> 2) * kAtom64 + (kk & 3) * 32, 16, 1024), kIdescS, 1u);
+#pragma unroll 1
+            for (int kk = 0; kk < 4; ++kk)
+              mma2_ss(d, sdesc_sw128(sbase + kQResBase + kk * 32, 16, 1024),
+                      sdesc_sw128(kst + 2 * kAtom64 + kk * 32, 16, 1024), kIdescS, 1u);
+          }
           mma2_commit_both(bar_addr(sbase, kBSFull + b));
           mma2_commit_both(bar_addr(sbase, kBKEmpty + sk));
+          if (res) mma2_commit_both(bar_addr(sbase, kBKEmpty + sr));
           trace_stage(p, role, j, 3);
         } else {
-          const int sv = j % kVStages;
+          const int sv = j % nv;
+          const uint32_t vpar = (j / nv) & 1;
           if (!wait_bar(p, bar_addr(sbase, kBPFull + b), (j / kSBufs) & 1)) { ctl->abort = 1; return; }
           trace_stage(p, role, j, 4);
-          if (!wait_bar(p, bar_addr(sbase, kBVFull + sv), (j / kVStages) & 1)) { ctl->abort = 1; return; }
+          if (!wait_bar(p, bar_addr(sbase, kBVFull + sv), vpar)) { ctl->abort = 1; return; }
           trace_stage(p, role, j, 5);
           tc_fence_after();
           const uint32_t v = sbase + kVBase + sv * kVStageBytes;
@@ -271,7 +320,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
       for (int i = 0; i < 32; ++i) rope_sincos_sfu(delta, p.rope_frac[i], &sn[i], &cs[i]);
       const bool landed = wait_bar_warp(p, bar_addr(sbase, kBQLand), 0);
       if (tid == 0) trace_stage(p, role, kTraceOnce, 1);
-      if (landed) {
+      if (landed && !(kExact && exact_tiles(p, J, k, n_tiles) > 0)) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t addr = sbase + kQBase + 2 * kAtomQ + sw128_off(r, c);
@@ -283,6 +332,23 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
             w4[i] = pack_bf16(x0 * cs[4 * c + i] - x1 * sn[4 * c + i], x0 * sn[4 * c + i] + x1 * cs[4 * c + i]);
           }
           sts128(addr, w4[0], w4[1], w4[2], w4[3]);
+        }
+      } else if (landed) {
+        // exact scores: the rotation's bf16 residual too, in the layout of a Q block
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t addr = sbase + kQBase + 2 * kAtomQ + sw128_off(r, c);
+          uint32_t w4[4], x4[4];
+          lds128(addr, w4);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float x0 = __uint_as_float(w4[i] << 16), x1 = __uint_as_float(w4[i] & 0xFFFF0000u);
+            const float y0 = x0 * cs[4 * c + i] - x1 * sn[4 * c + i], y1 = x0 * sn[4 * c + i] + x1 * cs[4 * c + i];
+            w4[i] = pack_bf16(y0, y1);
+            x4[i] = pack_bf16(y0 - __uint_as_float(w4[i] << 16), y1 - __uint_as_float(w4[i] & 0xFFFF0000u));
+          }
+          sts128(addr, w4[0], w4[1], w4[2], w4[3]);
+          sts128(sbase + kQResBase + sw128_off(r, c), x4[0], x4[1], x4[2], x4[3]);
         }
       }
       fence_proxy_async_smem();   // visible to the tensor core before the leader issues S
@@ -484,6 +550,55 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
   }
 }
 
+// Two ring blocks [128 tokens x 64 columns] from a thread's 128 packed bf16
+// values of its row (pk[0..31]: block 0, pk[32..63]: block 1): after an 8x8
+// transpose of 16-byte chunks across lanes, each warp store covers four whole
+// 128-byte rows.
+__device__ __forceinline__ void store_ring_blocks(uint16_t* dst, const uint32_t (&pk)[64], int lane, int st_row,
+                                                  int st_chunk, uint64_t pol) {
+#pragma unroll
+  for (int hb = 0; hb < 2; ++hb) {
+    uint4 c[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      c[e] = make_uint4(pk[32 * hb + 4 * e], pk[32 * hb + 4 * e + 1], pk[32 * hb + 4 * e + 2], pk[32 * hb + 4 * e + 3]);
+    transpose8x16B(c, lane);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      st_global_v4_hint(dst + (size_t)hb * (128 * 64) + (size_t)(st_row + e) * 64 + st_chunk * 8, c[e], pol);
+  }
+}
+
+// The K_nope residual K - bf16(K) of a thread's row (128 accumulator columns
+// at `acc`, scaled by oscale), rounded to bf16 and stored as two ring blocks,
+// one 64-column block at a time (32 words live, so the rare tiles that take
+// it cost the common path no registers).
+__device__ __forceinline__ void store_residual(uint32_t acc, float oscale, bool valid, uint16_t* dst, int lane,
+                                              int st_row, int st_chunk, uint64_t pol) {
+#pragma unroll 1
+  for (int hb = 0; hb < 2; ++hb) {
+    uint32_t w[32];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t a[32];
+      tmem_ld32(acc + (2 * hb + cc) * 32, a);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float x0 = __uint_as_float(a[2 * i]) * oscale, x1 = __uint_as_float(a[2 * i + 1]) * oscale;
+        const uint32_t h = pack_bf16(x0, x1);
+        w[16 * cc + i] = valid ? pack_bf16(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xFFFF0000u)) : 0u;
+      }
+    }
+    uint4 c[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) c[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    transpose8x16B(c, lane);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      st_global_v4_hint(dst + (size_t)hb * (128 * 64) + (size_t)(st_row + e) * 64 + st_chunk * 8, c[e], pol);
+  }
+}
+
 // =============================================================== producer pair
 // Passes pi, pi + n_prod, ... of 256 tokens; CTA r up-projects tokens
 // 128r..128r+127 of a pass (ring tile 2 pass + r).  Warps: 10 loads this CTA's
@@ -491,7 +606,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
 // rows through the stages (waiting for each to be free), 9 MMA (leader), 0-7
 // conversion: warpgroup 0 the K_nope columns, warpgroup 1 the V columns of the
 // CTA's tile, stored from registers into the ring.
-template <bool kCompute>
+template <bool kCompute, bool kExact>
 __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi, int role, uint32_t sbase,
                              uint32_t tmem, volatile Ctl* ctl, uint32_t rank) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -635,9 +750,17 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       if (!wait_bar_warp(p, bar_addr(sbase, kBAccFull + b), (n >> 1) & 1)) ctl->abort = 1;
       if (tid == 0) trace_stage(p, role, n, 2);
       tc_fence_after();
+      const uint32_t acc = tmem + lane_off + kTmAcc + 256 * b + 128 * wg;
+      if (kExact && wg == 0 && live_tile && t < exact_tiles_produced(p, J) && !ctl->abort) {
+        // a tile that a query row with few keys sees: its K_nope residual too,
+        // stored first, before this thread holds the tile's bf16 values.  Such
+        // tiles are on the lane's first lap (t < ring_depth), whose slot the
+        // lane check cleared before this pass's MMAs began.
+        store_residual(acc, oscale, valid, p.ring + (size_t)residual_block(p, job, slot) * (128 * 64), lane, st_row,
+                       st_chunk, pol_ring);
+      }
       uint32_t pk[64];
       if (live_tile && !ctl->abort) {
-        const uint32_t acc = tmem + lane_off + kTmAcc + 256 * b + 128 * wg;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t a[32];
@@ -674,20 +797,8 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       }
       if (live_tile && tid == 0) *consumed_flag(p, job, slot) = 0u;   // ordered before the release of `ready`
       if (live_tile) {
-        // ring block [128 tokens x 64 columns]: each warp store covers four
-        // whole 128-byte rows
-        uint16_t* dst = p.ring + ((size_t)ring_block(p, job, slot) + 2 * wg) * (128 * 64);
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          uint4 c[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            c[e] = make_uint4(pk[32 * hb + 4 * e], pk[32 * hb + 4 * e + 1], pk[32 * hb + 4 * e + 2], pk[32 * hb + 4 * e + 3]);
-          transpose8x16B(c, lane);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            st_global_v4_hint(dst + (size_t)hb * (128 * 64) + (size_t)(st_row + e) * 64 + st_chunk * 8, c[e], pol_ring);
-        }
+        store_ring_blocks(p.ring + ((size_t)ring_block(p, job, slot) + 2 * wg) * (128 * 64), pk, lane, st_row, st_chunk,
+                          pol_ring);
         if (tid == 0) trace_stage(p, role, n, 3);
       }
       pend = live_tile;
@@ -706,7 +817,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
 // control warps (8-11).  Cluster rank 0 takes the next role from the queue
 // and writes it into both CTAs; every exit decision is made there, so both
 // CTAs run the same sequence of cluster barriers.
-template <bool kCompute>
+template <bool kCompute, bool kExact>
 __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, uint8_t* sgen, volatile Ctl* ctl,
                                           uint32_t tmem, uint32_t rank) {
   const int tid = threadIdx.x;
@@ -777,8 +888,8 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
       trace_put(p, slot, 2, ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)producer << 31) | (unsigned)job);
     }
     if (!ctl->abort && !(producer && job == p.withhold_job)) {
-      if (producer) run_producer<kCompute>(p, J, job, idx, slot, sbase, tmem, ctl, rank);
-      else run_consumer<kCompute>(p, J, job, idx, slot, sbase, sgen, tmem, ctl, rank);
+      if (producer) run_producer<kCompute, kExact>(p, J, job, idx, slot, sbase, tmem, ctl, rank);
+      else run_consumer<kCompute, kExact>(p, J, job, idx, slot, sbase, sgen, tmem, ctl, rank);
     }
     tc_fence_before();
     __syncthreads();
@@ -787,6 +898,10 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
   }
 }
 
+// kExact: some job of the launch has query rows that see fewer than
+// kExactKeys keys (exact scores for them); the launches without such rows run
+// the instantiation that has none of that code.
+template <bool kExact>
 __global__ void __launch_bounds__(kThreads, 1) fused2_prefill_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -825,10 +940,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused2_prefill_kernel(const __gri
   // warpgroups 0 and 1 take 56 more each (256 x 56): the same total.
   if ((tid >> 5) >= 8) {
     setmaxnreg_dec<56>();
-    role_loop<false>(p, sbase, sgen, ctl, tmem, rank);
+    role_loop<false, kExact>(p, sbase, sgen, ctl, tmem, rank);
   } else {
     setmaxnreg_inc<224>();
-    role_loop<true>(p, sbase, sgen, ctl, tmem, rank);
+    role_loop<true, kExact>(p, sbase, sgen, ctl, tmem, rank);
   }
   tc_fence_before();
   cluster_sync_all();   // neither CTA releases TMEM while the pair's MMAs could still use it
@@ -842,7 +957,10 @@ int fused2_smem_bytes() { return (int)kSmemBytes; }
 static cudaError_t configure2(int dev) {
   static int configured_device = -1;
   if (configured_device == dev) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(fused2_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(fused2_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused2_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e == cudaSuccess) configured_device = dev;
   return e;
 }
@@ -871,7 +989,10 @@ cudaError_t launch_fused2(const FusedParams& p, int grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   cluster_config(&cfg, attr, grid, s);
-  e = cudaLaunchKernelEx(&cfg, fused2_prefill_kernel, p);
+  bool exact = false;
+  for (int i = 0; i < p.n_pieces; ++i) exact |= p.pieces[i].exact != 0;
+  e = exact ? cudaLaunchKernelEx(&cfg, fused2_prefill_kernel<true>, p)
+            : cudaLaunchKernelEx(&cfg, fused2_prefill_kernel<false>, p);
   count_launch();
   return e;
 }
@@ -886,7 +1007,7 @@ cudaError_t fused2_grid_size(int* grid) {
   cudaLaunchAttribute attr[1];
   cluster_config(&cfg, attr, 2 * ((sms + 1) / 2), nullptr);
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, fused2_prefill_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, fused2_prefill_kernel<false>, &cfg);
   if (e != cudaSuccess) return e;
   *grid = 2 * clusters;
   return *grid > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;

@@ -124,6 +124,8 @@ __device__ __forceinline__ Job make_job(const FusedParams& p, int piece, int hea
   J.slot = P.slot;
   J.row_block0 = P.row_block0;
   J.rope_offset = P.rope_offset;
+  J.n_exact_tiles = P.exact & 255;
+  J.n_exact_pairs = P.exact >> 8;
   return J;
 }
 
@@ -138,6 +140,12 @@ __device__ __forceinline__ int ring_slot(const FusedParams& p, int t) { return t
 // lane's slots are rewritten soon enough to be still in L2.
 __device__ __forceinline__ int ring_block(const FusedParams& p, int job, int slot) {
   return ((job % p.ring_lanes) * p.ring_depth + slot) * 4;
+}
+// First of the two [128 x 64] bf16 blocks (cols 0-63, 64-127) of the K_nope
+// residual K - bf16(K) of ring slot `slot` (< kExactSlots) of job `job`,
+// after all the lanes' slots.
+__device__ __forceinline__ int residual_block(const FusedParams& p, int job, int slot) {
+  return p.ring_lanes * p.ring_depth * 4 + ((job % p.ring_lanes) * min(p.ring_depth, kExactSlots) + slot) * 2;
 }
 
 __device__ __forceinline__ uint32_t* ready_flag(const FusedParams& p, int job, int slot) {

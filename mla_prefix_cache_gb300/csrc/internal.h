@@ -79,13 +79,23 @@ struct Piece {
   int32_t n_cons;      // consumer roles per head (128 queries each)
   int32_t n_prod;      // producer roles per head
   int32_t row_block0;  // the request's rows were gathered contiguously from this block on
-  int32_t pad;
+  int32_t exact;       // exact scores: tiles [0, exact & 255) of the piece carry the bf16 residual of
+                       // K_nope, used by consumer pairs below exact >> 8 (see kExactKeys)
   int64_t rope_offset;
 };
+
+// A query row that sees fewer than kExactKeys keys in all takes its scores
+// with K_nope as bf16 + bf16 residual (exact to about 2^-16): its lse would
+// otherwise carry the bf16 rounding of a handful of scores (about 1.4e-3 per
+// unit-variance score), which many keys average out.  Such rows see at most
+// kExactKeys + 63 keys of a piece from its aligned start: 9 tiles of 128.
+constexpr int kExactKeys = 1024;
+constexpr int kExactSlots = 16;   // ring slots per lane that hold residual tiles
 
 // Device-side view of one job.
 struct Job {
   int32_t req, head, q_begin, q_count, q_tok0, k_begin, k_end, t0, n_tiles, n_cons, n_prod, slot, row_block0;
+  int32_t n_exact_tiles, n_exact_pairs;
   int64_t rope_offset;
   const int32_t* q_tok;   // FusedParams::q_tok
 };

@@ -53,14 +53,15 @@ def _up(x, a=256):
 def fused_layout(pieces, heads, slots, total_q, seq_lens, ring_depth=128, ring_lanes=None, max_tiles=None):
     """Workspace of the fused path: 256 B header, per-job ring flags, the K/V
     ring lanes (`ring_lanes` x `ring_depth` 128-token bf16 tiles, shared by
-    the jobs in turn), the gathered rows (1152 B per token, whole 64-token
+    the jobs in turn, then the K_nope residual tiles of each lane's first 16
+    slots), the gathered rows (1152 B per token, whole 64-token
     blocks), then partial states."""
     jobs = pieces * heads
     if ring_lanes is None:                   # 32 MiB of the longest piece's tiles, within [4, 12]
         ring_lanes = max(4, min(12, (32 << 20) // (128 * 256 * 2 * min(max_tiles, ring_depth))))
     ring_lanes = min(ring_lanes, jobs)       # no more lanes than jobs
     ring_off = _up(256 + jobs * 2 * ring_depth * 4)
-    gath_off = _up(ring_off + ring_lanes * ring_depth * 128 * 256 * 2)
+    gath_off = _up(ring_off + ring_lanes * (ring_depth * 128 * 256 + min(ring_depth, 16) * 128 * 128) * 2)
     gath = sum((s + 63) // 64 for s in seq_lens) * 64 * 1152
     lse_off = _up(gath_off + gath)
     rows = slots * total_q * heads
@@ -71,15 +72,17 @@ def test_workspace_size_follows_plan(lib):
     # 1 request, C=256 in chunks of 128 plus the extend: the three ranges share
     # offset 0 and are contiguous, so they fold into one piece (no partial slots).
     n = _ws(lib, [320], [0, 64], 8, chunk=128)
-    assert n == fused_layout(1, 8, 0, 64, [320], max_tiles=3)
+    assert n == fused_layout(1, 8, 0, 64, [320], ring_depth=4, max_tiles=3)
     # segments: 4 documents of 64 (4 offsets) + extend = 5 pieces, 5 partial slots
     segs = [[0, 64 * d, 64, 64 * d] for d in range(4)]
-    assert _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64) == fused_layout(5, 1, 5, 2, [258], max_tiles=1)
+    assert _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64) == fused_layout(5, 1, 5, 2, [258], ring_depth=4, max_tiles=1)
     # a long context is cut into pieces of at most max(chunk, 16384) keys:
     # 16384 + 16384 + 7232 + 100, the longest 128 tiles -> 4 lanes
     assert _ws(lib, [40000 + 100], [0, 100], 2, chunk=4096) == fused_layout(3, 2, 3, 100, [40100], max_tiles=128)
-    # 8192 + 2048 keys in one piece: 80 tiles -> 6 lanes
+    # 8192 + 2048 keys in one piece: 80 tiles -> 6 lanes of 128 slots
     assert _ws(lib, [10240], [0, 2048], 2, chunk=4096) == fused_layout(1, 2, 0, 2048, [10240], max_tiles=80)
+    # 1000 keys: 8 tiles -> lanes of 8 slots
+    assert _ws(lib, [1000], [0, 100], 3, chunk=512) == fused_layout(1, 3, 0, 100, [1000], ring_depth=8, max_tiles=8)
 
 
 def test_min_workspace_size(lib):
@@ -145,28 +148,40 @@ def test_other_entry_points_validate(lib):
     assert lib.mla_block_compare(d, 1, 4, d, d, 0, d, None, None) == _lib.MLA_OK
 
 
-def test_absorbed_entry_validates_and_sizes(lib):
-    sl, cq = (ctypes.c_int32 * 1)(320), (ctypes.c_int32 * 2)(0, 64)
-    n = lib.mla_prefill_absorbed_workspace_size(1, sl, cq, 8, None, 0, 128, 3)
-    # header + gathered rows (5 blocks) + qlat + one slot of latent states and lse
-    rows = 64 * 8
-    want = 256 + 5 * 64 * 1152
+def _abs_layout(blocks, rows, slots=1, header=256):
+    """Absorbed-path workspace: header, gathered rows, qlat, `slots` key splits of latent states and lse."""
+    want = header + blocks * 64 * 1152
     want = (want + 255) // 256 * 256 + rows * 512 * 2
-    want = (want + 255) // 256 * 256 + rows * 512 * 4
-    want = (want + 255) // 256 * 256 + rows * 4
-    assert n == (want + 255) // 256 * 256
+    want = (want + 255) // 256 * 256 + slots * rows * 512 * 4
+    want = (want + 255) // 256 * 256 + slots * rows * 4
+    return (want + 255) // 256 * 256
+
+
+def test_absorbed_entry_validates_and_sizes(lib):
+    # 1036 cached + 64 new tokens: every row sees >= 1024 keys, so the whole
+    # request takes the absorbed path; the workspace leads with an empty
+    # up-projected part (its 256-byte header, flags of one 8-head piece of 4-slot lanes)
+    sl, cq = (ctypes.c_int32 * 1)(1100), (ctypes.c_int32 * 2)(0, 64)
+    n = lib.mla_prefill_absorbed_workspace_size(1, sl, cq, 8, None, 0, 128, 3)
+    fused_part = 256 + 8 * 2 * 4 * 4
+    assert any(n == fused_part + _abs_layout(18, 64 * 8, k) for k in range(1, 5))   # the keys cut in 1-4 splits
     assert lib.mla_prefill_absorbed_workspace_size(1, sl, cq, 8, None, 0, 100, 3) == 0   # chunk not a multiple of 64
+    # 256 cached tokens: rows see fewer than 1024 keys, so the request takes the
+    # up-projected path (exact scores) and the absorbed part is empty
+    sl2 = (ctypes.c_int32 * 1)(320)
+    assert lib.mla_prefill_absorbed_workspace_size(1, sl2, cq, 8, None, 0, 128, 3) > _ws(lib, [320], [0, 64], 8, chunk=128)
 
 
 def test_fp8_score_and_reuse_workspaces(lib):
     """Host-side sizing of the FP8-score absorbed path and of head-split reuse."""
-    sl, cq = (ctypes.c_int32 * 1)(320), (ctypes.c_int32 * 2)(0, 64)
-    base = lib.mla_prefill_absorbed_workspace_size(1, sl, cq, 8, None, 0, 128, 3)
+    sl, cq = (ctypes.c_int32 * 1)(1100), (ctypes.c_int32 * 2)(0, 64)
     fp8 = lib.mla_prefill_absorbed_fp8_workspace_size(1, sl, cq, 8, None, 0, 128, 3)
     rows = 64 * 8
-    extra = (5 * 64 * 640 + 255) // 256 * 256 + (rows * 512 + 255) // 256 * 256 + (rows * 4 + 255) // 256 * 256
-    assert fp8 == base + extra          # the FP8 rows as stored, E4M3 qlat, its row scales
+    extra = (18 * 64 * 640 + 255) // 256 * 256 + (rows * 512 + 255) // 256 * 256 + (rows * 4 + 255) // 256 * 256
+    # the FP8 rows as stored, E4M3 qlat, its row scales
+    assert any(fp8 == _abs_layout(18, rows, k) + extra for k in range(1, 5))
 
+    sl, cq = (ctypes.c_int32 * 1)(320), (ctypes.c_int32 * 2)(0, 64)
     g = (ctypes.c_int32 * 2)(1, 5)
     none = lib.mla_prefill_reuse_workspace_size(1, sl, cq, 8, None, 0, 128, 3, g, 0, None)
     two = lib.mla_prefill_reuse_workspace_size(1, sl, cq, 8, None, 0, 128, 3, g, 2, None)

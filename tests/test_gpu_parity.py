@@ -1,19 +1,17 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
 same seeded inputs.
 
-Tolerances (bf16 inputs, fp32 accumulation): out max abs <= 2e-2 and mean abs
-<= 2e-3, lse within 1e-3, plus a stricter internal gate of relative RMS error
-<= 1e-2 on out.  Gather and block-table indexing are bit-exact.
+Tolerances (bf16 inputs, fp32 accumulation), on every row: out max abs
+<= 2e-2 and mean abs <= 2e-3, lse within 1e-3, plus a stricter internal gate
+of relative RMS error <= 1e-2 on out.  Gather and block-table indexing are
+bit-exact.
 
-lse and key count: the tensor cores take bf16 operands, so every score
-carries the rounding of K_nope (fp32 -> bf16 after the up-projection) and of the
-rotated q_rope.  For unit-variance scores that is ~1e-3 (one sigma) per score;
-lse averages it over the visible keys, and once a row sees >= 512 keys the
-error stays below ~7e-4 (measured by emulating exactly those roundings in
-numpy: the kernel matched the emulation to three digits).  Every row of the
-full-size workloads sees >= 1024 keys and is held to 1e-3.  Rows of the small
-edge cases that see fewer than 512 keys (down to a single key) are held to
-6e-3, six sigma of one score's rounding error.
+lse and key count: the tensor cores take bf16 operands, so a score built
+from the up-projected K_nope rounded to bf16 carries about 1.4e-3 (one sigma,
+unit-variance scores) of rounding; lse averages that over the visible keys.
+Rows that see fewer than 1024 keys in all (the small edge cases, down to a
+single key) therefore take exact scores in the kernel (K_nope as bf16 plus
+its bf16 residual) and are held to the same 1e-3 as every other row.
 """
 import math
 
@@ -27,7 +25,6 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 OUT_MAX, OUT_MEAN, LSE_MAX, REL_RMS = 2e-2, 2e-3, 1e-3, 1e-2
-LSE_MAX_FEW_KEYS, FEW_KEYS = 6e-3, 512
 
 
 @pytest.fixture(scope="module")
@@ -61,13 +58,11 @@ def assert_close(out, lse, ref_out, ref_lse, nvis=None):
     assert err.max() <= OUT_MAX, f"max abs {err.max():.3e}"
     assert err.mean() <= OUT_MEAN, f"mean abs {err.mean():.3e}"
     if fin.any():
-        tol = np.full(ref_lse.shape, LSE_MAX)
-        if nvis is not None:
-            nv = np.asarray(nvis).reshape(nvis.shape[0], *([1] * (ref_lse.ndim - 1)))
-            tol = np.where(np.broadcast_to(nv, ref_lse.shape) < FEW_KEYS, LSE_MAX_FEW_KEYS, LSE_MAX)
         le = np.abs(lse - ref_lse)
-        bad = fin & (le > tol)
-        assert not bad.any(), f"lse err {le[fin].max():.3e} (tol {tol[bad].min():.0e} at {np.argwhere(bad)[:3].tolist()})"
+        bad = fin & (le > LSE_MAX)
+        where = np.argwhere(bad)[:3].tolist()
+        seen = [int(np.asarray(nvis)[w[0]]) for w in where] if nvis is not None else None
+        assert not bad.any(), f"lse err {le[fin].max():.3e} (tol {LSE_MAX:.0e} at {where}, visible keys {seen})"
     den = math.sqrt(float((ref_out ** 2).mean())) or 1.0
     rel = math.sqrt(float((err ** 2).mean())) / den
     assert rel <= REL_RMS, f"rel rms {rel:.3e}"
@@ -319,17 +314,22 @@ def test_prefill_small_grid(api, case, monkeypatch):
 
 # ---------------------------------------------------------------- absorbed (latent-space) path
 
+# The absorbed path takes the requests whose rows all see >= 1024 keys; the
+# others (few keys: exact scores) go through the up-projected kernel in the
+# same call.  Contexts of >= 1023 tokens keep these cases on the latent kernel.
 ABSORBED_CASES = [
-    dict(H=4, ctx=[300], ext=[20], chunk=128),                        # ragged kv tail, one row tile
-    dict(H=2, ctx=[0], ext=[130], chunk=64),                          # no context, causal only
-    dict(H=3, ctx=[64, 0, 777], ext=[1, 64, 29], chunk=256),          # ragged batch
-    dict(H=2, ctx=[513], ext=[77], chunk=192, kv="fp8_e4m3"),         # FP8 cache
-    dict(H=2, ctx=[256], ext=[40], chunk=64, doc=64),                 # relocated documents
-    dict(H=128, ctx=[200], ext=[3], chunk=128),                       # full head count, 3 row tiles
+    dict(H=4, ctx=[1100], ext=[20], chunk=128),                       # ragged kv tail, one row tile
+    dict(H=2, ctx=[0], ext=[130], chunk=64),                          # no context, causal only (up-projected)
+    dict(H=3, ctx=[1088, 0, 1777], ext=[1, 64, 29], chunk=256),       # ragged batch, one request up-projected
+    dict(H=2, ctx=[1537], ext=[77], chunk=192, kv="fp8_e4m3"),        # FP8 cache
+    dict(H=2, ctx=[1280], ext=[40], chunk=64, doc=64),                # 20 relocated documents
+    dict(H=128, ctx=[1200], ext=[3], chunk=128),                      # full head count, 3 row tiles
 ]
 
 
 def test_absorbed_tiny(api):
+    """The tiny workload's rows see 257-320 keys: the absorbed entry point
+    takes them through the up-projected kernel (exact scores)."""
     run_and_compare(api, W.tiny(), absorbed=True)
 
 
@@ -347,19 +347,19 @@ def test_absorbed_small(api, case, split, monkeypatch):
 
 @pytest.mark.parametrize("parts", [1, 2])
 def test_absorbed_parts(api, parts):
-    wl = W.make_workload("ap", 2, [260], [50], chunk=128, seed=41)
+    wl = W.make_workload("ap", 2, [1060], [50], chunk=128, seed=41)
     run_and_compare(api, wl, parts=parts, absorbed=True)
 
 
 def test_absorbed_bf16_out(api):
-    wl = W.make_workload("ab", 2, [190], [70], chunk=128, seed=42)
+    wl = W.make_workload("ab", 2, [1090], [70], chunk=128, seed=42)
     run_and_compare(api, wl, out_dtype=torch.bfloat16, absorbed=True)
 
 
 def test_absorbed_matches_fused_path(api):
     """Both entry points compute the same function: their outputs agree to the
     rounding of their different bf16 operands."""
-    wl = W.make_workload("am", 8, [1000], [33], chunk=256, seed=43)
+    wl = W.make_workload("am", 8, [1500], [33], chunk=256, seed=43)
     dw = api.DeviceWorkload(wl)
     o1, l1 = dw.run()
     o2, l2 = dw.run(absorbed=True)
@@ -378,7 +378,7 @@ def test_absorbed_long_context_sampled(api):
 
 def test_absorbed_bad_block_and_workspace(api):
     from mla_prefix_cache_gb300 import _lib
-    wl = W.make_workload("ae", 2, [256], [16], chunk=128, seed=45)
+    wl = W.make_workload("ae", 2, [1100], [16], chunk=128, seed=45)
     dw = api.DeviceWorkload(wl)
     dw.block_table[0, 1] = -5
     out, lse = dw.run(absorbed=True)
@@ -510,9 +510,9 @@ def test_prefill_reuse_reports_bad_blocks(api):
 # ---------------------------------------------------------------- edge cases of the extra entry points
 
 @pytest.mark.parametrize("case", [
-    dict(H=1, ctx=[300], ext=[45], chunk=128),                 # one head
+    dict(H=1, ctx=[1100], ext=[45], chunk=128),                # one head
     dict(H=4, ctx=[0], ext=[1], chunk=64),                     # a single query with no context: itself only
-    dict(H=3, ctx=[100, 64, 0], ext=[0, 5, 0], chunk=64),      # requests without queries in the batch
+    dict(H=3, ctx=[100, 1088, 0], ext=[0, 5, 0], chunk=64),    # requests without queries in the batch
 ])
 @pytest.mark.parametrize("absorbed", [False, True], ids=["fused", "absorbed"])
 def test_prefill_degenerate_shapes(api, case, absorbed):
@@ -639,13 +639,14 @@ def test_absorbed_fp8_scores_needs_fp8_cache(api):
 # ---------------------------------------------------------------- per-request dispatch
 
 @pytest.mark.parametrize("case", [
-    dict(H=4, ctx=[300, 500, 64, 0, 200], ext=[5, 300, 64, 129, 1], chunk=128),   # both paths, interleaved
-    dict(H=3, ctx=[256, 128], ext=[200, 40], chunk=64, doc=64),                   # relocated documents
-    dict(H=2, ctx=[513, 64], ext=[160, 7], chunk=192, kv="fp8_e4m3"),            # FP8 cache
-    dict(H=4, ctx=[300], ext=[20], chunk=128),                                    # absorbed only
-    dict(H=4, ctx=[300], ext=[200], chunk=128),                                   # up-projected only
-    dict(H=2, ctx=[200, 100], ext=[96, 97], chunk=128),                           # either side of the threshold
-], ids=["mixed", "docs", "fp8", "short_only", "long_only", "threshold"])
+    dict(H=4, ctx=[1300, 500, 1064, 0, 1200], ext=[5, 300, 64, 129, 1], chunk=128),   # both paths, interleaved
+    dict(H=3, ctx=[256, 1280], ext=[200, 40], chunk=64, doc=64),                     # relocated documents
+    dict(H=2, ctx=[1537, 64], ext=[160, 7], chunk=192, kv="fp8_e4m3"),              # FP8 cache
+    dict(H=4, ctx=[1300], ext=[20], chunk=128),                                      # absorbed only
+    dict(H=4, ctx=[300], ext=[200], chunk=128),                                      # up-projected only
+    dict(H=2, ctx=[1200, 1100], ext=[96, 97], chunk=128),                            # either side of the threshold
+    dict(H=2, ctx=[1022, 1023], ext=[8, 8], chunk=128),                              # either side of 1024 keys
+], ids=["mixed", "docs", "fp8", "short_only", "long_only", "threshold", "few_keys"])
 def test_prefill_auto_matches_oracle(api, case):
     wl = W.make_workload("au", case["H"], case["ctx"], case["ext"], chunk=case["chunk"],
                          kv_dtype=case.get("kv", "bf16"), doc_len=case.get("doc"), seed=95)
@@ -653,7 +654,7 @@ def test_prefill_auto_matches_oracle(api, case):
 
 
 def test_prefill_auto_reports_bad_blocks_of_either_path(api):
-    wl = W.make_workload("ab2", 2, [256, 256], [16, 200], chunk=128, seed=96)
+    wl = W.make_workload("ab2", 2, [1100, 256], [16, 200], chunk=128, seed=96)
     for req in (0, 1):                 # request 0: absorbed path, request 1: up-projected
         dw = api.DeviceWorkload(wl)
         dw.block_table[req, 1] = -5
