@@ -27,7 +27,7 @@
 //    those rows of O in TMEM before the tile's PV.
 // Each CTA loads its own 64-key stages (the S side latent + k_rope, the O
 // side latent only) and frees a stage as soon as its own MMA has read it: a
-// stage shared by multicast would stay busy from its load until the O side's
+// stage loaded once for both CTAs would stay busy from its load until the O side's
 // PV, a chain that three stages cannot cover.  The rows are read by every row
 // tile of the piece and stay in L2.
 #include "internal.h"
