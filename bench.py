@@ -461,6 +461,58 @@ def absorbed_compare(dev, flush, peak, source, reps=10, config="short_ext_32k", 
             "path": "absorbed_fp8" if fp8_scores else "absorbed"}
 
 
+def fp8w_compare(dev, flush, peak, source, reps=5, config="fp8_128k"):
+    """The FP8 cache workload through mla_prefill_ctx (bf16 up-projection of
+    the dequantised rows) and mla_prefill_ctx_fp8w (E4M3 rows as stored times
+    an E4M3 copy of kv_b_proj on the FP8 tensor cores): median CUDA-event time
+    of a whole call (L2 flushed before each) and of the fused kernel; the
+    E4M3 copy of kv_b_proj is made once, outside the timing (a model constant)."""
+    import torch
+    from mla_prefix_cache_gb300 import api, workload
+
+    wl = workload.by_name(config)
+    dw = api.DeviceWorkload(wl, dev)
+    T_q, H = wl.total_q, wl.num_heads
+    out = torch.empty((T_q, H, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
+    w_scale = api.kv_b_proj_absmax(dw.kv_b_proj) / 448.0
+    w8 = api.kv_b_proj_to_e4m3(dw.kv_b_proj, w_scale)
+    ws = torch.empty(api.prefill_workspace_size(wl.seq_lens, wl.cu_q, H, wl.segments, wl.chunk),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for fp8w in (False, True):
+        kw = dict(kv_b_proj_e4m3=w8, w_scale=w_scale) if fp8w else {}
+        for _ in range(3):
+            flush.zero_()
+            dw.run(out=out, lse=lse, workspace=ws, **kw)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for k in range(reps):
+            flush.zero_()
+            torch.cuda.synchronize(dev)
+            api.set_kernel_events(*kev[k])
+            ev[k][0].record(stream)
+            dw.run(out=out, lse=lse, workspace=ws, **kw)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        api.set_kernel_events(None, None)
+        if api.device_error(ws) != 0:
+            raise RuntimeError("device error word set in the FP8 up-projection comparison")
+        res[fp8w] = (float(statistics.median([a.elapsed_time(b) for a, b in ev])),
+                     float(statistics.median([a.elapsed_time(b) for a, b in kev])))
+    (ms_b, kms_b), (ms_8, kms_8) = res[False], res[True]
+    flops = wl.algorithmic_flops()
+    del ws, w8
+    torch.cuda.empty_cache()
+    return {"workload": config, "ms_bf16_proj": ms_b, "ms_fp8_proj": ms_8, "speedup": ms_b / ms_8,
+            "kernel_ms_bf16_proj": kms_b, "kernel_ms_fp8_proj": kms_8,
+            "tflops_fp8_proj": flops / (ms_8 / 1e3) / 1e12,
+            "kernel_frac_fp8_proj": flops / (kms_8 / 1e3) / 1e12 / peak,
+            "note": "algorithmic FLOPs over the kernel time against the bf16 peak; the up-projection "
+                    "(9% of the FLOPs here) runs on E4M3 tensor cores"}
+
+
 def auto_compare(dev, flush, reps=5, config="mixed_32k"):
     """Per-request dispatch against the up-projected path alone, on a mixed
     batch of long and short requests: median CUDA-event time of a whole call,
@@ -771,6 +823,9 @@ def run_ours(args):
     if not args.no_absorbed and world == 1 and not absorbed:
         cmp_abs = absorbed_compare(dev, flush, peak, source)
         cmp_abs8 = absorbed_compare(dev, flush, peak, source, reps=5, config="short_ext_fp8_128k", fp8_scores=True)
+    cmp_fp8w = None
+    if not args.no_fp8w and world == 1 and not absorbed:
+        cmp_fp8w = fp8w_compare(dev, flush, peak, source)
     cmp_reuse = cmp_auto = None
     if not args.no_reuse and world == 1:
         cmp_reuse = reuse_compare(dev, flush)
@@ -797,6 +852,7 @@ def run_ours(args):
         "absorbed_fp8": cmp_abs8,
         "reuse": cmp_reuse,
         "auto": cmp_auto,
+        "fp8w": cmp_fp8w,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": res["clocks"],
@@ -822,6 +878,8 @@ def main(argv=None):
                     help="skip the absorbed-vs-fused comparison on the short-extend workload")
     ap.add_argument("--no-auto", action="store_true",
                     help="skip the per-request dispatch comparison on the mixed batch")
+    ap.add_argument("--no-fp8w", action="store_true",
+                    help="skip the FP8 up-projection comparison on fp8_128k (mla_prefill_ctx_fp8w)")
     ap.add_argument("--no-reuse", action="store_true",
                     help="skip the head-split reuse comparison (16 Global heads, 10% protected rows on v3_8k)")
     ap.add_argument("--no-e2e", action="store_true")

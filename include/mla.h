@@ -159,6 +159,49 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos,
                     void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * mla_prefill_ctx_fp8w -- mla_prefill_ctx for an FP8 cache with the
+ * up-projection on the FP8 tensor cores ("DeepSeek MLA — Prefix Cache 与
+ * Chunked Prefill 深度解析", section 2.2, the FP8 cache; heading only there):
+ * the cache's E4M3 codes are read as stored (640-byte rows, no bf16
+ * dequantisation pass) and multiplied on tcgen05 kind::f8f6f4 by an E4M3 copy
+ * of kv_b_proj; the fp32 products are scaled by kv_scale * w_scale.  The
+ * attention that follows is that of mla_prefill_ctx (bf16 operands, exact
+ * scores for rows with few keys).
+ * The result is mla_prefill_ctx's with kv_b_proj replaced by
+ * e4m3(kv_b_proj / w_scale) * w_scale: the weights' E4M3 rounding (relative
+ * error up to 2^-4) moves each up-projected K_nope and V value by about 3%
+ * RMS, which the softmax averages over the keys.
+ *  kv_b_proj_e4m3_t  device uint8 [H*256][512]: E4M3 codes of kv_b_proj / w_scale,
+ *                 transposed (row c holds column c's 512 latent weights), as
+ *                 mla_kv_b_proj_to_e4m3 writes them; 16-byte aligned.
+ *  w_scale        positive, finite (absmax / 448 uses the whole E4M3 range).
+ *  kv_dtype       must be MLA_KV_FP8_E4M3 (MLA_KV_BF16: MLA_ERR_UNSUPPORTED).
+ *  workspace      as mla_prefill_ctx (mla_prefill_workspace_size).
+ *  other arguments, errors  as mla_prefill_ctx.
+ * ---------------------------------------------------------------------- */
+int mla_prefill_ctx_fp8w(const void* q, const int32_t* q_pos,
+                         const void* kv_cache, int kv_dtype, float kv_scale, int num_blocks,
+                         const int32_t* block_table, int max_blocks_per_req,
+                         const int32_t* seq_lens, const int32_t* cu_q, int num_reqs, int num_heads,
+                         const mla_segment* segments, int num_segments, int chunk,
+                         const void* kv_b_proj_e4m3_t, float w_scale,
+                         float softmax_scale, float rope_theta, int parts,
+                         void* out, int out_dtype, float* lse,
+                         void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* The E4M3 copy of kv_b_proj for mla_prefill_ctx_fp8w, made once per model.
+ * mla_kv_b_proj_absmax: *absmax (device fp32) = max |w| over the bf16
+ *   kv_b_proj [512, H*256] (one CTA; asynchronous on `stream`).
+ * mla_kv_b_proj_to_e4m3: out_e4m3_t[c][k] = e4m3(kv_b_proj[k][c] / w_scale),
+ *   rounded to nearest even and saturated to +-448, for c < H*256, k < 512.
+ *   out_e4m3_t: device uint8 [H*256][512].
+ * Errors: MLA_ERR_INVALID_ARG (null pointer, H outside [1, 128], w_scale not
+ * positive and finite), MLA_ERR_CUDA. */
+int mla_kv_b_proj_absmax(const void* kv_b_proj, int num_heads, float* absmax, mla_stream_t stream);
+int mla_kv_b_proj_to_e4m3(const void* kv_b_proj, int num_heads, float w_scale, void* out_e4m3_t,
+                          mla_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * mla_prefill_ctx_noalloc -- mla_prefill_ctx for callers that cannot allocate
  * device memory.  (No section of the pages has a counterpart: this is an
  * integration entry point.)

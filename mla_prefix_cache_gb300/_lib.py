@@ -61,6 +61,11 @@ SIGNATURES = {
     "mla_prefill_ctx_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_float, c_int, c_void_p, c_int,
                                         i32p, i32p, c_int, c_int, segp, c_int, c_int, c_void_p, c_float, c_float,
                                         c_int, c_void_p, c_int, c_void_p, c_void_p]),
+    "mla_prefill_ctx_fp8w": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_float, c_int, c_void_p, c_int,
+                                     i32p, i32p, c_int, c_int, segp, c_int, c_int, c_void_p, c_float, c_float,
+                                     c_float, c_int, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "mla_kv_b_proj_absmax": (c_int, [c_void_p, c_int, c_void_p, c_void_p]),
+    "mla_kv_b_proj_to_e4m3": (c_int, [c_void_p, c_int, c_float, c_void_p, c_void_p]),
     "mla_prefill_absorbed_workspace_size": (c_size_t, [c_int, i32p, i32p, c_int, segp, c_int, c_int, c_int]),
     "mla_prefill_ctx_absorbed": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_float, c_int, c_void_p, c_int,
                                          i32p, i32p, c_int, c_int, segp, c_int, c_int, c_void_p, c_float, c_float,

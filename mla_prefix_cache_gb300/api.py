@@ -103,12 +103,16 @@ def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_
             rope_theta: float = 10000.0, kv_scale: float = 1.0, segments=None, parts: int = PART_ALL,
             out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
             lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-            stream: Optional[torch.cuda.Stream] = None, absorbed=False) -> Tuple[torch.Tensor, torch.Tensor]:
+            stream: Optional[torch.cuda.Stream] = None, absorbed=False,
+            kv_b_proj_e4m3: Optional[torch.Tensor] = None, w_scale: Optional[float] = None
+            ) -> Tuple[torch.Tensor, torch.Tensor]:
     """MLA chunked prefill of one layer (mla_prefill_ctx; absorbed=True:
     mla_prefill_ctx_absorbed, the same result computed in latent space;
     absorbed="fp8": mla_prefill_ctx_absorbed_fp8, FP8 caches, latent scores
     on the FP8 tensor cores; absorbed="auto": mla_prefill_ctx_auto, the path
-    chosen per request by its number of queries).
+    chosen per request by its number of queries).  With kv_b_proj_e4m3 (uint8
+    [H*256, 512], see kv_b_proj_to_e4m3) and w_scale: mla_prefill_ctx_fp8w,
+    FP8 caches, the up-projection on the FP8 tensor cores.
 
     q bf16 [T_q, H, 192] (q_rope unrotated); q_pos int32 [T_q]; kv_cache bf16
     [NB,64,576] or uint8 [NB,64,640] (FP8); block_table int32 [B, max_blocks];
@@ -130,6 +134,9 @@ def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_
         lse = torch.empty((T_q, H), dtype=torch.float32, device=dev)
     fp8 = absorbed == "fp8"
     auto = absorbed == "auto"
+    fp8w = kv_b_proj_e4m3 is not None
+    if fp8w and (absorbed or w_scale is None):
+        raise ValueError("kv_b_proj_e4m3 takes w_scale and the up-projected path")
     if workspace is None:
         if absorbed:
             ws_bytes = absorbed_workspace_size(keep_sl, keep_cq, H, segments, chunk, parts,
@@ -138,21 +145,47 @@ def prefill(q: torch.Tensor, q_pos: torch.Tensor, kv_cache: torch.Tensor, block_
             ws_bytes = prefill_workspace_size(keep_sl, keep_cq, H, segments, chunk, parts)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_FP32
-    name = ("mla_prefill_ctx_auto" if auto else "mla_prefill_ctx_absorbed_fp8" if fp8
-            else "mla_prefill_ctx_absorbed" if absorbed else "mla_prefill_ctx")
-    fn = getattr(L, name)
-    st = fn(
-        _dev(q, "q", torch.bfloat16), _dev(q_pos, "q_pos", torch.int32), _dev(kv_cache, "kv_cache"),
-        kv_dtype_code(kv_cache), float(kv_scale), int(kv_cache.shape[0]),
-        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
-        sl, cq, B, H, sp, ns, int(chunk), _dev(kv_b_proj, "kv_b_proj", torch.bfloat16),
-        float(softmax_scale), float(rope_theta), int(parts),
-        _dev(out, "out", (torch.float32, torch.bfloat16)), od, _dev(lse, "lse", torch.float32),
-        _dev(workspace, "workspace"), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
-        _stream_ptr(stream))
+    common = (_dev(q, "q", torch.bfloat16), _dev(q_pos, "q_pos", torch.int32), _dev(kv_cache, "kv_cache"),
+              kv_dtype_code(kv_cache), float(kv_scale), int(kv_cache.shape[0]),
+              _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+              sl, cq, B, H, sp, ns, int(chunk))
+    tail = (float(softmax_scale), float(rope_theta), int(parts),
+            _dev(out, "out", (torch.float32, torch.bfloat16)), od, _dev(lse, "lse", torch.float32),
+            _dev(workspace, "workspace"), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+            _stream_ptr(stream))
+    if fp8w:
+        name = "mla_prefill_ctx_fp8w"
+        st = L.mla_prefill_ctx_fp8w(*common, _dev(kv_b_proj_e4m3, "kv_b_proj_e4m3", torch.uint8), float(w_scale),
+                                    *tail)
+    else:
+        name = ("mla_prefill_ctx_auto" if auto else "mla_prefill_ctx_absorbed_fp8" if fp8
+                else "mla_prefill_ctx_absorbed" if absorbed else "mla_prefill_ctx")
+        st = getattr(L, name)(*common, _dev(kv_b_proj, "kv_b_proj", torch.bfloat16), *tail)
     _lib.check(name, st)
     prefill.last_workspace = workspace
     return out, lse
+
+
+def kv_b_proj_absmax(kv_b_proj: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> float:
+    """The largest |w| of a bf16 kv_b_proj [512, H*256] (mla_kv_b_proj_absmax; synchronises)."""
+    H = int(kv_b_proj.shape[1]) // 256
+    out = torch.empty(1, dtype=torch.float32, device=kv_b_proj.device)
+    _lib.check("mla_kv_b_proj_absmax", _lib.load().mla_kv_b_proj_absmax(
+        _dev(kv_b_proj, "kv_b_proj", torch.bfloat16), H, _dev(out, "absmax"), _stream_ptr(stream)))
+    return float(out.item())
+
+
+def kv_b_proj_to_e4m3(kv_b_proj: torch.Tensor, w_scale: float, out: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """E4M3 codes of kv_b_proj / w_scale, transposed: uint8 [H*256, 512]
+    (mla_kv_b_proj_to_e4m3).  w_scale = absmax / 448 uses the whole range."""
+    cols = int(kv_b_proj.shape[1])
+    if out is None:
+        out = torch.empty((cols, 512), dtype=torch.uint8, device=kv_b_proj.device)
+    _lib.check("mla_kv_b_proj_to_e4m3", _lib.load().mla_kv_b_proj_to_e4m3(
+        _dev(kv_b_proj, "kv_b_proj", torch.bfloat16), cols // 256, float(w_scale), _dev(out, "out", torch.uint8),
+        _stream_ptr(stream)))
+    return out
 
 
 def _protected_host(protected_rows, T_q: int):

@@ -487,7 +487,8 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
                          int num_blocks, const int32_t* block_table, int max_blocks, int num_heads,
                          const void* kv_b_proj, float softmax_scale, float rope_theta, void* out, int out_dtype,
                          float* lse, void* workspace, const FusedPlan& fp, const FusedWs& fw, cudaStream_t s,
-                         const int32_t* q_tok = nullptr, bool keep_err = false) {
+                         const int32_t* q_tok = nullptr, bool keep_err = false, const void* w8 = nullptr,
+                         float w_scale = 1.f) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int H = num_heads;
   const int64_t T_q = fp.total_q;
@@ -497,18 +498,33 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   std::memset(&p, 0, sizeof(p));
 
   const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const bool fp8w = w8 != nullptr;   // FP8 up-projection: E4M3 rows as stored and the E4M3 kv_b_proj copy
   // The gather pass first copies every block the requests use, in logical
   // order, into the workspace (FP8 rows as exact bf16(e4m3), without the
-  // scale, which is applied to the fp32 up-projection accumulators), so the
-  // kernel reads each request's rows contiguously: one 256-row box per
-  // k-slice of a producer pass, one 128-row (or two 64-row, when paired) box
-  // of k_rope per consumer tile.
+  // scale, which is applied to the fp32 up-projection accumulators; with the
+  // FP8 up-projection, the 640-byte rows as stored), so the kernel reads each
+  // request's rows contiguously: one 128-row box per k-slice of a producer
+  // CTA's pass, one 64-row box of k_rope per consumer CTA and tile.
   const void* rows_base = static_cast<const void*>(ws + fw.gath_off);
   const uint64_t rows_total = (uint64_t)std::max(fp.gather_blocks, 1) * kBlock;
   bool ok = true;
   p.q_bf16 = static_cast<const uint16_t*>(q);
   p.q_tok = q_tok;
-  {
+  if (fp8w) {
+    // the 640-byte rows: codes as bytes (one 128-code k-slice of 128 rows a box), k_rope as bf16 [rows][320]
+    const uint64_t d[2] = {(uint64_t)kRowBytesFp8, rows_total};
+    const uint64_t st[1] = {(uint64_t)kRowBytesFp8};
+    const uint32_t b[2] = {128, 128};
+    ok &= encode_map(&p.tm_c8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, rows_base, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint64_t d2[2] = {(uint64_t)kRowBytesFp8 / 2, rows_total};
+    const uint32_t b2[2] = {64, 64};
+    ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d2, st, b2, CU_TENSOR_MAP_SWIZZLE_128B);
+    // E4M3 kv_b_proj transposed [H*256][512]: 128 columns x one 128-code k-slice a box
+    const uint64_t dw[2] = {(uint64_t)kDc, (uint64_t)H * (kDnope + kDv)};
+    const uint64_t sw[1] = {(uint64_t)kDc};
+    ok &= encode_map(&p.tm_w8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, w8, dw, sw, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    p.krope_col = kRowBytesFp8 / 2 - kDr;   // 256
+  } else {
     const uint64_t d[2] = {(uint64_t)kRowBf16, rows_total};
     const uint64_t st[1] = {(uint64_t)kRowBytesBf16};
     const uint32_t b64[2] = {64, 64}, b128[2] = {64, 128}, b256[2] = {64, 256};
@@ -516,13 +532,12 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
     ok &= encode_map(&p.tm_kr128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d, st, b128,
                      CU_TENSOR_MAP_SWIZZLE_128B);
     ok &= encode_map(&p.tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d, st, b256, CU_TENSOR_MAP_SWIZZLE_128B);
-  }
-  {
     // kv_b_proj [512][H*256] seen as 64-column blocks: (col in block, latent row, block)
-    const uint64_t d[3] = {64, (uint64_t)kDc, (uint64_t)H * (kDnope + kDv) / 64};
-    const uint64_t st[2] = {(uint64_t)H * (kDnope + kDv) * 2, 128};
-    const uint32_t b[3] = {64, 64, 2};
-    ok &= encode_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_b_proj, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint64_t dw[3] = {64, (uint64_t)kDc, (uint64_t)H * (kDnope + kDv) / 64};
+    const uint64_t sw[2] = {(uint64_t)H * (kDnope + kDv) * 2, 128};
+    const uint32_t bw[3] = {64, 64, 2};
+    ok &= encode_map(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_b_proj, dw, sw, bw, CU_TENSOR_MAP_SWIZZLE_128B);
+    p.krope_col = kDc;
   }
   {
     // ring lanes: per lane and slot four contiguous [128 x 64] blocks K_nope cols 0-63, 64-127, V cols 0-63,
@@ -579,7 +594,8 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   p.num_blocks = num_blocks;
   p.num_heads = H;
   p.out_bf16 = out_dtype == MLA_OUT_BF16;
-  p.out_scale = fp8 ? kv_scale : 1.f;
+  p.out_scale = fp8w ? kv_scale * w_scale : (fp8 ? kv_scale : 1.f);
+  p.fp8w = fp8w ? 1 : 0;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   rope_fracs((double)rope_theta, p.rope_frac);
 
@@ -609,8 +625,9 @@ static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cac
   // error word + role queue (keep_err: a caller running several sub-calls keeps the error word)
   st = keep_err ? cuda_status(cudaMemsetAsync(err + 1, 0, 256 - 4, s)) : cuda_status(cudaMemsetAsync(err, 0, 256, s));
   if (st != MLA_OK) return st;
-  if ((st = gather_rows(fp, kv_cache, fp8, num_blocks, block_table, max_blocks, ws + fw.gath_off, err, s)) != MLA_OK)
-    return st;
+  st = fp8w ? gather_rows_raw(fp, kv_cache, num_blocks, block_table, max_blocks, ws + fw.gath_off, err, s)
+            : gather_rows(fp, kv_cache, fp8, num_blocks, block_table, max_blocks, ws + fw.gath_off, err, s);
+  if (st != MLA_OK) return st;
 
   cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
   cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
@@ -1257,6 +1274,44 @@ int mla_prefill_ctx(const void* q, const int32_t* q_pos, const void* kv_cache, i
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return prefill_fused(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req, num_heads,
                          kv_b_proj, softmax_scale, rope_theta, out, out_dtype, lse, workspace, fplan, fw, s);
+}
+
+int mla_prefill_ctx_fp8w(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
+                         int num_blocks, const int32_t* block_table, int max_blocks_per_req, const int32_t* seq_lens,
+                         const int32_t* cu_q, int num_reqs, int num_heads, const mla_segment* segments,
+                         int num_segments, int chunk, const void* kv_b_proj_e4m3_t, float w_scale,
+                         float softmax_scale, float rope_theta, int parts, void* out, int out_dtype, float* lse,
+                         void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  if (kv_dtype != MLA_KV_FP8_E4M3) return kv_dtype == MLA_KV_BF16 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (!(std::isfinite(w_scale) && w_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  Plan plan;
+  FusedPlan fplan;
+  const int st = prefill_plans(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,
+                               seq_lens, cu_q, num_reqs, num_heads, segments, num_segments, chunk, kv_b_proj_e4m3_t,
+                               softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
+  if (st != MLA_OK || plan.total_q == 0) return st;
+  const FusedWs fw = fused_ws_fitting(fplan, num_heads, workspace_bytes);
+  if (workspace == nullptr || !aligned(workspace, 256) || fw.pieces_per_launch < 1) return MLA_ERR_WORKSPACE;
+  return prefill_fused(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req, num_heads,
+                       nullptr, softmax_scale, rope_theta, out, out_dtype, lse, workspace, fplan, fw,
+                       reinterpret_cast<cudaStream_t>(stream), nullptr, false, kv_b_proj_e4m3_t, w_scale);
+}
+
+int mla_kv_b_proj_absmax(const void* kv_b_proj, int num_heads, float* absmax, mla_stream_t stream) {
+  if (kv_b_proj == nullptr || absmax == nullptr || num_heads < 1 || num_heads > kMaxHeads) return MLA_ERR_INVALID_ARG;
+  if (!aligned(kv_b_proj, 16)) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_absmax_bf16(static_cast<const uint16_t*>(kv_b_proj),
+                                        (int64_t)kDc * num_heads * (kDnope + kDv), absmax,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mla_kv_b_proj_to_e4m3(const void* kv_b_proj, int num_heads, float w_scale, void* out_e4m3_t,
+                          mla_stream_t stream) {
+  if (kv_b_proj == nullptr || out_e4m3_t == nullptr || num_heads < 1 || num_heads > kMaxHeads)
+    return MLA_ERR_INVALID_ARG;
+  if (!(std::isfinite(w_scale) && w_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_t(static_cast<const uint16_t*>(kv_b_proj), num_heads * (kDnope + kDv), w_scale,
+                                       static_cast<uint8_t*>(out_e4m3_t), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int mla_prefill_ctx_noalloc(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,

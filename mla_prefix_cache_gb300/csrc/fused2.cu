@@ -91,6 +91,7 @@ constexpr uint32_t kTmAcc = 0;            // producer: accumulator b at 256 b
 constexpr uint32_t kIdescS = idesc_bf16(256, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(256, 128, false, true);
 constexpr uint32_t kIdescUp = idesc_bf16(256, 256, false, true);
+constexpr uint32_t kIdescUp8 = idesc_e4m3(256, 256);   // FP8 up-projection: E4M3 rows x E4M3 kv_b_proj, K-major
 
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays <= 256
 
@@ -214,7 +215,7 @@ __device__ void run_consumer(const FusedParams& p, const Job& J, int job, int k,
           if (leader) mbar_arrive_expect_tx(full, 2 * kKStageBytes);     // both halves land on the leader's count
           const int kt0 = J.t0 + 128 * j;
           tma_load_3d_pair_hint(st, &p.tm_ring64, 0, 64 * (int)rank, zb, full_leader, pol_ring);       // K_nope lo | hi
-          tma_load_2d_pair(st + 2 * kAtom64, &p.tm_kr, kDc, block_row(J, (kt0 >> 6) + (int)rank), full_leader);
+          tma_load_2d_pair(st + 2 * kAtom64, &p.tm_kr, p.krope_col, block_row(J, (kt0 >> 6) + (int)rank), full_leader);
           trace_stage(p, role, j, 0);
         } else {
           const uint32_t st = sbase + kVBase + s * kVStageBytes;
@@ -606,7 +607,7 @@ __device__ __forceinline__ void store_residual(uint32_t acc, float oscale, bool 
 // rows through the stages (waiting for each to be free), 9 MMA (leader), 0-7
 // conversion: warpgroup 0 the K_nope columns, warpgroup 1 the V columns of the
 // CTA's tile, stored from registers into the ring.
-template <bool kCompute, bool kExact>
+template <bool kCompute, bool kExact, bool kFp8W>
 __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi, int role, uint32_t sbase,
                              uint32_t tmem, volatile Ctl* ctl, uint32_t rank) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -617,6 +618,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
   int my_passes = 0;
   for (int pp = pi; pp < n_pass; pp += J.n_prod) ++my_passes;
   if (my_passes == 0) return;
+  constexpr int kSlices = kFp8W ? kDc / 128 : kDc / 64;   // k-slices (stages) of a pass
 
   if constexpr (!kCompute) {
     if (warp == 10) {
@@ -624,11 +626,19 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
       if (lane != 0) return;
       const uint32_t full = bar_addr(sbase, kBWFull);
       const uint32_t full_leader = mapa_shared(full, 0u);
-      if (leader) mbar_arrive_expect_tx(full, 2 * 8 * kAtomQ);
-      const int blk = rank == 0 ? 2 * h : (H * kDnope + h * kDv) / 64;
       const uint64_t pol = policy_stream(p);
-      for (int kx = 0; kx < kDc / 64; ++kx)
-        tma_load_3d_pair_hint(sbase + kPWBase + kx * kAtomQ, &p.tm_w, 0, 64 * kx, blk, full_leader, pol);
+      if constexpr (kFp8W) {
+        // E4M3 columns, K-major (the transposed copy [H*256][512]): 4 k-slices of [128 columns x 128 B]
+        if (leader) mbar_arrive_expect_tx(full, 2 * 4 * kAtomQ);
+        const int wrow = rank == 0 ? h * kDnope : H * kDnope + h * kDv;
+        for (int kx = 0; kx < kDc / 128; ++kx)
+          tma_load_2d_pair_hint(sbase + kPWBase + kx * kAtomQ, &p.tm_w8, 128 * kx, wrow, full_leader, pol);
+      } else {
+        if (leader) mbar_arrive_expect_tx(full, 2 * 8 * kAtomQ);
+        const int blk = rank == 0 ? 2 * h : (H * kDnope + h * kDv) / 64;
+        for (int kx = 0; kx < kDc / 64; ++kx)
+          tma_load_3d_pair_hint(sbase + kPWBase + kx * kAtomQ, &p.tm_w, 0, 64 * kx, blk, full_leader, pol);
+      }
       trace_stage(p, role, 0, 7);
       // This CTA writes tile t = 2 pass + rank of each pass into ring slot
       // t mod depth of lane job mod ring_lanes.  On the first lap the lane's
@@ -671,7 +681,8 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
           ctl->abort = 1;
           return;
         }
-        for (int kx = 0; kx < kDc / 64; ++kx, ++g) {
+        // a stage is one k-slice of the pass's rows: 64 bf16 values, or 128 E4M3 codes, of 128 tokens
+        for (int kx = 0; kx < kSlices; ++kx, ++g) {
           const int s = g % kPStages;
           if (g >= kPStages && !wait_bar(p, bar_addr(sbase, kBProdEmpty + s), ((g / kPStages) - 1) & 1)) {
             ctl->abort = 1;
@@ -679,7 +690,10 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
           }
           const uint32_t full = bar_addr(sbase, kBProdFull + s);
           if (leader) mbar_arrive_expect_tx(full, 2 * kPStageBytes);     // both CTAs' rows
-          tma_load_2d_pair(sbase + kPCBase + s * kPStageBytes, &p.tm_kr128, 64 * kx, row0, mapa_shared(full, 0u));
+          if constexpr (kFp8W)
+            tma_load_2d_pair(sbase + kPCBase + s * kPStageBytes, &p.tm_c8, 128 * kx, row0, mapa_shared(full, 0u));
+          else
+            tma_load_2d_pair(sbase + kPCBase + s * kPStageBytes, &p.tm_kr128, 64 * kx, row0, mapa_shared(full, 0u));
           if (kx == 0) trace_stage(p, role, n, 6);
         }
       }
@@ -701,7 +715,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
         tr_acc.end(p, wa);
         trace_stage(p, role, n, 0);
         tc_fence_after();
-        for (int kx = 0; kx < kDc / 64; ++kx, ++g) {
+        for (int kx = 0; kx < kSlices; ++kx, ++g) {
           const int s = g % kPStages;
           const uint64_t w0 = tr_op.begin(p);
           if (!wait_bar(p, bar_addr(sbase, kBProdFull + s), (g / kPStages) & 1)) { ctl->abort = 1; return; }
@@ -709,10 +723,18 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
           tc_fence_after();
           const uint32_t st = sbase + kPCBase + s * kPStageBytes;
           const uint32_t wst = sbase + kPWBase + kx * kAtomQ;
+          if constexpr (kFp8W) {
+            // K = 32 E4M3 values (32 bytes) per MMA, both operands K-major
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma2_ss(tmem + kTmAcc + 256 * b, sdesc_sw128(st + kk * 32, 16, 1024),
-                    sdesc_sw128(wst + kk * 2048, kAtom64, 1024), kIdescUp, (kx | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              mma2_ss_e4m3(tmem + kTmAcc + 256 * b, sdesc_sw128(st + kk * 32, 16, 1024),
+                           sdesc_sw128(wst + kk * 32, 16, 1024), kIdescUp8, (kx | kk) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma2_ss(tmem + kTmAcc + 256 * b, sdesc_sw128(st + kk * 32, 16, 1024),
+                      sdesc_sw128(wst + kk * 2048, kAtom64, 1024), kIdescUp, (kx | kk) ? 1u : 0u);
+          }
           mma2_commit_both(bar_addr(sbase, kBProdEmpty + s));
         }
         mma2_commit_both(bar_addr(sbase, kBAccFull + b));
@@ -817,7 +839,7 @@ __device__ void run_producer(const FusedParams& p, const Job& J, int job, int pi
 // control warps (8-11).  Cluster rank 0 takes the next role from the queue
 // and writes it into both CTAs; every exit decision is made there, so both
 // CTAs run the same sequence of cluster barriers.
-template <bool kCompute, bool kExact>
+template <bool kCompute, bool kExact, bool kFp8W>
 __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, uint8_t* sgen, volatile Ctl* ctl,
                                           uint32_t tmem, uint32_t rank) {
   const int tid = threadIdx.x;
@@ -888,7 +910,7 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
       trace_put(p, slot, 2, ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)producer << 31) | (unsigned)job);
     }
     if (!ctl->abort && !(producer && job == p.withhold_job)) {
-      if (producer) run_producer<kCompute, kExact>(p, J, job, idx, slot, sbase, tmem, ctl, rank);
+      if (producer) run_producer<kCompute, kExact, kFp8W>(p, J, job, idx, slot, sbase, tmem, ctl, rank);
       else run_consumer<kCompute, kExact>(p, J, job, idx, slot, sbase, sgen, tmem, ctl, rank);
     }
     tc_fence_before();
@@ -901,7 +923,9 @@ __device__ __forceinline__ void role_loop(const FusedParams& p, uint32_t sbase, 
 // kExact: some job of the launch has query rows that see fewer than
 // kExactKeys keys (exact scores for them); the launches without such rows run
 // the instantiation that has none of that code.
-template <bool kExact>
+// kFp8W: the up-projection takes the cache's E4M3 codes as stored and an E4M3
+// copy of kv_b_proj on the FP8 tensor cores.
+template <bool kExact, bool kFp8W>
 __global__ void __launch_bounds__(kThreads, 1) fused2_prefill_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -913,8 +937,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused2_prefill_kernel(const __gri
 
   if (tid == 0) {
     prefetch_tensormap(&p.tm_kr);
-    prefetch_tensormap(&p.tm_kr128);
-    prefetch_tensormap(&p.tm_w);
+    if (kFp8W) {
+      prefetch_tensormap(&p.tm_c8);
+      prefetch_tensormap(&p.tm_w8);
+    } else {
+      prefetch_tensormap(&p.tm_kr128);
+      prefetch_tensormap(&p.tm_w);
+    }
     prefetch_tensormap(&p.tm_ring);
     prefetch_tensormap(&p.tm_ring1);
     prefetch_tensormap(&p.tm_ring64);
@@ -940,10 +969,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused2_prefill_kernel(const __gri
   // warpgroups 0 and 1 take 56 more each (256 x 56): the same total.
   if ((tid >> 5) >= 8) {
     setmaxnreg_dec<56>();
-    role_loop<false, kExact>(p, sbase, sgen, ctl, tmem, rank);
+    role_loop<false, kExact, kFp8W>(p, sbase, sgen, ctl, tmem, rank);
   } else {
     setmaxnreg_inc<224>();
-    role_loop<true, kExact>(p, sbase, sgen, ctl, tmem, rank);
+    role_loop<true, kExact, kFp8W>(p, sbase, sgen, ctl, tmem, rank);
   }
   tc_fence_before();
   cluster_sync_all();   // neither CTA releases TMEM while the pair's MMAs could still use it
@@ -957,10 +986,17 @@ int fused2_smem_bytes() { return (int)kSmemBytes; }
 static cudaError_t configure2(int dev) {
   static int configured_device = -1;
   if (configured_device == dev) return cudaSuccess;
-  cudaError_t e =
-      cudaFuncSetAttribute(fused2_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(fused2_prefill_kernel<false, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused2_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    e = cudaFuncSetAttribute(fused2_prefill_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused2_prefill_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused2_prefill_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
   if (e == cudaSuccess) configured_device = dev;
   return e;
 }
@@ -991,8 +1027,12 @@ cudaError_t launch_fused2(const FusedParams& p, int grid, cudaStream_t s) {
   cluster_config(&cfg, attr, grid, s);
   bool exact = false;
   for (int i = 0; i < p.n_pieces; ++i) exact |= p.pieces[i].exact != 0;
-  e = exact ? cudaLaunchKernelEx(&cfg, fused2_prefill_kernel<true>, p)
-            : cudaLaunchKernelEx(&cfg, fused2_prefill_kernel<false>, p);
+  if (p.fp8w)
+    e = exact ? cudaLaunchKernelEx(&cfg, fused2_prefill_kernel<true, true>, p)
+              : cudaLaunchKernelEx(&cfg, fused2_prefill_kernel<false, true>, p);
+  else
+    e = exact ? cudaLaunchKernelEx(&cfg, fused2_prefill_kernel<true, false>, p)
+              : cudaLaunchKernelEx(&cfg, fused2_prefill_kernel<false, false>, p);
   count_launch();
   return e;
 }
@@ -1007,7 +1047,7 @@ cudaError_t fused2_grid_size(int* grid) {
   cudaLaunchAttribute attr[1];
   cluster_config(&cfg, attr, 2 * ((sms + 1) / 2), nullptr);
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, fused2_prefill_kernel<false>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, fused2_prefill_kernel<false, false>, &cfg);
   if (e != cudaSuccess) return e;
   *grid = 2 * clusters;
   return *grid > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;

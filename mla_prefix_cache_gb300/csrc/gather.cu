@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(kGatherThreads, 2) gather_blocks_kernel(const 
 
 // The FP8 rows of every block, as stored (640 B: 512 E4M3 codes, then k_rope
 // as bf16), in the same logical order as gather_blocks_kernel; slots past a
-// request's length and blocks with a bad id are zeroed.
+// request's length and blocks with a bad id are zeroed, and a bad id of a
+// block the request uses sets the error word.
 __global__ void __launch_bounds__(kGatherThreads, 2) gather_blocks_raw_kernel(const __grid_constant__ GatherBlocksParams p) {
   constexpr int kChunks = kBlock * kRowBytesFp8 / 16;   // 2560 per block
   constexpr int kRowChunks = kRowBytesFp8 / 16;         // 40
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(kGatherThreads, 2) gather_blocks_raw_kernel(co
     const int lb = gb - rq.base_block;
     const int blk = (lb < p.max_blocks) ? __ldg(p.block_table + (int64_t)rq.req * p.max_blocks + lb) : -1;
     const bool ok = (blk >= 0 && blk < p.num_blocks);
+    if (!ok && threadIdx.x == 0 && lb * kBlock < rq.seq_len && p.err != nullptr) atomicOr(p.err, kErrBadBlock);
     const int live_rows = min(kBlock, rq.seq_len - lb * kBlock);
     const uint4* src = reinterpret_cast<const uint4*>(p.cache + (int64_t)(ok ? blk : 0) * kBlock * kRowBytesFp8);
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dst) + (int64_t)gb * kBlock * kRowBytesFp8);

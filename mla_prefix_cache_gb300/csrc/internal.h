@@ -111,6 +111,8 @@ struct FusedParams {
   CUtensorMap tm_q;      // q as (column, head, row) of [T_q][H][192], box 64 x 1 x 128: 128 rows of one head
   CUtensorMap tm_out;    // out as (column, head, row) of [T_q][H][128], box 32 (fp32) or 64 (bf16) x 1 x 128
   CUtensorMap tm_part;   // partial states, fp32 [slots * T_q][H][128], box 32 x 1 x 128
+  CUtensorMap tm_c8;     // FP8 up-projection: gathered 640-byte rows as bytes, box 128 B x 128 rows (E4M3 codes)
+  CUtensorMap tm_w8;     // FP8 up-projection: E4M3 kv_b_proj transposed [H*256][512], box 128 B x 128 rows
   const uint16_t* q_bf16;  // q [T_q][H][192]
   const int32_t* q_tok;    // optional [T_q]: token index of each query row within its request (rows that are
                            // a sorted subset of the request's queries); nullptr: q_tok0 + row - q_begin
@@ -138,6 +140,8 @@ struct FusedParams {
   int prod_ahead;       // heads by which a job's producers precede their consumers in the queue
   uint64_t wait_limit_ns;   // bound of every wait of the kernel (a timeout sets kErrTimeout)
   int l2_hints;         // 1: ring tiles evict_last, streamed data evict_first; 0: evict_normal
+  int fp8w;             // 1: FP8 up-projection (E4M3 rows and kv_b_proj on kind::f8f6f4)
+  int krope_col;        // element column of k_rope in the gathered rows seen as bf16 (512, or 256 for 640-byte rows)
   int withhold_job;     // test hook: this job's producer roles do nothing, so its consumers' waits run
                         // out (-1: none)
   unsigned long long* trace;   // optional, kTraceWords per role slot (group * 2 + cluster rank; see fused_common.cuh)
@@ -306,6 +310,11 @@ cudaError_t launch_gather_q(const uint16_t* q, const int32_t* q_pos, const int32
 cudaError_t launch_gather_w(const uint16_t* w, const int32_t* heads, int n_heads, int H, uint16_t* w_sub,
                             cudaStream_t s);
 cudaError_t launch_reuse_assemble(const ReuseAssemble& p, cudaStream_t s);
+
+// E4M3 copy of kv_b_proj (quant.cu): the largest |x| of n bf16 values into
+// *out (device), and out[c][k] = e4m3(w[k][c] / scale) of the [512][cols] matrix.
+cudaError_t launch_absmax_bf16(const uint16_t* x, int64_t n, float* out, cudaStream_t s);
+cudaError_t launch_quantize_t(const uint16_t* w, int cols, float scale, uint8_t* out, cudaStream_t s);
 
 void count_launch(int n = 1);
 

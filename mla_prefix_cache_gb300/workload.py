@@ -63,6 +63,18 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def kv_b_proj_e4m3_t(kv_b_proj: np.ndarray, w_scale: float) -> np.ndarray:
+    """E4M3 codes of a bf16 kv_b_proj [512, H*256] (bit patterns) divided by
+    w_scale, saturated to +-448 and rounded to nearest even by the library
+    encoder, transposed to [H*256, 512] (the layout the FP8 up-projection
+    reads)."""
+    import torch  # library e4m3 encoder (CPU); only used to build inputs
+    w = (np.ascontiguousarray(kv_b_proj).astype(np.uint32) << 16).view(np.float32)
+    x = np.clip(w / np.float32(w_scale), np.float32(-448.0), np.float32(448.0)).astype(np.float32)
+    codes = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return np.ascontiguousarray(codes.T)
+
+
 @dataclasses.dataclass
 class Workload:
     """All inputs of one prefill call (host copies)."""

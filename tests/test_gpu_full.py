@@ -1,8 +1,8 @@
 """Full-size parity on the four large workloads, in the launch configuration the
 bench times: the GPU computes every (row, head); the CPU oracle recomputes a
-sample of rows (first and last of every request, q-tile boundaries, random
-rows) for a few heads, and properties that hold at any size are checked on the
-whole output."""
+sample of rows (first and last of every request, every query-tile boundary,
+random rows) for 8 heads spread over the role queue, and properties that hold
+at any size are checked on the whole output."""
 import numpy as np
 import pytest
 
@@ -16,15 +16,23 @@ pytestmark = pytest.mark.gpu
 
 
 def sample_rows(wl, rng, n_random=24):
+    """First and last row of every request, both rows at every 128-row query
+    tile boundary (a consumer CTA's tile; pairs of tiles are a consumer
+    pair's), and random rows."""
     cu = wl.cu_q
     rows = set()
     for r in range(wl.num_reqs):
         a, b = int(cu[r]), int(cu[r + 1])
-        for x in (a, a + 1, a + 127, a + 128, b - 1):
-            if a <= x < b:
-                rows.add(x)
+        rows.update((a, a + 1, b - 1))
+        for x in range(a + 128, b, 128):
+            rows.update((x - 1, x))
     rows.update(rng.integers(0, wl.total_q, size=n_random).tolist())
-    return np.array(sorted(rows))
+    return np.array(sorted(x for x in rows if 0 <= x < wl.total_q))
+
+
+# heads spread over the role queue: the first and last ones, the producers'
+# lookahead boundary (heads 0-2), and the middle of the queue
+SAMPLED_HEADS = [0, 1, 2, 63, 64, 125, 126, 127]
 
 
 @pytest.mark.parametrize("name", ["v3_8k", "batched", "fp8_128k", "reloc_256k"])
@@ -38,7 +46,7 @@ def test_full_size_sampled(name):
     assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all())
     rng = np.random.default_rng(100)
     rows = sample_rows(wl, rng)
-    heads = [0, int(rng.integers(1, wl.num_heads - 1)), wl.num_heads - 1]
+    heads = SAMPLED_HEADS
     ref_out, ref_lse = O.mla_prefill(**O.workload_args(wl), rows=rows, heads=heads)
     got_out = out[torch.from_numpy(rows).cuda()][:, heads].cpu().numpy()
     got_lse = lse[torch.from_numpy(rows).cuda()][:, heads].cpu().numpy()

@@ -661,3 +661,76 @@ def test_prefill_auto_reports_bad_blocks_of_either_path(api):
         dw.run(absorbed="auto")
         torch.cuda.synchronize()
         assert api.device_error(api.prefill.last_workspace) == 3
+
+
+# ---------------------------------------------------------------- FP8 up-projection (E4M3 kv_b_proj)
+
+def _pow2_scale(amax):
+    """The power of two >= amax / 448: e4m3 values times it are exact bf16."""
+    return float(2.0 ** math.ceil(math.log2(amax / 448.0)))
+
+
+def test_kv_b_proj_e4m3_bit_exact(api):
+    """The device quantizer against the host encoder: absmax exact, codes
+    bit-exact (round to nearest even, saturation at 448 included: the scale is
+    absmax / 448, so the largest weights land on or next to 448)."""
+    wl = W.make_workload("q8", 8, [64], [1], seed=60)
+    dw = api.DeviceWorkload(wl)
+    w = (wl.kv_b_proj.astype(np.uint32) << 16).view(np.float32)
+    amax = float(np.abs(w).max())
+    assert api.kv_b_proj_absmax(dw.kv_b_proj) == amax
+    scale = float(np.float32(amax / 448.0))
+    got = api.kv_b_proj_to_e4m3(dw.kv_b_proj, scale).cpu().numpy()
+    assert got.shape == (8 * 256, 512)
+    assert np.array_equal(got, W.kv_b_proj_e4m3_t(wl.kv_b_proj, scale))
+
+
+FP8W_CASES = [
+    dict(H=4, ctx=[513], ext=[200], chunk=192),                 # ragged kv and q tails, rows with few keys
+    dict(H=3, ctx=[1100, 0, 1777], ext=[1, 64, 129], chunk=256),   # ragged batch
+    dict(H=2, ctx=[1280], ext=[40], chunk=64, doc=64),          # relocated documents, partial states + merge
+    dict(H=128, ctx=[1200], ext=[130], chunk=128),              # full head count
+]
+
+
+@pytest.mark.parametrize("case", FP8W_CASES, ids=["ragged", "batch", "docs", "h128"])
+def test_prefill_fp8w_matches_oracle(api, case):
+    """mla_prefill_ctx_fp8w computes mla_prefill_ctx with kv_b_proj replaced by
+    its E4M3 rounding: against the oracle on those weights it is held to the
+    same bars as mla_prefill_ctx (a power-of-two scale makes the rounded
+    weights exact bf16, so the oracle takes them unchanged).  Against the
+    oracle on the unrounded weights it moves by the weights' rounding
+    (checked loosely: relative RMS of out <= 0.1, lse within 0.15)."""
+    wl = W.make_workload("w8", case["H"], case["ctx"], case["ext"], chunk=case["chunk"], kv_dtype="fp8_e4m3",
+                         doc_len=case.get("doc"), seed=61)
+    w = (wl.kv_b_proj.astype(np.uint32) << 16).view(np.float32)
+    scale = _pow2_scale(float(np.abs(w).max()))
+    codes = W.kv_b_proj_e4m3_t(wl.kv_b_proj, scale)
+    w_q = W.f32_to_bf16_bits(np.ascontiguousarray(O.e4m3_to_float(codes).T) * np.float32(scale))
+    dw = api.DeviceWorkload(wl)
+    out, lse = dw.run(kv_b_proj_e4m3=torch.from_numpy(codes).cuda(), w_scale=scale)
+    torch.cuda.synchronize()
+    assert api.device_error(api.prefill.last_workspace) == 0
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    args = O.workload_args(wl)
+    args["kv_b_proj"] = w_q
+    ref_out, ref_lse = O.mla_prefill(**args)
+    assert_close(out, lse, ref_out, ref_lse, visible_keys(wl))
+    raw_out, raw_lse = O.mla_prefill(**O.workload_args(wl))
+    rel = math.sqrt(float(((out - raw_out) ** 2).mean())) / math.sqrt(float((raw_out ** 2).mean()))
+    assert rel <= 0.1 and float(np.abs(lse - raw_lse).max()) <= 0.15
+
+
+def test_prefill_fp8w_reports_bad_block_and_needs_fp8_cache(api):
+    from mla_prefix_cache_gb300 import _lib
+    wl = W.make_workload("w8e", 2, [256], [16], chunk=128, kv_dtype="fp8_e4m3", seed=62)
+    dw = api.DeviceWorkload(wl)
+    codes = torch.from_numpy(W.kv_b_proj_e4m3_t(wl.kv_b_proj, 1.0 / 1024)).cuda()
+    dw.block_table[0, 1] = -5
+    out, lse = dw.run(kv_b_proj_e4m3=codes, w_scale=1.0 / 1024)
+    torch.cuda.synchronize()
+    assert api.device_error(api.prefill.last_workspace) == 3    # MLA_ERR_BAD_BLOCK_ID
+    assert torch.isfinite(out).all()
+    wb = W.make_workload("w8b", 2, [256], [16], chunk=128, seed=62)
+    with pytest.raises(_lib.MLAError):
+        api.DeviceWorkload(wb).run(kv_b_proj_e4m3=codes, w_scale=1.0 / 1024)
