@@ -1,181 +1,259 @@
 // Paged latent gather, _gather_cache of "DeepSeek MLA — Prefix Cache 与 Chunked
-// Prefill 深度解析", section 4.4 step 1: the rows of logical tokens
-// [start, start+len) of one request, found through its block-table row (token t
-// in block table[t/64], slot t%64; 64-token blocks per "PagedAttention assumed
-// MHA. DeepSeek-V4 says that assumption is broken"), written contiguously as
-// 576 bf16 values [c_kv | k_rope] (section 5.2 row layout).
+// Prefill 深度解析", section 4.4 step 1: the rows of logical tokens of a
+// request, found through its block-table row (token t in block table[t/64],
+// slot t%64; 64-token blocks per "PagedAttention assumed MHA. DeepSeek-V4 says
+// that assumption is broken"), written contiguously ([c_kv | k_rope] rows,
+// section 5.2).
 //
-// BF16 rows are copied bit-exactly.  FP8 rows (512 E4M3FN bytes + 64 bf16) are
-// dequantised to bf16(e4m3 * scale), rounded to nearest even.
+// The copy is driven by the bulk-copy (TMA) engine.  A destination tile is 64
+// rows; its rows come from at most two cache blocks, and each block's share is
+// one contiguous range of rows, so a tile is one or two cp.async.bulk loads
+// into a shared-memory stage.  BF16 rows (and FP8 rows copied as stored) go
+// from the stage straight back out by one cp.async.bulk store; FP8 rows to be
+// dequantised are converted by the CTA's threads from the stage and stored to
+// global memory in 512-byte warp stores (bf16(e4m3 * scale), round to nearest
+// even; k_rope copied).  Each CTA is persistent over its tiles, one thread
+// keeping the loads of the next stages (3 of 72 KB, or 5 of 40 KB) in flight.
 //
-// Work is cut into tiles of 64 destination rows (72 KB of bf16 output).  One
-// 256-thread CTA moves a tile: thread i owns chunks i, i+256, ..., i+17*256 of
-// the tile's 4608 16-byte output chunks, issues all 18 loads before any store
-// (about 73 KB in flight per CTA, which is what keeps HBM busy), and
-// consecutive threads touch consecutive chunks, so every warp access is 512
-// contiguous bytes.
+// Two callers: mla_gather_latent (one request's token range, any start) and
+// the fused path's pass over every block of its requests in logical order
+// (whole 64-row tiles, rows past a request's length zeroed: a kernel that reads
+// whole blocks multiplies them by zero weights, which must stay zero).  Rows
+// of a bad block id are zeroed and set the error word.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kChunksPerRow = kRowBytesBf16 / 16;  // 72
-constexpr int kGatherThreads = 256;
-constexpr int kChunksPerThread = kBlock * kChunksPerRow / kGatherThreads;  // 18
-static_assert(kChunksPerThread * kGatherThreads == kBlock * kChunksPerRow, "tile split");
+// kMode 0: bf16 rows copied; 1: FP8 rows dequantised to bf16; 2: FP8 rows copied as stored.
+template <int kMode>
+struct Cfg {
+  static constexpr int kSrcRow = kMode == 0 ? kRowBytesBf16 : kRowBytesFp8;
+  static constexpr int kDstRow = kMode == 1 ? kRowBytesBf16 : kSrcRow;
+  static constexpr int kInStages = kMode == 0 ? 3 : 5;
+  static constexpr int kOutBufs = 0;
+  static constexpr int kCtasPerSm = 1;
+  static constexpr int kThreads = kMode == 1 ? 1024 : 256;   // the dequantisation takes every warp the SM has
+  static constexpr uint32_t kInBytes = kBlock * kSrcRow;
+  static constexpr uint32_t kOutBytes = kBlock * kDstRow;
+  static constexpr uint32_t kSmem = kInStages * kInBytes + kOutBufs * kOutBytes;
+  static_assert(kSmem + 64 <= 232448, "shared memory");
+};
 
-// Chunk c (0..71) of a cache row: BF16 rows are 72 chunks of 16 bytes; an FP8
-// row's chunk c < 64 is 8 e4m3 bytes (expanded to 16 bytes of bf16 later) and
-// chunk c >= 64 is 16 bytes of its bf16 k_rope.
-__device__ __forceinline__ uint4 load_chunk(const uint8_t* row, int c, int fp8) {
-  if (!fp8) return __ldg(reinterpret_cast<const uint4*>(row) + c);
-  if (c < 64) {
-    const uint2 b = __ldg(reinterpret_cast<const uint2*>(row) + c);
-    return make_uint4(b.x, b.y, 0u, 0u);
+// One destination tile: rows [0, rows) of it are written; rows of segment g
+// ([row0, row0 + n) of the tile) come from block blk, slots slot0.. ; the
+// others (a bad block id, past a request's length) are zero.
+struct Tile {
+  int blk[2], slot0[2], row0[2], n[2];
+  int rows;
+  int64_t dst_row;
+};
+
+__device__ __forceinline__ bool valid_block(int blk, int num_blocks) { return blk >= 0 && blk < num_blocks; }
+
+// Tokens [start, start + len) of one request (mla_gather_latent).
+struct RangeSrc {
+  const int32_t* table;
+  int start, len;
+  __device__ int tiles() const { return (len + kBlock - 1) / kBlock; }
+  __device__ Tile tile(int i) const {
+    Tile t;
+    const int g0 = i * kBlock;
+    t.rows = min(kBlock, len - g0);
+    t.dst_row = g0;
+    const int t0 = start + g0;
+    const int lb = t0 >> 6, s0 = t0 & (kBlock - 1);
+    t.blk[0] = __ldg(table + lb);
+    t.slot0[0] = s0;
+    t.row0[0] = 0;
+    t.n[0] = min(kBlock - s0, t.rows);
+    t.n[1] = t.rows - t.n[0];
+    t.blk[1] = t.n[1] > 0 ? __ldg(table + lb + 1) : -1;
+    t.slot0[1] = 0;
+    t.row0[1] = t.n[0];
+    return t;
   }
-  return __ldg(reinterpret_cast<const uint4*>(row + kDc) + (c - 64));
-}
+};
 
-__device__ __forceinline__ uint4 finish_chunk(uint4 v, int c, int fp8, float scale) {
-  if (!fp8 || c >= 64) return v;
-  return make_uint4(e4m3x2_scaled_bf16x2(v.x, scale), e4m3x2_scaled_bf16x2(v.x >> 16, scale),
-                    e4m3x2_scaled_bf16x2(v.y, scale), e4m3x2_scaled_bf16x2(v.y >> 16, scale));
-}
+// Every block of several requests, in logical order (the fused path's pass);
+// passed by value, so the request list sits in the kernel's parameter space.
+struct BlocksSrc {
+  GatherBlocksParams p;
+  __device__ int tiles() const { return p.total_blocks; }
+  __device__ Tile tile(int gb) const {
+    int lo = 0, hi = p.n_reqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.reqs[mid].base_block <= gb) lo = mid; else hi = mid - 1;
+    }
+    const GatherReq rq = p.reqs[lo];
+    const int lb = gb - rq.base_block;
+    Tile t;
+    t.rows = kBlock;
+    t.dst_row = (int64_t)gb * kBlock;
+    t.blk[0] = lb < p.max_blocks ? __ldg(p.block_table + (int64_t)rq.req * p.max_blocks + lb) : -1;
+    t.slot0[0] = 0;
+    t.row0[0] = 0;
+    t.n[0] = max(0, min(kBlock, rq.seq_len - lb * kBlock));
+    t.blk[1] = -1;
+    t.slot0[1] = t.row0[1] = t.n[1] = 0;
+    return t;
+  }
+};
 
-// Tokens [start, start+len) of one request.  The tile's rows may straddle two
-// cache blocks, so each chunk looks up its own block (the table row is cached).
-__global__ void __launch_bounds__(kGatherThreads, 2) gather_kernel(const uint8_t* __restrict__ cache, int fp8,
-                                                                   float scale, int num_blocks,
-                                                                   const int32_t* __restrict__ table, int start,
-                                                                   int len, uint16_t* __restrict__ dst,
-                                                                   uint32_t* err) {
-  const int64_t row_bytes = fp8 ? kRowBytesFp8 : kRowBytesBf16;
-  const int tiles = (len + kBlock - 1) / kBlock;
-  for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-    uint4 v[kChunksPerThread];
-    bool ok[kChunksPerThread];
+template <int kMode>
+__device__ __forceinline__ void issue_tile(const Tile& t, const uint8_t* cache, int num_blocks, uint32_t stage,
+                                           uint32_t bar) {
+  using C = Cfg<kMode>;
+  uint32_t bytes = 0;
 #pragma unroll
-    for (int j = 0; j < kChunksPerThread; ++j) {
-      const int k = threadIdx.x + j * kGatherThreads;
-      const int r = k / kChunksPerRow, c = k - r * kChunksPerRow;
-      const int g = tile * kBlock + r;
-      v[j] = make_uint4(0u, 0u, 0u, 0u);
-      ok[j] = false;
-      if (g < len) {
-        const int t = start + g;
-        const int blk = __ldg(table + (t >> 6));
-        ok[j] = (blk >= 0 && blk < num_blocks);
-        if (ok[j]) v[j] = load_chunk(cache + ((int64_t)blk * kBlock + (t & 63)) * row_bytes, c, fp8);
-        else if (c == 0 && err != nullptr) atomicOr(err, kErrBadBlock);
+  for (int g = 0; g < 2; ++g)
+    if (t.n[g] > 0 && valid_block(t.blk[g], num_blocks)) bytes += (uint32_t)t.n[g] * C::kSrcRow;
+  if (bytes == 0) {
+    mbar_arrive(bar);
+    return;
+  }
+  mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+    if (t.n[g] > 0 && valid_block(t.blk[g], num_blocks))
+      bulk_load(stage + (uint32_t)t.row0[g] * C::kSrcRow,
+                cache + ((int64_t)t.blk[g] * kBlock + t.slot0[g]) * C::kSrcRow, (uint32_t)t.n[g] * C::kSrcRow, bar);
+}
+
+// Whether tile row r is read from the cache (else it is written as zeros).
+__device__ __forceinline__ bool row_loaded(const Tile& t, int r, int num_blocks) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+    if (r >= t.row0[g] && r < t.row0[g] + t.n[g]) return valid_block(t.blk[g], num_blocks);
+  return false;
+}
+
+template <int kMode, class Src>
+__global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
+    gather_tma_kernel(const __grid_constant__ Src src, const uint8_t* __restrict__ cache, int num_blocks, float scale,
+                      uint8_t* dst, uint32_t* err) {
+  using C = Cfg<kMode>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[C::kInStages];
+  const int tid = threadIdx.x;
+  const int n_tiles = src.tiles();
+  const int mine = n_tiles > (int)blockIdx.x ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const uint32_t sb = smem_u32(smem), bb = smem_u32(bars);
+  if (tid == 0) {
+    for (int s = 0; s < C::kInStages; ++s) mbar_init(bb + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int k = 0; k < C::kInStages && k < mine; ++k)
+      issue_tile<kMode>(src.tile(blockIdx.x + k * gridDim.x), cache, num_blocks, sb + k * C::kInBytes, bb + 8 * k);
+  bool landed = true;
+  for (int k = 0; k < mine; ++k) {
+    const int s = k % C::kInStages;
+    const uint32_t stage = sb + s * C::kInBytes;
+    const Tile t = src.tile(blockIdx.x + k * gridDim.x);
+    landed &= mbar_wait(bb + 8 * s, (k / C::kInStages) & 1);
+    if (tid == 0 && err != nullptr) {
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+        if (t.n[g] > 0 && !valid_block(t.blk[g], num_blocks)) atomicOr(err, kErrBadBlock);
+    }
+    if constexpr (kMode == 1) {
+      // dequantised from the stage straight to global memory: each warp store
+      // is 512 contiguous bytes of the destination rows
+      constexpr int kRowChunks = kRowBytesBf16 / 16;   // 72 output chunks of 16 bytes a row
+      uint4* out = reinterpret_cast<uint4*>(dst + t.dst_row * kRowBytesBf16);
+      for (int q = tid; q < t.rows * kRowChunks; q += C::kThreads) {
+        const int r = q / kRowChunks, c = q - r * kRowChunks;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (row_loaded(t, r, num_blocks)) {
+          const uint32_t row = stage + (uint32_t)r * kRowBytesFp8;
+          if (c < kDc / 8) {
+            const uint2 b = lds64(row + 8 * c);
+            w[0] = e4m3x2_scaled_bf16x2(b.x, scale);
+            w[1] = e4m3x2_scaled_bf16x2(b.x >> 16, scale);
+            w[2] = e4m3x2_scaled_bf16x2(b.y, scale);
+            w[3] = e4m3x2_scaled_bf16x2(b.y >> 16, scale);
+          } else {
+            lds128(row + kDc + 16 * (c - kDc / 8), w);
+          }
+        }
+        out[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      __syncthreads();   // every thread is done with the stage
+      if (tid == 0 && k + C::kInStages < mine)
+        issue_tile<kMode>(src.tile(blockIdx.x + (k + C::kInStages) * gridDim.x), cache, num_blocks, stage,
+                          bb + 8 * s);
+    } else {
+      // rows not loaded are zeroed in the stage itself, which is then stored as it is
+      constexpr int kRowChunks = C::kSrcRow / 16;
+      for (int q = tid; q < kBlock * kRowChunks; q += C::kThreads) {
+        const int r = q / kRowChunks;
+        if (r < t.rows && !row_loaded(t, r, num_blocks)) sts128(stage + 16 * q, 0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();   // the threads' shared-memory writes, to the bulk store
+      __syncthreads();
+      if (tid == 0) {
+        bulk_store(dst + t.dst_row * C::kDstRow, stage, (uint32_t)t.rows * C::kDstRow);
+        bulk_commit();
+        if (k + C::kInStages < mine) {
+          bulk_wait_read0();   // the stage is free once its store has read it
+          issue_tile<kMode>(src.tile(blockIdx.x + (k + C::kInStages) * gridDim.x), cache, num_blocks, stage,
+                            bb + 8 * s);
+        }
       }
     }
-#pragma unroll
-    for (int j = 0; j < kChunksPerThread; ++j) {
-      const int k = threadIdx.x + j * kGatherThreads;
-      const int r = k / kChunksPerRow, c = k - r * kChunksPerRow;
-      const int g = tile * kBlock + r;
-      if (g < len)
-        reinterpret_cast<uint4*>(dst + (int64_t)g * kRowBf16)[c] = ok[j] ? finish_chunk(v[j], c, fp8, scale) : v[j];
-    }
   }
+  if (tid == 0) bulk_wait0();   // every store complete before the CTA's shared memory goes
+  if (!landed && err != nullptr) atomicOr(err, kErrTimeout);
 }
 
-// Every block of several requests into one contiguous bf16 buffer: request i's
-// logical block lb becomes rows (base_i + lb) * 64 .. +63 of dst.  A tile is
-// one destination block, so it reads one whole cache block (72 KB of BF16 or
-// 40 KB of FP8, contiguous in the pool) and the lookup is uniform over the CTA.
-__global__ void __launch_bounds__(kGatherThreads, 2) gather_blocks_kernel(const __grid_constant__ GatherBlocksParams p) {
-  const int64_t row_bytes = p.fp8 ? kRowBytesFp8 : kRowBytesBf16;
-  for (int gb = blockIdx.x; gb < p.total_blocks; gb += gridDim.x) {
-    int lo = 0, hi = p.n_reqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.reqs[mid].base_block <= gb) lo = mid; else hi = mid - 1;
-    }
-    const GatherReq rq = p.reqs[lo];
-    const int lb = gb - rq.base_block;
-    const int blk = (lb < p.max_blocks) ? __ldg(p.block_table + (int64_t)rq.req * p.max_blocks + lb) : -1;
-    const bool ok = (blk >= 0 && blk < p.num_blocks);
-    if (!ok && threadIdx.x == 0 && lb * kBlock < rq.seq_len) atomicOr(p.err, kErrBadBlock);
-    const uint8_t* src = p.cache + (int64_t)(ok ? blk : 0) * kBlock * row_bytes;
-    uint16_t* out = p.dst + (int64_t)gb * kBlock * kRowBf16;
-    // slots past the request's length are zeroed: a kernel that reads a
-    // whole block multiplies them by zero weights, which must stay zero
-    const int live_rows = min(kBlock, rq.seq_len - lb * kBlock);
-    uint4 v[kChunksPerThread];
-#pragma unroll
-    for (int j = 0; j < kChunksPerThread; ++j) {
-      const int k = threadIdx.x + j * kGatherThreads;
-      const int r = k / kChunksPerRow, c = k - r * kChunksPerRow;
-      v[j] = (ok && r < live_rows) ? load_chunk(src + r * row_bytes, c, p.fp8) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int j = 0; j < kChunksPerThread; ++j) {
-      const int k = threadIdx.x + j * kGatherThreads;
-      const int r = k / kChunksPerRow, c = k - r * kChunksPerRow;
-      reinterpret_cast<uint4*>(out)[k] = (ok && r < live_rows) ? finish_chunk(v[j], c, p.fp8, p.scale) : v[j];
-    }
-  }
-}
-
-// The FP8 rows of every block, as stored (640 B: 512 E4M3 codes, then k_rope
-// as bf16), in the same logical order as gather_blocks_kernel; slots past a
-// request's length and blocks with a bad id are zeroed, and a bad id of a
-// block the request uses sets the error word.
-__global__ void __launch_bounds__(kGatherThreads, 2) gather_blocks_raw_kernel(const __grid_constant__ GatherBlocksParams p) {
-  constexpr int kChunks = kBlock * kRowBytesFp8 / 16;   // 2560 per block
-  constexpr int kRowChunks = kRowBytesFp8 / 16;         // 40
-  for (int gb = blockIdx.x; gb < p.total_blocks; gb += gridDim.x) {
-    int lo = 0, hi = p.n_reqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.reqs[mid].base_block <= gb) lo = mid; else hi = mid - 1;
-    }
-    const GatherReq rq = p.reqs[lo];
-    const int lb = gb - rq.base_block;
-    const int blk = (lb < p.max_blocks) ? __ldg(p.block_table + (int64_t)rq.req * p.max_blocks + lb) : -1;
-    const bool ok = (blk >= 0 && blk < p.num_blocks);
-    if (!ok && threadIdx.x == 0 && lb * kBlock < rq.seq_len && p.err != nullptr) atomicOr(p.err, kErrBadBlock);
-    const int live_rows = min(kBlock, rq.seq_len - lb * kBlock);
-    const uint4* src = reinterpret_cast<const uint4*>(p.cache + (int64_t)(ok ? blk : 0) * kBlock * kRowBytesFp8);
-    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dst) + (int64_t)gb * kBlock * kRowBytesFp8);
-    for (int k = threadIdx.x; k < kChunks; k += kGatherThreads)
-      dst[k] = (ok && k / kRowChunks < live_rows) ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
-int gather_grid(int64_t tiles) {
+template <int kMode, class Src>
+cudaError_t launch_tma(const Src& src, int tiles, const uint8_t* cache, int num_blocks, float scale, uint8_t* dst,
+                       uint32_t* err, cudaStream_t s) {
+  if (tiles == 0) return cudaSuccess;
+  static int configured = -1;
   int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t cap = (int64_t)sms * 2;  // two resident CTAs per SM, each looping over tiles
-  return (int)(tiles < cap ? tiles : cap);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (configured != dev) {
+    e = cudaFuncSetAttribute(gather_tma_kernel<kMode, Src>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Cfg<kMode>::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = dev;
+  }
+  const int grid = tiles < sms * Cfg<kMode>::kCtasPerSm ? tiles : sms * Cfg<kMode>::kCtasPerSm;
+  gather_tma_kernel<kMode, Src><<<grid, Cfg<kMode>::kThreads, Cfg<kMode>::kSmem, s>>>(src, cache, num_blocks, scale,
+                                                                                    dst, err);
+  count_launch();
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gather_blocks(const GatherBlocksParams& p, cudaStream_t s) {
-  if (p.total_blocks == 0) return cudaSuccess;
-  gather_blocks_kernel<<<gather_grid(p.total_blocks), kGatherThreads, 0, s>>>(p);
-  count_launch();
-  return cudaGetLastError();
+  const BlocksSrc src{p};
+  return p.fp8 ? launch_tma<1>(src, p.total_blocks, p.cache, p.num_blocks, p.scale, reinterpret_cast<uint8_t*>(p.dst),
+                               p.err, s)
+               : launch_tma<0>(src, p.total_blocks, p.cache, p.num_blocks, 1.f, reinterpret_cast<uint8_t*>(p.dst),
+                               p.err, s);
 }
 
 cudaError_t launch_gather_blocks_raw(const GatherBlocksParams& p, cudaStream_t s) {
-  if (p.total_blocks == 0) return cudaSuccess;
-  gather_blocks_raw_kernel<<<gather_grid(p.total_blocks), kGatherThreads, 0, s>>>(p);
-  count_launch();
-  return cudaGetLastError();
+  const BlocksSrc src{p};
+  return launch_tma<2>(src, p.total_blocks, p.cache, p.num_blocks, 1.f, reinterpret_cast<uint8_t*>(p.dst), p.err, s);
 }
 
 cudaError_t launch_gather(const uint8_t* cache, int fp8, float scale, int num_blocks, const int32_t* table_row,
                           int max_blocks, int start, int len, uint16_t* dst, uint32_t* err, cudaStream_t s) {
   (void)max_blocks;
-  if (len == 0) return cudaSuccess;
-  gather_kernel<<<gather_grid((len + kBlock - 1) / kBlock), kGatherThreads, 0, s>>>(cache, fp8, scale, num_blocks,
-                                                                                      table_row, start, len, dst, err);
-  count_launch();
-  return cudaGetLastError();
+  const RangeSrc src{table_row, start, len};
+  const int tiles = (len + kBlock - 1) / kBlock;
+  return fp8 ? launch_tma<1>(src, tiles, cache, num_blocks, scale, reinterpret_cast<uint8_t*>(dst), err, s)
+             : launch_tma<0>(src, tiles, cache, num_blocks, 1.f, reinterpret_cast<uint8_t*>(dst), err, s);
 }
 
 }  // namespace mla
