@@ -89,11 +89,12 @@ typedef struct {
  *   with merge_attn_states (see mla_merge_states).
  * The up-projection runs on the tensor cores inside the persistent attention
  * kernel, once per (key, head).  Its bf16 K_nope/V tiles pass from producer to
- * consumer CTAs through a few K/V ring lanes in the workspace (4 to 12 lanes
- * of 128 slots of 128 keys, whatever the problem size, sized so that the
- * lanes hold about 32 MiB of tiles); the jobs of the call take turns on the
- * lanes, and the tiles are cached in L2 with an evict-last policy, so a lane's
- * lines are rewritten while they sit in the 126 MB L2: the up-projected K/V
+ * consumer CTAs through K/V ring lanes in the workspace (4 to 64 lanes of up
+ * to 128 slots of 128 keys, whatever the number of pieces: enough lanes for
+ * the jobs that run at once, and about 32 MiB of tiles when jobs have many
+ * queries); the jobs of the call take turns on the lanes, and the tiles are
+ * cached in L2 with an evict-last policy, so a lane's lines are rewritten
+ * while they sit in the 126 MB L2: with long extends the up-projected K/V
  * is not written back to HBM (measured on GB300 with 128 heads: the fused
  * kernel writes 100 MB per call on 8K + 2K tokens, where the output alone is
  * 134 MB, and 5.5 GB on 256K + 4K tokens, where the partial states of the 17
@@ -124,7 +125,7 @@ typedef struct {
  *               -inf for a row with no visible key (its out row is 0).
  *  workspace    device, 256-B aligned; mla_prefill_workspace_size(...) bytes
  *               lets the whole call run as one kernel launch at full speed:
- *               the K/V ring lanes (32 to 96 MiB), per-job ring flags, every block
+ *               the K/V ring lanes (up to 0.5 GiB), per-job ring flags, every block
  *               of the requests gathered in logical order as bf16 (1152 B per
  *               token; FP8 rows dequantised) and fp32 partial states
  *               (516 B per query row, head and piece of a request cut into

@@ -313,24 +313,32 @@ static int max_ring_depth() {
 // (measured best of 1-3); MLA_PRODUCER_LOOKAHEAD, at most 8.
 static int producer_lookahead() { return std::min(8, std::max(1, env_int("MLA_PRODUCER_LOOKAHEAD", 2))); }
 
-// Ring lanes: the up-projected tiles of the lanes stay in L2 while the lanes
-// hold about 32 MiB of tiles (measured on GB300: 4 lanes of 16384-key pieces
-// keep the fused kernel's DRAM traffic at its compulsory bytes, 6 lanes of
-// them write most tiles back), so the count is 32 MiB over the longest
-// piece's tiles, within [lookahead + 2, 12].  A producer waits for the lane's
-// previous job, so lanes > lookahead is needed (its consumers then precede
-// the producer in the queue), and one more lane keeps those waits short.
-// MLA_RING_LANES sets the count (at least lookahead + 1).
+// Ring lanes.  Two needs set the count:
+// - L2: the lanes' tiles stay in L2 while they hold about 32 MiB (measured on
+//   GB300: 4 lanes of 16384-key pieces keep the fused kernel's DRAM traffic at
+//   its compulsory bytes, 6 lanes of them write most tiles back), that is 32
+//   MiB over the longest piece's tiles;
+// - occupancy: about as many jobs as the grid's CTA pairs hold at once must
+//   have a lane, or pairs go idle: the 76 pairs of a GB300 over the fewest
+//   pairs (producers + consumers) a job has.  Jobs with few queries have few
+//   consumer pairs each, and their lanes then outnumber what L2 holds.
+// The count is the larger of the two, within [lookahead + 2, 64].  A producer
+// waits for the lane's previous job, so lanes > lookahead is needed (its
+// consumers then precede the producer in the queue), and one more lane keeps
+// those waits short.  MLA_RING_LANES sets the count (at least lookahead + 1).
 static int ring_lanes_cfg(const FusedPlan& fp, int depth) {
   const int ahead = producer_lookahead();
   const int forced = env_int("MLA_RING_LANES", 0);
   if (forced > 0) return std::max(ahead + 1, forced);
-  int max_tiles = 1;
-  for (const Piece& pc : fp.pieces)
+  int max_tiles = 1, min_pairs = 1 << 30;
+  for (const Piece& pc : fp.pieces) {
     max_tiles = std::max(max_tiles, (pc.k_end - (pc.k_begin & ~(kBlock - 1)) + 127) / 128);
+    min_pairs = std::min(min_pairs, std::max(1, (pc.n_prod + 1) / 2) + (pc.n_cons + 1) / 2);
+  }
   const size_t tile_bytes = (size_t)128 * 256 * sizeof(uint16_t);
   const int fit = (int)(((size_t)32 << 20) / (tile_bytes * (size_t)std::min(max_tiles, depth)));
-  return std::max(ahead + 2, std::min(kRingLanes, fit));
+  const int busy = fp.pieces.empty() ? 0 : kLanePairs / min_pairs;
+  return std::max(ahead + 2, std::min(kRingLanes, std::max(fit, busy)));
 }
 
 // The preferred layout: every piece in one launch (up to kMaxPieces), lanes

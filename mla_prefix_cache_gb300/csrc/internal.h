@@ -62,7 +62,8 @@ struct MergeParams {
 
 // ------------------------------------------------------------ fused persistent kernel
 constexpr int kRingDepth = 128;   // deepest ring lane: 128-token K/V tiles (8 MB); a small workspace gets less
-constexpr int kRingLanes = 12;    // most ring lanes the jobs of a launch take turns on
+constexpr int kRingLanes = 64;    // most ring lanes the jobs of a launch take turns on
+constexpr int kLanePairs = 76;    // CTA pairs of a GB300's persistent grid (152 SMs), for the lane count
 constexpr int kMaxPieces = 448;   // pieces per launch (kernel-parameter budget)
 
 // One key range of one request attended with one RoPE offset, for every head.

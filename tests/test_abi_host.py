@@ -50,15 +50,17 @@ def _up(x, a=256):
     return (x + a - 1) // a * a
 
 
-def fused_layout(pieces, heads, slots, total_q, seq_lens, ring_depth=128, ring_lanes=None, max_tiles=None):
+def fused_layout(pieces, heads, slots, total_q, seq_lens, ring_depth=128, ring_lanes=None, max_tiles=None,
+                 min_pairs=None):
     """Workspace of the fused path: 256 B header, per-job ring flags, the K/V
     ring lanes (`ring_lanes` x `ring_depth` 128-token bf16 tiles, shared by
     the jobs in turn, then the K_nope residual tiles of each lane's first 16
     slots), the gathered rows (1152 B per token, whole 64-token
     blocks), then partial states."""
     jobs = pieces * heads
-    if ring_lanes is None:                   # 32 MiB of the longest piece's tiles, within [4, 12]
-        ring_lanes = max(4, min(12, (32 << 20) // (128 * 256 * 2 * min(max_tiles, ring_depth))))
+    if ring_lanes is None:   # 32 MiB of the longest piece's tiles, or 76 pairs over a job's fewest, within [4, 64]
+        fit = (32 << 20) // (128 * 256 * 2 * min(max_tiles, ring_depth))
+        ring_lanes = max(4, min(64, max(fit, 76 // min_pairs)))
     ring_lanes = min(ring_lanes, jobs)       # no more lanes than jobs
     ring_off = _up(256 + jobs * 2 * ring_depth * 4)
     gath_off = _up(ring_off + ring_lanes * (ring_depth * 128 * 256 + min(ring_depth, 16) * 128 * 128) * 2)
@@ -71,18 +73,26 @@ def fused_layout(pieces, heads, slots, total_q, seq_lens, ring_depth=128, ring_l
 def test_workspace_size_follows_plan(lib):
     # 1 request, C=256 in chunks of 128 plus the extend: the three ranges share
     # offset 0 and are contiguous, so they fold into one piece (no partial slots).
+    # (pairs of a job: max(1, ceil(producer CTAs / 2)) + ceil(query tiles / 2), producer CTAs = min(4, ceil(tiles / 2)))
     n = _ws(lib, [320], [0, 64], 8, chunk=128)
-    assert n == fused_layout(1, 8, 0, 64, [320], ring_depth=4, max_tiles=3)
+    assert n == fused_layout(1, 8, 0, 64, [320], ring_depth=4, max_tiles=3, min_pairs=2)
     # segments: 4 documents of 64 (4 offsets) + extend = 5 pieces, 5 partial slots
     segs = [[0, 64 * d, 64, 64 * d] for d in range(4)]
-    assert _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64) == fused_layout(5, 1, 5, 2, [258], ring_depth=4, max_tiles=1)
+    assert _ws(lib, [258], [0, 2], 1, segs=segs, chunk=64) == fused_layout(5, 1, 5, 2, [258], ring_depth=4,
+                                                                          max_tiles=1, min_pairs=2)
     # a long context is cut into pieces of at most max(chunk, 16384) keys:
-    # 16384 + 16384 + 7232 + 100, the longest 128 tiles -> 4 lanes
-    assert _ws(lib, [40000 + 100], [0, 100], 2, chunk=4096) == fused_layout(3, 2, 3, 100, [40100], max_tiles=128)
-    # 8192 + 2048 keys in one piece: 80 tiles -> 6 lanes of 128 slots
-    assert _ws(lib, [10240], [0, 2048], 2, chunk=4096) == fused_layout(1, 2, 0, 2048, [10240], max_tiles=80)
+    # 16384 + 16384 + 7232 + 100; 3 pairs a job -> 25 lanes
+    assert _ws(lib, [40000 + 100], [0, 100], 2, chunk=4096) == fused_layout(3, 2, 3, 100, [40100], max_tiles=128,
+                                                                            min_pairs=3)
+    # 8192 + 2048 keys in one piece: 80 tiles, 2 + 8 pairs a job -> 7 lanes of 128 slots
+    assert _ws(lib, [10240], [0, 2048], 2, chunk=4096) == fused_layout(1, 2, 0, 2048, [10240], max_tiles=80,
+                                                                       min_pairs=10)
+    # 16384 cached + 4096 new keys in two pieces: 2 + 16 pairs a job -> 4 lanes
+    assert _ws(lib, [20480], [0, 4096], 2, chunk=16384) == fused_layout(2, 2, 2, 4096, [20480], max_tiles=128,
+                                                                        min_pairs=18)
     # 1000 keys: 8 tiles -> lanes of 8 slots
-    assert _ws(lib, [1000], [0, 100], 3, chunk=512) == fused_layout(1, 3, 0, 100, [1000], ring_depth=8, max_tiles=8)
+    assert _ws(lib, [1000], [0, 100], 3, chunk=512) == fused_layout(1, 3, 0, 100, [1000], ring_depth=8,
+                                                                    max_tiles=8, min_pairs=3)
 
 
 def test_min_workspace_size(lib):
