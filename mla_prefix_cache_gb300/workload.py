@@ -294,6 +294,12 @@ def mixed_32k() -> Workload:
     return make_workload("mixed_32k", 128, ctx, ext, chunk=16384, seed=7)
 
 
+def long_16k() -> Workload:
+    """A long-piece profiling case: 128 heads, 16K cached + 4K new tokens, chunk 16K, BF16 (two pieces of the
+    long configurations' shape, small enough for a full ncu capture)."""
+    return make_workload("long_16k", 128, [16384], [4096], chunk=16384, seed=8)
+
+
 CONFIGS = {
     "tiny": tiny,
     "v3_8k": v3_8k,
@@ -303,6 +309,7 @@ CONFIGS = {
     "short_ext_32k": short_ext_32k,
     "short_ext_fp8_128k": short_ext_fp8_128k,
     "mixed_32k": mixed_32k,
+    "long_16k": long_16k,
 }
 
 
