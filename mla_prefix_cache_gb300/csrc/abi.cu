@@ -846,22 +846,44 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
                         MLA_OK)
     return st;
   {
-    QAbsorbParams qp;
-    qp.q = static_cast<const uint16_t*>(q);
-    qp.w = static_cast<const uint16_t*>(kv_b_proj);
-    qp.qlat = reinterpret_cast<uint16_t*>(ws + aw.qlat_off);
+    static QAbsorbParams qp;
+    std::memset(&qp, 0, sizeof(qp));
+    qp.qscale = fp8_scores ? reinterpret_cast<float*>(ws + aw.qscale_off) : nullptr;
+    qp.err = err;
     qp.scale = fp8_scores ? 1.f : vscale;   // E4M3 scores: kv_scale enters through the per-row score factor
     qp.num_heads = H;
-    // only the rows of this call's requests, one launch per run of adjacent ones
+    const uint64_t dw[2] = {(uint64_t)H * (kDnope + kDv), (uint64_t)kDc};
+    const uint64_t sw[1] = {(uint64_t)H * (kDnope + kDv) * 2};
+    const uint32_t bw[2] = {64, 256};
+    if (!encode_map(&qp.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_b_proj, dw, sw, bw, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MLA_ERR_CUDA;
+    // only the rows of this call's requests, one launch per run of adjacent ones;
+    // the maps end at the run's last token so the tile past it reads zeros and
+    // stores nothing
     for (size_t i = 0; i < ap.ranges.size();) {
       size_t j = i + 1;
       while (j < ap.ranges.size() && ap.ranges[j].row_begin == ap.ranges[j - 1].row_end) ++j;
       qp.row0 = ap.ranges[i].row_begin;
       qp.tokens = ap.ranges[j - 1].row_end - ap.ranges[i].row_begin;
-      st = fp8_scores ? cuda_status(launch_qabsorb_e4m3(qp, ws + aw.qlat8_off,
-                                                        reinterpret_cast<float*>(ws + aw.qscale_off), s))
-                      : cuda_status(launch_qabsorb(qp, s));
-      if (st != MLA_OK) return st;
+      const uint64_t row_end = (uint64_t)ap.ranges[j - 1].row_end;
+      const uint64_t dq[3] = {(uint64_t)kDqk, (uint64_t)H, row_end};
+      const uint64_t sq[2] = {(uint64_t)kDqk * 2, (uint64_t)H * kDqk * 2};
+      const uint32_t bq[3] = {64, 1, 128};
+      bool ok2 = encode_map(&qp.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dq, sq, bq, CU_TENSOR_MAP_SWIZZLE_128B);
+      const uint64_t dl[3] = {(uint64_t)kDc, (uint64_t)H, row_end};
+      if (fp8_scores) {
+        const uint64_t sl[2] = {(uint64_t)kDc, (uint64_t)H * kDc};
+        const uint32_t bl[3] = {128, 1, 128};
+        ok2 &= encode_map(&qp.tm_out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, ws + aw.qlat8_off, dl, sl, bl,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+      } else {
+        const uint64_t sl[2] = {(uint64_t)kDc * 2, (uint64_t)H * kDc * 2};
+        const uint32_t bl[3] = {64, 1, 128};
+        ok2 &= encode_map(&qp.tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + aw.qlat_off, dl, sl, bl,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+      }
+      if (!ok2) return MLA_ERR_CUDA;
+      if ((st = cuda_status(launch_qabsorb(qp, s))) != MLA_OK) return st;
       i = j;
     }
   }
@@ -928,9 +950,16 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
     }
   }
   std::memset(&pp, 0, sizeof(pp));
+  {
+    const uint64_t dw[2] = {(uint64_t)H * (kDnope + kDv), (uint64_t)kDc};
+    const uint64_t sw[1] = {(uint64_t)H * (kDnope + kDv) * 2};
+    const uint32_t bw[2] = {64, 128};
+    if (!encode_map(&pp.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_b_proj, dw, sw, bw, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MLA_ERR_CUDA;
+  }
   pp.lat_out = p.lat_out;
   pp.lat_lse = p.lat_lse;
-  pp.w = static_cast<const uint16_t*>(kv_b_proj);
+  pp.err = err;
   pp.out = out;
   pp.lse = lse;
   pp.out_bf16 = out_dtype == MLA_OUT_BF16;

@@ -3,10 +3,10 @@
 // the page pairs with decode): W_UK is folded into the query and W_UV applied
 // after the attention, so the keys are the cached latent rows themselves,
 // shared by every head:
-//   qlat_h = q_nope_h W_UK,h^T                      [512]   (qabsorb_kernel)
+//   qlat_h = q_nope_h W_UK,h^T                      [512]   (qabsorb_kernel, headproj.cu)
 //   s_t    = scale (qlat_h . c_t + R q_rope_h . k_rope_t)
 //   o_h    = sum_t softmax(s)_t c_t                  [512]   (absorb_attn_kernel)
-//   out_h  = o_h W_UV,h                              [128]   (absorb_proj_kernel)
+//   out_h  = o_h W_UV,h                              [128]   (absorb_proj_kernel, headproj.cu)
 // which equals the up-projected attention exactly, up to rounding.  Per
 // (query, key, head) it costs 2 (576 + 512) FLOP against 2 (192 + 128) for the
 // up-projected form, but it skips the 2 * 512 * 256 FLOP per (key, head) of the
@@ -521,221 +521,6 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
   }
 }
 
-// ---------------------------------------------------------------- q absorption
-// Block: 32 tokens x 128 latent columns of one head; 256 threads, each 4 x 4
-// outputs, fp32 accumulation over the 128 q_nope columns.
-__global__ void __launch_bounds__(256) qabsorb_kernel(const QAbsorbParams p) {
-  __shared__ float qs[32][128];
-  __shared__ __align__(16) uint16_t wt[128][128];   // [d][c]
-  const int H = p.num_heads;
-  const int h = blockIdx.z, c0 = blockIdx.y * 128, t0 = p.row0 + blockIdx.x * 32;
-  const int t_end = p.row0 + p.tokens;
-  const int tid = threadIdx.x;
-  const int64_t wrow = (int64_t)H * (kDnope + kDv);
-  for (int i = tid; i < 32 * 16; i += 256) {
-    const int t = i >> 4, ch = i & 15;
-    uint4 a = make_uint4(0, 0, 0, 0);
-    if (t0 + t < t_end) a = __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)(t0 + t) * H + h) * kDqk) + ch);
-    const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      qs[t][8 * ch + 2 * k] = __uint_as_float(w4[k] << 16);
-      qs[t][8 * ch + 2 * k + 1] = __uint_as_float(w4[k] & 0xFFFF0000u);
-    }
-  }
-  for (int i = tid; i < 128 * 16; i += 256) {
-    const int c = i >> 4, ch = i & 15;
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p.w + (int64_t)(c0 + c) * wrow + h * kDnope) + ch);
-    const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      wt[8 * ch + 2 * k][c] = (uint16_t)(w4[k] & 0xFFFFu);
-      wt[8 * ch + 2 * k + 1][c] = (uint16_t)(w4[k] >> 16);
-    }
-  }
-  __syncthreads();
-  const int ty = tid >> 5, tx = tid & 31;
-  float acc[4][4] = {};
-#pragma unroll 4
-  for (int d = 0; d < 128; ++d) {
-    const uint2 wb = *reinterpret_cast<const uint2*>(&wt[d][4 * tx]);
-    const float b0 = __uint_as_float(wb.x << 16), b1 = __uint_as_float(wb.x & 0xFFFF0000u);
-    const float b2 = __uint_as_float(wb.y << 16), b3 = __uint_as_float(wb.y & 0xFFFF0000u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float a = qs[4 * ty + i][d];
-      acc[i][0] = fmaf(a, b0, acc[i][0]);
-      acc[i][1] = fmaf(a, b1, acc[i][1]);
-      acc[i][2] = fmaf(a, b2, acc[i][2]);
-      acc[i][3] = fmaf(a, b3, acc[i][3]);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + 4 * ty + i;
-    if (t >= t_end) continue;
-    uint2 o;
-    o.x = pack_bf16(acc[i][0] * p.scale, acc[i][1] * p.scale);
-    o.y = pack_bf16(acc[i][2] * p.scale, acc[i][3] * p.scale);
-    *reinterpret_cast<uint2*>(p.qlat + ((int64_t)t * H + h) * kDc + c0 + 4 * tx) = o;
-  }
-}
-
-// ---------------------------------------------------------------- q absorption, E4M3 output
-// Block: 32 tokens x all 512 latent columns of one head, so each row's amax
-// is known: qlat8 = e4m3(qlat / s), s = amax / 448 per row (1 for a zero row),
-// qscale = s.  The 512 columns go in four chunks of 128 through the same
-// shared tiles as qabsorb_kernel.
-__global__ void __launch_bounds__(256) qabsorb_e4m3_kernel(const QAbsorbParams p, uint8_t* __restrict__ qlat8,
-                                                           float* __restrict__ qscale) {
-  __shared__ float qs[32][128];
-  __shared__ __align__(16) uint16_t wt[128][128];   // [d][c]
-  const int H = p.num_heads;
-  const int h = blockIdx.z, t0 = p.row0 + blockIdx.x * 32;
-  const int t_end = p.row0 + p.tokens;
-  const int tid = threadIdx.x;
-  const int64_t wrow = (int64_t)H * (kDnope + kDv);
-  for (int i = tid; i < 32 * 16; i += 256) {
-    const int t = i >> 4, ch = i & 15;
-    uint4 a = make_uint4(0, 0, 0, 0);
-    if (t0 + t < t_end) a = __ldg(reinterpret_cast<const uint4*>(p.q + ((int64_t)(t0 + t) * H + h) * kDqk) + ch);
-    const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      qs[t][8 * ch + 2 * k] = __uint_as_float(w4[k] << 16);
-      qs[t][8 * ch + 2 * k + 1] = __uint_as_float(w4[k] & 0xFFFF0000u);
-    }
-  }
-  const int ty = tid >> 5, tx = tid & 31;
-  float acc[4][4][4] = {};   // [chunk][token][column]
-#pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    __syncthreads();         // q tile loaded / previous chunk's W tile consumed
-    for (int i = tid; i < 128 * 16; i += 256) {
-      const int c = i >> 4, ch = i & 15;
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(p.w + (int64_t)(128 * cc + c) * wrow + h * kDnope) + ch);
-      const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        wt[8 * ch + 2 * k][c] = (uint16_t)(w4[k] & 0xFFFFu);
-        wt[8 * ch + 2 * k + 1][c] = (uint16_t)(w4[k] >> 16);
-      }
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int d = 0; d < 128; ++d) {
-      const uint2 wb = *reinterpret_cast<const uint2*>(&wt[d][4 * tx]);
-      const float b0 = __uint_as_float(wb.x << 16), b1 = __uint_as_float(wb.x & 0xFFFF0000u);
-      const float b2 = __uint_as_float(wb.y << 16), b3 = __uint_as_float(wb.y & 0xFFFF0000u);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a = qs[4 * ty + i][d];
-        acc[cc][i][0] = fmaf(a, b0, acc[cc][i][0]);
-        acc[cc][i][1] = fmaf(a, b1, acc[cc][i][1]);
-        acc[cc][i][2] = fmaf(a, b2, acc[cc][i][2]);
-        acc[cc][i][3] = fmaf(a, b3, acc[cc][i][3]);
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float m = 0.f;
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) m = fmaxf(m, fabsf(acc[cc][i][k]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float sc = m > 0.f ? m / 448.f : 1.f;
-    const float inv = 1.f / sc;
-    const int t = t0 + 4 * ty + i;
-    if (t >= t_end) continue;
-    const int64_t row = (int64_t)t * H + h;
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      const uint32_t lo = pack_e4m3x2(acc[cc][i][0] * inv, acc[cc][i][1] * inv);
-      const uint32_t hi = pack_e4m3x2(acc[cc][i][2] * inv, acc[cc][i][3] * inv);
-      *reinterpret_cast<uint32_t*>(qlat8 + row * kDc + 128 * cc + 4 * tx) = lo | (hi << 16);
-    }
-    if (tx == 0) qscale[row] = sc;
-  }
-}
-
-// ---------------------------------------------------------------- output projection
-// Block: 32 rows (tokens of the launch's ranges) x 128 output columns of one
-// head; the 512 latent columns in chunks of 64.
-__global__ void __launch_bounds__(256) absorb_proj_kernel(const __grid_constant__ ProjParams p) {
-  __shared__ float as[32][64 + 4];
-  __shared__ __align__(16) uint16_t ws[64][128];
-  __shared__ int64_t grow_s[32];
-  const int H = p.num_heads;
-  const int h = blockIdx.z, r0 = blockIdx.x * 32;
-  const int tid = threadIdx.x;
-  if (tid < 32) {
-    const int x = r0 + tid;
-    int64_t g = -1;
-    if (x < p.total_rows) {
-      int lo = 0, hi = p.num_ranges - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.ranges[mid].prefix <= x) lo = mid; else hi = mid - 1;
-      }
-      g = p.ranges[lo].row_begin + (x - p.ranges[lo].prefix);
-    }
-    grow_s[tid] = g;
-  }
-  __syncthreads();
-  const int64_t wrow = (int64_t)H * (kDnope + kDv);
-  const int ty = tid >> 5, tx = tid & 31;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < kDc; k0 += 64) {
-    for (int i = tid; i < 32 * 16; i += 256) {
-      const int t = i >> 4, ch = i & 15;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int64_t g = grow_s[t];
-      if (g >= 0) a = __ldg(reinterpret_cast<const float4*>(p.lat_out + (g * H + h) * kDc + k0) + ch);
-      as[t][4 * ch] = a.x; as[t][4 * ch + 1] = a.y; as[t][4 * ch + 2] = a.z; as[t][4 * ch + 3] = a.w;
-    }
-    for (int i = tid; i < 64 * 16; i += 256) {
-      const int c = i >> 4, ch = i & 15;
-      reinterpret_cast<uint4*>(&ws[c][0])[ch] =
-          __ldg(reinterpret_cast<const uint4*>(p.w + (int64_t)(k0 + c) * wrow + (int64_t)H * kDnope + h * kDv) + ch);
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int c = 0; c < 64; ++c) {
-      const uint2 wb = *reinterpret_cast<const uint2*>(&ws[c][4 * tx]);
-      const float b0 = __uint_as_float(wb.x << 16), b1 = __uint_as_float(wb.x & 0xFFFF0000u);
-      const float b2 = __uint_as_float(wb.y << 16), b3 = __uint_as_float(wb.y & 0xFFFF0000u);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a = as[4 * ty + i][c];
-        acc[i][0] = fmaf(a, b0, acc[i][0]);
-        acc[i][1] = fmaf(a, b1, acc[i][1]);
-        acc[i][2] = fmaf(a, b2, acc[i][2]);
-        acc[i][3] = fmaf(a, b3, acc[i][3]);
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t g = grow_s[4 * ty + i];
-    if (g < 0) continue;
-    const float o0 = acc[i][0] * p.scale, o1 = acc[i][1] * p.scale, o2 = acc[i][2] * p.scale, o3 = acc[i][3] * p.scale;
-    const int64_t o = (g * H + h) * kDv + 4 * tx;
-    if (p.out_bf16) {
-      uint2 v;
-      v.x = pack_bf16(o0, o1);
-      v.y = pack_bf16(o2, o3);
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + o) = v;
-    } else {
-      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = make_float4(o0, o1, o2, o3);
-    }
-    if (tx == 0) p.lse[g * H + h] = p.lat_lse[g * H + h];
-  }
-}
-
 }  // namespace
 
 static cudaError_t configure_absorb(int dev) {
@@ -771,30 +556,6 @@ cudaError_t launch_absorb_attn(const AbsorbParams& p, cudaStream_t s) {
                    : cudaLaunchKernelEx(&cfg, absorb_attn_kernel<false>, p);
   count_launch();
   return e;
-}
-
-cudaError_t launch_qabsorb(const QAbsorbParams& p, cudaStream_t s) {
-  if (p.tokens == 0) return cudaSuccess;
-  const dim3 grid((p.tokens + 31) / 32, kDc / 128, p.num_heads);
-  qabsorb_kernel<<<grid, 256, 0, s>>>(p);
-  count_launch();
-  return cudaGetLastError();
-}
-
-cudaError_t launch_qabsorb_e4m3(const QAbsorbParams& p, uint8_t* qlat8, float* qscale, cudaStream_t s) {
-  if (p.tokens == 0) return cudaSuccess;
-  const dim3 grid((p.tokens + 31) / 32, 1, p.num_heads);
-  qabsorb_e4m3_kernel<<<grid, 256, 0, s>>>(p, qlat8, qscale);
-  count_launch();
-  return cudaGetLastError();
-}
-
-cudaError_t launch_absorb_proj(const ProjParams& p, cudaStream_t s) {
-  if (p.total_rows == 0) return cudaSuccess;
-  const dim3 grid((p.total_rows + 31) / 32, 1, p.num_heads);
-  absorb_proj_kernel<<<grid, 256, 0, s>>>(p);
-  count_launch();
-  return cudaGetLastError();
 }
 
 }  // namespace mla

@@ -249,27 +249,33 @@ struct AbsorbParams {
 };
 static_assert(sizeof(AbsorbParams) <= 32000, "kernel parameter space");
 
-// q absorption: qlat[t][h][c] = bf16(scale * sum_d q[t][h][d] W[c][128 h + d]).
+// q absorption (headproj.cu), over tokens row0 .. row0 + tokens - 1:
+//   qlat[t][h][c] = bf16(scale sum_d q[t][h][d] W[c][128 h + d])        (qscale null)
+//   qlat8[t][h][c] = e4m3(qlat / s), qscale[t H + h] = s = amax / 448  (qscale set; scale unused)
 struct QAbsorbParams {
-  const uint16_t* q;       // [T_q][H][192]
-  const uint16_t* w;       // kv_b_proj [512][H * 256]
-  uint16_t* qlat;          // [T_q][H][512]
+  CUtensorMap tm_q;        // q as (column, head, token) up to token row0 + tokens, box 64 x 1 x 128
+  CUtensorMap tm_w;        // kv_b_proj as [512][H * 256], box 64 x 256
+  CUtensorMap tm_out;      // qlat (bf16, box 64 x 1 x 128) or qlat8 (bytes, box 128 x 1 x 128) as
+                           // (column, head, token) up to token row0 + tokens
+  float* qscale;           // [T_q * H]: E4M3 row scales, or null for bf16 qlat
+  uint32_t* err;
   float scale;
   int row0;                // first token row of this launch
   int tokens;              // rows row0 .. row0 + tokens - 1
   int num_heads;
 };
 
-// Output projection of the latent states: for the rows of each request
-// range, out[t][h][d] = scale * sum_c lat[t H + h][c] W[c][128 H + 128 h + d]
+// Output projection of the latent states (headproj.cu): for the rows of each
+// request range, out[t][h][d] = scale * sum_c lat[t H + h][c] W[c][128 H + 128 h + d]
 // and lse[t][h] = lat_lse[t H + h] (slot 0, where a request's splits were
 // merged).
 struct ProjParams {
+  CUtensorMap tm_w;               // kv_b_proj as [512][H * 256], box 64 x 128
   const float* lat_out;           // [T_q * H][512]
   const float* lat_lse;           // [T_q * H]
-  const uint16_t* w;
   void* out;
   float* lse;
+  uint32_t* err;
   int out_bf16;
   float scale;
   int num_heads;
@@ -281,7 +287,6 @@ struct ProjParams {
 cudaError_t launch_absorb_attn(const AbsorbParams& p, cudaStream_t s);
 cudaError_t launch_qabsorb(const QAbsorbParams& p, cudaStream_t s);
 cudaError_t launch_absorb_proj(const ProjParams& p, cudaStream_t s);
-cudaError_t launch_qabsorb_e4m3(const QAbsorbParams& p, uint8_t* qlat8, float* qscale, cudaStream_t s);
 
 // Content-addressed block store (blocks.cu): content hash of whole cache
 // blocks and byte comparison of block pairs.
