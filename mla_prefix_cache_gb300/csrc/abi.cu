@@ -702,26 +702,44 @@ struct AbsPlan {
   int max_slots = 0;
   bool any_merge = false;
   int64_t items = 0;
+  bool kernel1 = false;            // items for absorb_attn_kernel (else absorb_attn2_kernel)
 };
 
-// Work items of the absorbed path: each piece's 128-row tiles of (token, head)
-// rows, each tile's keys cut into splits of split_keys (a multiple of 64).
-// The split size aims at about four waves of the GPU's clusters over the
-// whole call and stays within [512, 8192] keys; MLA_ABS_SPLIT_KEYS overrides
-// it (rounded up to a multiple of 64).
-static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int num_reqs, AbsPlan* ap) {
+// The latent attention kernel: with bf16 scores absorb_attn2_kernel (items of
+// 256 rows, 128-key tiles on two CTA pairs: measured 1.24x the other on
+// short_ext_32k), with E4M3 scores absorb_attn_kernel (items of 128 rows,
+// 64-key tiles on one CTA pair: 1.08x the other on short_ext_fp8_128k, whose
+// softmax bounds both); MLA_ABS_KERNEL=1 or 2 forces one.
+static bool abs_kernel1(bool fp8_scores) {
+  static const int forced = env_int("MLA_ABS_KERNEL", 0);
+  return forced == 1 || (forced != 2 && fp8_scores);
+}
+
+// Work items of the absorbed path: each piece's tiles of 256 (or 128) rows of
+// (token, head) pairs, each tile's keys cut into splits of split_keys (a
+// multiple of the kernel's key tile).  The split size aims at about four
+// waves of the GPU's clusters over the whole call and stays within
+// [512, 8192] keys; MLA_ABS_SPLIT_KEYS overrides it (rounded up to a multiple
+// of the key tile).
+static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int num_reqs, AbsPlan* ap,
+                           bool fp8_scores = false) {
   ap->pieces.clear();
   ap->ranges.clear();
   ap->max_slots = 0;
   ap->any_merge = false;
   ap->items = 0;
+  const bool k1 = abs_kernel1(fp8_scores);
+  ap->kernel1 = k1;
+  const int64_t rows_per_item = k1 ? 128 : 256;
+  const int key_tile = k1 ? 64 : 128;
+  const double waves_items = k1 ? 304.0 : 144.0;   // four waves of 76 two-CTA or 36 four-CTA clusters
   double work = 0.0;
   for (const Piece& pc : fp.pieces)
-    work += (double)((pc.q_count * (int64_t)H + 127) / 128) * (double)(pc.k_end - pc.k_begin);
-  int split = (int)std::ceil(work / 304.0);
-  split = std::min(8192, std::max(512, (split + 63) & ~63));
+    work += (double)((pc.q_count * (int64_t)H + rows_per_item - 1) / rows_per_item) * (double)(pc.k_end - pc.k_begin);
+  int split = (int)std::ceil(work / waves_items);
+  split = std::min(8192, std::max(512, (split + key_tile - 1) & ~(key_tile - 1)));
   const int forced = env_int("MLA_ABS_SPLIT_KEYS", 0);
-  if (forced > 0) split = (forced + 63) & ~63;
+  if (forced > 0) split = (forced + key_tile - 1) & ~(key_tile - 1);
   std::vector<int> next_slot(num_reqs, 0);
   for (const Piece& pc : fp.pieces) {
     AbsPiece a{};
@@ -733,10 +751,10 @@ static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int 
     a.k_end = pc.k_end;
     a.row_block0 = pc.row_block0;
     a.rope_offset = pc.rope_offset;
-    a.n_row_tiles = (int)((pc.q_count * (int64_t)H + 127) / 128);
+    a.n_row_tiles = (int)((pc.q_count * (int64_t)H + rows_per_item - 1) / rows_per_item);
     const int keys = pc.k_end - pc.k_begin;
     a.n_splits = std::max(1, (keys + split - 1) / split);
-    a.split_keys = ((keys + a.n_splits - 1) / a.n_splits + 63) & ~63;
+    a.split_keys = ((keys + a.n_splits - 1) / a.n_splits + key_tile - 1) & ~(key_tile - 1);
     a.slot = next_slot[pc.req];
     next_slot[pc.req] += a.n_splits;
     ap->pieces.push_back(a);
@@ -816,8 +834,24 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
     ok &= encode_map(&p.tm_qlat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + aw.qlat_off, d3, st3, b3,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  {
+    // absorb_attn2_kernel: [c | k_rope] of a bf16 row as 9 blocks of 64 columns, three to a box; the
+    // latent blocks two to a box
+    const uint64_t d[3] = {64, rows_total, 9};
+    const uint64_t st[2] = {(uint64_t)kRowBytesBf16, 128};
+    const uint32_t b[3] = {64, 64, 3}, b2[3] = {64, 64, 2};
+    ok &= encode_map(&p.tm_c3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rows_base, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= encode_map(&p.tm_c2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rows_base, d, st, b2, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   if (fp8_scores) {
     const void* raw = static_cast<const void*>(ws + aw.raw_off);
+    {
+      // a 640-byte row as 5 blocks of 128 bytes (4 of E4M3 codes, k_rope as bf16), one box a stage
+      const uint64_t d[3] = {128, rows_total, 5};
+      const uint64_t st[2] = {(uint64_t)kRowBytesFp8, 128};
+      const uint32_t b[3] = {128, 64, 5};
+      ok &= encode_map(&p.tm_f5, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, raw, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     // latent codes of a 640-byte row as 4 blocks of 128 bytes: (byte, row, block); one box is a stage
     const uint64_t d[3] = {128, rows_total, 4};
     const uint64_t st[2] = {(uint64_t)kRowBytesFp8, 128};
@@ -918,7 +952,7 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
     if (items > (int64_t)1 << 30) return MLA_ERR_UNSUPPORTED;
     p.n_pieces = (int)n;
     p.n_items = (int)items;
-    if ((st = cuda_status(launch_absorb_attn(p, s))) != MLA_OK) return st;
+    if ((st = cuda_status(ap.kernel1 ? launch_absorb_attn(p, s) : launch_absorb_attn2(p, s))) != MLA_OK) return st;
   }
   if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_e, s))) != MLA_OK) return st;
 
@@ -1480,7 +1514,7 @@ size_t mla_prefill_absorbed_fp8_workspace_size(int num_reqs, const int32_t* seq_
   FusedPlan fp;
   build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fp);
   AbsPlan ap;
-  build_abs_plan(fp, num_heads, cu_q, num_reqs, &ap);
+  build_abs_plan(fp, num_heads, cu_q, num_reqs, &ap, true);
   return abs_ws_layout(fp, ap, num_heads, true).total;
 }
 
@@ -1498,7 +1532,7 @@ int mla_prefill_ctx_absorbed_fp8(const void* q, const int32_t* q_pos, const void
                                softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
   if (st != MLA_OK || plan.total_q == 0) return st;
   AbsPlan ap;
-  build_abs_plan(fplan, num_heads, cu_q, num_reqs, &ap);
+  build_abs_plan(fplan, num_heads, cu_q, num_reqs, &ap, true);
   const AbsWs aw = abs_ws_layout(fplan, ap, num_heads, true);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < aw.total) return MLA_ERR_WORKSPACE;
   return prefill_absorbed(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,

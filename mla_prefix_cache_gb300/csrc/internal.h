@@ -228,6 +228,10 @@ struct AbsorbParams {
   CUtensorMap tm_f8;    // their latent codes as 4 swizzled [64 rows x 128 B] blocks
   CUtensorMap tm_kr8;   // their k_rope as bf16 [rows][320], box 64 x 64 at column 256
   CUtensorMap tm_qlat8; // E4M3 qlat as [T_q * H rows][512 B], box 128 x 128
+  // absorb_attn2_kernel (items of 256 rows, 128-key tiles on CTA pairs)
+  CUtensorMap tm_c3;    // gathered bf16 rows as 9 blocks of 64 columns ([c | k_rope]), box 64 cols x 64 rows x 3 blocks
+  CUtensorMap tm_f5;    // FP8 rows as stored as 5 blocks of 128 B, box 128 x 64 x 5
+  CUtensorMap tm_c2;    // gathered bf16 rows, latent blocks, box 64 x 64 x 2
   const float* qscale;  // [T_q * H]: the E4M3 qlat row's scale
   float kv_scale;
   int fp8_scores;
@@ -285,6 +289,7 @@ struct ProjParams {
 };
 
 cudaError_t launch_absorb_attn(const AbsorbParams& p, cudaStream_t s);
+cudaError_t launch_absorb_attn2(const AbsorbParams& p, cudaStream_t s);
 cudaError_t launch_qabsorb(const QAbsorbParams& p, cudaStream_t s);
 cudaError_t launch_absorb_proj(const ProjParams& p, cudaStream_t s);
 
