@@ -1210,11 +1210,11 @@ static int prefill_reuse(const void* q, const int32_t* q_pos, const void* kv_cac
 // ------------------------------------------------------------------ per-request dispatch
 // A request with at most this many queries goes through the absorbed path,
 // the others through the up-projected one.  On GB300 (128 heads, 32K cached
-// tokens) the two break even near 112 queries: the absorbed path is 1.04x at
-// 96 and 0.89x at 128; on a 128K FP8 cache it breaks even near 128.  The FLOP
-// counts alone would put it near 170, but the up-projected kernel runs its
-// MMAs closer to peak.
-constexpr int kAutoAbsorbedMaxQueries = 96;
+// tokens) the two break even near 140 queries: the absorbed path is 1.07x at
+// 128 and 0.91x at 160; on a 128K FP8 cache it is 1.13x at 128 and 0.77x at
+// 192.  The FLOP counts alone would put it near 170, but the up-projected
+// kernel runs its MMAs closer to peak.
+constexpr int kAutoAbsorbedMaxQueries = 128;
 
 struct AutoPlan {
   Plan plan_f, plan_a;

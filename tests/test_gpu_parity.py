@@ -662,7 +662,7 @@ def test_absorbed_fp8_scores_needs_fp8_cache(api):
     dict(H=2, ctx=[1537, 64], ext=[160, 7], chunk=192, kv="fp8_e4m3"),              # FP8 cache
     dict(H=4, ctx=[1300], ext=[20], chunk=128),                                      # absorbed only
     dict(H=4, ctx=[300], ext=[200], chunk=128),                                      # up-projected only
-    dict(H=2, ctx=[1200, 1100], ext=[96, 97], chunk=128),                            # either side of the threshold
+    dict(H=2, ctx=[1200, 1100], ext=[128, 129], chunk=128),                          # either side of the threshold
     dict(H=2, ctx=[1022, 1023], ext=[8, 8], chunk=128),                              # either side of 1024 keys
 ], ids=["mixed", "docs", "fp8", "short_only", "long_only", "threshold", "few_keys"])
 def test_prefill_auto_matches_oracle(api, case):
