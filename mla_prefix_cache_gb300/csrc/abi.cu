@@ -715,12 +715,51 @@ static bool abs_kernel1(bool fp8_scores) {
   return forced == 1 || (forced != 2 && fp8_scores);
 }
 
+// Estimated run time, in keys of one work item, of the absorbed path's
+// latent attention and merge when every piece's keys are cut into splits of
+// at most `split` keys: the items (rows_per_item rows x one split each) are
+// placed longest first on the least-loaded of `clusters` resident clusters
+// (items of one piece and length go round by round), each item also paying
+// `item_keys` of start and epilogue; a request cut into several slots adds the
+// merge of its latent states, `merge_keys_per_row` per (row, slot + 1).
+static double abs_split_cost(const FusedPlan& fp, int H, int64_t rows_per_item, int split, int clusters,
+                             double item_keys, double merge_keys_per_row, int num_reqs) {
+  std::vector<std::pair<int, int64_t>> groups;   // (item length in keys, item count)
+  std::vector<int> slots(num_reqs, 0);
+  std::vector<int64_t> rows(num_reqs, 0);
+  for (const Piece& pc : fp.pieces) {
+    const int keys = pc.k_end - pc.k_begin;
+    const int ns = std::max(1, (keys + split - 1) / split);
+    const int64_t r_items = (pc.q_count * (int64_t)H + rows_per_item - 1) / rows_per_item;
+    groups.push_back({(keys + ns - 1) / ns, r_items * ns});
+    slots[pc.req] += ns;
+    rows[pc.req] = pc.q_count * (int64_t)H;
+  }
+  std::sort(groups.begin(), groups.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
+  std::vector<double> load(clusters, 0.0);
+  for (const auto& g : groups) {
+    const double len = g.first + item_keys;
+    const int64_t full = g.second / clusters;
+    const int rem = (int)(g.second - full * clusters);
+    if (full > 0)
+      for (double& l : load) l += (double)full * len;
+    if (rem > 0) {
+      std::partial_sort(load.begin(), load.begin() + rem, load.end());
+      for (int i = 0; i < rem; ++i) load[i] += len;
+    }
+  }
+  double t = *std::max_element(load.begin(), load.end());
+  for (int r = 0; r < num_reqs; ++r)
+    if (slots[r] > 1) t += merge_keys_per_row * (double)rows[r] * (slots[r] + 1) / (double)clusters;
+  return t;
+}
+
 // Work items of the absorbed path: each piece's tiles of 256 (or 128) rows of
 // (token, head) pairs, each tile's keys cut into splits of split_keys (a
-// multiple of the kernel's key tile).  The split size aims at about four
-// waves of the GPU's clusters over the whole call and stays within
-// [512, 8192] keys; MLA_ABS_SPLIT_KEYS overrides it (rounded up to a multiple
-// of the key tile).
+// multiple of the kernel's key tile, at least 512).  The split size is the one
+// of the longest piece's keys cut 1 to 16 ways with the least estimated time
+// (abs_split_cost, with the kernels' measured costs); MLA_ABS_SPLIT_KEYS
+// overrides it (rounded up to a multiple of the key tile).
 static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int num_reqs, AbsPlan* ap,
                            bool fp8_scores = false) {
   ap->pieces.clear();
@@ -732,12 +771,27 @@ static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int 
   ap->kernel1 = k1;
   const int64_t rows_per_item = k1 ? 128 : 256;
   const int key_tile = k1 ? 64 : 128;
-  const double waves_items = k1 ? 304.0 : 144.0;   // four waves of 76 two-CTA or 36 four-CTA clusters
-  double work = 0.0;
-  for (const Piece& pc : fp.pieces)
-    work += (double)((pc.q_count * (int64_t)H + rows_per_item - 1) / rows_per_item) * (double)(pc.k_end - pc.k_begin);
-  int split = (int)std::ceil(work / waves_items);
-  split = std::min(8192, std::max(512, (split + key_tile - 1) & ~(key_tile - 1)));
+  // resident clusters (76 of two CTAs or 36 of four on a GB300), an item's start and epilogue (about 8 us)
+  // and the latent merge (2 KB read or written per row and slot at about 3.5 TB/s) in keys of an item
+  // (1.3 us per 64 keys or 2.2 us per 128 keys)
+  const int clusters = k1 ? 76 : 36;
+  const double ns_per_key = k1 ? 20.3 : 17.2;
+  const double item_keys = 8000.0 / ns_per_key;
+  const double merge_keys_per_row = 2048.0 / 3.5 / ns_per_key;
+  int k_max = 0;
+  for (const Piece& pc : fp.pieces) k_max = std::max(k_max, pc.k_end - pc.k_begin);
+  auto round_split = [&](int v) { return std::max(512, (v + key_tile - 1) & ~(key_tile - 1)); };
+  int split = round_split(std::max(k_max, 1));
+  double best = abs_split_cost(fp, H, rows_per_item, split, clusters, item_keys, merge_keys_per_row, num_reqs);
+  for (int ways = 2; ways <= 16 && k_max > 512; ++ways) {
+    const int cand = round_split((k_max + ways - 1) / ways);
+    if (cand >= split) continue;
+    const double c = abs_split_cost(fp, H, rows_per_item, cand, clusters, item_keys, merge_keys_per_row, num_reqs);
+    if (c < best * 0.99) {   // a split must buy a clear gain: more items and slots cost workspace
+      best = c;
+      split = cand;
+    }
+  }
   const int forced = env_int("MLA_ABS_SPLIT_KEYS", 0);
   if (forced > 0) split = (forced + key_tile - 1) & ~(key_tile - 1);
   std::vector<int> next_slot(num_reqs, 0);
@@ -1210,8 +1264,8 @@ static int prefill_reuse(const void* q, const int32_t* q_pos, const void* kv_cac
 // ------------------------------------------------------------------ per-request dispatch
 // A request with at most this many queries goes through the absorbed path,
 // the others through the up-projected one.  On GB300 (128 heads, 32K cached
-// tokens) the two break even near 140 queries: the absorbed path is 1.07x at
-// 128 and 0.91x at 160; on a 128K FP8 cache it is 1.13x at 128 and 0.77x at
+// tokens) the two break even near 150 queries: the absorbed path is 1.14x at
+// 128 and 0.92x at 160; on a 128K FP8 cache it is 1.22x at 128 and 0.84x at
 // 192.  The FLOP counts alone would put it near 170, but the up-projected
 // kernel runs its MMAs closer to peak.
 constexpr int kAutoAbsorbedMaxQueries = 128;
