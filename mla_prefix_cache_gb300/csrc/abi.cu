@@ -721,13 +721,14 @@ static bool abs_kernel1(bool fp8_scores) {
 // placed longest first on the least-loaded of `clusters` resident clusters
 // (items of one piece and length go round by round), each item also paying
 // `item_keys` of start and epilogue; a request cut into several slots adds the
-// merge of its latent states, `merge_keys_per_row` per (row, slot + 1).
-static double abs_split_cost(const FusedPlan& fp, int H, int64_t rows_per_item, int split, int clusters,
-                             double item_keys, double merge_keys_per_row, int num_reqs) {
+// merge of its latent states (a pass over the whole GPU), `merge_keys_per_row`
+// per (row, slot + 1).
+static double abs_split_cost(const std::vector<Piece>& pieces, int H, int64_t rows_per_item, int split,
+                             int clusters, double item_keys, double merge_keys_per_row, int num_reqs) {
   std::vector<std::pair<int, int64_t>> groups;   // (item length in keys, item count)
   std::vector<int> slots(num_reqs, 0);
   std::vector<int64_t> rows(num_reqs, 0);
-  for (const Piece& pc : fp.pieces) {
+  for (const Piece& pc : pieces) {
     const int keys = pc.k_end - pc.k_begin;
     const int ns = std::max(1, (keys + split - 1) / split);
     const int64_t r_items = (pc.q_count * (int64_t)H + rows_per_item - 1) / rows_per_item;
@@ -750,14 +751,44 @@ static double abs_split_cost(const FusedPlan& fp, int H, int64_t rows_per_item, 
   }
   double t = *std::max_element(load.begin(), load.end());
   for (int r = 0; r < num_reqs; ++r)
-    if (slots[r] > 1) t += merge_keys_per_row * (double)rows[r] * (slots[r] + 1) / (double)clusters;
+    if (slots[r] > 1) t += merge_keys_per_row * (double)rows[r] * (slots[r] + 1);
   return t;
+}
+
+// The absorbed path's pieces: the fused plan's pieces of a request that share
+// its query rows and RoPE offset and whose key ranges meet are one piece (the
+// chunk bounds the up-projected K/V, which this path does not form), longest
+// first.
+static std::vector<Piece> abs_pieces(const FusedPlan& fp) {
+  std::vector<Piece> v = fp.pieces;
+  std::sort(v.begin(), v.end(), [](const Piece& a, const Piece& b) {
+    if (a.req != b.req) return a.req < b.req;
+    if (a.rope_offset != b.rope_offset) return a.rope_offset < b.rope_offset;
+    return a.k_begin < b.k_begin;
+  });
+  std::vector<Piece> out;
+  for (const Piece& pc : v) {
+    if (!out.empty()) {
+      Piece& l = out.back();
+      if (l.req == pc.req && l.rope_offset == pc.rope_offset && l.q_begin == pc.q_begin &&
+          l.q_count == pc.q_count && l.q_tok0 == pc.q_tok0 && l.row_block0 == pc.row_block0 &&
+          l.k_end == pc.k_begin) {
+        l.k_end = pc.k_end;
+        continue;
+      }
+    }
+    out.push_back(pc);
+  }
+  std::stable_sort(out.begin(), out.end(), [](const Piece& a, const Piece& b) {
+    return (int64_t)(a.k_end - a.k_begin) * a.q_count > (int64_t)(b.k_end - b.k_begin) * b.q_count;
+  });
+  return out;
 }
 
 // Work items of the absorbed path: each piece's tiles of 256 (or 128) rows of
 // (token, head) pairs, each tile's keys cut into splits of split_keys (a
 // multiple of the kernel's key tile, at least 512).  The split size is the one
-// of the longest piece's keys cut 1 to 16 ways with the least estimated time
+// of the longest piece's keys cut 1 to 64 ways with the least estimated time
 // (abs_split_cost, with the kernels' measured costs); MLA_ABS_SPLIT_KEYS
 // overrides it (rounded up to a multiple of the key tile).
 static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int num_reqs, AbsPlan* ap,
@@ -777,16 +808,18 @@ static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int 
   const int clusters = k1 ? 76 : 36;
   const double ns_per_key = k1 ? 20.3 : 17.2;
   const double item_keys = 8000.0 / ns_per_key;
-  const double merge_keys_per_row = 2048.0 / 3.5 / ns_per_key;
+  const double merge_keys_per_row = 2048.0 / 3500.0 / ns_per_key;   // bytes / (bytes per ns) / (ns per key)
+  const std::vector<Piece> pieces = abs_pieces(fp);
   int k_max = 0;
-  for (const Piece& pc : fp.pieces) k_max = std::max(k_max, pc.k_end - pc.k_begin);
+  for (const Piece& pc : pieces) k_max = std::max(k_max, pc.k_end - pc.k_begin);
   auto round_split = [&](int v) { return std::max(512, (v + key_tile - 1) & ~(key_tile - 1)); };
   int split = round_split(std::max(k_max, 1));
-  double best = abs_split_cost(fp, H, rows_per_item, split, clusters, item_keys, merge_keys_per_row, num_reqs);
-  for (int ways = 2; ways <= 16 && k_max > 512; ++ways) {
+  double best = abs_split_cost(pieces, H, rows_per_item, split, clusters, item_keys, merge_keys_per_row, num_reqs);
+  for (int ways = 2; ways <= 64 && k_max > 512; ++ways) {
     const int cand = round_split((k_max + ways - 1) / ways);
     if (cand >= split) continue;
-    const double c = abs_split_cost(fp, H, rows_per_item, cand, clusters, item_keys, merge_keys_per_row, num_reqs);
+    const double c = abs_split_cost(pieces, H, rows_per_item, cand, clusters, item_keys, merge_keys_per_row,
+                                    num_reqs);
     if (c < best * 0.99) {   // a split must buy a clear gain: more items and slots cost workspace
       best = c;
       split = cand;
@@ -795,7 +828,7 @@ static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int 
   const int forced = env_int("MLA_ABS_SPLIT_KEYS", 0);
   if (forced > 0) split = (forced + key_tile - 1) & ~(key_tile - 1);
   std::vector<int> next_slot(num_reqs, 0);
-  for (const Piece& pc : fp.pieces) {
+  for (const Piece& pc : pieces) {
     AbsPiece a{};
     a.req = pc.req;
     a.q_begin = pc.q_begin;
@@ -1264,8 +1297,8 @@ static int prefill_reuse(const void* q, const int32_t* q_pos, const void* kv_cac
 // ------------------------------------------------------------------ per-request dispatch
 // A request with at most this many queries goes through the absorbed path,
 // the others through the up-projected one.  On GB300 (128 heads, 32K cached
-// tokens) the two break even near 150 queries: the absorbed path is 1.14x at
-// 128 and 0.92x at 160; on a 128K FP8 cache it is 1.22x at 128 and 0.84x at
+// tokens) the two break even near 150 queries: the absorbed path is 1.21x at
+// 128 and 0.94x at 160; on a 128K FP8 cache it is 1.28x at 128 and 0.88x at
 // 192.  The FLOP counts alone would put it near 170, but the up-projected
 // kernel runs its MMAs closer to peak.
 constexpr int kAutoAbsorbedMaxQueries = 128;
