@@ -287,8 +287,8 @@ int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos,
  * a request with at most 128 queries (E_r <= 128) goes through the absorbed
  * path (mla_prefill_ctx_absorbed), the others through the up-projected one,
  * both writing their rows of the same out and lse.  On GB300 the absorbed
- * path is faster below about 150 queries per request (11x at one query,
- * 2.3x at 64, 1.2x at 128, on 32K cached tokens and 128 heads) and slower
+ * path is faster below about 155 queries per request (11.6x at one query,
+ * 2.4x at 64, 1.27x at 128, on 32K cached tokens and 128 heads) and slower
  * above.
  *  workspace      at least mla_prefill_auto_workspace_size(...) bytes: the
  *                 two paths' workspaces side by side; holds the device error

@@ -702,18 +702,7 @@ struct AbsPlan {
   int max_slots = 0;
   bool any_merge = false;
   int64_t items = 0;
-  bool kernel1 = false;            // items for absorb_attn_kernel (else absorb_attn2_kernel)
 };
-
-// The latent attention kernel: with bf16 scores absorb_attn2_kernel (items of
-// 256 rows, 128-key tiles on two CTA pairs: measured 1.24x the other on
-// short_ext_32k), with E4M3 scores absorb_attn_kernel (items of 128 rows,
-// 64-key tiles on one CTA pair: 1.08x the other on short_ext_fp8_128k, whose
-// softmax bounds both); MLA_ABS_KERNEL=1 or 2 forces one.
-static bool abs_kernel1(bool fp8_scores) {
-  static const int forced = env_int("MLA_ABS_KERNEL", 0);
-  return forced == 1 || (forced != 2 && fp8_scores);
-}
 
 // Estimated run time, in keys of one work item, of the absorbed path's
 // latent attention and merge when every piece's keys are cut into splits of
@@ -785,28 +774,25 @@ static std::vector<Piece> abs_pieces(const FusedPlan& fp) {
   return out;
 }
 
-// Work items of the absorbed path: each piece's tiles of 256 (or 128) rows of
+// Work items of the absorbed path: each piece's tiles of 256 rows of
 // (token, head) pairs, each tile's keys cut into splits of split_keys (a
-// multiple of the kernel's key tile, at least 512).  The split size is the one
+// multiple of the 128-key tile, at least 512).  The split size is the one
 // of the longest piece's keys cut 1 to 64 ways with the least estimated time
 // (abs_split_cost, with the kernels' measured costs); MLA_ABS_SPLIT_KEYS
 // overrides it (rounded up to a multiple of the key tile).
-static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int num_reqs, AbsPlan* ap,
-                           bool fp8_scores = false) {
+static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int num_reqs, AbsPlan* ap) {
   ap->pieces.clear();
   ap->ranges.clear();
   ap->max_slots = 0;
   ap->any_merge = false;
   ap->items = 0;
-  const bool k1 = abs_kernel1(fp8_scores);
-  ap->kernel1 = k1;
-  const int64_t rows_per_item = k1 ? 128 : 256;
-  const int key_tile = k1 ? 64 : 128;
-  // resident clusters (76 of two CTAs or 36 of four on a GB300), an item's start and epilogue (about 8 us)
-  // and the latent merge (2 KB read or written per row and slot at about 3.5 TB/s) in keys of an item
-  // (1.3 us per 64 keys or 2.2 us per 128 keys)
-  const int clusters = k1 ? 76 : 36;
-  const double ns_per_key = k1 ? 20.3 : 17.2;
+  const int64_t rows_per_item = 256;
+  const int key_tile = 128;
+  // resident clusters (36 of four CTAs on a GB300), an item's start and epilogue (about 8 us) and the
+  // latent merge (2 KB read or written per row and slot at about 3.5 TB/s) in keys of an item (about
+  // 2.2 us per 128 keys)
+  const int clusters = 36;
+  const double ns_per_key = 17.2;
   const double item_keys = 8000.0 / ns_per_key;
   const double merge_keys_per_row = 2048.0 / 3500.0 / ns_per_key;   // bytes / (bytes per ns) / (ns per key)
   const std::vector<Piece> pieces = abs_pieces(fp);
@@ -906,48 +892,27 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
   const uint64_t rows_total = (uint64_t)std::max(fp.gather_blocks, 1) * kBlock;
   bool ok = true;
   {
-    // the latent part of a row as 8 blocks of 64 columns: (column, row, block); a box is 4 blocks
-    const uint64_t d[3] = {64, rows_total, 8};
+    // [c | k_rope] of a bf16 row as 9 blocks of 64 columns: three to a box for the scores, the latent
+    // blocks two to a box for P c; qlat 128 rows x 64 columns to a box
+    const uint64_t d[3] = {64, rows_total, 9};
     const uint64_t st[2] = {(uint64_t)kRowBytesBf16, 128};
-    const uint32_t b[3] = {64, (uint32_t)64, 4};
-    ok &= encode_map(&p.tm_c4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rows_base, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
-    const uint64_t d2[2] = {(uint64_t)kRowBf16, rows_total};
-    const uint64_t st2[1] = {(uint64_t)kRowBytesBf16};
-    const uint32_t b2[2] = {64, 64};
-    ok &= encode_map(&p.tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_base, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint32_t b[3] = {64, 64, 3}, b2[3] = {64, 64, 2};
+    ok &= encode_map(&p.tm_c3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rows_base, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= encode_map(&p.tm_c2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rows_base, d, st, b2, CU_TENSOR_MAP_SWIZZLE_128B);
     const uint64_t d3[2] = {(uint64_t)kDc, (uint64_t)T_q * H};
     const uint64_t st3[1] = {(uint64_t)kDc * 2};
     const uint32_t b3[2] = {64, 128};
     ok &= encode_map(&p.tm_qlat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + aw.qlat_off, d3, st3, b3,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
-  {
-    // absorb_attn2_kernel: [c | k_rope] of a bf16 row as 9 blocks of 64 columns, three to a box; the
-    // latent blocks two to a box
-    const uint64_t d[3] = {64, rows_total, 9};
-    const uint64_t st[2] = {(uint64_t)kRowBytesBf16, 128};
-    const uint32_t b[3] = {64, 64, 3}, b2[3] = {64, 64, 2};
-    ok &= encode_map(&p.tm_c3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rows_base, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok &= encode_map(&p.tm_c2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, rows_base, d, st, b2, CU_TENSOR_MAP_SWIZZLE_128B);
-  }
   if (fp8_scores) {
+    // a 640-byte row as stored as 5 blocks of 128 bytes (4 of E4M3 codes, k_rope as bf16), one box a stage;
+    // the E4M3 qlat 128 rows x 128 bytes to a box
     const void* raw = static_cast<const void*>(ws + aw.raw_off);
-    {
-      // a 640-byte row as 5 blocks of 128 bytes (4 of E4M3 codes, k_rope as bf16), one box a stage
-      const uint64_t d[3] = {128, rows_total, 5};
-      const uint64_t st[2] = {(uint64_t)kRowBytesFp8, 128};
-      const uint32_t b[3] = {128, 64, 5};
-      ok &= encode_map(&p.tm_f5, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, raw, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
-    }
-    // latent codes of a 640-byte row as 4 blocks of 128 bytes: (byte, row, block); one box is a stage
-    const uint64_t d[3] = {128, rows_total, 4};
+    const uint64_t d[3] = {128, rows_total, 5};
     const uint64_t st[2] = {(uint64_t)kRowBytesFp8, 128};
-    const uint32_t b[3] = {128, 64, 4};
-    ok &= encode_map(&p.tm_f8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, raw, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
-    const uint64_t d2[2] = {(uint64_t)kRowBytesFp8 / 2, rows_total};   // the rows as bf16 [rows][320]
-    const uint64_t st2[1] = {(uint64_t)kRowBytesFp8};
-    const uint32_t b2[2] = {64, 64};
-    ok &= encode_map(&p.tm_kr8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, raw, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint32_t b[3] = {128, 64, 5};
+    ok &= encode_map(&p.tm_f5, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, raw, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
     const uint64_t d3[2] = {(uint64_t)kDc, (uint64_t)T_q * H};
     const uint64_t st3[1] = {(uint64_t)kDc};
     const uint32_t b3[2] = {128, 128};
@@ -1019,11 +984,6 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
   p.num_heads = H;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   rope_fracs((double)rope_theta, p.rope_frac);
-  // tracing: per-tile timestamps of one work item (MLA_ABS_TRACE_ITEM, default 0)
-  void* tr = g_trace.load();
-  p.trace = (tr != nullptr && g_trace_bytes.load() >= (size_t)8 * 4096 * 8) ? static_cast<unsigned long long*>(tr)
-                                                                             : nullptr;
-  p.trace_item = env_int("MLA_ABS_TRACE_ITEM", 0);
   cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
   cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
   if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_b, s))) != MLA_OK) return st;
@@ -1039,7 +999,7 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
     if (items > (int64_t)1 << 30) return MLA_ERR_UNSUPPORTED;
     p.n_pieces = (int)n;
     p.n_items = (int)items;
-    if ((st = cuda_status(ap.kernel1 ? launch_absorb_attn(p, s) : launch_absorb_attn2(p, s))) != MLA_OK) return st;
+    if ((st = cuda_status(launch_absorb_attn(p, s))) != MLA_OK) return st;
   }
   if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_e, s))) != MLA_OK) return st;
 
@@ -1297,9 +1257,9 @@ static int prefill_reuse(const void* q, const int32_t* q_pos, const void* kv_cac
 // ------------------------------------------------------------------ per-request dispatch
 // A request with at most this many queries goes through the absorbed path,
 // the others through the up-projected one.  On GB300 (128 heads, 32K cached
-// tokens) the two break even near 150 queries: the absorbed path is 1.21x at
-// 128 and 0.94x at 160; on a 128K FP8 cache it is 1.28x at 128 and 0.88x at
-// 192.  The FLOP counts alone would put it near 170, but the up-projected
+// tokens) the two break even near 155 queries: the absorbed path is 1.27x at
+// 128 and 0.98x at 160; on a 128K FP8 cache (E4M3 scores) it is 1.40x at 128
+// and 0.99x at 192.  The FLOP counts alone would put it near 170, but the up-projected
 // kernel runs its MMAs closer to peak.
 constexpr int kAutoAbsorbedMaxQueries = 128;
 
@@ -1601,7 +1561,7 @@ size_t mla_prefill_absorbed_fp8_workspace_size(int num_reqs, const int32_t* seq_
   FusedPlan fp;
   build_fused_plan(plan, seq_lens, cu_q, num_reqs, chunk, true, &fp);
   AbsPlan ap;
-  build_abs_plan(fp, num_heads, cu_q, num_reqs, &ap, true);
+  build_abs_plan(fp, num_heads, cu_q, num_reqs, &ap);
   return abs_ws_layout(fp, ap, num_heads, true).total;
 }
 
@@ -1619,7 +1579,7 @@ int mla_prefill_ctx_absorbed_fp8(const void* q, const int32_t* q_pos, const void
                                softmax_scale, rope_theta, parts, out, out_dtype, lse, &plan, &fplan);
   if (st != MLA_OK || plan.total_q == 0) return st;
   AbsPlan ap;
-  build_abs_plan(fplan, num_heads, cu_q, num_reqs, &ap, true);
+  build_abs_plan(fplan, num_heads, cu_q, num_reqs, &ap);
   const AbsWs aw = abs_ws_layout(fplan, ap, num_heads, true);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < aw.total) return MLA_ERR_WORKSPACE;
   return prefill_absorbed(q, q_pos, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks_per_req,

@@ -1,122 +1,142 @@
 // Absorbed (latent-space) MLA attention for short extends ("DeepSeek MLA —
 // Prefix Cache 与 Chunked Prefill 深度解析", section 3, the absorbed path that
 // the page pairs with decode): W_UK is folded into the query and W_UV applied
-// after the attention, so the keys are the cached latent rows themselves,
-// shared by every head:
+// after the attention, so the keys are the cached latent rows [c | k_rope]
+// themselves, shared by every head:
 //   qlat_h = q_nope_h W_UK,h^T                      [512]   (qabsorb_kernel, headproj.cu)
 //   s_t    = scale (qlat_h . c_t + R q_rope_h . k_rope_t)
-//   o_h    = sum_t softmax(s)_t c_t                  [512]   (absorb_attn_kernel)
+//   o_h    = sum_t softmax(s)_t c_t                  [512]   (absorb_attn_kernel, here)
 //   out_h  = o_h W_UV,h                              [128]   (absorb_proj_kernel, headproj.cu)
 // which equals the up-projected attention exactly, up to rounding.  Per
 // (query, key, head) it costs 2 (576 + 512) FLOP against 2 (192 + 128) for the
 // up-projected form, but it skips the 2 * 512 * 256 FLOP per (key, head) of the
-// up-projection: cheaper while a request has fewer than about 170 queries.
+// up-projection: cheaper while a request has fewer than about 150 queries.
 //
-// absorb_attn_kernel: clusters of two CTAs own one work item (128 rows of
-// (token, head) pairs of one piece, one key split).  O [128 x 512] fp32 fills
-// a CTA's whole tensor memory, so the item is split by operation:
-//  - CTA 0 ("S side") keeps Q [128 x 576] bf16 in TMEM, computes
-//    S = Q [c | k_rope]^T for 64 keys per tile (M = 128, N = 64), runs the
-//    online softmax and sends P (bf16) and each row's rescale factor into CTA
-//    1's shared memory with st.async;
-//  - CTA 1 ("O side") accumulates O += P c (two N = 256 MMAs per 16 keys)
-//    and writes O / l at the end.  With each P tile comes one flag per S-side
-//    warp, set when one of its rows raised its maximum (the lazy rescale, so
-//    rarely after the first tiles): only then does the MMA thread wait for the
-//    previous PV and hand the tile to the correction warps, which rescale
-//    those rows of O in TMEM before the tile's PV.
-// Each CTA loads its own 64-key stages (the S side latent + k_rope, the O
-// side latent only) and frees a stage as soon as its own MMA has read it: a
-// stage loaded once for both CTAs would stay busy from its load until the O side's
-// PV, a chain that three stages cannot cover.  The rows are read by every row
-// tile of the piece and stay in L2.
+// A work item is 256 rows of (token, head) pairs of one piece and one key
+// split.  Clusters of four CTAs own an item, as two CTA pairs whose tensor-core
+// work is issued by the pair's first CTA as M = 256 MMAs (rows 0..127 of A
+// and of the accumulator in the first CTA, rows 128..255 in its peer, each
+// CTA holding half of B):
+//  - S pair (ranks 0, 1): Q = [qlat | rotated q_rope] of its 128 rows
+//    (qlat in TMEM, q_rope in shared memory); per 128-key tile
+//    S = Q [c | k_rope]^T with N = 128, rank r loading keys 64 r .. 64 r + 63
+//    of the tile (bf16 rows, or the FP8 rows as stored with E4M3 scores on
+//    kind::f8f6f4); the online softmax of each CTA's rows writes P (bf16), the
+//    rows' rescale factors and one "rescaled" flag per warp into a staging
+//    buffer, which one thread copies in bulk into the shared memory of the O
+//    CTA that holds the same rows (2048 16-byte stores into the other SM took
+//    a quarter of the time with E4M3 scores).
+//  - O pair (ranks 2, 3): O [256 x 512] += P c with N = 256 per MMA, rank
+//    2 + r loading latent columns 128 r .. 128 r + 127 of each 256-column half
+//    of the keys; rows whose maximum rose are rescaled in TMEM by the CTA's
+//    correction warps before the tile's PV; at the end O / l leaves as fp32
+//    latent state.
+// Each key is read from L2 once per 256 rows by the S pair and once by the O
+// pair, half of it by each CTA.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kAThreads = 256;
-constexpr int kAKeys = 64;
-constexpr int kAStages = 3;                                    // O side
-constexpr uint32_t kAAtom = 8192;                              // [64 rows x 128 B] swizzled block
-constexpr uint32_t kACStage = 8 * kAAtom;                      // O side: bf16 latent part of 64 rows
-constexpr uint32_t kACBase = 0;                                // both CTAs
-constexpr uint32_t kAPBase = kAStages * kACStage;              // O side: two P tiles [128 x 64] bf16
-constexpr uint32_t kAPBytes = 16384;
-constexpr uint32_t kAAlphaBase = kAPBase + 2 * kAPBytes;       // O side: per P tile, 128 row factors
-constexpr uint32_t kALBase = kAAlphaBase + 2 * 512;            // O side: 128 final row sums
-constexpr uint32_t kAFlagBase = kALBase + 512;                 // O side: per P tile, 4 rescale flags; then
-                                                               // the tile handed to the correction warps
-constexpr uint32_t kABarBase = kAFlagBase + 2 * 16 + 16;
-enum : uint32_t {
-  kBFull = 0,      // 5, both: stage landed (S side: latent + k_rope; O side: latent)
-  kBEmpty = 5,     // 5, both: the CTA's MMA that reads the stage is done
-  kBSFull = 10,    // 2, S side: S buffer written
-  kBSFree = 12,    // 2, S side: the 4 softmax warps read the S buffer
-  kBPFree = 14,    // 2, S side: PV of the P tile done (commit from the O side)
-  kBQReady = 16,   // S side: the 4 softmax warps copied Q into TMEM (stages 1-2 free again)
-  kBPFull = 17,    // 2, O side: P tile, row factors and flags landed
-  kBCNeed = 19,    // O side: the MMA thread handed a tile (or the end) to the correction warps
-  kBCDone = 20,    // O side: the 4 correction warps rescaled the tile's rows
-  kBPvDone = 21,   // 2, O side: PV of the tile done
-  kBLFull = 23,    // O side: the final row sums landed
-  kBQFull = 24,    // S side: the tile's absorbed queries landed in stages 1-2
-  kANumBars = 25
-};
-constexpr uint32_t kATmemSlot = kABarBase + 8 * kANumBars;
-constexpr uint32_t kASmemBytes = kATmemSlot + 16 + 1024;       // + alignment of the base to 1024
-static_assert(kASmemBytes <= 232448, "more than 227 KB of shared memory per CTA");
+constexpr int kThreads2 = 256;   // warp 0: loads; 1: MMA; 2: TMEM; 4-7: softmax (S) or rescale and epilogue (O)
+constexpr uint32_t kBlk = 8192;            // [64 rows x 128 B] swizzled block
+constexpr uint32_t kBlk128 = 16384;        // [128 rows x 128 B] swizzled block
 
-// S side, by score precision: a stage is [latent | k_rope] of 64 keys
-// (bf16: 8 + 1 swizzled [64 x 128 B] blocks; E4M3 latent: 4 + 1), and the
-// tile's absorbed queries are staged over stages 1-2 at the start.
+// S side, by score precision: the rotated q_rope, the P staging buffer (a P
+// tile, its row factors and flags, in the O side's layout), then the ring.  A
+// stage is this CTA's 64 keys of a tile times kSBlocks blocks of 128 B of the
+// row ([c | k_rope]: 9 blocks of bf16 or 5 of the FP8 row as stored).  The
+// item's qlat is staged from the P staging buffer on, over the first ring
+// stages, before it is copied into TMEM.
 template <bool kF8>
-struct SSide {
-  static constexpr int kCAtoms = kF8 ? 4 : 8;
-  static constexpr int kStages = kF8 ? 5 : 3;
-  static constexpr uint32_t kStage = (kCAtoms + 1) * kAAtom;
-  static constexpr uint32_t kKr = kCAtoms * kAAtom;           // k_rope block within a stage
-  static constexpr uint32_t kTx = kStage;
+struct S2 {
+  static constexpr int kSBlocks = kF8 ? 5 : 3;                // blocks per stage
+  static constexpr int kStagesPerTile = kF8 ? 1 : 3;
+  static constexpr int kLatBlocks = kF8 ? 4 : 8;              // latent blocks of a row (the last block is k_rope)
+  static constexpr int kRing = kF8 ? 4 : 7;
+  static constexpr uint32_t kStage = kSBlocks * kBlk;
+  static constexpr uint32_t kQR = 0;                          // rotated q_rope [128 x 128 B]
+  static constexpr uint32_t kPS = kBlk128;                    // P staging: P [2 x 16 KB], factors [512 B], flags
+  static constexpr uint32_t kPSAlpha = kPS + 2 * kBlk128;
+  static constexpr uint32_t kPSFlags = kPSAlpha + 512;
+  static constexpr uint32_t kStage0 = (kPSFlags + 16 + 1023) & ~1023u;
   static constexpr int kQBoxes = kF8 ? 4 : 8;                 // [128 rows x 128 B] boxes of qlat
-  static constexpr uint32_t kQStage = kStage;                 // stage 1 on
-  static constexpr uint32_t kTmRope = kF8 ? 128 : 256;        // TMEM column of the rotated q_rope
-  static_assert(kStages * kStage <= kABarBase, "S-side stages overlap the barriers");
-  static_assert(kQStage + kQBoxes * 16384 <= 3 * kStage, "staged queries spill past stage 2");
+  static constexpr uint32_t kQBase = kPS;
+  static constexpr uint32_t kQEnd = kQBase + kQBoxes * kBlk128;
+  static constexpr uint32_t kEnd = kStage0 + kRing * kStage;
+  static_assert(kQEnd <= kEnd, "staged queries spill past the ring");
+  // ring stage s holds part of the staged queries until they are copied out
+  static __device__ __forceinline__ bool holds_q(int s) { return kStage0 + s * kStage < kQEnd; }
 };
 
-constexpr uint32_t kATmS = 320;   // S side: S buffer b at 320 + 64 b (Q in columns 0..287)
-constexpr uint32_t kIdescSA = idesc_bf16(128, 64, false, false);
-constexpr uint32_t kIdescS8 = idesc_e4m3(128, 64);
-constexpr uint32_t kIdescPVA = idesc_bf16(128, 256, false, true);
-constexpr uint32_t kTxO = kACStage;
-constexpr uint32_t kTxP = 128 * (128 + 4) + 16;   // per row: 64 bf16 of P and one fp32 factor; 4 flags
-constexpr float kARescale = 8.f;             // log2 units: P stays <= 256
+// O side: two P tiles [128 rows x 128 keys] bf16, their row factors, the
+// final row sums, per P tile four rescale flags (then the tile handed to the
+// correction warps), then kORing stages of 64 keys x this CTA's 256 latent
+// columns (blocks 2 r, 2 r + 1 of each half).
+constexpr uint32_t kOP = 0;
+constexpr uint32_t kOPBytes = 2 * kBlk128;
+constexpr uint32_t kOAlpha = 2 * kOPBytes;
+constexpr uint32_t kOL = kOAlpha + 2 * 512;
+constexpr uint32_t kOFlags = kOL + 512;
+constexpr uint32_t kOC = (kOFlags + 64 + 1023) & ~1023u;
+constexpr int kORing = 4;
+constexpr uint32_t kOStage = 4 * kBlk;
+constexpr uint32_t kOEnd = kOC + kORing * kOStage;
+constexpr uint32_t kTxP2 = 128 * (256 + 4) + 16;   // per row: 128 bf16 of P and one factor; 4 flags
 
-__device__ __forceinline__ uint32_t abar(uint32_t sbase, uint32_t i) { return sbase + kABarBase + 8u * i; }
+enum : uint32_t {
+  // S side
+  kSF = 0,     // 8: stage landed in both S CTAs (first CTA's count)
+  kSE = 8,     // 8: the stage's MMAs are done (both S CTAs)
+  kSSF = 16,   // 2: S buffer written (both S CTAs)
+  kSSR = 18,   // 2: the 8 softmax warps of the pair read the S buffer (first CTA, count 8)
+  kQF = 20,    // this CTA's qlat landed
+  kQL = 21,    // this CTA's 4 softmax warps copied it out (count 4)
+  kQR = 22,    // Q of both S CTAs in place (first CTA, count 8)
+  kPFR = 23,   // 2: PV of the P tile done (both S CTAs, from the O pair)
+  kSTF = 42,   // the P staging buffer's last copy landed in the O CTA (S CTA, from its O CTA)
+  // O side
+  kCF = 25,    // 4: stage landed in both O CTAs (first CTA's count)
+  kCE = 29,    // 4: the stage's MMAs are done (both O CTAs)
+  kPF = 33,    // 2: P tile, factors and flags landed in this CTA
+  kPR = 35,    // 2: P tile ready (and rows rescaled) in both O CTAs (first CTA, count 2)
+  kPVD = 37,   // 2: PV of the tile done (both O CTAs)
+  kCN = 39,    // this CTA's control thread handed a tile (or the end) to its correction warps
+  kCD = 40,    // the 4 correction warps rescaled their rows (count 4)
+  kLF = 41,    // the final row sums landed
+  kNBars2 = 43
+};
 
-// Bounded waits (a timeout records the error; the caller then skips its work).
-__device__ __forceinline__ bool await(const AbsorbParams& p, uint32_t bar, uint32_t parity) {
+template <bool kF8>
+struct L2 {
+  static constexpr uint32_t kBars = (S2<kF8>::kEnd > kOEnd ? S2<kF8>::kEnd : kOEnd);
+  static constexpr uint32_t kSlot = kBars + 8 * kNBars2;
+  static constexpr uint32_t kSmem = kSlot + 16 + 1024;
+  static_assert(kSmem <= 232448, "more than 227 KB of shared memory per CTA");
+};
+
+constexpr uint32_t kIdS2 = idesc_bf16(256, 128, false, false);
+constexpr uint32_t kIdS2f8 = idesc_e4m3(256, 128);
+constexpr uint32_t kIdPV2 = idesc_bf16(256, 256, false, true);
+constexpr float kRescale2 = 8.f;   // log2 units: P stays <= 256
+constexpr uint16_t kMaskS = 0x3, kMaskO = 0xC;
+
+__device__ __forceinline__ uint32_t bar2(uint32_t sbase, uint32_t off_bars, uint32_t i) {
+  return sbase + off_bars + 8u * i;
+}
+__device__ __forceinline__ bool await2(const AbsorbParams& p, uint32_t bar, uint32_t parity) {
   if (mbar_wait(bar, parity)) return true;
   atomicOr(p.err, kErrTimeout);
   return false;
 }
-__device__ __forceinline__ bool await_warp(const AbsorbParams& p, uint32_t bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, await(p, bar, parity));
-}
-
-// Optional tracing (p.trace non-null): %globaltimer of each tile j of work
-// item p.trace_item (j < 4096) in words 8 j + k:
-//   [0] S side: loads issued    [1] S MMA thread: stage landed   [2] S issued
-//   [3] softmax saw S           [4] P computed (before waiting for its tile buffer)
-//   [5] P sent                  [6] O side: PV issued            [7] O side: P landed
-__device__ __forceinline__ void tstamp(const AbsorbParams& p, bool on, int j, int k) {
-  if (on && j < 4096) p.trace[8 * j + k] = global_timer_ns();
+__device__ __forceinline__ bool await2_warp(const AbsorbParams& p, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, await2(p, bar, parity));
 }
 
 struct AItem {
   const AbsPiece* P;
-  int row0;      // first row of the tile within the piece (rows = token * H + head)
+  int row0;      // first row of the item within the piece (rows = token * H + head)
   int k_lo, k_hi, t0, n_tiles;
   int slot;
 };
@@ -132,133 +152,135 @@ __device__ AItem decode_item(const AbsorbParams& p, int item) {
   const int tile = local / P.n_splits, split = local - tile * P.n_splits;
   AItem it;
   it.P = &P;
-  it.row0 = tile * 128;
+  it.row0 = tile * 256;
   it.slot = P.slot + split;
-  // the tile's last query token bounds its causal keys
+  // the item's last query token bounds its causal keys
   const int rows = P.q_count * p.num_heads;
-  const int last_t = min(rows - 1, it.row0 + 127) / p.num_heads;
-  const int k_hi_tile = min(P.k_end, P.q_tok0 + last_t + 1);
+  const int last_t = min(rows - 1, it.row0 + 255) / p.num_heads;
+  const int k_hi_item = min(P.k_end, P.q_tok0 + last_t + 1);
   it.k_lo = P.k_begin + split * P.split_keys;
-  it.k_hi = min(it.k_lo + P.split_keys, k_hi_tile);
-  it.t0 = it.k_lo & ~(kAKeys - 1);
-  it.n_tiles = it.k_hi > it.k_lo ? (it.k_hi - it.t0 + kAKeys - 1) / kAKeys : 0;
+  it.k_hi = min(it.k_lo + P.split_keys, k_hi_item);
+  it.t0 = it.k_lo & ~127;
+  it.n_tiles = it.k_hi > it.k_lo ? (it.k_hi - it.t0 + 127) / 128 : 0;
   return it;
 }
 
 template <bool kF8>
-__global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_constant__ AbsorbParams p) {
-  using SS = SSide<kF8>;
+__global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_constant__ AbsorbParams p) {
+  using SS = S2<kF8>;
+  using LL = L2<kF8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - raw_base);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
-  const AItem it = decode_item(p, blockIdx.x >> 1);
+  const bool s_side = rank < 2;
+  const uint32_t half = rank & 1;          // row half of the item (and key or column half of B)
+  const bool first = half == 0;            // issues the pair's MMAs
+  const AItem it = decode_item(p, blockIdx.x >> 2);
   const AbsPiece& P = *it.P;
   const int H = p.num_heads;
   const int n = it.n_tiles;
-  const bool tr = p.trace != nullptr && (int)(blockIdx.x >> 1) == p.trace_item;
+  const uint32_t B = LL::kBars;
+  auto bar = [&](uint32_t i) { return bar2(sbase, B, i); };
 
   if (tid == 0) {
-    prefetch_tensormap(&p.tm_c4);
-    if (kF8) {
-      prefetch_tensormap(&p.tm_f8);
-      prefetch_tensormap(&p.tm_kr8);
-      prefetch_tensormap(&p.tm_qlat8);
+    if (s_side) {
+      prefetch_tensormap(kF8 ? &p.tm_f5 : &p.tm_c3);
+      prefetch_tensormap(kF8 ? &p.tm_qlat8 : &p.tm_qlat);
     } else {
-      prefetch_tensormap(&p.tm_kr);
-      prefetch_tensormap(&p.tm_qlat);
+      prefetch_tensormap(&p.tm_c2);
     }
-    for (uint32_t i = 0; i < kANumBars; ++i) {
+    for (uint32_t i = 0; i < kNBars2; ++i) {
       uint32_t cnt = 1;
-      if ((i >= kBSFree && i < kBSFree + 2) || i == kBQReady || i == kBCDone) cnt = 4;
-      mbar_init(abar(sbase, i), cnt);
+      if (i == kSSR || i == kSSR + 1 || i == kQR) cnt = 8;
+      else if (i == kQL || i == kCD) cnt = 4;
+      else if (i == kPR || i == kPR + 1) cnt = 2;
+      mbar_init(bar(i), cnt);
     }
     fence_mbar_init();
   }
+  cluster_sync_all();   // every CTA's barriers exist before any is signalled; the pairs run before TMEM is allocated
   if (warp == 2) {
-    tmem_alloc(sbase + kATmemSlot, 512);
-    tmem_relinquish();
+    tmem_alloc2(sbase + LL::kSlot, 512);
+    tmem_relinquish2();
   }
   tc_fence_before();
-  cluster_sync_all();   // both CTAs' barriers exist before either signals the other's
+  __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + kATmemSlot);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + LL::kSlot);
   const int64_t row_base = (int64_t)P.row_block0 * kBlock;   // gathered row of key token 0
 
-  if (rank == 0) {
-    // ================================================================ S side
-    if (warp == 0 || warp == 2 || warp == 3) {
-      // ---------------------------------------------------------- TMA: a stage's boxes leave from up to
-      // three warps (warp 0: latent blocks 0-3, warp 3: bf16 blocks 4-7, warp 2: k_rope); warp 0 arms the
-      // stage's barrier and loads Q
-      if (lane == 0) {
-        bool ok = true;
-        if (warp == 0 && n > 0) {
-          // the tile's absorbed queries: rows q_begin H + row0 .. +127 of qlat, staged over stages 1-2
-          mbar_arrive_expect_tx(abar(sbase, kBQFull), SS::kQBoxes * 16384);
-          const int qrow = P.q_begin * H + it.row0;
+  if (s_side) {
+    // ================================================================ S pair
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- loads: qlat, then this CTA's keys of each tile
+      bool ok = true;
+      const int U = n * SS::kStagesPerTile;
+      if (n > 0) {
+        mbar_arrive_expect_tx(bar(kQF), SS::kQBoxes * kBlk128);
+        const int qrow = P.q_begin * H + it.row0 + 128 * (int)half;
 #pragma unroll 1
-          for (int cc = 0; cc < SS::kQBoxes; ++cc)
-            tma_load_2d(sbase + SS::kQStage + cc * 16384, kF8 ? &p.tm_qlat8 : &p.tm_qlat, (kF8 ? 128 : 64) * cc, qrow,
-                        abar(sbase, kBQFull));
-        }
-        for (int j = 0; j < n && ok; ++j) {
-          const int s = j % SS::kStages;
-          if (j >= SS::kStages && !await(p, abar(sbase, kBEmpty + s), ((j / SS::kStages) - 1) & 1)) { ok = false; break; }
-          if (j == 1 && !await(p, abar(sbase, kBQReady), 0)) { ok = false; break; }   // Q copied out of stages 1-2
-          const int row = (int)(row_base + it.t0 + kAKeys * j);
-          const uint32_t full = abar(sbase, kBFull + s), st = sbase + s * SS::kStage;
-          if (warp == 0) {
-            mbar_arrive_expect_tx(full, SS::kTx);
-            tstamp(p, tr, j, 0);
-            tma_load_3d(st, kF8 ? &p.tm_f8 : &p.tm_c4, 0, row, 0, full);
-          } else if (warp == 3) {
-            if (!kF8) tma_load_3d(st + 4 * kAAtom, &p.tm_c4, 0, row, 4, full);
-          } else if (kF8) {
-            tma_load_2d(st + SS::kKr, &p.tm_kr8, kDc / 2, row, full);   // k_rope at byte 512 of a 640-byte row
-          } else {
-            tma_load_2d(st + SS::kKr, &p.tm_kr, kDc, row, full);
-          }
-        }
-        // the last commits land on this CTA's barriers before it exits
-        if (warp == 0)
-          for (int j = max(0, n - SS::kStages); j < n && ok; ++j)
-            if (!await(p, abar(sbase, kBEmpty + j % SS::kStages), (j / SS::kStages) & 1)) ok = false;
+        for (int cc = 0; cc < SS::kQBoxes; ++cc)
+          tma_load_2d(sbase + SS::kQBase + cc * kBlk128, kF8 ? &p.tm_qlat8 : &p.tm_qlat, (kF8 ? 128 : 64) * cc, qrow,
+                      bar(kQF));
       }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- S = Q [c | k_rope]^T
-      if (lane == 0 && n > 0) {
-        bool ok = await(p, abar(sbase, kBQReady), 0);
-        for (int j = 0; j < n && ok; ++j) {
-          const int s = j % SS::kStages, b = j & 1;
-          if (!await(p, abar(sbase, kBFull + s), (j / SS::kStages) & 1)) { ok = false; break; }
-          tstamp(p, tr, j, 1);
-          if (j >= 2 && !await(p, abar(sbase, kBSFree + b), ((j >> 1) - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t c = sbase + s * SS::kStage, kr = c + SS::kKr;
-          const uint32_t d = tmem + kATmS + 64 * b;
-          // latent part: K = 16 (bf16) or 32 (E4M3) per MMA, four k-steps per 128-byte block
-          constexpr int kLat = kF8 ? 16 : 32;
-#pragma unroll
-          for (int kk = 0; kk < kLat; ++kk) {
-            const uint64_t bdesc = sdesc_sw128(c + (kk >> 2) * kAAtom + (kk & 3) * 32, 16, 1024);
-            if (kF8) mma_e4m3_ts(d, tmem + kk * 8, bdesc, kIdescS8, kk > 0 ? 1u : 0u);
-            else mma_bf16_ts(d, tmem + kk * 8, bdesc, kIdescSA, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ts(d, tmem + SS::kTmRope + kk * 8, sdesc_sw128(kr + kk * 32, 16, 1024), kIdescSA, 1u);
-          mma_commit(abar(sbase, kBSFull + b));
-          mma_commit(abar(sbase, kBEmpty + s));
-          tstamp(p, tr, j, 2);
+      const uint32_t full0 = mapa_shared(bar(kSF), 0u);
+      bool q_copied = false;
+      for (int u = 0; u < U && ok; ++u) {
+        const int s = u % SS::kRing, j = u / SS::kStagesPerTile, m = u - j * SS::kStagesPerTile;
+        if (u >= SS::kRing && !await2(p, bar(kSE + s), ((u / SS::kRing) - 1) & 1)) { ok = false; break; }
+        if (SS::holds_q(s) && !q_copied) {   // the staged queries are out of the stages before keys overwrite them
+          if (!await2(p, bar(kQL), 0)) { ok = false; break; }
+          q_copied = true;
         }
+        const int row = (int)(row_base + it.t0 + 128 * j + 64 * (int)half);
+        if (first) mbar_arrive_expect_tx(bar(kSF + s), 2 * SS::kStage);
+        if (kF8) tma_load_3d_pair(sbase + SS::kStage0 + s * SS::kStage, &p.tm_f5, 0, row, 0, full0 + 8u * s);
+        else tma_load_3d_pair(sbase + SS::kStage0 + s * SS::kStage, &p.tm_c3, 0, row, 3 * m, full0 + 8u * s);
+      }
+      // the last commits land on this CTA's barriers before it exits
+      for (int u = max(0, U - SS::kRing); u < U && ok; ++u)
+        if (!await2(p, bar(kSE + u % SS::kRing), (u / SS::kRing) & 1)) ok = false;
+    } else if (warp == 1 && lane == 0 && first && n > 0) {
+      // ---------------------------------------------------------- S = Q [c | k_rope]^T, N = 128 keys
+      bool ok = await2(p, bar(kQR), 0);
+      for (int j = 0; j < n && ok; ++j) {
+        const int b = j & 1;
+        if (j >= 2 && !await2(p, bar(kSSR + b), ((j >> 1) - 1) & 1)) { ok = false; break; }
+        const uint32_t d = tmem + 256 + 128 * b;
+#pragma unroll 1
+        for (int m = 0; m < SS::kStagesPerTile && ok; ++m) {
+          const int u = j * SS::kStagesPerTile + m, s = u % SS::kRing;
+          if (!await2(p, bar(kSF + s), (u / SS::kRing) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = sbase + SS::kStage0 + s * SS::kStage;
+#pragma unroll
+          for (int kb = 0; kb < SS::kSBlocks; ++kb) {
+            const int g = m * SS::kSBlocks + kb;
+            if (g < SS::kLatBlocks) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = sdesc_sw128(st + kb * kBlk + kk * 32, 16, 1024);
+                if (kF8) mma2_ts_e4m3(d, tmem + 32 * g + 8 * kk, bd, kIdS2f8, (g | kk) ? 1u : 0u);
+                else mma2_ts(d, tmem + 32 * g + 8 * kk, bd, kIdS2, (g | kk) ? 1u : 0u);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma2_ss(d, sdesc_sw128(sbase + SS::kQR + kk * 32, 16, 1024),
+                        sdesc_sw128(st + kb * kBlk + kk * 32, 16, 1024), kIdS2, 1u);
+            }
+          }
+          mma2_commit_mc(bar(kSE + s), kMaskS);
+        }
+        if (ok) mma2_commit_mc(bar(kSSF + b), kMaskS);
       }
     } else if (warp >= 4) {
-      // ---------------------------------------------------------- Q -> TMEM, then softmax
+      // ---------------------------------------------------------- Q -> TMEM and shared memory, then softmax
       const int r = tid - 128;
-      const int prow = it.row0 + r;
+      const int prow = it.row0 + 128 * (int)half + r;
       const bool live = prow < P.q_count * H;
       const int tl = live ? prow / H : 0, h = live ? prow - (prow / H) * H : 0;
       const int64_t grow = (int64_t)P.q_begin + tl;
@@ -267,209 +289,235 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
       // E4M3 scores: the latent part of S counts in units of qscale[row] * kv_scale, so q_rope is divided
       // by it (the two parts share one accumulator) and the softmax multiplies it back
       const float qs = kF8 ? (live ? __ldg(p.qscale + orow) : 1.f) * p.kv_scale : 1.f;
+      const uint32_t orank = 2u + half;   // the O CTA holding the same rows
       if (n > 0) {
-        // rotated q_rope from global memory (its loads overlap the qlat TMA)
+        // rotated q_rope from global memory, into shared memory as a K-major swizzled block
         const uint4* qr = reinterpret_cast<const uint4*>(p.q + orow * kDqk + kDnope);
         const int64_t delta = live ? (int64_t)__ldg(p.q_pos + grow) - P.rope_offset : 0;
         const float rq = 1.f / qs;
         uint4 qv[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) qv[c] = live ? __ldg(qr + c) : make_uint4(0, 0, 0, 0);
-        uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t w4[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+          uint32_t o4[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            // (measured: the SFU form is 2% faster here with bf16 scores, the
-            // accurate one 16% faster with E4M3 scores)
             float sn, cs;
             if constexpr (kF8) rope_sincos(delta, p.rope_frac[4 * c + i], &sn, &cs);
             else rope_sincos_sfu(delta, p.rope_frac[4 * c + i], &sn, &cs);
             const float x0 = __uint_as_float(w4[i] << 16), x1 = __uint_as_float(w4[i] & 0xFFFF0000u);
-            w[4 * c + i] = pack_bf16((x0 * cs - x1 * sn) * rq, (x0 * sn + x1 * cs) * rq);
+            o4[i] = pack_bf16((x0 * cs - x1 * sn) * rq, (x0 * sn + x1 * cs) * rq);
           }
+          sts128(sbase + SS::kQR + sw128_off((uint32_t)r, (uint32_t)c), o4[0], o4[1], o4[2], o4[3]);
         }
-        tmem_st32(tmem + lane_off + SS::kTmRope, w);
-        // qlat: shared memory (TMA, 128-byte swizzled [128 x 128 B] blocks) -> TMEM columns from 0
-        const bool qok = await_warp(p, abar(sbase, kBQFull), 0);
+        // qlat: shared memory (TMA, swizzled [128 x 128 B] blocks) -> TMEM columns from 0
+        const bool qok = await2_warp(p, bar(kQF), 0);
 #pragma unroll 1
         for (int cc = 0; cc < SS::kQBoxes; ++cc) {
           uint32_t u[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint32_t v4[4];
-            if (qok) lds128(sbase + SS::kQStage + cc * 16384 + sw128_off((uint32_t)r, (uint32_t)c), v4);
+            if (qok) lds128(sbase + SS::kQBase + cc * kBlk128 + sw128_off((uint32_t)r, (uint32_t)c), v4);
             else v4[0] = v4[1] = v4[2] = v4[3] = 0u;
             u[4 * c] = v4[0]; u[4 * c + 1] = v4[1]; u[4 * c + 2] = v4[2]; u[4 * c + 3] = v4[3];
           }
           tmem_st32(tmem + lane_off + 32 * cc, u);
         }
         tmem_wait_st();
+        fence_proxy_async_smem();   // q_rope, written here, is an MMA operand
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(abar(sbase, kBQReady));
+        if (lane == 0) {
+          mbar_arrive(bar(kQL));
+          mbar_arrive_cluster(mapa_shared(bar(kQR), 0u));   // release: this CTA's q_rope and TMEM rows
+        }
       }
       const int qk = live ? P.q_tok0 + tl : -1;   // last visible key token of the row
       const float sl2 = p.scale_log2 * qs;
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
-      const uint32_t peer_p = mapa_shared(sbase + kAPBase, 1u);
-      const uint32_t peer_alpha = mapa_shared(sbase + kAAlphaBase, 1u);
+      const uint32_t ssr0 = mapa_shared(bar(kSSR), 0u);
       for (int j = 0; j < n; ++j) {
         const int b = j & 1;
-        uint32_t v[64];
+        uint32_t v0[64], v1[64];
         float mx = -INFINITY;
-        if (ok && !await_warp(p, abar(sbase, kBSFull + b), (j >> 1) & 1)) ok = false;
+        bool wok = await2_warp(p, bar(kSSF + b), (j >> 1) & 1);
         tc_fence_after();
-        if (ok) mx = tmem_ld64_max(tmem + lane_off + kATmS + 64 * b, v);   // the row maximum comes with the load
+        if (wok) {
+          const float m0 = tmem_ld64_max(tmem + lane_off + 256 + 128 * b, v0);   // keys 0..63 of the tile
+          const float m1 = tmem_ld64_max(tmem + lane_off + 256 + 128 * b + 64, v1);
+          mx = fmaxf(m0, m1);
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(abar(sbase, kBSFree + b));
-        if (!ok) break;
-        if (tid == 128) tstamp(p, tr, j, 3);
-        const int kt0 = it.t0 + kAKeys * j;
-        if (!(kt0 >= it.k_lo && kt0 + kAKeys - 1 < it.k_hi && kt0 + kAKeys - 1 <= qk)) {
+        if (lane == 0 && wok) mbar_arrive_cluster_relaxed(ssr0 + 8u * b);
+        // the staging buffer is free once the previous tile's copy landed; the four warps go on, or
+        // leave, together
+        if (wok && j >= 1) wok = await2_warp(p, bar(kSTF), (j - 1) & 1);
+        if (named_bar_or(1, 128, !wok)) { ok = false; break; }
+        const int kt0 = it.t0 + 128 * j;
+        if (!(kt0 >= it.k_lo && kt0 + 127 < it.k_hi && kt0 + 127 <= qk)) {
           float m8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
-            const int kt = kt0 + c;
-            const bool vis = kt >= it.k_lo && kt < it.k_hi && kt <= qk;
-            const float x = vis ? __uint_as_float(v[c]) : -INFINITY;
-            v[c] = __float_as_uint(x);
-            m8[c & 7] = fmaxf(m8[c & 7], x);
+            const int ka = kt0 + c, kb = kt0 + 64 + c;
+            const float xa = (ka >= it.k_lo && ka < it.k_hi && ka <= qk) ? __uint_as_float(v0[c]) : -INFINITY;
+            const float xb = (kb >= it.k_lo && kb < it.k_hi && kb <= qk) ? __uint_as_float(v1[c]) : -INFINITY;
+            v0[c] = __float_as_uint(xa);
+            v1[c] = __float_as_uint(xb);
+            m8[c & 7] = fmax3(m8[c & 7], xa, xb);
           }
           mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
         const float m_tile = mx * sl2;
         float alpha = 1.f;
-        if (m_tile > m_used + kARescale) {
+        if (m_tile > m_used + kRescale2) {
           alpha = ex2(m_used - m_tile);   // 0 when m_used = -inf
           m_used = m_tile;
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-mref, -mref);
         uint64_t s4[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float x0, x1;
-          f2unpack(ffma2(f2pack(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])), sc2, nm2), x0, x1);
-          const float a = ex2(x0), bb = ex2(x1);
-          s4[c & 3] = fadd2(s4[c & 3], f2pack(a, bb));
-          pk[c] = pack_bf16(a, bb);
+        for (int hk = 0; hk < 2; ++hk) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t x0u = hk ? v1[2 * c] : v0[2 * c], x1u = hk ? v1[2 * c + 1] : v0[2 * c + 1];
+            float x0, x1;
+            f2unpack(ffma2(f2pack(__uint_as_float(x0u), __uint_as_float(x1u)), sc2, nm2), x0, x1);
+            const float a = ex2(x0), bb = ex2(x1);
+            s4[c & 3] = fadd2(s4[c & 3], f2pack(a, bb));
+            pk[c] = pack_bf16(a, bb);
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            sts128(sbase + SS::kPS + hk * kBlk128 + sw128_off((uint32_t)r, (uint32_t)c), pk[4 * c], pk[4 * c + 1],
+                   pk[4 * c + 2], pk[4 * c + 3]);
         }
         float s8[4];
         f2unpack(fadd2(s4[0], s4[1]), s8[0], s8[1]);
         f2unpack(fadd2(s4[2], s4[3]), s8[2], s8[3]);
         l = l * alpha + ((s8[0] + s8[2]) + (s8[1] + s8[3]));
-        if (tid == 128) tstamp(p, tr, j, 4);
-        // P tile b is free once the PV of tile j - 2 is done
-        if (j >= 2 && !await_warp(p, abar(sbase, kBPFree + b), ((j - 2) >> 1) & 1)) { ok = false; break; }
-        const uint32_t cbar = mapa_shared(abar(sbase, kBPFull + b), 1u);
-        const uint32_t prow_addr = peer_p + b * kAPBytes;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(prow_addr + sw128_off((uint32_t)r, (uint32_t)c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                      pk[4 * c + 3], cbar);
-        st_async_b32(peer_alpha + b * 512 + 4 * r, __float_as_uint(alpha), cbar);
+        reinterpret_cast<float*>(sgen + SS::kPSAlpha)[r] = alpha;
         const uint32_t any_rescale = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
-        if (lane == 0) st_async_b32(mapa_shared(sbase + kAFlagBase + 16 * b + 4 * (warp & 3), 1u), any_rescale, cbar);
-        if (tid == 128) tstamp(p, tr, j, 5);
+        if (lane == 0) reinterpret_cast<uint32_t*>(sgen + SS::kPSFlags)[warp & 3] = any_rescale;
+        fence_proxy_async_smem();   // the staged tile is read by the bulk copy (async proxy)
+        named_bar_sync(1, 128);
+        if (r == 0) {
+          // P tile b of the O CTA is free once the PV of tile j - 2 is done
+          if (j >= 2 && !await2(p, bar(kPFR + b), ((j - 2) >> 1) & 1)) continue;   // the others time out next tile
+          const uint32_t cbar = mapa_shared(bar(kPF + b), orank);
+          bulk_copy_to_peer(mapa_shared(sbase + kOP + b * kOPBytes, orank), sbase + SS::kPS, kOPBytes, cbar);
+          bulk_copy_to_peer(mapa_shared(sbase + kOAlpha + b * 512, orank), sbase + SS::kPSAlpha, 512, cbar);
+          bulk_copy_to_peer(mapa_shared(sbase + kOFlags + 16 * b, orank), sbase + SS::kPSFlags, 16, cbar);
+        }
       }
-      // final row sums to the O side; lse of the item
-      st_async_b32(mapa_shared(sbase + kALBase + 4 * r, 1u), __float_as_uint(ok ? l : 0.f),
-                   mapa_shared(abar(sbase, kBLFull), 1u));
+      // final row sums to the O CTA; lse of the item
+      st_async_b32(mapa_shared(sbase + kOL + 4 * r, orank), __float_as_uint(ok ? l : 0.f),
+                   mapa_shared(bar(kLF), orank));
       if (live) {
         const float lse = (ok && l > 0.f) ? (m_used + __log2f(l)) * 0.6931471805599453f : -INFINITY;
         p.lat_lse[(int64_t)it.slot * p.slot_stride_rows + orow] = lse;
       }
       // the last two PV commits land on this CTA's barriers before it exits
       for (int j = max(0, n - 2); j < n && ok; ++j)
-        if (!await_warp(p, abar(sbase, kBPFree + (j & 1)), (j >> 1) & 1)) ok = false;
+        if (!await2_warp(p, bar(kPFR + (j & 1)), (j >> 1) & 1)) ok = false;
     }
   } else {
-    // ================================================================ O side
-    if (warp == 0 || warp == 3) {
-      // ---------------------------------------------------------- TMA (latent rows; blocks 0-3 from warp 0,
-      // which arms the barrier, blocks 4-7 from warp 3)
-      if (lane == 0) {
-        bool ok = true;
-        for (int j = 0; j < n && ok; ++j) {
-          const int s = j % kAStages;
-          if (j >= kAStages && !await(p, abar(sbase, kBEmpty + s), ((j / kAStages) - 1) & 1)) { ok = false; break; }
-          const int row = (int)(row_base + it.t0 + kAKeys * j);
-          if (warp == 0) {
-            mbar_arrive_expect_tx(abar(sbase, kBFull + s), kTxO);
-            tma_load_3d(sbase + kACBase + s * kACStage, &p.tm_c4, 0, row, 0, abar(sbase, kBFull + s));
-          } else {
-            tma_load_3d(sbase + kACBase + s * kACStage + 4 * kAAtom, &p.tm_c4, 0, row, 4, abar(sbase, kBFull + s));
+    // ================================================================ O pair
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- loads: this CTA's latent columns of 64 keys a stage
+      bool ok = true;
+      const int U = 2 * n;
+      const uint32_t full0 = mapa_shared(bar(kCF), 2u);
+      for (int u = 0; u < U && ok; ++u) {
+        const int s = u % kORing;
+        if (u >= kORing && !await2(p, bar(kCE + s), ((u / kORing) - 1) & 1)) { ok = false; break; }
+        const int row = (int)(row_base + it.t0 + 64 * u);
+        if (first) mbar_arrive_expect_tx(bar(kCF + s), 2 * kOStage);
+        const uint32_t st = sbase + kOC + s * kOStage;
+        tma_load_3d_pair(st, &p.tm_c2, 0, row, 2 * (int)half, full0 + 8u * s);              // columns 128 r ..
+        tma_load_3d_pair(st + 2 * kBlk, &p.tm_c2, 0, row, 4 + 2 * (int)half, full0 + 8u * s);   // 256 + 128 r ..
+      }
+      for (int u = max(0, U - kORing); u < U && ok; ++u)
+        if (!await2(p, bar(kCE + u % kORing), (u / kORing) & 1)) ok = false;
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- per tile: P landed, rows rescaled; then (first
+      // CTA) O += P c for the pair
+      for (int b = 0; b < min(n, 2); ++b) mbar_arrive_expect_tx(bar(kPF + b), kTxP2);
+      mbar_arrive_expect_tx(bar(kLF), 512);
+      bool ok = true;
+      volatile int* hand = reinterpret_cast<volatile int*>(sgen + kOFlags + 32);
+      const uint32_t pr0 = mapa_shared(bar(kPR), 2u);
+      const uint32_t stf_s = mapa_shared(bar(kSTF), half);   // the S CTA that sends this CTA's P
+      int events = 0;
+      for (int j = 0; j < n && ok; ++j) {
+        const int b = j & 1;
+        if (!await2(p, bar(kPF + b), (j >> 1) & 1)) { ok = false; break; }
+        mbar_arrive_cluster_relaxed(stf_s);   // the S CTA's staging buffer may take the next tile
+        if (j > 0) {
+          uint32_t f[4];
+          lds128(sbase + kOFlags + 16 * b, f);
+          if (f[0] | f[1] | f[2] | f[3]) {
+            // O must hold PV of every earlier tile before its rows are rescaled
+            if (!await2(p, bar(kPVD + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
+            *hand = b;
+            mbar_arrive(bar(kCN));
+            if (!await2(p, bar(kCD), events & 1)) { ok = false; break; }
+            ++events;
           }
         }
-        if (warp == 0)
-          for (int j = max(0, n - kAStages); j < n && ok; ++j)
-            if (!await(p, abar(sbase, kBEmpty + j % kAStages), (j / kAStages) & 1)) ok = false;
-      }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- O += P c
-      if (lane == 0) {
-        for (int b = 0; b < min(n, 2); ++b) mbar_arrive_expect_tx(abar(sbase, kBPFull + b), kTxP);
-        mbar_arrive_expect_tx(abar(sbase, kBLFull), 512);
-        bool ok = true;
-        volatile int* hand = reinterpret_cast<volatile int*>(sgen + kAFlagBase + 32);
-        int events = 0;
-        for (int j = 0; j < n && ok; ++j) {
-          const int s = j % kAStages, b = j & 1;
-          if (!await(p, abar(sbase, kBFull + s), (j / kAStages) & 1)) { ok = false; break; }
-          if (!await(p, abar(sbase, kBPFull + b), (j >> 1) & 1)) { ok = false; break; }
-          tstamp(p, tr, j, 7);
-          if (j > 0) {
-            uint32_t f[4];
-            lds128(sbase + kAFlagBase + 16 * b, f);
-            if (f[0] | f[1] | f[2] | f[3]) {
-              // O must hold PV of every earlier tile before its rows are rescaled
-              if (!await(p, abar(sbase, kBPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
-              *hand = b;
-              mbar_arrive(abar(sbase, kBCNeed));
-              if (!await(p, abar(sbase, kBCDone), events & 1)) { ok = false; break; }
-              ++events;
-            }
-          }
-          fence_proxy_async_smem();   // P was written by the peer's stores, the MMA reads it as an operand
+        fence_proxy_async_smem();   // P was written by the S CTA's stores, the MMA reads it as an operand
+        tc_fence_before();
+        if (first) mbar_arrive(bar(kPR + b));
+        else mbar_arrive_cluster(pr0 + 8u * b);   // release: P and the rescaled rows of this CTA
+        if (j + 2 < n) mbar_arrive_expect_tx(bar(kPF + b), kTxP2);
+        if (first) {
+          if (!await2(p, bar(kPR + b), (j >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t c = sbase + kACBase + s * kACStage, pt = sbase + kAPBase + b * kAPBytes;
+          const uint32_t pt = sbase + kOP + b * kOPBytes;
+#pragma unroll 1
+          for (int kh = 0; kh < 2 && ok; ++kh) {
+            const int u = 2 * j + kh, s = u % kORing;
+            if (!await2(p, bar(kCF + s), (u / kORing) & 1)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t c = sbase + kOC + s * kOStage;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = sdesc_sw128(pt + kk * 32, 16, 1024);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128(pt + kh * kBlk128 + kk * 32, 16, 1024);
 #pragma unroll
-            for (int half = 0; half < 2; ++half)
-              mma_bf16(tmem + 256 * half, adesc, sdesc_sw128(c + kk * 2048 + half * 4 * kAAtom, kAAtom, 1024),
-                       kIdescPVA, (j > 0 || kk > 0) ? 1u : 0u);
+              for (int nh = 0; nh < 2; ++nh)
+                mma2_ss(tmem + 256 * nh, ad, sdesc_sw128(c + nh * 2 * kBlk + kk * 2048, kBlk, 1024), kIdPV2,
+                        (j | kh | kk) ? 1u : 0u);
+            }
+            mma2_commit_mc(bar(kCE + s), kMaskO);
           }
-          mma_commit(abar(sbase, kBPvDone + b));
-          mma_commit(abar(sbase, kBEmpty + s));
-          tstamp(p, tr, j, 6);
-          mma_commit_mc(abar(sbase, kBPFree + b), 1);
-          if (j + 2 < n) mbar_arrive_expect_tx(abar(sbase, kBPFull + b), kTxP);
+          if (!ok) break;
+          mma2_commit_mc(bar(kPVD + b), kMaskO);
+          mma2_commit_mc(bar(kPFR + b), kMaskS);
         }
-        *hand = -1;   // no more tiles: the correction warps go on to the epilogue
-        mbar_arrive(abar(sbase, kBCNeed));
       }
+      *hand = -1;   // no more tiles: the correction warps go on to the epilogue
+      mbar_arrive(bar(kCN));
     } else if (warp >= 4) {
       // ---------------------------------------------------------- rescale O rows; epilogue
       const int r = tid - 128;
-      const int prow = it.row0 + r;
+      const int prow = it.row0 + 128 * (int)half + r;
       const bool live = prow < P.q_count * H;
       const int tl = live ? prow / H : 0, h = live ? prow - (prow / H) * H : 0;
       const int64_t orow = ((int64_t)P.q_begin + tl) * H + h;
       const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-      const float* alpha_s = reinterpret_cast<const float*>(sgen + kAAlphaBase);
-      const volatile int* hand = reinterpret_cast<const volatile int*>(sgen + kAFlagBase + 32);
+      const float* alpha_s = reinterpret_cast<const float*>(sgen + kOAlpha);
+      const volatile int* hand = reinterpret_cast<const volatile int*>(sgen + kOFlags + 32);
       bool ok = true;
       for (int ev = 0;; ++ev) {
-        if (!await_warp(p, abar(sbase, kBCNeed), ev & 1)) { ok = false; break; }
+        if (!await2_warp(p, bar(kCN), ev & 1)) { ok = false; break; }
         const int b = *hand;
         if (b < 0) break;
         tc_fence_after();
@@ -487,12 +535,12 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(abar(sbase, kBCDone));
+        if (lane == 0) mbar_arrive(bar(kCD));
       }
-      if (ok && n > 0 && !await_warp(p, abar(sbase, kBPvDone + ((n - 1) & 1)), ((n - 1) >> 1) & 1)) ok = false;
-      if (ok && !await_warp(p, abar(sbase, kBLFull), 0)) ok = false;
+      if (ok && n > 0 && !await2_warp(p, bar(kPVD + ((n - 1) & 1)), ((n - 1) >> 1) & 1)) ok = false;
+      if (ok && !await2_warp(p, bar(kLF), 0)) ok = false;
       tc_fence_after();
-      const float lsum = ok ? reinterpret_cast<const float*>(sgen + kALBase)[r] : 0.f;
+      const float lsum = ok ? reinterpret_cast<const float*>(sgen + kOL)[r] : 0.f;
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       float4* dst = reinterpret_cast<float4*>(p.lat_out + ((int64_t)it.slot * p.slot_stride_rows + orow) * kDc);
 #pragma unroll 1
@@ -514,40 +562,38 @@ __global__ void __launch_bounds__(kAThreads, 1) absorb_attn_kernel(const __grid_
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();   // no peer operation targets this CTA's shared memory any more
+  cluster_sync_all();   // no operation of another CTA targets this one's memory, and the pair's MMAs are done
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc2(tmem, 512);
   }
 }
 
 }  // namespace
 
-static cudaError_t configure_absorb(int dev) {
-  static int configured_device = -1;
-  if (configured_device == dev) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(absorb_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kASmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(absorb_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmemBytes);
-  if (e == cudaSuccess) configured_device = dev;
-  return e;
-}
-
 cudaError_t launch_absorb_attn(const AbsorbParams& p, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
+  static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = configure_absorb(dev);
   if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(absorb_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)L2<false>::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(absorb_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)L2<true>::kSmem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(2 * p.n_items);
-  cfg.blockDim = dim3(kAThreads);
-  cfg.dynamicSmemBytes = kASmemBytes;
+  cfg.gridDim = dim3(4 * p.n_items);
+  cfg.blockDim = dim3(kThreads2);
+  cfg.dynamicSmemBytes = p.fp8_scores ? L2<true>::kSmem : L2<false>::kSmem;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = 4;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;

@@ -212,26 +212,22 @@ struct AbsPiece {
   int32_t k_end;       // one past the last key token
   int32_t row_block0;  // the request's rows were gathered contiguously from this block on
   int32_t slot;        // partial-state slot of split 0 (split i uses slot + i)
-  int32_t n_row_tiles; // ceil(q_count * H / 128)
+  int32_t n_row_tiles; // ceil(q_count * H / 256)
   int32_t n_splits;    // key splits per row tile
-  int32_t split_keys;  // keys per split (a multiple of 64)
+  int32_t split_keys;  // keys per split (a multiple of 128)
   int32_t item_begin;  // first work item of this piece in the launch
   int64_t rope_offset;
 };
 constexpr int kMaxAbsPieces = 448;
 
+// The latent attention (absorb.cu): items of 256 rows, 128-key tiles on two CTA pairs.
 struct AbsorbParams {
-  CUtensorMap tm_c4;   // gathered rows: half the latent part of 64 rows as 4 swizzled [64 x 64] blocks
-  CUtensorMap tm_kr;   // gathered rows, box 64 x 64 (k_rope at column 512)
-  CUtensorMap tm_qlat; // qlat as [T_q * H rows][512], box 64 x 128
-  // E4M3 scores (fp8_scores): the cache's FP8 rows gathered as stored (640 B)
-  CUtensorMap tm_f8;    // their latent codes as 4 swizzled [64 rows x 128 B] blocks
-  CUtensorMap tm_kr8;   // their k_rope as bf16 [rows][320], box 64 x 64 at column 256
-  CUtensorMap tm_qlat8; // E4M3 qlat as [T_q * H rows][512 B], box 128 x 128
-  // absorb_attn2_kernel (items of 256 rows, 128-key tiles on CTA pairs)
+  CUtensorMap tm_qlat;  // qlat as [T_q * H rows][512], box 64 x 128
   CUtensorMap tm_c3;    // gathered bf16 rows as 9 blocks of 64 columns ([c | k_rope]), box 64 cols x 64 rows x 3 blocks
-  CUtensorMap tm_f5;    // FP8 rows as stored as 5 blocks of 128 B, box 128 x 64 x 5
   CUtensorMap tm_c2;    // gathered bf16 rows, latent blocks, box 64 x 64 x 2
+  // E4M3 scores (fp8_scores): the cache's FP8 rows gathered as stored (640 B)
+  CUtensorMap tm_f5;    // as 5 blocks of 128 B (4 of E4M3 codes, k_rope as bf16), box 128 x 64 x 5
+  CUtensorMap tm_qlat8; // E4M3 qlat as [T_q * H rows][512 B], box 128 x 128
   const float* qscale;  // [T_q * H]: the E4M3 qlat row's scale
   float kv_scale;
   int fp8_scores;
@@ -246,8 +242,6 @@ struct AbsorbParams {
   int n_pieces;
   int n_items;
   float scale_log2;
-  unsigned long long* trace;   // optional: per-tile timestamps of work item trace_item (see absorb.cu)
-  int trace_item;
   uint64_t rope_frac[kDr / 2];
   AbsPiece pieces[kMaxAbsPieces];
 };
@@ -289,7 +283,6 @@ struct ProjParams {
 };
 
 cudaError_t launch_absorb_attn(const AbsorbParams& p, cudaStream_t s);
-cudaError_t launch_absorb_attn2(const AbsorbParams& p, cudaStream_t s);
 cudaError_t launch_qabsorb(const QAbsorbParams& p, cudaStream_t s);
 cudaError_t launch_absorb_proj(const ProjParams& p, cudaStream_t s);
 

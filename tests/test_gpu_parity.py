@@ -629,24 +629,6 @@ def test_absorbed_fp8_scores_long_context_sampled(api):
                             visible_keys(wl)[rows])
 
 
-def test_absorbed_alternate_kernels_match_oracle():
-    """Each score precision has a default latent attention kernel (bf16: the
-    two-pair kernel with 128-key tiles; E4M3: the one-pair kernel with 64-key
-    tiles).  MLA_ABS_KERNEL forces the other one; it passes the same absorbed
-    parity cases (run in a child process, since the library reads the
-    variable once)."""
-    import os
-    import subprocess
-    import sys
-    runs = (("1", "absorbed and not fp8_scores and not alternate"), ("2", "absorbed_fp8_scores and not alternate"))
-    for k, sel in runs:
-        env = dict(os.environ, MLA_ABS_KERNEL=k)
-        r = subprocess.run([sys.executable, "-m", "pytest", __file__, "-q", "-m", "gpu", "-k", sel,
-                            "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=900)
-        assert r.returncode == 0, f"MLA_ABS_KERNEL={k}:\n" + r.stdout[-4000:]
-        assert " passed" in r.stdout and " error" not in r.stdout
-
-
 def test_absorbed_fp8_scores_needs_fp8_cache(api):
     from mla_prefix_cache_gb300 import _lib
     wl = W.make_workload("afb", 2, [128], [4], chunk=64, seed=92)
