@@ -789,6 +789,7 @@ def run_ours(args):
     flops = wl.algorithmic_flops()
     value = weak_scaling_value(flops, K, world, total_ms) / 1e12
     tok_s = weak_scaling_value(wl.total_q, K, world, total_ms)
+    scan_tok_s = weak_scaling_value(int(wl.ctx_lens.sum()), K, world, total_ms)   # cached tokens attended per s
     e2e = None
     if res["e2e_ms"] is not None:
         ems = max_over_ranks(res["e2e_ms"], world, dev)
@@ -840,6 +841,7 @@ def run_ours(args):
                                              "synchronize outside the step events; the events hold the "
                                              "call's host planning and launches too)"}),
         "prefill_tok_s": tok_s,
+        "context_scan_tok_s": scan_tok_s,
         "frac_of_bf16_peak": value / world / peak,
         "roofline": roof,
         "host_us_per_call": res["host_us"],
