@@ -7,11 +7,12 @@
 // context chunks and extend stage) in one pass, which equals the pages'
 // sequential fold up to rounding.
 //
-// One warp per (row, head) of W values (W = 128 for attention outputs, 512 for
-// the latent states of the absorbed path): lane i owns float4 columns
-// i, i + 32, ..., so every load/store is a 16-byte vector and a warp moves 512
-// contiguous bytes per access.  The output may alias slot 0 of the states:
-// each lane writes only the columns it read, after a warp barrier.
+// The n-state form: an 8-lane group per (row, head) of W values (W = 128 for
+// attention outputs, 512 for the latent states of the absorbed path), four
+// consecutive (row, head) items per warp, so a warp reads each slot as 4 W x 4
+// contiguous bytes; the lse of a row's slots is read once, one slot per lane.
+// The output may alias slot 0 of the states: each lane writes only the
+// columns it read, after a warp barrier.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -22,15 +23,20 @@ constexpr int kWarpsPerBlock = 8;
 
 template <int W>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_slots_kernel(const __grid_constant__ MergeParams p) {
-  constexpr int kV = W / 128;   // float4 columns per lane
-  const int lane = threadIdx.x & 31;
+  // an 8-lane group per (row, head) item, four consecutive items per warp: each slot is read as 4 x W x 4
+  // contiguous bytes; lane q of a group owns float4 columns q, q + 8, ... of its item
+  constexpr int kV = W / 32;                  // float4 columns per lane
+  constexpr int kUnroll = W == 128 ? 4 : 1;   // slots whose loads are in flight together
+  const int lane = threadIdx.x & 31, grp = lane >> 3, q = lane & 7;
   const int64_t wid = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int H = p.num_heads;
   const int64_t total = (int64_t)p.total_rows * H;
-  for (int64_t item = wid; item < total; item += (int64_t)gridDim.x * kWarpsPerBlock) {
+  for (int64_t base = wid * 4; base < total; base += (int64_t)gridDim.x * kWarpsPerBlock * 4) {
+    const int64_t item = base + grp;
+    const bool live_item = item < total;
     // item -> (range, row within range, head); ranges are consecutive in item space
-    const int64_t local = item / H;
-    const int h = (int)(item - local * H);
+    const int64_t local = live_item ? item / H : 0;
+    const int h = live_item ? (int)(item - local * H) : 0;
     int lo = 0, hi = p.num_ranges - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -38,47 +44,60 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_slots_kernel(const 
     }
     const int ri = lo;
     const int64_t row = p.ranges[ri].row_begin + (local - p.ranges[ri].prefix);
-    const int ns = p.ranges[ri].nslots;
+    const int ns = live_item ? p.ranges[ri].nslots : 0;
+    auto lse_at = [&](int s) { return __ldg(p.part_lse + ((int64_t)s * p.slot_stride_rows + row) * H + h); };
 
+    // lane q holds the lse of slots q, q + 8, ...: one round trip for all of them, then group maxima
     float m = -INFINITY;
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) m = fmaxf(m, __ldg(p.part_lse + ((int64_t)s * p.slot_stride_rows + row) * H + h));
+    for (int s0 = 0; s0 < ns; s0 += 8) m = fmaxf(m, s0 + q < ns ? lse_at(s0 + q) : -INFINITY);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float4 acc[kV];
 #pragma unroll
     for (int v = 0; v < kV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
-    if (m != -INFINITY) {
-      // Predicated rather than branched, so the unrolled loads of several
-      // slots are in flight together; an empty state (lse = -inf) adds 0.
-#pragma unroll 4
-      for (int s = 0; s < ns; ++s) {
-        const int64_t g = ((int64_t)s * p.slot_stride_rows + row) * H + h;
-        const float l = __ldg(p.part_lse + g);
-        const bool live = (l != -INFINITY);
-        const float w = live ? __expf(l - m) : 0.f;
+    // every lane of the warp runs the same number of slot rounds (the groups' items may differ)
+    int ns_max = ns;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ns_max = max(ns_max, __shfl_xor_sync(0xffffffffu, ns_max, o));
+    for (int s0 = 0; s0 < ns_max; s0 += 8) {
+      // this lane's slot weight (0 for an empty or absent state); the states are then read together,
+      // each slot's weight taken from the lane of the group that holds it
+      const float l = s0 + q < ns ? lse_at(s0 + q) : -INFINITY;
+      const float w = (l == -INFINITY || m == -INFINITY) ? 0.f : __expf(l - m);
+      float ws = w;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+      wsum += ws;
+      const int n = min(8, ns_max - s0);
+#pragma unroll kUnroll
+      for (int i = 0; i < n; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, w, (lane & ~7) + i);
+        const int64_t g = ((int64_t)(s0 + i) * p.slot_stride_rows + row) * H + h;
 #pragma unroll
         for (int v = 0; v < kV; ++v) {
           float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (live) o = reinterpret_cast<const float4*>(p.part_out + g * W)[lane + 32 * v];
-          acc[v].x += w * o.x; acc[v].y += w * o.y; acc[v].z += w * o.z; acc[v].w += w * o.w;
+          if (wi != 0.f) o = __ldg(reinterpret_cast<const float4*>(p.part_out + g * W) + q + 8 * v);
+          acc[v].x += wi * o.x; acc[v].y += wi * o.y; acc[v].z += wi * o.z; acc[v].w += wi * o.w;
         }
-        wsum += w;
       }
     }
     const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
     const int64_t orow = row * H + h;
     __syncwarp();   // every lane has read the states (the output may alias slot 0)
+    if (live_item) {
 #pragma unroll
-    for (int v = 0; v < kV; ++v) {
-      const float4 r = make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
-      if (p.out_bf16) {
-        uint2 b = make_uint2(pack_bf16(r.x, r.y), pack_bf16(r.z, r.w));
-        reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * W)[lane + 32 * v] = b;
-      } else {
-        reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * W)[lane + 32 * v] = r;
+      for (int v = 0; v < kV; ++v) {
+        const float4 r = make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
+        if (p.out_bf16) {
+          uint2 b = make_uint2(pack_bf16(r.x, r.y), pack_bf16(r.z, r.w));
+          reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * W)[q + 8 * v] = b;
+        } else {
+          reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * W)[q + 8 * v] = r;
+        }
       }
+      if (q == 0) p.lse[orow] = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
     }
-    if (lane == 0) p.lse[orow] = (wsum > 0.f) ? m + logf(wsum) : -INFINITY;
   }
 }
 
@@ -162,7 +181,7 @@ int grid_for(int64_t warps_needed, int warps_per_block) {
 cudaError_t launch_merge_slots(const MergeParams& p, cudaStream_t s) {
   const int64_t items = (int64_t)p.total_rows * p.num_heads;
   if (items == 0) return cudaSuccess;
-  merge_slots_kernel<kDv><<<grid_for(items, kWarpsPerBlock), kWarpsPerBlock * 32, 0, s>>>(p);
+  merge_slots_kernel<kDv><<<grid_for((items + 3) / 4, kWarpsPerBlock), kWarpsPerBlock * 32, 0, s>>>(p);
   count_launch();
   return cudaGetLastError();
 }
@@ -170,7 +189,7 @@ cudaError_t launch_merge_slots(const MergeParams& p, cudaStream_t s) {
 cudaError_t launch_merge_slots_latent(const MergeParams& p, cudaStream_t s) {
   const int64_t items = (int64_t)p.total_rows * p.num_heads;
   if (items == 0) return cudaSuccess;
-  merge_slots_kernel<kDc><<<grid_for(items, kWarpsPerBlock), kWarpsPerBlock * 32, 0, s>>>(p);
+  merge_slots_kernel<kDc><<<grid_for((items + 3) / 4, kWarpsPerBlock), kWarpsPerBlock * 32, 0, s>>>(p);
   count_launch();
   return cudaGetLastError();
 }
