@@ -555,8 +555,9 @@ def auto_compare(dev, flush, reps=5, config="mixed_32k"):
 def reuse_compare(dev, flush, reps=5, config="v3_8k", n_global=16, protected_frac=0.10):
     """Head-split reuse against full recomputation on the same inputs: the
     Global heads (every 8th head: 16 of 128, the RedKnot page's 8 of 64) and
-    a seeded 10% of the query rows recomputed, the rest taken from an
-    artifact.  Median CUDA-event time of a whole call, L2 flushed before each."""
+    a seeded share of the query rows (`protected_frac`) recomputed, the rest
+    taken from an artifact.  Median CUDA-event time of a whole call, L2
+    flushed before each."""
     import torch
     from mla_prefix_cache_gb300 import api, workload
 
@@ -830,6 +831,8 @@ def run_ours(args):
     cmp_reuse = cmp_auto = None
     if not args.no_reuse and world == 1:
         cmp_reuse = reuse_compare(dev, flush)
+        # few protected rows (61 of 2048): the call takes them through the absorbed path
+        cmp_reuse["small_protected_set"] = reuse_compare(dev, flush, protected_frac=0.03)
     if not args.no_auto and world == 1 and not absorbed:
         cmp_auto = auto_compare(dev, flush)
     line = {

@@ -345,7 +345,10 @@ int mla_prefill_ctx_absorbed_fp8(const void* q, const int32_t* q_pos,
  *                      arguments, if h is a Global head or row t is protected;
  *                      (art_out, art_lse)[t, h] otherwise.
  * Only the recomputed (row, head) pairs are computed: the Global heads for
- * every row, and the Local heads for the protected rows.
+ * every row, and the Local heads for the protected rows.  The protected rows
+ * go through the latent-space (absorbed) path when every request has at most
+ * 128 of them and each sees at least 1024 keys (where that path is the
+ * faster one), else through the up-projected kernel.
  *  global_heads   HOST int32 [n_global], head indices in [0, H) (repeats ignored).
  *  row_protected  HOST uint8 [T_q], nonzero for a protected row; NULL: none.
  *  art_out        device fp32 [T_q, H, 128];  art_lse  device fp32 [T_q, H].

@@ -874,7 +874,8 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
                             int num_blocks, const int32_t* block_table, int max_blocks, int H, const void* kv_b_proj,
                             float softmax_scale, float rope_theta, void* out, int out_dtype, float* lse,
                             void* workspace, const FusedPlan& fp, const AbsPlan& ap, const AbsWs& aw,
-                            cudaStream_t s, bool fp8_scores = false, uint32_t* err_word = nullptr) {
+                            cudaStream_t s, bool fp8_scores = false, uint32_t* err_word = nullptr,
+                            const int32_t* q_tok = nullptr) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int64_t T_q = fp.total_q;
   static AbsorbParams p;           // large; built on the host under a lock
@@ -977,6 +978,7 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
   p.q = static_cast<const uint16_t*>(q);
   p.qlat = reinterpret_cast<const uint16_t*>(ws + aw.qlat_off);
   p.q_pos = q_pos;
+  p.q_tok = q_tok;
   p.lat_out = reinterpret_cast<float*>(ws + aw.lat_out_off);
   p.lat_lse = reinterpret_cast<float*>(ws + aw.lat_lse_off);
   p.slot_stride_rows = T_q * H;
@@ -1086,11 +1088,22 @@ static int prefill_plans(const void* q, const int32_t* q_pos, const void* kv_cac
 }
 
 // ------------------------------------------------------------------ head-split reuse
+// A request with at most this many queries goes through the absorbed path,
+// the others through the up-projected one.  On GB300 (128 heads, 32K cached
+// tokens) the two break even near 155 queries: the absorbed path is 1.27x at
+// 128 and 0.98x at 160; on a 128K FP8 cache (E4M3 scores) it is 1.40x at 128
+// and 0.99x at 192.  The FLOP counts alone would put it near 170, but the up-projected
+// kernel runs its MMAs closer to peak.
+constexpr int kAutoAbsorbedMaxQueries = 128;
+
 struct ReusePlan {
   std::vector<int32_t> global, local, prot_rows, prot_tok, gidx, lidx, pidx, cu_p, ctx;
   Plan plan_g, plan_p;
   FusedPlan fp_g, fp_p;
   FusedWs fw_g, fw_p;
+  bool prot_absorbed = false;      // the protected part goes through the absorbed path
+  AbsPlan ap_p;
+  AbsWs aw_p;
   size_t off_maps = 0, off_qg = 0, off_wg = 0, off_og = 0, off_lg = 0, off_qp = 0, off_posp = 0, off_tokp = 0,
          off_wp = 0, off_op = 0, off_lp = 0, off_fused = 0, total = 0;
   size_t map_words = 0;
@@ -1151,14 +1164,34 @@ static int build_reuse_plan(int num_reqs, const int32_t* seq_lens, const int32_t
     rp->fw_g = fused_ws_layout(rp->fp_g, nG);
     fused_bytes = std::max(fused_bytes, rp->fw_g.total);
   }
+  rp->prot_absorbed = false;
   if (nP > 0 && nL > 0) {
     if ((st = build_plan(num_reqs, seq_lens, rp->cu_p.data(), nL, segs, nseg, chunk, parts, &rp->plan_p,
                          rp->ctx.data())) != MLA_OK)
       return st;
     build_fused_plan(rp->plan_p, seq_lens, rp->cu_p.data(), num_reqs, chunk, true, &rp->fp_p, rp->ctx.data(),
                      rp->prot_tok.data());
-    rp->fw_p = fused_ws_layout(rp->fp_p, nL);
-    fused_bytes = std::max(fused_bytes, rp->fw_p.total);
+    // The protected rows take the absorbed path when it is the faster one for every request (at most
+    // kAutoAbsorbedMaxQueries of them) and no row needs exact scores (each sees kExactKeys keys or more,
+    // counting its context and causal extend keys).
+    bool absorbed = true;
+    for (int r = 0; r < num_reqs && absorbed; ++r) {
+      const int np_r = rp->cu_p[r + 1] - rp->cu_p[r];
+      if (np_r == 0) continue;
+      const int64_t first_keys = ((parts & MLA_PART_CONTEXT) ? (int64_t)rp->ctx[r] : 0) +
+                                 ((parts & MLA_PART_EXTEND) ? (int64_t)rp->prot_tok[rp->cu_p[r]] - rp->ctx[r] + 1 : 0);
+      absorbed = np_r <= kAutoAbsorbedMaxQueries && first_keys >= kExactKeys;
+    }
+    if (env_int("MLA_REUSE_ABSORBED", 1) == 0) absorbed = false;
+    if (absorbed) {
+      build_abs_plan(rp->fp_p, nL, rp->cu_p.data(), num_reqs, &rp->ap_p);
+      rp->aw_p = abs_ws_layout(rp->fp_p, rp->ap_p, nL);
+      fused_bytes = std::max(fused_bytes, rp->aw_p.total);
+      rp->prot_absorbed = true;
+    } else {
+      rp->fw_p = fused_ws_layout(rp->fp_p, nL);
+      fused_bytes = std::max(fused_bytes, rp->fw_p.total);
+    }
   }
   rp->map_words = 2 * (size_t)H + (size_t)T_q + 2 * (size_t)nP + (size_t)nG + (size_t)nL;
   rp->off_fused = 0;
@@ -1228,11 +1261,18 @@ static int prefill_reuse(const void* q, const int32_t* q_pos, const void* kv_cac
     if ((st = cuda_status(launch_gather_q(qb, q_pos, d_prows, d_local, nP, nL, H, qp, posp, s))) != MLA_OK)
       return st;
     if ((st = cuda_status(launch_gather_w(wb, d_local, nL, H, wp, s))) != MLA_OK) return st;
-    if ((st = prefill_fused(qp, posp, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks, nL, wp,
-                            softmax_scale, rope_theta, ws + rp.off_op, MLA_OUT_FP32,
-                            reinterpret_cast<float*>(ws + rp.off_lp), fused_ws, rp.fp_p, rp.fw_p, s, d_ptok,
-                            true)) != MLA_OK)
+    if (rp.prot_absorbed) {
+      if ((st = prefill_absorbed(qp, posp, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks, nL, wp,
+                                 softmax_scale, rope_theta, ws + rp.off_op, MLA_OUT_FP32,
+                                 reinterpret_cast<float*>(ws + rp.off_lp), fused_ws, rp.fp_p, rp.ap_p, rp.aw_p, s,
+                                 false, reinterpret_cast<uint32_t*>(ws), d_ptok)) != MLA_OK)
+        return st;
+    } else if ((st = prefill_fused(qp, posp, kv_cache, kv_dtype, kv_scale, num_blocks, block_table, max_blocks, nL,
+                                   wp, softmax_scale, rope_theta, ws + rp.off_op, MLA_OUT_FP32,
+                                   reinterpret_cast<float*>(ws + rp.off_lp), fused_ws, rp.fp_p, rp.fw_p, s, d_ptok,
+                                   true)) != MLA_OK) {
       return st;
+    }
   }
   ReuseAssemble ra;
   ra.out_g = reinterpret_cast<const float*>(ws + rp.off_og);
@@ -1255,13 +1295,6 @@ static int prefill_reuse(const void* q, const int32_t* q_pos, const void* kv_cac
 }
 
 // ------------------------------------------------------------------ per-request dispatch
-// A request with at most this many queries goes through the absorbed path,
-// the others through the up-projected one.  On GB300 (128 heads, 32K cached
-// tokens) the two break even near 155 queries: the absorbed path is 1.27x at
-// 128 and 0.98x at 160; on a 128K FP8 cache (E4M3 scores) it is 1.40x at 128
-// and 0.99x at 192.  The FLOP counts alone would put it near 170, but the up-projected
-// kernel runs its MMAs closer to peak.
-constexpr int kAutoAbsorbedMaxQueries = 128;
 
 struct AutoPlan {
   Plan plan_f, plan_a;

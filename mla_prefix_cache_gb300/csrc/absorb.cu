@@ -157,7 +157,8 @@ __device__ AItem decode_item(const AbsorbParams& p, int item) {
   // the item's last query token bounds its causal keys
   const int rows = P.q_count * p.num_heads;
   const int last_t = min(rows - 1, it.row0 + 255) / p.num_heads;
-  const int k_hi_item = min(P.k_end, P.q_tok0 + last_t + 1);
+  const int last_tok = p.q_tok ? __ldg(p.q_tok + P.q_begin + last_t) : P.q_tok0 + last_t;   // rows in token order
+  const int k_hi_item = min(P.k_end, last_tok + 1);
   it.k_lo = P.k_begin + split * P.split_keys;
   it.k_hi = min(it.k_lo + P.split_keys, k_hi_item);
   it.t0 = it.k_lo & ~127;
@@ -335,7 +336,8 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
           mbar_arrive_cluster(mapa_shared(bar(kQR), 0u));   // release: this CTA's q_rope and TMEM rows
         }
       }
-      const int qk = live ? P.q_tok0 + tl : -1;   // last visible key token of the row
+      // last visible key token of the row
+      const int qk = live ? (p.q_tok ? __ldg(p.q_tok + grow) : P.q_tok0 + tl) : -1;
       const float sl2 = p.scale_log2 * qs;
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;

@@ -234,6 +234,7 @@ struct AbsorbParams {
   const uint16_t* q;     // [T_q][H][192]: q_rope at 128..191, not rotated
   const uint16_t* qlat;  // [T_q][H][512] bf16: kv_scale * q_nope W_UK,h^T
   const int32_t* q_pos;
+  const int32_t* q_tok;  // optional [T_q]: each row's token index (compacted rows); else q_tok0 + row
   float* lat_out;        // [slots][T_q * H][512] fp32, normalised by the row sum
   float* lat_lse;        // [slots][T_q * H], natural log
   int64_t slot_stride_rows;   // T_q * H

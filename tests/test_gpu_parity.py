@@ -467,11 +467,21 @@ REUSE_CASES = [
     dict(H=128, ctx=[300], ext=[130], chunk=128, glob=list(range(0, 128, 8)), prot=[0, 64, 127, 128, 129]),
     dict(H=5, ctx=[200], ext=[50], chunk=128, glob=[0, 1, 2, 3, 4], prot=[]),          # every head Global
     dict(H=5, ctx=[200], ext=[50], chunk=128, glob=[], prot=[]),                       # all from the artifact
+    # protected rows that take the absorbed path (at most 128 a request, each seeing 1024 keys or more)
+    dict(H=8, ctx=[1100, 2048], ext=[90, 40], chunk=512, glob=[2, 5], prot=[0, 7, 50, 89, 90, 95, 129]),
+    dict(H=6, ctx=[1536], ext=[64], chunk=256, doc=512, glob=[0], prot=[1, 2, 30, 63]),
+    dict(H=4, ctx=[1200], ext=[33], chunk=256, kv="fp8_e4m3", glob=[3], prot=list(range(0, 33, 4))),
 ]
 
 
-@pytest.mark.parametrize("case", REUSE_CASES, ids=["batch", "docs", "fp8", "h128", "all_global", "all_artifact"])
-def test_prefill_reuse_matches_oracle(api, case):
+@pytest.mark.parametrize("case", REUSE_CASES, ids=["batch", "docs", "fp8", "h128", "all_global", "all_artifact",
+                                                   "absorbed_batch", "absorbed_docs", "absorbed_fp8"])
+def test_prefill_reuse_matches_oracle(api, case, monkeypatch):
+    """Each case through the call's own choice for its protected rows, and,
+    where that is the absorbed path (at most 128 protected rows a request,
+    each seeing 1024 keys or more), again with the up-projected path forced
+    (MLA_REUSE_ABSORBED=0): both meet the oracle, and the two routes launch
+    different kernels."""
     from oracle import head_reuse as R
     wl = W.make_workload("ru", case["H"], case["ctx"], case["ext"], chunk=case["chunk"],
                          kv_dtype=case.get("kv", "bf16"), doc_len=case.get("doc"), seed=70)
@@ -479,20 +489,29 @@ def test_prefill_reuse_matches_oracle(api, case):
     rng = np.random.default_rng(71)
     art_out = rng.standard_normal((wl.total_q, wl.num_heads, 128)).astype(np.float32)
     art_lse = rng.standard_normal((wl.total_q, wl.num_heads)).astype(np.float32)
-    out, lse = api.prefill_reuse(dw.q, dw.q_pos, dw.kv_cache, dw.block_table, wl.seq_lens, wl.cu_q, dw.kv_b_proj,
-                                 torch.from_numpy(art_out).cuda(), torch.from_numpy(art_lse).cuda(),
-                                 global_heads=case["glob"], protected_rows=case["prot"], chunk=wl.chunk,
-                                 softmax_scale=wl.softmax_scale, kv_scale=wl.kv_scale, segments=wl.segments)
-    torch.cuda.synchronize()
-    assert api.device_error(api.prefill_reuse.last_workspace) == 0
-    out, lse = out.cpu().numpy(), lse.cpu().numpy()
     ref_out, ref_lse = R.prefill_reuse(O.workload_args(wl), case["glob"], case["prot"], art_out, art_lse)
     m = R.reuse_mask(wl.total_q, wl.num_heads, case["glob"], case["prot"])
-    # reused entries are copied bit for bit; recomputed ones meet the attention tolerances
-    assert np.array_equal(out[~m], art_out[~m]) and np.array_equal(lse[~m], art_lse[~m])
-    if m.any():
-        nvis = np.broadcast_to(visible_keys(wl)[:, None], m.shape)[m]
-        assert_close(out[m][:, None], lse[m][:, None], ref_out[m][:, None], ref_lse[m][:, None], nvis)
+    nvis = np.broadcast_to(visible_keys(wl)[:, None], m.shape)[m]
+    protected_absorbed = min(case["ctx"]) + 1 >= 1024 and bool(case["prot"]) and len(case["glob"]) < case["H"]
+    launches = []
+    for forced_fused in ([False, True] if protected_absorbed else [False]):
+        if forced_fused:
+            monkeypatch.setenv("MLA_REUSE_ABSORBED", "0")
+        n0 = api.launch_count()
+        out, lse = api.prefill_reuse(dw.q, dw.q_pos, dw.kv_cache, dw.block_table, wl.seq_lens, wl.cu_q,
+                                     dw.kv_b_proj, torch.from_numpy(art_out).cuda(), torch.from_numpy(art_lse).cuda(),
+                                     global_heads=case["glob"], protected_rows=case["prot"], chunk=wl.chunk,
+                                     softmax_scale=wl.softmax_scale, kv_scale=wl.kv_scale, segments=wl.segments)
+        torch.cuda.synchronize()
+        launches.append(api.launch_count() - n0)
+        assert api.device_error(api.prefill_reuse.last_workspace) == 0
+        out, lse = out.cpu().numpy(), lse.cpu().numpy()
+        # reused entries are copied bit for bit; recomputed ones meet the attention tolerances
+        assert np.array_equal(out[~m], art_out[~m]) and np.array_equal(lse[~m], art_lse[~m])
+        if m.any():
+            assert_close(out[m][:, None], lse[m][:, None], ref_out[m][:, None], ref_lse[m][:, None], nvis)
+    if protected_absorbed:
+        assert launches[0] != launches[1]
 
 
 def test_prefill_reuse_reports_bad_blocks(api):
