@@ -309,7 +309,7 @@ def fused_kernel_name():
 
 KERNEL_SOURCES = {
     "fused": ("fused2.cu", "fused_common.cuh", "ptx.cuh", "internal.h"),
-    "absorbed": ("absorb.cu", "ptx.cuh", "internal.h"),
+    "absorbed": ("absorb.cu", "absorb.h", "ptx.cuh", "internal.h"),
 }
 
 

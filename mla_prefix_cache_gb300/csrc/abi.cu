@@ -12,6 +12,7 @@
 #include <mutex>
 #include <vector>
 
+#include "absorb.h"
 #include "internal.h"
 #include "mla.h"
 

@@ -33,6 +33,7 @@
 //    latent state.
 // Each key is read from L2 once per 256 rows by the S pair and once by the O
 // pair, half of it by each CTA.
+#include "absorb.h"
 #include "internal.h"
 #include "ptx.cuh"
 

@@ -10,6 +10,7 @@
 // kv_b_proj is [512][H * 256]: W_UK,h[c][d] at column 128 h + d, W_UV,h[c][j]
 // at column 128 H + 128 h + j.  So W_UK,h is K-major for the q absorption (K =
 // d) and W_UV,h is MN-major for the projection (K = c, N = j contiguous).
+#include "absorb.h"
 #include "internal.h"
 #include "ptx.cuh"
 
