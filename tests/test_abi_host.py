@@ -182,6 +182,21 @@ def test_absorbed_entry_validates_and_sizes(lib):
     assert lib.mla_prefill_absorbed_workspace_size(1, sl2, cq, 8, None, 0, 128, 3) > _ws(lib, [320], [0, 64], 8, chunk=128)
 
 
+def test_absorbed_plan_joins_chunk_pieces_and_spreads_single_rows(lib):
+    """The absorbed planner's choices, seen through its workspace (one latent
+    state slot per key split): a short extend over 32K cached tokens in 16K
+    chunks plans one uncut key range (32 items of 256 rows fill the GPU's
+    clusters in one wave, so no merge); one new token (a single item of 128
+    rows) is cut into many key splits so that it spreads over the GPU."""
+    blocks = (32768 + 64 + 63) // 64
+    sl, cq = (ctypes.c_int32 * 1)(32768 + 64), (ctypes.c_int32 * 2)(0, 64)
+    n = lib.mla_prefill_absorbed_workspace_size(1, sl, cq, 128, None, 0, 16384, 3)
+    assert _abs_layout(blocks, 64 * 128, 1) < n < _abs_layout(blocks, 64 * 128, 2)
+    sl1, cq1 = (ctypes.c_int32 * 1)(32768 + 1), (ctypes.c_int32 * 2)(0, 1)
+    n1 = lib.mla_prefill_absorbed_workspace_size(1, sl1, cq1, 128, None, 0, 16384, 3)
+    assert n1 > _abs_layout((32768 + 1 + 63) // 64, 128, 16)
+
+
 def test_fp8_score_and_reuse_workspaces(lib):
     """Host-side sizing of the FP8-score absorbed path and of head-split reuse."""
     sl, cq = (ctypes.c_int32 * 1)(1100), (ctypes.c_int32 * 2)(0, 64)
