@@ -713,18 +713,32 @@ struct AbsPlan {
 // `item_keys` of start and epilogue; a request cut into several slots adds the
 // merge of its latent states (a pass over the whole GPU), `merge_keys_per_row`
 // per (row, slot + 1).
+// With `bound` > 0 it stops at a lower bound (the items' work spread evenly,
+// plus the merge) when that is already at least `bound`, returns it and sets
+// *bounded.
 static double abs_split_cost(const std::vector<Piece>& pieces, int H, int64_t rows_per_item, int split,
-                             int clusters, double item_keys, double merge_keys_per_row, int num_reqs) {
+                             int clusters, double item_keys, double merge_keys_per_row, int num_reqs,
+                             double bound = 0.0, bool* bounded = nullptr) {
   std::vector<std::pair<int, int64_t>> groups;   // (item length in keys, item count)
   std::vector<int> slots(num_reqs, 0);
   std::vector<int64_t> rows(num_reqs, 0);
+  double work = 0.0;
   for (const Piece& pc : pieces) {
     const int keys = pc.k_end - pc.k_begin;
     const int ns = std::max(1, (keys + split - 1) / split);
     const int64_t r_items = (pc.q_count * (int64_t)H + rows_per_item - 1) / rows_per_item;
     groups.push_back({(keys + ns - 1) / ns, r_items * ns});
+    work += (double)r_items * ns * ((keys + ns - 1) / ns + item_keys);
     slots[pc.req] += ns;
     rows[pc.req] = pc.q_count * (int64_t)H;
+  }
+  double merge = 0.0;
+  for (int r = 0; r < num_reqs; ++r)
+    if (slots[r] > 1) merge += merge_keys_per_row * (double)rows[r] * (slots[r] + 1);
+  const double lower = work / clusters + merge;
+  if (bound > 0.0 && lower >= bound) {
+    if (bounded) *bounded = true;
+    return lower;
   }
   std::sort(groups.begin(), groups.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
   std::vector<double> load(clusters, 0.0);
@@ -739,10 +753,7 @@ static double abs_split_cost(const std::vector<Piece>& pieces, int H, int64_t ro
       for (int i = 0; i < rem; ++i) load[i] += len;
     }
   }
-  double t = *std::max_element(load.begin(), load.end());
-  for (int r = 0; r < num_reqs; ++r)
-    if (slots[r] > 1) t += merge_keys_per_row * (double)rows[r] * (slots[r] + 1);
-  return t;
+  return *std::max_element(load.begin(), load.end()) + merge;
 }
 
 // The absorbed path's pieces: the fused plan's pieces of a request that share
@@ -801,18 +812,26 @@ static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int 
   for (const Piece& pc : pieces) k_max = std::max(k_max, pc.k_end - pc.k_begin);
   auto round_split = [&](int v) { return std::max(512, (v + key_tile - 1) & ~(key_tile - 1)); };
   int split = round_split(std::max(k_max, 1));
-  double best = abs_split_cost(pieces, H, rows_per_item, split, clusters, item_keys, merge_keys_per_row, num_reqs);
-  for (int ways = 2; ways <= 64 && k_max > 512; ++ways) {
+  const int forced = env_int("MLA_ABS_SPLIT_KEYS", 0);
+  double best = forced > 0 ? 0.0
+                           : abs_split_cost(pieces, H, rows_per_item, split, clusters, item_keys, merge_keys_per_row,
+                                            num_reqs);
+  int last = split;
+  for (int ways = 2; ways <= 64 && k_max > 512 && forced <= 0; ++ways) {
     const int cand = round_split((k_max + ways - 1) / ways);
-    if (cand >= split) continue;
+    if (cand >= last) continue;   // the same cut as a fewer-way one once rounded
+    last = cand;
+    // finer cuts only add items (each with its start and epilogue) and slots to merge, so once the
+    // lower bound of a cut reaches the best estimate the search ends
+    bool bounded = false;
     const double c = abs_split_cost(pieces, H, rows_per_item, cand, clusters, item_keys, merge_keys_per_row,
-                                    num_reqs);
+                                    num_reqs, best * 0.99, &bounded);
+    if (bounded) break;
     if (c < best * 0.99) {   // a split must buy a clear gain: more items and slots cost workspace
       best = c;
       split = cand;
     }
   }
-  const int forced = env_int("MLA_ABS_SPLIT_KEYS", 0);
   if (forced > 0) split = (forced + key_tile - 1) & ~(key_tile - 1);
   std::vector<int> next_slot(num_reqs, 0);
   for (const Piece& pc : pieces) {
