@@ -245,39 +245,45 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
       // the last commits land on this CTA's barriers before it exits
       for (int u = max(0, U - SS::kRing); u < U && ok; ++u)
         if (!await2(p, bar(kSE + u % SS::kRing), (u / SS::kRing) & 1)) ok = false;
-    } else if (warp == 1 && lane == 0 && first && n > 0) {
+    } else if (warp == 1 && first && n > 0) {
       // ---------------------------------------------------------- S = Q [c | k_rope]^T, N = 128 keys
-      bool ok = await2(p, bar(kQR), 0);
+      // (the whole warp runs the loop; one elected lane issues each MMA)
+      bool ok = await2_warp(p, bar(kQR), 0);
+      const uint64_t qd = sdesc_sw128(sbase + SS::kQR, 16, 1024);        // rotated q_rope
+      const uint64_t sd0 = sdesc_sw128(sbase + SS::kStage0, 16, 1024);   // ring stage 0
+      const uint32_t sf0 = bar(kSF), se0 = bar(kSE);
+      int s = 0;          // ring slot of the next stage
+      uint32_t ph = 0;    // and the parity of its fill
       for (int j = 0; j < n && ok; ++j) {
         const int b = j & 1;
-        if (j >= 2 && !await2(p, bar(kSSR + b), ((j >> 1) - 1) & 1)) { ok = false; break; }
+        if (j >= 2 && !await2_warp(p, bar(kSSR + b), ((j >> 1) - 1) & 1)) { ok = false; break; }
         const uint32_t d = tmem + 256 + 128 * b;
-#pragma unroll 1
-        for (int m = 0; m < SS::kStagesPerTile && ok; ++m) {
-          const int u = j * SS::kStagesPerTile + m, s = u % SS::kRing;
-          if (!await2(p, bar(kSF + s), (u / SS::kRing) & 1)) { ok = false; break; }
+#pragma unroll
+        for (int m = 0; m < SS::kStagesPerTile; ++m) {
+          if (!await2_warp(p, sf0 + 8u * s, ph)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t st = sbase + SS::kStage0 + s * SS::kStage;
+          const uint64_t sd = sdesc_add(sd0, s * SS::kStage);
+          const uint32_t ta = tmem + 32 * SS::kSBlocks * m;   // qlat columns of the stage's latent blocks
 #pragma unroll
           for (int kb = 0; kb < SS::kSBlocks; ++kb) {
-            const int g = m * SS::kSBlocks + kb;
-            if (g < SS::kLatBlocks) {
+            if (m * SS::kSBlocks + kb < SS::kLatBlocks) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bd = sdesc_sw128(st + kb * kBlk + kk * 32, 16, 1024);
-                if (kF8) mma2_ts_e4m3(d, tmem + 32 * g + 8 * kk, bd, kIdS2f8, (g | kk) ? 1u : 0u);
-                else mma2_ts(d, tmem + 32 * g + 8 * kk, bd, kIdS2, (g | kk) ? 1u : 0u);
+                const uint64_t bd = sdesc_add(sd, kb * kBlk + kk * 32);
+                const uint32_t acc = (m | kb | kk) ? 1u : 0u;
+                if (kF8) mma2_ts_e4m3_elect(d, ta + 32 * kb + 8 * kk, bd, kIdS2f8, acc);
+                else mma2_ts_elect(d, ta + 32 * kb + 8 * kk, bd, kIdS2, acc);
               }
             } else {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma2_ss(d, sdesc_sw128(sbase + SS::kQR + kk * 32, 16, 1024),
-                        sdesc_sw128(st + kb * kBlk + kk * 32, 16, 1024), kIdS2, 1u);
+                mma2_ss_elect(d, sdesc_add(qd, kk * 32), sdesc_add(sd, kb * kBlk + kk * 32), kIdS2, 1u);
             }
           }
-          mma2_commit_mc(bar(kSE + s), kMaskS);
+          mma2_commit_mc_elect(se0 + 8u * s, kMaskS);
+          if (++s == SS::kRing) { s = 0; ph ^= 1u; }
         }
-        if (ok) mma2_commit_mc(bar(kSSF + b), kMaskS);
+        if (ok) mma2_commit_mc_elect(bar(kSSF + b), kMaskS);
       }
     } else if (warp >= 4) {
       // ---------------------------------------------------------- Q -> TMEM and shared memory, then softmax
@@ -357,10 +363,6 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && wok) mbar_arrive_cluster_relaxed(ssr0 + 8u * b);
-        // the staging buffer is free once the previous tile's copy landed; the four warps go on, or
-        // leave, together
-        if (wok && j >= 1) wok = await2_warp(p, bar(kSTF), (j - 1) & 1);
-        if (named_bar_or(1, 128, !wok)) { ok = false; break; }
         const int kt0 = it.t0 + 128 * j;
         if (!(kt0 >= it.k_lo && kt0 + 127 < it.k_hi && kt0 + 127 <= qk)) {
           float m8[8];
@@ -385,24 +387,30 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t sc2 = f2pack(sl2, sl2), nm2 = f2pack(-mref, -mref);
+        // P of the tile in registers while the previous tile's copy is still in flight
         uint64_t s4[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[64];
+        if (wok) {
 #pragma unroll
-        for (int hk = 0; hk < 2; ++hk) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const uint32_t x0u = hk ? v1[2 * c] : v0[2 * c], x1u = hk ? v1[2 * c + 1] : v0[2 * c + 1];
+          for (int c = 0; c < 64; ++c) {
+            const uint32_t x0u = c < 32 ? v0[2 * c] : v1[2 * c - 64], x1u = c < 32 ? v0[2 * c + 1] : v1[2 * c - 63];
             float x0, x1;
             f2unpack(ffma2(f2pack(__uint_as_float(x0u), __uint_as_float(x1u)), sc2, nm2), x0, x1);
             const float a = ex2(x0), bb = ex2(x1);
             s4[c & 3] = fadd2(s4[c & 3], f2pack(a, bb));
             pk[c] = pack_bf16(a, bb);
           }
+        }
+        // the staging buffer is free once the previous tile's copy landed; the four warps go on, or
+        // leave, together
+        if (wok && j >= 1) wok = await2_warp(p, bar(kSTF), (j - 1) & 1);
+        if (named_bar_or(1, 128, !wok)) { ok = false; break; }
+#pragma unroll
+        for (int hk = 0; hk < 2; ++hk)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            sts128(sbase + SS::kPS + hk * kBlk128 + sw128_off((uint32_t)r, (uint32_t)c), pk[4 * c], pk[4 * c + 1],
-                   pk[4 * c + 2], pk[4 * c + 3]);
-        }
+            sts128(sbase + SS::kPS + hk * kBlk128 + sw128_off((uint32_t)r, (uint32_t)c), pk[32 * hk + 4 * c],
+                   pk[32 * hk + 4 * c + 1], pk[32 * hk + 4 * c + 2], pk[32 * hk + 4 * c + 3]);
         float s8[4];
         f2unpack(fadd2(s4[0], s4[1]), s8[0], s8[1]);
         f2unpack(fadd2(s4[2], s4[3]), s8[2], s8[3]);

@@ -146,6 +146,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= (uint64_t)2u << 61;  // 128-byte swizzle
   return d;
 }
+// The descriptor of the operand `off` bytes (a multiple of 16) past the one
+// that `d` describes.  Shared addresses stay below 2^18, so the start-address
+// field (address / 16, bits 0-13) takes off / 16 without a carry into the
+// next field, and one 32-bit add replaces a descriptor build.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t off) {
+  return (d & 0xFFFFFFFF00000000ull) | (uint64_t)((uint32_t)d + (off >> 4));
+}
 
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128B-swizzled tile
 // whose rows are 128 B apart (tile base 1024-B aligned).
@@ -577,6 +584,51 @@ __device__ __forceinline__ void mma2_ts_e4m3(uint32_t d_tmem, uint32_t a_tmem, u
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same MMAs issued by a whole (converged) warp: every lane computes the
+// operands, one lane chosen by elect.sync issues the instruction.  An MMA loop
+// run this way keeps its warp-uniform descriptors and addresses out of a
+// one-lane branch; where the issuing loop itself sets the pace (the latent
+// score MMAs), it issues faster than the same loop in one lane.
+__device__ __forceinline__ void mma2_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_ts_e4m3_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// mma2_commit_mc from one elected lane of a converged warp.
+__device__ __forceinline__ void mma2_commit_mc_elect(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
 // Completion of the pair's MMAs issued so far, signalled on the barrier at the
 // same offset in every CTA of the cluster that `mask` names.
 __device__ __forceinline__ void mma2_commit_mc(uint32_t bar, uint16_t mask) {
