@@ -82,6 +82,7 @@ constexpr uint32_t kOL = kOAlpha + 2 * 512;
 constexpr uint32_t kOFlags = kOL + 512;
 constexpr uint32_t kOC = (kOFlags + 64 + 1023) & ~1023u;
 constexpr int kORing = 4;
+static_assert((kORing & (kORing - 1)) == 0, "the O ring's slot is a mask of the stage use");
 constexpr uint32_t kOStage = 4 * kBlk;
 constexpr uint32_t kOEnd = kOC + kORing * kOStage;
 constexpr uint32_t kTxP2 = 128 * (256 + 4) + 16;   // per row: 128 bf16 of P and one factor; 4 flags
@@ -458,64 +459,74 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
       }
       for (int u = max(0, U - kORing); u < U && ok; ++u)
         if (!await2(p, bar(kCE + u % kORing), (u / kORing) & 1)) ok = false;
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ---------------------------------------------------------- per tile: P landed, rows rescaled; then (first
-      // CTA) O += P c for the pair
-      for (int b = 0; b < min(n, 2); ++b) mbar_arrive_expect_tx(bar(kPF + b), kTxP2);
-      mbar_arrive_expect_tx(bar(kLF), 512);
+      // CTA) O += P c for the pair.  The whole warp runs the loop: lane 0 arrives and arms the barriers, one
+      // elected lane issues each MMA and commit.
+      if (lane == 0) {
+        for (int b = 0; b < min(n, 2); ++b) mbar_arrive_expect_tx(bar(kPF + b), kTxP2);
+        mbar_arrive_expect_tx(bar(kLF), 512);
+      }
       bool ok = true;
       volatile int* hand = reinterpret_cast<volatile int*>(sgen + kOFlags + 32);
       const uint32_t pr0 = mapa_shared(bar(kPR), 2u);
       const uint32_t stf_s = mapa_shared(bar(kSTF), half);   // the S CTA that sends this CTA's P
+      const uint64_t pd0 = sdesc_sw128(sbase + kOP, 16, 1024);     // P tiles, K-major
+      const uint64_t cd0 = sdesc_sw128(sbase + kOC, kBlk, 1024);   // latent stages, MN-major
       int events = 0;
       for (int j = 0; j < n && ok; ++j) {
         const int b = j & 1;
-        if (!await2(p, bar(kPF + b), (j >> 1) & 1)) { ok = false; break; }
-        mbar_arrive_cluster_relaxed(stf_s);   // the S CTA's staging buffer may take the next tile
+        if (!await2_warp(p, bar(kPF + b), (j >> 1) & 1)) { ok = false; break; }
+        if (lane == 0) mbar_arrive_cluster_relaxed(stf_s);   // the S CTA's staging buffer may take the next tile
         if (j > 0) {
           uint32_t f[4];
           lds128(sbase + kOFlags + 16 * b, f);
           if (f[0] | f[1] | f[2] | f[3]) {
             // O must hold PV of every earlier tile before its rows are rescaled
-            if (!await2(p, bar(kPVD + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
-            *hand = b;
-            mbar_arrive(bar(kCN));
-            if (!await2(p, bar(kCD), events & 1)) { ok = false; break; }
+            if (!await2_warp(p, bar(kPVD + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
+            if (lane == 0) {
+              *hand = b;
+              mbar_arrive(bar(kCN));
+            }
+            if (!await2_warp(p, bar(kCD), events & 1)) { ok = false; break; }
             ++events;
           }
         }
         fence_proxy_async_smem();   // P was written by the S CTA's stores, the MMA reads it as an operand
         tc_fence_before();
-        if (first) mbar_arrive(bar(kPR + b));
-        else mbar_arrive_cluster(pr0 + 8u * b);   // release: P and the rescaled rows of this CTA
-        if (j + 2 < n) mbar_arrive_expect_tx(bar(kPF + b), kTxP2);
+        __syncwarp();
+        if (lane == 0) {
+          if (first) mbar_arrive(bar(kPR + b));
+          else mbar_arrive_cluster(pr0 + 8u * b);   // release: P and the rescaled rows of this CTA
+          if (j + 2 < n) mbar_arrive_expect_tx(bar(kPF + b), kTxP2);
+        }
         if (first) {
-          if (!await2(p, bar(kPR + b), (j >> 1) & 1)) { ok = false; break; }
+          if (!await2_warp(p, bar(kPR + b), (j >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t pt = sbase + kOP + b * kOPBytes;
-#pragma unroll 1
-          for (int kh = 0; kh < 2 && ok; ++kh) {
-            const int u = 2 * j + kh, s = u % kORing;
-            if (!await2(p, bar(kCF + s), (u / kORing) & 1)) { ok = false; break; }
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh) {
+            const int u = 2 * j + kh, s = u & (kORing - 1);
+            if (!await2_warp(p, bar(kCF + s), (u / kORing) & 1)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t c = sbase + kOC + s * kOStage;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sdesc_sw128(pt + kh * kBlk128 + kk * 32, 16, 1024);
+              const uint64_t ad = sdesc_add(pd0, b * kOPBytes + kh * kBlk128 + kk * 32);
 #pragma unroll
               for (int nh = 0; nh < 2; ++nh)
-                mma2_ss(tmem + 256 * nh, ad, sdesc_sw128(c + nh * 2 * kBlk + kk * 2048, kBlk, 1024), kIdPV2,
-                        (j | kh | kk) ? 1u : 0u);
+                mma2_ss_elect(tmem + 256 * nh, ad, sdesc_add(cd0, s * kOStage + nh * 2 * kBlk + kk * 2048), kIdPV2,
+                              (j | kh | kk) ? 1u : 0u);
             }
-            mma2_commit_mc(bar(kCE + s), kMaskO);
+            mma2_commit_mc_elect(bar(kCE + s), kMaskO);
           }
           if (!ok) break;
-          mma2_commit_mc(bar(kPVD + b), kMaskO);
-          mma2_commit_mc(bar(kPFR + b), kMaskS);
+          mma2_commit_mc_elect(bar(kPVD + b), kMaskO);
+          mma2_commit_mc_elect(bar(kPFR + b), kMaskS);
         }
       }
-      *hand = -1;   // no more tiles: the correction warps go on to the epilogue
-      mbar_arrive(bar(kCN));
+      if (lane == 0) {
+        *hand = -1;   // no more tiles: the correction warps go on to the epilogue
+        mbar_arrive(bar(kCN));
+      }
     } else if (warp >= 4) {
       // ---------------------------------------------------------- rescale O rows; epilogue
       const int r = tid - 128;
