@@ -40,7 +40,7 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads2 = 256;   // warp 0: loads; 1: MMA; 2: TMEM; 4-7: softmax (S) or rescale and epilogue (O)
+constexpr int kThreads2 = 256;   // warp 0: loads; 1: MMA; 2: TMEM; 3 (O): P landed; 4-7: softmax (S) or rescale and epilogue (O)
 constexpr uint32_t kBlk = 8192;            // [64 rows x 128 B] swizzled block
 constexpr uint32_t kBlk128 = 16384;        // [128 rows x 128 B] swizzled block
 
@@ -470,14 +470,12 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
       bool ok = true;
       volatile int* hand = reinterpret_cast<volatile int*>(sgen + kOFlags + 32);
       const uint32_t pr0 = mapa_shared(bar(kPR), 2u);
-      const uint32_t stf_s = mapa_shared(bar(kSTF), half);   // the S CTA that sends this CTA's P
       const uint64_t pd0 = sdesc_sw128(sbase + kOP, 16, 1024);     // P tiles, K-major
       const uint64_t cd0 = sdesc_sw128(sbase + kOC, kBlk, 1024);   // latent stages, MN-major
       int events = 0;
       for (int j = 0; j < n && ok; ++j) {
         const int b = j & 1;
         if (!await2_warp(p, bar(kPF + b), (j >> 1) & 1)) { ok = false; break; }
-        if (lane == 0) mbar_arrive_cluster_relaxed(stf_s);   // the S CTA's staging buffer may take the next tile
         if (j > 0) {
           uint32_t f[4];
           lds128(sbase + kOFlags + 16 * b, f);
@@ -496,9 +494,9 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (first) mbar_arrive(bar(kPR + b));
-          else mbar_arrive_cluster(pr0 + 8u * b);   // release: P and the rescaled rows of this CTA
-          if (j + 2 < n) mbar_arrive_expect_tx(bar(kPF + b), kTxP2);
+          if (first) mbar_arrive_relaxed(bar(kPR + b));   // this warp waits on it itself
+          else mbar_arrive_cluster(pr0 + 8u * b);         // release: P and the rescaled rows of this CTA
+          if (j + 2 < n) mbar_arrive_expect_tx_relaxed(bar(kPF + b), kTxP2);
         }
         if (first) {
           if (!await2_warp(p, bar(kPR + b), (j >> 1) & 1)) { ok = false; break; }
@@ -526,6 +524,16 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
       if (lane == 0) {
         *hand = -1;   // no more tiles: the correction warps go on to the epilogue
         mbar_arrive(bar(kCN));
+      }
+    } else if (warp == 3 && lane == 0) {
+      // ---------------------------------------------------------- each P tile landed: the S CTA that sent it
+      // may stage the next one.  A thread of its own, so that the control thread's release arrives never wait
+      // for this remote arrive to complete.  PF(b) cannot complete tile j + 2 before this thread has signalled
+      // tile j + 1, so its phases never run ahead of this loop.
+      const uint32_t stf_s = mapa_shared(bar(kSTF), half);
+      for (int j = 0; j < n; ++j) {
+        if (!await2(p, bar(kPF + (j & 1)), (j >> 1) & 1)) break;
+        mbar_arrive_cluster_relaxed(stf_s);
       }
     } else if (warp >= 4) {
       // ---------------------------------------------------------- rescale O rows; epilogue

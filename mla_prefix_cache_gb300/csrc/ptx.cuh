@@ -686,6 +686,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
+// Relaxed arrive, and relaxed arrive with a byte count, on a barrier of this
+// CTA.  An arrive with the default release semantics waits until the thread's
+// earlier memory operations are performed, a remote arrive among them (about
+// 0.4 us); where the barrier's waiter needs no data released by this thread
+// (the same thread waits on it, or the barrier only counts bytes), these do
+// not wait.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
 
 // Asynchronous stores into another CTA of the cluster: each store adds its
 // bytes to the complete-tx count of an mbarrier in that CTA (`caddr` and
