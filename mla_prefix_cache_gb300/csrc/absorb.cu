@@ -493,9 +493,14 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
         fence_proxy_async_smem();   // P was written by the S CTA's stores, the MMA reads it as an operand
         tc_fence_before();
         __syncwarp();
+        // P and the rescaled rows of this CTA are ready for the leader's MMAs.  Both arrives are relaxed: P
+        // is in this CTA's shared memory once its copy's completion was observed above, and the MMAs the
+        // leader issues after seeing this arrive read that memory directly; the rescaled rows were stored and
+        // waited for (tcgen05.wait::st) and the tcgen05 fences around this arrive and the leader's wait order
+        // them.  (A cluster-scope release here held the peer's thread 0.6 us a tile, on the path to each PV.)
         if (lane == 0) {
-          if (first) mbar_arrive_relaxed(bar(kPR + b));   // this warp waits on it itself
-          else mbar_arrive_cluster(pr0 + 8u * b);         // release: P and the rescaled rows of this CTA
+          if (first) mbar_arrive_relaxed(bar(kPR + b));
+          else mbar_arrive_cluster_relaxed(pr0 + 8u * b);
           if (j + 2 < n) mbar_arrive_expect_tx_relaxed(bar(kPF + b), kTxP2);
         }
         if (first) {
