@@ -44,24 +44,26 @@ constexpr int kThreads2 = 256;   // warp 0: loads; 1: MMA; 2: TMEM; 3 (O): P lan
 constexpr uint32_t kBlk = 8192;            // [64 rows x 128 B] swizzled block
 constexpr uint32_t kBlk128 = 16384;        // [128 rows x 128 B] swizzled block
 
-// S side, by score precision: the rotated q_rope, the P staging buffer (a P
-// tile, its row factors and flags, in the O side's layout), then the ring.  A
-// stage is this CTA's 64 keys of a tile times kSBlocks blocks of 128 B of the
-// row ([c | k_rope]: 9 blocks of bf16 or 5 of the FP8 row as stored).  The
-// item's qlat is staged from the P staging buffer on, over the first ring
+// S side, by score precision: the rotated q_rope, two P staging buffers (a P
+// tile, its row factors and flags, in the O side's layout: one is filled while
+// the other's copy into the O CTA is in flight), then the ring.  A stage is
+// this CTA's 64 keys of a tile times kSBlocks blocks of 128 B of the row
+// ([c | k_rope]: 9 blocks of bf16 or 5 of the FP8 row as stored).  The item's
+// qlat is staged from the first P staging buffer on, over the first ring
 // stages, before it is copied into TMEM.
 template <bool kF8>
 struct S2 {
   static constexpr int kSBlocks = kF8 ? 5 : 3;                // blocks per stage
   static constexpr int kStagesPerTile = kF8 ? 1 : 3;
   static constexpr int kLatBlocks = kF8 ? 4 : 8;              // latent blocks of a row (the last block is k_rope)
-  static constexpr int kRing = kF8 ? 4 : 7;
+  static constexpr int kRing = kF8 ? 3 : 5;
   static constexpr uint32_t kStage = kSBlocks * kBlk;
   static constexpr uint32_t kQR = 0;                          // rotated q_rope [128 x 128 B]
-  static constexpr uint32_t kPS = kBlk128;                    // P staging: P [2 x 16 KB], factors [512 B], flags
-  static constexpr uint32_t kPSAlpha = kPS + 2 * kBlk128;
+  static constexpr uint32_t kPS = kBlk128;                    // P staging i at kPS + i kPSBuf: P [2 x 16 KB],
+  static constexpr uint32_t kPSAlpha = 2 * kBlk128;           //   factors [512 B] and flags at these offsets
   static constexpr uint32_t kPSFlags = kPSAlpha + 512;
-  static constexpr uint32_t kStage0 = (kPSFlags + 16 + 1023) & ~1023u;
+  static constexpr uint32_t kPSBuf = (kPSFlags + 16 + 1023) & ~1023u;
+  static constexpr uint32_t kStage0 = kPS + 2 * kPSBuf;
   static constexpr int kQBoxes = kF8 ? 4 : 8;                 // [128 rows x 128 B] boxes of qlat
   static constexpr uint32_t kQBase = kPS;
   static constexpr uint32_t kQEnd = kQBase + kQBoxes * kBlk128;
@@ -97,7 +99,7 @@ enum : uint32_t {
   kQL = 21,    // this CTA's 4 softmax warps copied it out (count 4)
   kQR = 22,    // Q of both S CTAs in place (first CTA, count 8)
   kPFR = 23,   // 2: PV of the P tile done (both S CTAs, from the O pair)
-  kSTF = 42,   // the P staging buffer's last copy landed in the O CTA (S CTA, from its O CTA)
+  kSTF = 42,   // 2: the P staging buffer's last copy landed in the O CTA (S CTA, from its O CTA)
   // O side
   kCF = 25,    // 4: stage landed in both O CTAs (first CTA's count)
   kCE = 29,    // 4: the stage's MMAs are done (both O CTAs)
@@ -107,7 +109,7 @@ enum : uint32_t {
   kCN = 39,    // this CTA's control thread handed a tile (or the end) to its correction warps
   kCD = 40,    // the 4 correction warps rescaled their rows (count 4)
   kLF = 41,    // the final row sums landed
-  kNBars2 = 43
+  kNBars2 = 44
 };
 
 template <bool kF8>
@@ -365,6 +367,7 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
         __syncwarp();
         if (lane == 0 && wok) mbar_arrive_cluster_relaxed(ssr0 + 8u * b);
         const int kt0 = it.t0 + 128 * j;
+        const uint32_t stg = sbase + SS::kPS + b * SS::kPSBuf;   // this tile's staging buffer
         if (!(kt0 >= it.k_lo && kt0 + 127 < it.k_hi && kt0 + 127 <= qk)) {
           float m8[8];
 #pragma unroll
@@ -404,30 +407,30 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
         }
         // the staging buffer is free once the previous tile's copy landed; the four warps go on, or
         // leave, together
-        if (wok && j >= 1) wok = await2_warp(p, bar(kSTF), (j - 1) & 1);
+        if (wok && j >= 2) wok = await2_warp(p, bar(kSTF + b), ((j - 2) >> 1) & 1);
         if (named_bar_or(1, 128, !wok)) { ok = false; break; }
 #pragma unroll
         for (int hk = 0; hk < 2; ++hk)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            sts128(sbase + SS::kPS + hk * kBlk128 + sw128_off((uint32_t)r, (uint32_t)c), pk[32 * hk + 4 * c],
+            sts128(stg + hk * kBlk128 + sw128_off((uint32_t)r, (uint32_t)c), pk[32 * hk + 4 * c],
                    pk[32 * hk + 4 * c + 1], pk[32 * hk + 4 * c + 2], pk[32 * hk + 4 * c + 3]);
         float s8[4];
         f2unpack(fadd2(s4[0], s4[1]), s8[0], s8[1]);
         f2unpack(fadd2(s4[2], s4[3]), s8[2], s8[3]);
         l = l * alpha + ((s8[0] + s8[2]) + (s8[1] + s8[3]));
-        reinterpret_cast<float*>(sgen + SS::kPSAlpha)[r] = alpha;
+        reinterpret_cast<float*>(sgen + SS::kPS + b * SS::kPSBuf + SS::kPSAlpha)[r] = alpha;
         const uint32_t any_rescale = __any_sync(0xffffffffu, alpha != 1.f) ? 1u : 0u;
-        if (lane == 0) reinterpret_cast<uint32_t*>(sgen + SS::kPSFlags)[warp & 3] = any_rescale;
+        if (lane == 0) reinterpret_cast<uint32_t*>(sgen + SS::kPS + b * SS::kPSBuf + SS::kPSFlags)[warp & 3] = any_rescale;
         fence_proxy_async_smem();   // the staged tile is read by the bulk copy (async proxy)
         named_bar_sync(1, 128);
         if (r == 0) {
           // P tile b of the O CTA is free once the PV of tile j - 2 is done
           if (j >= 2 && !await2(p, bar(kPFR + b), ((j - 2) >> 1) & 1)) continue;   // the others time out next tile
           const uint32_t cbar = mapa_shared(bar(kPF + b), orank);
-          bulk_copy_to_peer(mapa_shared(sbase + kOP + b * kOPBytes, orank), sbase + SS::kPS, kOPBytes, cbar);
-          bulk_copy_to_peer(mapa_shared(sbase + kOAlpha + b * 512, orank), sbase + SS::kPSAlpha, 512, cbar);
-          bulk_copy_to_peer(mapa_shared(sbase + kOFlags + 16 * b, orank), sbase + SS::kPSFlags, 16, cbar);
+          bulk_copy_to_peer(mapa_shared(sbase + kOP + b * kOPBytes, orank), stg, kOPBytes, cbar);
+          bulk_copy_to_peer(mapa_shared(sbase + kOAlpha + b * 512, orank), stg + SS::kPSAlpha, 512, cbar);
+          bulk_copy_to_peer(mapa_shared(sbase + kOFlags + 16 * b, orank), stg + SS::kPSFlags, 16, cbar);
         }
       }
       // final row sums to the O CTA; lse of the item
@@ -532,13 +535,13 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
       }
     } else if (warp == 3 && lane == 0) {
       // ---------------------------------------------------------- each P tile landed: the S CTA that sent it
-      // may stage the next one.  A thread of its own, so that the control thread's release arrives never wait
-      // for this remote arrive to complete.  PF(b) cannot complete tile j + 2 before this thread has signalled
-      // tile j + 1, so its phases never run ahead of this loop.
+      // may stage the tile after next in that staging buffer.  A thread of its own, so that the control
+      // thread's arrives never wait for this remote arrive to complete.  The copy of tile j + 2 into PF(b)'s
+      // buffer waits for this thread's signal of tile j, so PF(b)'s phases never run ahead of this loop.
       const uint32_t stf_s = mapa_shared(bar(kSTF), half);
       for (int j = 0; j < n; ++j) {
         if (!await2(p, bar(kPF + (j & 1)), (j >> 1) & 1)) break;
-        mbar_arrive_cluster_relaxed(stf_s);
+        mbar_arrive_cluster_relaxed(stf_s + 8u * (j & 1));
       }
     } else if (warp >= 4) {
       // ---------------------------------------------------------- rescale O rows; epilogue
