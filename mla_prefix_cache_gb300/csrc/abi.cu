@@ -802,9 +802,9 @@ static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int 
   const int key_tile = 128;
   // resident clusters (36 of four CTAs on a GB300), an item's start and epilogue (about 8 us) and the
   // latent merge (2 KB read or written per row and slot at about 3.5 TB/s) in keys of an item (about
-  // 2.2 us per 128 keys)
+  // 1.36 us per 128 keys)
   const int clusters = 36;
-  const double ns_per_key = 17.2;
+  const double ns_per_key = 10.6;
   const double item_keys = 8000.0 / ns_per_key;
   const double merge_keys_per_row = 2048.0 / 3500.0 / ns_per_key;   // bytes / (bytes per ns) / (ns per key)
   const std::vector<Piece> pieces = abs_pieces(fp);
@@ -1110,11 +1110,11 @@ static int prefill_plans(const void* q, const int32_t* q_pos, const void* kv_cac
 // ------------------------------------------------------------------ head-split reuse
 // A request with at most this many queries goes through the absorbed path,
 // the others through the up-projected one.  On GB300 (128 heads, 32K cached
-// tokens) the two break even near 155 queries: the absorbed path is 1.27x at
-// 128 and 0.98x at 160; on a 128K FP8 cache (E4M3 scores) it is 1.40x at 128
-// and 0.99x at 192.  The FLOP counts alone would put it near 170, but the up-projected
-// kernel runs its MMAs closer to peak.
-constexpr int kAutoAbsorbedMaxQueries = 128;
+// tokens) the two break even near 215 queries: the absorbed path is 1.81x at
+// 128, 1.18x at 192 and 0.98x at 224; on a 128K FP8 cache it is 1.28x at 192
+// and 0.96x at 256.  The FLOP counts alone put it near 170: the latent kernel
+// runs its MMAs closer to peak than the up-projected one.
+constexpr int kAutoAbsorbedMaxQueries = 192;
 
 struct ReusePlan {
   std::vector<int32_t> global, local, prot_rows, prot_tok, gidx, lidx, pidx, cu_p, ctx;
