@@ -925,6 +925,12 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
     const uint32_t b3[2] = {64, 128};
     ok &= encode_map(&p.tm_qlat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + aw.qlat_off, d3, st3, b3,
                      CU_TENSOR_MAP_SWIZZLE_128B);
+    // the latent states of every slot, 32 columns x 128 rows to a box (the epilogue's stores)
+    const uint64_t dl[2] = {(uint64_t)kDc, (uint64_t)std::max(ap.max_slots, 1) * (uint64_t)T_q * H};
+    const uint64_t sl[1] = {(uint64_t)kDc * sizeof(float)};
+    const uint32_t bl[2] = {32, 128};
+    ok &= encode_map(&p.tm_lat, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws + aw.lat_out_off, dl, sl, bl,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (fp8_scores) {
     // a 640-byte row as stored as 5 blocks of 128 bytes (4 of E4M3 codes, k_rope as bf16), one box a stage;

@@ -580,20 +580,49 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
       tc_fence_after();
       const float lsum = ok ? reinterpret_cast<const float*>(sgen + kOL)[r] : 0.f;
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      float4* dst = reinterpret_cast<float4*>(p.lat_out + ((int64_t)it.slot * p.slot_stride_rows + orow) * kDc);
+      // every row of this CTA live (all but an item's last row tile): O / l leaves by TMA stores of
+      // 32-column boxes staged in the latent stage ring, which the last PV has finished reading
+      const bool full = ok && n > 0 && it.row0 + 128 * (int)half + 128 <= P.q_count * H;
+      if (!named_bar_or(2, 128, !full)) {
+        const int grow0 = (int)((int64_t)it.slot * p.slot_stride_rows + (int64_t)P.q_begin * H + it.row0 + 128 * (int)half);
 #pragma unroll 1
-      for (int cc = 0; cc < 16; ++cc) {
-        uint32_t o[32];
-        if (ok && n > 0) tmem_ld32(tmem + lane_off + 32 * cc, o);
-        else {
+        for (int cc = 0; cc < 16; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + 32 * cc, o);
+          const uint32_t box = sbase + kOC + (uint32_t)(cc & 7) * kBlk128;
+          if (cc >= 8) {   // the box's store of 8 chunks ago has read it
+            if (r == 0) bulk_wait_read<7>();
+            named_bar_sync(2, 128);
+          }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
+          for (int c = 0; c < 8; ++c)
+            sts128(box + sw128_off((uint32_t)r, (uint32_t)c), __float_as_uint(__uint_as_float(o[4 * c]) * inv),
+                   __float_as_uint(__uint_as_float(o[4 * c + 1]) * inv), __float_as_uint(__uint_as_float(o[4 * c + 2]) * inv),
+                   __float_as_uint(__uint_as_float(o[4 * c + 3]) * inv));
+          fence_proxy_async_smem();   // the box is read by the TMA store
+          named_bar_sync(2, 128);
+          if (r == 0) {
+            tma_store_2d(&p.tm_lat, box, 32 * cc, grow0);
+            bulk_commit();
+          }
         }
-        if (live) {
+        if (r == 0) bulk_wait0();
+      } else {
+        float4* dst = reinterpret_cast<float4*>(p.lat_out + ((int64_t)it.slot * p.slot_stride_rows + orow) * kDc);
+#pragma unroll 1
+        for (int cc = 0; cc < 16; ++cc) {
+          uint32_t o[32];
+          if (ok && n > 0) tmem_ld32(tmem + lane_off + 32 * cc, o);
+          else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[8 * cc + i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                          __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          if (live) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[8 * cc + i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                            __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+          }
         }
       }
     }

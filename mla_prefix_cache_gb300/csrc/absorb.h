@@ -36,6 +36,7 @@ struct AbsorbParams {
   // E4M3 scores (fp8_scores): the cache's FP8 rows gathered as stored (640 B)
   CUtensorMap tm_f5;    // as 5 blocks of 128 B (4 of E4M3 codes, k_rope as bf16), box 128 x 64 x 5
   CUtensorMap tm_qlat8; // E4M3 qlat as [T_q * H rows][512 B], box 128 x 128
+  CUtensorMap tm_lat;   // lat_out as [slots * T_q * H rows][512] fp32, box 32 x 128
   const float* qscale;  // [T_q * H]: the E4M3 qlat row's scale
   float kv_scale;
   int fp8_scores;

@@ -467,6 +467,11 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 __device__ __forceinline__ void bulk_wait1() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
+// the shared-memory sources of all but the N most recent committed bulk groups have been read
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 
 // Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
 // Named barrier that also returns the OR of `pred` over the participating
