@@ -22,15 +22,18 @@
 //    S = Q [c | k_rope]^T with N = 128, rank r loading keys 64 r .. 64 r + 63
 //    of the tile (bf16 rows, or the FP8 rows as stored with E4M3 scores on
 //    kind::f8f6f4); the online softmax of each CTA's rows writes P (bf16), the
-//    rows' rescale factors and one "rescaled" flag per warp into a staging
-//    buffer, which one thread copies in bulk into the shared memory of the O
-//    CTA that holds the same rows (2048 16-byte stores into the other SM took
-//    a quarter of the time with E4M3 scores).
+//    rows' rescale factors and one "rescaled" flag per warp into one of two
+//    staging buffers (alternate tiles), which one thread copies in bulk into
+//    the shared memory of the O CTA that holds the same rows (2048 16-byte
+//    stores into the other SM took a quarter of the time with E4M3 scores).
 //  - O pair (ranks 2, 3): O [256 x 512] += P c with N = 256 per MMA, rank
 //    2 + r loading latent columns 128 r .. 128 r + 127 of each 256-column half
 //    of the keys; rows whose maximum rose are rescaled in TMEM by the CTA's
 //    correction warps before the tile's PV; at the end O / l leaves as fp32
 //    latent state.
+// Each pair's MMAs are issued by a whole warp through one elected lane, and
+// the per-tile signals between the CTAs are relaxed arrives wherever the
+// waiter needs no memory released by the arriving thread.
 // Each key is read from L2 once per 256 rows by the S pair and once by the O
 // pair, half of it by each CTA.
 #include "absorb.h"
