@@ -492,6 +492,39 @@ static int gather_rows_raw(const FusedPlan& fp, const void* kv_cache, int num_bl
   return MLA_OK;
 }
 
+// The last block of each of the plan's requests (rows past the sequence as
+// zeros), request i of the plan's gather list into block i of `dst`: what the
+// absorbed path's P c side reads for a request's last block while it reads
+// the cache's other blocks in place.
+static int gather_last_blocks(const FusedPlan& fp, const void* kv_cache, int num_blocks, const int32_t* block_table,
+                              int max_blocks, uint8_t* dst, uint32_t* err, cudaStream_t s) {
+  static GatherBlocksParams gp;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  std::memset(&gp, 0, sizeof(gp));
+  gp.cache = static_cast<const uint8_t*>(kv_cache);
+  gp.block_table = block_table;
+  gp.err = err;
+  gp.scale = 1.f;
+  gp.num_blocks = num_blocks;
+  gp.max_blocks = max_blocks;
+  for (size_t g0 = 0; g0 < fp.gather.size(); g0 += kMaxGatherReqs) {
+    const size_t n = std::min(fp.gather.size() - g0, (size_t)kMaxGatherReqs);
+    for (size_t i = 0; i < n; ++i) {
+      GatherReq g = fp.gather[g0 + i];
+      g.first_block = std::max(0, (g.seq_len + kBlock - 1) / kBlock - 1);
+      g.base_block = (int32_t)i;
+      gp.reqs[i] = g;
+    }
+    gp.dst = reinterpret_cast<uint16_t*>(dst) + g0 * kBlock * kRowBf16;
+    gp.n_reqs = (int)n;
+    gp.total_blocks = (int)n;
+    const int st = cuda_status(launch_gather_blocks(gp, s));
+    if (st != MLA_OK) return st;
+  }
+  return MLA_OK;
+}
+
 static int prefill_fused(const void* q, const int32_t* q_pos, const void* kv_cache, int kv_dtype, float kv_scale,
                          int num_blocks, const int32_t* block_table, int max_blocks, int num_heads,
                          const void* kv_b_proj, float softmax_scale, float rope_theta, void* out, int out_dtype,
@@ -932,6 +965,30 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
     ok &= encode_map(&p.tm_lat, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws + aw.lat_out_off, dl, sl, bl,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  // Rows read in place: a score stage or a P c stage is one whole cache block, so both sides read a BF16
+  // cache's blocks where they are (P c takes a request's last block from a copy whose rows past the
+  // sequence are zeros), and E4M3 scores read an FP8 cache's rows as stored; an FP8 cache's P c side, and
+  // its bf16 scores, read the dequantised rows of the gather pass.
+  p.s_in_place = (!fp8 || fp8_scores) ? 1 : 0;
+  p.o_in_place = fp8 ? 0 : 1;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.num_blocks = num_blocks;
+  {
+    const uint64_t rows_cache = (uint64_t)std::max(num_blocks, 1) * kBlock;
+    if (!fp8) {
+      const uint64_t d[3] = {64, rows_cache, 9};
+      const uint64_t st[2] = {(uint64_t)kRowBytesBf16, 128};
+      const uint32_t b[3] = {64, 64, 3}, b2[3] = {64, 64, 2};
+      ok &= encode_map(&p.tm_k3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok &= encode_map(&p.tm_k2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, d, st, b2, CU_TENSOR_MAP_SWIZZLE_128B);
+    } else if (fp8_scores) {
+      const uint64_t d[3] = {128, rows_cache, 5};
+      const uint64_t st[2] = {(uint64_t)kRowBytesFp8, 128};
+      const uint32_t b[3] = {128, 64, 5};
+      ok &= encode_map(&p.tm_kf5, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv_cache, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+  }
   if (fp8_scores) {
     // a 640-byte row as stored as 5 blocks of 128 bytes (4 of E4M3 codes, k_rope as bf16), one box a stage;
     // the E4M3 qlat 128 rows x 128 bytes to a box
@@ -953,11 +1010,9 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
 
   int st = err_word ? MLA_OK : cuda_status(cudaMemsetAsync(err, 0, 256, s));
   if (st != MLA_OK) return st;
-  if ((st = gather_rows(fp, kv_cache, fp8, num_blocks, block_table, max_blocks, ws + aw.gath_off, err, s)) != MLA_OK)
-    return st;
-  if (fp8_scores && (st = gather_rows_raw(fp, kv_cache, num_blocks, block_table, max_blocks, ws + aw.raw_off, err, s)) !=
-                        MLA_OK)
-    return st;
+  st = p.o_in_place ? gather_last_blocks(fp, kv_cache, num_blocks, block_table, max_blocks, ws + aw.gath_off, err, s)
+                    : gather_rows(fp, kv_cache, fp8, num_blocks, block_table, max_blocks, ws + aw.gath_off, err, s);
+  if (st != MLA_OK) return st;
   {
     static QAbsorbParams qp;
     std::memset(&qp, 0, sizeof(qp));
@@ -1015,11 +1070,18 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
   cudaEvent_t ev_b = static_cast<cudaEvent_t>(g_ev_begin.load());
   cudaEvent_t ev_e = static_cast<cudaEvent_t>(g_ev_end.load());
   if (ev_b != nullptr && ev_e != nullptr && (st = cuda_status(cudaEventRecord(ev_b, s))) != MLA_OK) return st;
+  int req_max = 0;
+  for (const GatherReq& g : fp.gather) req_max = std::max(req_max, g.req + 1);
+  std::vector<int> greq(req_max, 0);   // request -> its place in the gather list
+  for (size_t i = 0; i < fp.gather.size(); ++i) greq[fp.gather[i].req] = (int)i;
   for (size_t b0 = 0; b0 < ap.pieces.size(); b0 += kMaxAbsPieces) {
     const size_t n = std::min(ap.pieces.size() - b0, (size_t)kMaxAbsPieces);
     int64_t items = 0;
     for (size_t i = 0; i < n; ++i) {
       AbsPiece a = ap.pieces[b0 + i];
+      const int gi = greq[a.req];
+      a.last_lb = std::max(0, (fp.gather[gi].seq_len + kBlock - 1) / kBlock - 1);
+      if (p.o_in_place) a.row_block0 = gi;   // the copy of the request's last block
       a.item_begin = (int32_t)items;
       items += (int64_t)a.n_row_tiles * a.n_splits;
       p.pieces[i] = a;

@@ -141,6 +141,21 @@ __device__ __forceinline__ bool await2_warp(const AbsorbParams& p, uint32_t bar,
   return __all_sync(0xffffffffu, await2(p, bar, parity));
 }
 
+// Row of the paged cache that holds the 64 keys from key token kt (a multiple
+// of 64) of the piece's request, for a load that reads the cache in place.
+// Keys past the request's last block, and a bad block id (reported), give a
+// row before the map, which a TMA load reads as zeros.
+__device__ __forceinline__ int cache_row(const AbsorbParams& p, const AbsPiece& P, int kt) {
+  const int lb = kt >> 6;
+  if (lb > P.last_lb) return -kBlock;
+  const int id = lb < p.max_blocks ? __ldg(p.block_table + (int64_t)P.req * p.max_blocks + lb) : -1;
+  if (id < 0 || id >= p.num_blocks) {
+    atomicOr(p.err, kErrBadBlock);
+    return -kBlock;
+  }
+  return id * kBlock;
+}
+
 struct AItem {
   const AbsPiece* P;
   int row0;      // first row of the item within the piece (rows = token * H + head)
@@ -195,10 +210,11 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
 
   if (tid == 0) {
     if (s_side) {
-      prefetch_tensormap(kF8 ? &p.tm_f5 : &p.tm_c3);
+      prefetch_tensormap(kF8 ? (p.s_in_place ? &p.tm_kf5 : &p.tm_f5) : (p.s_in_place ? &p.tm_k3 : &p.tm_c3));
       prefetch_tensormap(kF8 ? &p.tm_qlat8 : &p.tm_qlat);
     } else {
       prefetch_tensormap(&p.tm_c2);
+      if (p.o_in_place) prefetch_tensormap(&p.tm_k2);
     }
     for (uint32_t i = 0; i < kNBars2; ++i) {
       uint32_t cnt = 1;
@@ -218,7 +234,7 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + LL::kSlot);
-  const int64_t row_base = (int64_t)P.row_block0 * kBlock;   // gathered row of key token 0
+  const int64_t row_base = (int64_t)P.row_block0 * kBlock;   // gathered row of key token 0 (rows read in place: the copy of the last block)
 
   if (s_side) {
     // ================================================================ S pair
@@ -238,15 +254,22 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
       bool q_copied = false;
       for (int u = 0; u < U && ok; ++u) {
         const int s = u % SS::kRing, j = u / SS::kStagesPerTile, m = u - j * SS::kStagesPerTile;
+        // this CTA's 64 keys of the tile (looked up before the slot wait, which hides the table load): masked
+        // past the item's keys, so read in place whatever they hold
+        const int kt = it.t0 + 128 * j + 64 * (int)half;
+        const int row = p.s_in_place ? cache_row(p, P, kt) : (int)(row_base + kt);
         if (u >= SS::kRing && !await2(p, bar(kSE + s), ((u / SS::kRing) - 1) & 1)) { ok = false; break; }
         if (SS::holds_q(s) && !q_copied) {   // the staged queries are out of the stages before keys overwrite them
           if (!await2(p, bar(kQL), 0)) { ok = false; break; }
           q_copied = true;
         }
-        const int row = (int)(row_base + it.t0 + 128 * j + 64 * (int)half);
         if (first) mbar_arrive_expect_tx(bar(kSF + s), 2 * SS::kStage);
-        if (kF8) tma_load_3d_pair(sbase + SS::kStage0 + s * SS::kStage, &p.tm_f5, 0, row, 0, full0 + 8u * s);
-        else tma_load_3d_pair(sbase + SS::kStage0 + s * SS::kStage, &p.tm_c3, 0, row, 3 * m, full0 + 8u * s);
+        if (kF8)
+          tma_load_3d_pair(sbase + SS::kStage0 + s * SS::kStage, p.s_in_place ? &p.tm_kf5 : &p.tm_f5, 0, row, 0,
+                           full0 + 8u * s);
+        else
+          tma_load_3d_pair(sbase + SS::kStage0 + s * SS::kStage, p.s_in_place ? &p.tm_k3 : &p.tm_c3, 0, row, 3 * m,
+                           full0 + 8u * s);
       }
       // the last commits land on this CTA's barriers before it exits
       for (int u = max(0, U - SS::kRing); u < U && ok; ++u)
@@ -456,12 +479,24 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
       const uint32_t full0 = mapa_shared(bar(kCF), 2u);
       for (int u = 0; u < U && ok; ++u) {
         const int s = u % kORing;
+        // 64 keys: P is zero past the item's keys, so those rows must be finite: a request's last block comes
+        // from its copy (zeros past the sequence), the others in place (looked up before the slot wait)
+        const int kt = it.t0 + 64 * u;
+        int row = (int)(row_base + kt);
+        const void* map = &p.tm_c2;
+        if (p.o_in_place) {
+          if ((kt >> 6) == P.last_lb) {
+            row = (int)row_base;
+          } else {
+            row = cache_row(p, P, kt);
+            map = &p.tm_k2;
+          }
+        }
         if (u >= kORing && !await2(p, bar(kCE + s), ((u / kORing) - 1) & 1)) { ok = false; break; }
-        const int row = (int)(row_base + it.t0 + 64 * u);
         if (first) mbar_arrive_expect_tx(bar(kCF + s), 2 * kOStage);
         const uint32_t st = sbase + kOC + s * kOStage;
-        tma_load_3d_pair(st, &p.tm_c2, 0, row, 2 * (int)half, full0 + 8u * s);              // columns 128 r ..
-        tma_load_3d_pair(st + 2 * kBlk, &p.tm_c2, 0, row, 4 + 2 * (int)half, full0 + 8u * s);   // 256 + 128 r ..
+        tma_load_3d_pair(st, map, 0, row, 2 * (int)half, full0 + 8u * s);              // columns 128 r ..
+        tma_load_3d_pair(st + 2 * kBlk, map, 0, row, 4 + 2 * (int)half, full0 + 8u * s);   // 256 + 128 r ..
       }
       for (int u = max(0, U - kORing); u < U && ok; ++u)
         if (!await2(p, bar(kCE + u % kORing), (u / kORing) & 1)) ok = false;

@@ -18,7 +18,9 @@ struct AbsPiece {
   int32_t q_tok0;      // token index of the request's first query (C_r)
   int32_t k_begin;     // first key token
   int32_t k_end;       // one past the last key token
-  int32_t row_block0;  // the request's rows were gathered contiguously from this block on
+  int32_t row_block0;  // the request's rows were gathered contiguously from this block on (rows read in place:
+                       // the block holding the copy of its last block)
+  int32_t last_lb;     // the request's last logical block
   int32_t slot;        // partial-state slot of split 0 (split i uses slot + i)
   int32_t n_row_tiles; // ceil(q_count * H / 256)
   int32_t n_splits;    // key splits per row tile
@@ -37,6 +39,16 @@ struct AbsorbParams {
   CUtensorMap tm_f5;    // as 5 blocks of 128 B (4 of E4M3 codes, k_rope as bf16), box 128 x 64 x 5
   CUtensorMap tm_qlat8; // E4M3 qlat as [T_q * H rows][512 B], box 128 x 128
   CUtensorMap tm_lat;   // lat_out as [slots * T_q * H rows][512] fp32, box 32 x 128
+  // rows read in place: the paged cache itself (rows = num_blocks x 64), boxes as tm_c3 / tm_c2 (BF16 cache)
+  // or tm_f5 (FP8 cache as stored)
+  CUtensorMap tm_k3;
+  CUtensorMap tm_k2;
+  CUtensorMap tm_kf5;
+  const int32_t* block_table;   // [num_reqs][max_blocks]
+  int max_blocks;
+  int num_blocks;
+  int s_in_place;       // the score side reads the cache's blocks in place
+  int o_in_place;       // the P c side reads them in place, a request's last block from its copy
   const float* qscale;  // [T_q * H]: the E4M3 qlat row's scale
   float kv_scale;
   int fp8_scores;

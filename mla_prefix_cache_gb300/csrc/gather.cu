@@ -76,8 +76,10 @@ struct RangeSrc {
   }
 };
 
-// Every block of several requests, in logical order (the fused path's pass);
-// passed by value, so the request list sits in the kernel's parameter space.
+// Every block of several requests from each one's first_block on, in logical
+// order (the fused path's pass; the absorbed path's copies of each request's
+// last block); passed by value, so the request list sits in the kernel's
+// parameter space.
 struct BlocksSrc {
   GatherBlocksParams p;
   __device__ int tiles() const { return p.total_blocks; }
@@ -88,7 +90,7 @@ struct BlocksSrc {
       if (p.reqs[mid].base_block <= gb) lo = mid; else hi = mid - 1;
     }
     const GatherReq rq = p.reqs[lo];
-    const int lb = gb - rq.base_block;
+    const int lb = gb - rq.base_block + rq.first_block;
     Tile t;
     t.rows = kBlock;
     t.dst_row = (int64_t)gb * kBlock;

@@ -177,9 +177,9 @@ cudaError_t launch_gather(const uint8_t* cache, int fp8, float scale, int num_bl
 
 struct GatherReq {
   int32_t req;
-  int32_t base_block;  // first destination block
+  int32_t base_block;   // first destination block
   int32_t seq_len;
-  int32_t pad;
+  int32_t first_block;  // first logical block copied (blocks first_block .. of the request)
 };
 constexpr int kMaxGatherReqs = 1024;
 struct GatherBlocksParams {
