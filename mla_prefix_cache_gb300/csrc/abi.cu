@@ -898,7 +898,7 @@ static void build_abs_plan(const FusedPlan& fp, int H, const int32_t* cu_q, int 
 }
 
 struct AbsWs {
-  size_t gath_off = 0, qlat_off = 0, lat_out_off = 0, lat_lse_off = 0, raw_off = 0, qlat8_off = 0, qscale_off = 0,
+  size_t gath_off = 0, qlat_off = 0, lat_out_off = 0, lat_lse_off = 0, qlat8_off = 0, qscale_off = 0,
          total = 0;
 };
 
@@ -914,9 +914,8 @@ static AbsWs abs_ws_layout(const FusedPlan& fp, const AbsPlan& ap, int H, bool f
   w.lat_out_off = up256(w.qlat_off + rows * kDc * sizeof(uint16_t));
   w.lat_lse_off = up256(w.lat_out_off + slots * rows * kDc * sizeof(float));
   w.total = up256(w.lat_lse_off + slots * rows * sizeof(float));
-  if (fp8_scores) {   // E4M3 scores: the FP8 rows as stored, E4M3 qlat and its row scales
-    w.raw_off = w.total;
-    w.qlat8_off = up256(w.raw_off + (size_t)fp.gather_blocks * kBlock * kRowBytesFp8);
+  if (fp8_scores) {   // E4M3 scores: E4M3 qlat and its row scales (the FP8 rows are read in place)
+    w.qlat8_off = w.total;
     w.qscale_off = up256(w.qlat8_off + rows * kDc);
     w.total = up256(w.qscale_off + rows * sizeof(float));
   }
@@ -983,20 +982,15 @@ static int prefill_absorbed(const void* q, const int32_t* q_pos, const void* kv_
       ok &= encode_map(&p.tm_k3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
       ok &= encode_map(&p.tm_k2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_cache, d, st, b2, CU_TENSOR_MAP_SWIZZLE_128B);
     } else if (fp8_scores) {
+      // a 640-byte row as stored as 5 blocks of 128 bytes (4 of E4M3 codes, k_rope as bf16), one box a stage
       const uint64_t d[3] = {128, rows_cache, 5};
       const uint64_t st[2] = {(uint64_t)kRowBytesFp8, 128};
       const uint32_t b[3] = {128, 64, 5};
-      ok &= encode_map(&p.tm_kf5, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv_cache, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok &= encode_map(&p.tm_f5, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv_cache, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
     }
   }
   if (fp8_scores) {
-    // a 640-byte row as stored as 5 blocks of 128 bytes (4 of E4M3 codes, k_rope as bf16), one box a stage;
-    // the E4M3 qlat 128 rows x 128 bytes to a box
-    const void* raw = static_cast<const void*>(ws + aw.raw_off);
-    const uint64_t d[3] = {128, rows_total, 5};
-    const uint64_t st[2] = {(uint64_t)kRowBytesFp8, 128};
-    const uint32_t b[3] = {128, 64, 5};
-    ok &= encode_map(&p.tm_f5, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, raw, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+    // the E4M3 qlat 128 rows x 128 bytes to a box (the FP8 rows themselves are read in place, tm_f5 below)
     const uint64_t d3[2] = {(uint64_t)kDc, (uint64_t)T_q * H};
     const uint64_t st3[1] = {(uint64_t)kDc};
     const uint32_t b3[2] = {128, 128};

@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
 
   if (tid == 0) {
     if (s_side) {
-      prefetch_tensormap(kF8 ? (p.s_in_place ? &p.tm_kf5 : &p.tm_f5) : (p.s_in_place ? &p.tm_k3 : &p.tm_c3));
+      prefetch_tensormap(kF8 ? &p.tm_f5 : (p.s_in_place ? &p.tm_k3 : &p.tm_c3));
       prefetch_tensormap(kF8 ? &p.tm_qlat8 : &p.tm_qlat);
     } else {
       prefetch_tensormap(&p.tm_c2);
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
         // this CTA's 64 keys of the tile (looked up before the slot wait, which hides the table load): masked
         // past the item's keys, so read in place whatever they hold
         const int kt = it.t0 + 128 * j + 64 * (int)half;
-        const int row = p.s_in_place ? cache_row(p, P, kt) : (int)(row_base + kt);
+        const int row = (kF8 || p.s_in_place) ? cache_row(p, P, kt) : (int)(row_base + kt);
         if (u >= SS::kRing && !await2(p, bar(kSE + s), ((u / SS::kRing) - 1) & 1)) { ok = false; break; }
         if (SS::holds_q(s) && !q_copied) {   // the staged queries are out of the stages before keys overwrite them
           if (!await2(p, bar(kQL), 0)) { ok = false; break; }
@@ -265,8 +265,7 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
         }
         if (first) mbar_arrive_expect_tx(bar(kSF + s), 2 * SS::kStage);
         if (kF8)
-          tma_load_3d_pair(sbase + SS::kStage0 + s * SS::kStage, p.s_in_place ? &p.tm_kf5 : &p.tm_f5, 0, row, 0,
-                           full0 + 8u * s);
+          tma_load_3d_pair(sbase + SS::kStage0 + s * SS::kStage, &p.tm_f5, 0, row, 0, full0 + 8u * s);
         else
           tma_load_3d_pair(sbase + SS::kStage0 + s * SS::kStage, p.s_in_place ? &p.tm_k3 : &p.tm_c3, 0, row, 3 * m,
                            full0 + 8u * s);

@@ -35,19 +35,17 @@ struct AbsorbParams {
   CUtensorMap tm_qlat;  // qlat as [T_q * H rows][512], box 64 x 128
   CUtensorMap tm_c3;    // gathered bf16 rows as 9 blocks of 64 columns ([c | k_rope]), box 64 cols x 64 rows x 3 blocks
   CUtensorMap tm_c2;    // gathered bf16 rows, latent blocks, box 64 x 64 x 2
-  // E4M3 scores (fp8_scores): the cache's FP8 rows gathered as stored (640 B)
+  // E4M3 scores (fp8_scores): the paged FP8 cache's rows as stored (640 B, rows = num_blocks x 64)
   CUtensorMap tm_f5;    // as 5 blocks of 128 B (4 of E4M3 codes, k_rope as bf16), box 128 x 64 x 5
   CUtensorMap tm_qlat8; // E4M3 qlat as [T_q * H rows][512 B], box 128 x 128
   CUtensorMap tm_lat;   // lat_out as [slots * T_q * H rows][512] fp32, box 32 x 128
-  // rows read in place: the paged cache itself (rows = num_blocks x 64), boxes as tm_c3 / tm_c2 (BF16 cache)
-  // or tm_f5 (FP8 cache as stored)
+  // rows read in place: the paged BF16 cache itself (rows = num_blocks x 64), boxes as tm_c3 / tm_c2
   CUtensorMap tm_k3;
   CUtensorMap tm_k2;
-  CUtensorMap tm_kf5;
   const int32_t* block_table;   // [num_reqs][max_blocks]
   int max_blocks;
   int num_blocks;
-  int s_in_place;       // the score side reads the cache's blocks in place
+  int s_in_place;       // the score side reads the cache's blocks in place (always, with E4M3 scores)
   int o_in_place;       // the P c side reads them in place, a request's last block from its copy
   const float* qscale;  // [T_q * H]: the E4M3 qlat row's scale
   float kv_scale;
