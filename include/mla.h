@@ -287,8 +287,8 @@ int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos,
  * a request with at most 192 queries (E_r <= 192) goes through the absorbed
  * path (mla_prefill_ctx_absorbed), the others through the up-projected one,
  * both writing their rows of the same out and lse.  On GB300 the absorbed
- * path is faster below about 215 queries per request (10.5x at one query,
- * 3.4x at 64, 1.81x at 128, 1.18x at 192, on 32K cached tokens and 128
+ * path is faster below about 230 queries per request (13x at one query,
+ * 3.5x at 64, 1.85x at 128, 1.23x at 192, on 32K cached tokens and 128
  * heads) and slower above.
  *  workspace      at least mla_prefill_auto_workspace_size(...) bytes: the
  *                 two paths' workspaces side by side; holds the device error

@@ -1172,9 +1172,9 @@ static int prefill_plans(const void* q, const int32_t* q_pos, const void* kv_cac
 // ------------------------------------------------------------------ head-split reuse
 // A request with at most this many queries goes through the absorbed path,
 // the others through the up-projected one.  On GB300 (128 heads, 32K cached
-// tokens) the two break even near 215 queries: the absorbed path is 1.81x at
-// 128, 1.18x at 192 and 0.98x at 224; on a 128K FP8 cache it is 1.28x at 192
-// and 0.96x at 256.  The FLOP counts alone put it near 170: the latent kernel
+// tokens) the two break even near 230 queries: the absorbed path is 1.85x at
+// 128, 1.23x at 192 and 1.02x at 224; on a 128K FP8 cache it is 1.31x at 192
+// and 0.97x at 256.  The FLOP counts alone put it near 170: the latent kernel
 // runs its MMAs closer to peak than the up-projected one.
 constexpr int kAutoAbsorbedMaxQueries = 192;
 
