@@ -32,8 +32,8 @@
 //    correction warps before the tile's PV; at the end O / l leaves as fp32
 //    latent state.
 // Each pair's MMAs are issued by a whole warp through one elected lane, and
-// the per-tile signals between the CTAs are relaxed arrives wherever the
-// waiter needs no memory released by the arriving thread.
+// the per-tile signals between the CTAs are relaxed arrives (each says why
+// no release is needed there).
 // Each key is read from L2 once per 256 rows by the S pair and once by the O
 // pair, half of it by each CTA.
 #include "absorb.h"
@@ -102,7 +102,7 @@ enum : uint32_t {
   kQL = 21,    // this CTA's 4 softmax warps copied it out (count 4)
   kQR = 22,    // Q of both S CTAs in place (first CTA, count 8)
   kPFR = 23,   // 2: PV of the P tile done (both S CTAs, from the O pair)
-  kSTF = 42,   // 2: the P staging buffer's last copy landed in the O CTA (S CTA, from its O CTA)
+  kSTF = 42,   // 2: a P staging buffer's last copy landed in the O CTA (S CTA, from its O CTA)
   // O side
   kCF = 25,    // 4: stage landed in both O CTAs (first CTA's count)
   kCE = 29,    // 4: the stage's MMAs are done (both O CTAs)
@@ -390,6 +390,7 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
         }
         tc_fence_before();
         __syncwarp();
+        // relaxed: the S buffer's reads are ordered for the next MMAs by the tcgen05 fences around it
         if (lane == 0 && wok) mbar_arrive_cluster_relaxed(ssr0 + 8u * b);
         const int kt0 = it.t0 + 128 * j;
         const uint32_t stg = sbase + SS::kPS + b * SS::kPSBuf;   // this tile's staging buffer
@@ -430,8 +431,8 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
             pk[c] = pack_bf16(a, bb);
           }
         }
-        // the staging buffer is free once the previous tile's copy landed; the four warps go on, or
-        // leave, together
+        // the tile's staging buffer is free once the copy it held two tiles ago landed; the four warps
+        // go on, or leave, together
         if (wok && j >= 2) wok = await2_warp(p, bar(kSTF + b), ((j - 2) >> 1) & 1);
         if (named_bar_or(1, 128, !wok)) { ok = false; break; }
 #pragma unroll
@@ -578,7 +579,7 @@ __global__ void __launch_bounds__(kThreads2, 1) absorb_attn_kernel(const __grid_
       const uint32_t stf_s = mapa_shared(bar(kSTF), half);
       for (int j = 0; j < n; ++j) {
         if (!await2(p, bar(kPF + (j & 1)), (j >> 1) & 1)) break;
-        mbar_arrive_cluster_relaxed(stf_s + 8u * (j & 1));
+        mbar_arrive_cluster_relaxed(stf_s + 8u * (j & 1));   // relaxed: a landed copy has read its source
       }
     } else if (warp >= 4) {
       // ---------------------------------------------------------- rescale O rows; epilogue
