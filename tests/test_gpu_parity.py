@@ -376,17 +376,24 @@ def test_absorbed_long_context_sampled(api):
     run_and_compare(api, wl, rows=rows, heads=np.arange(0, 128, 9), absorbed=True)
 
 
-def test_absorbed_bad_block_and_workspace(api):
+@pytest.mark.parametrize("kv,mode,block", [("bf16", True, 1), ("bf16", True, 17), ("fp8_e4m3", "fp8", 1),
+                                           ("fp8_e4m3", "fp8", 17)],
+                         ids=["middle", "last", "fp8_scores_middle", "fp8_scores_last"])
+def test_absorbed_bad_block_and_workspace(api, kv, mode, block):
+    """A bad block id in the middle of a request or in its last block (read in
+    place by the score side, from a copy by the P c side of a BF16 cache)
+    reaches the error word, and the rows it stands for read as zeros, so the
+    output stays finite."""
     from mla_prefix_cache_gb300 import _lib
-    wl = W.make_workload("ae", 2, [1100], [16], chunk=128, seed=45)
+    wl = W.make_workload("ae", 2, [1100], [16], chunk=128, kv_dtype=kv, seed=45)   # 1116 tokens: blocks 0-17
     dw = api.DeviceWorkload(wl)
-    dw.block_table[0, 1] = -5
-    out, lse = dw.run(absorbed=True)
+    dw.block_table[0, block] = -5
+    out, lse = dw.run(absorbed=mode)
     torch.cuda.synchronize()
     assert api.device_error(api.prefill.last_workspace) == 3    # MLA_ERR_BAD_BLOCK_ID
     assert torch.isfinite(out).all()
     with pytest.raises(_lib.MLAError):
-        dw.run(absorbed=True, workspace=torch.empty(4096, dtype=torch.uint8, device="cuda"))
+        dw.run(absorbed=mode, workspace=torch.empty(4096, dtype=torch.uint8, device="cuda"))
 
 
 # ---------------------------------------------------------------- content-addressed block store
