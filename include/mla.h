@@ -284,7 +284,7 @@ int mla_prefill_ctx_absorbed(const void* q, const int32_t* q_pos,
 
 /* ------------------------------------------------------------------------
  * mla_prefill_ctx_auto -- mla_prefill_ctx with the path chosen per request:
- * a request with at most 192 queries (E_r <= 192) goes through the absorbed
+ * a request with at most 208 queries (E_r <= 208) goes through the absorbed
  * path (mla_prefill_ctx_absorbed), the others through the up-projected one,
  * both writing their rows of the same out and lse.  On GB300 the absorbed
  * path is faster below about 230 queries per request (13x at one query,

@@ -1175,8 +1175,10 @@ static int prefill_plans(const void* q, const int32_t* q_pos, const void* kv_cac
 // tokens) the two break even near 230 queries: the absorbed path is 1.85x at
 // 128, 1.23x at 192 and 1.02x at 224; on a 128K FP8 cache it is 1.31x at 192
 // and 0.97x at 256.  The FLOP counts alone put it near 170: the latent kernel
-// runs its MMAs closer to peak than the up-projected one.
-constexpr int kAutoAbsorbedMaxQueries = 192;
+// runs its MMAs closer to peak than the up-projected one.  208 keeps a margin
+// below the crossover and takes v3_8k's 10% protected rows (205) through the
+// absorbed path (1.77x against 1.70x for head-split reuse).
+constexpr int kAutoAbsorbedMaxQueries = 208;
 
 struct ReusePlan {
   std::vector<int32_t> global, local, prot_rows, prot_tok, gidx, lidx, pidx, cu_p, ctx;

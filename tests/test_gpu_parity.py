@@ -474,7 +474,7 @@ REUSE_CASES = [
     dict(H=128, ctx=[300], ext=[130], chunk=128, glob=list(range(0, 128, 8)), prot=[0, 64, 127, 128, 129]),
     dict(H=5, ctx=[200], ext=[50], chunk=128, glob=[0, 1, 2, 3, 4], prot=[]),          # every head Global
     dict(H=5, ctx=[200], ext=[50], chunk=128, glob=[], prot=[]),                       # all from the artifact
-    # protected rows that take the absorbed path (at most 192 a request, each seeing 1024 keys or more)
+    # protected rows that take the absorbed path (at most 208 a request, each seeing 1024 keys or more)
     dict(H=8, ctx=[1100, 2048], ext=[90, 40], chunk=512, glob=[2, 5], prot=[0, 7, 50, 89, 90, 95, 129]),
     dict(H=6, ctx=[1536], ext=[64], chunk=256, doc=512, glob=[0], prot=[1, 2, 30, 63]),
     dict(H=4, ctx=[1200], ext=[33], chunk=256, kv="fp8_e4m3", glob=[3], prot=list(range(0, 33, 4))),
@@ -485,7 +485,7 @@ REUSE_CASES = [
                                                    "absorbed_batch", "absorbed_docs", "absorbed_fp8"])
 def test_prefill_reuse_matches_oracle(api, case, monkeypatch):
     """Each case through the call's own choice for its protected rows, and,
-    where that is the absorbed path (at most 192 protected rows a request,
+    where that is the absorbed path (at most 208 protected rows a request,
     each seeing 1024 keys or more), again with the up-projected path forced
     (MLA_REUSE_ABSORBED=0): both meet the oracle, and the two routes launch
     different kernels."""
@@ -670,7 +670,7 @@ def test_absorbed_fp8_scores_needs_fp8_cache(api):
     dict(H=2, ctx=[1537, 64], ext=[160, 7], chunk=192, kv="fp8_e4m3"),              # FP8 cache
     dict(H=4, ctx=[1300], ext=[20], chunk=128),                                      # absorbed only
     dict(H=4, ctx=[300], ext=[200], chunk=128),                                      # up-projected only
-    dict(H=2, ctx=[1200, 1100], ext=[192, 193], chunk=128),                          # either side of the threshold
+    dict(H=2, ctx=[1200, 1100], ext=[208, 209], chunk=128),                          # either side of the threshold
     dict(H=2, ctx=[1022, 1023], ext=[8, 8], chunk=128),                              # either side of 1024 keys
 ], ids=["mixed", "docs", "fp8", "short_only", "long_only", "threshold", "few_keys"])
 def test_prefill_auto_matches_oracle(api, case):
